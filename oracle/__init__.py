@@ -1,0 +1,281 @@
+"""fp64 CPU oracle of one DSpark round (TEST INFRASTRUCTURE).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. It wraps ``dspark_oracle.c`` (plain C,
+fp64, its own Philox) through ctypes and numpy. It shares no code with the
+CUDA library; see the C file's header for what each entry computes and which
+passage of the pages it follows.
+
+Sampling margins are returned so that callers can apply the parity rule:
+decisions whose margin is below ``MARGIN`` are "flagged" (too close to call in
+fp32) and are counted instead of compared.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+MARGIN = 1e-5          # parity margin on sampling keys, accept ratios and Theta
+
+# purposes of the random stream (counter word 3, bits 24..31)
+P_DRAFT_BLOCK, P_DRAFT_TOKEN, P_ACCEPT = 1, 2, 3
+P_BONUS_BLOCK, P_BONUS_TOKEN, P_RESID_BLOCK, P_RESID_TOKEN = 4, 5, 6, 7
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dspark_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libdspark_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (fp contraction off so x86 and Arm agree)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Dims(C.Structure):
+    _fields_ = [("B", C.c_int), ("gamma", C.c_int), ("V", C.c_int), ("r", C.c_int),
+                ("H", C.c_int), ("w_bf16", C.c_int)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            l = C.CDLL(build())
+            P = C.c_void_p
+            u32, u64, i32, dbl = C.c_uint32, C.c_uint64, C.c_int, C.c_double
+            l.orc_philox4x32_10.argtypes = [P, P, P]
+            l.orc_word.argtypes = [u64, u64, u32, u32, u32, u32]
+            l.orc_word.restype = u32
+            l.orc_uniform.argtypes = [u64, u64, u32, u32, u32, u32]
+            l.orc_uniform.restype = dbl
+            l.orc_gumbel.argtypes = [u64, u64, u32, u32, u32, u32]
+            l.orc_gumbel.restype = dbl
+            l.orc_logsumexp.argtypes = [P, C.c_long]
+            l.orc_logsumexp.restype = dbl
+            l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P]
+            l.orc_plan_sync.argtypes = [i32, i32, P, P, P, P]
+            l.orc_plan_sync.restype = i32
+            l.orc_plan_capacity.argtypes = [i32, i32, P, P, P]
+            l.orc_plan_capacity.restype = i32
+            l.orc_plan_topk.argtypes = [i32, i32, P, i32, P, P]
+            l.orc_survival.argtypes = [i32, i32, P, P]
+            l.orc_verify.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32,
+                                     P, P, P, P, P]
+            l.orc_sample.argtypes = [P, C.c_long, u64, u64, u32, u32, u32, u32, P]
+            l.orc_sample.restype = i32
+            l.orc_residual.argtypes = [P, P, C.c_long, u64, u64, u32, u32, P]
+            l.orc_residual.restype = i32
+            l.orc_markov_logits.argtypes = [P, P, P, P, i32, P]
+            l.orc_block_width.restype = i32
+            l.orc_set_threads.argtypes = [i32]
+            l.orc_get_threads.restype = i32
+            _lib = l
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def set_threads(n: int) -> None:
+    lib().orc_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().orc_get_threads())
+
+
+def block_width() -> int:
+    return int(lib().orc_block_width())
+
+
+# ---------------------------------------------------------------- random stream
+def philox(ctr: Sequence[int], key: Sequence[int]) -> np.ndarray:
+    c = _c(ctr, np.uint32)
+    k = _c(key, np.uint32)
+    o = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(_p(c), _p(k), _p(o))
+    return o
+
+
+def word(seed, rnd, purpose, b, j, v) -> int:
+    return int(lib().orc_word(seed, rnd, purpose, b, j, v))
+
+
+def uniform(seed, rnd, purpose, b, j, v) -> float:
+    return float(lib().orc_uniform(seed, rnd, purpose, b, j, v))
+
+
+def gumbel(seed, rnd, purpose, b, j, v) -> float:
+    return float(lib().orc_gumbel(seed, rnd, purpose, b, j, v))
+
+
+def logsumexp(x) -> float:
+    a = _c(x, np.float64)
+    return float(lib().orc_logsumexp(_p(a), a.size))
+
+
+def sample(logw, seed=0, rnd=0, pblk=P_DRAFT_BLOCK, ptok=P_DRAFT_TOKEN, b=0, j=0):
+    """One two-level Gumbel-max draw from weights exp(logw). Returns (v, margin)."""
+    a = _c(logw, np.float64)
+    m = np.zeros(1, np.float64)
+    v = lib().orc_sample(_p(a), a.size, seed, rnd, pblk, ptok, b, j, _p(m))
+    return int(v), float(m[0])
+
+
+def residual(pt, pd, seed=0, rnd=0, b=0, j=0):
+    """One draw from norm(max(0, pt - pd)); v = -1 when there is no mass."""
+    a, d = _c(pt, np.float64), _c(pd, np.float64)
+    m = np.zeros(1, np.float64)
+    v = lib().orc_residual(_p(a), _p(d), a.size, seed, rnd, b, j, _p(m))
+    return int(v), float(m[0])
+
+
+# ---------------------------------------------------------------- round stages
+def _dims(B, gamma, V, r, H, w_bf16) -> _Dims:
+    return _Dims(B, gamma, V, r, H, 1 if w_bf16 else 0)
+
+
+def _weights(W) -> (np.ndarray, bool):
+    """Accept fp32 arrays or raw bf16 bit patterns (uint16/int16)."""
+    a = np.asarray(W)
+    if a.dtype in (np.uint16, np.int16):
+        return np.ascontiguousarray(a.view(np.uint16)), True
+    return _c(a, np.float32), False
+
+
+def draft(U, W1, W2, anchor, h, w, T, seed: int, rnd: int,
+          reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+    """Markov-head draft tail + confidence head, eq. (4), (5), (7).
+
+    U [B, gamma, V] fp32, W1 [V, r], W2 [r, V] (fp32 or bf16 bits), anchor [B],
+    h [B, gamma, H], w [H + r], T [gamma]. ``reqs`` restricts the work to a
+    subset of requests (global indices keep their random streams).
+    """
+    U = _c(U, np.float32)
+    B, g, V = U.shape
+    w1, bf = _weights(W1)
+    w2, _ = _weights(W2)
+    r = w1.shape[1]
+    h = _c(h, np.float32)
+    H = h.shape[2]
+    anchor = _c(anchor, np.int32)
+    w = _c(w, np.float32)
+    T = _c(T, np.float32)
+    rq = _c(range(B) if reqs is None else reqs, np.int32)
+    d = _dims(B, g, V, r, H, bf)
+    out = {"tokens": np.full((B, g), -1, np.int32), "pd_tok": np.full((B, g), np.nan),
+           "lse": np.full((B, g), np.nan), "conf": np.full((B, g), np.nan),
+           "margin": np.full((B, g), np.inf)}
+    lib().orc_draft(C.byref(d), _p(U), _p(w1), _p(w2), _p(anchor), _p(h), _p(w), _p(T),
+                    seed, rnd, _p(rq), rq.size, _p(out["tokens"]), _p(out["pd_tok"]),
+                    _p(out["lse"]), _p(out["conf"]), _p(out["margin"]))
+    return out
+
+
+def survival(conf) -> np.ndarray:
+    c = _c(conf, np.float32)
+    B, g = c.shape
+    a = np.zeros((B, g), np.float64)
+    lib().orc_survival(B, g, _p(c), _p(a))
+    return a
+
+
+def plan_sync(conf, sps):
+    """Algorithm 1 with early stop -> (lengths [B], admitted m, margin)."""
+    c = _c(conf, np.float32)
+    B, g = c.shape
+    s = _c(sps, np.float64)
+    assert s.size >= 1 + B * (g + 1)
+    L = np.zeros(B, np.int32)
+    m = np.zeros(1, np.float64)
+    k = lib().orc_plan_sync(B, g, _p(c), _p(s), _p(L), _p(m))
+    return L, int(k), float(m[0])
+
+
+def plan_capacity(conf, sps):
+    """K = argmax_m Theta_m over the full admission path -> (K, margin)."""
+    c = _c(conf, np.float32)
+    B, g = c.shape
+    s = _c(sps, np.float64)
+    m = np.zeros(1, np.float64)
+    K = lib().orc_plan_capacity(B, g, _p(c), _p(s), _p(m))
+    return int(K), float(m[0])
+
+
+def plan_topk(conf, K: int):
+    c = _c(conf, np.float32)
+    B, g = c.shape
+    L = np.zeros(B, np.int32)
+    m = np.zeros(1, np.float64)
+    lib().orc_plan_topk(B, g, _p(c), int(K), _p(L), _p(m))
+    return L, float(m[0])
+
+
+def plan_lagged(conf_now, conf_lagged, sps):
+    """Asynchronous planner: capacity from lagged confidences, top-K of current.
+
+    Returns (lengths, K, margin) where margin covers both the capacity choice
+    and the cut of the top-K.
+    """
+    K, m1 = plan_capacity(conf_lagged, sps)
+    L, m2 = plan_topk(conf_now, K)
+    return L, K, min(m1, m2)
+
+
+def verify(P_packed, row_off, lengths, anchor, tokens, U, W1, W2, seed: int, rnd: int,
+           reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+    """Lossless ragged verify. Returns n_acc, next_anchor, margins, resid flag."""
+    P = _c(P_packed, np.float32)
+    U = _c(U, np.float32)
+    B, g, V = U.shape
+    w1, bf = _weights(W1)
+    w2, _ = _weights(W2)
+    r = w1.shape[1]
+    ro = _c(row_off, np.int32)
+    L = _c(lengths, np.int32)
+    anchor = _c(anchor, np.int32)
+    tokens = _c(tokens, np.int32)
+    rq = _c(range(B) if reqs is None else reqs, np.int32)
+    d = _dims(B, g, V, r, 0, bf)
+    out = {"n_acc": np.full(B, -1, np.int32), "next_anchor": np.full(B, -1, np.int32),
+           "acc_margin": np.full(B, np.inf), "smp_margin": np.full(B, np.inf),
+           "resid": np.zeros(B, np.int32)}
+    lib().orc_verify(C.byref(d), _p(P), _p(ro), _p(L), _p(anchor), _p(tokens), _p(U),
+                     _p(w1), _p(w2), seed, rnd, _p(rq), rq.size, _p(out["n_acc"]),
+                     _p(out["next_anchor"]), _p(out["acc_margin"]), _p(out["smp_margin"]),
+                     _p(out["resid"]))
+    return out
+
+
+def markov_logits(Urow, W1, W2, x_prev: int) -> np.ndarray:
+    u = _c(Urow, np.float32)
+    w1, bf = _weights(W1)
+    w2, _ = _weights(W2)
+    V, r = w1.shape
+    d = _dims(1, 1, V, r, 0, bf)
+    z = np.zeros(V, np.float64)
+    lib().orc_markov_logits(C.byref(d), _p(u), _p(w1), _p(w2), int(x_prev), _p(z))
+    return z

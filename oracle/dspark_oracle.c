@@ -1,0 +1,509 @@
+/*
+ * dspark_oracle.c -- plain, slow, fp64 CPU reference of one DSpark round.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load this library. The product path never calls it,
+ * and it shares no code, header or constant generator with the CUDA library.
+ *
+ * Sources (web pages about DSpark; cited by title and section/equation):
+ *   [V4.1 blog]  "DeepSeek-V4.1 模型结构（6）：解码，DSpark" (blog.javazero.top)
+ *   [spec_dspark] zdszero.github.io "spec_dspark", section "在 SGLang 里"
+ *   [ailearn]    "DSpark：不让大模型更聪明，而让它「吐字更快」", sections 02 and 05
+ *   [csdn]       deepseek.csdn.net close reading of the DSpark paper, sections 2.1-8
+ *
+ * What each function computes, in the pages' notation:
+ *   draft   -- eq. (4)/(5): p_k = softmax(U_k + W1[x_{k-1}] W2), x_0 = anchor,
+ *              sampled left to right (the sequential Markov loop of [V4.1 blog],
+ *              section "Markov head"), plus eq. (7) c_k = sigma(w^T[h_k; W1[x_{k-1}]] / T_k)
+ *              with the STS temperature of [spec_dspark] (sigmoid(raw / T)).
+ *   plan    -- survival a_j = prod_{i<=j} c_i, B = sum(1 + l_r),
+ *              tau = sum(1 + sum_{j<=l_r} a_{r,j}), Theta = tau * SPS(B), and
+ *              Algorithm 1: admit candidates in decreasing a while Theta rises
+ *              ([V4.1 blog] "目标函数", "贪心就能解"; [csdn] 5.3). The
+ *              asynchronous variant takes the capacity K = argmax Theta from
+ *              lagged confidences and the top-K current candidates ([csdn] 8).
+ *   verify  -- accept x with probability min(1, p_t(x)/p_d(x)); at the first
+ *              rejection resample from norm(max(0, p_t - p_d)); if every
+ *              verified draft is accepted draw the bonus token from the
+ *              target ([V4.1 blog] "投机解码"; [ailearn] 02; [csdn] 2.1).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   * sampler: the pages only write sample(logits). Every sample here is an
+ *     exact draw by a two-level Gumbel-max over vocabulary blocks of 64
+ *     tokens: a block is drawn with probability (block mass / total mass) by
+ *     argmax_s (log mass_s + G_s), then a token inside it by
+ *     argmax_v (log weight_v + G_v). Temperature is 1.
+ *   * random stream: Philox4x32-10 (Salmon et al., SC'11), key = seed,
+ *     counter = (v >> 2, b, j, purpose << 24 | round mod 2^24), word v & 3,
+ *     u = (2 * (word >> 9) + 1) * 2^-24, G = -log(-log u).
+ *   * accept test written as u * p_d < p_t (no division).
+ *   * a residual with no positive mass falls back to sampling p_t.
+ *
+ * Margins: each decision also reports how far it was from flipping, in the
+ * units the parity rule uses (key gap for samples, |u - p_t/p_d| for accept
+ * tests, relative Theta gap for the planner); see the header of each entry.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_BLOCK 64
+
+enum {
+    ORC_P_DRAFT_BLOCK = 1,
+    ORC_P_DRAFT_TOKEN = 2,
+    ORC_P_ACCEPT = 3,
+    ORC_P_BONUS_BLOCK = 4,
+    ORC_P_BONUS_TOKEN = 5,
+    ORC_P_RESID_BLOCK = 6,
+    ORC_P_RESID_TOKEN = 7
+};
+
+/* ------------------------------------------------------------------ */
+/* Philox4x32-10, from the round function and key schedule of Salmon,  */
+/* Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3" */
+/* ------------------------------------------------------------------ */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;   /* golden ratio */
+            k1 += 0xBB67AE85u;   /* sqrt(3) - 1 */
+        }
+        uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)x0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+uint32_t orc_word(uint64_t seed, uint64_t round, uint32_t purpose,
+                  uint32_t b, uint32_t j, uint32_t v)
+{
+    uint32_t ctr[4] = { v >> 2, b, j, (purpose << 24) | (uint32_t)(round & 0xFFFFFFu) };
+    uint32_t key[2] = { (uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32) };
+    uint32_t o[4];
+    orc_philox4x32_10(ctr, key, o);
+    return o[v & 3u];
+}
+
+/* Uniform on the odd grid {(2m+1) 2^-24}: never 0 or 1, exact in fp32 and fp64. */
+double orc_uniform(uint64_t seed, uint64_t round, uint32_t purpose,
+                   uint32_t b, uint32_t j, uint32_t v)
+{
+    uint32_t x = orc_word(seed, round, purpose, b, j, v);
+    return (double)(2u * (x >> 9) + 1u) * 0x1p-24;
+}
+
+double orc_gumbel(uint64_t seed, uint64_t round, uint32_t purpose,
+                  uint32_t b, uint32_t j, uint32_t v)
+{
+    double u = orc_uniform(seed, round, purpose, b, j, v);
+    return -log(-log(u));
+}
+
+/* ------------------------------------------------------------------ */
+/* small fp64 helpers                                                  */
+/* ------------------------------------------------------------------ */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* element (i, c) of a row-major [rows, cols] weight stored as fp32 or bf16 */
+static double wget(const void* W, int bf16, long i, long cols, long c)
+{
+    if (bf16) return bf16_to_double(((const uint16_t*)W)[i * cols + c]);
+    return (double)((const float*)W)[i * cols + c];
+}
+
+/* log sum_v exp(x_v), max-subtracted; -inf entries contribute nothing */
+double orc_logsumexp(const double* x, long n)
+{
+    double m = -INFINITY;
+    for (long i = 0; i < n; ++i) if (x[i] > m) m = x[i];
+    if (m == -INFINITY) return -INFINITY;
+    double s = 0.0;
+    for (long i = 0; i < n; ++i) s += exp(x[i] - m);
+    return m + log(s);
+}
+
+/* ------------------------------------------------------------------ */
+/* Two-level Gumbel-max draw of v with probability exp(logw_v)/sum.    */
+/* tol[v] (optional) widens the margin of keys whose fp32 evaluation   */
+/* is known to be loose (the residual); margin = top-2 key gap minus   */
+/* the two tolerances, minimised over both levels.                     */
+/* Returns -1 if no token has positive weight.                         */
+/* ------------------------------------------------------------------ */
+static int sample_two_level(const double* logw, const double* tol, long V,
+                            uint64_t seed, uint64_t round, uint32_t pblk, uint32_t ptok,
+                            uint32_t b, uint32_t j, double* margin)
+{
+    long nblk = (V + ORC_BLOCK - 1) / ORC_BLOCK;
+    double best = -INFINITY, second = -INFINITY, tb = 0.0, ts = 0.0;
+    long bs = -1;
+    for (long s = 0; s < nblk; ++s) {
+        long lo = s * ORC_BLOCK, hi = lo + ORC_BLOCK < V ? lo + ORC_BLOCK : V;
+        double mass_log = orc_logsumexp(logw + lo, hi - lo);
+        if (mass_log == -INFINITY) continue;
+        double t = 0.0;
+        if (tol) {
+            /* block tolerance: relative error of the block mass, i.e. the
+               element tolerances weighted by their share of the mass */
+            for (long v = lo; v < hi; ++v)
+                if (logw[v] > -INFINITY) t += exp(logw[v] - mass_log) * tol[v];
+        }
+        double key = mass_log + orc_gumbel(seed, round, pblk, b, j, (uint32_t)s);
+        if (key > best) { second = best; ts = tb; best = key; tb = t; bs = s; }
+        else if (key > second) { second = key; ts = t; }
+    }
+    if (bs < 0) { *margin = INFINITY; return -1; }
+    double m1 = (second == -INFINITY) ? INFINITY : (best - second) - (tb + ts);
+
+    long lo = bs * ORC_BLOCK, hi = lo + ORC_BLOCK < V ? lo + ORC_BLOCK : V;
+    double kb = -INFINITY, k2 = -INFINITY, t1 = 0.0, t2 = 0.0;
+    long vb = -1;
+    for (long v = lo; v < hi; ++v) {
+        if (logw[v] == -INFINITY) continue;
+        double key = logw[v] + orc_gumbel(seed, round, ptok, b, j, (uint32_t)v);
+        double t = tol ? tol[v] : 0.0;
+        if (key > kb) { k2 = kb; t2 = t1; kb = key; t1 = t; vb = v; }
+        else if (key > k2) { k2 = key; t2 = t; }
+    }
+    double m2 = (k2 == -INFINITY) ? INFINITY : (kb - k2) - (t1 + t2);
+    *margin = m1 < m2 ? m1 : m2;
+    return (int)vb;
+}
+
+/* ------------------------------------------------------------------ */
+/* Draft: eq. (4), (5) and (7).                                        */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int B, gamma, V, r, H;
+    int w_bf16;   /* W1/W2 stored as bf16 bit patterns (else fp32) */
+} orc_dims;
+
+/* z_v = U_k(v) + sum_i W1[x, i] W2[i, v] for one draft position, fp64 */
+static void markov_logits(const orc_dims* d, const float* Urow, const void* W1,
+                          const void* W2, int x_prev, double* z)
+{
+    long V = d->V, r = d->r;
+    for (long v = 0; v < V; ++v) z[v] = 0.0;
+    for (long i = 0; i < r; ++i) {
+        double e = wget(W1, d->w_bf16, x_prev, r, i);   /* W1[x_{k-1}] row */
+        for (long v = 0; v < V; ++v) z[v] += e * wget(W2, d->w_bf16, i, V, v);
+    }
+    for (long v = 0; v < V; ++v) z[v] += (double)Urow[v];
+}
+
+/*
+ * For each request b in reqs[0..n_req): draft x_1..x_gamma.
+ * Outputs (indexed [b][k-1], full-size arrays, only listed rows written):
+ *   tokens, pd_tok = p_k(x_k), lse = log sum exp(z_k), conf = c_k,
+ *   margin = sampling key gap (see sample_two_level).
+ */
+void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2,
+               const int32_t* anchor, const float* h, const float* w, const float* T,
+               uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+               int32_t* tokens, double* pd_tok, double* lse, double* conf, double* margin)
+{
+    const long V = d->V, g = d->gamma, r = d->r, H = d->H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_req; ++q) {
+        const long b = reqs[q];
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        int x_prev = anchor[b];                 /* x_0 = anchor */
+        for (long k = 1; k <= g; ++k) {
+            const long o = b * g + (k - 1);
+            /* eq. (7): c_k = sigma(w^T [h_k; W1[x_{k-1}]] / T_k) */
+            double s = 0.0;
+            for (long i = 0; i < H; ++i) s += (double)w[i] * (double)h[o * H + i];
+            for (long i = 0; i < r; ++i) s += (double)w[H + i] * wget(W1, d->w_bf16, x_prev, r, i);
+            conf[o] = 1.0 / (1.0 + exp(-s / (double)T[k - 1]));
+            /* eq. (4)/(5) */
+            markov_logits(d, U + o * V, W1, W2, x_prev, z);
+            double L = orc_logsumexp(z, V);
+            double m = 0.0;
+            int x = sample_two_level(z, NULL, V, seed, round, ORC_P_DRAFT_BLOCK,
+                                     ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            tokens[o] = x;
+            pd_tok[o] = exp(z[x] - L);
+            lse[o] = L;
+            margin[o] = m;
+            x_prev = x;
+        }
+        free(z);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Planner                                                             */
+/* ------------------------------------------------------------------ */
+typedef struct { double a; int j; int b; } orc_cand;
+
+/* order: a descending, then position j ascending, then request b ascending */
+static int cand_cmp(const void* pa, const void* pb)
+{
+    const orc_cand* x = (const orc_cand*)pa;
+    const orc_cand* y = (const orc_cand*)pb;
+    if (x->a > y->a) return -1;
+    if (x->a < y->a) return 1;
+    if (x->j != y->j) return x->j < y->j ? -1 : 1;
+    if (x->b != y->b) return x->b < y->b ? -1 : 1;
+    return 0;
+}
+
+/* a_{b,j} = prod_{i<=j} c_{b,i} (left-to-right fp64 products), sorted */
+static orc_cand* sorted_candidates(int B, int g, const float* conf)
+{
+    orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)B * (size_t)g);
+    for (int b = 0; b < B; ++b) {
+        double a = 1.0;
+        for (int j = 1; j <= g; ++j) {
+            a = a * (double)conf[(long)b * g + (j - 1)];
+            orc_cand* e = &c[(long)b * g + (j - 1)];
+            e->a = a; e->j = j; e->b = b;
+        }
+    }
+    qsort(c, (size_t)B * (size_t)g, sizeof(orc_cand), cand_cmp);
+    return c;
+}
+
+static double rel_gap(double x, double y)
+{
+    double m = fabs(x) > fabs(y) ? fabs(x) : fabs(y);
+    return m > 0.0 ? fabs(x - y) / m : INFINITY;
+}
+
+/* survival probabilities of each request in candidate order (for tests) */
+void orc_survival(int B, int g, const float* conf, double* a_out)
+{
+    for (int b = 0; b < B; ++b) {
+        double a = 1.0;
+        for (int j = 1; j <= g; ++j) {
+            a = a * (double)conf[(long)b * g + (j - 1)];
+            a_out[(long)b * g + (j - 1)] = a;
+        }
+    }
+}
+
+/*
+ * Algorithm 1 with early stop. sps[n] = SPS(n) for n = 1 .. B*(g+1).
+ * lengths[b] = 1 + number of admitted drafts of b (the anchor is always verified).
+ * Returns the number of admitted candidates m*. margin = smallest relative Theta
+ * gap over the decisions taken, and the relative a gap at the cut.
+ */
+int orc_plan_sync(int B, int g, const float* conf, const double* sps,
+                  int32_t* lengths, double* margin)
+{
+    orc_cand* c = sorted_candidates(B, g, conf);
+    const int M = B * g;
+    double tau = (double)B;           /* every request yields at least one token */
+    long n = B;                        /* verify batch: one anchor per request */
+    double theta = tau * sps[n];
+    double mg = INFINITY;
+    int m = 0;
+    for (; m < M; ++m) {
+        double next = (tau + c[m].a) * sps[n + 1];
+        double gap = rel_gap(next, theta);
+        if (gap < mg) mg = gap;
+        if (!(next > theta)) break;   /* stop as soon as Theta no longer rises */
+        tau += c[m].a;
+        n += 1;
+        theta = next;
+    }
+    if (m > 0 && m < M) {
+        double ga = rel_gap(c[m - 1].a, c[m].a);
+        if (ga < mg) mg = ga;
+    }
+    for (int b = 0; b < B; ++b) lengths[b] = 1;
+    for (int i = 0; i < m; ++i) lengths[c[i].b] += 1;
+    *margin = mg;
+    free(c);
+    return m;
+}
+
+/*
+ * Full-path search: K = argmax_m Theta_m over m = 0 .. B*g (ties -> smallest m),
+ * with Theta_m = (B + sum of the m largest a) * SPS(B + m). Used for the
+ * capacity of the lagged planner, and by tests as the retrospective
+ * (non-early-stop) planner. margin = relative gap between the best and the
+ * second-best Theta.
+ */
+int orc_plan_capacity(int B, int g, const float* conf, const double* sps, double* margin)
+{
+    orc_cand* c = sorted_candidates(B, g, conf);
+    const int M = B * g;
+    double tau = (double)B;
+    double best = tau * sps[B], second = -INFINITY;
+    int K = 0;
+    for (int m = 1; m <= M; ++m) {
+        tau += c[m - 1].a;
+        double th = tau * sps[B + m];
+        if (th > best) { second = best; best = th; K = m; }
+        else if (th > second) second = th;
+    }
+    *margin = second == -INFINITY ? INFINITY : rel_gap(best, second);
+    free(c);
+    return K;
+}
+
+/* lengths from the K best current candidates; margin = relative a gap at the cut */
+void orc_plan_topk(int B, int g, const float* conf, int K, int32_t* lengths, double* margin)
+{
+    orc_cand* c = sorted_candidates(B, g, conf);
+    const int M = B * g;
+    if (K > M) K = M;
+    for (int b = 0; b < B; ++b) lengths[b] = 1;
+    for (int i = 0; i < K; ++i) lengths[c[i].b] += 1;
+    *margin = (K > 0 && K < M) ? rel_gap(c[K - 1].a, c[K].a) : INFINITY;
+    free(c);
+}
+
+/* ------------------------------------------------------------------ */
+/* Verify                                                              */
+/* ------------------------------------------------------------------ */
+/*
+ * For each request b in reqs: rows P + row_off[b] .. + lengths[b]-1 of the
+ * packed target logits (row j = target distribution after x_j, x_0 = anchor).
+ * Draft tokens tokens[b][0..g) are x_1..x_g. The draft distribution p_d at
+ * position j+1 is recomputed here in fp64 from (U, W1, W2, x_j).
+ * Outputs: n_acc[b] (leading accepted drafts), next_anchor[b],
+ *   acc_margin[b] = min |u - p_t/p_d| over the tests taken,
+ *   smp_margin[b] = key-gap margin of the final draw (residual or bonus),
+ *   resid[b] = 1 if the next anchor came from the residual distribution.
+ */
+void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
+                const int32_t* lengths, const int32_t* anchor, const int32_t* tokens,
+                const float* U, const void* W1, const void* W2,
+                uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                int32_t* n_acc, int32_t* next_anchor, double* acc_margin,
+                double* smp_margin, int32_t* resid)
+{
+    const long V = d->V, g = d->gamma;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_req; ++q) {
+        const long b = reqs[q];
+        const int ell = lengths[b];
+        double* lt = (double*)malloc(sizeof(double) * (size_t)V);   /* log p_t */
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* lw = (double*)malloc(sizeof(double) * (size_t)V);
+        double* tol = (double*)malloc(sizeof(double) * (size_t)V);
+        double am = INFINITY, sm = INFINITY;
+        int n = ell - 1, out = -1, from_resid = 0;
+        for (int j = 0; j < ell - 1; ++j) {
+            const float* Prow = P + (long)(row_off[b] + j) * V;
+            for (long v = 0; v < V; ++v) lt[v] = (double)Prow[v];
+            double Lt = orc_logsumexp(lt, V);
+            for (long v = 0; v < V; ++v) lt[v] -= Lt;
+            const int x_prev = j == 0 ? anchor[b] : tokens[b * g + (j - 1)];
+            const int x = tokens[b * g + j];
+            markov_logits(d, U + (b * g + j) * V, W1, W2, x_prev, z);
+            double Ld = orc_logsumexp(z, V);
+            double pt = exp(lt[x]), pd = exp(z[x] - Ld);
+            double u = orc_uniform(seed, round, ORC_P_ACCEPT, (uint32_t)b, (uint32_t)j, 0u);
+            double ratio_gap = fabs(u - pt / pd);
+            if (ratio_gap < am) am = ratio_gap;
+            if (u * pd < pt) continue;         /* accepted with prob min(1, p_t/p_d) */
+            /* first rejection: resample from norm(max(0, p_t - p_d)) */
+            n = j;
+            for (long v = 0; v < V; ++v) {
+                double lpd = z[v] - Ld;
+                if (lt[v] > lpd) {
+                    double c = -expm1(lpd - lt[v]);      /* (p_t - p_d) / p_t */
+                    lw[v] = lt[v] + log(c);
+                    /* an fp32 evaluation of lpd - lt carries about 4e-6 absolute
+                       error, which moves log c by 4e-6 * (1 - c) / c */
+                    tol[v] = 4e-6 * (1.0 - c) / c;
+                } else {
+                    lw[v] = -INFINITY;
+                    tol[v] = 0.0;
+                }
+            }
+            out = sample_two_level(lw, tol, V, seed, round, ORC_P_RESID_BLOCK,
+                                   ORC_P_RESID_TOKEN, (uint32_t)b, (uint32_t)j, &sm);
+            from_resid = 1;
+            if (out < 0) {   /* no positive residual mass: sample p_t itself */
+                out = sample_two_level(lt, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
+                                       ORC_P_BONUS_TOKEN, (uint32_t)b, (uint32_t)j, &sm);
+                from_resid = 0;
+            }
+            break;
+        }
+        if (out < 0) {   /* every verified draft accepted: bonus from row ell-1 */
+            const float* Prow = P + (long)(row_off[b] + n) * V;
+            for (long v = 0; v < V; ++v) lt[v] = (double)Prow[v];
+            out = sample_two_level(lt, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
+                                   ORC_P_BONUS_TOKEN, (uint32_t)b, (uint32_t)n, &sm);
+        }
+        n_acc[b] = n;
+        next_anchor[b] = out;
+        acc_margin[b] = am;
+        smp_margin[b] = sm;
+        resid[b] = from_resid;
+        free(lt); free(z); free(lw); free(tol);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Generic helpers exposed for pin tests                               */
+/* ------------------------------------------------------------------ */
+/* one exact draw from weights exp(logw) with the two-level sampler */
+int orc_sample(const double* logw, long V, uint64_t seed, uint64_t round,
+               uint32_t pblk, uint32_t ptok, uint32_t b, uint32_t j, double* margin)
+{
+    return sample_two_level(logw, NULL, V, seed, round, pblk, ptok, b, j, margin);
+}
+
+/* residual draw for explicit p_t, p_d (pin tests); returns -1 if no mass */
+int orc_residual(const double* pt, const double* pd, long V, uint64_t seed,
+                 uint64_t round, uint32_t b, uint32_t j, double* margin)
+{
+    double* lw = (double*)malloc(sizeof(double) * (size_t)V);
+    for (long v = 0; v < V; ++v) lw[v] = pt[v] > pd[v] ? log(pt[v] - pd[v]) : -INFINITY;
+    int out = sample_two_level(lw, NULL, V, seed, round, ORC_P_RESID_BLOCK,
+                               ORC_P_RESID_TOKEN, b, j, margin);
+    free(lw);
+    return out;
+}
+
+/* the Markov logits of one position (bias GEMM pin) */
+void orc_markov_logits(const orc_dims* d, const float* Urow, const void* W1,
+                       const void* W2, int x_prev, double* z)
+{
+    markov_logits(d, Urow, W1, W2, x_prev, z);
+}
+
+int orc_block_width(void) { return ORC_BLOCK; }
+
+void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int orc_get_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,558 @@
+"""Pins of the fp64 oracle against what the pages and mathematics fix.
+
+Nothing here compares the oracle with itself: every expected value is a number
+printed by the pages (tests/golden), a closed form, an invariant, a library
+routine (scipy, numpy, cuRAND's host Philox) or a Monte-Carlo statistic of a
+distribution the pages derive.
+"""
+
+import ctypes
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy import special, stats
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def bf16_bits(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+
+
+def bf16_values(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def binom_ok(k, n, p, nsig=5.0):
+    sd = np.sqrt(max(p * (1 - p), 1e-12) / n)
+    return abs(k / n - p) <= nsig * sd + 1e-12
+
+
+def chi2_p(counts, probs):
+    counts = np.asarray(counts, np.float64)
+    probs = np.asarray(probs, np.float64)
+    keep = probs > 0
+    assert counts[~keep].sum() == 0, "a zero-probability token was drawn"
+    exp = probs[keep] / probs[keep].sum() * counts.sum()
+    return stats.chisquare(counts[keep], exp).pvalue
+
+
+# ------------------------------------------------------------------ Philox
+def test_philox_known_answers():
+    g = gold("philox_kat.json")
+    for vec in g["vectors"]:
+        ctr = [int(x, 16) for x in vec["ctr"]]
+        key = [int(x, 16) for x in vec["key"]]
+        out = [int(x, 16) for x in vec["out"]]
+        assert list(oracle.philox(ctr, key)) == out
+
+
+def _curand():
+    for p in ("/usr/local/cuda/lib64/libcurand.so", "libcurand.so", "libcurand.so.10"):
+        try:
+            return ctypes.CDLL(p)
+        except OSError:
+            continue
+    return None
+
+
+def test_philox_matches_curand_host_generator():
+    """cuRAND's host Philox4_32_10 emits block i from counter (0, 0, i, 0), key = seed."""
+    cur = _curand()
+    if cur is None:
+        pytest.skip("libcurand not available")
+    for seed in (0, 1, 0x123456789ABCDEF0):
+        g = ctypes.c_void_p()
+        if cur.curandCreateGeneratorHost(ctypes.byref(g), 161) != 0:
+            pytest.skip("cuRAND host generator unavailable")
+        cur.curandSetPseudoRandomGeneratorSeed(g, ctypes.c_ulonglong(seed))
+        n = 4 * 512
+        buf = (ctypes.c_uint * n)()
+        assert cur.curandGenerate(g, buf, ctypes.c_size_t(n)) == 0
+        cur.curandDestroyGenerator(g)
+        ref = np.array(buf, np.uint32).reshape(-1, 4)
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        for i in range(ref.shape[0]):
+            assert (oracle.philox([0, 0, i, 0], key) == ref[i]).all(), (seed, i)
+
+
+def test_counter_layout_and_uniform_grid():
+    seed, rnd = 0xDEADBEEF12345678, 0x1234567   # round is taken mod 2^24
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for (purpose, b, j, v) in [(1, 0, 1, 0), (2, 7, 3, 5), (3, 127, 0, 0), (7, 255, 15, 151935)]:
+        w = oracle.philox([v >> 2, b, j, (purpose << 24) | (rnd & 0xFFFFFF)], key)[v & 3]
+        assert oracle.word(seed, rnd, purpose, b, j, v) == w
+        u = oracle.uniform(seed, rnd, purpose, b, j, v)
+        m = u * 2 ** 24
+        assert m == int(m) and int(m) % 2 == 1 and int(m) == 2 * (int(w) >> 9) + 1
+        assert np.float32(u) == u                        # exact in fp32
+    us = np.array([oracle.uniform(1, 0, 1, 0, 0, v) for v in range(40000)])
+    assert us.min() >= 2.0 ** -24 and us.max() <= 1 - 2.0 ** -24
+    assert stats.kstest(us, "uniform").pvalue > 1e-4
+
+
+def test_gumbel_is_standard_gumbel():
+    g = np.array([oracle.gumbel(3, 1, 2, 5, 1, v) for v in range(60000)])
+    assert stats.kstest(g, stats.gumbel_r.cdf).pvalue > 1e-4
+    # bounds implied by the uniform grid
+    assert g.max() <= -np.log(-np.log1p(-2.0 ** -24)) + 1e-12
+    assert g.min() >= -np.log(-np.log(2.0 ** -24)) - 1e-12
+
+
+def test_logsumexp_matches_scipy():
+    rng = np.random.default_rng(0)
+    for n in (1, 7, 1000):
+        x = rng.normal(0, 5, n) + 700.0          # overflow if not max-subtracted
+        assert abs(oracle.logsumexp(x) - special.logsumexp(x)) < 1e-9
+    x = np.array([-np.inf, 0.0, -np.inf, np.log(3.0)])
+    assert abs(oracle.logsumexp(x) - np.log(4.0)) < 1e-12
+
+
+# ------------------------------------------------------------------ sampler
+@pytest.mark.parametrize("V", [5, 64, 200])
+def test_two_level_sampler_marginal_is_softmax(V):
+    rng = np.random.default_rng(V)
+    logw = rng.normal(0, 1.5, V)
+    if V > 5:
+        logw[rng.choice(V, V // 10, replace=False)] = -np.inf   # zero-weight tokens
+    N = 60000
+    counts = np.zeros(V)
+    for b in range(N):
+        v, _ = oracle.sample(logw, seed=11, rnd=2, b=b, j=1)
+        counts[v] += 1
+    p = np.exp(logw - special.logsumexp(logw))
+    assert chi2_p(counts, p) > 1e-4
+
+
+def test_sampler_block_and_token_levels_both_matter():
+    """Mass concentrated in one block is always drawn from that block."""
+    V = 256
+    logw = np.full(V, -np.inf)
+    logw[130:140] = np.log(np.arange(1, 11, dtype=float))
+    seen = set()
+    for b in range(3000):
+        v, _ = oracle.sample(logw, seed=5, b=b)
+        assert 130 <= v < 140
+        seen.add(v)
+    assert seen == set(range(130, 140))
+    assert oracle.sample(np.full(10, -np.inf))[0] == -1
+
+
+# ------------------------------------------------------------------ helpers
+def token_independent_round(qs, ps, N, seed=7, ell=None, tokens=None, rnd=0):
+    """Draft + verify with zero Markov weights: position k drafts from qs[k-1],
+    target row j is ps[j]. Returns (draft, verify) oracle outputs."""
+    qs, ps = np.asarray(qs, float), np.asarray(ps, float)
+    g, V = qs.shape
+    U = np.broadcast_to(np.log(qs).astype(np.float32), (N, g, V)).copy()
+    W1 = np.zeros((V, 1), np.float32)
+    W2 = np.zeros((1, V), np.float32)
+    anchor = np.zeros(N, np.int32)
+    h = np.zeros((N, g, 1), np.float32)
+    w = np.zeros(2, np.float32)
+    T = np.ones(g, np.float32)
+    d = oracle.draft(U, W1, W2, anchor, h, w, T, seed, rnd)
+    toks = d["tokens"] if tokens is None else np.broadcast_to(np.asarray(tokens, np.int32), (N, g)).copy()
+    L = np.full(N, g + 1 if ell is None else ell, np.int32)
+    Pfull = np.broadcast_to(np.log(ps).astype(np.float32), (N, g + 1, V))
+    ro = np.zeros(N + 1, np.int32)
+    ro[1:] = np.cumsum(L)
+    P = np.concatenate([Pfull[b, :L[b]] for b in range(N)])
+    vo = oracle.verify(P, ro, L, anchor, toks, U, W1, W2, seed, rnd)
+    return d, vo, toks
+
+
+def first_emitted(vo, toks):
+    return np.where(vo["n_acc"] > 0, toks[:, 0], vo["next_anchor"])
+
+
+# ------------------------------------------------------------------ verify pins
+def test_two_token_worked_example():
+    g = gold("two_token_example.json")
+    pt, pd = np.array(g["p_t"]), np.array(g["p_d"])
+    N = 40000
+    # draft token A: always accepted
+    _, vo, _ = token_independent_round([pd], [pt, pt], N, tokens=[0], ell=2)
+    assert (vo["n_acc"] == 1).all()
+    assert g["accept_prob"][0] == 1.0
+    # draft token B: accepted with prob 0.3/0.5; on rejection the residual is (1, 0)
+    _, vo, _ = token_independent_round([pd], [pt, pt], N, tokens=[1], ell=2, seed=9)
+    k = int((vo["n_acc"] == 1).sum())
+    assert binom_ok(k, N, g["accept_prob"][1])
+    rej = vo["n_acc"] == 0
+    assert (vo["next_anchor"][rej] == 0).all() and (vo["resid"][rej] == 1).all()
+    assert np.allclose(np.maximum(pt - pd, 0), g["residual_mass"])
+    # end to end: drafted from p_d, the first emitted token follows p_t
+    _, vo, toks = token_independent_round([pd], [pt, pt], N, ell=2, seed=13)
+    out = first_emitted(vo, toks)
+    assert binom_ok(int((out == 0).sum()), N, g["output"][0])
+    assert binom_ok(int((vo["n_acc"] == 1).sum()), N, g["beta"])
+
+
+def test_collision_example_and_markov_repair():
+    g = gold("collision.json")
+    # position 2 after "of": target (course, problem) = (1, 0); parallel draft (0.5, 0.5)
+    N = 40000
+    pt = np.array(g["p_target_given_of"])
+    q = np.array(g["q_parallel_draft"])
+    ptl = np.where(pt > 0, pt, 1e-45)
+    _, vo, _ = token_independent_round([q], [ptl, ptl], N, ell=2, seed=21)
+    assert binom_ok(int((vo["n_acc"] == 1).sum()), N, g["beta"])
+    # Markov bias W1[of] W2 raising "course" and lowering "problem" repairs it
+    V = 4                      # of, no, course, problem
+    U = np.zeros((N, 1, V), np.float32)
+    U[:, 0, :2] = -60.0        # position 2 only proposes course/problem
+    W1 = np.zeros((V, 1), np.float32)
+    W1[0, 0] = 1.0             # "of"
+    W2 = np.array([[0.0, 0.0, 12.0, -12.0]], np.float32)
+    anchor = np.zeros(N, np.int32)   # previous token x_0 = "of"
+    h = np.zeros((N, 1, 1), np.float32)
+    d = oracle.draft(U, W1, W2, anchor, h, np.zeros(2, np.float32), np.ones(1, np.float32), 3, 0)
+    L = np.full(N, 2, np.int32)
+    ro = np.arange(0, 2 * N + 1, 2, dtype=np.int32)
+    P = np.tile(np.log(np.array([1e-45, 1e-45, 1.0, 1e-45], np.float32)), (2 * N, 1))
+    vo = oracle.verify(P, ro, L, anchor, d["tokens"], U, W1, W2, 3, 0)
+    assert (vo["n_acc"] == 1).mean() > 0.999
+
+
+def test_lossless_for_arbitrary_draft_distributions():
+    """Output marginal = p_t for any p_d, and acceptance = sum min = 1 - TV."""
+    rng = np.random.default_rng(1)
+    V, N = 100, 60000                      # two sampler blocks, ragged tail
+    for trial in range(2):
+        pt = rng.dirichlet(np.full(V, 0.5))
+        pd = rng.dirichlet(np.full(V, 0.5))
+        _, vo, toks = token_independent_round([pd], [pt, pt], N, ell=2, seed=100 + trial)
+        beta = np.minimum(pt, pd).sum()
+        assert abs(beta - (1 - 0.5 * np.abs(pt - pd).sum())) < 1e-12
+        assert binom_ok(int((vo["n_acc"] == 1).sum()), N, beta)
+        out = first_emitted(vo, toks)
+        assert chi2_p(np.bincount(out, minlength=V), pt) > 1e-4
+        # after a rejection the token follows norm(max(0, p_t - p_d))
+        rej = vo["n_acc"] == 0
+        res = np.maximum(pt - pd, 0)
+        assert chi2_p(np.bincount(vo["next_anchor"][rej], minlength=V), res) > 1e-4
+
+
+def test_expected_accepted_length_is_sum_of_survival():
+    """E[n] = sum_j prod_{i<=j} beta_i for token-independent rows; bonus follows p_t."""
+    rng = np.random.default_rng(4)
+    V, g, N = 8, 3, 60000
+    qs = rng.dirichlet(np.ones(V), g)
+    ps = rng.dirichlet(np.ones(V), g + 1)
+    betas = np.minimum(qs, ps[:g]).sum(1)
+    _, vo, toks = token_independent_round(qs, ps, N, seed=31)
+    n = vo["n_acc"]
+    for j in range(1, g + 1):
+        assert binom_ok(int((n >= j).sum()), N, float(np.prod(betas[:j])))
+    full = n == g
+    assert chi2_p(np.bincount(vo["next_anchor"][full], minlength=V), ps[g]) > 1e-4
+    # a length-1 verify (anchor only) is plain target sampling from row 0
+    _, vo1, _ = token_independent_round(qs, ps, N, seed=32, ell=1)
+    assert (vo1["n_acc"] == 0).all() and (vo1["resid"] == 0).all()
+    assert chi2_p(np.bincount(vo1["next_anchor"], minlength=V), ps[0]) > 1e-4
+
+
+# ------------------------------------------------------------------ draft pins
+def test_markov_logits_match_matmul():
+    rng = np.random.default_rng(2)
+    V, r = 300, 24
+    U = rng.normal(0, 2, V).astype(np.float32)
+    W1 = rng.normal(0, 0.1, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.1, (r, V)).astype(np.float32)
+    for x in (0, 17, V - 1):
+        z = oracle.markov_logits(U, W1, W2, x)
+        ref = U.astype(np.float64) + W1[x].astype(np.float64) @ W2.astype(np.float64)
+        assert np.abs(z - ref).max() < 1e-12
+        zb = oracle.markov_logits(U, bf16_bits(W1), bf16_bits(W2), x)
+        refb = U.astype(np.float64) + bf16_values(W1)[x] @ bf16_values(W2)
+        assert np.abs(zb - refb).max() < 1e-12
+
+
+def test_draft_outputs_lse_pd_conf():
+    rng = np.random.default_rng(3)
+    B, g, V, r, H = 3, 4, 300, 8, 16
+    U = rng.normal(0, 2, (B, g, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.3, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.3, (r, V)).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    h = rng.normal(0, 1, (B, g, H)).astype(np.float32)
+    w = rng.normal(0, 0.3, H + r).astype(np.float32)
+    T = np.array([0.8, 1.0, 1.3, 1.5], np.float32)
+    d = oracle.draft(U, W1, W2, anchor, h, w, T, seed=5, rnd=1)
+    for b in range(B):
+        prev = anchor[b]
+        for k in range(g):
+            z = U[b, k].astype(float) + W1[prev].astype(float) @ W2.astype(float)
+            assert abs(d["lse"][b, k] - special.logsumexp(z)) < 1e-9
+            x = d["tokens"][b, k]
+            assert abs(d["pd_tok"][b, k] - special.softmax(z)[x]) < 1e-12
+            raw = w[:H].astype(float) @ h[b, k] + w[H:].astype(float) @ W1[prev].astype(float)
+            assert abs(d["conf"][b, k] - special.expit(raw / T[k])) < 1e-12
+            prev = x
+
+
+def test_draft_marginal_is_markov_softmax():
+    rng = np.random.default_rng(6)
+    N, V, r = 40000, 130, 4
+    u0 = rng.normal(0, 1, V).astype(np.float32)
+    U = np.broadcast_to(u0, (N, 1, V)).copy()
+    W1 = rng.normal(0, 0.5, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.5, (r, V)).astype(np.float32)
+    anchor = np.full(N, 9, np.int32)
+    d = oracle.draft(U, W1, W2, anchor, np.zeros((N, 1, 1), np.float32),
+                     np.zeros(1 + r, np.float32), np.ones(1, np.float32), 8, 0)
+    z = u0.astype(float) + W1[9].astype(float) @ W2.astype(float)
+    assert chi2_p(np.bincount(d["tokens"][:, 0], minlength=V), special.softmax(z)) > 1e-4
+
+
+def test_draft_uses_previous_token_and_position_row():
+    """x_k depends on x_{k-1} through W1 (eq. 5) and on U row k-1 (eq. 4)."""
+    V, g, B = 6, 5, 4
+    # bias: after token t the next token is (t + 1) mod V, overwhelmingly
+    W1 = np.eye(V, dtype=np.float32)
+    W2 = np.full((V, V), -40.0, np.float32)
+    for t in range(V):
+        W2[t, (t + 1) % V] = 40.0
+    U = np.zeros((B, g, V), np.float32)
+    anchor = np.arange(B, dtype=np.int32)
+    d = oracle.draft(U, W1, W2, anchor, np.zeros((B, g, 1), np.float32),
+                     np.zeros(1 + V, np.float32), np.ones(g, np.float32), 1, 0)
+    for b in range(B):
+        assert list(d["tokens"][b]) == [(b + k) % V for k in range(1, g + 1)]
+    # no Markov bias: position k follows U row k-1
+    U = np.full((B, g, V), -40.0, np.float32)
+    for k in range(g):
+        U[:, k, (2 * k + 1) % V] = 40.0
+    d = oracle.draft(U, np.zeros((V, 1), np.float32), np.zeros((1, V), np.float32), anchor,
+                     np.zeros((B, g, 1), np.float32), np.zeros(2, np.float32),
+                     np.ones(g, np.float32), 1, 0)
+    for b in range(B):
+        assert list(d["tokens"][b]) == [(2 * k + 1) % V for k in range(g)]
+
+
+def test_confidence_is_non_anticipating_and_temperature_monotone():
+    rng = np.random.default_rng(8)
+    B, g, V, r, H = 6, 3, 50, 4, 8
+    U = rng.normal(0, 2, (B, g, V)).astype(np.float32)
+    W1 = rng.normal(0, 0.5, (V, r)).astype(np.float32)
+    W2 = rng.normal(0, 0.5, (r, V)).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    h = rng.normal(0, 1, (B, g, H)).astype(np.float32)
+    w = rng.normal(0, 0.5, H + r).astype(np.float32)
+    d1 = oracle.draft(U, W1, W2, anchor, h, w, np.ones(g, np.float32), 4, 0)
+    # the W1 row of the token drafted at the last position feeds no confidence
+    # of this block (c_k reads x_{k-1}, never x_k)
+    used = set(anchor.tolist()) | set(d1["tokens"][:, :-1].ravel().tolist())
+    for b in range(B):
+        x_last = d1["tokens"][b, -1]
+        if x_last in used:
+            continue
+        W1b = W1.copy()
+        W1b[x_last] += 100.0
+        d2 = oracle.draft(U, W1b, W2, anchor, h, w, np.ones(g, np.float32), 4, 0)
+        assert (d2["conf"] == d1["conf"]).all()
+        break
+    # T = 1 is a plain sigmoid; a temperature keeps the order of confidences
+    T = np.array([2.0, 0.5, 1.7], np.float32)
+    d3 = oracle.draft(U, W1, W2, anchor, h, w, T, 4, 0)
+    for k in range(g):
+        o1 = np.argsort(d1["conf"][:, k], kind="stable")
+        o3 = np.argsort(d3["conf"][:, k], kind="stable")
+        assert (o1 == o3).all()
+        logit1 = special.logit(d1["conf"][:, k])
+        assert np.allclose(special.expit(logit1 / T[k]), d3["conf"][:, k], rtol=1e-9, atol=1e-15)
+
+
+# ------------------------------------------------------------------ planner pins
+def appendix_sps(n_max):
+    g = gold("appendix_a.json")
+    s = np.zeros(n_max + 1)
+    for k, v in g["sps"].items():
+        s[int(k)] = v
+    s[0] = s[1]
+    return s
+
+
+def test_appendix_a_planner_numbers():
+    g = gold("appendix_a.json")
+    sps = appendix_sps(3)
+    for case in ("case_high", "case_low"):
+        c = np.array([[g["a1"], g[case]["c2"]]], np.float32)
+        a = oracle.survival(c)
+        assert abs(a[0, 1] - g[case]["a2"]) < 1e-6
+        # theta values of the admission path, from the pages
+        th = [(1 + sum(a[0, :m])) * sps[1 + m] for m in range(3)]
+        assert np.allclose(th, [g["theta0"], g["theta1"], g[case]["theta2"]], atol=1e-6)
+        # Algorithm 1 stops at Theta_1 < Theta_0 whatever c_2 is
+        L, m, margin = oracle.plan_sync(c, sps)
+        assert m == g["early_stop_drafts_verified"] and L[0] == 1
+        assert abs(margin - 0.1) < 1e-6
+        # the retrospective global argmax does look at c_2
+        K, _ = oracle.plan_capacity(c, sps)
+        assert K == g[case]["retrospective_drafts_verified"]
+
+
+def appendix_a_pipeline(N, planner, seed):
+    """Appendix A through the oracle's draft -> plan -> verify, one request per batch.
+
+    V = {A, B}; p_d = (0.5, 0.5) at position 1; c_1 = 0.8; c_2 = 0.9 after A and
+    ~0 after B (eq. 7 with r = 1, w_r = 1); SPS(1..3) = (1.0, 0.5, 0.45).
+    """
+    g = gold("appendix_a.json")
+    V, gam = 2, 2
+    U = np.zeros((N, gam, V), np.float32)
+    W1 = np.array([[special.logit(0.9)], [-80.0]], np.float32)   # row of A, row of B
+    W2 = np.zeros((1, V), np.float32)
+    anchor = np.ones(N, np.int32)          # x_0 = B: c_1 = sigma(s_h1 + W1[B]) -> set s_h1
+    H = 1
+    h = np.zeros((N, gam, H), np.float32)
+    h[:, 0, 0] = special.logit(0.8) + 80.0     # so c_1 = sigma(logit(0.8)) = 0.8
+    w = np.array([1.0, 1.0], np.float32)
+    T = np.ones(gam, np.float32)
+    d = oracle.draft(U, W1, W2, anchor, h, w, T, seed, 0)
+    conf = d["conf"].astype(np.float32)
+    sps = appendix_sps(3)
+    L = np.zeros(N, np.int32)
+    for b in range(N):
+        c = conf[b:b + 1]
+        if planner == "sync":
+            L[b] = oracle.plan_sync(c, sps)[0][0]
+        elif planner == "retrospective":
+            K, _ = oracle.plan_capacity(c, sps)
+            L[b] = oracle.plan_topk(c, K)[0][0]
+        else:   # lagged: capacity from an independent earlier round's confidences
+            lag = np.array([[0.8, 0.9 if b % 2 else 0.0]], np.float32)
+            L[b] = oracle.plan_lagged(c, lag, sps)[0][0]
+    pt = np.log(np.array(g["p_t"], np.float32))
+    ro = np.zeros(N + 1, np.int32)
+    ro[1:] = np.cumsum(L)
+    P = np.tile(pt, (int(ro[-1]), 1))
+    vo = oracle.verify(P, ro, L, anchor, d["tokens"], U, W1, W2, seed, 0)
+    out = first_emitted(vo, d["tokens"])
+    return out, L, d
+
+
+def test_appendix_a_monte_carlo():
+    g = gold("appendix_a.json")
+    N = 30000
+    out, L, d = appendix_a_pipeline(N, "retrospective", seed=41)
+    assert np.allclose(d["conf"][:, 0], 0.8, atol=1e-6)
+    assert set(np.unique(L)) == {1, 3}
+    assert binom_ok(int((out == 0).sum()), N, g["retrospective_output"][0])
+    out, L, _ = appendix_a_pipeline(N, "sync", seed=42)
+    assert (L == 1).all()
+    assert binom_ok(int((out == 0).sum()), N, g["early_stop_output"][0])
+    # capacity from information older than the current draft keeps p_t
+    out, L, _ = appendix_a_pipeline(N, "lagged", seed=43)
+    assert binom_ok(int((out == 0).sum()), N, g["p_t"][0])
+
+
+def ref_order(conf):
+    """Candidate order (a desc, j asc, b asc) with a from numpy cumprod."""
+    a = np.cumprod(conf.astype(np.float64), axis=1)
+    B, g = a.shape
+    bb, jj = np.meshgrid(np.arange(B), np.arange(1, g + 1), indexing="ij")
+    order = np.lexsort((bb.ravel(), jj.ravel(), -a.ravel()))
+    return a.ravel()[order], jj.ravel()[order], bb.ravel()[order]
+
+
+def sps_curve(B, g, knee):
+    n = np.arange(1 + B * (g + 1), dtype=np.float64)
+    n[0] = 1
+    return 400.0 / (1.0 + n / knee)
+
+
+@pytest.mark.parametrize("knee", [16.0, 128.0, 512.0, 1e6])
+def test_planner_greedy_prefix_threshold_and_domain(knee):
+    rng = np.random.default_rng(int(knee) % 1000)
+    B, g = 40, 6
+    conf = special.expit(rng.normal(0, 3, (B, g))).astype(np.float32)
+    sps = sps_curve(B, g, knee)
+    L, m, _ = oracle.plan_sync(conf, sps)
+    assert L.min() >= 1 and L.max() <= g + 1          # anchor always verified
+    assert int((L - 1).sum()) == m
+    a, j, b = ref_order(conf)
+    # admitted = the m best candidates, which are per-request prefixes
+    cnt = np.bincount(b[:m], minlength=B)
+    assert (cnt == L - 1).all()
+    for bb in range(B):
+        assert sorted(j[:m][b[:m] == bb].tolist()) == list(range(1, cnt[bb] + 1))
+    # marginal admission threshold: a > tau (SPS(n)/SPS(n+1) - 1)
+    tau, n = float(B), B
+    for i in range(len(a)):
+        thr = tau * (sps[n] / sps[n + 1] - 1.0)
+        if i < m:
+            assert a[i] > thr - 1e-12 * tau
+            tau, n = tau + a[i], n + 1
+        else:
+            assert a[i] <= thr + 1e-12 * tau
+            break
+
+
+def test_planner_flat_table_is_full_verify():
+    rng = np.random.default_rng(9)
+    B, g = 17, 7
+    conf = special.expit(rng.normal(0, 3, (B, g))).astype(np.float32)
+    L, m, _ = oracle.plan_sync(conf, np.full(1 + B * (g + 1), 400.0))
+    assert (L == g + 1).all() and m == B * g
+
+
+@pytest.mark.parametrize("B,g", [(1, 3), (2, 2), (3, 3), (2, 3)])
+def test_planner_bruteforce_optimality(B, g):
+    rng = np.random.default_rng(B * 10 + g)
+    for trial in range(30):
+        conf = special.expit(rng.normal(0.5, 2, (B, g))).astype(np.float32)
+        knee = [1.0, 3.0, 10.0][trial % 3]
+        sps = sps_curve(B, g, knee)
+        a = np.cumprod(conf.astype(np.float64), axis=1)
+        best_tau = {}
+        best_theta = -1.0
+        for alloc in itertools.product(range(g + 1), repeat=B):
+            tot = sum(alloc)
+            tau = B + sum(a[bb, :alloc[bb]].sum() for bb in range(B))
+            best_tau[tot] = max(best_tau.get(tot, -1.0), tau)
+            best_theta = max(best_theta, tau * sps[B + tot])
+        # the greedy top-m set is the best allocation of every total size m
+        av, _, _ = ref_order(conf)
+        for mm in range(B * g + 1):
+            assert abs(B + av[:mm].sum() - best_tau[mm]) < 1e-12
+        # the full-path search finds the global optimum of Theta
+        K, _ = oracle.plan_capacity(conf, sps)
+        LK, _ = oracle.plan_topk(conf, K)
+        tauK = B + sum(a[bb, :LK[bb] - 1].sum() for bb in range(B))
+        assert abs(tauK * sps[B + K] - best_theta) < 1e-12 * best_theta
+        # early stop reaches it when Theta along the path is unimodal
+        th = [(B + av[:mm].sum()) * sps[B + mm] for mm in range(B * g + 1)]
+        peak = int(np.argmax(th))
+        if all(th[i] < th[i + 1] for i in range(peak)) and \
+           all(th[i] >= th[i + 1] for i in range(peak, len(th) - 1)):
+            L, m, _ = oracle.plan_sync(conf, sps)
+            assert m == peak
+
+
+def test_lagged_planner_takes_capacity_from_lag_and_order_from_now():
+    rng = np.random.default_rng(12)
+    B, g = 30, 5
+    now = special.expit(rng.normal(0, 3, (B, g))).astype(np.float32)
+    lag = special.expit(rng.normal(0, 3, (B, g))).astype(np.float32)
+    sps = sps_curve(B, g, 64.0)
+    L, K, _ = oracle.plan_lagged(now, lag, sps)
+    K2, _ = oracle.plan_capacity(lag, sps)
+    assert K == K2 and int((L - 1).sum()) == K
+    a, j, b = ref_order(now)
+    assert (np.bincount(b[:K], minlength=B) == L - 1).all()
+    # with no lag (same confidences) the capacity is the full-path optimum
+    L0, K0, _ = oracle.plan_lagged(now, now, sps)
+    assert K0 == oracle.plan_capacity(now, sps)[0]
