@@ -1,0 +1,398 @@
+"""Benchmark of one DSpark round (draft -> plan -> verify) on the GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prod] [--impl ours|reference]
+
+A step is one whole round over one batch: the Markov-head draft tail with the
+confidence head, the planner, and the ragged verify, through the C-ABI
+(dspark_round). Inputs are seeded synthetic tensors of the workload's shapes
+and distributions, resident in HBM; the round counter is fixed so that every
+timed step plans the same lengths and the packed target logits stay valid.
+U (331 MB) and P (>= 66 MB) exceed the 129 MB L2, so no flush is needed.
+
+Printed on rank 0: one JSON line with the throughput (rounds/s), the
+roofline of the dominant stage, the oracle timed on host cores (cpu_baseline)
+and an end-to-end figure through the same C-ABI with host buffers.
+Under torchrun each rank runs its own replica on its own GPU (weak scaling,
+no data-path collective); the timing is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofline"
+NORTH_STAR_BW = 8000.0   # GB/s, the roofline constant the metric is quoted against
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="prod")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(wl, sum_len):
+    return {"workload": f"{wl.name}: B={wl.B} gamma={wl.gamma} V={wl.V} r={wl.r} H={wl.H} "
+                        f"W={wl.wdtype} mode={wl.mode}",
+            "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "H": wl.H, "weights": wl.wdtype,
+            "logits": "f32", "mode": wl.mode, "verified_rows": int(sum_len),
+            "l2": "inputs larger than L2 (U and P stream >129 MB per round); no flush",
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int):
+    """Time the oracle (draft + plan + verify) on a bounded sample of requests.
+
+    Returns (rounds_per_s, cores, sample description). Draft and verify run on
+    the sampled requests (their cost is linear in the number of requests), the
+    planner on the confidences the oracle drafted; verify takes every target
+    row of a request (gamma + 1, the longest verify), so no input comes from
+    the GPU run.
+    """
+    import numpy as np
+    import oracle
+    import torch
+    oracle.set_threads(os.cpu_count() or 1)
+    cores = oracle.get_threads()
+    npi = {k: (v.contiguous().view(torch.int16).numpy() if v.dtype == torch.bfloat16 else v.numpy())
+           for k, v in inp_cpu.items()}
+    L = np.full(wl.B, wl.gamma + 1, np.int32)
+    ro = np.zeros(wl.B + 1, np.int32)
+    ro[1:] = np.cumsum(L)
+    P = npi["P_full"].reshape(-1, wl.V)
+    n = max(1, min(cores, wl.B))
+    done_req, spent = 0, 0.0
+    while True:
+        reqs = [(done_req + i) % wl.B for i in range(n)]
+        t0 = time.perf_counter()
+        od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"],
+                          seed, rnd, reqs=reqs)
+        if wl.mode != "static":
+            conf = np.nan_to_num(od["conf"].astype(np.float32), nan=0.5)
+            oracle.plan_sync(conf, npi["sps"])
+        oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], seed, rnd,
+                      reqs=reqs)
+        spent += time.perf_counter() - t0
+        done_req += n
+        if spent >= budget_s or done_req >= 4 * wl.B:
+            break
+        n = max(1, min(4 * cores, wl.B, int(n * max(1.0, (budget_s - spent) / max(spent, 1e-3)))))
+    per_req = spent / done_req
+    rounds_per_s = 1.0 / (per_req * wl.B)
+    return rounds_per_s, cores, (f"oracle draft + verify (gamma+1 rows) of {done_req} requests of the "
+                                 f"{wl.name} workload, plus the plan each pass: {spent:.1f} s on {cores} "
+                                 f"threads, scaled to a {wl.B}-request round")
+
+
+def run_reference(args):
+    """The oracle itself as the reference arm (rank 0 only)."""
+    import torch
+    world, rank, local = dist_init(args)
+    if rank != 0:
+        return
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, pack_rows
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, device="cpu")
+    times = []
+    cores, sample = 1, ""
+    for i in range(args.warmup + args.steps):
+        v, cores, sample = oracle_sample(wl, inp, args.cpu_seconds / max(1, args.steps), wl.seed, 0)
+        if i >= args.warmup:
+            times.append(1.0 / v)
+    t = sum(times) / len(times)
+    val = 1.0 / t
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "rounds/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, wl.B * (wl.gamma + 1)),
+            "cpu_baseline": {"value": val, "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+    from speculative_decoding_head_gb300 import build as bmod
+    from speculative_decoding_head_gb300.binding import Workspace
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, hbm_bytes, make_inputs, pack_rows
+
+    world, rank, local = dist_init(args)
+    torch.cuda.set_device(local)
+    bmod.build()
+    wl = WORKLOADS[args.workload]
+    dev_inp = make_inputs(wl, device="cuda")
+    ws = Workspace.for_workload(wl)
+    seed, rnd = wl.seed, 0
+    s = torch.cuda.current_stream()
+
+    # one untimed round fixes this round's lengths; pack the target rows for them
+    out = {**ws.new_draft_outputs(), **ws.new_plan_outputs(), **ws.new_verify_outputs()}
+    for _ in range(max(1, wl.lag + 1)):
+        ws.draft(dev_inp["U"], dev_inp["W1"], dev_inp["W2"], dev_inp["anchor"], dev_inp["h"], dev_inp["w"],
+                 dev_inp["T"], seed, rnd, out=out)
+        ws.plan(out["conf"], dev_inp["sps"], out=out)
+    torch.cuda.synchronize()
+    lengths = out["lengths"].clone()
+    P = pack_rows(dev_inp["P_full"], lengths)
+    sum_len = int(lengths.sum().item())
+    P_full_cpu = dev_inp["P_full"].cpu() if (rank == 0 and not args.no_cpu_baseline) else None
+    del dev_inp["P_full"]
+    torch.cuda.empty_cache()
+
+    def step():
+        ws.round(dev_inp["U"], dev_inp["W1"], dev_inp["W2"], dev_inp["anchor"], dev_inp["h"], dev_inp["w"],
+                 dev_inp["T"], dev_inp["sps"], P, seed, rnd, out=out)
+
+    step()
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0, ws.device_status()
+    assert int(out["lengths"].sum().item()) == sum_len, "lengths changed between identical rounds"
+    launches_per_round = ws.last_launches
+
+    graph = None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            graph = g
+        except Exception as e:  # pragma: no cover - reported in the JSON line
+            print(f"# graph capture failed, timing direct calls: {e}", file=sys.stderr)
+            graph = None
+    run = graph.replay if graph is not None else step
+
+    for _ in range(max(3, args.warmup)):
+        run()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = ClockSampler(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(args.steps):
+        run()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, world)
+    assert ws.device_status() == 0
+
+    # stage times (direct calls, events on the launching stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    st = {"draft": 0.0, "plan": 0.0, "verify": 0.0}
+    reps = max(5, min(args.steps, 30))
+    for _ in range(reps):
+        ev[0].record(s)
+        ws.draft(dev_inp["U"], dev_inp["W1"], dev_inp["W2"], dev_inp["anchor"], dev_inp["h"], dev_inp["w"],
+                 dev_inp["T"], seed, rnd, out=out)
+        ev[1].record(s)
+        ws.plan(out["conf"], dev_inp["sps"], out=out)
+        ev[2].record(s)
+        ws.verify(P, out["row_off"], out["lengths"], dev_inp["anchor"], out["tokens"], out["pd_tok"], out["lse"],
+                  dev_inp["U"], dev_inp["W1"], dev_inp["W2"], seed, rnd, out=out)
+        ev[3].record(s)
+        torch.cuda.synchronize()
+        st["draft"] += ev[0].elapsed_time(ev[1]) / reps
+        st["plan"] += ev[1].elapsed_time(ev[2]) / reps
+        st["verify"] += ev[2].elapsed_time(ev[3]) / reps
+
+    bts = hbm_bytes(wl, sum_len)
+    peak, peak_kind = peaks()
+    t_round = ms * 1e-3
+    draft_bytes = bts["U"] + wl.gamma * bts["W2_per_step"]
+    draft_gbs = draft_bytes / (st["draft"] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": f"draft stage ({ws.draft_path})", "achieved": draft_gbs,
+                "peak": peak, "unit": "GB/s", "frac": draft_gbs / peak, "peak_kind": peak_kind,
+                "traffic": None, "alg_bytes_per_launch": draft_bytes,
+                "launch_ms": st["draft"]}
+
+    # end to end through the same C-ABI with host buffers: H2D of the round's
+    # inputs from pinned memory, the round, D2H of its results
+    e2e = None
+    if not args.no_e2e:
+        host = {k: dev_inp[k].cpu().pin_memory() for k in ("U", "h", "anchor")}
+        host["P"] = P.cpu().pin_memory()
+        dstage = {k: torch.empty_like(dev_inp[k]) for k in ("U", "h", "anchor")}
+        dstage["P"] = torch.empty_like(P)
+        res_host = {k: torch.empty(out[k].shape, dtype=out[k].dtype, pin_memory=True)
+                    for k in ("tokens", "lengths", "n_acc", "next_anchor")}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+
+        def e2e_step():
+            for k in host:
+                dstage[k].copy_(host[k], non_blocking=True)
+            ws.round(dstage["U"], dev_inp["W1"], dev_inp["W2"], dstage["anchor"], dstage["h"], dev_inp["w"],
+                     dev_inp["T"], dev_inp["sps"], dstage["P"], seed, rnd, out=out)
+            for k in res_host:
+                res_host[k].copy_(out[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n2 = max(3, min(args.steps, 10))
+        e0.record(s)
+        for _ in range(n2):
+            e2e_step()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms2 = max_over_ranks(e0.elapsed_time(e1) / n2, world)
+        e2e = {"value": world * 1e3 / ms2, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms2}
+        del host, dstage
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        inp_cpu = {k: dev_inp[k].cpu() for k in ("U", "W1", "W2", "anchor", "h", "w", "T", "sps")}
+        inp_cpu["P_full"] = P_full_cpu
+        v, cores, sample = oracle_sample(wl, inp_cpu, args.cpu_seconds, seed, rnd)
+        cpu_base = {"value": v, "unit": "rounds/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        value = world / t_round
+        emitted = int((out["n_acc"].to(torch.int64) + 1).sum().item())
+        line = {
+            "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(wl, sum_len),
+            "hbm_roofline": {"alg_bytes_per_round": bts["alg"], "alg_bytes_w2_once": bts["alg_w2_once"],
+                             "frac_of_8TBs": bts["alg"] / t_round / 1e9 / NORTH_STAR_BW,
+                             "frac_of_measured": bts["alg"] / t_round / 1e9 / peak,
+                             "frac_w2_once_of_measured": bts["alg_w2_once"] / t_round / 1e9 / peak},
+            "verified_positions_per_s": value * sum_len,
+            "emitted_tokens_per_round": emitted,
+            "stage_ms": st,
+            "roofline": roofline,
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": launches_per_round * args.steps,
+            "launches_per_round": launches_per_round,
+            "graph": graph is not None,
+            "draft_path": ws.draft_path,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

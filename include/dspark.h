@@ -1,0 +1,178 @@
+/*
+ * dspark.h -- C-ABI of the GB300 DSpark round library (libdspark.so).
+ *
+ * One DSpark round over a batch of B requests, in three calls:
+ *
+ *   dspark_markov_draft  Markov-head draft tail + confidence head.
+ *       "DeepSeek-V4.1 模型结构（6）：解码，DSpark", eq. (4) and (5):
+ *       p_k(v) = softmax_v(U_k(v) + W1[x_{k-1}] . W2[:, v]), x_0 = anchor,
+ *       sampled left to right for k = 1..gamma (section "Markov head", the
+ *       sequential loop); eq. (7) with the STS temperature of the
+ *       zdszero.github.io "spec_dspark" page (section "在 SGLang 里",
+ *       sigmoid(raw / T)): c_k = sigma((w^T [h_k; W1[x_{k-1}]]) / T_k).
+ *   dspark_plan          confidence-scheduled planner.
+ *       Same blog, sections "目标函数" and "贪心就能解"; deepseek.csdn.net
+ *       close reading §5.3 (Algorithm 1): survival a_{b,j} = prod_{i<=j} c_{b,i};
+ *       candidates are admitted in decreasing a while Theta = tau * SPS(B_tot)
+ *       rises. COMPACT_LAGGED is the asynchronous planner of the same
+ *       close reading §8: capacity K = argmax Theta over the full path on the
+ *       confidences of round t - lag, then the top-K current candidates.
+ *       lengths[b] in [1, gamma+1] counts the anchor ("spec_dspark", SGLang
+ *       section: the anchor is always verified).
+ *   dspark_verify        lossless ragged rejection-sampling verify.
+ *       Same blog, section "投机解码" and the derivation box;
+ *       "DSpark：不让大模型更聪明，而让它「吐字更快」" §02: accept x_{j+1} with
+ *       probability min(1, p_t(x_{j+1}) / p_d(x_{j+1})); at the first rejection
+ *       draw from norm(max(0, p_t - p_d)); if every verified draft passes, draw
+ *       the bonus token from the last verified target row.
+ *
+ * Conventions
+ *   - Every data pointer is a DEVICE pointer owned by the caller. The library
+ *     reads inputs and writes outputs during the call's stream work and keeps
+ *     no pointer past it. Inputs are const and must not alias outputs.
+ *   - Layouts are dense row-major: U [B, gamma, V] fp32; W1 [V, r] and
+ *     W2 [r, V] in the workspace's weight dtype (fp32 or bf16); h [B, gamma, H]
+ *     fp32; w [H + r] fp32 (hidden part first); T [gamma] fp32; per-position
+ *     outputs [B, gamma] with column k-1 for draft position k; P packed
+ *     [row_off[B], V] fp32 where rows row_off[b] + j, j < lengths[b], are the
+ *     target logits for the token after x_j (x_0 = anchor).
+ *   - Base pointers must be 16-byte aligned; V % 8 == 0 for bf16 weights.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and returns at once. Host-detectable errors (null pointer,
+ *     misalignment, bad dims) return a status and enqueue nothing.
+ *     Device-detected errors (non-finite confidence or SPS entry, token id out
+ *     of range, a grid-barrier timeout) set the workspace status word, the
+ *     kernels stop early and the outputs of that round are undefined; read it
+ *     with dspark_last_error after synchronising the stream.
+ *   - Random numbers come from Philox4x32-10 (Salmon et al., SC'11) with key
+ *     = seed and counter = (v >> 2, b, j, purpose << 24 | round mod 2^24);
+ *     the same (seed, round, inputs) always give the same outputs, whatever
+ *     the GPU's SM count.
+ *   - The workspace holds per-round scratch and the planner's confidence
+ *     ring; calls that share a workspace must be ordered on one stream.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that callers need no CUDA header. */
+typedef struct CUstream_st* dspark_stream_t;
+
+typedef enum {
+    DSPARK_OK = 0,
+    DSPARK_EINVAL = 1,        /* bad argument: null, misaligned, bad dims */
+    DSPARK_ECUDA = 2,         /* a CUDA runtime call failed */
+    DSPARK_ETIMEOUT = 3,      /* a grid barrier did not complete in time (device) */
+    DSPARK_ENUMERIC = 4,      /* non-finite or non-positive confidence/SPS (device) */
+    DSPARK_EUNSUPPORTED = 5,  /* valid but unsupported shape or mode */
+    DSPARK_ERANGE = 6         /* token id or length out of range (device) */
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_wdtype;
+
+typedef enum {
+    DSPARK_STATIC = 0,          /* no planner: every request verifies gamma + 1 rows */
+    DSPARK_COMPACT = 1,         /* Algorithm 1 with early stop */
+    DSPARK_COMPACT_LAGGED = 2   /* capacity from confidences `lag` rounds old, top-K now */
+} dspark_mode;
+
+typedef struct {
+    int B;                  /* requests, 1 .. 4096 */
+    int gamma;              /* draft positions, 1 .. 32 */
+    int V;                  /* vocabulary size */
+    int r;                  /* Markov rank, 1 .. 1024 */
+    int H;                  /* confidence-head hidden size, >= 0 */
+    dspark_wdtype wdtype;   /* storage type of W1 and W2 */
+    dspark_mode mode;
+    int lag;                /* lag depth for DSPARK_COMPACT_LAGGED, 1 .. 8 */
+} dspark_dims;
+
+typedef struct dspark_ws dspark_ws;
+
+/* Create a workspace for `dims` on the current CUDA device. This is the only
+ * call that allocates device memory (one arena: scratch, barrier words, the
+ * confidence ring, the status word). Returns EINVAL/EUNSUPPORTED/ECUDA. */
+dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out);
+
+/* Free the workspace (synchronises the device first). NULL is a no-op. */
+void dspark_ws_destroy(dspark_ws* ws);
+
+/* Clear the device status word and the lagged planner's round counter and
+ * ring, on `stream`. */
+dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream);
+
+/* Copy the device status word into *device_status (a synchronous 4-byte copy;
+ * synchronise the work's stream first). Returns the host status of the copy. */
+dspark_status dspark_last_error(dspark_ws* ws, int* device_status);
+
+/* Static text for a status code. */
+const char* dspark_status_string(int status);
+
+/* Kernels launched by the last call on this workspace (for accounting). */
+int dspark_last_launch_count(dspark_ws* ws);
+
+/* Name of the draft path the workspace will use ("tcgen05" or "simt"). */
+const char* dspark_draft_path(dspark_ws* ws);
+
+/*
+ * Draft x_1..x_gamma for every request. Outputs, each [B, gamma]:
+ *   tokens  int32   x_k
+ *   pd_tok  fp32    p_k(x_k), the draft probability of the drafted token
+ *   lse     fp32    log sum_v exp(U_k(v) + W1[x_{k-1}] . W2[:, v])
+ *   conf    fp32    c_k
+ * anchor [B] int32 in [0, V). Sampling: two-level Gumbel-max (vocabulary
+ * blocks of 64 tokens), temperature 1.
+ */
+dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                  const int32_t* anchor, const float* h, const float* w,
+                                  const float* T, uint64_t seed, uint64_t round,
+                                  int32_t* tokens, float* pd_tok, float* lse, float* conf,
+                                  dspark_stream_t stream);
+
+/*
+ * Verify lengths from the confidences conf [B, gamma] and the SPS table
+ * sps [1 + B * (gamma + 1)] (fp64; sps[n] = engine steps per second at n
+ * verify tokens; entry 0 unused). Outputs lengths [B] int32 in [1, gamma+1]
+ * and row_off [B + 1] int32, the exclusive scan of lengths (row_off[B] =
+ * total verify rows). STATIC mode ignores conf and sps. COMPACT_LAGGED pushes
+ * conf into the workspace ring; its first `lag` calls after a reset plan
+ * synchronously (Algorithm 1).
+ */
+dspark_status dspark_plan(dspark_ws* ws, const float* conf, const double* sps,
+                          int32_t* lengths, int32_t* row_off, dspark_stream_t stream);
+
+/*
+ * Verify. P packed [row_off[B], V] fp32 target logits; row_off and lengths as
+ * written by dspark_plan; anchor [B]; tokens, pd_tok, lse [B, gamma] as written
+ * by dspark_markov_draft; U, W1, W2 as given to it (the draft distribution at
+ * a rejected position is recomputed from them). Outputs n_accepted [B] (drafts
+ * accepted, 0 .. lengths[b]-1) and next_anchor [B] (residual or bonus token).
+ */
+dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_off,
+                            const int32_t* lengths, const int32_t* anchor, const int32_t* tokens,
+                            const float* pd_tok, const float* lse, const float* U,
+                            const void* W1, const void* W2, uint64_t seed, uint64_t round,
+                            int32_t* n_accepted, int32_t* next_anchor, dspark_stream_t stream);
+
+/*
+ * A whole round: draft, plan, then verify on P, which the caller has packed
+ * for the lengths this round produces (benchmark use: with fixed inputs and
+ * round the lengths are deterministic). Same arguments as the three calls.
+ */
+dspark_status dspark_round(dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                           const int32_t* anchor, const float* h, const float* w, const float* T,
+                           const double* sps, const float* P, uint64_t seed, uint64_t round,
+                           int32_t* tokens, float* pd_tok, float* lse, float* conf,
+                           int32_t* lengths, int32_t* row_off, int32_t* n_accepted,
+                           int32_t* next_anchor, dspark_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSPARK_H */

@@ -1,0 +1,225 @@
+"""Python binding of libdspark.so (ctypes; argument marshalling only).
+
+Every step of a round runs in the library's CUDA kernels. PyTorch supplies
+device memory and the current stream. If the library has not been built the
+binding raises; there is no CPU fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from typing import Dict, Optional
+
+import torch
+
+from .build import LIB_PATH
+
+MODES = {"static": 0, "compact": 1, "lagged": 2}
+WDTYPES = {"f32": 0, "bf16": 1}
+
+SYMBOLS = [
+    "dspark_ws_create", "dspark_ws_destroy", "dspark_ws_reset", "dspark_last_error",
+    "dspark_status_string", "dspark_last_launch_count", "dspark_draft_path",
+    "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round",
+]
+
+
+class DsparkError(RuntimeError):
+    pass
+
+
+class Dims(C.Structure):
+    _fields_ = [("B", C.c_int), ("gamma", C.c_int), ("V", C.c_int), ("r", C.c_int), ("H", C.c_int),
+                ("wdtype", C.c_int), ("mode", C.c_int), ("lag", C.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> C.CDLL:
+    """Load libdspark.so (built by __graft_entry__.build() or build.py)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise DsparkError(f"libdspark.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = C.CDLL(LIB_PATH)
+        P, i32, u64 = C.c_void_p, C.c_int, C.c_uint64
+        lib.dspark_ws_create.argtypes = [C.POINTER(Dims), C.POINTER(P)]
+        lib.dspark_ws_create.restype = i32
+        lib.dspark_ws_destroy.argtypes = [P]
+        lib.dspark_ws_destroy.restype = None
+        lib.dspark_ws_reset.argtypes = [P, P]
+        lib.dspark_ws_reset.restype = i32
+        lib.dspark_last_error.argtypes = [P, C.POINTER(i32)]
+        lib.dspark_last_error.restype = i32
+        lib.dspark_status_string.argtypes = [i32]
+        lib.dspark_status_string.restype = C.c_char_p
+        lib.dspark_last_launch_count.argtypes = [P]
+        lib.dspark_last_launch_count.restype = i32
+        lib.dspark_draft_path.argtypes = [P]
+        lib.dspark_draft_path.restype = C.c_char_p
+        lib.dspark_markov_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, P, P, P, P]
+        lib.dspark_markov_draft.restype = i32
+        lib.dspark_plan.argtypes = [P, P, P, P, P, P]
+        lib.dspark_plan.restype = i32
+        lib.dspark_verify.argtypes = [P, P, P, P, P, P, P, P, P, P, P, u64, u64, P, P, P]
+        lib.dspark_verify.restype = i32
+        lib.dspark_round.argtypes = [P] * 10 + [u64, u64] + [P] * 9
+        lib.dspark_round.restype = i32
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().dspark_status_string(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != 0:
+        raise DsparkError(f"{what}: {status_string(code)} ({code})")
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="") -> C.c_void_p:
+    if t is None:
+        return C.c_void_p(0)
+    if not t.is_cuda:
+        raise DsparkError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise DsparkError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise DsparkError(f"{name} must be {dtype}, got {t.dtype}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+class Workspace:
+    """One DSpark workspace: the library's scratch arena for a fixed shape."""
+
+    def __init__(self, B: int, gamma: int, V: int, r: int, H: int, wdtype: str = "bf16",
+                 mode: str = "compact", lag: int = 2):
+        self.lib = load()
+        self.dims = Dims(B, gamma, V, r, H, WDTYPES[wdtype], MODES[mode], lag if mode == "lagged" else 0)
+        self.wdtype = torch.bfloat16 if wdtype == "bf16" else torch.float32
+        self._h = C.c_void_p()
+        _check(self.lib.dspark_ws_create(C.byref(self.dims), C.byref(self._h)), "dspark_ws_create")
+
+    @classmethod
+    def for_workload(cls, wl) -> "Workspace":
+        return cls(wl.B, wl.gamma, wl.V, wl.r, wl.H, wl.wdtype, wl.mode, wl.lag or 2)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) and self._h.value:
+            self.lib.dspark_ws_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ state
+    @property
+    def handle(self) -> C.c_void_p:
+        return self._h
+
+    @property
+    def draft_path(self) -> str:
+        return self.lib.dspark_draft_path(self._h).decode()
+
+    @property
+    def last_launches(self) -> int:
+        return int(self.lib.dspark_last_launch_count(self._h))
+
+    def reset(self, stream=None) -> None:
+        _check(self.lib.dspark_ws_reset(self._h, _stream(stream)), "dspark_ws_reset")
+
+    def device_status(self) -> int:
+        v = C.c_int(0)
+        _check(self.lib.dspark_last_error(self._h, C.byref(v)), "dspark_last_error")
+        return int(v.value)
+
+    # ------------------------------------------------------------ outputs
+    def new_draft_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:
+        B, g = self.dims.B, self.dims.gamma
+        return {"tokens": torch.empty((B, g), dtype=torch.int32, device=device),
+                "pd_tok": torch.empty((B, g), dtype=torch.float32, device=device),
+                "lse": torch.empty((B, g), dtype=torch.float32, device=device),
+                "conf": torch.empty((B, g), dtype=torch.float32, device=device)}
+
+    def new_plan_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:
+        B = self.dims.B
+        return {"lengths": torch.empty(B, dtype=torch.int32, device=device),
+                "row_off": torch.empty(B + 1, dtype=torch.int32, device=device)}
+
+    def new_verify_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:
+        B = self.dims.B
+        return {"n_acc": torch.empty(B, dtype=torch.int32, device=device),
+                "next_anchor": torch.empty(B, dtype=torch.int32, device=device)}
+
+    # ------------------------------------------------------------ calls
+    def draft(self, U, W1, W2, anchor, h, w, T, seed: int, rnd: int, out=None, stream=None):
+        out = out or self.new_draft_outputs(U.device)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_markov_draft(
+            self._h, _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"), _ptr(W2, self.wdtype, "W2"),
+            _ptr(anchor, i32, "anchor"), _ptr(h, f32, "h") if self.dims.H > 0 else C.c_void_p(0),
+            _ptr(w, f32, "w"), _ptr(T, f32, "T"), int(seed), int(rnd),
+            _ptr(out["tokens"], i32, "tokens"), _ptr(out["pd_tok"], f32, "pd_tok"),
+            _ptr(out["lse"], f32, "lse"), _ptr(out["conf"], f32, "conf"), _stream(stream))
+        _check(code, "dspark_markov_draft")
+        return out
+
+    def plan(self, conf, sps, out=None, stream=None):
+        out = out or self.new_plan_outputs(conf.device)
+        code = self.lib.dspark_plan(self._h, _ptr(conf, torch.float32, "conf"),
+                                    _ptr(sps, torch.float64, "sps"),
+                                    _ptr(out["lengths"], torch.int32, "lengths"),
+                                    _ptr(out["row_off"], torch.int32, "row_off"), _stream(stream))
+        _check(code, "dspark_plan")
+        return out
+
+    def verify(self, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed: int, rnd: int,
+               out=None, stream=None):
+        out = out or self.new_verify_outputs(P.device)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_verify(
+            self._h, _ptr(P, f32, "P"), _ptr(row_off, i32, "row_off"), _ptr(lengths, i32, "lengths"),
+            _ptr(anchor, i32, "anchor"), _ptr(tokens, i32, "tokens"), _ptr(pd_tok, f32, "pd_tok"),
+            _ptr(lse, f32, "lse"), _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"),
+            _ptr(W2, self.wdtype, "W2"), int(seed), int(rnd), _ptr(out["n_acc"], i32, "n_acc"),
+            _ptr(out["next_anchor"], i32, "next_anchor"), _stream(stream))
+        _check(code, "dspark_verify")
+        return out
+
+    def round(self, U, W1, W2, anchor, h, w, T, sps, P, seed: int, rnd: int, out=None, stream=None):
+        """draft -> plan -> verify on P packed for this round's lengths."""
+        if out is None:
+            out = {**self.new_draft_outputs(U.device), **self.new_plan_outputs(U.device),
+                   **self.new_verify_outputs(U.device)}
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_round(
+            self._h, _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"), _ptr(W2, self.wdtype, "W2"),
+            _ptr(anchor, i32, "anchor"), _ptr(h, f32, "h") if self.dims.H > 0 else C.c_void_p(0),
+            _ptr(w, f32, "w"), _ptr(T, f32, "T"), _ptr(sps, torch.float64, "sps"), _ptr(P, f32, "P"),
+            int(seed), int(rnd), _ptr(out["tokens"], i32, "tokens"), _ptr(out["pd_tok"], f32, "pd_tok"),
+            _ptr(out["lse"], f32, "lse"), _ptr(out["conf"], f32, "conf"),
+            _ptr(out["lengths"], i32, "lengths"), _ptr(out["row_off"], i32, "row_off"),
+            _ptr(out["n_acc"], i32, "n_acc"), _ptr(out["next_anchor"], i32, "next_anchor"),
+            _stream(stream))
+        _check(code, "dspark_round")
+        return out

@@ -1,0 +1,139 @@
+// dspark_common.cuh -- device helpers shared by the DSpark kernels.
+//
+// Random stream: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies
+// (0xD2511F53 on word 0, 0xCD9E8D57 on word 2) with the key bumped by the Weyl
+// constants 0x9E3779B9 / 0xBB67AE85 between rounds. Counter layout of this
+// library: (v >> 2, b, j, purpose << 24 | round mod 2^24), key = seed, output
+// word v & 3. Uniforms live on the odd grid u = (2m + 1) 2^-24 (never 0 or 1,
+// exact in fp32); Gumbel noise is -log(-log u).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// Stream purposes (counter word 3, bits 24..31).
+enum : uint32_t {
+  kDraftBlock = 1,
+  kDraftToken = 2,
+  kAccept = 3,
+  kBonusBlock = 4,
+  kBonusToken = 5,
+  kResidBlock = 6,
+  kResidToken = 7,
+};
+
+// Width of the vocabulary blocks of the two-level Gumbel-max sampler: a block
+// is drawn by argmax_s (log mass_s + G_s), then a token inside it by
+// argmax_v (log weight_v + G_v); together an exact draw from the softmax.
+constexpr int kBlockW = 64;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+struct Rng {
+  uint32_t k0, k1, tag;  // tag = purpose << 24 | round mod 2^24 (without purpose)
+  __host__ __device__ static Rng make(uint64_t seed, uint64_t round) {
+    Rng r;
+    r.k0 = (uint32_t)(seed & 0xFFFFFFFFull);
+    r.k1 = (uint32_t)(seed >> 32);
+    r.tag = (uint32_t)(round & 0xFFFFFFull);
+    return r;
+  }
+  // all four words of the counter block that holds token v
+  __device__ __forceinline__ uint4 block4(uint32_t purpose, uint32_t b, uint32_t j, uint32_t v) const {
+    return philox4x32_10(make_uint4(v >> 2, b, j, (purpose << 24) | tag), k0, k1);
+  }
+  __device__ __forceinline__ uint32_t word(uint32_t purpose, uint32_t b, uint32_t j, uint32_t v) const {
+    const uint4 o = block4(purpose, b, j, v);
+    const uint32_t s = v & 3u;
+    return s == 0 ? o.x : (s == 1 ? o.y : (s == 2 ? o.z : o.w));
+  }
+};
+
+__device__ __forceinline__ float u01(uint32_t x) {
+  return (float)(2u * (x >> 9) + 1u) * 0x1p-24f;  // exact: 2m+1 < 2^24
+}
+
+__device__ __forceinline__ float gumbel(uint32_t x) { return -logf(-logf(u01(x))); }
+
+__device__ __forceinline__ float ld_w(const void* W, int bf16, size_t i) {
+  if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(W)[i]);
+  return reinterpret_cast<const float*>(W)[i];
+}
+
+// Largest key wins; equal keys go to the smaller index (the first maximum).
+// "Nothing yet" is {-inf, kNoIdx}.
+constexpr int kNoIdx = 0x7FFFFFFF;
+struct KeyIdx {
+  float key;
+  int idx;
+};
+__device__ __forceinline__ KeyIdx key_none() { return KeyIdx{-INFINITY, kNoIdx}; }
+__device__ __forceinline__ KeyIdx better(KeyIdx a, KeyIdx b) {
+  return (b.key > a.key || (b.key == a.key && b.idx < a.idx)) ? b : a;
+}
+__device__ __forceinline__ KeyIdx warp_best(KeyIdx x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    KeyIdx y;
+    y.key = __shfl_xor_sync(0xFFFFFFFFu, x.key, o);
+    y.idx = __shfl_xor_sync(0xFFFFFFFFu, x.idx, o);
+    x = better(x, y);
+  }
+  return x;
+}
+
+// (max, sum of exp(x - max)) pair combination for online log-sum-exp.
+struct MS {
+  float m, s;
+};
+__device__ __forceinline__ MS ms_combine(MS a, MS b) {
+  if (a.m == -INFINITY) return b;
+  if (b.m == -INFINITY) return a;
+  const float m = fmaxf(a.m, b.m);
+  return MS{m, a.s * __expf(a.m - m) + b.s * __expf(b.m - m)};
+}
+__device__ __forceinline__ MS warp_ms(MS x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    MS y;
+    y.m = __shfl_xor_sync(0xFFFFFFFFu, x.m, o);
+    y.s = __shfl_xor_sync(0xFFFFFFFFu, x.s, o);
+    x = ms_combine(x, y);
+  }
+  return x;
+}
+__device__ __forceinline__ float ms_log(MS a) { return a.m == -INFINITY ? -INFINITY : a.m + logf(a.s); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+// First error wins; kernels poll it to stop early.
+__device__ __forceinline__ void raise_status(int* st, int code) { atomicCAS(st, 0, code); }
+
+}  // namespace dspark

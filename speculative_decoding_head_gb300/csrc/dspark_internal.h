@@ -1,0 +1,109 @@
+// dspark_internal.h -- workspace layout and kernel launchers shared by the
+// translation units of libdspark.so (not part of the public C-ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dspark.h"
+
+namespace dspark {
+
+// Tunables of the launch shapes (none of them changes a result).
+constexpr int kSweepChunk = 16384;  // target-logit elements per verify-sweep work item
+constexpr int kResidChunks = 32;    // CTAs per rejected request in the SIMT residual pass
+
+struct DraftArgs {
+  const float* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* anchor;
+  const float* h;
+  const float* w;
+  const float* T;
+  uint64_t seed, round;
+  int32_t* tokens;
+  float* pd_tok;
+  float* lse;
+  float* conf;
+};
+
+struct VerifyArgs {
+  const float* P;
+  const int32_t* row_off;
+  const int32_t* lengths;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const float* pd_tok;
+  const float* lse;
+  const float* U;
+  const void* W1;
+  const void* W2;
+  uint64_t seed, round;
+  int32_t* n_acc;
+  int32_t* next_anchor;
+};
+
+// Device scratch carved out of one arena by dspark_ws_create.
+struct Scratch {
+  int* status;            // [1] first device error, 0 = none
+  float* s_h;             // [B*gamma] hidden half of the confidence logit
+  float* blk;             // [B*nblk] block log-masses of one draft step (SIMT path)
+  float* ring;            // [(lag+1)*B*gamma] confidence ring of the lagged planner
+  uint32_t* plan_round;   // [1] rounds planned since the last reset
+  float4* vpart;          // [B*(gamma+1)*S] verify-sweep partials (m, s, key, block)
+  int* vflag;             // [B] 1 = next anchor comes from the residual
+  int* vrow;              // [B] packed row of the first rejection
+  float* vlset;           // [B] target log-sum-exp of that row
+  float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
+  // persistent tcgen05 draft kernel
+  float4* dpart;          // [grid*rowsTotal] per-CTA (max, sum, key, block)
+  float* drec;            // [grid*rowsTotal*64] per-CTA z values of its best block
+  unsigned* barrier;      // [4] grid-barrier words
+  int32_t* xbuf;          // [B] current x_{k-1}
+};
+
+struct Geometry {
+  int nblk;     // ceil(V / 64)
+  int S;        // verify-sweep items per row
+  int chunk;    // elements per verify-sweep item (multiple of 64)
+  int num_sms;
+  // persistent draft kernel
+  int tc_ok;        // tcgen05 path usable for these dims
+  int tc_grid;      // CTAs of the persistent draft kernel
+  int tc_groups;    // 128-row groups
+};
+
+}  // namespace dspark
+
+struct dspark_ws {
+  dspark_dims d;
+  int device;
+  void* arena;
+  size_t arena_bytes;
+  dspark::Scratch s;
+  dspark::Geometry geo;
+  int last_launches;
+};
+
+namespace dspark {
+
+// Launchers: return cudaGetLastError() of their launches; add their launch
+// count to *launches.
+cudaError_t launch_conf_hidden(const dspark_ws* ws, const float* h, const float* w, cudaStream_t st,
+                               int* launches);
+cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches);
+cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
+                        int32_t* row_off, cudaStream_t st, int* launches);
+cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t st, int* launches);
+
+// Whether the tcgen05 draft kernel supports these dims, and its launch shape.
+int draft_tc_supported(const dspark_dims& d);
+cudaError_t draft_tc_configure(dspark_ws* ws);
+size_t draft_tc_scratch_rows(const dspark_dims& d, int grid);
+
+size_t plan_smem_bytes(const dspark_dims& d);
+cudaError_t plan_configure();
+
+}  // namespace dspark

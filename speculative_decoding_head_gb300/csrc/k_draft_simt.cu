@@ -1,0 +1,233 @@
+// k_draft_simt.cu -- Markov-head draft tail on CUDA cores (fp32 FMA).
+//
+// "DeepSeek-V4.1 模型结构（6）：解码，DSpark", eq. (4)/(5) and the sequential
+// loop of section "Markov head": for k = 1..gamma the logits of position k
+// are z = U_k + W1[x_{k-1}] W2 (x_0 = anchor) and x_k ~ softmax(z); eq. (7)
+// gives c_k = sigma((w^T [h_k; W1[x_{k-1}]]) / T_k).
+//
+// This path serves every weight dtype and rank (the tiny fp32 workload, and
+// as a plain baseline of the tensor-core path). Per step two kernels run:
+//   k_draft_blocks  grid (chunks, B): z for every token, folded into the
+//                   log-mass of each 64-token vocabulary block;
+//   k_draft_pick    grid (B): log-sum-exp over blocks, the block draw
+//                   argmax_s(log mass_s + G_s), then z of the 64 tokens of the
+//                   drawn block recomputed and the token draw
+//                   argmax_v(z_v + G_v); also c_k.
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+constexpr int kSimtThreads = 256;
+
+// s_h[row] = sum_{i<H} w[i] h[row, i]: the part of the confidence logit that
+// does not depend on drafted tokens (one warp per row of h).
+__global__ void __launch_bounds__(256) k_conf_hidden(const float* __restrict__ h,
+                                                     const float* __restrict__ w, int H, int rows,
+                                                     float* __restrict__ s_h) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (row >= rows) return;
+  const float* hr = h + (size_t)row * H;
+  float acc = 0.f;
+  if ((H & 3) == 0) {
+    const float4* h4 = reinterpret_cast<const float4*>(hr);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    for (int i = lane; i < H / 4; i += 32) {
+      const float4 a = __ldcs(h4 + i);  // streamed once
+      const float4 c = __ldg(w4 + i);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+      acc = fmaf(a.z, c.z, acc);
+      acc = fmaf(a.w, c.w, acc);
+    }
+  } else {
+    for (int i = lane; i < H; i += 32) acc = fmaf(hr[i], w[i], acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) s_h[row] = acc;
+}
+
+__device__ __forceinline__ int prev_token(const int32_t* anchor, const int32_t* tokens, int b, int g,
+                                          int k) {
+  return k == 1 ? anchor[b] : tokens[(size_t)b * g + (k - 2)];
+}
+
+// z_v - U_k(v) = sum_i e_i W2[i, v] for one token (fp32 FMA in i order)
+template <int BF16>
+__device__ __forceinline__ float markov_dot(const float* __restrict__ e, const void* __restrict__ W2,
+                                            int r, int V, int v) {
+  float acc = 0.f;
+  for (int i = 0; i < r; ++i) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
+  return acc;
+}
+
+template <int BF16>
+__global__ void __launch_bounds__(kSimtThreads)
+    k_draft_blocks(const float* __restrict__ U, const void* __restrict__ W1, const void* __restrict__ W2,
+                   const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int g, int V,
+                   int r, int k, int nblk, float* __restrict__ blk, int* __restrict__ status) {
+  extern __shared__ float e[];  // W1[x_{k-1}] as fp32, [r]
+  const int b = blockIdx.y;
+  const int x = prev_token(anchor, tokens, b, g, k);
+  if (x < 0 || x >= V) {
+    if (threadIdx.x == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  for (int i = threadIdx.x; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+  __syncthreads();
+  const float* Urow = U + ((size_t)b * g + (k - 1)) * V;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpc = blockDim.x >> 5;
+  for (int s = blockIdx.x * wpc + warp; s < nblk; s += gridDim.x * wpc) {
+    const int v0 = s * kBlockW + lane, v1 = v0 + 32;
+    float z0 = -INFINITY, z1 = -INFINITY;
+    if (v0 < V) z0 = Urow[v0] + markov_dot<BF16>(e, W2, r, V, v0);
+    if (v1 < V) z1 = Urow[v1] + markov_dot<BF16>(e, W2, r, V, v1);
+    const float m = warp_max(fmaxf(z0, z1));
+    float t = (v0 < V ? expf(z0 - m) : 0.f) + (v1 < V ? expf(z1 - m) : 0.f);
+    t = warp_sum(t);
+    if (lane == 0) blk[(size_t)b * nblk + s] = m + logf(t);
+  }
+}
+
+template <int BF16>
+__global__ void __launch_bounds__(kSimtThreads)
+    k_draft_pick(const float* __restrict__ U, const void* __restrict__ W1, const void* __restrict__ W2,
+                 const int32_t* __restrict__ anchor, const float* __restrict__ w,
+                 const float* __restrict__ T, const float* __restrict__ s_h, int g, int V, int r, int H,
+                 int k, int nblk, const float* __restrict__ blk, Rng rng, int32_t* __restrict__ tokens,
+                 float* __restrict__ pd_tok, float* __restrict__ lse_out, float* __restrict__ conf,
+                 int* __restrict__ status) {
+  extern __shared__ float e[];  // [r]
+  __shared__ float red_f[32];
+  __shared__ MS red_ms[32];
+  __shared__ KeyIdx red_k[32];
+  __shared__ float zpart[4][kBlockW];
+  __shared__ float zblk[kBlockW];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  const int x = prev_token(anchor, tokens, b, g, k);
+  if (x < 0 || x >= V) {
+    if (tid == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+  __syncthreads();
+  const size_t o = (size_t)b * g + (k - 1);
+
+  // eq. (7): c_k = sigma((s_h + w_r . W1[x_{k-1}]) / T_k)
+  float cr = 0.f;
+  for (int i = tid; i < r; i += blockDim.x) cr = fmaf(w[H + i], e[i], cr);
+  cr = warp_sum(cr);
+  if (lane == 0) red_f[warp] = cr;
+  // log-sum-exp over the block log-masses
+  MS ms{-INFINITY, 0.f};
+  for (int s = tid; s < nblk; s += blockDim.x) ms = ms_combine(ms, MS{blk[(size_t)b * nblk + s], 1.f});
+  ms = warp_ms(ms);
+  if (lane == 0) red_ms[warp] = ms;
+  // block draw: argmax_s (log mass_s + G_s)
+  KeyIdx kb = key_none();
+  for (int s = tid; s < nblk; s += blockDim.x) {
+    const float lm = blk[(size_t)b * nblk + s];
+    if (lm > -INFINITY) kb = better(kb, KeyIdx{lm + gumbel(rng.word(kDraftBlock, b, k, s)), s});
+  }
+  kb = warp_best(kb);
+  if (lane == 0) red_k[warp] = kb;
+  __syncthreads();
+  if (warp == 0) {
+    float c = lane < nw ? red_f[lane] : 0.f;
+    c = warp_sum(c);
+    MS m2 = lane < nw ? red_ms[lane] : MS{-INFINITY, 0.f};
+    m2 = warp_ms(m2);
+    KeyIdx k2 = lane < nw ? red_k[lane] : key_none();
+    k2 = warp_best(k2);
+    if (lane == 0) {
+      const float raw = s_h[o] + c;
+      const float cf = 1.f / (1.f + expf(-raw / T[k - 1]));
+      if (!isfinite(cf)) raise_status(status, DSPARK_ENUMERIC);
+      conf[o] = cf;
+      red_f[0] = ms_log(m2);
+      red_k[0] = k2;
+    }
+  }
+  __syncthreads();
+  const float L = red_f[0];
+  const int sb = red_k[0].idx;
+  if (sb == kNoIdx) {
+    if (tid == 0) raise_status(status, DSPARK_ENUMERIC);
+    return;
+  }
+  // token draw inside block sb: recompute z for its 64 tokens (4 partial dots)
+  {
+    const int vl = tid & (kBlockW - 1), q = tid >> 6;
+    const int v = sb * kBlockW + vl;
+    if (q < 4) {
+      float acc = 0.f;
+      if (v < V)
+        for (int i = q; i < r; i += 4) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
+      zpart[q][vl] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < kBlockW) {
+    const int v = sb * kBlockW + tid;
+    float z = -INFINITY;
+    if (v < V) z = U[o * V + v] + ((zpart[0][tid] + zpart[1][tid]) + (zpart[2][tid] + zpart[3][tid]));
+    zblk[tid] = z;
+    KeyIdx kt = key_none();
+    if (v < V) kt = KeyIdx{z + gumbel(rng.word(kDraftToken, b, k, v)), v};
+    kt = warp_best(kt);
+    if (lane == 0) red_k[1 + warp] = kt;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const KeyIdx kt = better(red_k[1], red_k[2]);
+    int xk = kt.idx;
+    if (xk == kNoIdx) {  // only non-finite logits get here
+      raise_status(status, DSPARK_ENUMERIC);
+      xk = sb * kBlockW;
+    }
+    tokens[o] = xk;
+    pd_tok[o] = expf(zblk[xk - sb * kBlockW] - L);
+    lse_out[o] = L;
+  }
+}
+
+cudaError_t launch_conf_hidden(const dspark_ws* ws, const float* h, const float* w, cudaStream_t st,
+                               int* launches) {
+  const int rows = ws->d.B * ws->d.gamma;
+  if (ws->d.H == 0) return cudaMemsetAsync(ws->s.s_h, 0, sizeof(float) * rows, st);
+  const int wpc = 4;
+  k_conf_hidden<<<(rows + wpc - 1) / wpc, 32 * wpc, 0, st>>>(h, w, ws->d.H, rows, ws->s.s_h);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+template <int BF16>
+static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st,
+                                   int* launches) {
+  const dspark_dims& d = ws->d;
+  const int nblk = ws->geo.nblk;
+  const size_t smem = sizeof(float) * d.r;
+  const int wpc = kSimtThreads / 32;
+  int chunks = (nblk + 4 * wpc - 1) / (4 * wpc);  // about 4 blocks per warp
+  if (chunks < 1) chunks = 1;
+  const Rng rng = Rng::make(a.seed, a.round);
+  for (int k = 1; k <= d.gamma; ++k) {
+    k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
+        a.U, a.W1, a.W2, a.anchor, a.tokens, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+    k_draft_pick<BF16><<<d.B, kSimtThreads, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h,
+                                                       d.gamma, d.V, d.r, d.H, k, nblk, ws->s.blk, rng,
+                                                       a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
+    *launches += 2;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches) {
+  if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches);
+  return draft_simt_impl<0>(ws, a, st, launches);
+}
+
+}  // namespace dspark

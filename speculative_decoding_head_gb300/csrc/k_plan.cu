@@ -1,0 +1,295 @@
+// k_plan.cu -- confidence-scheduled planner (one CTA, fp64).
+//
+// "DeepSeek-V4.1 模型结构（6）：解码，DSpark", sections "目标函数" and
+// "贪心就能解"; deepseek.csdn.net close reading §5.3 (Algorithm 1):
+//   a_{b,j} = prod_{i<=j} c_{b,i}                      (prefix survival)
+//   B_tot = sum_b (1 + l_b),  tau = sum_b (1 + sum_{j<=l_b} a_{b,j})
+//   Theta = tau * SPS(B_tot)
+// Candidates (b, j) are taken in decreasing a (ties: smaller j, then smaller
+// b) and admitted one at a time while Theta strictly rises; because a is
+// non-increasing in j, the admitted set is a prefix of every request.
+// The asynchronous planner of the close reading's §8 takes the capacity
+// K = argmax_m Theta_m over the whole path (no early stop; first maximum) on
+// the confidences of round t - lag, then admits the K best current
+// candidates. "spec_dspark" (section "在 SGLang 里"): lengths lie in
+// [1, gamma+1] because the anchor is always verified.
+//
+// Layout: survival values are sorted as 64-bit patterns of non-negative
+// doubles (their integer order is their numeric order) with a 32-bit id
+// (j-1)*B + b that carries the tie order.
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+
+namespace dspark {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxCand = 8192;  // B * gamma supported by the one-CTA planner
+
+__host__ __device__ inline int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+size_t plan_smem_bytes(const dspark_dims& d) {
+  const int Mp = pow2_at_least(d.B * d.gamma < 2 ? 2 : d.B * d.gamma);
+  return (size_t)Mp * (sizeof(unsigned long long) + sizeof(unsigned) + sizeof(double)) +
+         sizeof(int) * (size_t)(d.B + 1) + 64;
+}
+
+struct PlanSmem {
+  unsigned long long* key;  // [Mp] bits of a
+  unsigned* id;             // [Mp]
+  double* pre;              // [Mp] exclusive prefix sums of sorted a
+  int* cnt;                 // [B]
+};
+
+// "x goes before y": larger a first, then smaller id
+__device__ __forceinline__ bool before(unsigned long long ka, unsigned ia, unsigned long long kb, unsigned ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+// Fill and sort the candidates of confidences `c` [B, g]. Returns via smem.
+__device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem sm, int* status) {
+  const int M = B * g;
+  for (int i = threadIdx.x; i < Mp; i += blockDim.x) {
+    sm.key[i] = 0ull;
+    sm.id[i] = 0xFFFFFFFFu;  // padding sorts last
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    double a = 1.0;
+    for (int j = 1; j <= g; ++j) {
+      const float cf = c[(size_t)b * g + (j - 1)];
+      if (!(cf >= 0.f && cf <= 1.f)) raise_status(status, DSPARK_ENUMERIC);  // also catches NaN
+      a = __dmul_rn(a, (double)cf);
+      const int i = (j - 1) * B + b;
+      sm.key[i] = (unsigned long long)__double_as_longlong(a);
+      sm.id[i] = (unsigned)i;
+    }
+  }
+  __syncthreads();
+  (void)M;
+  // bitonic sort into "before" order
+  for (int size = 2; size <= Mp; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < Mp / 2; t += blockDim.x) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;  // this half ends in "before" order
+        const unsigned long long kl = sm.key[lo], kh = sm.key[hi];
+        const unsigned il = sm.id[lo], ih = sm.id[hi];
+        const bool swap = up ? before(kh, ih, kl, il) : before(kl, il, kh, ih);
+        if (swap) {
+          sm.key[lo] = kh;
+          sm.key[hi] = kl;
+          sm.id[lo] = ih;
+          sm.id[hi] = il;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// pre[m] = sum_{i<m} a_(i) for m = 0..Mp-1 (padding contributes 0)
+__device__ void prefix_sums(int Mp, PlanSmem sm, double* warp_tot) {
+  const int T = blockDim.x;
+  const int per = (Mp + T - 1) / T;
+  const int lo = threadIdx.x * per;
+  double loc = 0.0;
+  for (int i = lo; i < lo + per && i < Mp; ++i) loc += __longlong_as_double((long long)sm.key[i]);
+  // exclusive scan of the per-thread totals
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = T >> 5;
+    double x = lane < nw ? warp_tot[lane] : 0.0;
+    double inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane < nw) warp_tot[lane] = inc - x;  // exclusive
+  }
+  __syncthreads();
+  double run = warp_tot[warp] + (incl - loc);
+  for (int i = lo; i < lo + per && i < Mp; ++i) {
+    sm.pre[i] = run;
+    run += __longlong_as_double((long long)sm.key[i]);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ double theta_at(const double* sps, int B, double pre_m, int m) {
+  return ((double)B + pre_m) * sps[B + m];
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    k_plan(const float* __restrict__ conf, const double* __restrict__ sps, int B, int g, int mode, int lag,
+           float* __restrict__ ring, uint32_t* __restrict__ plan_round, int32_t* __restrict__ lengths,
+           int32_t* __restrict__ row_off, int* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ double warp_tot[32];
+  __shared__ double warp_bv[32];
+  __shared__ int warp_bm[32];
+  __shared__ int warp_int[32];
+  __shared__ int s_cut;
+  __shared__ int s_bestm;
+  const int M = B * g;
+  const int Mp = pow2_at_least(M < 2 ? 2 : M);
+  PlanSmem sm;
+  sm.key = reinterpret_cast<unsigned long long*>(smem_raw);
+  sm.pre = reinterpret_cast<double*>(sm.key + Mp);
+  sm.id = reinterpret_cast<unsigned*>(sm.pre + Mp);
+  sm.cnt = reinterpret_cast<int*>(sm.id + Mp);
+
+  for (int b = threadIdx.x; b < B; b += blockDim.x) sm.cnt[b] = 0;
+  int cut = 0;
+  if (mode != DSPARK_STATIC) {
+    // validate the SPS entries the search can reach
+    for (int n = 1 + threadIdx.x; n <= B + M; n += blockDim.x)
+      if (!(sps[n] > 0.0) || !isfinite(sps[n])) raise_status(status, DSPARK_ENUMERIC);
+    const uint32_t t = *plan_round;
+    const float* cnow = conf;
+    bool lagged = false;
+    if (mode == DSPARK_COMPACT_LAGGED) {
+      const int depth = lag + 1;
+      float* slot = ring + (size_t)(t % depth) * M;
+      for (int i = threadIdx.x; i < M; i += blockDim.x) slot[i] = conf[i];
+      lagged = t >= (uint32_t)lag;
+      __syncthreads();
+      if (lagged) {
+        // capacity from the confidences of round t - lag: full-path argmax
+        const float* clag = ring + (size_t)((t - lag) % depth) * M;
+        sort_candidates(clag, B, g, Mp, sm, status);
+        prefix_sums(Mp, sm, warp_tot);
+        // first maximum of Theta_m, m = 0..M
+        double bv = -1.0;
+        int bm = 0x7FFFFFFF;
+        for (int m = threadIdx.x; m <= M; m += blockDim.x) {
+          const double pm = m < Mp ? sm.pre[m] : sm.pre[Mp - 1] + __longlong_as_double((long long)sm.key[Mp - 1]);
+          const double th = theta_at(sps, B, pm, m);
+          if (th > bv) {
+            bv = th;
+            bm = m;
+          }
+        }
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const double ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+          const int om = __shfl_xor_sync(0xFFFFFFFFu, bm, o);
+          if (ov > bv || (ov == bv && om < bm)) {
+            bv = ov;
+            bm = om;
+          }
+        }
+        if (lane == 0) {
+          warp_bv[warp] = bv;
+          warp_bm[warp] = bm;
+        }
+        __syncthreads();
+        if (warp == 0) {
+          const int nw = blockDim.x >> 5;
+          bv = lane < nw ? warp_bv[lane] : -1.0;
+          bm = lane < nw ? warp_bm[lane] : 0x7FFFFFFF;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const double ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int om = __shfl_xor_sync(0xFFFFFFFFu, bm, o);
+            if (ov > bv || (ov == bv && om < bm)) {
+              bv = ov;
+              bm = om;
+            }
+          }
+          if (lane == 0) s_bestm = bm;
+        }
+        __syncthreads();
+        cut = s_bestm;
+        __syncthreads();
+      }
+    }
+    // current candidates in admission order
+    sort_candidates(cnow, B, g, Mp, sm, status);
+    if (!lagged) {
+      prefix_sums(Mp, sm, warp_tot);
+      if (threadIdx.x == 0) s_cut = M;
+      __syncthreads();
+      // Algorithm 1: stop at the first m whose admission does not raise Theta
+      for (int m = threadIdx.x; m < M; m += blockDim.x) {
+        const double next_pre = (m + 1 < Mp) ? sm.pre[m + 1] : sm.pre[m] + __longlong_as_double((long long)sm.key[m]);
+        const double th0 = theta_at(sps, B, sm.pre[m], m);
+        const double th1 = theta_at(sps, B, next_pre, m + 1);
+        if (!(th1 > th0)) atomicMin(&s_cut, m);
+      }
+      __syncthreads();
+      cut = s_cut;
+    }
+    for (int i = threadIdx.x; i < cut; i += blockDim.x) atomicAdd(&sm.cnt[sm.id[i] % B], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) *plan_round = t + 1;
+  }
+  // lengths and their exclusive scan row_off
+  __syncthreads();
+  {
+    const int T = blockDim.x, per = (B + T - 1) / T, lo = threadIdx.x * per;
+    int loc = 0;
+    for (int b = lo; b < lo + per && b < B; ++b) {
+      const int l = mode == DSPARK_STATIC ? g + 1 : 1 + sm.cnt[b];
+      lengths[b] = l;
+      loc += l;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_int[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = T >> 5;
+      const int x = lane < nw ? warp_int[lane] : 0;
+      int inc = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane < nw) warp_int[lane] = inc - x;
+      if (lane == nw - 1) row_off[B] = inc;
+    }
+    __syncthreads();
+    int run = warp_int[warp] + (incl - loc);
+    for (int b = lo; b < lo + per && b < B; ++b) {
+      row_off[b] = run;
+      run += mode == DSPARK_STATIC ? g + 1 : 1 + sm.cnt[b];
+    }
+  }
+}
+
+cudaError_t plan_configure() {
+  return cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
+                        int32_t* row_off, cudaStream_t st, int* launches) {
+  const dspark_dims& d = ws->d;
+  k_plan<<<1, kPlanThreads, plan_smem_bytes(d), st>>>(conf, sps, d.B, d.gamma, (int)d.mode, d.lag,
+                                                     ws->s.ring, ws->s.plan_round, lengths, row_off,
+                                                     ws->s.status);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

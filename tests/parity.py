@@ -1,0 +1,136 @@
+"""GPU-vs-oracle parity helpers for the tests.
+
+Parity rule: token ids, lengths, accepted counts and next anchors must be
+bit-exact, except at decisions the fp64 oracle calls too close to take in
+fp32 (margin < oracle.MARGIN); such "flagged" decisions are counted, and
+everything downstream of one in the same request is not compared. Draft
+probabilities, log-sum-exps and confidences must agree within 1e-4 relative.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_head_gb300 import workloads as wlmod
+
+RTOL = 1e-4
+
+
+@dataclasses.dataclass
+class Tally:
+    compared: int = 0
+    flagged: int = 0
+    excluded_requests: int = 0
+
+    def add(self, other: "Tally") -> "Tally":
+        return Tally(self.compared + other.compared, self.flagged + other.flagged,
+                     self.excluded_requests + other.excluded_requests)
+
+    def check_rate(self, limit: float = 1e-4) -> None:
+        # the expected count is ~1e-5 per draw; allow one stray flag on small samples
+        assert self.flagged <= max(1, int(limit * max(self.compared, 1))), self
+
+
+def np_inputs(inp: Dict[str, torch.Tensor]) -> Dict[str, np.ndarray]:
+    out = {}
+    for k, v in inp.items():
+        if v.dtype == torch.bfloat16:
+            out[k] = v.contiguous().view(torch.int16).cpu().numpy()
+        else:
+            out[k] = v.cpu().numpy()
+    return out
+
+
+def to_device(inp: Dict[str, torch.Tensor], device="cuda") -> Dict[str, torch.Tensor]:
+    return {k: v.to(device).contiguous() for k, v in inp.items()}
+
+
+def rel_close(a, b, rtol=RTOL) -> np.ndarray:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.abs(a - b) <= rtol * np.abs(b) + 1e-30
+
+
+def compare_draft(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Sequence[int]):
+    """Compare draft outputs request by request; returns (tally, set of clean requests)."""
+    t = Tally()
+    clean = set()
+    for b in reqs:
+        ok = True
+        for k in range(o["tokens"].shape[1]):
+            # lse_k and c_k depend on x_{k-1} only, which matched so far
+            assert rel_close(g["lse"][b, k], o["lse"][b, k]), ("lse", b, k, g["lse"][b, k], o["lse"][b, k])
+            assert rel_close(g["conf"][b, k], o["conf"][b, k]), ("conf", b, k, g["conf"][b, k], o["conf"][b, k])
+            if o["margin"][b, k] < oracle.MARGIN:
+                t.flagged += 1
+                ok = False
+                break
+            assert g["tokens"][b, k] == o["tokens"][b, k], ("token", b, k, g["tokens"][b, k], o["tokens"][b, k],
+                                                             o["margin"][b, k])
+            assert rel_close(g["pd_tok"][b, k], o["pd_tok"][b, k]), ("pd", b, k, g["pd_tok"][b, k], o["pd_tok"][b, k])
+            t.compared += 1
+        if ok:
+            clean.add(b)
+        else:
+            t.excluded_requests += 1
+    return t, clean
+
+
+def compare_verify(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Sequence[int]) -> Tally:
+    t = Tally()
+    for b in reqs:
+        if o["acc_margin"][b] < oracle.MARGIN or o["smp_margin"][b] < oracle.MARGIN:
+            t.flagged += 1
+            t.excluded_requests += 1
+            continue
+        assert g["n_acc"][b] == o["n_acc"][b], ("n_acc", b, g["n_acc"][b], o["n_acc"][b])
+        assert g["next_anchor"][b] == o["next_anchor"][b], (
+            "next_anchor", b, g["next_anchor"][b], o["next_anchor"][b], o["resid"][b], o["smp_margin"][b])
+        t.compared += 2
+    return t
+
+
+def oracle_plan(wl: wlmod.Workload, conf32: np.ndarray, sps: np.ndarray, lagged_conf=None):
+    """Lengths the oracle assigns; margin is +inf in static mode."""
+    B, g = conf32.shape
+    if wl.mode == "static":
+        return np.full(B, g + 1, np.int32), np.inf
+    if wl.mode == "compact" or lagged_conf is None:
+        L, _, m = oracle.plan_sync(conf32, sps)
+        return L, m
+    L, _, m = oracle.plan_lagged(conf32, lagged_conf, sps)
+    return L, m
+
+
+def pack_np(P_full: np.ndarray, lengths: np.ndarray) -> np.ndarray:
+    B, R, V = P_full.shape
+    return np.concatenate([P_full[b, :lengths[b]] for b in range(B)]).reshape(-1, V)
+
+
+def row_off_np(lengths: np.ndarray) -> np.ndarray:
+    ro = np.zeros(len(lengths) + 1, np.int32)
+    ro[1:] = np.cumsum(lengths)
+    return ro
+
+
+def gpu_np(d: Dict[str, torch.Tensor]) -> Dict[str, np.ndarray]:
+    return {k: v.cpu().numpy() for k, v in d.items()}
+
+
+def run_gpu_round(ws, dev: Dict[str, torch.Tensor], seed: int, rnd: int, anchor: Optional[torch.Tensor] = None):
+    """draft -> plan -> (pack P by the GPU's lengths) -> verify, through the C-ABI."""
+    anchor = dev["anchor"] if anchor is None else anchor
+    d = ws.draft(dev["U"], dev["W1"], dev["W2"], anchor, dev["h"], dev["w"], dev["T"], seed, rnd)
+    p = ws.plan(d["conf"], dev["sps"])
+    P = wlmod.pack_rows(dev["P_full"], p["lengths"])
+    v = ws.verify(P, p["row_off"], p["lengths"], anchor, d["tokens"], d["pd_tok"], d["lse"], dev["U"],
+                  dev["W1"], dev["W2"], seed, rnd)
+    torch.cuda.synchronize()
+    st = ws.device_status()
+    assert st == 0, f"device status {st}"
+    return {**gpu_np(d), **gpu_np(p), **gpu_np(v)}

@@ -1,0 +1,245 @@
+"""GPU (C-ABI) vs fp64 oracle parity on seeded synthetic rounds.
+
+Sizes: small enough for the oracle to finish in seconds yet spanning many
+64-token blocks, a ragged last block, several 128-row groups; plus the
+benchmark workloads at full size on sampled requests (requests are
+independent in draft and verify, and keep their global random streams).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_head_gb300 import build
+from speculative_decoding_head_gb300.binding import Workspace
+from speculative_decoding_head_gb300.workloads import WORKLOADS, Workload, make_inputs, pack_rows
+
+from parity import (Tally, compare_draft, compare_verify, gpu_np, np_inputs, oracle_plan, pack_np,
+                    rel_close, row_off_np, run_gpu_round, to_device)
+
+pytestmark = pytest.mark.gpu
+
+MID = {
+    "tiny": WORKLOADS["tiny"],
+    "mid_ragged": Workload("mid_ragged", B=16, gamma=5, V=4104, r=256, H=128, wdtype="bf16", mode="compact",
+                           seed=11, u_std=2.0, w_std=0.05, temp_range=(0.8, 1.5), sps_knee=48.0),
+    "mid_static_f32": Workload("mid_static_f32", B=8, gamma=4, V=3000, r=32, H=40, wdtype="f32",
+                               mode="static", seed=12, u_std=2.0, w_std=0.1),
+    "mid_b200": Workload("mid_b200", B=200, gamma=3, V=2048, r=128, H=64, wdtype="bf16", mode="compact",
+                         seed=13, u_std=2.0, w_std=0.05, sps_knee=256.0),
+    "mid_lagged": Workload("mid_lagged", B=40, gamma=4, V=1536, r=64, H=32, wdtype="bf16", mode="lagged",
+                           seed=14, u_std=2.0, w_std=0.05, sps_knee=32.0, noise="per_request",
+                           noise_args=(0.1, 0.5, 1.0), lag=2, rounds=5),
+    "small": WORKLOADS["small"],
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _oracle_round(wl, npi, seed, rnd, anchor, lag_conf=None):
+    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], anchor, npi["h"], npi["w"], npi["T"], seed, rnd)
+    oL, pm = oracle_plan(wl, od["conf"].astype(np.float32), npi["sps"], lag_conf)
+    oP = pack_np(npi["P_full"], oL)
+    ov = oracle.verify(oP, row_off_np(oL), oL, anchor, od["tokens"], npi["U"], npi["W1"], npi["W2"], seed, rnd)
+    return od, oL, pm, ov
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_round_parity(name):
+    wl = MID[name]
+    inp = make_inputs(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    ws = Workspace.for_workload(wl)
+    tally = Tally()
+    anchor_gpu = dev["anchor"].clone()
+    anchor_np = npi["anchor"].copy()
+    confs = []
+    for rnd in range(wl.rounds):
+        g = run_gpu_round(ws, dev, wl.seed, rnd, anchor_gpu)
+        lag_conf = confs[rnd - wl.lag] if (wl.mode == "lagged" and rnd >= wl.lag) else None
+        od, oL, pm, ov = _oracle_round(wl, npi, wl.seed, rnd, anchor_np, lag_conf)
+        t, clean = compare_draft(g, od, range(wl.B))
+        tally = tally.add(t)
+        if len(clean) < wl.B or pm < oracle.MARGIN:
+            # a flagged draft token changes later confidences and so the whole plan
+            break
+        assert (g["lengths"] == oL).all(), (g["lengths"], oL)
+        assert (g["row_off"] == row_off_np(oL)).all()
+        tally = tally.add(compare_verify(g, ov, range(wl.B)))
+        confs.append(od["conf"].astype(np.float32))
+        # chain rounds: both sides continue from their (equal) next anchors
+        if not (g["next_anchor"] == ov["next_anchor"]).all():
+            break
+        anchor_np = ov["next_anchor"].astype(np.int32)
+        anchor_gpu = torch.from_numpy(anchor_np).cuda()
+    tally.check_rate()
+    assert tally.compared > 0
+
+
+def _rand_conf(B, g, seed):
+    rng = np.random.default_rng(seed)
+    return (1.0 / (1.0 + np.exp(-rng.normal(0, 3.6, (B, g))))).astype(np.float32)
+
+
+@pytest.mark.parametrize("name", ["prod", "loaded", "long", "tiny"])
+def test_plan_parity_full_size(name):
+    wl = WORKLOADS[name]
+    sps = make_inputs(wl.with_(V=8, r=1, H=0), with_target=False)["sps"]   # sps depends on B, gamma only
+    mode = "compact" if wl.mode == "static" else wl.mode
+    wl = wl.with_(mode=mode)
+    ws = Workspace(wl.B, wl.gamma, 64, 1, 0, "f32", mode, wl.lag or 2)
+    sps_d = sps.cuda()
+    confs = []
+    flagged = 0
+    for t in range(6 if mode == "lagged" else 3):
+        c = _rand_conf(wl.B, wl.gamma, 1000 * wl.seed + t)
+        confs.append(c)
+        out = ws.plan(torch.from_numpy(c).cuda(), sps_d)
+        torch.cuda.synchronize()
+        assert ws.device_status() == 0
+        lag = confs[t - wl.lag] if (mode == "lagged" and t >= wl.lag) else None
+        oL, pm = oracle_plan(wl, c, sps.numpy(), lag)
+        if pm < oracle.MARGIN:
+            flagged += 1
+            continue
+        assert (out["lengths"].cpu().numpy() == oL).all()
+        assert (out["row_off"].cpu().numpy() == row_off_np(oL)).all()
+    assert flagged <= 1
+
+
+def test_plan_static_and_flat():
+    ws = Workspace(5, 3, 64, 1, 0, "f32", "static")
+    out = ws.plan(torch.zeros((5, 3), device="cuda"), torch.ones(1 + 5 * 4, dtype=torch.float64, device="cuda"))
+    torch.cuda.synchronize()
+    assert (out["lengths"].cpu() == 4).all() and out["row_off"].cpu().tolist() == [0, 4, 8, 12, 16, 20]
+    ws = Workspace(5, 3, 64, 1, 0, "f32", "compact")
+    c = torch.from_numpy(_rand_conf(5, 3, 1)).cuda()
+    out = ws.plan(c, torch.full((21,), 400.0, dtype=torch.float64, device="cuda"))
+    torch.cuda.synchronize()
+    assert (out["lengths"].cpu() == 4).all()   # flat SPS table: full verify
+
+
+@pytest.mark.parametrize("name", ["prod", "long", "loaded"])
+def test_draft_and_verify_full_size_sampled(name):
+    """Full-size workload in the benchmark's launch configuration; the oracle
+    checks a few requests (static verify lengths so that both sides agree on
+    them without the oracle drafting every request)."""
+    wl = WORKLOADS[name].with_(mode="static")
+    inp = make_inputs(wl)
+    dev = to_device(inp)
+    ws = Workspace.for_workload(wl)
+    rnd = 3
+    g = run_gpu_round(ws, dev, wl.seed, rnd)
+    reqs = [0, wl.B // 2 + 1, wl.B - 1]
+    sub = {k: v for k, v in np_inputs({k: inp[k] for k in ("W1", "W2", "w", "T")}).items()}
+    U = inp["U"].numpy()
+    h = inp["h"].numpy()
+    anchor = inp["anchor"].numpy()
+    od = oracle.draft(U, sub["W1"], sub["W2"], anchor, h, sub["w"], sub["T"], wl.seed, rnd, reqs=reqs)
+    t, clean = compare_draft(g, od, reqs)
+    t.check_rate()
+    L = np.full(wl.B, wl.gamma + 1, np.int32)
+    ro = row_off_np(L)
+    P = inp["P_full"].numpy().reshape(-1, wl.V)
+    ok = sorted(clean)
+    ov = oracle.verify(P, ro, L, anchor, od["tokens"], U, sub["W1"], sub["W2"], wl.seed, rnd, reqs=ok)
+    compare_verify(g, ov, ok).check_rate()
+    del dev, inp
+
+
+def test_verify_stagewise_on_oracle_drafts():
+    """Both sides verify the oracle's drafts (rounded to fp32) under many length patterns."""
+    wl = MID["mid_ragged"].with_(B=48, seed=21)
+    inp = make_inputs(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], 5, 9)
+    ws = Workspace.for_workload(wl)
+    rng = np.random.default_rng(3)
+    tally = Tally()
+    for trial in range(3):
+        L = rng.integers(1, wl.gamma + 2, wl.B).astype(np.int32)
+        ro = row_off_np(L)
+        P = pack_np(npi["P_full"], L)
+        out = ws.verify(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(L).cuda(),
+                        dev["anchor"], torch.from_numpy(od["tokens"]).cuda(),
+                        torch.from_numpy(od["pd_tok"].astype(np.float32)).cuda(),
+                        torch.from_numpy(od["lse"].astype(np.float32)).cuda(), dev["U"], dev["W1"], dev["W2"],
+                        5, 9 + trial)
+        torch.cuda.synchronize()
+        assert ws.device_status() == 0
+        ov = oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], 5, 9 + trial)
+        tally = tally.add(compare_verify(gpu_np(out), ov, range(wl.B)))
+        assert (out["n_acc"].cpu().numpy() <= L - 1).all()
+    tally.check_rate()
+    assert tally.compared > 0
+
+
+def test_determinism_and_launch_accounting():
+    wl = MID["mid_b200"]
+    dev = to_device(make_inputs(wl))
+    ws = Workspace.for_workload(wl)
+    a = run_gpu_round(ws, dev, 77, 5)
+    b = run_gpu_round(ws, dev, 77, 5)
+    for k in a:
+        assert (a[k] == b[k]).all(), k
+    c = run_gpu_round(ws, dev, 77, 6)
+    assert not (a["tokens"] == c["tokens"]).all()   # another round draws other numbers
+    assert ws.last_launches > 0
+
+
+def test_device_errors_are_reported_not_faulted():
+    wl = MID["tiny"]
+    dev = to_device(make_inputs(wl))
+    ws = Workspace.for_workload(wl)
+    bad = dev["anchor"].clone()
+    bad[1] = wl.V + 5                                  # out-of-range token id
+    ws.draft(dev["U"], dev["W1"], dev["W2"], bad, dev["h"], dev["w"], dev["T"], 1, 0)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 6
+    ws.reset()
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    conf = torch.full((wl.B, wl.gamma), float("nan"), device="cuda")
+    ws.plan(conf, dev["sps"])
+    torch.cuda.synchronize()
+    assert ws.device_status() == 4
+    ws.reset()
+    with pytest.raises(Exception):
+        ws.plan(conf.cpu(), dev["sps"])               # host tensors are refused by the binding
+
+
+def test_gpu_losslessness_chi_square():
+    """Replicated requests with token-independent rows: the first emitted token follows p_t."""
+    from scipy import stats
+    V, B = 100, 4096
+    rng = np.random.default_rng(5)
+    pt = rng.dirichlet(np.full(V, 0.5))
+    pd = rng.dirichlet(np.full(V, 0.5))
+    U = torch.from_numpy(np.broadcast_to(np.log(pd), (B, 1, V)).astype(np.float32).copy()).cuda()
+    W1 = torch.zeros((V, 8), device="cuda")
+    W2 = torch.zeros((8, V), device="cuda")
+    anchor = torch.zeros(B, dtype=torch.int32, device="cuda")
+    P = torch.from_numpy(np.broadcast_to(np.log(pt), (2 * B, V)).astype(np.float32).copy()).cuda()
+    L = torch.full((B,), 2, dtype=torch.int32, device="cuda")
+    ro = torch.arange(0, 2 * B + 1, 2, dtype=torch.int32, device="cuda")
+    ws = Workspace(B, 1, V, 8, 0, "f32", "static")
+    counts = np.zeros(V)
+    acc = 0
+    rounds = 12
+    for rnd in range(rounds):
+        d = ws.draft(U, W1, W2, anchor, None, torch.zeros(8, device="cuda"), torch.ones(1, device="cuda"), 9, rnd)
+        v = ws.verify(P, ro, L, anchor, d["tokens"], d["pd_tok"], d["lse"], U, W1, W2, 9, rnd)
+        torch.cuda.synchronize()
+        n = v["n_acc"].cpu().numpy()
+        tok = np.where(n > 0, d["tokens"].cpu().numpy()[:, 0], v["next_anchor"].cpu().numpy())
+        counts += np.bincount(tok, minlength=V)
+        acc += int(n.sum())
+    N = rounds * B
+    beta = np.minimum(pt, pd).sum()
+    assert abs(acc / N - beta) < 5 * np.sqrt(beta * (1 - beta) / N)
+    keep = pt > 0
+    assert stats.chisquare(counts[keep], pt[keep] / pt[keep].sum() * N).pvalue > 1e-4
