@@ -203,20 +203,41 @@ def survival(conf) -> np.ndarray:
     return a
 
 
+class PlanMargin:
+    """How close a planner outcome was to changing.
+
+    theta: smallest relative Theta gap over the comparisons taken (flips only
+           under rounding of that size: fp64 reassociation on identical
+           inputs, fp32 differences of the confidences otherwise);
+    cut:   relative gap between the survival values on both sides of the cut
+           (two candidates closer than this may swap across it when their
+           confidences differ in the last bits).
+    """
+
+    def __init__(self, theta=np.inf, cut=np.inf):
+        self.theta, self.cut = float(theta), float(cut)
+
+    def flagged(self, theta_tol: float, cut_tol: float) -> bool:
+        return self.theta < theta_tol or self.cut < cut_tol
+
+    def __repr__(self):
+        return f"PlanMargin(theta={self.theta:.3g}, cut={self.cut:.3g})"
+
+
 def plan_sync(conf, sps):
-    """Algorithm 1 with early stop -> (lengths [B], admitted m, margin)."""
+    """Algorithm 1 with early stop -> (lengths [B], admitted m, PlanMargin)."""
     c = _c(conf, np.float32)
     B, g = c.shape
     s = _c(sps, np.float64)
     assert s.size >= 1 + B * (g + 1)
     L = np.zeros(B, np.int32)
-    m = np.zeros(1, np.float64)
+    m = np.zeros(2, np.float64)
     k = lib().orc_plan_sync(B, g, _p(c), _p(s), _p(L), _p(m))
-    return L, int(k), float(m[0])
+    return L, int(k), PlanMargin(m[0], m[1])
 
 
 def plan_capacity(conf, sps):
-    """K = argmax_m Theta_m over the full admission path -> (K, margin)."""
+    """K = argmax_m Theta_m over the full admission path -> (K, theta margin)."""
     c = _c(conf, np.float32)
     B, g = c.shape
     s = _c(sps, np.float64)
@@ -226,6 +247,7 @@ def plan_capacity(conf, sps):
 
 
 def plan_topk(conf, K: int):
+    """Lengths of the K best candidates -> (lengths, cut margin)."""
     c = _c(conf, np.float32)
     B, g = c.shape
     L = np.zeros(B, np.int32)
@@ -237,12 +259,11 @@ def plan_topk(conf, K: int):
 def plan_lagged(conf_now, conf_lagged, sps):
     """Asynchronous planner: capacity from lagged confidences, top-K of current.
 
-    Returns (lengths, K, margin) where margin covers both the capacity choice
-    and the cut of the top-K.
+    Returns (lengths, K, PlanMargin(theta of the capacity argmax, cut of the top-K)).
     """
     K, m1 = plan_capacity(conf_lagged, sps)
     L, m2 = plan_topk(conf_now, K)
-    return L, K, min(m1, m2)
+    return L, K, PlanMargin(m1, m2)
 
 
 def verify(P_packed, row_off, lengths, anchor, tokens, U, W1, W2, seed: int, rnd: int,

@@ -302,8 +302,10 @@ void orc_survival(int B, int g, const float* conf, double* a_out)
 /*
  * Algorithm 1 with early stop. sps[n] = SPS(n) for n = 1 .. B*(g+1).
  * lengths[b] = 1 + number of admitted drafts of b (the anchor is always verified).
- * Returns the number of admitted candidates m*. margin = smallest relative Theta
- * gap over the decisions taken, and the relative a gap at the cut.
+ * Returns the number of admitted candidates m*. margin[0] = smallest relative
+ * Theta gap over the admission decisions taken (how far a comparison was
+ * from flipping); margin[1] = relative gap between the survival values on the
+ * two sides of the cut (how far two candidates were from swapping across it).
  */
 int orc_plan_sync(int B, int g, const float* conf, const double* sps,
                   int32_t* lengths, double* margin)
@@ -324,13 +326,10 @@ int orc_plan_sync(int B, int g, const float* conf, const double* sps,
         n += 1;
         theta = next;
     }
-    if (m > 0 && m < M) {
-        double ga = rel_gap(c[m - 1].a, c[m].a);
-        if (ga < mg) mg = ga;
-    }
     for (int b = 0; b < B; ++b) lengths[b] = 1;
     for (int i = 0; i < m; ++i) lengths[c[i].b] += 1;
-    *margin = mg;
+    margin[0] = mg;
+    margin[1] = (m > 0 && m < M) ? rel_gap(c[m - 1].a, c[m].a) : INFINITY;
     free(c);
     return m;
 }
@@ -360,7 +359,8 @@ int orc_plan_capacity(int B, int g, const float* conf, const double* sps, double
     return K;
 }
 
-/* lengths from the K best current candidates; margin = relative a gap at the cut */
+/* lengths from the K best current candidates; margin = relative a gap at the cut
+   (the Theta margin does not apply: the capacity K is given) */
 void orc_plan_topk(int B, int g, const float* conf, int K, int32_t* lengths, double* margin)
 {
     orc_cand* c = sorted_candidates(B, g, conf);

@@ -19,6 +19,17 @@ import oracle
 from speculative_decoding_head_gb300 import workloads as wlmod
 
 RTOL = 1e-4
+# Planner flags. With identical fp32 confidences both sides form the same fp64
+# survival products and sort order; only the prefix sums are associated
+# differently (relative error below M * 2^-53 < 1e-12 for M <= 8192), so a
+# decision is flagged only when its relative Theta gap is below 1e-11.
+PLAN_THETA_TOL_SAME_INPUT = 1e-11
+# When each side computes its own confidences (fp32 on the GPU, fp64 rounded to
+# fp32 in the oracle) they differ by ~1e-6 relative, survival products by up
+# to gamma times that; decisions and the order across the cut are flagged
+# below 1e-5 relative.
+PLAN_THETA_TOL_OWN_INPUT = 1e-5
+PLAN_CUT_TOL_OWN_INPUT = 1e-5
 
 
 @dataclasses.dataclass
@@ -96,10 +107,10 @@ def compare_verify(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Seq
 
 
 def oracle_plan(wl: wlmod.Workload, conf32: np.ndarray, sps: np.ndarray, lagged_conf=None):
-    """Lengths the oracle assigns; margin is +inf in static mode."""
+    """Lengths the oracle assigns and its PlanMargin (infinite in static mode)."""
     B, g = conf32.shape
     if wl.mode == "static":
-        return np.full(B, g + 1, np.int32), np.inf
+        return np.full(B, g + 1, np.int32), oracle.PlanMargin()
     if wl.mode == "compact" or lagged_conf is None:
         L, _, m = oracle.plan_sync(conf32, sps)
         return L, m

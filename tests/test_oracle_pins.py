@@ -398,7 +398,7 @@ def test_appendix_a_planner_numbers():
         # Algorithm 1 stops at Theta_1 < Theta_0 whatever c_2 is
         L, m, margin = oracle.plan_sync(c, sps)
         assert m == g["early_stop_drafts_verified"] and L[0] == 1
-        assert abs(margin - 0.1) < 1e-6
+        assert abs(margin.theta - 0.1) < 1e-6
         # the retrospective global argmax does look at c_2
         K, _ = oracle.plan_capacity(c, sps)
         assert K == g[case]["retrospective_drafts_verified"]
