@@ -120,6 +120,12 @@ int dspark_last_launch_count(dspark_ws* ws);
 /* Name of the draft path the workspace will use ("tcgen05" or "simt"). */
 const char* dspark_draft_path(dspark_ws* ws);
 
+/* Choose the draft path: "tcgen05" (persistent tensor-core kernel; bf16
+ * weights, r % 64 == 0, r <= 256, B <= 1024) or "simt" (CUDA-core kernels, any
+ * shape). Both compute the same draw; the default is "tcgen05" where it
+ * applies. Returns EUNSUPPORTED if the tcgen05 path does not apply. */
+dspark_status dspark_ws_set_draft_path(dspark_ws* ws, const char* path);
+
 /*
  * Draft x_1..x_gamma for every request. Outputs, each [B, gamma]:
  *   tokens  int32   x_k

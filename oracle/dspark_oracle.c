@@ -302,10 +302,16 @@ void orc_survival(int B, int g, const float* conf, double* a_out)
 /*
  * Algorithm 1 with early stop. sps[n] = SPS(n) for n = 1 .. B*(g+1).
  * lengths[b] = 1 + number of admitted drafts of b (the anchor is always verified).
+ * The admission test "Theta rises", (tau + a) SPS(n+1) > tau SPS(n), is taken
+ * in the blog's threshold form a SPS(n+1) > tau (SPS(n) - SPS(n+1))
+ * ("阈值随负载变化"): the same inequality, without absorbing a tiny a into tau
+ * (so that a flat table admits every a > 0: full verify, as "spec_dspark"
+ * states for the SGLang planner without an SPS table).
  * Returns the number of admitted candidates m*. margin[0] = smallest relative
- * Theta gap over the admission decisions taken (how far a comparison was
- * from flipping); margin[1] = relative gap between the survival values on the
- * two sides of the cut (how far two candidates were from swapping across it).
+ * difference between the two sides over the decisions taken (how far a
+ * comparison was from flipping); margin[1] = relative gap between the
+ * survival values on the two sides of the cut (how far two candidates were
+ * from swapping across it).
  */
 int orc_plan_sync(int B, int g, const float* conf, const double* sps,
                   int32_t* lengths, double* margin)
@@ -314,17 +320,16 @@ int orc_plan_sync(int B, int g, const float* conf, const double* sps,
     const int M = B * g;
     double tau = (double)B;           /* every request yields at least one token */
     long n = B;                        /* verify batch: one anchor per request */
-    double theta = tau * sps[n];
     double mg = INFINITY;
     int m = 0;
     for (; m < M; ++m) {
-        double next = (tau + c[m].a) * sps[n + 1];
-        double gap = rel_gap(next, theta);
+        double gain = c[m].a * sps[n + 1];            /* expected tokens won, at the new rate */
+        double cost = tau * (sps[n] - sps[n + 1]);    /* rate lost on the tokens already expected */
+        double gap = rel_gap(gain, cost);
         if (gap < mg) mg = gap;
-        if (!(next > theta)) break;   /* stop as soon as Theta no longer rises */
+        if (!(gain > cost)) break;    /* stop as soon as Theta no longer rises */
         tau += c[m].a;
         n += 1;
-        theta = next;
     }
     for (int b = 0; b < B; ++b) lengths[b] = 1;
     for (int i = 0; i < m; ++i) lengths[c[i].b] += 1;

@@ -131,6 +131,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.xbuf = reinterpret_cast<int32_t*>(base + o_xbuf);
   s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
   s.drec = geo.tc_ok ? reinterpret_cast<float*>(base + o_drec) : nullptr;
+  ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(ws->arena);
     delete ws;
@@ -165,7 +166,21 @@ int dspark_last_launch_count(dspark_ws* ws) { return ws ? ws->last_launches : -1
 
 const char* dspark_draft_path(dspark_ws* ws) {
   if (!ws) return "none";
-  return ws->geo.tc_ok ? "tcgen05" : "simt";
+  return ws->use_tc ? "tcgen05" : "simt";
+}
+
+dspark_status dspark_ws_set_draft_path(dspark_ws* ws, const char* path) {
+  if (!ws || !path) return DSPARK_EINVAL;
+  if (strcmp(path, "simt") == 0) {
+    ws->use_tc = 0;
+    return DSPARK_OK;
+  }
+  if (strcmp(path, "tcgen05") == 0) {
+    if (!ws->geo.tc_ok) return DSPARK_EUNSUPPORTED;
+    ws->use_tc = 1;
+    return DSPARK_OK;
+  }
+  return DSPARK_EINVAL;
 }
 
 dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2,
@@ -182,7 +197,7 @@ dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1,
   int launches = 0;
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
   cudaError_t e = launch_conf_hidden(ws, h, w, st, &launches);
-  if (e == cudaSuccess) e = ws->geo.tc_ok ? launch_draft_tc(ws, a, st, &launches) : launch_draft_simt(ws, a, st, &launches);
+  if (e == cudaSuccess) e = ws->use_tc ? launch_draft_tc(ws, a, st, &launches) : launch_draft_simt(ws, a, st, &launches);
   ws->last_launches = launches;
   return cuda_fail(e);
 }

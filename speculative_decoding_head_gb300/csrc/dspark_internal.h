@@ -83,6 +83,7 @@ struct dspark_ws {
   size_t arena_bytes;
   dspark::Scratch s;
   dspark::Geometry geo;
+  int use_tc;  // draft on the tcgen05 path (geo.tc_ok must hold)
   int last_launches;
 };
 

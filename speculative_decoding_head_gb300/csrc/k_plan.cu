@@ -7,7 +7,9 @@
 //   Theta = tau * SPS(B_tot)
 // Candidates (b, j) are taken in decreasing a (ties: smaller j, then smaller
 // b) and admitted one at a time while Theta strictly rises; because a is
-// non-increasing in j, the admitted set is a prefix of every request.
+// non-increasing in j, the admitted set is a prefix of every request. The
+// rise test (tau + a) SPS(n+1) > tau SPS(n) is evaluated in its threshold
+// form a SPS(n+1) > tau (SPS(n) - SPS(n+1)) (section "阈值随负载变化").
 // The asynchronous planner of the close reading's §8 takes the capacity
 // K = argmax_m Theta_m over the whole path (no early stop; first maximum) on
 // the confidences of round t - lag, then admits the K best current
@@ -224,12 +226,15 @@ __global__ void __launch_bounds__(kPlanThreads)
       prefix_sums(Mp, sm, warp_tot);
       if (threadIdx.x == 0) s_cut = M;
       __syncthreads();
-      // Algorithm 1: stop at the first m whose admission does not raise Theta
+      // Algorithm 1: stop at the first m whose admission does not raise
+      // Theta, tested in the threshold form a SPS(n+1) > tau (SPS(n) - SPS(n+1))
+      // (same blog, "阈值随负载变化"), which does not absorb a tiny a into tau.
       for (int m = threadIdx.x; m < M; m += blockDim.x) {
-        const double next_pre = (m + 1 < Mp) ? sm.pre[m + 1] : sm.pre[m] + __longlong_as_double((long long)sm.key[m]);
-        const double th0 = theta_at(sps, B, sm.pre[m], m);
-        const double th1 = theta_at(sps, B, next_pre, m + 1);
-        if (!(th1 > th0)) atomicMin(&s_cut, m);
+        const double a = __longlong_as_double((long long)sm.key[m]);
+        const double tau = (double)B + sm.pre[m];
+        const double gain = __dmul_rn(a, sps[B + m + 1]);
+        const double cost = __dmul_rn(tau, sps[B + m] - sps[B + m + 1]);
+        if (!(gain > cost)) atomicMin(&s_cut, m);
       }
       __syncthreads();
       cut = s_cut;

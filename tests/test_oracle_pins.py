@@ -398,7 +398,8 @@ def test_appendix_a_planner_numbers():
         # Algorithm 1 stops at Theta_1 < Theta_0 whatever c_2 is
         L, m, margin = oracle.plan_sync(c, sps)
         assert m == g["early_stop_drafts_verified"] and L[0] == 1
-        assert abs(margin.theta - 0.1) < 1e-6
+        # threshold form at m = 0: a1 SPS(2) = 0.4 against tau (SPS(1) - SPS(2)) = 0.5
+        assert abs(margin.theta - 0.2) < 1e-6
         # the retrospective global argmax does look at c_2
         K, _ = oracle.plan_capacity(c, sps)
         assert K == g[case]["retrospective_drafts_verified"]
@@ -507,6 +508,12 @@ def test_planner_flat_table_is_full_verify():
     conf = special.expit(rng.normal(0, 3, (B, g))).astype(np.float32)
     L, m, _ = oracle.plan_sync(conf, np.full(1 + B * (g + 1), 400.0))
     assert (L == g + 1).all() and m == B * g
+    # even survival values far below tau's fp64 resolution are admitted
+    B, g = 128, 15
+    conf = special.expit(rng.normal(-4, 3, (B, g))).astype(np.float32)
+    assert np.cumprod(conf.astype(np.float64), 1).min() < 1e-30
+    L, m, pm = oracle.plan_sync(conf, np.full(1 + B * (g + 1), 400.0))
+    assert (L == g + 1).all() and pm.theta == 1.0
 
 
 @pytest.mark.parametrize("B,g", [(1, 3), (2, 2), (3, 3), (2, 3)])
