@@ -99,6 +99,84 @@ __global__ void __launch_bounds__(kSweepThreads)
   }
 }
 
+// Vectorised sweep for V % 4 == 0 (rows 16-byte aligned): each thread streams
+// float4 values, four loads in flight per thread; a half-warp holds one
+// 64-token block per load, so the bonus row's block masses need only
+// 16-lane shuffles.
+constexpr int kSweepUnroll = 4;
+
+__global__ void __launch_bounds__(kSweepThreads)
+    k_verify_sweep4(const float* __restrict__ P, const int32_t* __restrict__ row_off,
+                    const int32_t* __restrict__ lengths, int B, int V, int S, int chunk, int Rmax, Rng rng,
+                    float4* __restrict__ part) {
+  __shared__ MS red_ms[kSweepThreads / 32];
+  __shared__ KeyIdx red_k[kSweepThreads / 32];
+  const int R = min(max(row_off[B], 0), Rmax);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int V4 = V >> 2;
+  for (int item = blockIdx.x; item < R * S; item += gridDim.x) {
+    const int q = item / S, sp = item - q * S;
+    const int b = request_of_row(row_off, B, q);
+    const int j = q - row_off[b];
+    const bool bonus = j == lengths[b] - 1;
+    const int lo4 = (sp * chunk) >> 2, hi4 = min(V4, lo4 + (chunk >> 2));
+    const float4* row = reinterpret_cast<const float4*>(P + (size_t)q * V);
+    MS ms{-INFINITY, 0.f};
+    KeyIdx kb = key_none();
+    // uniform trip count across the CTA: the bonus branch shuffles over full warps
+    for (int base = lo4; base < hi4; base += kSweepUnroll * kSweepThreads) {
+      const int f0 = base + threadIdx.x;
+      float4 x[kSweepUnroll];
+#pragma unroll
+      for (int u = 0; u < kSweepUnroll; ++u) {
+        const int f = f0 + u * kSweepThreads;
+        x[u] = f < hi4 ? __ldcs(row + f) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < kSweepUnroll; ++u) {
+        const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+        if (bonus) {
+          // this half-warp's 16 float4 are one 64-token block
+          float m = m4;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+          float t = 0.f;
+          if (m != -INFINITY)
+            t = __expf(x[u].x - m) + __expf(x[u].y - m) + __expf(x[u].z - m) + __expf(x[u].w - m);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+          const int f = f0 + u * kSweepThreads;
+          if ((lane & 15) == 0 && f < hi4 && m != -INFINITY) {
+            const int s0 = f >> 4;  // 16 float4 per block
+            ms = ms_combine(ms, MS{m, t});
+            kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, b, j, s0)), s0});
+          }
+        } else if (m4 != -INFINITY) {
+          const float m = fmaxf(m4, ms.m);
+          float t = ms.m == -INFINITY ? 0.f : ms.s * __expf(ms.m - m);
+          t += __expf(x[u].x - m) + __expf(x[u].y - m) + __expf(x[u].z - m) + __expf(x[u].w - m);
+          ms = MS{m, t};
+        }
+      }
+    }
+    ms = warp_ms(ms);
+    kb = warp_best(kb);
+    if (lane == 0) {
+      red_ms[warp] = ms;
+      red_k[warp] = kb;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      MS m2 = lane < nw ? red_ms[lane] : MS{-INFINITY, 0.f};
+      KeyIdx k2 = lane < nw ? red_k[lane] : key_none();
+      m2 = warp_ms(m2);
+      k2 = warp_best(k2);
+      if (lane == 0) part[item] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(128)
     k_verify_finalize(const float* __restrict__ P, const int32_t* __restrict__ row_off,
                       const int32_t* __restrict__ lengths, const int32_t* __restrict__ anchor,
@@ -337,9 +415,13 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
   const Rng rng = Rng::make(a.seed, a.round);
-  int grid = geo.num_sms * 8;
-  k_verify_sweep<<<grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.S, geo.chunk,
-                                                 d.B * (d.gamma + 1), rng, ws->s.vpart);
+  const int grid = geo.num_sms * 8;
+  if ((d.V & 3) == 0)
+    k_verify_sweep4<<<grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.S, geo.chunk,
+                                                    d.B * (d.gamma + 1), rng, ws->s.vpart);
+  else
+    k_verify_sweep<<<grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.S, geo.chunk,
+                                                   d.B * (d.gamma + 1), rng, ws->s.vpart);
   k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma,
                                                    d.V, geo.S, rng, ws->s.vpart, a.n_acc, a.next_anchor,
                                                    ws->s.vflag, ws->s.vrow, ws->s.vlset, ws->s.status);
