@@ -178,6 +178,30 @@ dspark_status dspark_round(dspark_ws* ws, const float* U, const void* W1, const 
                            int32_t* lengths, int32_t* row_off, int32_t* n_accepted,
                            int32_t* next_anchor, dspark_stream_t stream);
 
+/*
+ * Draft without a workspace and without allocating anything, for callers that
+ * cannot call cudaMalloc (an engine whose memory pool owns all device memory,
+ * a plug-in that must not grow the process's device footprint, code under a
+ * hard memory budget). The pages describe no such call; it exists only for
+ * those callers.
+ *
+ * Same inputs and outputs as dspark_markov_draft, computed by the same
+ * CUDA-core draft kernels (the "simt" path), plus device_status: a caller-owned
+ * device int32 that the call zeroes and the kernels set to a dspark_status code
+ * on a device error (read it after synchronising `stream`). Scratch comes from
+ * a 4 MiB array built into the library (2^20 floats): calls whose
+ * B*gamma (rounded up to 64) + B*ceil(V/64) exceeds 2^20 return
+ * DSPARK_EUNSUPPORTED and enqueue nothing. The first call on a device looks up
+ * the array's device address, so make it before any stream capture. Every
+ * call shares the array: calls whose work overlaps on the GPU race, so issue
+ * them on one stream. No cudaMalloc, cudaFree or allocating routine is called.
+ */
+dspark_status dspark_markov_draft_noalloc(const dspark_dims* dims, const float* U, const void* W1,
+                                          const void* W2, const int32_t* anchor, const float* h,
+                                          const float* w, const float* T, uint64_t seed, uint64_t round,
+                                          int32_t* tokens, float* pd_tok, float* lse, float* conf,
+                                          int32_t* device_status, dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
