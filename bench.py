@@ -37,7 +37,7 @@ NORTH_STAR_BW = 8000.0   # GB/s, the roofline constant the metric is quoted agai
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="prod")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -74,7 +74,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -317,7 +317,7 @@ def main():
     t_round = ms * 1e-3
     draft_bytes = bts["U"] + wl.gamma * bts["W2_per_step"]
     draft_gbs = draft_bytes / (st["draft"] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": f"draft stage ({ws.draft_path})", "achieved": draft_gbs,
+    roofline = {"bound": "hbm", "kernel": f"draft stage ({ws.path})", "achieved": draft_gbs,
                 "peak": peak, "unit": "GB/s", "frac": draft_gbs / peak, "peak_kind": peak_kind,
                 "traffic": None, "alg_bytes_per_launch": draft_bytes,
                 "launch_ms": st["draft"]}
@@ -385,7 +385,7 @@ def main():
             "gpu_launches": launches_per_round * args.steps,
             "launches_per_round": launches_per_round,
             "graph": graph is not None,
-            "draft_path": ws.draft_path,
+            "path": ws.path,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -117,14 +117,15 @@ const char* dspark_status_string(int status);
 /* Kernels launched by the last call on this workspace (for accounting). */
 int dspark_last_launch_count(dspark_ws* ws);
 
-/* Name of the draft path the workspace will use ("tcgen05" or "simt"). */
-const char* dspark_draft_path(dspark_ws* ws);
+/* Name of the compute path the workspace uses ("tcgen05" or "simt"). */
+const char* dspark_path(dspark_ws* ws);
 
-/* Choose the draft path: "tcgen05" (persistent tensor-core kernel; bf16
+/* Choose the compute path of the two stages that contract with W2 (the draft
+ * and the residual recompute of verify): "tcgen05" (tensor-core kernels; bf16
  * weights, r % 64 == 0, r <= 256, B <= 1024) or "simt" (CUDA-core kernels, any
- * shape). Both compute the same draw; the default is "tcgen05" where it
+ * shape). Both compute the same draws; the default is "tcgen05" where it
  * applies. Returns EUNSUPPORTED if the tcgen05 path does not apply. */
-dspark_status dspark_ws_set_draft_path(dspark_ws* ws, const char* path);
+dspark_status dspark_ws_set_path(dspark_ws* ws, const char* path);
 
 /*
  * Draft x_1..x_gamma for every request. Outputs, each [B, gamma]:

@@ -142,12 +142,14 @@ double orc_logsumexp(const double* x, long n)
 
 /* ------------------------------------------------------------------ */
 /* Two-level Gumbel-max draw of v with probability exp(logw_v)/sum.    */
-/* tol[v] (optional) widens the margin of keys whose fp32 evaluation   */
-/* is known to be loose (the residual); margin = top-2 key gap minus   */
-/* the two tolerances, minimised over both levels.                     */
+/* tol[v] (optional) widens the margin of token keys whose fp32        */
+/* evaluation is known to be loose (the residual), and tol_mass[v] the */
+/* block keys: a block's tolerance is sum(tol_mass) / block mass.      */
+/* margin = top-2 key gap minus the two tolerances, minimised over     */
+/* both levels.                                                        */
 /* Returns -1 if no token has positive weight.                         */
 /* ------------------------------------------------------------------ */
-static int sample_two_level(const double* logw, const double* tol, long V,
+static int sample_two_level(const double* logw, const double* tol, const double* tol_mass, long V,
                             uint64_t seed, uint64_t round, uint32_t pblk, uint32_t ptok,
                             uint32_t b, uint32_t j, double* margin)
 {
@@ -159,11 +161,11 @@ static int sample_two_level(const double* logw, const double* tol, long V,
         double mass_log = orc_logsumexp(logw + lo, hi - lo);
         if (mass_log == -INFINITY) continue;
         double t = 0.0;
-        if (tol) {
-            /* block tolerance: relative error of the block mass, i.e. the
-               element tolerances weighted by their share of the mass */
-            for (long v = lo; v < hi; ++v)
-                if (logw[v] > -INFINITY) t += exp(logw[v] - mass_log) * tol[v];
+        if (tol_mass) {
+            /* block tolerance: absolute error bound of the block mass over the mass */
+            double num = 0.0;
+            for (long v = lo; v < hi; ++v) num += tol_mass[v];
+            t = num / exp(mass_log);
         }
         double key = mass_log + orc_gumbel(seed, round, pblk, b, j, (uint32_t)s);
         if (key > best) { second = best; ts = tb; best = key; tb = t; bs = s; }
@@ -236,7 +238,7 @@ void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2
             markov_logits(d, U + o * V, W1, W2, x_prev, z);
             double L = orc_logsumexp(z, V);
             double m = 0.0;
-            int x = sample_two_level(z, NULL, V, seed, round, ORC_P_DRAFT_BLOCK,
+            int x = sample_two_level(z, NULL, NULL, V, seed, round, ORC_P_DRAFT_BLOCK,
                                      ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
             tokens[o] = x;
             pd_tok[o] = exp(z[x] - L);
@@ -406,6 +408,7 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         double* z = (double*)malloc(sizeof(double) * (size_t)V);
         double* lw = (double*)malloc(sizeof(double) * (size_t)V);
         double* tol = (double*)malloc(sizeof(double) * (size_t)V);
+        double* tm = (double*)malloc(sizeof(double) * (size_t)V);
         double am = INFINITY, sm = INFINITY;
         int n = ell - 1, out = -1, from_resid = 0;
         for (int j = 0; j < ell - 1; ++j) {
@@ -432,16 +435,20 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
                     /* an fp32 evaluation of lpd - lt carries about 4e-6 absolute
                        error, which moves log c by 4e-6 * (1 - c) / c */
                     tol[v] = 4e-6 * (1.0 - c) / c;
+                    /* a block mass summed as max(0, p_t - p_d) in fp32 carries
+                       about 4e-6 (p_t + p_d) absolute error per token */
+                    tm[v] = 4e-6 * exp(lt[v]) * (2.0 - c);
                 } else {
                     lw[v] = -INFINITY;
                     tol[v] = 0.0;
+                    tm[v] = 0.0;
                 }
             }
-            out = sample_two_level(lw, tol, V, seed, round, ORC_P_RESID_BLOCK,
+            out = sample_two_level(lw, tol, tm, V, seed, round, ORC_P_RESID_BLOCK,
                                    ORC_P_RESID_TOKEN, (uint32_t)b, (uint32_t)j, &sm);
             from_resid = 1;
             if (out < 0) {   /* no positive residual mass: sample p_t itself */
-                out = sample_two_level(lt, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
+                out = sample_two_level(lt, NULL, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
                                        ORC_P_BONUS_TOKEN, (uint32_t)b, (uint32_t)j, &sm);
                 from_resid = 0;
             }
@@ -450,7 +457,7 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         if (out < 0) {   /* every verified draft accepted: bonus from row ell-1 */
             const float* Prow = P + (long)(row_off[b] + n) * V;
             for (long v = 0; v < V; ++v) lt[v] = (double)Prow[v];
-            out = sample_two_level(lt, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
+            out = sample_two_level(lt, NULL, NULL, V, seed, round, ORC_P_BONUS_BLOCK,
                                    ORC_P_BONUS_TOKEN, (uint32_t)b, (uint32_t)n, &sm);
         }
         n_acc[b] = n;
@@ -458,7 +465,7 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         acc_margin[b] = am;
         smp_margin[b] = sm;
         resid[b] = from_resid;
-        free(lt); free(z); free(lw); free(tol);
+        free(lt); free(z); free(lw); free(tol); free(tm);
     }
 }
 
@@ -469,7 +476,7 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
 int orc_sample(const double* logw, long V, uint64_t seed, uint64_t round,
                uint32_t pblk, uint32_t ptok, uint32_t b, uint32_t j, double* margin)
 {
-    return sample_two_level(logw, NULL, V, seed, round, pblk, ptok, b, j, margin);
+    return sample_two_level(logw, NULL, NULL, V, seed, round, pblk, ptok, b, j, margin);
 }
 
 /* residual draw for explicit p_t, p_d (pin tests); returns -1 if no mass */
@@ -478,7 +485,7 @@ int orc_residual(const double* pt, const double* pd, long V, uint64_t seed,
 {
     double* lw = (double*)malloc(sizeof(double) * (size_t)V);
     for (long v = 0; v < V; ++v) lw[v] = pt[v] > pd[v] ? log(pt[v] - pd[v]) : -INFINITY;
-    int out = sample_two_level(lw, NULL, V, seed, round, ORC_P_RESID_BLOCK,
+    int out = sample_two_level(lw, NULL, NULL, V, seed, round, ORC_P_RESID_BLOCK,
                                ORC_P_RESID_TOKEN, b, j, margin);
     free(lw);
     return out;

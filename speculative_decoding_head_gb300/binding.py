@@ -21,8 +21,8 @@ WDTYPES = {"f32": 0, "bf16": 1}
 
 SYMBOLS = [
     "dspark_ws_create", "dspark_ws_destroy", "dspark_ws_reset", "dspark_last_error",
-    "dspark_status_string", "dspark_last_launch_count", "dspark_draft_path",
-    "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_draft_path",
+    "dspark_status_string", "dspark_last_launch_count", "dspark_path",
+    "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
 ]
 
 
@@ -65,10 +65,10 @@ def load() -> C.CDLL:
         lib.dspark_status_string.restype = C.c_char_p
         lib.dspark_last_launch_count.argtypes = [P]
         lib.dspark_last_launch_count.restype = i32
-        lib.dspark_draft_path.argtypes = [P]
-        lib.dspark_draft_path.restype = C.c_char_p
-        lib.dspark_ws_set_draft_path.argtypes = [P, C.c_char_p]
-        lib.dspark_ws_set_draft_path.restype = i32
+        lib.dspark_path.argtypes = [P]
+        lib.dspark_path.restype = C.c_char_p
+        lib.dspark_ws_set_path.argtypes = [P, C.c_char_p]
+        lib.dspark_ws_set_path.restype = i32
         lib.dspark_markov_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, P, P, P, P]
         lib.dspark_markov_draft.restype = i32
         lib.dspark_plan.argtypes = [P, P, P, P, P, P]
@@ -112,18 +112,18 @@ class Workspace:
     """One DSpark workspace: the library's scratch arena for a fixed shape."""
 
     def __init__(self, B: int, gamma: int, V: int, r: int, H: int, wdtype: str = "bf16",
-                 mode: str = "compact", lag: int = 2, draft_path: Optional[str] = None):
+                 mode: str = "compact", lag: int = 2, path: Optional[str] = None):
         self.lib = load()
         self.dims = Dims(B, gamma, V, r, H, WDTYPES[wdtype], MODES[mode], lag if mode == "lagged" else 0)
         self.wdtype = torch.bfloat16 if wdtype == "bf16" else torch.float32
         self._h = C.c_void_p()
         _check(self.lib.dspark_ws_create(C.byref(self.dims), C.byref(self._h)), "dspark_ws_create")
-        if draft_path is not None:
-            self.set_draft_path(draft_path)
+        if path is not None:
+            self.set_path(path)
 
     @classmethod
-    def for_workload(cls, wl, draft_path: Optional[str] = None) -> "Workspace":
-        return cls(wl.B, wl.gamma, wl.V, wl.r, wl.H, wl.wdtype, wl.mode, wl.lag or 2, draft_path)
+    def for_workload(cls, wl, path: Optional[str] = None) -> "Workspace":
+        return cls(wl.B, wl.gamma, wl.V, wl.r, wl.H, wl.wdtype, wl.mode, wl.lag or 2, path)
 
     def close(self) -> None:
         if getattr(self, "_h", None) and self._h.value:
@@ -142,11 +142,11 @@ class Workspace:
         return self._h
 
     @property
-    def draft_path(self) -> str:
-        return self.lib.dspark_draft_path(self._h).decode()
+    def path(self) -> str:
+        return self.lib.dspark_path(self._h).decode()
 
-    def set_draft_path(self, path: str) -> None:
-        _check(self.lib.dspark_ws_set_draft_path(self._h, path.encode()), "dspark_ws_set_draft_path")
+    def set_path(self, path: str) -> None:
+        _check(self.lib.dspark_ws_set_path(self._h, path.encode()), "dspark_ws_set_path")
 
     @property
     def last_launches(self) -> int:

@@ -93,7 +93,11 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
   const size_t o_vlset = carve(sizeof(float) * d.B);
-  const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * kResidChunks);
+  geo.resid_tc_ok = resid_tc_supported(d);
+  if (geo.resid_tc_ok && resid_tc_configure(ws) != cudaSuccess) geo.resid_tc_ok = 0;
+  cudaGetLastError();
+  geo.rchunks = geo.num_sms > kResidChunks ? geo.num_sms : kResidChunks;
+  const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * geo.rchunks);
   const size_t o_xbuf = carve(sizeof(int32_t) * d.B);
   size_t o_dpart = 0, o_drec = 0;
   if (geo.tc_ok) {
@@ -164,12 +168,12 @@ dspark_status dspark_last_error(dspark_ws* ws, int* device_status) {
 
 int dspark_last_launch_count(dspark_ws* ws) { return ws ? ws->last_launches : -1; }
 
-const char* dspark_draft_path(dspark_ws* ws) {
+const char* dspark_path(dspark_ws* ws) {
   if (!ws) return "none";
   return ws->use_tc ? "tcgen05" : "simt";
 }
 
-dspark_status dspark_ws_set_draft_path(dspark_ws* ws, const char* path) {
+dspark_status dspark_ws_set_path(dspark_ws* ws, const char* path) {
   if (!ws || !path) return DSPARK_EINVAL;
   if (strcmp(path, "simt") == 0) {
     ws->use_tc = 0;
@@ -197,7 +201,8 @@ dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1,
   int launches = 0;
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
   cudaError_t e = launch_conf_hidden(ws, h, w, st, &launches);
-  if (e == cudaSuccess) e = ws->use_tc ? launch_draft_tc(ws, a, st, &launches) : launch_draft_simt(ws, a, st, &launches);
+  if (e == cudaSuccess)
+    e = (ws->use_tc && ws->geo.tc_ok) ? launch_draft_tc(ws, a, st, &launches) : launch_draft_simt(ws, a, st, &launches);
   ws->last_launches = launches;
   return cuda_fail(e);
 }

@@ -72,6 +72,8 @@ struct Geometry {
   int tc_ok;        // tcgen05 path usable for these dims
   int tc_grid;      // CTAs of the persistent draft kernel
   int tc_groups;    // 128-row groups
+  int resid_tc_ok;  // tcgen05 residual kernel usable for these dims
+  int rchunks;      // residual partials per request (CTAs of the residual pass)
 };
 
 }  // namespace dspark
@@ -83,7 +85,7 @@ struct dspark_ws {
   size_t arena_bytes;
   dspark::Scratch s;
   dspark::Geometry geo;
-  int use_tc;  // draft on the tcgen05 path (geo.tc_ok must hold)
+  int use_tc;  // tensor-core draft and residual where geo.tc_ok / geo.resid_tc_ok hold
   int last_launches;
 };
 
@@ -103,6 +105,10 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 int draft_tc_supported(const dspark_dims& d);
 cudaError_t draft_tc_configure(dspark_ws* ws);
 size_t draft_tc_scratch_rows(const dspark_dims& d, int grid);
+
+int resid_tc_supported(const dspark_dims& d);
+cudaError_t resid_tc_configure(dspark_ws* ws);
+cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st);
 
 size_t plan_smem_bytes(const dspark_dims& d);
 cudaError_t plan_configure();

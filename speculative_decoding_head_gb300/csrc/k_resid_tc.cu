@@ -1,0 +1,430 @@
+// k_resid_tc.cu -- residual block draw on tcgen05 (sm_103a).
+//
+// After the first rejection n of request b, the next anchor is drawn from
+// norm(max(0, p_t - p_d)) ("DeepSeek-V4.1 模型结构（6）：解码，DSpark",
+// derivation box; "DSpark：不让大模型更聪明，而让它「吐字更快」" §02), with
+//   p_t(v) = exp(P[row, v] - lse_t)   (row = the rejected target row),
+//   p_d(v) = exp(U[b, n, v] + W1[x_n] . W2[:, v] - lse_d)   (draft position n+1),
+// recomputed rather than stored. This kernel makes the block draw of the
+// two-level sampler: for each 64-token block s the residual mass
+// W_s = sum_v max(0, p_t(v) - p_d(v)) and the key log W_s + G_s; the token
+// draw inside the winning block is k_resid_pick's.
+//
+// Orientation: D[v, i] = sum_k W2[k, v] W1[x_i, k] with M = 128 vocabulary
+// entries (A = W2 tile, N-major in memory, 128-byte swizzle, two 64-wide
+// boxes) and N = 128 rejected requests (B = gathered W1 rows, K-major). Each
+// epilogue thread owns one vocabulary entry and reads U and P of every
+// request with loads that are coalesced across the warp; a block's mass is a
+// sum over two warps' lanes (a 31-shuffle transpose-reduce per 32 requests,
+// then shared memory). Requests are taken in groups of 128 (the list of
+// rejected requests is compacted in each CTA from the verify flags).
+// Persistent, one CTA per SM over 128-wide vocabulary tiles; W2 is read with
+// the L2 evict_last policy (the draft kept it there), U and P with evict-first
+// streaming loads. Every wait is bounded.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "dspark_common.cuh"
+#include "dspark_internal.h"
+#include "tc_ptx.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kRThreads = 192;
+constexpr int kRM = 128;          // vocabulary entries per tile (MMA M)
+constexpr int kRN = 128;          // requests per group (MMA N)
+constexpr int kRNW = 2;           // W2 ring depth
+constexpr int kRTmemCols = 256;   // two 128-column accumulators
+constexpr int kRMaxB = 1024;
+
+struct RSmem {
+  uint32_t bop, w2, col, part, best, list, bars, misc, total;
+  __host__ __device__ static RSmem make(int r) {
+    RSmem s;
+    s.bop = 0;                              // [128 requests x r] bf16, K-major swizzled
+    s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r x 64] bf16)
+    s.col = s.w2 + kRNW * 2 * r * 128;      // per-request: b, n, row (int), lse_d, lse_t (float)
+    s.part = s.col + 5 * 4 * kRN;           // [4 warps][128] block partial sums
+    s.best = s.part + 4 * 4 * kRN;          // [128] best key, [128] best block
+    s.list = s.best + 2 * 4 * kRN;          // [kRMaxB] rejected requests
+    s.bars = s.list + 4 * kRMaxB;
+    s.misc = s.bars + 8 * (2 * kRNW + 4 + 2);
+    s.total = s.misc + 64;
+    return s;
+  }
+};
+
+struct RParams {
+  int B, g, V, r;
+  int ntiles, G;
+  Rng rng;
+  const float* P;
+  const float* U;
+  const void* W1;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const float* lse;
+  const int* vflag;
+  const int32_t* n_acc;
+  const int* vrow;
+  const float* vlset;
+  float2* rpart;  // [B][G] (key, block) of each CTA
+  int* status;
+};
+
+// Sum over the 32 lanes of 32 per-lane values: afterwards a[0] of lane L holds
+// the sum of every lane's a[L] (each step keeps the half whose index bit
+// matches the lane's bit and adds the partner's other half).
+__device__ __forceinline__ float transpose_sum32(float (&a)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? a[k] : a[k + o];
+      const float keep = upper ? a[k + o] : a[k];
+      a[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+  return a[0];
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    k_resid_tc(const __grid_constant__ CUtensorMap tm_w2, const RParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const RSmem L = RSmem::make(p.r);
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sB = sbase + L.bop, sW2 = sbase + L.w2;
+  int* col_b = reinterpret_cast<int*>(smem + L.col);
+  int* col_n = col_b + kRN;
+  int* col_row = col_n + kRN;
+  float* col_lsed = reinterpret_cast<float*>(col_row + kRN);
+  float* col_lset = col_lsed + kRN;
+  float* part = reinterpret_cast<float*>(smem + L.part);   // [4][128]
+  float* best_key = reinterpret_cast<float*>(smem + L.best);
+  int* best_blk = reinterpret_cast<int*>(best_key + kRN);
+  int* list = reinterpret_cast<int*>(smem + L.list);
+  const uint32_t bars = sbase + L.bars;
+  auto w2_full = [&](int i) { return bars + 8u * i; };
+  auto w2_empty = [&](int i) { return bars + 8u * (kRNW + i); };
+  auto t_full = [&](int i) { return bars + 8u * (2 * kRNW + i); };
+  auto t_empty = [&](int i) { return bars + 8u * (2 * kRNW + 2 + i); };
+  const uint32_t a_full = bars + 8u * (2 * kRNW + 4);
+  const uint32_t drain = a_full + 8u;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
+  int* s_nrej = reinterpret_cast<int*>(smem + L.misc + 32);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+  const int tile_lo = (int)((long long)c * p.ntiles / p.G);
+  const int tile_hi = (int)((long long)(c + 1) * p.ntiles / p.G);
+  const int nt = tile_hi - tile_lo;
+  const uint32_t box_bytes = (uint32_t)p.r * 128u;  // one [r x 64] bf16 box
+  const uint32_t w2_bytes = 2u * box_bytes;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRNW; ++i) {
+      tc::mbar_init(w2_full(i), 1);
+      tc::mbar_init(w2_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(t_full(i), 1);
+      tc::mbar_init(t_empty(i), 4);
+    }
+    tc::mbar_init(a_full, 4);
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_barrier_init();
+    tc::prefetch_tmap(&tm_w2);
+  }
+  // the rejected requests, in request order (every CTA builds the same list)
+  if (warp == 2) {
+    int base = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      const bool f = b < p.B && p.vflag[b] != 0;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+      if (f) list[base + __popc(m & ((1u << lane) - 1u))] = b;
+      base += __popc(m);
+    }
+    if (lane == 0) *s_nrej = base;
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_holder), kRTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int nrej = *s_nrej;
+  const int ngroups = (nrej + kRN - 1) / kRN;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (W2 tiles)
+    if (lane == 0 && ngroups > 0) {
+      const uint64_t keep = tc::policy_evict_last();
+      int issued = 0;
+      bool ok = true;
+      for (int gq = 0; gq < ngroups && ok; ++gq) {
+        for (int i = 0; i < nt && ok; ++i) {
+          const int it = gq * nt + i, t = tile_lo + i, ws = it % kRNW;
+          ok = tc::mbar_wait(w2_empty(ws), ((it / kRNW) & 1) ^ 1, abort);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
+          tc::tma_load_2d(sW2 + ws * w2_bytes, &tm_w2, t * kRM, 0, w2_full(ws), keep);
+          tc::tma_load_2d(sW2 + ws * w2_bytes + box_bytes, &tm_w2, t * kRM + 64, 0, w2_full(ws), keep);
+          issued = it + 1;
+        }
+      }
+      if (!ok) {
+        if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
+        *abort = 1;
+        for (int it = issued - 1; it >= 0 && it >= issued - kRNW; --it) {
+          volatile int never = 0;
+          tc::mbar_wait(w2_full(it % kRNW), (it / kRNW) & 1, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && ngroups > 0) {
+      // A = W2 tile, M-major (vocabulary contiguous); B = W1 rows, K-major
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(kRN >> 3) << 17) |
+                             ((uint32_t)(kRM >> 4) << 24);
+      bool ok = true;
+      for (int gq = 0; gq < ngroups && ok; ++gq) {
+        ok = tc::mbar_wait(a_full, gq & 1, abort);
+        if (!ok) break;
+        tc::tc_fence_after();
+        for (int i = 0; i < nt && ok; ++i) {
+          const int it = gq * nt + i, ws = it % kRNW, ab = it & 1;
+          ok = tc::mbar_wait(w2_full(ws), (it / kRNW) & 1, abort) &&
+               tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
+          if (!ok) break;
+          tc::tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(ab * kRN);
+          const uint32_t astage = sW2 + ws * w2_bytes;
+          for (int ks = 0; ks < p.r / 16; ++ks) {
+            // A: two 64-wide M atoms (LBO apart), 8 K rows per 1 KB atom (SBO)
+            const uint64_t ad = tc::smem_desc(astage + ks * 2048, box_bytes, 1024);
+            const uint64_t bd = tc::smem_desc(sB + (ks >> 2) * (kRN * 128) + (ks & 3) * 32, 16, 1024);
+            tc::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(w2_empty(ws));
+          tc::mma_commit(t_full(ab));
+        }
+      }
+      if (!ok) {
+        if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
+        *abort = 1;
+      }
+      tc::mma_commit(drain);
+      volatile int never = 0;
+      tc::mbar_wait(drain, 0, &never);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // All four warps run every group and both named barriers of every tile;
+    // an abort only skips work.
+    const int q = warp & 3;         // TMEM lane quarter = vocabulary entries 32q..32q+31
+    const int et = threadIdx.x - 64;  // 0..127
+    auto aborted = [&]() { return __any_sync(0xFFFFFFFFu, *abort != 0); };
+    const __nv_bfloat16* W1 = reinterpret_cast<const __nv_bfloat16*>(p.W1);
+    for (int gq = 0; gq < ngroups; ++gq) {
+      // ---- gather B = W1[x_n] of this group's requests; per-request constants
+      if (!aborted()) {
+        const int i = gq * kRN + et;
+        int x = 0;
+        const bool valid = i < nrej;
+        if (valid) {
+          const int b = list[i];
+          const int n = p.n_acc[b];
+          x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
+          col_b[et] = b;
+          col_n[et] = n;
+          col_row[et] = p.vrow[b];
+          col_lsed[et] = p.lse[(size_t)b * p.g + n];
+          col_lset[et] = p.vlset[b];
+          if (x < 0 || x >= p.V) {
+            raise_status(p.status, DSPARK_ERANGE);
+            x = 0;
+          }
+        }
+        best_key[et] = -INFINITY;
+        best_blk[et] = kNoIdx;
+        const int m = et;
+        for (int kb = 0; kb < p.r / 64; ++kb) {
+          const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r + kb * 64);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const uint4 v = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+            const uint32_t dst = sB + kb * (kRN * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
+                                 ((uint32_t)(ch ^ (m & 7)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
+                         "r"(v.w)
+                         : "memory");
+          }
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(a_full);
+      }
+      asm volatile("bar.sync 2, 128;" ::: "memory");  // column constants visible to all epilogue warps
+      const int ncols = min(kRN, nrej - gq * kRN);
+      for (int i = 0; i < nt; ++i) {
+        const int it = gq * nt + i, t = tile_lo + i, ab = it & 1;
+        bool live = !aborted();
+        if (live) {
+          bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) {
+            if (lane == 0 && !*abort) {
+              raise_status(p.status, DSPARK_ETIMEOUT);
+              *abort = 1;
+            }
+            live = false;
+          }
+        }
+        const int v = t * kRM + q * 32 + lane;
+        if (live) {
+          tc::tc_fence_after();
+          for (int cc = 0; cc * 32 < ncols; ++cc) {
+            float a[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + cc * 32), a);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = cc * 32 + j;
+              float w = 0.f;
+              if (col < ncols && v < p.V) {
+                const int b = col_b[col];
+                const float u = __ldcs(p.U + ((size_t)b * p.g + col_n[col]) * p.V + v);
+                const float pv = __ldcs(p.P + (size_t)col_row[col] * p.V + v);
+                w = fmaxf(0.f, __expf(pv - col_lset[col]) - __expf(a[j] + u - col_lsed[col]));
+              }
+              a[j] = w;
+            }
+            const float s = transpose_sum32(a);  // this warp's 32 entries, request cc*32 + lane
+            part[q * kRN + cc * 32 + lane] = s;
+          }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(t_empty(ab));
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (live && q == 0) {
+          // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
+          for (int col = lane; col < ncols; col += 32) {
+            const int b = col_b[col], n = col_n[col];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int s = 2 * t + h;
+              if (s * 64 >= p.V) continue;
+              const float W = part[(2 * h) * kRN + col] + part[(2 * h + 1) * kRN + col];
+              if (!(W > 0.f)) continue;
+              const float key = logf(W) + gumbel(p.rng.word(kResidBlock, b, n, s));
+              if (key > best_key[col]) {  // blocks arrive in increasing order: ties keep the first
+                best_key[col] = key;
+                best_blk[col] = s;
+              }
+            }
+          }
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");  // part[] is rewritten by the next tile
+      }
+      if (q == 0 && !aborted()) {
+        for (int col = lane; col < ncols; col += 32)
+          p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
+      }
+      asm volatile("bar.sync 2, 128;" ::: "memory");  // constants are rewritten by the next group
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kRTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+}  // namespace
+
+int resid_tc_supported(const dspark_dims& d) {
+  return d.wdtype == DSPARK_BF16 && d.r % 64 == 0 && d.r <= 256 && d.V % 8 == 0 && d.B <= kRMaxB;
+}
+
+cudaError_t resid_tc_configure(dspark_ws* ws) {
+  const RSmem L = RSmem::make(ws->d.r);
+  const size_t smem = L.total + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_resid_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_resid_tc, kRThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1 || !encode_fn()) return cudaErrorNotSupported;
+  return cudaSuccess;
+}
+
+// The residual block draw for the requests verify flagged; writes
+// rpart[b * grid + cta]. Grid = one CTA per SM (no grid-wide barrier, so no
+// co-residency requirement).
+cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
+  const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)d.r};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  RParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = d.B;
+  p.g = d.gamma;
+  p.V = d.V;
+  p.r = d.r;
+  p.ntiles = (d.V + kRM - 1) / kRM;
+  p.G = grid;
+  p.rng = Rng::make(a.seed, a.round);
+  p.P = a.P;
+  p.U = a.U;
+  p.W1 = a.W1;
+  p.anchor = a.anchor;
+  p.tokens = a.tokens;
+  p.lse = a.lse;
+  p.vflag = ws->s.vflag;
+  p.n_acc = a.n_acc;
+  p.vrow = ws->s.vrow;
+  p.vlset = ws->s.vlset;
+  p.rpart = rpart;
+  p.status = ws->s.status;
+  const RSmem L = RSmem::make(d.r);
+  k_resid_tc<<<grid, kRThreads, L.total + 1024, st>>>(tm, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -426,11 +426,19 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
                                                    d.V, geo.S, rng, ws->s.vpart, a.n_acc, a.next_anchor,
                                                    ws->s.vflag, ws->s.vrow, ws->s.vlset, ws->s.status);
   const size_t smem = sizeof(float) * d.r;
-  k_resid_blocks<BF16><<<dim3(kResidChunks, d.B), 256, smem, st>>>(
-      a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
-      ws->s.vrow, ws->s.vlset, rng, ws->s.rpart);
+  int nchunk = kResidChunks;
+  if (BF16 && ws->use_tc && geo.resid_tc_ok) {
+    // residual block draw on tensor cores: one CTA per SM
+    nchunk = geo.num_sms;
+    cudaError_t e = launch_resid_tc(ws, a, ws->s.rpart, nchunk, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    k_resid_blocks<BF16><<<dim3(kResidChunks, d.B), 256, smem, st>>>(
+        a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
+        ws->s.vrow, ws->s.vlset, rng, ws->s.rpart);
+  }
   k_resid_pick<BF16><<<d.B, 256, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
-                                             d.r, geo.nblk, kResidChunks, ws->s.vflag, a.n_acc, ws->s.vrow,
+                                             d.r, geo.nblk, nchunk, ws->s.vflag, a.n_acc, ws->s.vrow,
                                              ws->s.vlset, rng, ws->s.rpart, a.next_anchor);
   *launches += 4;
   return cudaGetLastError();

@@ -30,8 +30,8 @@ def _wl(name, B, gamma, V, r, H=32, seed=31):
 
 
 def _draft(wl, dev, path, seed, rnd):
-    ws = Workspace.for_workload(wl, draft_path=path)
-    assert ws.draft_path == path
+    ws = Workspace.for_workload(wl, path=path)
+    assert ws.path == path
     d = ws.draft(dev["U"], dev["W1"], dev["W2"], dev["anchor"], dev["h"], dev["w"], dev["T"], seed, rnd)
     torch.cuda.synchronize()
     st = ws.device_status()
@@ -95,3 +95,37 @@ def test_tc_repeatable_and_round_sensitive():
     for k in a:
         assert (a[k] == b[k]).all()
     assert not (a["tokens"] == c["tokens"]).all()
+
+
+@pytest.mark.parametrize("B,gamma,V,r,sigma", [
+    (24, 3, 1000, 128, 2.0),     # vocabulary ends inside a 128-wide tile
+    (300, 2, 3000, 256, 3.0),    # most drafts rejected: three groups of 128 requests
+    (128, 5, 8192, 192, 0.5),
+])
+def test_residual_paths_match_oracle(B, gamma, V, r, sigma):
+    """Verify on the oracle's drafts with the tcgen05 and the SIMT residual pass."""
+    from parity import Tally, compare_verify, pack_np, row_off_np
+    wl = Workload(f"resid_{B}_{V}", B=B, gamma=gamma, V=V, r=r, H=16, wdtype="bf16", mode="static",
+                  seed=B + V, u_std=2.0, w_std=0.05, noise="const", noise_args=(sigma,))
+    inp = make_inputs(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], 3, 1)
+    rng = np.random.default_rng(B)
+    L = rng.integers(1, gamma + 2, B).astype(np.int32)
+    ro = row_off_np(L)
+    P = pack_np(npi["P_full"], L)
+    ov = oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], 3, 1)
+    assert ov["resid"].sum() > 0
+    outs = {}
+    for path in ("tcgen05", "simt"):
+        ws = Workspace.for_workload(wl, path=path)
+        out = ws.verify(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(L).cuda(),
+                        dev["anchor"], torch.from_numpy(od["tokens"]).cuda(),
+                        torch.from_numpy(od["pd_tok"].astype(np.float32)).cuda(),
+                        torch.from_numpy(od["lse"].astype(np.float32)).cuda(), dev["U"], dev["W1"], dev["W2"], 3, 1)
+        torch.cuda.synchronize()
+        assert ws.device_status() == 0, path
+        outs[path] = gpu_np(out)
+        t = compare_verify(outs[path], ov, range(B))
+        t.check_rate()
+        assert t.compared > 0

@@ -62,7 +62,7 @@ def test_noalloc_draft_matches_workspace_draft_on_two_calls():
     wl = Workload("noalloc", B=48, gamma=4, V=5000, r=256, H=96, wdtype="bf16", mode="static", seed=41,
                   u_std=2.0, w_std=0.05)
     dev = {k: v.cuda().contiguous() for k, v in make_inputs(wl, with_target=False).items()}
-    ws = Workspace.for_workload(wl, draft_path="simt")
+    ws = Workspace.for_workload(wl, path="simt")
     anchors = [dev["anchor"], torch.roll(dev["anchor"], 7).contiguous()]
     for call, (rnd, anchor) in enumerate(zip((3, 4), anchors)):
         ref = ws.draft(dev["U"], dev["W1"], dev["W2"], anchor, dev["h"], dev["w"], dev["T"], 9, rnd)
