@@ -71,8 +71,11 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   Geometry& geo = ws->geo;
   geo.num_sms = sms > 0 ? sms : 1;
   geo.nblk = (d.V + kBlockW - 1) / kBlockW;
-  geo.chunk = d.V > kSweepChunk ? kSweepChunk : (int)round_up((size_t)d.V, kBlockW);
-  geo.S = (d.V + geo.chunk - 1) / geo.chunk;
+  geo.sweep_bulk = (d.V % kBlockW) == 0 && sweep_bulk_configure() == cudaSuccess;
+  cudaGetLastError();
+  geo.sweep_grid = geo.num_sms * (geo.sweep_bulk ? 2 : 4);  // bulk: 2 x 96 KB ring per SM
+  // a range of ceil(R*nblk/grid) blocks touches at most ceil(R/grid) + 1 rows
+  geo.SL = (d.B * (d.gamma + 1) + geo.sweep_grid - 1) / geo.sweep_grid + 2;
   geo.tc_ok = draft_tc_supported(d);
 
   const size_t BG = (size_t)d.B * d.gamma;
@@ -89,7 +92,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_sh = carve(sizeof(float) * BG);
   const size_t o_blk = carve(sizeof(float) * (size_t)d.B * geo.nblk);
   const size_t o_ring = carve(d.mode == DSPARK_COMPACT_LAGGED ? sizeof(float) * (d.lag + 1) * BG : 0);
-  const size_t o_vpart = carve(sizeof(float4) * rows * geo.S);
+  const size_t o_vpart = carve(sizeof(float4) * (size_t)geo.sweep_grid * geo.SL);
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
   const size_t o_vlset = carve(sizeof(float) * d.B);
@@ -99,7 +102,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   geo.rchunks = geo.num_sms > kResidChunks ? geo.num_sms : kResidChunks;
   const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * geo.rchunks);
   const size_t o_xbuf = carve(sizeof(int32_t) * d.B);
-  size_t o_dpart = 0, o_drec = 0;
+  size_t o_dpart = 0, o_drec = 0, o_aimg = 0;
   if (geo.tc_ok) {
     if (draft_tc_configure(ws) != cudaSuccess) geo.tc_ok = 0;
   }
@@ -107,6 +110,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
     const size_t nrows = draft_tc_scratch_rows(d, geo.tc_grid);
     o_dpart = carve(sizeof(float4) * nrows);
     o_drec = carve(sizeof(float) * kBlockW * nrows);
+    o_aimg = carve((size_t)geo.tc_groups * 128 * d.r * 2);
   }
   if (plan_configure() != cudaSuccess) {
     delete ws;
@@ -135,6 +139,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.xbuf = reinterpret_cast<int32_t*>(base + o_xbuf);
   s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
   s.drec = geo.tc_ok ? reinterpret_cast<float*>(base + o_drec) : nullptr;
+  s.aimg = geo.tc_ok ? static_cast<void*>(base + o_aimg) : nullptr;
   ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(ws->arena);

@@ -10,7 +10,6 @@
 namespace dspark {
 
 // Tunables of the launch shapes (none of them changes a result).
-constexpr int kSweepChunk = 16384;  // target-logit elements per verify-sweep work item
 constexpr int kResidChunks = 32;    // CTAs per rejected request in the SIMT residual pass
 
 struct DraftArgs {
@@ -51,7 +50,7 @@ struct Scratch {
   float* blk;             // [B*nblk] block log-masses of one draft step (SIMT path)
   float* ring;            // [(lag+1)*B*gamma] confidence ring of the lagged planner
   uint32_t* plan_round;   // [1] rounds planned since the last reset
-  float4* vpart;          // [B*(gamma+1)*S] verify-sweep partials (m, s, key, block)
+  float4* vpart;          // [sweep_grid*SL] verify-sweep partials (m, s, key, block)
   int* vflag;             // [B] 1 = next anchor comes from the residual
   int* vrow;              // [B] packed row of the first rejection
   float* vlset;           // [B] target log-sum-exp of that row
@@ -59,14 +58,16 @@ struct Scratch {
   // persistent tcgen05 draft kernel
   float4* dpart;          // [grid*rowsTotal] per-CTA (max, sum, key, block)
   float* drec;            // [grid*rowsTotal*64] per-CTA z values of its best block
+  void* aimg;             // [groups][128 x r] bf16: next A operand in its swizzled shared layout
   unsigned* barrier;      // [4] grid-barrier words
   int32_t* xbuf;          // [B] current x_{k-1}
 };
 
 struct Geometry {
-  int nblk;     // ceil(V / 64)
-  int S;        // verify-sweep items per row
-  int chunk;    // elements per verify-sweep item (multiple of 64)
+  int nblk;        // ceil(V / 64)
+  int sweep_grid;  // CTAs of the verify sweep
+  int sweep_bulk;  // bulk-copy sweep (V % 64 == 0)
+  int SL;          // sweep partial slots per CTA (rows one range can touch)
   int num_sms;
   // persistent draft kernel
   int tc_ok;        // tcgen05 path usable for these dims
@@ -111,6 +112,7 @@ cudaError_t resid_tc_configure(dspark_ws* ws);
 cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st);
 
 size_t plan_smem_bytes(const dspark_dims& d);
+cudaError_t sweep_bulk_configure();
 cudaError_t plan_configure();
 
 }  // namespace dspark

@@ -45,6 +45,7 @@ constexpr int kUStage = kTcRows * kTcN * 4;  // 32 KB: two 128 x 32 fp32 boxes
 constexpr int kUBox = kTcRows * 32 * 4;      // 16 KB
 constexpr int kTmemCols = 128;      // two 64-column fp32 accumulators
 constexpr int kMaxGroups = 8;       // B <= 1024
+constexpr int kMaxPartLanes = 8;    // partials per lane in the row reduction (grid <= 256)
 
 static_assert(kTcN == kBlockW, "a vocabulary tile is one sampler block");
 
@@ -56,7 +57,7 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     s.w2 = s.a + kTcRows * r * 2;
     s.u = s.w2 + kNW * r * 128;
     s.bars = s.u + kNU * kUStage;
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 4 + 2);
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 4 + 3);
     s.total = s.misc + 64;
     return s;
   }
@@ -78,6 +79,7 @@ struct TcParams {
   int32_t* xbuf;
   float4* dpart;  // [nG * 128][Ggmax]
   float* drec;    // [G][128][64]
+  __nv_bfloat16* aimg;  // [nG][128 x r] next A operand, already in its swizzled shared layout
   unsigned* bar;  // [0] arrivals, [1] generation
   int* status;
 };
@@ -137,6 +139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + 2 + i); };
   const uint32_t a_full = bars + 8u * (2 * kNW + 2 * kNU + 4);
   const uint32_t drain = a_full + 8u;
+  const uint32_t a_img = a_full + 16u;  // the bulk copy of the next A image
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
 
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc::mbar_init(a_full, 4);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(a_img, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -269,27 +273,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float* rec = p.drec + ((size_t)c * kTcRows + m) * kTcN;
     for (int k = 1; k <= p.g; ++k) {
       // ---- gather A = W1[x_{k-1}] rows (K-major, 128-byte swizzle) and c_k
-      if (!aborted()) {
+      if (!aborted() && k > 1) {
+        // the reducers of the last step wrote this group's A (rows W1[x_{k-1}]
+        // in the swizzled layout) as one contiguous image: one bulk copy
+        if (leader) {
+          tc::fence_proxy_async_global();
+          const uint32_t bytes = (uint32_t)kTcRows * p.r * 2u;
+          tc::mbar_arrive_expect_tx(a_img, bytes);
+          tc::bulk_load(sA, p.aimg + (size_t)grp * kTcRows * p.r, bytes, a_img);
+        }
+        bool ok = tc::mbar_wait(a_img, (k - 2) & 1, abort);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) {
+          if (lane == 0 && !*abort) {
+            raise_status(p.status, DSPARK_ETIMEOUT);
+            *abort = 1;
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(a_full);
+        }
+      } else if (!aborted()) {
         int x = 0;
         if (valid) {
-          x = k == 1 ? p.anchor[b] : __ldcg(p.xbuf + b);  // written by another CTA
+          x = p.anchor[b];
           if (x < 0 || x >= p.V) {
             raise_status(p.status, DSPARK_ERANGE);
             x = 0;
           }
         }
-        float cdot = 0.f;
+        // every 16-byte piece of the row in flight at once (cp.async), written
+        // straight into its 128-byte-swizzled position
+        const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r);
         for (int kb = 0; kb < p.r / 64; ++kb) {
-          const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r + kb * 64);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
-            uint4 v = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
             const uint32_t dst = sA + kb * (kTcRows * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
                                  ((uint32_t)(ch ^ (m & 7)) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
-                         "r"(v.w)
-                         : "memory");
-            if (cg == 0 && valid) {
+            if (valid) {
+              tc::cp_async16(dst, src + kb * 8 + ch);
+            } else {
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+            }
+          }
+        }
+        tc::cp_async_wait_all();
+        float cdot = 0.f;
+        if (cg == 0 && valid) {
+          for (int kb = 0; kb < p.r / 64; ++kb) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              uint4 v;
+              const uint32_t a = sA + kb * (kTcRows * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
+                                 ((uint32_t)(ch ^ (m & 7)) << 4);
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
               const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
               const float* wr = p.w + p.H + kb * 64 + ch * 8;
 #pragma unroll
@@ -397,12 +434,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         MS ms{-INFINITY, 0.f};
         KeyIdx kb = key_none();
         int owner = -1;
-        for (int i = lane; i < Gg2; i += 32) {
-          const float4 d = __ldcg(p.dpart + (size_t)br * p.Ggmax + i);  // written by other CTAs
-          ms = ms_combine(ms, MS{d.x, d.y});
-          const KeyIdx nb = better(kb, KeyIdx{d.z, __float_as_int(d.w)});
-          if (nb.idx != kb.idx || nb.key != kb.key) owner = i;
-          kb = nb;
+        {
+          // every partial of the row in flight at once (written by other CTAs)
+          float4 dd[kMaxPartLanes];
+#pragma unroll
+          for (int u = 0; u < kMaxPartLanes; ++u) {
+            const int i = lane + 32 * u;
+            dd[u] = i < Gg2 ? __ldcg(p.dpart + (size_t)br * p.Ggmax + i) : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
+          }
+#pragma unroll
+          for (int u = 0; u < kMaxPartLanes; ++u) {
+            const float4 d = dd[u];
+            ms = ms_combine(ms, MS{d.x, d.y});
+            const KeyIdx nb = better(kb, KeyIdx{d.z, __float_as_int(d.w)});
+            if (nb.idx != kb.idx || nb.key != kb.key) owner = lane + 32 * u;
+            kb = nb;
+          }
         }
         ms = warp_ms(ms);
         const KeyIdx best = warp_best(kb);
@@ -434,6 +481,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.pd_tok[o] = expf(zx - L2);
           p.lse[o] = L2;
           p.xbuf[br] = kt.idx;
+        }
+        if (k < p.g) {
+          // the next step's A row W1[x_k] into the group's image, and
+          // c_{k+1} = sigma((s_h + w_r . W1[x_k]) / T_{k+1}) while the row is at hand
+          const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)kt.idx * p.r);
+          __nv_bfloat16* img = p.aimg + (size_t)g2 * kTcRows * p.r;
+          float cd = 0.f;
+          for (int ci = lane; ci < p.r / 8; ci += 32) {
+            const int kb2 = ci >> 3, ch = ci & 7;
+            const uint4 v = __ldg(src + ci);
+            *reinterpret_cast<uint4*>(img + kb2 * (kTcRows * 64) + (m2 >> 3) * 512 + (m2 & 7) * 64 +
+                                      ((ch ^ (m2 & 7)) << 3)) = v;
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+            const float* wr = p.w + p.H + ci * 8;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __bfloat1622float2(h2[e]);
+              cd = fmaf(f.x, wr[2 * e], cd);
+              cd = fmaf(f.y, wr[2 * e + 1], cd);
+            }
+          }
+          tc::fence_proxy_async_global();  // the image is read by bulk copies
+          cd = warp_sum(cd);
+          if (lane == 0) {
+            const size_t o2 = (size_t)br * p.g + k;
+            const float cf = 1.f / (1.f + expf(-(p.s_h[o2] + cd) / p.T[k]));
+            if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
+            p.conf[o2] = cf;
+          }
         }
       }
       grid_sync(p, leader, abort);
@@ -549,6 +625,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.xbuf = ws->s.xbuf;
   p.dpart = ws->s.dpart;
   p.drec = ws->s.drec;
+  p.aimg = reinterpret_cast<__nv_bfloat16*>(ws->s.aimg);
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
 

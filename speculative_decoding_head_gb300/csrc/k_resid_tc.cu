@@ -32,7 +32,8 @@ namespace dspark {
 
 namespace {
 
-constexpr int kRThreads = 192;
+constexpr int kRThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter)
+constexpr int kREpi = 8;
 constexpr int kRM = 128;          // vocabulary entries per tile (MMA M)
 constexpr int kRN = 128;          // requests per group (MMA N)
 constexpr int kRNW = 2;           // W2 ring depth
@@ -135,9 +136,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(t_full(i), 1);
-      tc::mbar_init(t_empty(i), 4);
+      tc::mbar_init(t_empty(i), kREpi);
     }
-    tc::mbar_init(a_full, 4);
+    tc::mbar_init(a_full, kREpi);
     tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_barrier_init();
@@ -231,10 +232,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // All four warps run every group and both named barriers of every tile;
-    // an abort only skips work.
+    // All eight warps run every group and every named barrier of every tile;
+    // an abort only skips work. Warps w and w + 4 share a TMEM lane quarter and
+    // split its 32-request chunks between them.
     const int q = warp & 3;         // TMEM lane quarter = vocabulary entries 32q..32q+31
-    const int et = threadIdx.x - 64;  // 0..127
+    const int half = (warp - 2) >> 2;
+    const int et = threadIdx.x - 64;  // 0..255
     auto aborted = [&]() { return __any_sync(0xFFFFFFFFu, *abort != 0); };
     const __nv_bfloat16* W1 = reinterpret_cast<const __nv_bfloat16*>(p.W1);
     for (int gq = 0; gq < ngroups; ++gq) {
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       if (!aborted()) {
         const int i = gq * kRN + et;
         int x = 0;
-        const bool valid = i < nrej;
+        const bool valid = et < kRN && i < nrej;
         if (valid) {
           const int b = list[i];
           const int n = p.n_acc[b];
@@ -257,10 +260,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
             x = 0;
           }
         }
-        best_key[et] = -INFINITY;
-        best_blk[et] = kNoIdx;
+        if (et < kRN) {
+          best_key[et] = -INFINITY;
+          best_blk[et] = kNoIdx;
+        }
         const int m = et;
-        for (int kb = 0; kb < p.r / 64; ++kb) {
+        for (int kb = 0; kb < p.r / 64 && et < kRN; ++kb) {
           const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r + kb * 64);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
@@ -276,8 +281,24 @@ __global__ void __launch_bounds__(kRThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(a_full);
       }
-      asm volatile("bar.sync 2, 128;" ::: "memory");  // column constants visible to all epilogue warps
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // column constants visible to all epilogue warps
       const int ncols = min(kRN, nrej - gq * kRN);
+      // pull the U and P rows of local tile ti (4 lines of 128 B per row and
+      // request) into L2 ahead of the demand loads, two tiles ahead
+      auto prefetch_tile = [&](int ti) {
+        if (ti >= nt) return;
+        const int vb = (tile_lo + ti) * kRM;
+        for (int l = et; l < ncols * 8; l += 32 * kREpi) {
+          const int col = l >> 3, part8 = l & 7;
+          const int v = vb + (part8 & 3) * 32;
+          if (v >= p.V) continue;
+          const float* a = part8 < 4 ? p.U + ((size_t)col_b[col] * p.g + col_n[col]) * p.V + v
+                                     : p.P + (size_t)col_row[col] * p.V + v;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+        }
+      };
+      prefetch_tile(0);
+      prefetch_tile(1);
       for (int i = 0; i < nt; ++i) {
         const int it = gq * nt + i, t = tile_lo + i, ab = it & 1;
         bool live = !aborted();
@@ -293,9 +314,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
         }
         const int v = t * kRM + q * 32 + lane;
+        if (live) prefetch_tile(i + 2);
         if (live) {
           tc::tc_fence_after();
-          for (int cc = 0; cc * 32 < ncols; ++cc) {
+          for (int cc = half; cc * 32 < ncols; cc += 2) {
             float a[32];
             tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + cc * 32), a);
             tc::tmem_wait_ld();
@@ -318,8 +340,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
         }
-        asm volatile("bar.sync 2, 128;" ::: "memory");
-        if (live && q == 0) {
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (live && warp == 4) {
           // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
           for (int col = lane; col < ncols; col += 32) {
             const int b = col_b[col], n = col_n[col];
@@ -337,13 +359,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
           }
         }
-        asm volatile("bar.sync 2, 128;" ::: "memory");  // part[] is rewritten by the next tile
+        asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
       }
-      if (q == 0 && !aborted()) {
+      if (warp == 4 && !aborted()) {
         for (int col = lane; col < ncols; col += 32)
           p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
       }
-      asm volatile("bar.sync 2, 128;" ::: "memory");  // constants are rewritten by the next group
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // constants are rewritten by the next group
     }
   }
   tc::tc_fence_before();

@@ -16,15 +16,17 @@
 // Every draw is the library's two-level Gumbel-max (64-token blocks).
 //
 // Kernels (all launched with grids that do not depend on device-side sizes):
-//   k_verify_sweep     persistent grid-stride over (row, chunk) items: online
-//                      log-sum-exp of P; for the last verified row of a
-//                      request also the block draw of the bonus token.
-//   k_verify_finalize  one warp per request: accept tests, first rejection,
-//                      bonus token draw inside its block.
+//   k_verify_sweep     the verified rows split into equal contiguous ranges of
+//                      64-token blocks, one per CTA: online log-sum-exp of P;
+//                      for the last verified row of a request also the block
+//                      draw of the bonus token.
+//   k_verify_finalize  one warp per request, one lane per row: accept tests,
+//                      first rejection, bonus token draw inside its block.
 //   k_resid_blocks     grid (chunks, B): residual block masses and block draw.
 //   k_resid_pick       grid (B): residual token draw inside the drawn block.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
+#include "tc_ptx.cuh"
 
 namespace dspark {
 
@@ -40,121 +42,85 @@ __device__ __forceinline__ int request_of_row(const int32_t* __restrict__ row_of
   return lo;
 }
 
+// The verified rows, flattened into 64-token block units u = q * nblk + s
+// (row q, block s), are split into gridDim.x contiguous ranges of (almost)
+// equal length, one per CTA: every CTA streams the same number of bytes.
+// A range touches a few consecutive rows; for each it writes one partial
+// (max, sum exp, best block key, best block) to part[cta * SL + row - first].
+__device__ __forceinline__ long long unit_lo(int c, long long T, int G) { return (long long)c * T / G; }
+// the CTA whose range holds unit u
+__device__ __forceinline__ int unit_owner(long long u, long long T, int G) {
+  return (int)(((u + 1) * (long long)G - 1) / T);
+}
+
+constexpr int kSweepUnroll = 4;
+
 __global__ void __launch_bounds__(kSweepThreads)
     k_verify_sweep(const float* __restrict__ P, const int32_t* __restrict__ row_off,
-                   const int32_t* __restrict__ lengths, int B, int V, int S, int chunk, int Rmax, Rng rng,
+                   const int32_t* __restrict__ lengths, int B, int V, int nblk, int Rmax, int SL, Rng rng,
                    float4* __restrict__ part) {
   __shared__ MS red_ms[kSweepThreads / 32];
   __shared__ KeyIdx red_k[kSweepThreads / 32];
   const int R = min(max(row_off[B], 0), Rmax);  // finalize reports an inconsistent row_off
+  const long long T = (long long)R * nblk;
+  if (T == 0) return;
+  const int G = gridDim.x, c = blockIdx.x;
+  const long long lo = unit_lo(c, T, G), hi = unit_lo(c + 1, T, G);
+  if (lo >= hi) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int item = blockIdx.x; item < R * S; item += gridDim.x) {
-    const int q = item / S, sp = item - q * S;
+  const int half = lane >> 4, l16 = lane & 15;
+  const bool vec = (V & 3) == 0;
+  const int q0 = (int)(lo / nblk);
+  for (int q = q0; (long long)q * nblk < hi; ++q) {
+    const int s0 = (int)max(lo - (long long)q * nblk, 0ll);
+    const int s1 = (int)min(hi - (long long)q * nblk, (long long)nblk);
     const int b = request_of_row(row_off, B, q);
     const int j = q - row_off[b];
     const bool bonus = j == lengths[b] - 1;
-    const int lo = sp * chunk, hi = min(V, lo + chunk);
     const float* row = P + (size_t)q * V;
     MS ms{-INFINITY, 0.f};
     KeyIdx kb = key_none();
-    // each warp takes whole 64-token blocks: lanes read v and v + 32
-    for (int s0 = lo / kBlockW + warp; s0 * kBlockW < hi; s0 += nw) {
-      const int v0 = s0 * kBlockW + lane, v1 = v0 + 32;
-      const float x0 = v0 < hi ? __ldcs(row + v0) : -INFINITY;
-      const float x1 = v1 < hi ? __ldcs(row + v1) : -INFINITY;
-      if (bonus) {
-        const float m = warp_max(fmaxf(x0, x1));
-        if (m == -INFINITY) continue;  // a fully masked block has no mass
-        float t = (v0 < hi ? __expf(x0 - m) : 0.f) + (v1 < hi ? __expf(x1 - m) : 0.f);
-        t = warp_sum(t);
-        const MS blk{m, t};
-        if (lane == 0) {
-          ms = ms_combine(ms, blk);
-          kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, b, j, s0)), s0});
+    // a half-warp takes one 64-token block: 16 lanes x 4 tokens
+    for (int sb = s0 + 2 * warp; sb < s1; sb += 2 * nw * kSweepUnroll) {
+      float x[kSweepUnroll][4];
+#pragma unroll
+      for (int u = 0; u < kSweepUnroll; ++u) {
+        const int s = sb + half + 2 * nw * u;
+        const int v = s * kBlockW + 4 * l16;
+        if (s < s1 && v < V) {
+          if (vec) {
+            const float4 f = __ldcs(reinterpret_cast<const float4*>(row + v));
+            x[u][0] = f.x; x[u][1] = f.y; x[u][2] = f.z; x[u][3] = f.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[u][e] = v + e < V ? __ldcs(row + v + e) : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[u][e] = -INFINITY;
         }
-      } else {
-        const float m = fmaxf(fmaxf(x0, x1), ms.m);
-        if (m == -INFINITY) continue;
-        float t = ms.m == -INFINITY ? 0.f : ms.s * __expf(ms.m - m);
-        if (v0 < hi) t += __expf(x0 - m);
-        if (v1 < hi) t += __expf(x1 - m);
-        ms = MS{m, t};
-      }
-    }
-    ms = warp_ms(ms);
-    kb = warp_best(kb);
-    if (lane == 0) {
-      red_ms[warp] = ms;
-      red_k[warp] = kb;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      MS m2 = lane < nw ? red_ms[lane] : MS{-INFINITY, 0.f};
-      KeyIdx k2 = lane < nw ? red_k[lane] : key_none();
-      m2 = warp_ms(m2);
-      k2 = warp_best(k2);
-      if (lane == 0) part[item] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
-    }
-    __syncthreads();
-  }
-}
-
-// Vectorised sweep for V % 4 == 0 (rows 16-byte aligned): each thread streams
-// float4 values, four loads in flight per thread; a half-warp holds one
-// 64-token block per load, so the bonus row's block masses need only
-// 16-lane shuffles.
-constexpr int kSweepUnroll = 4;
-
-__global__ void __launch_bounds__(kSweepThreads)
-    k_verify_sweep4(const float* __restrict__ P, const int32_t* __restrict__ row_off,
-                    const int32_t* __restrict__ lengths, int B, int V, int S, int chunk, int Rmax, Rng rng,
-                    float4* __restrict__ part) {
-  __shared__ MS red_ms[kSweepThreads / 32];
-  __shared__ KeyIdx red_k[kSweepThreads / 32];
-  const int R = min(max(row_off[B], 0), Rmax);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int V4 = V >> 2;
-  for (int item = blockIdx.x; item < R * S; item += gridDim.x) {
-    const int q = item / S, sp = item - q * S;
-    const int b = request_of_row(row_off, B, q);
-    const int j = q - row_off[b];
-    const bool bonus = j == lengths[b] - 1;
-    const int lo4 = (sp * chunk) >> 2, hi4 = min(V4, lo4 + (chunk >> 2));
-    const float4* row = reinterpret_cast<const float4*>(P + (size_t)q * V);
-    MS ms{-INFINITY, 0.f};
-    KeyIdx kb = key_none();
-    // uniform trip count across the CTA: the bonus branch shuffles over full warps
-    for (int base = lo4; base < hi4; base += kSweepUnroll * kSweepThreads) {
-      const int f0 = base + threadIdx.x;
-      float4 x[kSweepUnroll];
-#pragma unroll
-      for (int u = 0; u < kSweepUnroll; ++u) {
-        const int f = f0 + u * kSweepThreads;
-        x[u] = f < hi4 ? __ldcs(row + f) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
 #pragma unroll
       for (int u = 0; u < kSweepUnroll; ++u) {
-        const float m4 = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+        const float m4 = fmaxf(fmaxf(x[u][0], x[u][1]), fmaxf(x[u][2], x[u][3]));
         if (bonus) {
-          // this half-warp's 16 float4 are one 64-token block
           float m = m4;
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
           float t = 0.f;
           if (m != -INFINITY)
-            t = __expf(x[u].x - m) + __expf(x[u].y - m) + __expf(x[u].z - m) + __expf(x[u].w - m);
+            t = __expf(x[u][0] - m) + __expf(x[u][1] - m) + __expf(x[u][2] - m) + __expf(x[u][3] - m);
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-          const int f = f0 + u * kSweepThreads;
-          if ((lane & 15) == 0 && f < hi4 && m != -INFINITY) {
-            const int s0 = f >> 4;  // 16 float4 per block
+          const int s = sb + half + 2 * nw * u;
+          if (l16 == 0 && s < s1 && m != -INFINITY) {
             ms = ms_combine(ms, MS{m, t});
-            kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, b, j, s0)), s0});
+            kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, b, j, s)), s});
           }
         } else if (m4 != -INFINITY) {
           const float m = fmaxf(m4, ms.m);
           float t = ms.m == -INFINITY ? 0.f : ms.s * __expf(ms.m - m);
-          t += __expf(x[u].x - m) + __expf(x[u].y - m) + __expf(x[u].z - m) + __expf(x[u].w - m);
+          t += __expf(x[u][0] - m) + __expf(x[u][1] - m) + __expf(x[u][2] - m) + __expf(x[u][3] - m);
           ms = MS{m, t};
         }
       }
@@ -171,62 +137,221 @@ __global__ void __launch_bounds__(kSweepThreads)
       KeyIdx k2 = lane < nw ? red_k[lane] : key_none();
       m2 = warp_ms(m2);
       k2 = warp_best(k2);
-      if (lane == 0) part[item] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
+      if (lane == 0 && q - q0 < SL) part[(size_t)c * SL + (q - q0)] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
     }
     __syncthreads();
   }
 }
 
+// Bulk-copy sweep for V % 64 == 0: unit u is then tokens [64u, 64u + 64) of
+// the packed rows, so a CTA's range is one contiguous byte range of P. It is
+// streamed through a 3-deep ring of 32 KB stages by cp.async.bulk and
+// consumed from shared memory one 64-token block per thread: the thread reads
+// its block's 16 float4 in a rotated order (conflict-free across the warp;
+// the order does not matter for a max and a sum), forms the block's
+// (max, sum exp) with 64 independent exponentials, folds it into the row and,
+// on the last verified row of a request, draws the bonus block key. Rows
+// change only at block boundaries; a thread flushes a finished row into its
+// per-row slot.
+constexpr int kBulkThreads = 128;
+constexpr int kBulkStages = 3;
+constexpr int kBulkUnits = kBulkThreads;             // one block per thread per stage
+constexpr int kBulkFloats = kBulkUnits * kBlockW;   // 8192 fp32 = 32 KB
+constexpr int kBulkMaxSlots = 8;
+
+size_t sweep_bulk_smem_bytes() {
+  return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 128;
+}
+
+__global__ void __launch_bounds__(kBulkThreads)
+    k_verify_sweep_bulk(const float* __restrict__ P, const int32_t* __restrict__ row_off,
+                        const int32_t* __restrict__ lengths, int B, int nblk, int Rmax, int SL, Rng rng,
+                        float4* __restrict__ part, int* __restrict__ status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* stage = reinterpret_cast<float*>(smem);
+  float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
+                                               (size_t)kBulkMaxSlots * kBulkThreads * 16);
+  const int R = min(max(row_off[B], 0), Rmax);
+  const long long T = (long long)R * nblk;
+  if (T == 0) return;
+  const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x;
+  const long long lo = unit_lo(c, T, G), hi = unit_lo(c + 1, T, G);
+  if (lo >= hi) return;
+  const int q0 = (int)(lo / nblk);
+  const int nslots = (int)((hi - 1) / nblk) - q0 + 1;
+  if (nslots > SL || nslots > kBulkMaxSlots) {  // a range never spans this many rows
+    if (tid == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  const int nchunks = (int)((hi - lo + kBulkUnits - 1) / kBulkUnits);
+  const uint32_t bar0 = tc::smem_u32(bars);
+  const uint32_t st0 = tc::smem_u32(stage);
+  for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
+    slot[i] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
+  if (tid == 0) {
+    for (int i = 0; i < kBulkStages; ++i) tc::mbar_init(bar0 + 8u * i, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  auto issue = [&](int ch) {
+    const long long u = lo + (long long)ch * kBulkUnits;
+    const int units = (int)min((long long)kBulkUnits, hi - u);
+    const uint32_t bytes = (uint32_t)units * kBlockW * 4u;
+    const int sidx = ch % kBulkStages;
+    tc::mbar_arrive_expect_tx(bar0 + 8u * sidx, bytes);
+    tc::bulk_load(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, bar0 + 8u * sidx);
+  };
+  int issued = 0;  // chunks issued (thread 0's count)
+  if (tid == 0)
+    for (; issued < kBulkStages && issued < nchunks; ++issued) issue(issued);
+  volatile int never = 0;
+  int q_cur = -1, bcur = 0, jcur = 0;
+  bool bonus = false;
+  MS ms{-INFINITY, 0.f};
+  KeyIdx kb = key_none();
+  auto flush = [&]() {
+    if (q_cur >= 0) {
+      float4& sl = slot[(q_cur - q0) * kBulkThreads + tid];
+      const MS mm = ms_combine(MS{sl.x, sl.y}, ms);
+      const KeyIdx kk = better(KeyIdx{sl.z, __float_as_int(sl.w)}, kb);
+      sl = make_float4(mm.m, mm.s, kk.key, __int_as_float(kk.idx));
+    }
+    ms = MS{-INFINITY, 0.f};
+    kb = key_none();
+  };
+  bool failed = false;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const int sidx = ch % kBulkStages;
+    bool ok = tc::mbar_wait(bar0 + 8u * sidx, (ch / kBulkStages) & 1, &never);
+    if (__syncthreads_or(!ok)) {  // the same answer in every thread
+      if (tid == 0) raise_status(status, DSPARK_ETIMEOUT);
+      failed = true;
+      break;
+    }
+    const long long u = lo + (long long)ch * kBulkUnits + tid;
+    if (u < hi) {
+      const float4* blk4 = reinterpret_cast<const float4*>(stage + (size_t)sidx * kBulkFloats) + tid * 16;
+      float4 x[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = blk4[(i + tid) & 15];  // rotated: conflict-free
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
+      float t = 0.f;
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          t += (__expf(x[i].x - m) + __expf(x[i].y - m)) + (__expf(x[i].z - m) + __expf(x[i].w - m));
+        const int q = (int)(u / nblk), sblk = (int)(u - (long long)q * nblk);
+        if (q != q_cur) {
+          flush();
+          q_cur = q;
+          bcur = request_of_row(row_off, B, q);
+          jcur = q - row_off[bcur];
+          bonus = jcur == lengths[bcur] - 1;
+        }
+        ms = ms_combine(ms, MS{m, t});
+        if (bonus) kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, bcur, jcur, sblk)), sblk});
+      }
+    }
+    __syncthreads();  // every thread is done with this stage
+    if (tid == 0 && issued < nchunks) issue(issued++);
+  }
+  if (failed) {
+    if (tid == 0)  // let the copies already issued land before the CTA exits
+      for (int ch = max(0, issued - kBulkStages); ch < issued; ++ch) {
+        volatile int nv = 0;
+        tc::mbar_wait(bar0 + 8u * (ch % kBulkStages), (ch / kBulkStages) & 1, &nv);
+      }
+    return;
+  }
+  flush();
+  __syncthreads();
+  // reduce each row slot over the CTA's threads: warp w takes slots w, w + 4, ...
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int sl = warp; sl < nslots; sl += kBulkThreads / 32) {
+    MS m2{-INFINITY, 0.f};
+    KeyIdx k2 = key_none();
+    for (int i = lane; i < kBulkThreads; i += 32) {
+      const float4 d = slot[sl * kBulkThreads + i];
+      m2 = ms_combine(m2, MS{d.x, d.y});
+      k2 = better(k2, KeyIdx{d.z, __float_as_int(d.w)});
+    }
+    m2 = warp_ms(m2);
+    k2 = warp_best(k2);
+    if (lane == 0) part[(size_t)c * SL + sl] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
+  }
+}
+
+// One warp per request. Lane j handles target row j: its log-sum-exp from the
+// sweep partials, p_t of draft x_{j+1} and the accept test; the first
+// rejection is the lowest failing lane. Then the bonus token draw inside its
+// block, or the hand-over to the residual pass.
 __global__ void __launch_bounds__(128)
     k_verify_finalize(const float* __restrict__ P, const int32_t* __restrict__ row_off,
                       const int32_t* __restrict__ lengths, const int32_t* __restrict__ anchor,
-                      const int32_t* __restrict__ tokens,
-                      const float* __restrict__ pd_tok, int B, int g, int V, int S, Rng rng,
-                      const float4* __restrict__ part, int32_t* __restrict__ n_acc,
-                      int32_t* __restrict__ next_anchor, int* __restrict__ vflag, int* __restrict__ vrow,
-                      float* __restrict__ vlset, int* __restrict__ status) {
+                      const int32_t* __restrict__ tokens, const float* __restrict__ pd_tok, int B, int g, int V,
+                      int nblk, int SL, int Gs, Rng rng, const float4* __restrict__ part,
+                      int32_t* __restrict__ n_acc, int32_t* __restrict__ next_anchor, int* __restrict__ vflag,
+                      int* __restrict__ vrow, float* __restrict__ vlset, int* __restrict__ status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + warp;
   if (b >= B) return;
   if (lane == 0) vflag[b] = 0;  // no residual pass unless a rejection is found below
   const int ell = lengths[b], base = row_off[b];
   const int Rmax = B * (g + 1);
-  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > Rmax || base + ell > row_off[B] ||
-      anchor[b] < 0 || anchor[b] >= V) {
+  const int R = min(max(row_off[B], 0), Rmax);
+  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > R || anchor[b] < 0 || anchor[b] >= V) {
     if (lane == 0) raise_status(status, DSPARK_ERANGE);
     return;
   }
-  int n = ell - 1;
-  bool rejected = false;
-  float lset = 0.f;
-  for (int j = 0; j < ell - 1; ++j) {
-    const size_t q = (size_t)base + j;
+  const long long T = (long long)R * nblk;
+  // partials of row q: the CTAs whose unit ranges meet [q nblk, (q+1) nblk)
+  auto row_partials = [&](int q, MS* ms_out, KeyIdx* kb_out) {
+    const long long u0 = (long long)q * nblk, u1 = u0 + nblk - 1;
+    const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
     MS ms{-INFINITY, 0.f};
-    for (int i = lane; i < S; i += 32) {
-      const float4 p = part[q * S + i];
-      ms = ms_combine(ms, MS{p.x, p.y});
+    KeyIdx kb = key_none();
+    for (int c = c0; c <= c1; ++c) {
+      const long long clo = unit_lo(c, T, Gs);
+      if (clo >= unit_lo(c + 1, T, Gs)) continue;  // an empty range wrote nothing
+      const int first = (int)(clo / nblk);
+      if (q - first >= SL) continue;
+      const float4 d = part[(size_t)c * SL + (q - first)];
+      ms = ms_combine(ms, MS{d.x, d.y});
+      kb = better(kb, KeyIdx{d.z, __float_as_int(d.w)});
     }
-    ms = warp_ms(ms);
-    const float Lt = ms_log(ms);
-    if (!isfinite(Lt)) {
-      if (lane == 0) raise_status(status, DSPARK_ENUMERIC);
-      return;
-    }
-    const int x = tokens[(size_t)b * g + j];
-    if (x < 0 || x >= V) {
-      if (lane == 0) raise_status(status, DSPARK_ERANGE);
-      return;
-    }
-    const float pt = expf(P[q * V + x] - Lt);
-    const float u = u01(rng.word(kAccept, b, j, 0));
-    if (!(u * pd_tok[(size_t)b * g + j] < pt)) {
-      n = j;
-      rejected = true;
-      lset = Lt;
-      break;
+    *ms_out = ms;
+    *kb_out = kb;
+  };
+  // ---- accept tests of rows 0 .. ell-2, one per lane
+  bool acc = true, bad = false;
+  float Lt = 0.f;
+  if (lane < ell - 1) {
+    const int q = base + lane;
+    MS ms;
+    KeyIdx unused;
+    row_partials(q, &ms, &unused);
+    Lt = ms_log(ms);
+    const int x = tokens[(size_t)b * g + lane];
+    if (!isfinite(Lt) || x < 0 || x >= V) {
+      bad = true;
+    } else {
+      const float pt = expf(P[(size_t)q * V + x] - Lt);
+      const float u = u01(rng.word(kAccept, b, lane, 0));
+      acc = u * pd_tok[(size_t)b * g + lane] < pt;
     }
   }
-  if (rejected) {
+  const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
+  if (badm) {
+    if (lane == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  const unsigned rej = __ballot_sync(0xFFFFFFFFu, !acc);
+  if (rej) {
+    const int n = __ffs(rej) - 1;
+    const float lset = __shfl_sync(0xFFFFFFFFu, Lt, n);
     if (lane == 0) {
       n_acc[b] = n;
       vflag[b] = 1;
@@ -235,14 +360,14 @@ __global__ void __launch_bounds__(128)
     }
     return;
   }
-  // bonus token from row ell - 1: the block draw was made by the sweep
+  // ---- every verified draft accepted: bonus token from row ell - 1
+  const int n = ell - 1;
   const size_t q = (size_t)base + n;
+  MS unused;
   KeyIdx kb = key_none();
-  for (int i = lane; i < S; i += 32) {
-    const float4 p = part[q * S + i];
-    kb = better(kb, KeyIdx{p.z, __float_as_int(p.w)});
-  }
-  kb = warp_best(kb);
+  if (lane == 0) row_partials((int)q, &unused, &kb);
+  kb.key = __shfl_sync(0xFFFFFFFFu, kb.key, 0);
+  kb.idx = __shfl_sync(0xFFFFFFFFu, kb.idx, 0);
   if (kb.idx == kNoIdx) {
     if (lane == 0) raise_status(status, DSPARK_ENUMERIC);
     return;
@@ -254,7 +379,6 @@ __global__ void __launch_bounds__(128)
   if (lane == 0) {
     n_acc[b] = n;
     next_anchor[b] = kt.idx;
-    vflag[b] = 0;
   }
 }
 
@@ -334,13 +458,14 @@ __global__ void __launch_bounds__(256)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
   const int n = n_acc[b];
   const float* Prow = P + (size_t)vrow[b] * V;
-  if (tid == 0) {
+  if (warp == 0) {
     KeyIdx k2 = key_none();
-    for (int i = 0; i < nchunk; ++i) {
+    for (int i = lane; i < nchunk; i += 32) {
       const float2 p = rpart[(size_t)b * nchunk + i];
       k2 = better(k2, KeyIdx{p.x, __float_as_int(p.y)});
     }
-    s_blk = k2.idx;
+    k2 = warp_best(k2);
+    if (lane == 0) s_blk = k2.idx;
   }
   __syncthreads();
   const int sb = s_blk;
@@ -384,8 +509,10 @@ __global__ void __launch_bounds__(256)
     const int v = sb * kBlockW + vl;
     if (q < 4) {
       float acc = 0.f;
-      if (v < V)
+      if (v < V) {
+#pragma unroll 8
         for (int i = q; i < r; i += 4) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
+      }
       zpart[q][vl] = acc;
     }
   }
@@ -415,16 +542,16 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
   const Rng rng = Rng::make(a.seed, a.round);
-  const int grid = geo.num_sms * 8;
-  if ((d.V & 3) == 0)
-    k_verify_sweep4<<<grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.S, geo.chunk,
-                                                    d.B * (d.gamma + 1), rng, ws->s.vpart);
+  if (geo.sweep_bulk)
+    k_verify_sweep_bulk<<<geo.sweep_grid, kBulkThreads, sweep_bulk_smem_bytes(), st>>>(
+        a.P, a.row_off, a.lengths, d.B, geo.nblk, d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status);
   else
-    k_verify_sweep<<<grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.S, geo.chunk,
-                                                   d.B * (d.gamma + 1), rng, ws->s.vpart);
-  k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma,
-                                                   d.V, geo.S, rng, ws->s.vpart, a.n_acc, a.next_anchor,
-                                                   ws->s.vflag, ws->s.vrow, ws->s.vlset, ws->s.status);
+    k_verify_sweep<<<geo.sweep_grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.nblk,
+                                                            d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart);
+  k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B,
+                                                   d.gamma, d.V, geo.nblk, geo.SL, geo.sweep_grid, rng,
+                                                   ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
+                                                   ws->s.vlset, ws->s.status);
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
   if (BF16 && ws->use_tc && geo.resid_tc_ok) {
@@ -449,4 +576,11 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
   return verify_impl<0>(ws, a, st, launches);
 }
 
+}  // namespace dspark
+
+namespace dspark {
+cudaError_t sweep_bulk_configure() {
+  return cudaFuncSetAttribute(k_verify_sweep_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sweep_bulk_smem_bytes());
+}
 }  // namespace dspark

@@ -32,6 +32,8 @@ MID = {
     "mid_lagged": Workload("mid_lagged", B=40, gamma=4, V=1536, r=64, H=32, wdtype="bf16", mode="lagged",
                            seed=14, u_std=2.0, w_std=0.05, sps_knee=32.0, noise="per_request",
                            noise_args=(0.1, 0.5, 1.0), lag=2, rounds=5),
+    "mid_oddV": Workload("mid_oddV", B=6, gamma=3, V=1001, r=16, H=24, wdtype="f32", mode="compact",
+                         seed=15, u_std=2.0, w_std=0.1, sps_knee=8.0),
     "small": WORKLOADS["small"],
 }
 
