@@ -297,8 +297,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
         }
       };
-      prefetch_tile(0);
-      prefetch_tile(1);
+      // the rejected rows' slices of this CTA are small (ncols x 2 x 512 B per
+      // tile): pull all of them into L2 up front when they fit in 512 KB,
+      // else run two tiles ahead
+      const bool all_ahead = ncols * 8 * nt <= 4096;
+      if (all_ahead) {
+        for (int ti = 0; ti < nt; ++ti) prefetch_tile(ti);
+      } else {
+        prefetch_tile(0);
+        prefetch_tile(1);
+      }
       for (int i = 0; i < nt; ++i) {
         const int it = gq * nt + i, t = tile_lo + i, ab = it & 1;
         bool live = !aborted();
@@ -314,24 +322,29 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
         }
         const int v = t * kRM + q * 32 + lane;
-        if (live) prefetch_tile(i + 2);
+        if (live && !all_ahead) prefetch_tile(i + 2);
         if (live) {
           tc::tc_fence_after();
           for (int cc = half; cc * 32 < ncols; cc += 2) {
             float a[32];
             tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + cc * 32), a);
             tc::tmem_wait_ld();
+            // all 64 loads first (clamped addresses, no branches between a load
+            // and the next one), then the arithmetic
+            float uu[32], pp[32];
+            const int vv = min(v, p.V - 1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = min(cc * 32 + j, ncols - 1);
+              uu[j] = __ldcs(p.U + ((size_t)col_b[col] * p.g + col_n[col]) * p.V + vv);
+              pp[j] = __ldcs(p.P + (size_t)col_row[col] * p.V + vv);
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int col = cc * 32 + j;
-              float w = 0.f;
-              if (col < ncols && v < p.V) {
-                const int b = col_b[col];
-                const float u = __ldcs(p.U + ((size_t)b * p.g + col_n[col]) * p.V + v);
-                const float pv = __ldcs(p.P + (size_t)col_row[col] * p.V + v);
-                w = fmaxf(0.f, __expf(pv - col_lset[col]) - __expf(a[j] + u - col_lsed[col]));
-              }
-              a[j] = w;
+              const int cl = min(col, ncols - 1);
+              const float w = fmaxf(0.f, __expf(pp[j] - col_lset[cl]) - __expf(a[j] + uu[j] - col_lsed[cl]));
+              a[j] = (col < ncols && v < p.V) ? w : 0.f;
             }
             const float s = transpose_sum32(a);  // this warp's 32 entries, request cc*32 + lane
             part[q * kRN + cc * 32 + lane] = s;
