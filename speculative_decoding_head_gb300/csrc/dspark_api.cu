@@ -101,15 +101,14 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   cudaGetLastError();
   geo.rchunks = geo.num_sms > kResidChunks ? geo.num_sms : kResidChunks;
   const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * geo.rchunks);
-  const size_t o_xbuf = carve(sizeof(int32_t) * d.B);
-  size_t o_dpart = 0, o_drec = 0, o_aimg = 0;
+  size_t o_dpart = 0, o_dwin = 0, o_dxw = 0, o_aimg = 0;
   if (geo.tc_ok) {
     if (draft_tc_configure(ws) != cudaSuccess) geo.tc_ok = 0;
   }
   if (geo.tc_ok) {
-    const size_t nrows = draft_tc_scratch_rows(d, geo.tc_grid);
-    o_dpart = carve(sizeof(float4) * nrows);
-    o_drec = carve(sizeof(float) * kBlockW * nrows);
+    o_dpart = carve(sizeof(float2) * draft_tc_partials(d, geo.tc_grid));
+    o_dwin = carve(sizeof(unsigned long long) * draft_tc_winners(d));
+    o_dxw = carve(sizeof(unsigned long long) * draft_tc_winners(d));
     o_aimg = carve((size_t)geo.tc_groups * 128 * d.r * 2);
   }
   if (plan_configure() != cudaSuccess) {
@@ -136,9 +135,9 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vrow = reinterpret_cast<int*>(base + o_vrow);
   s.vlset = reinterpret_cast<float*>(base + o_vlset);
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
-  s.xbuf = reinterpret_cast<int32_t*>(base + o_xbuf);
-  s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
-  s.drec = geo.tc_ok ? reinterpret_cast<float*>(base + o_drec) : nullptr;
+  s.dpart = geo.tc_ok ? reinterpret_cast<float2*>(base + o_dpart) : nullptr;
+  s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
+  s.dxw = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dxw) : nullptr;
   s.aimg = geo.tc_ok ? static_cast<void*>(base + o_aimg) : nullptr;
   ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
@@ -163,6 +162,10 @@ dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream) {
   cudaError_t e = cudaMemsetAsync(ws->s.status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.plan_round, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 4 * sizeof(unsigned), st);
+  if (e == cudaSuccess && ws->s.dwin)
+    e = cudaMemsetAsync(ws->s.dwin, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
+  if (e == cudaSuccess && ws->s.dxw)
+    e = cudaMemsetAsync(ws->s.dxw, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
   return cuda_fail(e);
 }
 
@@ -205,9 +208,13 @@ dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int launches = 0;
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
-  cudaError_t e = launch_conf_hidden(ws, h, w, st, &launches);
-  if (e == cudaSuccess)
-    e = (ws->use_tc && ws->geo.tc_ok) ? launch_draft_tc(ws, a, st, &launches) : launch_draft_simt(ws, a, st, &launches);
+  cudaError_t e;
+  if (ws->use_tc && ws->geo.tc_ok) {
+    e = launch_draft_tc(ws, a, st, &launches);  // its prologue computes the hidden half of c_k
+  } else {
+    e = launch_conf_hidden(ws, h, w, st, &launches);
+    if (e == cudaSuccess) e = launch_draft_simt(ws, a, st, &launches);
+  }
   ws->last_launches = launches;
   return cuda_fail(e);
 }

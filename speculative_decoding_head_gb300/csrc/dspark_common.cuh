@@ -133,6 +133,34 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
+// sum_{i<H} w[i] hr[i] by a CTA of 128 threads (all of a thread's float4
+// loads in flight together); the result is valid in thread 0. `red` is a
+// 4-float shared array of the caller.
+__device__ __forceinline__ float hidden_dot128(const float* __restrict__ hr, const float* __restrict__ w, int H,
+                                               float* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc = 0.f;
+  if ((H & 3) == 0) {
+    const float4* h4 = reinterpret_cast<const float4*>(hr);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < H / 4; i += 128) {
+      const float4 a = __ldcs(h4 + i);  // streamed once
+      const float4 c = __ldg(w4 + i);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+      acc = fmaf(a.z, c.z, acc);
+      acc = fmaf(a.w, c.w, acc);
+    }
+  } else {
+    for (int i = threadIdx.x; i < H; i += 128) acc = fmaf(hr[i], w[i], acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
 // First error wins; kernels poll it to stop early.
 __device__ __forceinline__ void raise_status(int* st, int code) { atomicCAS(st, 0, code); }
 

@@ -56,11 +56,13 @@ struct Scratch {
   float* vlset;           // [B] target log-sum-exp of that row
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
-  float4* dpart;          // [grid*rowsTotal] per-CTA (max, sum, key, block)
-  float* drec;            // [grid*rowsTotal*64] per-CTA z values of its best block
+  float2* dpart;          // [gamma][groups*128][2*ceil(grid/groups)] per-CTA, per-epilogue-set
+                          // (max, sum exp) of a row's blocks
+  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, block) winners
+  unsigned long long* dxw;   // [2][gamma][groups*128] released (z, token + 1) of each draw
+                             // (the two halves of dwin and dxw alternate between launches)
   void* aimg;             // [groups][128 x r] bf16: next A operand in its swizzled shared layout
-  unsigned* barrier;      // [4] grid-barrier words
-  int32_t* xbuf;          // [B] current x_{k-1}
+  unsigned* barrier;      // [4] grid-barrier words: arrivals, generation, draft launch count
 };
 
 struct Geometry {
@@ -105,7 +107,8 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 // Whether the tcgen05 draft kernel supports these dims, and its launch shape.
 int draft_tc_supported(const dspark_dims& d);
 cudaError_t draft_tc_configure(dspark_ws* ws);
-size_t draft_tc_scratch_rows(const dspark_dims& d, int grid);
+size_t draft_tc_partials(const dspark_dims& d, int grid);  // float2 entries of Scratch::dpart
+size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch::dwin and of dxw
 
 int resid_tc_supported(const dspark_dims& d);
 cudaError_t resid_tc_configure(dspark_ws* ws);

@@ -24,33 +24,12 @@ constexpr int kSimtThreads = 256;
 // does not depend on drafted tokens (one CTA of 128 threads per row of h, all
 // of a thread's float4 loads in flight together).
 __global__ void __launch_bounds__(128) k_conf_hidden(const float* __restrict__ h,
-                                                     const float* __restrict__ w, int H, int rows,
+                                                     const float* __restrict__ w, int H,
                                                      float* __restrict__ s_h) {
   __shared__ float red[4];
   const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float* hr = h + (size_t)row * H;
-  float acc = 0.f;
-  if ((H & 3) == 0) {
-    const float4* h4 = reinterpret_cast<const float4*>(hr);
-    const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < H / 4; i += 128) {
-      const float4 a = __ldcs(h4 + i);  // streamed once
-      const float4 c = __ldg(w4 + i);
-      acc = fmaf(a.x, c.x, acc);
-      acc = fmaf(a.y, c.y, acc);
-      acc = fmaf(a.z, c.z, acc);
-      acc = fmaf(a.w, c.w, acc);
-    }
-  } else {
-    for (int i = threadIdx.x; i < H; i += 128) acc = fmaf(hr[i], w[i], acc);
-  }
-  acc = warp_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) s_h[row] = (red[0] + red[1]) + (red[2] + red[3]);
-  (void)rows;
+  const float d = hidden_dot128(h + (size_t)row * H, w, H, red);
+  if (threadIdx.x == 0) s_h[row] = d;
 }
 
 __device__ __forceinline__ int prev_token(const int32_t* anchor, const int32_t* tokens, int b, int g,
@@ -203,7 +182,7 @@ cudaError_t launch_conf_hidden(const dspark_ws* ws, const float* h, const float*
                                int* launches) {
   const int rows = ws->d.B * ws->d.gamma;
   if (ws->d.H == 0) return cudaMemsetAsync(ws->s.s_h, 0, sizeof(float) * rows, st);
-  k_conf_hidden<<<rows, 128, 0, st>>>(h, w, ws->d.H, rows, ws->s.s_h);
+  k_conf_hidden<<<rows, 128, 0, st>>>(h, w, ws->d.H, ws->s.s_h);
   ++*launches;
   return cudaGetLastError();
 }

@@ -6,23 +6,38 @@
 // and eq. (7): c_k = sigma((w^T [h_k; W1[x_{k-1}]]) / T_k) (the temperature is
 // the STS sigmoid(raw / T) of the zdszero.github.io "spec_dspark" page).
 //
-// One cooperative launch runs all gamma steps. Each CTA (one per SM) owns a
-// contiguous range of 64-token vocabulary tiles of one 128-row group:
-//   warp 0      TMA producer: W2 tile [r x 64] bf16 (128-byte swizzle, L2
-//               evict_last: W2 is reused by every step) and U tile [128 x 64]
-//               fp32 (evict_first: streamed once), into rings of 2 and 3 stages;
-//   warp 1      allocates 128 TMEM columns and issues tcgen05.mma
-//               (M = 128 rows, N = 64, K = r in steps of 16) into one of two
-//               TMEM accumulators; A = gathered rows W1[x_{k-1}] in shared memory;
-//   warps 2-5   epilogue, one thread per row: z = TMEM + U, the block's
+// Two launches. k_draft_prologue computes the hidden half of every confidence
+// logit and writes the rows W1[anchor] as the first A operand image (the
+// swizzled shared-memory layout, so that a CTA loads it with one bulk copy).
+// k_draft_tc, one cooperative launch, runs all gamma steps. Each CTA (one per
+// SM) owns a contiguous range of 64-token vocabulary tiles of one 128-row group:
+//   warp 0      TMA producer of W2, in chunks of 32 K rows x up to 256 tokens
+//               (four 128-byte-swizzled boxes; L2 evict_last: W2 is reused by
+//               every step), into a ring of 4 stages;
+//   warp 10     TMA producer of U, one 64-token block [128 x 64] fp32 at a
+//               time (evict_first: streamed once), into a ring of 3 stages
+//               (two producers, so that neither stream waits behind the other);
+//   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma with
+//               M = 128 rows, N = 64 x (blocks of the tile, up to 4), K = r in
+//               steps of 16, into one of two 256-column accumulators; A = the
+//               rows W1[x_{k-1}] in shared memory. (A narrower N costs about as
+//               much per instruction, so the tile is as wide as TMEM allows.)
+//   warps 2-9   epilogue, two sets of four warps; set s takes the blocks of
+//               parity s, one thread per row: z = TMEM + U, the block's
 //               log-mass (max, sum exp), the block draw key log mass + G_s,
-//               the row's online log-sum-exp, and a copy of z for the row's
-//               best block so far (to global scratch).
-// Between steps the epilogue warps of all CTAs meet at a grid barrier, reduce
-// each row's per-CTA partials (one warp per row: log-sum-exp, winning block,
-// token draw argmax_v (z_v + G_v) inside it), meet again, and gather the next
-// A. The producer keeps prefetching the next step's tiles meanwhile (they do
-// not depend on the drafted token).
+//               the row's online log-sum-exp, and a register copy of z for the
+//               set's best block so far.
+// Step boundary. The block draw is a grid-wide argmax: each set publishes its
+// best (key, block) per row with a 64-bit atomic max, then all CTAs meet at
+// one grid barrier. The token draw inside the winning block needs only that
+// block's z, which the set that found it still holds in registers: that
+// warp draws the token (lanes split the 64 tokens), writes W1[x_k] into the
+// group's A image and releases a per-row flag carrying x_k. Every CTA polls
+// its group's flags and loads the image with one bulk copy. The producer
+// keeps prefetching the next step's tiles meanwhile (they do not depend on
+// the drafted token). Log-sum-exps, probabilities of the drawn tokens and
+// confidences are off that chain: per-set partials (max, sum exp) are kept
+// per step and combined after the last step, one warp per (row, step).
 //
 // Every wait is bounded (tc_ptx.cuh); a timeout sets DSPARK_ETIMEOUT, every
 // role leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
@@ -36,18 +51,25 @@
 
 namespace dspark {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 352;
+constexpr int kEpiThreads = 256;    // warps 2..9
+constexpr int kUWarp = 10;          // U producer
 constexpr int kTcRows = 128;        // MMA M: rows of one row group
-constexpr int kTcN = 64;            // vocabulary tile = one sampler block
-constexpr int kNW = 2;              // W2 ring depth
-constexpr int kNU = 3;              // U ring depth
-constexpr int kUStage = kTcRows * kTcN * 4;  // 32 KB: two 128 x 32 fp32 boxes
+constexpr int kBlk = 64;            // sampler block = one 64-column slice of the accumulator
+constexpr int kTileBlocks = 4;      // MMA N = 64 x blocks of the tile (<= 256)
+constexpr int kKc = 32;             // K rows of W2 per ring stage
+constexpr int kW2Box = kKc * 128;   // 4 KB: 32 K rows x 64 tokens (128-byte rows)
+constexpr int kW2Stage = kTileBlocks * kW2Box;  // 16 KB
+constexpr int kNW = 4;              // W2 ring depth (K chunks)
+constexpr int kNU = 3;              // U ring depth (blocks)
+constexpr int kUStage = kTcRows * kBlk * 4;  // 32 KB: two 128 x 32 fp32 boxes
 constexpr int kUBox = kTcRows * 32 * 4;      // 16 KB
-constexpr int kTmemCols = 128;      // two 64-column fp32 accumulators
+constexpr int kAccCols = kTileBlocks * kBlk; // 256 columns per accumulator
+constexpr int kTmemCols = 2 * kAccCols;      // two accumulators: all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
-constexpr int kMaxPartLanes = 8;    // partials per lane in the row reduction (grid <= 256)
+constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (two per CTA, <= 256 CTAs a group)
 
-static_assert(kTcN == kBlockW, "a vocabulary tile is one sampler block");
+static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
 
 struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
   uint32_t a, w2, u, bars, misc, total;
@@ -55,9 +77,11 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     TcSmem s;
     s.a = 0;
     s.w2 = s.a + kTcRows * r * 2;
-    s.u = s.w2 + kNW * r * 128;
+    s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 4 + 3);
+    // w2 full/empty, u full (one per stage and set), u empty, t full/empty,
+    // a_full, drain, a_img
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + kNU + 4 + 3);
     s.total = s.misc + 64;
     return s;
   }
@@ -65,7 +89,7 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
 
 struct TcParams {
   int B, g, V, r, H;
-  int ntiles, nG, G, Ggmax;
+  int nblk, nG, G, Ggmax, P, rowsG;
   Rng rng;
   const int32_t* anchor;
   const void* W1;
@@ -76,21 +100,39 @@ struct TcParams {
   float* pd_tok;
   float* lse;
   float* conf;
-  int32_t* xbuf;
-  float4* dpart;  // [nG * 128][Ggmax]
-  float* drec;    // [G][128][64]
-  __nv_bfloat16* aimg;  // [nG][128 x r] next A operand, already in its swizzled shared layout
-  unsigned* bar;  // [0] arrivals, [1] generation
+  float2* dpart;            // [g][rowsG][P]: (max, sum exp) per CTA and set
+  unsigned long long* win;  // [2][g][rowsG]: packed (block key, block), 0 = none
+  unsigned long long* xw;   // [2][g][rowsG]: (z of x_k) << 32 | (x_k + 1), 0 = not yet drawn
+  __nv_bfloat16* aimg;      // [nG][128 x r]: next A operand in its swizzled shared layout
+  unsigned* bar;            // [0] arrivals, [1] generation, [2] launches (parity of win, xw)
   int* status;
 };
 
 __device__ __forceinline__ int group_ctas(int G, int nG, int g) { return (G - g + nG - 1) / nG; }
 
-// Grid barrier among the epilogue warps (128 threads, named barrier 1) of all
+// (key, block) as one unsigned 64-bit word whose unsigned order is: larger
+// key first, then the smaller block. Never 0.
+__device__ __forceinline__ unsigned long long pack_win(float key, int s) {
+  uint32_t u = __float_as_uint(key);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)s);
+}
+__device__ __forceinline__ int win_block(unsigned long long w) {
+  return w ? (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull)) : -1;
+}
+
+// Offset (in bf16 elements) of the 16-byte piece ch of K-block kb of row m in
+// the A operand: K-major, 128-byte swizzle, 8-row atoms of 1 KB, K-blocks of
+// 64 elements 16 KB apart.
+__device__ __forceinline__ size_t a_piece(int m, int kb, int ch) {
+  return (size_t)kb * (kTcRows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
+}
+
+// Grid barrier among the epilogue warps (256 threads, named barrier 1) of all
 // CTAs. Self-resetting: the last arriver zeroes the count and bumps the
 // generation. Returns false if the round is being abandoned.
 __device__ bool grid_sync(const TcParams& p, bool leader, volatile int* abort) {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
   if (leader && !*abort) {
     const unsigned g0 = tc::ld_acquire_gpu(p.bar + 1);
     __threadfence();
@@ -116,8 +158,56 @@ __device__ bool grid_sync(const TcParams& p, bool leader, volatile int* abort) {
     }
     __threadfence();
   }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
   return !*abort;
+}
+
+// Bounded wait for a released x_k flag (0 = not yet written). Returns 0 on
+// timeout or when another part of the launch raised an error.
+__device__ unsigned long long wait_flag(const unsigned long long* f, int* status) {
+  unsigned long long v = tc::ld_acquire_gpu(f);
+  if (v) return v;
+  const unsigned long long t0 = tc::globaltimer();
+  while ((v = tc::ld_acquire_gpu(f)) == 0ull) {
+    if (*(volatile int*)status != 0) return 0ull;
+    if (tc::globaltimer() - t0 > tc::kWaitNs) {
+      raise_status(status, DSPARK_ETIMEOUT);
+      return 0ull;
+    }
+    __nanosleep(32);
+  }
+  return v;
+}
+
+// The hidden half of every confidence logit, s_h[row] = w_h . h[row] (one CTA
+// per row of h), and the first A operand: the rows W1[anchor[b]] written into
+// each group's image by the CTAs of step 1 (row = b * gamma).
+__global__ void __launch_bounds__(128) k_draft_prologue(const float* __restrict__ h, const float* __restrict__ w,
+                                                        int H, float* __restrict__ s_h,
+                                                        const __nv_bfloat16* __restrict__ W1,
+                                                        const int32_t* __restrict__ anchor,
+                                                        __nv_bfloat16* __restrict__ aimg, int g, int V, int r,
+                                                        int* status) {
+  __shared__ float red[4];
+  const int row = blockIdx.x;
+  if (H > 0) {
+    const float d = hidden_dot128(h + (size_t)row * H, w, H, red);
+    if (threadIdx.x == 0) s_h[row] = d;
+  } else if (threadIdx.x == 0) {
+    s_h[row] = 0.f;
+  }
+  if (row % g == 0 && threadIdx.x < r / 8) {
+    const int b = row / g;
+    int x = anchor[b];
+    if (x < 0 || x >= V) {
+      if (threadIdx.x == 0) raise_status(status, DSPARK_ERANGE);
+      x = 0;
+    }
+    const int ci = threadIdx.x;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * r) + ci);
+    *reinterpret_cast<uint4*>(aimg + (size_t)(b / kTcRows) * kTcRows * r + a_piece(b % kTcRows, ci >> 3, ci & 7)) = v;
+    tc::fence_proxy_async_global();  // read by the draft kernel's bulk copies
+  }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -131,15 +221,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sA = sbase + L.a, sW2 = sbase + L.w2, sU = sbase + L.u;
   const uint32_t bars = sbase + L.bars;
+  // u_full has one barrier per (stage, set): the two sets consume alternate
+  // blocks, so a barrier shared by both could be waited on one phase early
   auto w2_full = [&](int i) { return bars + 8u * i; };
   auto w2_empty = [&](int i) { return bars + 8u * (kNW + i); };
-  auto u_full = [&](int i) { return bars + 8u * (2 * kNW + i); };
-  auto u_empty = [&](int i) { return bars + 8u * (2 * kNW + kNU + i); };
-  auto t_full = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + i); };
-  auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + 2 + i); };
-  const uint32_t a_full = bars + 8u * (2 * kNW + 2 * kNU + 4);
+  auto u_full = [&](int gb) { return bars + 8u * (2 * kNW + gb % (2 * kNU)); };
+  auto u_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + i); };
+  auto t_full = [&](int i) { return bars + 8u * (2 * kNW + 3 * kNU + i); };
+  auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 3 * kNU + 2 + i); };
+  const uint32_t a_full = bars + 8u * (2 * kNW + 3 * kNU + 4);
   const uint32_t drain = a_full + 8u;
-  const uint32_t a_img = a_full + 16u;  // the bulk copy of the next A image
+  const uint32_t a_img = a_full + 16u;  // the bulk copy of the A image
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
 
@@ -147,25 +239,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int c = blockIdx.x;
   const int grp = c % p.nG, cg = c / p.nG;  // row group, index within the group
   const int Gg = group_ctas(p.G, p.nG, grp);
-  const int tile_lo = (int)((long long)cg * p.ntiles / Gg);
-  const int tile_hi = (int)((long long)(cg + 1) * p.ntiles / Gg);
-  const int nt = tile_hi - tile_lo;
-  const uint32_t w2_bytes = (uint32_t)p.r * 128u;
+  // this CTA's sampler blocks [blo, blo + nbc), in MMA tiles of up to four
+  const int blo = (int)((long long)cg * p.nblk / Gg);
+  const int nbc = (int)((long long)(cg + 1) * p.nblk / Gg) - blo;
+  const int ntl = (nbc + kTileBlocks - 1) / kTileBlocks;
+  const int nkc = p.r / kKc;  // W2 chunks per tile
+  auto tile_blocks = [&](int tj) { return min(kTileBlocks, nbc - tj * kTileBlocks); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNW; ++i) {
       tc::mbar_init(w2_full(i), 1);
       tc::mbar_init(w2_empty(i), 1);
     }
-    for (int i = 0; i < kNU; ++i) {
-      tc::mbar_init(u_full(i), 1);
-      tc::mbar_init(u_empty(i), 4);
-    }
+    for (int i = 0; i < 2 * kNU; ++i) tc::mbar_init(u_full(i), 1);
+    for (int i = 0; i < kNU; ++i) tc::mbar_init(u_empty(i), 4);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(t_full(i), 1);
-      tc::mbar_init(t_empty(i), 4);
+      tc::mbar_init(t_empty(i), kEpiThreads / 32);
     }
-    tc::mbar_init(a_full, 4);
+    tc::mbar_init(a_full, kEpiThreads / 32);
     tc::mbar_init(drain, 1);
     tc::mbar_init(a_img, 1);
     *abort = 0;
@@ -183,68 +275,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ W2 producer
     if (lane == 0) {
-      const uint64_t keep = tc::policy_evict_last(), stream = tc::policy_evict_first();
-      int issued = 0;
+      const uint64_t keep = tc::policy_evict_last();
+      int wiss = 0;  // chunks issued
       bool ok = true;
       for (int k = 1; k <= p.g && ok; ++k) {
-        for (int i = 0; i < nt && ok; ++i) {
-          const int it = (k - 1) * nt + i, t = tile_lo + i;
-          const int ws = it % kNW, us = it % kNU;
-          ok = tc::mbar_wait(w2_empty(ws), ((it / kNW) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
-          tc::tma_load_2d(sW2 + ws * w2_bytes, &tm_w2, t * kTcN, 0, w2_full(ws), keep);
-          ok = tc::mbar_wait(u_empty(us), ((it / kNU) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(u_full(us), kUStage);
-          tc::tma_load_3d(sU + us * kUStage, &tm_u, t * kTcN, k - 1, grp * kTcRows, u_full(us), stream);
-          tc::tma_load_3d(sU + us * kUStage + kUBox, &tm_u, t * kTcN + 32, k - 1, grp * kTcRows, u_full(us),
-                          stream);
-          issued = it + 1;
+        for (int tj = 0; tj < ntl && ok; ++tj) {
+          const int it = (k - 1) * ntl + tj, nbt = tile_blocks(tj);
+          const int v0 = (blo + tj * kTileBlocks) * kBlk;
+          for (int ch = 0; ch < nkc && ok; ++ch) {
+            const int wc = it * nkc + ch, ws = wc % kNW;
+            ok = tc::mbar_wait(w2_empty(ws), ((wc / kNW) & 1) ^ 1, abort);
+            if (!ok) break;
+            tc::mbar_arrive_expect_tx(w2_full(ws), (uint32_t)(nbt * kW2Box));
+            for (int j = 0; j < nbt; ++j)
+              tc::tma_load_2d(sW2 + ws * kW2Stage + j * kW2Box, &tm_w2, v0 + j * kBlk, ch * kKc, w2_full(ws), keep);
+            wiss = wc + 1;
+          }
         }
       }
       if (!ok) {
         if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
         *abort = 1;
-        // let the copies already issued land before the CTA can exit
-        for (int it = issued - 1; it >= 0 && it >= issued - kNU; --it) {
-          volatile int never = 0;
-          tc::mbar_wait(u_full(it % kNU), (it / kNU) & 1, &never);
-          if (it >= issued - kNW) tc::mbar_wait(w2_full(it % kNW), (it / kNW) & 1, &never);
+        volatile int never = 0;  // let the copies already issued land before the CTA can exit
+        for (int wc = wiss - 1; wc >= 0 && wc >= wiss - kNW; --wc)
+          tc::mbar_wait(w2_full(wc % kNW), (wc / kNW) & 1, &never);
+      }
+    }
+  } else if (warp == kUWarp) {
+    // ------------------------------------------------------------ U producer
+    if (lane == 0) {
+      const uint64_t stream = tc::policy_evict_first();
+      int uiss = 0;  // blocks issued
+      bool ok = true;
+      for (int k = 1; k <= p.g && ok; ++k) {
+        for (int i = 0; i < nbc && ok; ++i) {
+          const int gb = (k - 1) * nbc + i, us = gb % kNU, v = (blo + i) * kBlk;
+          ok = tc::mbar_wait(u_empty(us), ((gb / kNU) & 1) ^ 1, abort);
+          if (!ok) break;
+          tc::mbar_arrive_expect_tx(u_full(gb), kUStage);
+          tc::tma_load_3d(sU + us * kUStage, &tm_u, v, k - 1, grp * kTcRows, u_full(gb), stream);
+          tc::tma_load_3d(sU + us * kUStage + kUBox, &tm_u, v + 32, k - 1, grp * kTcRows, u_full(gb), stream);
+          uiss = gb + 1;
         }
+      }
+      if (!ok) {
+        if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
+        *abort = 1;
+        volatile int never = 0;
+        for (int gb = uiss - 1; gb >= 0 && gb >= uiss - kNU; --gb)
+          tc::mbar_wait(u_full(gb), (gb / (2 * kNU)) & 1, &never);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16_f32(kTcRows, kTcN, true);
       bool ok = true;
       for (int k = 1; k <= p.g && ok; ++k) {
         ok = tc::mbar_wait(a_full, (k - 1) & 1, abort);
         if (!ok) break;
         tc::tc_fence_after();
-        for (int i = 0; i < nt && ok; ++i) {
-          const int it = (k - 1) * nt + i;
-          const int ws = it % kNW, ab = it & 1;
-          ok = tc::mbar_wait(w2_full(ws), (it / kNW) & 1, abort) &&
-               tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc::tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)(ab * kTcN);
-          const uint32_t bstage = sW2 + ws * w2_bytes;
-          for (int ks = 0; ks < p.r / 16; ++ks) {
-            // A: K-major, 128-byte swizzle; K-block of 64 is [128 rows x 128 B],
-            // the 16-wide K step moves 32 B inside the swizzled row.
-            const uint64_t ad = tc::smem_desc(sA + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
-            // B: N-major (W2 rows are contiguous in N), 128-byte swizzle; each
-            // K row is 128 B, 8 rows form a 1 KB atom, 16 rows per K step.
-            const uint64_t bd = tc::smem_desc(bstage + ks * 2048, w2_bytes, 1024);
-            tc::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+        for (int tj = 0; tj < ntl && ok; ++tj) {
+          const int it = (k - 1) * ntl + tj, ab = it & 1, nbt = tile_blocks(tj);
+          const uint32_t idesc = tc::idesc_bf16_f32(kTcRows, nbt * kBlk, true);
+          const uint32_t d = tmem + (uint32_t)(ab * kAccCols);
+          ok = tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
+          for (int ch = 0; ch < nkc && ok; ++ch) {
+            const int wc = it * nkc + ch, ws = wc % kNW;
+            ok = tc::mbar_wait(w2_full(ws), (wc / kNW) & 1, abort);
+            if (!ok) break;
+            tc::tc_fence_after();
+            for (int kk = 0; kk < kKc / 16; ++kk) {
+              // A: K-major, 128-byte swizzle; K-block ks / 4 is [128 rows x
+              // 128 B], the 16-wide K step moves 32 B inside the swizzled row.
+              const int ks = ch * (kKc / 16) + kk;
+              const uint64_t ad = tc::smem_desc(sA + (ks >> 2) * (kTcRows * 128) + (ks & 3) * 32, 16, 1024);
+              // B: N-major (W2 rows are contiguous in N), 128-byte swizzle;
+              // 8 K rows of 128 B form a 1 KB atom, 16 K rows per step, the
+              // 64-token boxes of the chunk are 4 KB apart.
+              const uint64_t bd = tc::smem_desc(sW2 + ws * kW2Stage + kk * 2048, kW2Box, 1024);
+              tc::mma_bf16(d, ad, bd, idesc, (ch | kk) ? 1u : 0u);
+            }
+            tc::mma_commit(w2_empty(ws));
           }
-          tc::mma_commit(w2_empty(ws));
-          tc::mma_commit(t_full(ab));
+          if (ok) tc::mma_commit(t_full(ab));
         }
       }
       if (!ok) {
@@ -258,105 +373,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Every epilogue warp runs all gamma steps and both grid barriers of each
-    // step even after an abort (the named barrier inside grid_sync has no
-    // timeout, so no warp may skip one); an abort only skips the work.
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Every epilogue warp runs all gamma steps and every grid barrier even
+    // after an abort (the named barrier inside grid_sync has no timeout, so no
+    // warp may skip one); an abort only skips the work.
+    const int ew = warp - 2;     // 0..7
+    const int set = ew >> 2;     // TMEM accumulator and tile parity of this warp
+    const int q = warp & 3;      // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
     const int b = grp * kTcRows + m;
     const bool valid = b < p.B;
     const bool leader = warp == 2 && lane == 0;
-    const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
     const __nv_bfloat16* W1 = reinterpret_cast<const __nv_bfloat16*>(p.W1);
+    __nv_bfloat16* img = p.aimg + (size_t)grp * kTcRows * p.r;
     // warp-uniform view of the abort word (the loops below hold warp collectives)
     auto aborted = [&]() { return __any_sync(0xFFFFFFFFu, *abort != 0); };
-    float* rec = p.drec + ((size_t)c * kTcRows + m) * kTcN;
+    // this launch's half of the winner and flag slots; the other half, last
+    // used by the previous launch, is cleared for the next one
+    const int par = (int)(__ldcg(p.bar + 2) & 1u);
+    const size_t half = (size_t)p.g * p.rowsG;
+    unsigned long long* win = p.win + par * half;
+    unsigned long long* xw = p.xw + par * half;
+    {
+      const int et = threadIdx.x - 64;
+      for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads) {
+        p.win[(par ^ 1) * half + i] = 0ull;
+        p.xw[(par ^ 1) * half + i] = 0ull;
+      }
+    }
     for (int k = 1; k <= p.g; ++k) {
-      // ---- gather A = W1[x_{k-1}] rows (K-major, 128-byte swizzle) and c_k
-      if (!aborted() && k > 1) {
-        // the reducers of the last step wrote this group's A (rows W1[x_{k-1}]
-        // in the swizzled layout) as one contiguous image: one bulk copy
+      // ---- A = W1[x_{k-1}]: the group's image, complete once every row's
+      // flag of step k-1 was seen (step 1: written by the prologue kernel)
+      if (!aborted()) {
         if (leader) {
           tc::fence_proxy_async_global();
           const uint32_t bytes = (uint32_t)kTcRows * p.r * 2u;
           tc::mbar_arrive_expect_tx(a_img, bytes);
-          tc::bulk_load(sA, p.aimg + (size_t)grp * kTcRows * p.r, bytes, a_img);
+          tc::bulk_load(sA, img, bytes, a_img);
         }
-        bool ok = tc::mbar_wait(a_img, (k - 2) & 1, abort);
+        bool ok = tc::mbar_wait(a_img, (k - 1) & 1, abort);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) {
           if (lane == 0 && !*abort) {
             raise_status(p.status, DSPARK_ETIMEOUT);
             *abort = 1;
           }
-        } else {
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(a_full);
+        } else if (lane == 0) {
+          tc::mbar_arrive(a_full);
         }
-      } else if (!aborted()) {
-        int x = 0;
-        if (valid) {
-          x = p.anchor[b];
-          if (x < 0 || x >= p.V) {
-            raise_status(p.status, DSPARK_ERANGE);
-            x = 0;
-          }
-        }
-        // every 16-byte piece of the row in flight at once (cp.async), written
-        // straight into its 128-byte-swizzled position
-        const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r);
-        for (int kb = 0; kb < p.r / 64; ++kb) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint32_t dst = sA + kb * (kTcRows * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
-                                 ((uint32_t)(ch ^ (m & 7)) << 4);
-            if (valid) {
-              tc::cp_async16(dst, src + kb * 8 + ch);
-            } else {
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
-            }
-          }
-        }
-        tc::cp_async_wait_all();
-        float cdot = 0.f;
-        if (cg == 0 && valid) {
-          for (int kb = 0; kb < p.r / 64; ++kb) {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-              uint4 v;
-              const uint32_t a = sA + kb * (kTcRows * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
-                                 ((uint32_t)(ch ^ (m & 7)) << 4);
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-              const float* wr = p.w + p.H + kb * 64 + ch * 8;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(h2[e]);
-                cdot = fmaf(f.x, wr[2 * e], cdot);
-                cdot = fmaf(f.y, wr[2 * e + 1], cdot);
-              }
-            }
-          }
-        }
-        if (cg == 0 && valid) {
-          const size_t o = (size_t)b * p.g + (k - 1);
-          const float raw = p.s_h[o] + cdot;
-          const float cf = 1.f / (1.f + expf(-raw / p.T[k - 1]));
-          if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
-          p.conf[o] = cf;
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(a_full);
       }
 
-      // ---- vocabulary tiles of this CTA
+      // ---- this CTA's tiles; set s takes the blocks whose running index has
+      // parity s (so the sets share each tile and the U ring evenly)
       float M = -INFINITY, S = 0.f, bk = -INFINITY;
       int bs = kNoIdx;
-      for (int i = 0; i < nt && !aborted(); ++i) {
-        const int it = (k - 1) * nt + i, t = tile_lo + i;
-        const int ab = it & 1, us = it % kNU;
-        bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort) && tc::mbar_wait(u_full(us), (it / kNU) & 1, abort);
+      float zb[kBlk];
+#pragma unroll
+      for (int j = 0; j < kBlk; ++j) zb[j] = 0.f;
+      for (int tj = 0; tj < ntl && !aborted(); ++tj) {
+        const int it = (k - 1) * ntl + tj, ab = it & 1, nbt = tile_blocks(tj);
+        const int gb0 = (k - 1) * nbc + tj * kTileBlocks;
+        const int j0 = (gb0 & 1) == set ? 0 : 1;   // first block of this set in the tile
+        const int jl = j0 + ((nbt - 1 - j0) & ~1);  // last one (>= nbt: none)
+        bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
         ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) {
           if (lane == 0 && !*abort) {
@@ -366,154 +444,252 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc::tc_fence_after();
-        float z[kTcN];
-        tc::tmem_ld32(trow + (uint32_t)(ab * kTcN), z);
-        tc::tmem_ld32(trow + (uint32_t)(ab * kTcN + 32), z + 32);
-        tc::tmem_wait_ld();
-        const uint32_t ub = sU + us * kUStage + m * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            float4 u;
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w)
-                         : "r"(ub + h * kUBox + ((uint32_t)(cc ^ (m & 7)) << 4)));
-            z[h * 32 + cc * 4 + 0] += u.x;
-            z[h * 32 + cc * 4 + 1] += u.y;
-            z[h * 32 + cc * 4 + 2] += u.z;
-            z[h * 32 + cc * 4 + 3] += u.w;
-          }
-        }
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(t_empty(ab));
-          tc::mbar_arrive(u_empty(us));
-        }
-        if (valid) {
-          const int v0 = t * kTcN;
-          if (v0 + kTcN > p.V) {
-#pragma unroll
-            for (int j = 0; j < kTcN; ++j)
-              if (v0 + j >= p.V) z[j] = -INFINITY;
-          }
-          float mb = z[0];
-#pragma unroll
-          for (int j = 1; j < kTcN; ++j) mb = fmaxf(mb, z[j]);
-          float sb = 0.f;
-#pragma unroll
-          for (int j = 0; j < kTcN; ++j) sb += __expf(z[j] - mb);
-          const float lm = mb + logf(sb);
-          if (mb > M) {
-            S = S * __expf(M - mb) + sb;
-            M = mb;
-          } else {
-            S += sb * __expf(mb - M);
-          }
-          const float key = lm + gumbel(p.rng.word(kDraftBlock, b, k, t));
-          if (key > bk) {  // ties keep the smaller block (processed first)
-            bk = key;
-            bs = t;
-            float4* r4 = reinterpret_cast<float4*>(rec);
-#pragma unroll
-            for (int j = 0; j < kTcN / 4; ++j) r4[j] = make_float4(z[4 * j], z[4 * j + 1], z[4 * j + 2], z[4 * j + 3]);
-          }
-        }
-      }
-      if (valid && !*abort) p.dpart[(size_t)b * p.Ggmax + cg] = make_float4(M, S, bk, __int_as_float(bs));
-      grid_sync(p, leader, abort);
-
-      // ---- per-row reduction and the token draw inside the winning block
-      const int ew = warp - 2;
-      for (int jr = ew; !aborted(); jr += 4) {
-        const int br = c + jr * p.G;
-        if (br >= p.B) break;
-        const int g2 = br / kTcRows, m2 = br % kTcRows;
-        const int Gg2 = group_ctas(p.G, p.nG, g2);
-        MS ms{-INFINITY, 0.f};
-        KeyIdx kb = key_none();
-        int owner = -1;
-        {
-          // every partial of the row in flight at once (written by other CTAs)
-          float4 dd[kMaxPartLanes];
-#pragma unroll
-          for (int u = 0; u < kMaxPartLanes; ++u) {
-            const int i = lane + 32 * u;
-            dd[u] = i < Gg2 ? __ldcg(p.dpart + (size_t)br * p.Ggmax + i) : make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
-          }
-#pragma unroll
-          for (int u = 0; u < kMaxPartLanes; ++u) {
-            const float4 d = dd[u];
-            ms = ms_combine(ms, MS{d.x, d.y});
-            const KeyIdx nb = better(kb, KeyIdx{d.z, __float_as_int(d.w)});
-            if (nb.idx != kb.idx || nb.key != kb.key) owner = lane + 32 * u;
-            kb = nb;
-          }
-        }
-        ms = warp_ms(ms);
-        const KeyIdx best = warp_best(kb);
-        const unsigned own_mask =
-            __ballot_sync(0xFFFFFFFFu, owner >= 0 && kb.idx == best.idx && kb.key == best.key);
-        const int own_cg = own_mask ? __shfl_sync(0xFFFFFFFFu, owner, __ffs(own_mask) - 1) : -1;
-        if (best.idx == kNoIdx || own_cg < 0) {
-          if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
+        if (j0 >= nbt) {  // no block of this set in the tile
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(t_empty(ab));
           continue;
         }
-        const int own_c = g2 + p.nG * own_cg;
-        const float* r2 = p.drec + ((size_t)own_c * kTcRows + m2) * kTcN;
-        const int v0 = best.idx * kTcN + lane, v1 = v0 + 32;
-        const float z0 = __ldcg(r2 + lane), z1 = __ldcg(r2 + lane + 32);
-        KeyIdx kt = key_none();
-        if (v0 < p.V) kt = KeyIdx{z0 + gumbel(p.rng.word(kDraftToken, br, k, v0)), v0};
-        if (v1 < p.V) kt = better(kt, KeyIdx{z1 + gumbel(p.rng.word(kDraftToken, br, k, v1)), v1});
-        kt = warp_best(kt);
-        if (kt.idx == kNoIdx) {
-          if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
-          continue;
-        }
-        const int jx = kt.idx - best.idx * kTcN;  // 0..63
-        const float zx = __shfl_sync(0xFFFFFFFFu, jx < 32 ? z0 : z1, jx & 31);
-        if (lane == 0) {
-          const float L2 = ms_log(ms);
-          const size_t o = (size_t)br * p.g + (k - 1);
-          p.tokens[o] = kt.idx;
-          p.pd_tok[o] = expf(zx - L2);
-          p.lse[o] = L2;
-          p.xbuf[br] = kt.idx;
-        }
-        if (k < p.g) {
-          // the next step's A row W1[x_k] into the group's image, and
-          // c_{k+1} = sigma((s_h + w_r . W1[x_k]) / T_{k+1}) while the row is at hand
-          const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)kt.idx * p.r);
-          __nv_bfloat16* img = p.aimg + (size_t)g2 * kTcRows * p.r;
-          float cd = 0.f;
-          for (int ci = lane; ci < p.r / 8; ci += 32) {
-            const int kb2 = ci >> 3, ch = ci & 7;
-            const uint4 v = __ldg(src + ci);
-            *reinterpret_cast<uint4*>(img + kb2 * (kTcRows * 64) + (m2 >> 3) * 512 + (m2 & 7) * 64 +
-                                      ((ch ^ (m2 & 7)) << 3)) = v;
-            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
-            const float* wr = p.w + p.H + ci * 8;
+        for (int j = j0; j < nbt; j += 2) {
+          const int gb = gb0 + j, us = gb % kNU, t = blo + tj * kTileBlocks + j;
+          ok = tc::mbar_wait(u_full(gb), (gb / (2 * kNU)) & 1, abort);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) {
+            if (lane == 0 && !*abort) {
+              raise_status(p.status, DSPARK_ETIMEOUT);
+              *abort = 1;
+            }
+            break;
+          }
+          float z[kBlk];
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kAccCols + j * kBlk);
+          tc::tmem_ld32(ta, z);
+          tc::tmem_ld32(ta + 32, z + 32);
+          tc::tmem_wait_ld();
+          if (j == jl) {  // the accumulator is free once the last slice of this set is read
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(t_empty(ab));
+          }
+          const uint32_t ub = sU + us * kUStage + m * 128;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = __bfloat1622float2(h2[e]);
-              cd = fmaf(f.x, wr[2 * e], cd);
-              cd = fmaf(f.y, wr[2 * e + 1], cd);
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              float4 u;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w)
+                           : "r"(ub + h * kUBox + ((uint32_t)(cc ^ (m & 7)) << 4)));
+              z[h * 32 + cc * 4 + 0] += u.x;
+              z[h * 32 + cc * 4 + 1] += u.y;
+              z[h * 32 + cc * 4 + 2] += u.z;
+              z[h * 32 + cc * 4 + 3] += u.w;
             }
           }
-          tc::fence_proxy_async_global();  // the image is read by bulk copies
-          cd = warp_sum(cd);
-          if (lane == 0) {
-            const size_t o2 = (size_t)br * p.g + k;
-            const float cf = 1.f / (1.f + expf(-(p.s_h[o2] + cd) / p.T[k]));
-            if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
-            p.conf[o2] = cf;
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(u_empty(us));
+          if (valid) {
+            const int v0 = t * kBlk;
+            if (v0 + kBlk > p.V) {
+#pragma unroll
+              for (int e = 0; e < kBlk; ++e)
+                if (v0 + e >= p.V) z[e] = -INFINITY;
+            }
+            // block max and sum of exponentials as 8-way trees (short chains)
+            float m8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(z[e], z[e + 8]);
+#pragma unroll
+            for (int i = 16; i < kBlk; i += 8)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], z[i + e]);
+            const float mb = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float s8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s8[e] = __expf(z[e] - mb);
+#pragma unroll
+            for (int i = 8; i < kBlk; i += 8)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) s8[e] += __expf(z[i + e] - mb);
+            const float sb = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+            const float lm = mb + logf(sb);
+            if (mb > M) {
+              S = S * __expf(M - mb) + sb;
+              M = mb;
+            } else {
+              S += sb * __expf(mb - M);
+            }
+            const float key = lm + gumbel(p.rng.word(kDraftBlock, b, k, t));
+            if (key > bk) {  // this set sees its blocks in increasing order: ties keep the first
+              bk = key;
+              bs = t;
+#pragma unroll
+              for (int e = 0; e < kBlk; ++e) zb[e] = z[e];
+            }
           }
         }
       }
+
+      // ---- publish this set's best (block key, block) and its (max, sum exp)
+      if (valid && !*abort) {
+        if (bs != kNoIdx && bk > -INFINITY) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bs));
+        // every set writes its slot every step (a set without blocks writes
+        // the neutral partial), so no entry of an earlier launch is combined
+        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + 2 * cg + set] = make_float2(M, S);
+      }
       grid_sync(p, leader, abort);
+
+      // ---- the token draw inside the winning block, by the warp whose lane
+      // holds that block's z: lanes take tokens 2l, 2l + 1, then
+      // x_k = argmax_v (z_v + G_v); W1[x_k] goes into the group's A image and
+      // a released flag carries x_k (and z_{x_k} for the finalize)
+      if (!aborted()) {
+        const unsigned long long wv = valid ? __ldcg(win + (size_t)(k - 1) * p.rowsG + b) : 0ull;
+        if (valid && wv == 0ull) {
+          raise_status(p.status, DSPARK_ENUMERIC);
+          *abort = 1;
+        }
+        unsigned om = __ballot_sync(0xFFFFFFFFu, valid && bs != kNoIdx && win_block(wv) == bs);
+        while (om) {
+          const int src = __ffs(om) - 1;
+          om &= om - 1;
+          const int ob = __shfl_sync(0xFFFFFFFFu, b, src);
+          const int blk = __shfl_sync(0xFFFFFFFFu, bs, src);
+          float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < kBlk; ++e) {
+            const float v = __shfl_sync(0xFFFFFFFFu, zb[e], src);
+            if ((e >> 1) == lane) {
+              if (e & 1) z1 = v;
+              else z0 = v;
+            }
+          }
+          const int v0 = blk * kBlk + 2 * lane;
+          const uint4 wd = p.rng.block4(kDraftToken, ob, k, v0);  // words of v0 .. v0 + 1
+          KeyIdx kt = key_none();
+          if (v0 < p.V) kt = KeyIdx{z0 + gumbel((lane & 1) ? wd.z : wd.x), v0};
+          if (v0 + 1 < p.V) kt = better(kt, KeyIdx{z1 + gumbel((lane & 1) ? wd.w : wd.y), v0 + 1});
+          kt = warp_best(kt);
+          if (kt.idx == kNoIdx) {
+            if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
+            *abort = 1;
+            break;
+          }
+          const int x = kt.idx, xl = x - blk * kBlk;
+          const float zx = __shfl_sync(0xFFFFFFFFu, (xl & 1) ? z1 : z0, xl >> 1);
+          if (k < p.g) {
+            const int m2 = ob - grp * kTcRows;
+            for (int ci = lane; ci < p.r / 8; ci += 32) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r) + ci);
+              *reinterpret_cast<uint4*>(img + a_piece(m2, ci >> 3, ci & 7)) = v;
+            }
+            tc::fence_proxy_async_global();  // the image is read by bulk copies
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            tc::st_release_gpu(xw + (size_t)(k - 1) * p.rowsG + ob,
+                               ((unsigned long long)__float_as_uint(zx) << 32) | (unsigned)(x + 1));
+          }
+        }
+        // the next A image is complete once every row of the group has its flag
+        // (a lane polls its four rows together with relaxed loads; the fence
+        // after the last one orders the bulk copy of the image behind them)
+        if (k < p.g && warp == 2) {
+          const unsigned long long* f = xw + (size_t)(k - 1) * p.rowsG + grp * kTcRows;
+          unsigned pending = 0;
+#pragma unroll
+          for (int u = 0; u < kTcRows / 32; ++u)
+            if (grp * kTcRows + lane + 32 * u < p.B) pending |= 1u << u;
+          bool ok = true;
+          const unsigned long long t0 = tc::globaltimer();
+          while (pending) {
+            unsigned long long v[kTcRows / 32];
+#pragma unroll
+            for (int u = 0; u < kTcRows / 32; ++u) v[u] = (pending >> u) & 1u ? tc::ld_relaxed_gpu(f + lane + 32 * u) : 0ull;
+#pragma unroll
+            for (int u = 0; u < kTcRows / 32; ++u)
+              if (v[u]) pending &= ~(1u << u);
+            if (!pending) break;
+            if (*(volatile int*)p.status != 0) {
+              ok = false;
+              break;
+            }
+            if (tc::globaltimer() - t0 > tc::kWaitNs) {
+              raise_status(p.status, DSPARK_ETIMEOUT);
+              ok = false;
+              break;
+            }
+            __nanosleep(32);
+          }
+          if (__any_sync(0xFFFFFFFFu, !ok) && lane == 0) *abort = 1;
+          __threadfence();
+        }
+      }
     }
+
+    // ---- after the last step: per (row, step), one warp combines the
+    // partials into the log-sum-exp, the drawn token's probability, and the
+    // confidence c_k from W1[x_{k-1}]
+    if (!aborted()) {
+      const int nw = p.G * (kEpiThreads / 32);
+      for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
+        const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
+        const int Pr = 2 * group_ctas(p.G, p.nG, br / kTcRows);
+        unsigned long long fx = 0ull, fp = 0ull;
+        if (lane == 0) {
+          fx = wait_flag(xw + (size_t)kk * p.rowsG + br, p.status);
+          if (kk > 0) fp = wait_flag(xw + (size_t)(kk - 1) * p.rowsG + br, p.status);
+        }
+        fx = __shfl_sync(0xFFFFFFFFu, fx, 0);
+        fp = __shfl_sync(0xFFFFFFFFu, fp, 0);
+        if (fx == 0ull || (kk > 0 && fp == 0ull)) {
+          if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
+          continue;
+        }
+        const int x = (int)(uint32_t)fx - 1;
+        const float zx = __uint_as_float((uint32_t)(fx >> 32));
+        int xp = kk == 0 ? p.anchor[br] : (int)(uint32_t)fp - 1;
+        if (xp < 0 || xp >= p.V) xp = 0;  // an anchor out of range was reported by the prologue
+        const float2* pr = p.dpart + ((size_t)kk * p.rowsG + br) * p.P;
+        float2 dd[kMaxPartLanes];
+#pragma unroll
+        for (int u = 0; u < kMaxPartLanes; ++u) {
+          const int i = lane + 32 * u;
+          dd[u] = i < Pr ? __ldcg(pr + i) : make_float2(-INFINITY, 0.f);
+        }
+        float cd = 0.f;
+        for (int ci = lane; ci < p.r / 8; ci += 32) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)xp * p.r) + ci);
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+          const float* wr = p.w + p.H + ci * 8;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            cd = fmaf(f.x, wr[2 * e], cd);
+            cd = fmaf(f.y, wr[2 * e + 1], cd);
+          }
+        }
+        MS ms{-INFINITY, 0.f};
+#pragma unroll
+        for (int u = 0; u < kMaxPartLanes; ++u) ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
+        ms = warp_ms(ms);
+        cd = warp_sum(cd);
+        if (lane == 0) {
+          const size_t o = (size_t)br * p.g + kk;
+          const float L2 = ms_log(ms);
+          p.tokens[o] = x;
+          p.pd_tok[o] = expf(zx - L2);
+          p.lse[o] = L2;
+          const float cf = 1.f / (1.f + expf(-(p.s_h[o] + cd) / p.T[kk]));
+          if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
+          p.conf[o] = cf;
+        }
+      }
+    }
+    // the launch count picks the slots' half; every CTA read it before the
+    // first grid barrier
+    if (leader && c == 0) atomicAdd(p.bar + 2, 1u);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -565,15 +741,21 @@ cudaError_t draft_tc_configure(dspark_ws* ws) {
   ws->geo.tc_groups = (d.B + kTcRows - 1) / kTcRows;
   ws->geo.tc_grid = ws->geo.num_sms;  // one CTA per SM, all co-resident
   if (ws->geo.tc_grid < ws->geo.tc_groups) return cudaErrorInvalidConfiguration;
+  // the finalize holds a row's partials (two per CTA of its group) in registers
+  const int Ggmax = (ws->geo.tc_grid + ws->geo.tc_groups - 1) / ws->geo.tc_groups;
+  if (2 * Ggmax > 32 * kMaxPartLanes) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
-size_t draft_tc_scratch_rows(const dspark_dims& d, int grid) {
+size_t draft_tc_partials(const dspark_dims& d, int grid) {
   const int nG = (d.B + kTcRows - 1) / kTcRows;
   const int Ggmax = (grid + nG - 1) / nG;
-  const size_t a = (size_t)nG * kTcRows * Ggmax;
-  const size_t b = (size_t)grid * kTcRows;
-  return a > b ? a : b;
+  return (size_t)d.gamma * nG * kTcRows * 2 * Ggmax;
+}
+
+size_t draft_tc_winners(const dspark_dims& d) {
+  const int nG = (d.B + kTcRows - 1) / kTcRows;
+  return (size_t)2 * d.gamma * nG * kTcRows;
 }
 
 cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches) {
@@ -584,7 +766,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   {
     const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
     const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kTcN, (cuuint32_t)d.r};
+    const cuuint32_t box[2] = {(cuuint32_t)kBlk, (cuuint32_t)kKc};
     const cuuint32_t es[2] = {1, 1};
     if (enc(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -608,10 +790,12 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.V = d.V;
   p.r = d.r;
   p.H = d.H;
-  p.ntiles = ws->geo.nblk;
+  p.nblk = ws->geo.nblk;
   p.nG = ws->geo.tc_groups;
   p.G = ws->geo.tc_grid;
   p.Ggmax = (p.G + p.nG - 1) / p.nG;
+  p.P = 2 * p.Ggmax;
+  p.rowsG = p.nG * kTcRows;
   p.rng = Rng::make(a.seed, a.round);
   p.anchor = a.anchor;
   p.W1 = a.W1;
@@ -622,12 +806,19 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.pd_tok = a.pd_tok;
   p.lse = a.lse;
   p.conf = a.conf;
-  p.xbuf = ws->s.xbuf;
   p.dpart = ws->s.dpart;
-  p.drec = ws->s.drec;
+  p.win = ws->s.dwin;
+  p.xw = ws->s.dxw;
   p.aimg = reinterpret_cast<__nv_bfloat16*>(ws->s.aimg);
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
+
+  k_draft_prologue<<<d.B * d.gamma, 128, 0, st>>>(a.h, a.w, d.H, ws->s.s_h,
+                                                 reinterpret_cast<const __nv_bfloat16*>(a.W1), a.anchor, p.aimg,
+                                                 d.gamma, d.V, d.r, ws->s.status);
+  ++*launches;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
 
   const TcSmem L = TcSmem::make(d.r);
   cudaLaunchConfig_t cfg;
@@ -641,7 +832,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_draft_tc, tm_w2, tm_u, p);
+  e = cudaLaunchKernelEx(&cfg, k_draft_tc, tm_w2, tm_u, p);
   ++*launches;
   return e;
 }
