@@ -88,7 +88,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   };
   const size_t o_status = carve(sizeof(int));
   const size_t o_round = carve(sizeof(uint32_t));
-  const size_t o_bar = carve(4 * sizeof(unsigned));
+  const size_t o_bar = carve(8 * sizeof(unsigned));
   const size_t o_sh = carve(sizeof(float) * BG);
   const size_t o_blk = carve(sizeof(float) * (size_t)d.B * geo.nblk);
   const size_t o_ring = carve(d.mode == DSPARK_COMPACT_LAGGED ? sizeof(float) * (d.lag + 1) * BG : 0);
@@ -161,7 +161,7 @@ dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws->s.status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.plan_round, 0, sizeof(uint32_t), st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 4 * sizeof(unsigned), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 8 * sizeof(unsigned), st);
   if (e == cudaSuccess && ws->s.dwin)
     e = cudaMemsetAsync(ws->s.dwin, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
   if (e == cudaSuccess && ws->s.dxw)

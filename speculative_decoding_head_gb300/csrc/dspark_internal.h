@@ -56,13 +56,13 @@ struct Scratch {
   float* vlset;           // [B] target log-sum-exp of that row
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
-  float2* dpart;          // [gamma][groups*128][2*ceil(grid/groups)] per-CTA, per-epilogue-set
+  float2* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
                           // (max, sum exp) of a row's blocks
   unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, block) winners
   unsigned long long* dxw;   // [2][gamma][groups*128] released (z, token + 1) of each draw
                              // (the two halves of dwin and dxw alternate between launches)
   void* aimg;             // [groups][128 x r] bf16: next A operand in its swizzled shared layout
-  unsigned* barrier;      // [4] grid-barrier words: arrivals, generation, draft launch count
+  unsigned* barrier;      // [8] draft kernel words: [2] launch count, [4 + launch parity] barrier arrivals
 };
 
 struct Geometry {

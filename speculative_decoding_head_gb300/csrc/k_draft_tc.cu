@@ -10,31 +10,36 @@
 // logit and writes the rows W1[anchor] as the first A operand image (the
 // swizzled shared-memory layout, so that a CTA loads it with one bulk copy).
 // k_draft_tc, one cooperative launch, runs all gamma steps. Each CTA (one per
-// SM) owns a contiguous range of 64-token vocabulary tiles of one 128-row group:
-//   warp 0      TMA producer of W2, in chunks of 32 K rows x up to 256 tokens
-//               (four 128-byte-swizzled boxes; L2 evict_last: W2 is reused by
-//               every step), into a ring of 4 stages;
-//   warp 10     TMA producer of U, one 64-token block [128 x 64] fp32 at a
-//               time (evict_first: streamed once), into a ring of 3 stages
-//               (two producers, so that neither stream waits behind the other);
+// SM) owns a contiguous range of 64-token sampler blocks of one 128-row group,
+// taken two at a time as MMA tiles:
+//   warp 0      TMA producer of W2, in chunks of 64 K rows x 128 tokens (two
+//               128-byte-swizzled boxes; L2 evict_last: W2 is reused by every
+//               step), into a ring of 4 stages;
+//   warp 10     TMA producer of U, one block [128 x 64] fp32 at a time
+//               (evict_first: streamed once), into a ring of 3 stages (two
+//               producers, so that neither stream waits behind the other);
 //   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma with
-//               M = 128 rows, N = 64 x (blocks of the tile, up to 4), K = r in
-//               steps of 16, into one of two 256-column accumulators; A = the
-//               rows W1[x_{k-1}] in shared memory. (A narrower N costs about as
-//               much per instruction, so the tile is as wide as TMEM allows.)
-//   warps 2-9   epilogue, two sets of four warps; set s takes the blocks of
-//               parity s, one thread per row: z = TMEM + U, the block's
-//               log-mass (max, sum exp), the block draw key log mass + G_s,
-//               the row's online log-sum-exp, and a register copy of z for the
-//               set's best block so far.
+//               M = 128 rows, N = 64 x (blocks of the tile), K = r in steps of
+//               16, into one of four 128-column accumulators, so the MMA can
+//               run up to three tiles ahead; A = the rows W1[x_{k-1}] in shared
+//               memory. Each accumulator starts as the tile's U blocks, copied
+//               from shared memory by tcgen05.cp, so a U stage is free as soon
+//               as that copy lands and z = U + A W2 comes out of TMEM. (The
+//               tensor core takes about as long per instruction for N = 64 as
+//               for N = 128, hence two blocks per tile.)
+//   warps 2-9   epilogue, two sets of four warps (one per TMEM lane quarter);
+//               set s takes the blocks gb with gb % 2 == s, one thread per row:
+//               z = TMEM, the block's log-mass (max, sum exp), the block
+//               draw key log mass + G_s, the row's online log-sum-exp, and a
+//               register copy of z for the set's best block so far.
 // Step boundary. The block draw is a grid-wide argmax: each set publishes its
 // best (key, block) per row with a 64-bit atomic max, then all CTAs meet at
 // one grid barrier. The token draw inside the winning block needs only that
-// block's z, which the set that found it still holds in registers: that
-// warp draws the token (lanes split the 64 tokens), writes W1[x_k] into the
+// block's z, which the set that found it recorded: that set's warp draws the
+// token (lanes split the 64 tokens), writes W1[x_k] into the
 // group's A image and releases a per-row flag carrying x_k. Every CTA polls
-// its group's flags and loads the image with one bulk copy. The producer
-// keeps prefetching the next step's tiles meanwhile (they do not depend on
+// its group's flags and loads the image with one bulk copy. The producers
+// keep prefetching the next step's tiles meanwhile (they do not depend on
 // the drafted token). Log-sum-exps, probabilities of the drawn tokens and
 // confidences are off that chain: per-set partials (max, sum exp) are kept
 // per step and combined after the last step, one warp per (row, step).
@@ -51,23 +56,25 @@
 
 namespace dspark {
 
-constexpr int kTcThreads = 352;
-constexpr int kEpiThreads = 256;    // warps 2..9
-constexpr int kUWarp = 10;          // U producer
+constexpr int kSets = 2;            // epilogue sets of four warps (one warp per TMEM lane quarter)
+constexpr int kEpiThreads = kSets * 128;  // warps 2 .. 2 + 4 * kSets - 1
+constexpr int kUWarp = 2 + 4 * kSets;     // U producer
+constexpr int kTcThreads = 32 * (kUWarp + 1);
 constexpr int kTcRows = 128;        // MMA M: rows of one row group
 constexpr int kBlk = 64;            // sampler block = one 64-column slice of the accumulator
-constexpr int kTileBlocks = 4;      // MMA N = 64 x blocks of the tile (<= 256)
-constexpr int kKc = 32;             // K rows of W2 per ring stage
-constexpr int kW2Box = kKc * 128;   // 4 KB: 32 K rows x 64 tokens (128-byte rows)
+constexpr int kTileBlocks = 2;      // MMA N = 64 x blocks of the tile
+constexpr int kKc = 64;             // K rows of W2 per ring stage
+constexpr int kW2Box = kKc * 128;   // 8 KB: 64 K rows x 64 tokens (128-byte rows)
 constexpr int kW2Stage = kTileBlocks * kW2Box;  // 16 KB
 constexpr int kNW = 4;              // W2 ring depth (K chunks)
 constexpr int kNU = 3;              // U ring depth (blocks)
 constexpr int kUStage = kTcRows * kBlk * 4;  // 32 KB: two 128 x 32 fp32 boxes
 constexpr int kUBox = kTcRows * 32 * 4;      // 16 KB
-constexpr int kAccCols = kTileBlocks * kBlk; // 256 columns per accumulator
-constexpr int kTmemCols = 2 * kAccCols;      // two accumulators: all of TMEM
+constexpr int kAccCols = kTileBlocks * kBlk; // 128 columns per accumulator
+constexpr int kNAcc = 4;                     // accumulators: the MMA runs up to three tiles ahead
+constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
-constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (two per CTA, <= 256 CTAs a group)
+constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
 
 static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
 
@@ -79,9 +86,9 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     s.w2 = s.a + kTcRows * r * 2;
     s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
-    // w2 full/empty, u full (one per stage and set), u empty, t full/empty,
+    // w2 full/empty, u full, u empty, t full/empty,
     // a_full, drain, a_img
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + kNU + 4 + 3);
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 3);
     s.total = s.misc + 64;
     return s;
   }
@@ -104,7 +111,7 @@ struct TcParams {
   unsigned long long* win;  // [2][g][rowsG]: packed (block key, block), 0 = none
   unsigned long long* xw;   // [2][g][rowsG]: (z of x_k) << 32 | (x_k + 1), 0 = not yet drawn
   __nv_bfloat16* aimg;      // [nG][128 x r]: next A operand in its swizzled shared layout
-  unsigned* bar;            // [0] arrivals, [1] generation, [2] launches (parity of win, xw)
+  unsigned* bar;            // [2] launches (parity of win, xw, counters), [4 + parity] grid-barrier arrivals
   int* status;
 };
 
@@ -128,37 +135,30 @@ __device__ __forceinline__ size_t a_piece(int m, int kb, int ch) {
   return (size_t)kb * (kTcRows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
 }
 
-// Grid barrier among the epilogue warps (256 threads, named barrier 1) of all
-// CTAs. Self-resetting: the last arriver zeroes the count and bumps the
-// generation. Returns false if the round is being abandoned.
-__device__ bool grid_sync(const TcParams& p, bool leader, volatile int* abort) {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+// Grid barrier among the epilogue warps (named barrier 1) of all CTAs: the
+// leader of each CTA adds one to this launch's arrival counter (release) and
+// waits (acquire) until it reaches `target` = G x (barriers so far). The
+// counter only grows within a launch; the other launch parity's counter is
+// cleared at the start of each launch. Returns false if the round is being
+// abandoned.
+__device__ bool grid_sync(const TcParams& p, unsigned* ctr, unsigned target, bool leader, volatile int* abort) {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
   if (leader && !*abort) {
-    const unsigned g0 = tc::ld_acquire_gpu(p.bar + 1);
-    __threadfence();
-    const unsigned arrived = atomicAdd(p.bar, 1u);
-    if (arrived == (unsigned)p.G - 1) {
-      atomicExch(p.bar, 0u);
-      __threadfence();
-      atomicAdd(p.bar + 1, 1u);
-    } else {
-      const unsigned long long t0 = tc::globaltimer();
-      while (tc::ld_acquire_gpu(p.bar + 1) == g0) {
-        if (*(volatile int*)p.status != 0) {
-          *abort = 1;
-          break;
-        }
-        if (tc::globaltimer() - t0 > tc::kWaitNs) {
-          raise_status(p.status, DSPARK_ETIMEOUT);
-          *abort = 1;
-          break;
-        }
-        __nanosleep(64);
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+    const unsigned long long t0 = tc::globaltimer();
+    while (tc::ld_acquire_gpu(ctr) < target) {
+      if (*(volatile int*)p.status != 0) {
+        *abort = 1;
+        break;
+      }
+      if (tc::globaltimer() - t0 > tc::kWaitNs) {
+        raise_status(p.status, DSPARK_ETIMEOUT);
+        *abort = 1;
+        break;
       }
     }
-    __threadfence();
   }
-  asm volatile("bar.sync 1, 256;" ::: "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
   return !*abort;
 }
 
@@ -221,15 +221,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sA = sbase + L.a, sW2 = sbase + L.w2, sU = sbase + L.u;
   const uint32_t bars = sbase + L.bars;
-  // u_full has one barrier per (stage, set): the two sets consume alternate
-  // blocks, so a barrier shared by both could be waited on one phase early
   auto w2_full = [&](int i) { return bars + 8u * i; };
   auto w2_empty = [&](int i) { return bars + 8u * (kNW + i); };
-  auto u_full = [&](int gb) { return bars + 8u * (2 * kNW + gb % (2 * kNU)); };
-  auto u_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + i); };
-  auto t_full = [&](int i) { return bars + 8u * (2 * kNW + 3 * kNU + i); };
-  auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 3 * kNU + 2 + i); };
-  const uint32_t a_full = bars + 8u * (2 * kNW + 3 * kNU + 4);
+  auto u_full = [&](int gb) { return bars + 8u * (2 * kNW + gb % kNU); };
+  auto u_empty = [&](int i) { return bars + 8u * (2 * kNW + kNU + i); };
+  auto t_full = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + i); };
+  auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + kNAcc + i); };
+  const uint32_t a_full = bars + 8u * (2 * kNW + 2 * kNU + 2 * kNAcc);
   const uint32_t drain = a_full + 8u;
   const uint32_t a_img = a_full + 16u;  // the bulk copy of the A image
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
@@ -251,9 +249,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(w2_full(i), 1);
       tc::mbar_init(w2_empty(i), 1);
     }
-    for (int i = 0; i < 2 * kNU; ++i) tc::mbar_init(u_full(i), 1);
-    for (int i = 0; i < kNU; ++i) tc::mbar_init(u_empty(i), 4);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNU; ++i) {
+      tc::mbar_init(u_full(i), 1);
+      tc::mbar_init(u_empty(i), 1);
+    }
+    for (int i = 0; i < kNAcc; ++i) {
       tc::mbar_init(t_full(i), 1);
       tc::mbar_init(t_empty(i), kEpiThreads / 32);
     }
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *abort = 1;
         volatile int never = 0;
         for (int gb = uiss - 1; gb >= 0 && gb >= uiss - kNU; --gb)
-          tc::mbar_wait(u_full(gb), (gb / (2 * kNU)) & 1, &never);
+          tc::mbar_wait(u_full(gb), (gb / kNU) & 1, &never);
       }
     }
   } else if (warp == 1) {
@@ -337,10 +337,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
         for (int tj = 0; tj < ntl && ok; ++tj) {
-          const int it = (k - 1) * ntl + tj, ab = it & 1, nbt = tile_blocks(tj);
+          const int it = (k - 1) * ntl + tj, ab = it % kNAcc, nbt = tile_blocks(tj);
           const uint32_t idesc = tc::idesc_bf16_f32(kTcRows, nbt * kBlk, true);
           const uint32_t d = tmem + (uint32_t)(ab * kAccCols);
-          ok = tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
+          ok = tc::mbar_wait(t_empty(ab), ((it / kNAcc) & 1) ^ 1, abort);
+          // the accumulator starts as U: each block [128 x 64] fp32 (two
+          // 128-byte-swizzled boxes of 32 columns) copied into its columns
+          for (int j = 0; j < nbt && ok; ++j) {
+            const int gb = (k - 1) * nbc + tj * kTileBlocks + j, us = gb % kNU;
+            ok = tc::mbar_wait(u_full(gb), (gb / kNU) & 1, abort);
+            if (!ok) break;
+            tc::tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                tc::cp_128x256b(d + (uint32_t)(j * kBlk + h * 32 + cc * 8),
+                                tc::smem_desc(sU + us * kUStage + h * kUBox + cc * 32, 16, 1024));
+            tc::mma_commit(u_empty(us));  // the stage is free once the copies are done
+          }
           for (int ch = 0; ch < nkc && ok; ++ch) {
             const int wc = it * nkc + ch, ws = wc % kNW;
             ok = tc::mbar_wait(w2_full(ws), (wc / kNW) & 1, abort);
@@ -355,7 +370,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               // 8 K rows of 128 B form a 1 KB atom, 16 K rows per step, the
               // 64-token boxes of the chunk are 4 KB apart.
               const uint64_t bd = tc::smem_desc(sW2 + ws * kW2Stage + kk * 2048, kW2Box, 1024);
-              tc::mma_bf16(d, ad, bd, idesc, (ch | kk) ? 1u : 0u);
+              tc::mma_bf16(d, ad, bd, idesc, 1u);
             }
             tc::mma_commit(w2_empty(ws));
           }
@@ -376,8 +391,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Every epilogue warp runs all gamma steps and every grid barrier even
     // after an abort (the named barrier inside grid_sync has no timeout, so no
     // warp may skip one); an abort only skips the work.
-    const int ew = warp - 2;     // 0..7
-    const int set = ew >> 2;     // TMEM accumulator and tile parity of this warp
+    const int ew = warp - 2;     // 0 .. 4 * kSets - 1
+    const int set = ew >> 2;     // this warp takes the blocks gb with gb % kSets == set
     const int q = warp & 3;      // TMEM lane quarter this warp may access
     const int m = q * 32 + lane;
     const int b = grp * kTcRows + m;
@@ -390,11 +405,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // this launch's half of the winner and flag slots; the other half, last
     // used by the previous launch, is cleared for the next one
     const int par = (int)(__ldcg(p.bar + 2) & 1u);
+    unsigned* gctr = p.bar + 4 + par;
     const size_t half = (size_t)p.g * p.rowsG;
     unsigned long long* win = p.win + par * half;
     unsigned long long* xw = p.xw + par * half;
     {
       const int et = threadIdx.x - 64;
+      if (c == 0 && et == 0) p.bar[4 + (par ^ 1)] = 0u;
       for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads) {
         p.win[(par ^ 1) * half + i] = 0ull;
         p.xw[(par ^ 1) * half + i] = 0ull;
@@ -422,19 +439,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
-      // ---- this CTA's tiles; set s takes the blocks whose running index has
-      // parity s (so the sets share each tile and the U ring evenly)
+      // ---- this CTA's tiles; set s takes the blocks whose running index gb
+      // has gb % kSets == s (so the sets share the tiles and the U ring evenly)
       float M = -INFINITY, S = 0.f, bk = -INFINITY;
       int bs = kNoIdx;
-      float zb[kBlk];
+      float zb[kBlk];  // z of this set's best block so far
 #pragma unroll
-      for (int j = 0; j < kBlk; ++j) zb[j] = 0.f;
+      for (int e = 0; e < kBlk; ++e) zb[e] = 0.f;
+      // G_s of the set's next block, drawn one block ahead so that the Philox
+      // rounds and logarithms interleave with the current block's exponentials
+      const int tlast = blo + nbc - 1;
+      float g_next = gumbel(p.rng.word(kDraftBlock, b, k, min(blo + (set - ((k - 1) * nbc) % kSets + kSets) % kSets, tlast)));
       for (int tj = 0; tj < ntl && !aborted(); ++tj) {
-        const int it = (k - 1) * ntl + tj, ab = it & 1, nbt = tile_blocks(tj);
+        const int it = (k - 1) * ntl + tj, ab = it % kNAcc, nbt = tile_blocks(tj);
         const int gb0 = (k - 1) * nbc + tj * kTileBlocks;
-        const int j0 = (gb0 & 1) == set ? 0 : 1;   // first block of this set in the tile
-        const int jl = j0 + ((nbt - 1 - j0) & ~1);  // last one (>= nbt: none)
-        bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
+        const int j0 = (set - gb0 % kSets + kSets) % kSets;  // first block of this set in the tile
+        const int jl = j0 + (nbt - 1 - j0) / kSets * kSets;  // last one (j0 >= nbt: none)
+        bool ok = tc::mbar_wait(t_full(ab), (it / kNAcc) & 1, abort);
         ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld below is warp-collective
         if (!ok) {
           if (lane == 0 && !*abort) {
@@ -449,18 +470,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
           continue;
         }
-        for (int j = j0; j < nbt; j += 2) {
-          const int gb = gb0 + j, us = gb % kNU, t = blo + tj * kTileBlocks + j;
-          ok = tc::mbar_wait(u_full(gb), (gb / (2 * kNU)) & 1, abort);
-          ok = __all_sync(0xFFFFFFFFu, ok);
-          if (!ok) {
-            if (lane == 0 && !*abort) {
-              raise_status(p.status, DSPARK_ETIMEOUT);
-              *abort = 1;
-            }
-            break;
-          }
-          float z[kBlk];
+        for (int j = j0; j < nbt; j += kSets) {
+          const int t = blo + tj * kTileBlocks + j;
+          float z[kBlk];  // U + W1[x_{k-1}] W2: the accumulator started as U
           const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kAccCols + j * kBlk);
           tc::tmem_ld32(ta, z);
           tc::tmem_ld32(ta + 32, z + 32);
@@ -470,23 +482,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(t_empty(ab));
           }
-          const uint32_t ub = sU + us * kUStage + m * 128;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-              float4 u;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w)
-                           : "r"(ub + h * kUBox + ((uint32_t)(cc ^ (m & 7)) << 4)));
-              z[h * 32 + cc * 4 + 0] += u.x;
-              z[h * 32 + cc * 4 + 1] += u.y;
-              z[h * 32 + cc * 4 + 2] += u.z;
-              z[h * 32 + cc * 4 + 3] += u.w;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(u_empty(us));
+          const float g_cur = g_next;
+          g_next = gumbel(p.rng.word(kDraftBlock, b, k, min(t + kSets, tlast)));
           if (valid) {
             const int v0 = t * kBlk;
             if (v0 + kBlk > p.V) {
@@ -519,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               S += sb * __expf(mb - M);
             }
-            const float key = lm + gumbel(p.rng.word(kDraftBlock, b, k, t));
+            const float key = lm + g_cur;
             if (key > bk) {  // this set sees its blocks in increasing order: ties keep the first
               bk = key;
               bs = t;
@@ -535,9 +532,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (bs != kNoIdx && bk > -INFINITY) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bs));
         // every set writes its slot every step (a set without blocks writes
         // the neutral partial), so no entry of an earlier launch is combined
-        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + 2 * cg + set] = make_float2(M, S);
+        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] = make_float2(M, S);
       }
-      grid_sync(p, leader, abort);
+      grid_sync(p, gctr, (unsigned)(p.G * k), leader, abort);
 
       // ---- the token draw inside the winning block, by the warp whose lane
       // holds that block's z: lanes take tokens 2l, 2l + 1, then
@@ -555,7 +552,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           om &= om - 1;
           const int ob = __shfl_sync(0xFFFFFFFFu, b, src);
           const int blk = __shfl_sync(0xFFFFFFFFu, bs, src);
-          float z0 = 0.f, z1 = 0.f;
+          float z0 = 0.f, z1 = 0.f;  // z of tokens 2 lane, 2 lane + 1, from lane src
 #pragma unroll
           for (int e = 0; e < kBlk; ++e) {
             const float v = __shfl_sync(0xFFFFFFFFu, zb[e], src);
@@ -565,6 +562,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
           const int v0 = blk * kBlk + 2 * lane;
+          if (k < p.g) {  // the drawn token's W1 row is needed next: start pulling the candidates into L2
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              if (v0 + e < p.V)
+                for (int o = 0; o < p.r * 2; o += 128)
+                  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(W1 + (size_t)(v0 + e) * p.r) + o));
+          }
           const uint4 wd = p.rng.block4(kDraftToken, ob, k, v0);  // words of v0 .. v0 + 1
           KeyIdx kt = key_none();
           if (v0 < p.V) kt = KeyIdx{z0 + gumbel((lane & 1) ? wd.z : wd.x), v0};
@@ -586,11 +590,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::fence_proxy_async_global();  // the image is read by bulk copies
           }
           __syncwarp();
-          if (lane == 0) {
-            __threadfence();
+          if (lane == 0)  // the release covers the image pieces of every lane (ordered by the warp sync)
             tc::st_release_gpu(xw + (size_t)(k - 1) * p.rowsG + ob,
                                ((unsigned long long)__float_as_uint(zx) << 32) | (unsigned)(x + 1));
-          }
         }
         // the next A image is complete once every row of the group has its flag
         // (a lane polls its four rows together with relaxed loads; the fence
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nw = p.G * (kEpiThreads / 32);
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
         const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
-        const int Pr = 2 * group_ctas(p.G, p.nG, br / kTcRows);
+        const int Pr = kSets * group_ctas(p.G, p.nG, br / kTcRows);
         unsigned long long fx = 0ull, fp = 0ull;
         if (lane == 0) {
           fx = wait_flag(xw + (size_t)kk * p.rowsG + br, p.status);
@@ -743,14 +745,14 @@ cudaError_t draft_tc_configure(dspark_ws* ws) {
   if (ws->geo.tc_grid < ws->geo.tc_groups) return cudaErrorInvalidConfiguration;
   // the finalize holds a row's partials (two per CTA of its group) in registers
   const int Ggmax = (ws->geo.tc_grid + ws->geo.tc_groups - 1) / ws->geo.tc_groups;
-  if (2 * Ggmax > 32 * kMaxPartLanes) return cudaErrorInvalidConfiguration;
+  if (kSets * Ggmax > 32 * kMaxPartLanes) return cudaErrorInvalidConfiguration;
   return cudaSuccess;
 }
 
 size_t draft_tc_partials(const dspark_dims& d, int grid) {
   const int nG = (d.B + kTcRows - 1) / kTcRows;
   const int Ggmax = (grid + nG - 1) / nG;
-  return (size_t)d.gamma * nG * kTcRows * 2 * Ggmax;
+  return (size_t)d.gamma * nG * kTcRows * kSets * Ggmax;
 }
 
 size_t draft_tc_winners(const dspark_dims& d) {
@@ -794,7 +796,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.nG = ws->geo.tc_groups;
   p.G = ws->geo.tc_grid;
   p.Ggmax = (p.G + p.nG - 1) / p.nG;
-  p.P = 2 * p.Ggmax;
+  p.P = kSets * p.Ggmax;
   p.rowsG = p.nG * kTcRows;
   p.rng = Rng::make(a.seed, a.round);
   p.anchor = a.anchor;

@@ -195,6 +195,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Shared memory -> TMEM: 128 rows of 256 bits (row i to lane i, eight
+// consecutive 32-bit columns from taddr), the source described like an MMA
+// operand. Issued by one thread; ordered with the MMAs it issues later.
+__device__ __forceinline__ void cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
