@@ -546,8 +546,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           raise_status(p.status, DSPARK_ENUMERIC);
           *abort = 1;
         }
-        unsigned om = __ballot_sync(0xFFFFFFFFu, valid && bs != kNoIdx && win_block(wv) == bs);
-        while (om) {
+        // all the warp's draws first (each lane keeps its own row's result),
+        // then every owner's W1 row is loaded at once, written to the image,
+        // and the flags released together
+        const unsigned owners = __ballot_sync(0xFFFFFFFFu, valid && bs != kNoIdx && win_block(wv) == bs);
+        int my_x = -1;
+        float my_zx = 0.f;
+        bool drawn = true;
+        for (unsigned om = owners; om;) {
           const int src = __ffs(om) - 1;
           om &= om - 1;
           const int ob = __shfl_sync(0xFFFFFFFFu, b, src);
@@ -575,24 +581,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (v0 + 1 < p.V) kt = better(kt, KeyIdx{z1 + gumbel((lane & 1) ? wd.w : wd.y), v0 + 1});
           kt = warp_best(kt);
           if (kt.idx == kNoIdx) {
-            if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
-            *abort = 1;
+            drawn = false;
             break;
           }
-          const int x = kt.idx, xl = x - blk * kBlk;
+          const int xl = kt.idx - blk * kBlk;
           const float zx = __shfl_sync(0xFFFFFFFFu, (xl & 1) ? z1 : z0, xl >> 1);
+          if (lane == src) {
+            my_x = kt.idx;
+            my_zx = zx;
+          }
+        }
+        if (!drawn) {
+          if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
+          *abort = 1;
+        } else {
           if (k < p.g) {
-            const int m2 = ob - grp * kTcRows;
-            for (int ci = lane; ci < p.r / 8; ci += 32) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r) + ci);
-              *reinterpret_cast<uint4*>(img + a_piece(m2, ci >> 3, ci & 7)) = v;
+            // up to four rows' loads in flight before their stores
+            for (unsigned om = owners; om;) {
+              int srcs[4], n = 0;
+              uint4 v[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                srcs[u] = om ? __ffs(om) - 1 : -1;
+                if (om) {
+                  om &= om - 1;
+                  ++n;
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int x = __shfl_sync(0xFFFFFFFFu, my_x, srcs[u] < 0 ? 0 : srcs[u]);
+                v[u] = (srcs[u] >= 0 && lane < p.r / 8) ? __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r) + lane)
+                                                        : make_uint4(0, 0, 0, 0);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                if (u < n && lane < p.r / 8)
+                  *reinterpret_cast<uint4*>(img + a_piece(q * 32 + srcs[u], lane >> 3, lane & 7)) = v[u];
             }
             tc::fence_proxy_async_global();  // the image is read by bulk copies
           }
           __syncwarp();
-          if (lane == 0)  // the release covers the image pieces of every lane (ordered by the warp sync)
-            tc::st_release_gpu(xw + (size_t)(k - 1) * p.rowsG + ob,
-                               ((unsigned long long)__float_as_uint(zx) << 32) | (unsigned)(x + 1));
+          // each owner lane releases its row; the release covers the image
+          // pieces every lane wrote (ordered by the warp sync)
+          if ((owners >> lane) & 1u)
+            tc::st_release_gpu(xw + (size_t)(k - 1) * p.rowsG + b,
+                               ((unsigned long long)__float_as_uint(my_zx) << 32) | (unsigned)(my_x + 1));
         }
         // the next A image is complete once every row of the group has its flag
         // (a lane polls its four rows together with relaxed loads; the fence
