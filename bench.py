@@ -31,6 +31,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofline"
+
+# DRAM bytes (read + write) of one k_draft_tc launch on the prod workload, from
+# the ncu capture summarised in profiles/draft_tc_prod.md, and a hash of the
+# kernel source it was taken on; the roofline's "traffic" is reported only
+# while the source is unchanged.
+DRAFT_TRAFFIC = {"sha256": "1b7ffa5bb61c3b65b19b548e869c5eb413c157c3f5dc99ee92ded8eabb52feec",
+                 "bytes": 419816448 + 3190272}
 NORTH_STAR_BW = 8000.0   # GB/s, the roofline constant the metric is quoted against
 
 
@@ -46,6 +53,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
+
+
+def draft_traffic():
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "speculative_decoding_head_gb300", "csrc", "k_draft_tc.cu"), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return DRAFT_TRAFFIC["bytes"] if h == DRAFT_TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -319,7 +336,7 @@ def main():
     draft_gbs = draft_bytes / (st["draft"] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": f"draft stage ({ws.path})", "achieved": draft_gbs,
                 "peak": peak, "unit": "GB/s", "frac": draft_gbs / peak, "peak_kind": peak_kind,
-                "traffic": None, "alg_bytes_per_launch": draft_bytes,
+                "traffic": draft_traffic(), "alg_bytes_per_launch": draft_bytes,
                 "launch_ms": st["draft"]}
 
     # end to end through the same C-ABI with host buffers: H2D of the round's
