@@ -27,14 +27,15 @@ namespace dspark {
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanMaxCand = 8192;  // B * gamma supported by the one-CTA planner
 
-__host__ __device__ inline int pow2_at_least(int n) {
-  int p = 1;
-  while (p < n) p <<= 1;
+// Padded candidate count: a power of two, at least one warp's 64-element chunk.
+__host__ __device__ inline int plan_mp(int M) {
+  int p = 64;
+  while (p < M) p <<= 1;
   return p;
 }
 
 size_t plan_smem_bytes(const dspark_dims& d) {
-  const int Mp = pow2_at_least(d.B * d.gamma < 2 ? 2 : d.B * d.gamma);
+  const int Mp = plan_mp(d.B * d.gamma);
   return (size_t)Mp * (sizeof(unsigned long long) + sizeof(unsigned) + sizeof(double)) +
          sizeof(int) * (size_t)(d.B + 1) + 64;
 }
@@ -72,9 +73,55 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
   }
   __syncthreads();
   (void)M;
-  // bitonic sort into "before" order
-  for (int size = 2; size <= Mp; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+  // Bitonic sort into "before" order. A warp keeps a 64-element chunk in
+  // registers (lane l: elements 64c + l and 64c + 32 + l), so every stage of
+  // stride <= 32 is an in-lane swap or a shuffle with no block barrier; only
+  // strides >= 64 go through shared memory, one barrier each.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  auto reg_stages = [&](int size_lo, int size_hi, int s_hi) {
+    for (int c = warp; c < Mp / 64; c += nwarps) {
+      const int e0 = 64 * c + lane, e1 = e0 + 32;
+      unsigned long long k0 = sm.key[e0], k1 = sm.key[e1];
+      unsigned i0 = sm.id[e0], i1 = sm.id[e1];
+      for (int size = size_lo; size <= size_hi; size <<= 1) {
+        for (int st = min(size >> 1, s_hi); st > 0; st >>= 1) {
+          if (st == 32) {  // e0 and e1 pair up inside the lane; e0 is the lower index
+            const bool up = (e0 & size) == 0;
+            if (before(k0, i0, k1, i1) != up) {
+              const unsigned long long tk = k0;
+              k0 = k1;
+              k1 = tk;
+              const unsigned ti = i0;
+              i0 = i1;
+              i1 = ti;
+            }
+          } else {
+            const unsigned long long p0 = __shfl_xor_sync(0xFFFFFFFFu, k0, st), p1 = __shfl_xor_sync(0xFFFFFFFFu, k1, st);
+            const unsigned q0 = __shfl_xor_sync(0xFFFFFFFFu, i0, st), q1 = __shfl_xor_sync(0xFFFFFFFFu, i1, st);
+            // keep the element that goes first iff (this index is the lower one) == up
+            const bool keep0 = ((e0 & st) == 0) == ((e0 & size) == 0);
+            const bool keep1 = ((e1 & st) == 0) == ((e1 & size) == 0);
+            if (before(k0, i0, p0, q0) != keep0) {
+              k0 = p0;
+              i0 = q0;
+            }
+            if (before(k1, i1, p1, q1) != keep1) {
+              k1 = p1;
+              i1 = q1;
+            }
+          }
+        }
+      }
+      sm.key[e0] = k0;
+      sm.key[e1] = k1;
+      sm.id[e0] = i0;
+      sm.id[e1] = i1;
+    }
+    __syncthreads();
+  };
+  reg_stages(2, 64, 32);
+  for (int size = 128; size <= Mp; size <<= 1) {
+    for (int stride = size >> 1; stride >= 64; stride >>= 1) {
       for (int t = threadIdx.x; t < Mp / 2; t += blockDim.x) {
         const int lo = 2 * t - (t & (stride - 1));
         const int hi = lo + stride;
@@ -91,6 +138,7 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
       }
       __syncthreads();
     }
+    reg_stages(size, size, 32);
   }
 }
 
@@ -147,7 +195,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   __shared__ int s_cut;
   __shared__ int s_bestm;
   const int M = B * g;
-  const int Mp = pow2_at_least(M < 2 ? 2 : M);
+  const int Mp = plan_mp(M);
   PlanSmem sm;
   sm.key = reinterpret_cast<unsigned long long*>(smem_raw);
   sm.pre = reinterpret_cast<double*>(sm.key + Mp);
