@@ -12,12 +12,14 @@
 //
 // Orientation: D[v, i] = sum_k W2[k, v] W1[x_i, k] with M = 128 vocabulary
 // entries (A = W2 tile, N-major in memory, 128-byte swizzle, two 64-wide
-// boxes) and N = 128 rejected requests (B = gathered W1 rows, K-major). Each
-// epilogue thread owns one vocabulary entry and reads U and P of every
-// request with loads that are coalesced across the warp; a block's mass is a
-// sum over two warps' lanes (a 31-shuffle transpose-reduce per 32 requests,
-// then shared memory). Requests are taken in groups of 128 (the list of
-// rejected requests is compacted in each CTA from the verify flags).
+// boxes) and N = 32 rejected requests (B = gathered W1 rows, K-major). A
+// producer warp stages, per tile, each request's 512-byte slices of U and P in
+// shared memory with bulk copies (a two-stage ring), so each epilogue thread
+// owns one vocabulary entry and reads U and P of every request from shared
+// memory; a block's mass is a sum over two warps' lanes (a 31-shuffle
+// transpose-reduce per 32 requests, then shared memory). Requests are taken in
+// groups of 32 (the list of rejected requests is compacted in each CTA from
+// the verify flags); more groups re-read W2, which the draft left in L2.
 // Persistent, one CTA per SM over 128-wide vocabulary tiles; W2 is read with
 // the L2 evict_last policy (the draft kept it there), U and P with evict-first
 // streaming loads. Every wait is bounded.
@@ -32,26 +34,31 @@ namespace dspark {
 
 namespace {
 
-constexpr int kRThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter)
+constexpr int kRThreads = 352;   // warp 0 W2 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 U/P bulk copies
 constexpr int kREpi = 8;
+constexpr int kRUPWarp = 10;
 constexpr int kRM = 128;          // vocabulary entries per tile (MMA M)
-constexpr int kRN = 128;          // requests per group (MMA N)
+constexpr int kRN = 32;           // requests per group (MMA N)
 constexpr int kRNW = 2;           // W2 ring depth
-constexpr int kRTmemCols = 256;   // two 128-column accumulators
+constexpr int kRUP = 2;           // U/P ring depth (tiles)
+constexpr int kRUPStage = kRN * 2 * kRM * 4;  // 32 KB: per request a 512-byte slice of U and of P
+constexpr int kRTmemCols = 64;    // two 32-column accumulators
+static_assert(kRN == 32, "one 32-request chunk per tile: the four warps of half 0 consume each U/P stage");
 constexpr int kRMaxB = 1024;
 
 struct RSmem {
-  uint32_t bop, w2, col, part, best, list, bars, misc, total;
+  uint32_t bop, w2, up, col, part, best, list, bars, misc, total;
   __host__ __device__ static RSmem make(int r) {
     RSmem s;
     s.bop = 0;                              // [128 requests x r] bf16, K-major swizzled
     s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r x 64] bf16)
-    s.col = s.w2 + kRNW * 2 * r * 128;      // per-request: b, n, row (int), lse_d, lse_t (float)
+    s.up = s.w2 + kRNW * 2 * r * 128;       // kRUP x [request][U slice | P slice] fp32
+    s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row (int), lse_d, lse_t (float)
     s.part = s.col + 5 * 4 * kRN;           // [4 warps][128] block partial sums
     s.best = s.part + 4 * 4 * kRN;          // [128] best key, [128] best block
     s.list = s.best + 2 * 4 * kRN;          // [kRMaxB] rejected requests
     s.bars = s.list + 4 * kRMaxB;
-    s.misc = s.bars + 8 * (2 * kRNW + 4 + 2);
+    s.misc = s.bars + 8 * (2 * kRNW + 4 + 2 + 2 * kRUP);
     s.total = s.misc + 64;
     return s;
   }
@@ -117,6 +124,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
   auto t_empty = [&](int i) { return bars + 8u * (2 * kRNW + 2 + i); };
   const uint32_t a_full = bars + 8u * (2 * kRNW + 4);
   const uint32_t drain = a_full + 8u;
+  auto up_full = [&](int i) { return drain + 8u * (1 + i); };
+  auto up_empty = [&](int i) { return drain + 8u * (1 + kRUP + i); };
+  const uint32_t sUP = sbase + L.up;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
   int* s_nrej = reinterpret_cast<int*>(smem + L.misc + 32);
@@ -140,6 +150,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     tc::mbar_init(a_full, kREpi);
     tc::mbar_init(drain, 1);
+    for (int i = 0; i < kRUP; ++i) {
+      tc::mbar_init(up_full(i), 1);
+      tc::mbar_init(up_empty(i), 4);  // the four warps that read the stage
+    }
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -192,6 +206,46 @@ __global__ void __launch_bounds__(kRThreads, 1)
           tc::mbar_wait(w2_full(it % kRNW), (it / kRNW) & 1, &never);
         }
       }
+    }
+  } else if (warp == kRUPWarp) {
+    // ------------------------------------------------------------ U/P producer
+    // per tile, lane i copies request i's 512-byte slices of U (row n, the
+    // draft position that was rejected) and of P (its target row) with two
+    // bulk copies, so the epilogue reads them from shared memory
+    bool ok = true;
+    int issued = 0;
+    for (int gq = 0; gq < ngroups && ok; ++gq) {
+      const int ncols = min(kRN, nrej - gq * kRN);
+      const float* urow = p.U;
+      const float* prow = p.P;
+      if (lane < ncols) {
+        const int b = list[gq * kRN + lane];
+        urow = p.U + ((size_t)b * p.g + p.n_acc[b]) * p.V;
+        prow = p.P + (size_t)p.vrow[b] * p.V;
+      }
+      for (int i = 0; i < nt && ok; ++i) {
+        const int it = gq * nt + i, us = it % kRUP, v0 = (tile_lo + i) * kRM;
+        const uint32_t bytes = (uint32_t)min(kRM, p.V - v0) * 4u;  // a multiple of 32 (V % 8 == 0)
+        int got = 1;
+        if (lane == 0) got = tc::mbar_wait(up_empty(us), ((it / kRUP) & 1) ^ 1, abort) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), 2u * bytes * (uint32_t)ncols);
+        __syncwarp();
+        if (lane < ncols) {
+          const uint32_t dst = sUP + us * kRUPStage + lane * (2 * kRM * 4);
+          tc::bulk_load(dst, urow + v0, bytes, up_full(us));
+          tc::bulk_load(dst + kRM * 4, prow + v0, bytes, up_full(us));
+        }
+        issued = it + 1;
+      }
+    }
+    if (!ok && lane == 0) {
+      if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
+      *abort = 1;
+      volatile int never = 0;  // let the copies already issued land before the CTA can exit
+      for (int it = issued - 1; it >= 0 && it >= issued - kRUP; --it)
+        tc::mbar_wait(up_full(it % kRUP), (it / kRUP) & 1, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -283,35 +337,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
       asm volatile("bar.sync 2, 256;" ::: "memory");  // column constants visible to all epilogue warps
       const int ncols = min(kRN, nrej - gq * kRN);
-      // pull the U and P rows of local tile ti (4 lines of 128 B per row and
-      // request) into L2 ahead of the demand loads, two tiles ahead
-      auto prefetch_tile = [&](int ti) {
-        if (ti >= nt) return;
-        const int vb = (tile_lo + ti) * kRM;
-        for (int l = et; l < ncols * 8; l += 32 * kREpi) {
-          const int col = l >> 3, part8 = l & 7;
-          const int v = vb + (part8 & 3) * 32;
-          if (v >= p.V) continue;
-          const float* a = part8 < 4 ? p.U + ((size_t)col_b[col] * p.g + col_n[col]) * p.V + v
-                                     : p.P + (size_t)col_row[col] * p.V + v;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-        }
-      };
-      // the rejected rows' slices of this CTA are small (ncols x 2 x 512 B per
-      // tile): pull all of them into L2 up front when they fit in 512 KB,
-      // else run two tiles ahead
-      const bool all_ahead = ncols * 8 * nt <= 4096;
-      if (all_ahead) {
-        for (int ti = 0; ti < nt; ++ti) prefetch_tile(ti);
-      } else {
-        prefetch_tile(0);
-        prefetch_tile(1);
-      }
       for (int i = 0; i < nt; ++i) {
-        const int it = gq * nt + i, t = tile_lo + i, ab = it & 1;
+        const int it = gq * nt + i, t = tile_lo + i, ab = it & 1, us = it % kRUP;
         bool live = !aborted();
         if (live) {
           bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
+          if (half == 0) ok = ok && tc::mbar_wait(up_full(us), (it / kRUP) & 1, abort);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
             if (lane == 0 && !*abort) {
@@ -322,22 +353,20 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
         }
         const int v = t * kRM + q * 32 + lane;
-        if (live && !all_ahead) prefetch_tile(i + 2);
         if (live) {
           tc::tc_fence_after();
           for (int cc = half; cc * 32 < ncols; cc += 2) {
             float a[32];
             tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + cc * 32), a);
             tc::tmem_wait_ld();
-            // all 64 loads first (clamped addresses, no branches between a load
-            // and the next one), then the arithmetic
+            // U and P of request j at this entry, from the staged slices
+            // (consecutive lanes read consecutive words)
             float uu[32], pp[32];
-            const int vv = min(v, p.V - 1);
+            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const int col = min(cc * 32 + j, ncols - 1);
-              uu[j] = __ldcs(p.U + ((size_t)col_b[col] * p.g + col_n[col]) * p.V + vv);
-              pp[j] = __ldcs(p.P + (size_t)col_row[col] * p.V + vv);
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * (2 * kRM * 4)));
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * (2 * kRM * 4) + kRM * 4));
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -348,6 +377,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
             const float s = transpose_sum32(a);  // this warp's 32 entries, request cc*32 + lane
             part[q * kRN + cc * 32 + lane] = s;
+          }
+          if (half == 0) {  // the four warps of half 0 read the stage (kRN = 32: one chunk)
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(up_empty(us));
           }
           tc::tc_fence_before();
           __syncwarp();
