@@ -31,6 +31,7 @@
 namespace dspark {
 
 constexpr int kSweepThreads = 256;
+constexpr int kPickThreads = 1024;  // k_resid_pick: 16 groups of K rows x 64 tokens
 
 __device__ __forceinline__ int request_of_row(const int32_t* __restrict__ row_off, int B, int q) {
   int lo = 0, hi = B - 1;  // largest b with row_off[b] <= q
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(256)
 }
 
 template <int BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPickThreads)
     k_resid_pick(const float* __restrict__ P, const float* __restrict__ U, const void* __restrict__ W1,
                  const void* __restrict__ W2, const int32_t* __restrict__ anchor,
                  const int32_t* __restrict__ tokens, const float* __restrict__ lse, int g, int V, int r,
@@ -450,14 +451,20 @@ __global__ void __launch_bounds__(256)
                  const int* __restrict__ vrow, const float* __restrict__ vlset, Rng rng,
                  const float2* __restrict__ rpart, int32_t* __restrict__ next_anchor) {
   extern __shared__ float e[];  // [r]
-  __shared__ KeyIdx red_k[8];
-  __shared__ float zpart[4][kBlockW];
+  __shared__ KeyIdx red_k[kPickThreads / 32];
+  __shared__ float zpart[kPickThreads / kBlockW][kBlockW];
   __shared__ int s_blk;
   const int b = blockIdx.x;
   if (!vflag[b]) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
   const int n = n_acc[b];
   const float* Prow = P + (size_t)vrow[b] * V;
+  // W1[x_n] (the previous token's row) does not depend on the drawn block:
+  // its load overlaps the reduction of the block keys
+  {
+    const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
+    for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+  }
   if (warp == 0) {
     KeyIdx k2 = key_none();
     for (int i = lane; i < nchunk; i += 32) {
@@ -501,28 +508,34 @@ __global__ void __launch_bounds__(256)
     }
     return;
   }
-  const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
-  for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
-  __syncthreads();
   {
+    // z_v - U = sum_i e_i W2[i, v] for the 64 tokens of the block: 16 groups
+    // of K rows, each thread's loads (r / 16 of them) all in flight together
+    constexpr int kQ = kPickThreads / kBlockW;
     const int vl = tid & (kBlockW - 1), q = tid >> 6;
     const int v = sb * kBlockW + vl;
-    if (q < 4) {
-      float acc = 0.f;
-      if (v < V) {
-#pragma unroll 8
-        for (int i = q; i < r; i += 4) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
-      }
-      zpart[q][vl] = acc;
+    float acc = 0.f;
+    if (v < V) {
+#pragma unroll 16
+      for (int i = q; i < r; i += kQ) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
     }
+    zpart[q][vl] = acc;
+  }
+  float uz = 0.f, pz = 0.f;
+  if (tid < kBlockW && sb * kBlockW + tid < V) {  // issued before the barrier, used after it
+    uz = U[((size_t)b * g + n) * V + sb * kBlockW + tid];
+    pz = Prow[sb * kBlockW + tid];
   }
   __syncthreads();
   if (tid < kBlockW) {
     const int v = sb * kBlockW + tid;
     KeyIdx kt = key_none();
     if (v < V) {
-      const float z = U[((size_t)b * g + n) * V + v] + ((zpart[0][tid] + zpart[1][tid]) + (zpart[2][tid] + zpart[3][tid]));
-      const float lw = resid_logw(Prow[v] - vlset[b], z - lse[(size_t)b * g + n]);
+      float zs = 0.f;
+#pragma unroll
+      for (int q = 0; q < kPickThreads / kBlockW; ++q) zs += zpart[q][tid];
+      const float z = uz + zs;
+      const float lw = resid_logw(pz - vlset[b], z - lse[(size_t)b * g + n]);
       if (lw > -INFINITY) kt = KeyIdx{lw + gumbel(rng.word(kResidToken, b, n, v)), v};
     }
     kt = warp_best(kt);
@@ -564,7 +577,7 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
         a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
         ws->s.vrow, ws->s.vlset, rng, ws->s.rpart);
   }
-  k_resid_pick<BF16><<<d.B, 256, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
+  k_resid_pick<BF16><<<d.B, kPickThreads, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
                                              d.r, geo.nblk, nchunk, ws->s.vflag, a.n_acc, ws->s.vrow,
                                              ws->s.vlset, rng, ws->s.rpart, a.next_anchor);
   *launches += 4;
