@@ -43,11 +43,12 @@ constexpr int kRNW = 2;           // W2 ring depth
 constexpr int kRUP = 2;           // U/P ring depth (tiles)
 constexpr int kRUPStage = kRN * 2 * kRM * 4;  // 32 KB: per request a 512-byte slice of U and of P
 constexpr int kRTmemCols = 64;    // two 32-column accumulators
-static_assert(kRN == 32, "one 32-request chunk per tile: the four warps of half 0 consume each U/P stage");
+static_assert(kRN == 32, "one 32-request chunk per tile, 16 requests for each warp of a TMEM lane quarter");
+constexpr int kRGMax = 16;        // block Gumbels of a group kept in shared memory (blocks per CTA)
 constexpr int kRMaxB = 1024;
 
 struct RSmem {
-  uint32_t bop, w2, up, col, part, best, list, bars, misc, total;
+  uint32_t bop, w2, up, col, part, best, gum, list, bars, misc, total;
   __host__ __device__ static RSmem make(int r) {
     RSmem s;
     s.bop = 0;                              // [128 requests x r] bf16, K-major swizzled
@@ -56,7 +57,8 @@ struct RSmem {
     s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row (int), lse_d, lse_t (float)
     s.part = s.col + 5 * 4 * kRN;           // [4 warps][128] block partial sums
     s.best = s.part + 4 * 4 * kRN;          // [128] best key, [128] best block
-    s.list = s.best + 2 * 4 * kRN;          // [kRMaxB] rejected requests
+    s.gum = s.best + 2 * 4 * kRN;           // [kRN][kRGMax] block Gumbels of this CTA's blocks
+    s.list = s.gum + 4 * kRN * kRGMax;      // [kRMaxB] rejected requests
     s.bars = s.list + 4 * kRMaxB;
     s.misc = s.bars + 8 * (2 * kRNW + 4 + 2 + 2 * kRUP);
     s.total = s.misc + 64;
@@ -82,13 +84,14 @@ struct RParams {
   int* status;
 };
 
-// Sum over the 32 lanes of 32 per-lane values: afterwards a[0] of lane L holds
-// the sum of every lane's a[L] (each step keeps the half whose index bit
-// matches the lane's bit and adds the partner's other half).
-__device__ __forceinline__ float transpose_sum32(float (&a)[32]) {
+// Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
+// sum of every lane's a[L & 15]. Each step keeps the half whose index bit
+// matches the lane's bit and adds the partner's other half (four steps over
+// the lanes that share bit 4), then the two half-warps are added.
+__device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = 8; o >= 1; o >>= 1) {
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int k = 0; k < o; ++k) {
@@ -97,7 +100,7 @@ __device__ __forceinline__ float transpose_sum32(float (&a)[32]) {
       a[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
     }
   }
-  return a[0];
+  return a[0] + __shfl_xor_sync(0xFFFFFFFFu, a[0], 16);
 }
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   float* best_key = reinterpret_cast<float*>(smem + L.best);
   int* best_blk = reinterpret_cast<int*>(best_key + kRN);
   int* list = reinterpret_cast<int*>(smem + L.list);
+  float* gsm = reinterpret_cast<float*>(smem + L.gum);
   const uint32_t bars = sbase + L.bars;
   auto w2_full = [&](int i) { return bars + 8u * i; };
   auto w2_empty = [&](int i) { return bars + 8u * (kRNW + i); };
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tc::mbar_init(drain, 1);
     for (int i = 0; i < kRUP; ++i) {
       tc::mbar_init(up_full(i), 1);
-      tc::mbar_init(up_empty(i), 4);  // the four warps that read the stage
+      tc::mbar_init(up_empty(i), kREpi);  // every epilogue warp reads the stage
     }
     *abort = 0;
     tc::fence_barrier_init();
@@ -337,12 +341,22 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
       asm volatile("bar.sync 2, 256;" ::: "memory");  // column constants visible to all epilogue warps
       const int ncols = min(kRN, nrej - gq * kRN);
+      // the block draw's Gumbel noise of every (request, block) of this CTA,
+      // computed once up front (visible to the combining warp after the first
+      // tile's barrier) instead of on the per-tile critical path
+      const int nbl = 2 * nt;
+      const bool gpre = nbl <= kRGMax;
+      if (gpre)
+        for (int idx = et; idx < ncols * nbl; idx += 32 * kREpi) {
+          const int col = idx / nbl, lb = idx - col * nbl;
+          gsm[col * kRGMax + lb] = gumbel(p.rng.word(kResidBlock, col_b[col], col_n[col], 2 * tile_lo + lb));
+        }
       for (int i = 0; i < nt; ++i) {
         const int it = gq * nt + i, t = tile_lo + i, ab = it & 1, us = it % kRUP;
         bool live = !aborted();
         if (live) {
           bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
-          if (half == 0) ok = ok && tc::mbar_wait(up_full(us), (it / kRUP) & 1, abort);
+          ok = ok && tc::mbar_wait(up_full(us), (it / kRUP) & 1, abort);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
             if (lane == 0 && !*abort) {
@@ -355,33 +369,32 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const int v = t * kRM + q * 32 + lane;
         if (live) {
           tc::tc_fence_after();
-          for (int cc = half; cc * 32 < ncols; cc += 2) {
-            float a[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + cc * 32), a);
+          {
+            // the two warps of a lane quarter take requests 16 half .. 16 half + 15
+            float a[16];
+            tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kRN + half * 16), a);
             tc::tmem_wait_ld();
             // U and P of request j at this entry, from the staged slices
             // (consecutive lanes read consecutive words)
-            float uu[32], pp[32];
-            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(q * 32 + lane) * 4u;
+            float uu[16], pp[16];
+            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(half * 16) * (2 * kRM * 4) + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * (2 * kRM * 4)));
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * (2 * kRM * 4) + kRM * 4));
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = cc * 32 + j;
+            for (int j = 0; j < 16; ++j) {
+              const int col = half * 16 + j;
               const int cl = min(col, ncols - 1);
               const float w = fmaxf(0.f, __expf(pp[j] - col_lset[cl]) - __expf(a[j] + uu[j] - col_lsed[cl]));
               a[j] = (col < ncols && v < p.V) ? w : 0.f;
             }
-            const float s = transpose_sum32(a);  // this warp's 32 entries, request cc*32 + lane
-            part[q * kRN + cc * 32 + lane] = s;
+            const float s = transpose_sum16(a);  // this warp's 32 entries, request 16 half + (lane & 15)
+            if (lane < 16) part[q * kRN + half * 16 + lane] = s;
           }
-          if (half == 0) {  // the four warps of half 0 read the stage (kRN = 32: one chunk)
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(up_empty(us));
-          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(up_empty(us));
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
               if (s * 64 >= p.V) continue;
               const float W = part[(2 * h) * kRN + col] + part[(2 * h + 1) * kRN + col];
               if (!(W > 0.f)) continue;
-              const float key = logf(W) + gumbel(p.rng.word(kResidBlock, b, n, s));
+              const float key = logf(W) + (gpre ? gsm[col * kRGMax + 2 * i + h] : gumbel(p.rng.word(kResidBlock, b, n, s)));
               if (key > best_key[col]) {  // blocks arrive in increasing order: ties keep the first
                 best_key[col] = key;
                 best_blk[col] = s;
