@@ -314,34 +314,56 @@ __global__ void __launch_bounds__(128)
     const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
     MS ms{-INFINITY, 0.f};
     KeyIdx kb = key_none();
-    for (int c = c0; c <= c1; ++c) {
-      const long long clo = unit_lo(c, T, Gs);
-      if (clo >= unit_lo(c + 1, T, Gs)) continue;  // an empty range wrote nothing
-      const int first = (int)(clo / nblk);
-      if (q - first >= SL) continue;
-      const float4 d = part[(size_t)c * SL + (q - first)];
-      ms = ms_combine(ms, MS{d.x, d.y});
-      kb = better(kb, KeyIdx{d.z, __float_as_int(d.w)});
+    for (int cb = c0; cb <= c1; cb += 4) {  // four partials' loads in flight at a time
+      float4 d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = cb + e;
+        d[e] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
+        if (c > c1) continue;
+        const long long clo = unit_lo(c, T, Gs);
+        if (clo >= unit_lo(c + 1, T, Gs)) continue;  // an empty range wrote nothing
+        const int first = (int)(clo / nblk);
+        if (q - first >= SL) continue;
+        d[e] = part[(size_t)c * SL + (q - first)];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ms = ms_combine(ms, MS{d[e].x, d[e].y});
+        kb = better(kb, KeyIdx{d[e].z, __float_as_int(d[e].w)});
+      }
     }
     *ms_out = ms;
     *kb_out = kb;
   };
-  // ---- accept tests of rows 0 .. ell-2, one per lane
+  // ---- one lane per verified row: accept tests of rows 0 .. ell-2, and the
+  // bonus block key of row ell-1; the draft token's target logit is loaded
+  // alongside the row's partials
   bool acc = true, bad = false;
   float Lt = 0.f;
-  if (lane < ell - 1) {
-    const int q = base + lane;
+  KeyIdx kbonus = key_none();
+  const bool arow = lane < ell - 1;
+  int x = 0;
+  float Px = 0.f, pdx = 0.f;
+  if (arow) {
+    x = tokens[(size_t)b * g + lane];
+    pdx = pd_tok[(size_t)b * g + lane];
+    if (x >= 0 && x < V) Px = P[(size_t)(base + lane) * V + x];
+  }
+  if (lane < ell) {
     MS ms;
-    KeyIdx unused;
-    row_partials(q, &ms, &unused);
+    KeyIdx kb;
+    row_partials(base + lane, &ms, &kb);
     Lt = ms_log(ms);
-    const int x = tokens[(size_t)b * g + lane];
+    kbonus = kb;
+  }
+  if (arow) {
     if (!isfinite(Lt) || x < 0 || x >= V) {
       bad = true;
     } else {
-      const float pt = expf(P[(size_t)q * V + x] - Lt);
+      const float pt = expf(Px - Lt);
       const float u = u01(rng.word(kAccept, b, lane, 0));
-      acc = u * pd_tok[(size_t)b * g + lane] < pt;
+      acc = u * pdx < pt;
     }
   }
   const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
@@ -364,11 +386,13 @@ __global__ void __launch_bounds__(128)
   // ---- every verified draft accepted: bonus token from row ell - 1
   const int n = ell - 1;
   const size_t q = (size_t)base + n;
-  MS unused;
-  KeyIdx kb = key_none();
-  if (lane == 0) row_partials((int)q, &unused, &kb);
-  kb.key = __shfl_sync(0xFFFFFFFFu, kb.key, 0);
-  kb.idx = __shfl_sync(0xFFFFFFFFu, kb.idx, 0);
+  KeyIdx kb = kbonus;
+  if (n >= 32) {  // gamma = 32: the bonus row has no lane of its own
+    MS unused;
+    if (lane == 0) row_partials((int)q, &unused, &kb);
+  }
+  kb.key = __shfl_sync(0xFFFFFFFFu, kb.key, n < 32 ? n : 0);
+  kb.idx = __shfl_sync(0xFFFFFFFFu, kb.idx, n < 32 ? n : 0);
   if (kb.idx == kNoIdx) {
     if (lane == 0) raise_status(status, DSPARK_ENUMERIC);
     return;
