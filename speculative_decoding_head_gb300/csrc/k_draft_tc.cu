@@ -58,8 +58,9 @@ namespace dspark {
 
 constexpr int kSets = 2;            // epilogue sets of four warps (one warp per TMEM lane quarter)
 constexpr int kEpiThreads = kSets * 128;  // warps 2 .. 2 + 4 * kSets - 1
-constexpr int kUWarp = 2 + 4 * kSets;     // U producer
-constexpr int kTcThreads = 32 * (kUWarp + 1);
+constexpr int kUWarp = 2 + 4 * kSets;     // U producer (TMA)
+constexpr int kCWarp = kUWarp + 1;        // U copier (shared memory -> accumulator)
+constexpr int kTcThreads = 32 * (kCWarp + 1);
 constexpr int kTcRows = 128;        // MMA M: rows of one row group
 constexpr int kBlk = 64;            // sampler block = one 64-column slice of the accumulator
 constexpr int kTileBlocks = 2;      // MMA N = 64 x blocks of the tile
@@ -86,9 +87,9 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     s.w2 = s.a + kTcRows * r * 2;
     s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
-    // w2 full/empty, u full, u empty, t full/empty,
-    // a_full, drain, a_img
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 3);
+    // w2 full/empty, u full, u empty, t full/empty, a_full, drain, a_img,
+    // acc_u (accumulator holds U), the copier's drain
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 3 + kNAcc + 1);
     s.total = s.misc + 64;
     return s;
   }
@@ -230,6 +231,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t a_full = bars + 8u * (2 * kNW + 2 * kNU + 2 * kNAcc);
   const uint32_t drain = a_full + 8u;
   const uint32_t a_img = a_full + 16u;  // the bulk copy of the A image
+  auto acc_u = [&](int i) { return a_full + 24u + 8u * i; };
+  const uint32_t drain_c = a_full + 24u + 8u * kNAcc;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
 
@@ -260,6 +263,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::mbar_init(a_full, kEpiThreads / 32);
     tc::mbar_init(drain, 1);
     tc::mbar_init(a_img, 1);
+    for (int i = 0; i < kNAcc; ++i) tc::mbar_init(acc_u(i), 1);
+    tc::mbar_init(drain_c, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -328,6 +333,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::mbar_wait(u_full(gb), (gb / kNU) & 1, &never);
       }
     }
+  } else if (warp == kCWarp) {
+    // ------------------------------------------------------------ U copier
+    // Each accumulator starts as the tile's U blocks ([128 x 64] fp32, two
+    // 128-byte-swizzled boxes of 32 columns each), copied into its columns by
+    // tcgen05.cp once the epilogue has released it. The copier's commits track
+    // only its own copies, so a U stage is free as soon as they land, not
+    // when the MMA queue drains.
+    if (lane == 0) {
+      bool ok = true;
+      for (int k = 1; k <= p.g && ok; ++k) {
+        for (int tj = 0; tj < ntl && ok; ++tj) {
+          const int it = (k - 1) * ntl + tj, ab = it % kNAcc, nbt = tile_blocks(tj);
+          const uint32_t d = tmem + (uint32_t)(ab * kAccCols);
+          ok = tc::mbar_wait(t_empty(ab), ((it / kNAcc) & 1) ^ 1, abort);
+          for (int j = 0; j < nbt && ok; ++j) {
+            const int gb = (k - 1) * nbc + tj * kTileBlocks + j, us = gb % kNU;
+            ok = tc::mbar_wait(u_full(gb), (gb / kNU) & 1, abort);
+            if (!ok) break;
+            tc::tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                tc::cp_128x256b(d + (uint32_t)(j * kBlk + h * 32 + cc * 8),
+                                tc::smem_desc(sU + us * kUStage + h * kUBox + cc * 32, 16, 1024));
+            tc::mma_commit(u_empty(us));
+          }
+          if (ok) tc::mma_commit(acc_u(ab));
+        }
+      }
+      if (!ok) {
+        if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
+        *abort = 1;
+      }
+      // every copy this thread issued completes before TMEM is freed
+      tc::mma_commit(drain_c);
+      volatile int never = 0;
+      tc::mbar_wait(drain_c, 0, &never);
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -340,22 +384,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int it = (k - 1) * ntl + tj, ab = it % kNAcc, nbt = tile_blocks(tj);
           const uint32_t idesc = tc::idesc_bf16_f32(kTcRows, nbt * kBlk, true);
           const uint32_t d = tmem + (uint32_t)(ab * kAccCols);
-          ok = tc::mbar_wait(t_empty(ab), ((it / kNAcc) & 1) ^ 1, abort);
-          // the accumulator starts as U: each block [128 x 64] fp32 (two
-          // 128-byte-swizzled boxes of 32 columns) copied into its columns
-          for (int j = 0; j < nbt && ok; ++j) {
-            const int gb = (k - 1) * nbc + tj * kTileBlocks + j, us = gb % kNU;
-            ok = tc::mbar_wait(u_full(gb), (gb / kNU) & 1, abort);
-            if (!ok) break;
-            tc::tc_fence_after();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc)
-                tc::cp_128x256b(d + (uint32_t)(j * kBlk + h * 32 + cc * 8),
-                                tc::smem_desc(sU + us * kUStage + h * kUBox + cc * 32, 16, 1024));
-            tc::mma_commit(u_empty(us));  // the stage is free once the copies are done
-          }
+          // the copier has filled the (free) accumulator with the tile's U
+          ok = tc::mbar_wait(acc_u(ab), (it / kNAcc) & 1, abort);
+          if (ok) tc::tc_fence_after();
           for (int ch = 0; ch < nkc && ok; ++ch) {
             const int wc = it * nkc + ch, ws = wc % kNW;
             ok = tc::mbar_wait(w2_full(ws), (wc / kNW) & 1, abort);
