@@ -133,9 +133,8 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// sum_{i<H} w[i] hr[i] by a CTA of 128 threads (all of a thread's float4
-// loads in flight together); the result is valid in thread 0. `red` is a
-// 4-float shared array of the caller.
+// sum_{i<H} w[i] hr[i] by a CTA of 128 threads; the result is valid in
+// every thread. `red` is a 4-float shared array of the caller.
 __device__ __forceinline__ float hidden_dot128(const float* __restrict__ hr, const float* __restrict__ w, int H,
                                                float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,14 +142,24 @@ __device__ __forceinline__ float hidden_dot128(const float* __restrict__ hr, con
   if ((H & 3) == 0) {
     const float4* h4 = reinterpret_cast<const float4*>(hr);
     const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < H / 4; i += 128) {
-      const float4 a = __ldcs(h4 + i);  // streamed once
-      const float4 c = __ldg(w4 + i);
-      acc = fmaf(a.x, c.x, acc);
-      acc = fmaf(a.y, c.y, acc);
-      acc = fmaf(a.z, c.z, acc);
-      acc = fmaf(a.w, c.w, acc);
+    // up to 16 of a thread's float4 pairs loaded before any is used (H = 5120
+    // is one round), then accumulated in index order
+    for (int i0 = threadIdx.x; i0 < H / 4; i0 += 16 * 128) {
+      float4 a[16], c[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int i = i0 + u * 128;
+        a[u] = i < H / 4 ? __ldcs(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);  // h is streamed once
+        c[u] = i < H / 4 ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (i0 + u * 128 >= H / 4) break;
+        acc = fmaf(a[u].x, c[u].x, acc);
+        acc = fmaf(a[u].y, c[u].y, acc);
+        acc = fmaf(a[u].z, c[u].z, acc);
+        acc = fmaf(a[u].w, c[u].w, acc);
+      }
     }
   } else {
     for (int i = threadIdx.x; i < H; i += 128) acc = fmaf(hr[i], w[i], acc);
