@@ -36,8 +36,8 @@ METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofli
 # the ncu capture summarised in profiles/draft_tc_prod.md, and a hash of the
 # kernel source it was taken on; the roofline's "traffic" is reported only
 # while the source is unchanged.
-DRAFT_TRAFFIC = {"sha256": "1b7ffa5bb61c3b65b19b548e869c5eb413c157c3f5dc99ee92ded8eabb52feec",
-                 "bytes": 419816448 + 3190272}
+DRAFT_TRAFFIC = {"sha256": "1de0532ea374c07b04b9338d084f3d60ac4712384cf5c6bfddf66bd0a0c2d580",
+                 "bytes": 418118912 + 3596032}
 NORTH_STAR_BW = 8000.0   # GB/s, the roofline constant the metric is quoted against
 
 
