@@ -116,6 +116,7 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
 
 size_t plan_smem_bytes(const dspark_dims& d);
 cudaError_t sweep_bulk_configure();
+int sweep_bulk_max_slots();  // rows one CTA range of the bulk sweep may span
 cudaError_t plan_configure();
 
 }  // namespace dspark

@@ -160,6 +160,8 @@ constexpr int kBulkUnits = kBulkThreads;             // one block per thread per
 constexpr int kBulkFloats = kBulkUnits * kBlockW;   // 8192 fp32 = 32 KB
 constexpr int kBulkMaxSlots = 8;
 
+int sweep_bulk_max_slots() { return kBulkMaxSlots; }
+
 size_t sweep_bulk_smem_bytes() {
   return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 128;
 }
