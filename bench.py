@@ -310,24 +310,39 @@ def main():
     ms = max_over_ranks(ms, world)
     assert ws.device_status() == 0
 
-    # stage times (direct calls, events on the launching stream)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    st = {"draft": 0.0, "plan": 0.0, "verify": 0.0}
-    reps = max(5, min(args.steps, 30))
-    for _ in range(reps):
-        ev[0].record(s)
+    # stage times: each stage captured alone in a CUDA graph and replayed back
+    # to back between events on the launching stream (no host launch gaps)
+    def draft_stage():
         ws.draft(dev_inp["U"], dev_inp["W1"], dev_inp["W2"], dev_inp["anchor"], dev_inp["h"], dev_inp["w"],
                  dev_inp["T"], seed, rnd, out=out)
-        ev[1].record(s)
+
+    def plan_stage():
         ws.plan(out["conf"], dev_inp["sps"], out=out)
-        ev[2].record(s)
+
+    def verify_stage():
         ws.verify(P, out["row_off"], out["lengths"], dev_inp["anchor"], out["tokens"], out["pd_tok"], out["lse"],
                   dev_inp["U"], dev_inp["W1"], dev_inp["W2"], seed, rnd, out=out)
-        ev[3].record(s)
+
+    st = {}
+    reps = max(5, min(args.steps, 50))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for name, fn in (("draft", draft_stage), ("plan", plan_stage), ("verify", verify_stage)):
+        srun = fn
+        if graph is not None:
+            sg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(sg):
+                fn()
+            srun = sg.replay
+        for _ in range(3):
+            srun()
         torch.cuda.synchronize()
-        st["draft"] += ev[0].elapsed_time(ev[1]) / reps
-        st["plan"] += ev[1].elapsed_time(ev[2]) / reps
-        st["verify"] += ev[2].elapsed_time(ev[3]) / reps
+        ev[0].record(s)
+        for _ in range(reps):
+            srun()
+        ev[1].record(s)
+        torch.cuda.synchronize()
+        st[name] = ev[0].elapsed_time(ev[1]) / reps
+    assert ws.device_status() == 0
 
     bts = hbm_bytes(wl, sum_len)
     peak, peak_kind = peaks()

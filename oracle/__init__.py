@@ -81,6 +81,8 @@ def lib():
                                      P, P, P, P, P]
             l.orc_sample.argtypes = [P, C.c_long, u64, u64, u32, u32, u32, u32, P]
             l.orc_sample.restype = i32
+            l.orc_sample_draft.argtypes = [P, C.c_long, u64, u64, u32, u32, P]
+            l.orc_sample_draft.restype = i32
             l.orc_residual.argtypes = [P, P, C.c_long, u64, u64, u32, u32, P]
             l.orc_residual.restype = i32
             l.orc_markov_logits.argtypes = [P, P, P, P, i32, P]
@@ -142,6 +144,15 @@ def sample(logw, seed=0, rnd=0, pblk=P_DRAFT_BLOCK, ptok=P_DRAFT_TOKEN, b=0, j=0
     a = _c(logw, np.float64)
     m = np.zeros(1, np.float64)
     v = lib().orc_sample(_p(a), a.size, seed, rnd, pblk, ptok, b, j, _p(m))
+    return int(v), float(m[0])
+
+
+def sample_draft(logw, seed=0, rnd=0, b=0, j=0):
+    """One draw with the draft's sampler (block by Gumbel-max, token inside the
+    block by inverse CDF). Returns (v, margin)."""
+    a = _c(logw, np.float64)
+    m = np.zeros(1, np.float64)
+    v = lib().orc_sample_draft(_p(a), a.size, seed, rnd, b, j, _p(m))
     return int(v), float(m[0])
 
 

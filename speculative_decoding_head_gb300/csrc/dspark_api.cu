@@ -105,15 +105,13 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   cudaGetLastError();
   geo.rchunks = geo.num_sms > kResidChunks ? geo.num_sms : kResidChunks;
   const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * geo.rchunks);
-  size_t o_dpart = 0, o_dwin = 0, o_dxw = 0, o_aimg = 0;
+  size_t o_dpart = 0, o_dwin = 0;
   if (geo.tc_ok) {
     if (draft_tc_configure(ws) != cudaSuccess) geo.tc_ok = 0;
   }
   if (geo.tc_ok) {
-    o_dpart = carve(sizeof(float2) * draft_tc_partials(d, geo.tc_grid));
+    o_dpart = carve(sizeof(float4) * draft_tc_partials(d, geo.tc_grid));
     o_dwin = carve(sizeof(unsigned long long) * draft_tc_winners(d));
-    o_dxw = carve(sizeof(unsigned long long) * draft_tc_winners(d));
-    o_aimg = carve((size_t)geo.tc_groups * 128 * d.r * 2);
   }
   if (plan_configure() != cudaSuccess) {
     delete ws;
@@ -139,10 +137,8 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vrow = reinterpret_cast<int*>(base + o_vrow);
   s.vlset = reinterpret_cast<float*>(base + o_vlset);
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
-  s.dpart = geo.tc_ok ? reinterpret_cast<float2*>(base + o_dpart) : nullptr;
+  s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
-  s.dxw = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dxw) : nullptr;
-  s.aimg = geo.tc_ok ? static_cast<void*>(base + o_aimg) : nullptr;
   ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(ws->arena);
@@ -168,8 +164,6 @@ dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 8 * sizeof(unsigned), st);
   if (e == cudaSuccess && ws->s.dwin)
     e = cudaMemsetAsync(ws->s.dwin, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
-  if (e == cudaSuccess && ws->s.dxw)
-    e = cudaMemsetAsync(ws->s.dxw, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
   return cuda_fail(e);
 }
 

@@ -28,9 +28,11 @@ enum : uint32_t {
   kResidToken = 7,
 };
 
-// Width of the vocabulary blocks of the two-level Gumbel-max sampler: a block
-// is drawn by argmax_s (log mass_s + G_s), then a token inside it by
-// argmax_v (log weight_v + G_v); together an exact draw from the softmax.
+// Width of the vocabulary blocks of the two-level sampler: a block is drawn
+// by argmax_s (log mass_s + G_s), then a token inside it with probability
+// weight / block mass (the draft: inverse CDF with one uniform of the block;
+// the verify draws: argmax_v (log weight_v + G_v)); together an exact draw
+// from the softmax.
 constexpr int kBlockW = 64;
 
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {

@@ -56,12 +56,10 @@ struct Scratch {
   float* vlset;           // [B] target log-sum-exp of that row
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
-  float2* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
+  float4* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
                           // (max, sum exp) of a row's blocks
-  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, block) winners
-  unsigned long long* dxw;   // [2][gamma][groups*128] released (z, token + 1) of each draw
-                             // (the two halves of dwin and dxw alternate between launches)
-  void* aimg;             // [groups][128 x r] bf16: next A operand in its swizzled shared layout
+  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, token) winners; the
+                             // two halves alternate between launches
   unsigned* barrier;      // [8] draft kernel words: [2] launch count, [4 + launch parity] barrier arrivals
 };
 
@@ -107,8 +105,8 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 // Whether the tcgen05 draft kernel supports these dims, and its launch shape.
 int draft_tc_supported(const dspark_dims& d);
 cudaError_t draft_tc_configure(dspark_ws* ws);
-size_t draft_tc_partials(const dspark_dims& d, int grid);  // float2 entries of Scratch::dpart
-size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch::dwin and of dxw
+size_t draft_tc_partials(const dspark_dims& d, int grid);  // float4 entries of Scratch::dpart
+size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch::dwin
 
 int resid_tc_supported(const dspark_dims& d);
 cudaError_t resid_tc_configure(dspark_ws* ws);

@@ -11,8 +11,8 @@
 //                   log-mass of each 64-token vocabulary block;
 //   k_draft_pick    grid (B): log-sum-exp over blocks, the block draw
 //                   argmax_s(log mass_s + G_s), then z of the 64 tokens of the
-//                   drawn block recomputed and the token draw
-//                   argmax_v(z_v + G_v); also c_k.
+//                   drawn block recomputed and the token inside it drawn by
+//                   inverse CDF with one uniform of the block; also c_k.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -159,21 +159,29 @@ __global__ void __launch_bounds__(kSimtThreads)
     float z = -INFINITY;
     if (v < V) z = U[o * V + v] + ((zpart[0][tid] + zpart[1][tid]) + (zpart[2][tid] + zpart[3][tid]));
     zblk[tid] = z;
-    KeyIdx kt = key_none();
-    if (v < V) kt = KeyIdx{z + gumbel(rng.word(kDraftToken, b, k, v)), v};
-    kt = warp_best(kt);
-    if (lane == 0) red_k[1 + warp] = kt;
   }
   __syncthreads();
   if (tid == 0) {
-    const KeyIdx kt = better(red_k[1], red_k[2]);
-    int xk = kt.idx;
-    if (xk == kNoIdx) {  // only non-finite logits get here
-      raise_status(status, DSPARK_ENUMERIC);
-      xk = sb * kBlockW;
+    // inverse CDF with one uniform u of the block: e_v = exp(z_v - max) in
+    // token order, x = the first v whose running sum exceeds u times the
+    // total (the same running sum, so for u < 1 some v always does)
+    float mx = -INFINITY;
+    for (int i = 0; i < kBlockW; ++i) mx = fmaxf(mx, zblk[i]);
+    float tot = 0.f;
+    for (int i = 0; i < kBlockW; ++i) tot += __expf(zblk[i] - mx);
+    const float thr = u01(rng.word(kDraftToken, b, k, sb)) * tot;
+    float cum = 0.f;
+    int xl = -1;
+    for (int i = 0; i < kBlockW && xl < 0; ++i) {
+      cum += __expf(zblk[i] - mx);
+      if (cum > thr) xl = i;
     }
-    tokens[o] = xk;
-    pd_tok[o] = expf(zblk[xk - sb * kBlockW] - L);
+    if (xl < 0) {  // only non-finite logits get here
+      raise_status(status, DSPARK_ENUMERIC);
+      xl = 0;
+    }
+    tokens[o] = sb * kBlockW + xl;
+    pd_tok[o] = expf(zblk[xl] - L);
     lse_out[o] = L;
   }
 }

@@ -7,8 +7,7 @@
 // the STS sigmoid(raw / T) of the zdszero.github.io "spec_dspark" page).
 //
 // Two launches. k_draft_prologue computes the hidden half of every confidence
-// logit and writes the rows W1[anchor] as the first A operand image (the
-// swizzled shared-memory layout, so that a CTA loads it with one bulk copy).
+// logit.
 // k_draft_tc, one cooperative launch, runs all gamma steps. Each CTA (one per
 // SM) owns a contiguous range of 64-token sampler blocks of one 128-row group,
 // taken two at a time as MMA tiles:
@@ -36,9 +35,10 @@
 // best (key, block) per row with a 64-bit atomic max, then all CTAs meet at
 // one grid barrier. The token draw inside the winning block needs only that
 // block's z, which the set that found it recorded: that set's warp draws the
-// token (lanes split the 64 tokens), writes W1[x_k] into the
-// group's A image and releases a per-row flag carrying x_k. Every CTA polls
-// its group's flags and loads the image with one bulk copy. The producers
+// token (lanes split the 64 tokens) and stores a per-row flag carrying x_k.
+// In every CTA of the group, the epilogue thread of each row waits for that
+// flag and gathers W1[x_k] straight into the swizzled A operand in shared
+// memory (the anchors' rows at step 1). The producers
 // keep prefetching the next step's tiles meanwhile (they do not depend on
 // the drafted token). Log-sum-exps, probabilities of the drawn tokens and
 // confidences are off that chain: per-set partials (max, sum exp) are kept
@@ -78,6 +78,7 @@ constexpr int kMaxGroups = 8;       // B <= 1024
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
 
 static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
+static_assert(kSets == 2, "the A gather splits a lane quarter's rows into even and odd");
 
 struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
   uint32_t a, w2, u, bars, misc, total;
@@ -87,9 +88,9 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     s.w2 = s.a + kTcRows * r * 2;
     s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
-    // w2 full/empty, u full, u empty, t full/empty, a_full, drain, a_img,
-    // acc_u (accumulator holds U), the copier's drain
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 3 + kNAcc + 1);
+    // w2 full/empty, u full, u empty, t full/empty, a_full, drain, acc_u
+    // (accumulator holds U), the copier's drain
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 2 + kNAcc + 1);
     s.total = s.misc + 64;
     return s;
   }
@@ -108,25 +109,24 @@ struct TcParams {
   float* pd_tok;
   float* lse;
   float* conf;
-  float2* dpart;            // [g][rowsG][P]: (max, sum exp) per CTA and set
-  unsigned long long* win;  // [2][g][rowsG]: packed (block key, block), 0 = none
-  unsigned long long* xw;   // [2][g][rowsG]: (z of x_k) << 32 | (x_k + 1), 0 = not yet drawn
-  __nv_bfloat16* aimg;      // [nG][128 x r]: next A operand in its swizzled shared layout
-  unsigned* bar;            // [2] launches (parity of win, xw, counters), [4 + parity] grid-barrier arrivals
+  float4* dpart;            // [g][rowsG][P]: (max, sum exp, z of its token, its token) per CTA and set
+  unsigned long long* win;  // [2][g][rowsG]: packed (block key, token), 0 = none
+  unsigned* bar;            // [2] launches (parity of win and counters), [4 + parity] grid-barrier arrivals
   int* status;
 };
 
 __device__ __forceinline__ int group_ctas(int G, int nG, int g) { return (G - g + nG - 1) / nG; }
 
-// (key, block) as one unsigned 64-bit word whose unsigned order is: larger
-// key first, then the smaller block. Never 0.
-__device__ __forceinline__ unsigned long long pack_win(float key, int s) {
+// (block key, token drawn in the block) as one unsigned 64-bit word whose
+// unsigned order is: larger key first, then the smaller token (blocks are
+// token ranges, so the smaller block). Never 0.
+__device__ __forceinline__ unsigned long long pack_win(float key, int x) {
   uint32_t u = __float_as_uint(key);
   u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)s);
+  return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)x);
 }
-__device__ __forceinline__ int win_block(unsigned long long w) {
-  return w ? (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull)) : -1;
+__device__ __forceinline__ int win_token(unsigned long long w) {
+  return (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
 }
 
 // Offset (in bf16 elements) of the 16-byte piece ch of K-block kb of row m in
@@ -163,32 +163,10 @@ __device__ bool grid_sync(const TcParams& p, unsigned* ctr, unsigned target, boo
   return !*abort;
 }
 
-// Bounded wait for a released x_k flag (0 = not yet written). Returns 0 on
-// timeout or when another part of the launch raised an error.
-__device__ unsigned long long wait_flag(const unsigned long long* f, int* status) {
-  unsigned long long v = tc::ld_acquire_gpu(f);
-  if (v) return v;
-  const unsigned long long t0 = tc::globaltimer();
-  while ((v = tc::ld_acquire_gpu(f)) == 0ull) {
-    if (*(volatile int*)status != 0) return 0ull;
-    if (tc::globaltimer() - t0 > tc::kWaitNs) {
-      raise_status(status, DSPARK_ETIMEOUT);
-      return 0ull;
-    }
-    __nanosleep(32);
-  }
-  return v;
-}
-
 // The hidden half of every confidence logit, s_h[row] = w_h . h[row] (one CTA
-// per row of h), and the first A operand: the rows W1[anchor[b]] written into
-// each group's image by the CTAs of step 1 (row = b * gamma).
+// per row of h).
 __global__ void __launch_bounds__(128) k_draft_prologue(const float* __restrict__ h, const float* __restrict__ w,
-                                                        int H, float* __restrict__ s_h,
-                                                        const __nv_bfloat16* __restrict__ W1,
-                                                        const int32_t* __restrict__ anchor,
-                                                        __nv_bfloat16* __restrict__ aimg, int g, int V, int r,
-                                                        int* status) {
+                                                        int H, float* __restrict__ s_h) {
   __shared__ float red[4];
   const int row = blockIdx.x;
   if (H > 0) {
@@ -196,18 +174,6 @@ __global__ void __launch_bounds__(128) k_draft_prologue(const float* __restrict_
     if (threadIdx.x == 0) s_h[row] = d;
   } else if (threadIdx.x == 0) {
     s_h[row] = 0.f;
-  }
-  if (row % g == 0 && threadIdx.x < r / 8) {
-    const int b = row / g;
-    int x = anchor[b];
-    if (x < 0 || x >= V) {
-      if (threadIdx.x == 0) raise_status(status, DSPARK_ERANGE);
-      x = 0;
-    }
-    const int ci = threadIdx.x;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * r) + ci);
-    *reinterpret_cast<uint4*>(aimg + (size_t)(b / kTcRows) * kTcRows * r + a_piece(b % kTcRows, ci >> 3, ci & 7)) = v;
-    tc::fence_proxy_async_global();  // read by the draft kernel's bulk copies
   }
 }
 
@@ -230,9 +196,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto t_empty = [&](int i) { return bars + 8u * (2 * kNW + 2 * kNU + kNAcc + i); };
   const uint32_t a_full = bars + 8u * (2 * kNW + 2 * kNU + 2 * kNAcc);
   const uint32_t drain = a_full + 8u;
-  const uint32_t a_img = a_full + 16u;  // the bulk copy of the A image
-  auto acc_u = [&](int i) { return a_full + 24u + 8u * i; };
-  const uint32_t drain_c = a_full + 24u + 8u * kNAcc;
+  auto acc_u = [&](int i) { return a_full + 16u + 8u * i; };
+  const uint32_t drain_c = a_full + 16u + 8u * kNAcc;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
 
@@ -262,7 +227,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc::mbar_init(a_full, kEpiThreads / 32);
     tc::mbar_init(drain, 1);
-    tc::mbar_init(a_img, 1);
     for (int i = 0; i < kNAcc; ++i) tc::mbar_init(acc_u(i), 1);
     tc::mbar_init(drain_c, 1);
     *abort = 0;
@@ -430,7 +394,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool valid = b < p.B;
     const bool leader = warp == 2 && lane == 0;
     const __nv_bfloat16* W1 = reinterpret_cast<const __nv_bfloat16*>(p.W1);
-    __nv_bfloat16* img = p.aimg + (size_t)grp * kTcRows * p.r;
     // warp-uniform view of the abort word (the loops below hold warp collectives)
     auto aborted = [&]() { return __any_sync(0xFFFFFFFFu, *abort != 0); };
     // this launch's half of the winner and flag slots; the other half, last
@@ -439,40 +402,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned* gctr = p.bar + 4 + par;
     const size_t half = (size_t)p.g * p.rowsG;
     unsigned long long* win = p.win + par * half;
-    unsigned long long* xw = p.xw + par * half;
     {
       const int et = threadIdx.x - 64;
       if (c == 0 && et == 0) p.bar[4 + (par ^ 1)] = 0u;
-      for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads) {
+      for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads)
         p.win[(par ^ 1) * half + i] = 0ull;
-        p.xw[(par ^ 1) * half + i] = 0ull;
-      }
     }
     for (int k = 1; k <= p.g; ++k) {
-      // ---- A = W1[x_{k-1}]: the group's image, complete once every row's
-      // flag of step k-1 was seen (step 1: written by the prologue kernel)
+      // ---- A = W1[x_{k-1}], gathered by the epilogue warps into the swizzled
+      // operand. x_0 is the anchor; x_{k-1} is the token of the row's winning
+      // word of step k-1, final since that step's grid barrier. Every MMA of
+      // step k-1 has completed (this warp waited for all of its tiles), so the
+      // operand is free.
       if (!aborted()) {
-        if (leader) {
-          tc::fence_proxy_async_global();
-          const uint32_t bytes = (uint32_t)kTcRows * p.r * 2u;
-          tc::mbar_arrive_expect_tx(a_img, bytes);
-          tc::bulk_load(sA, img, bytes, a_img);
-        }
-        bool ok = tc::mbar_wait(a_img, (k - 1) & 1, abort);
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        if (!ok) {
-          if (lane == 0 && !*abort) {
-            raise_status(p.status, DSPARK_ETIMEOUT);
-            *abort = 1;
+        int x = 0;
+        if (valid) {
+          if (k == 1) {
+            x = p.anchor[b];
+          } else {
+            const unsigned long long wv = __ldcg(win + (size_t)(k - 2) * p.rowsG + b);
+            x = wv ? win_token(wv) : -1;
           }
-        } else if (lane == 0) {
-          tc::mbar_arrive(a_full);
+          if (x < 0 || x >= p.V) {
+            if (k == 1) {
+              raise_status(p.status, DSPARK_ERANGE);  // reported; the row drafts from token 0
+            } else {
+              raise_status(p.status, DSPARK_ENUMERIC);  // no block with finite mass
+              *abort = 1;
+            }
+            x = 0;
+          }
         }
+        // coalesced: the warp copies one row at a time (lane l takes the
+        // 16-byte piece l of the row); the two sets' warps of a lane quarter
+        // take its even and odd rows
+        uint4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int rl = 2 * i + set;  // row (lane) within the quarter
+          const int xr = __shfl_sync(0xFFFFFFFFu, x, rl);
+          const bool vr = __shfl_sync(0xFFFFFFFFu, valid, rl);
+          v[i] = (vr && lane < p.r / 8) ? __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)xr * p.r) + lane)
+                                        : make_uint4(0, 0, 0, 0);
+        }
+        if (lane < p.r / 8) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             sA + 2u * (uint32_t)a_piece(q * 32 + 2 * i + set, lane >> 3, lane & 7)),
+                         "r"(v[i].x), "r"(v[i].y), "r"(v[i].z), "r"(v[i].w)
+                         : "memory");
+        }
+        tc::fence_proxy_async_smem();  // read by tcgen05.mma
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(a_full);
       }
 
       // ---- this CTA's tiles; set s takes the blocks whose running index gb
       // has gb % kSets == s (so the sets share the tiles and the U ring evenly)
-      float M = -INFINITY, S = 0.f, bk = -INFINITY;
+      float M = -INFINITY, S = 0.f, bk = -INFINITY, bm = 0.f;
       int bs = kNoIdx;
       float zb[kBlk];  // z of this set's best block so far
 #pragma unroll
@@ -551,6 +539,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (key > bk) {  // this set sees its blocks in increasing order: ties keep the first
               bk = key;
               bs = t;
+              bm = mb;
 #pragma unroll
               for (int e = 0; e < kBlk; ++e) zb[e] = z[e];
             }
@@ -558,141 +547,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
-      // ---- publish this set's best (block key, block) and its (max, sum exp)
-      if (valid && !*abort) {
-        if (bs != kNoIdx && bk > -INFINITY) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bs));
-        // every set writes its slot every step (a set without blocks writes
-        // the neutral partial), so no entry of an earlier launch is combined
-        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] = make_float2(M, S);
-      }
-      grid_sync(p, gctr, (unsigned)(p.G * k), leader, abort);
-
-      // ---- the token draw inside the winning block, by the warp whose lane
-      // holds that block's z: lanes take tokens 2l, 2l + 1, then
-      // x_k = argmax_v (z_v + G_v); W1[x_k] goes into the group's A image and
-      // a released flag carries x_k (and z_{x_k} for the finalize)
-      if (!aborted()) {
-        const unsigned long long wv = valid ? __ldcg(win + (size_t)(k - 1) * p.rowsG + b) : 0ull;
-        if (valid && wv == 0ull) {
-          raise_status(p.status, DSPARK_ENUMERIC);
-          *abort = 1;
-        }
-        // all the warp's draws first (each lane keeps its own row's result),
-        // then every owner's W1 row is loaded at once, written to the image,
-        // and the flags released together
-        const unsigned owners = __ballot_sync(0xFFFFFFFFu, valid && bs != kNoIdx && win_block(wv) == bs);
-        int my_x = -1;
-        float my_zx = 0.f;
-        bool drawn = true;
-        for (unsigned om = owners; om;) {
-          const int src = __ffs(om) - 1;
-          om &= om - 1;
-          const int ob = __shfl_sync(0xFFFFFFFFu, b, src);
-          const int blk = __shfl_sync(0xFFFFFFFFu, bs, src);
-          float z0 = 0.f, z1 = 0.f;  // z of tokens 2 lane, 2 lane + 1, from lane src
+      // ---- the token inside this set's best block, by inverse CDF with one
+      // uniform u of the block: e_v = exp(z_v - max) in token order, and x is
+      // the first v whose running sum exceeds u times the total. Both passes
+      // form the same running sum, so for u < 1 some v always does.
+      int bx = -1;
+      float bzx = 0.f;
+      if (valid && bs != kNoIdx && !*abort) {
+        float tot = 0.f;
 #pragma unroll
-          for (int e = 0; e < kBlk; ++e) {
-            const float v = __shfl_sync(0xFFFFFFFFu, zb[e], src);
-            if ((e >> 1) == lane) {
-              if (e & 1) z1 = v;
-              else z0 = v;
-            }
-          }
-          const int v0 = blk * kBlk + 2 * lane;
-          if (k < p.g) {  // the drawn token's W1 row is needed next: start pulling the candidates into L2
+        for (int e = 0; e < kBlk; ++e) tot += __expf(zb[e] - bm);
+        const float thr = u01(p.rng.word(kDraftToken, b, k, bs)) * tot;
+        float cum = 0.f;
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-              if (v0 + e < p.V)
-                for (int o = 0; o < p.r * 2; o += 128)
-                  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(W1 + (size_t)(v0 + e) * p.r) + o));
-          }
-          const uint4 wd = p.rng.block4(kDraftToken, ob, k, v0);  // words of v0 .. v0 + 1
-          KeyIdx kt = key_none();
-          if (v0 < p.V) kt = KeyIdx{z0 + gumbel((lane & 1) ? wd.z : wd.x), v0};
-          if (v0 + 1 < p.V) kt = better(kt, KeyIdx{z1 + gumbel((lane & 1) ? wd.w : wd.y), v0 + 1});
-          kt = warp_best(kt);
-          if (kt.idx == kNoIdx) {
-            drawn = false;
-            break;
-          }
-          const int xl = kt.idx - blk * kBlk;
-          const float zx = __shfl_sync(0xFFFFFFFFu, (xl & 1) ? z1 : z0, xl >> 1);
-          if (lane == src) {
-            my_x = kt.idx;
-            my_zx = zx;
+        for (int e = 0; e < kBlk; ++e) {
+          cum += __expf(zb[e] - bm);
+          if (bx < 0 && cum > thr) {
+            bx = e;
+            bzx = zb[e];
           }
         }
-        if (!drawn) {
-          if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
+        if (bx < 0) {
+          raise_status(p.status, DSPARK_ENUMERIC);  // non-finite logits in the block
           *abort = 1;
         } else {
-          if (k < p.g) {
-            // up to four rows' loads in flight before their stores
-            for (unsigned om = owners; om;) {
-              int srcs[4], n = 0;
-              uint4 v[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                srcs[u] = om ? __ffs(om) - 1 : -1;
-                if (om) {
-                  om &= om - 1;
-                  ++n;
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int x = __shfl_sync(0xFFFFFFFFu, my_x, srcs[u] < 0 ? 0 : srcs[u]);
-                v[u] = (srcs[u] >= 0 && lane < p.r / 8) ? __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r) + lane)
-                                                        : make_uint4(0, 0, 0, 0);
-              }
-#pragma unroll
-              for (int u = 0; u < 4; ++u)
-                if (u < n && lane < p.r / 8)
-                  *reinterpret_cast<uint4*>(img + a_piece(q * 32 + srcs[u], lane >> 3, lane & 7)) = v[u];
-            }
-            tc::fence_proxy_async_global();  // the image is read by bulk copies
-          }
-          __syncwarp();
-          // each owner lane releases its row; the release covers the image
-          // pieces every lane wrote (ordered by the warp sync)
-          if ((owners >> lane) & 1u)
-            tc::st_release_gpu(xw + (size_t)(k - 1) * p.rowsG + b,
-                               ((unsigned long long)__float_as_uint(my_zx) << 32) | (unsigned)(my_x + 1));
-        }
-        // the next A image is complete once every row of the group has its flag
-        // (a lane polls its four rows together with relaxed loads; the fence
-        // after the last one orders the bulk copy of the image behind them)
-        if (k < p.g && warp == 2) {
-          const unsigned long long* f = xw + (size_t)(k - 1) * p.rowsG + grp * kTcRows;
-          unsigned pending = 0;
-#pragma unroll
-          for (int u = 0; u < kTcRows / 32; ++u)
-            if (grp * kTcRows + lane + 32 * u < p.B) pending |= 1u << u;
-          bool ok = true;
-          const unsigned long long t0 = tc::globaltimer();
-          while (pending) {
-            unsigned long long v[kTcRows / 32];
-#pragma unroll
-            for (int u = 0; u < kTcRows / 32; ++u) v[u] = (pending >> u) & 1u ? tc::ld_relaxed_gpu(f + lane + 32 * u) : 0ull;
-#pragma unroll
-            for (int u = 0; u < kTcRows / 32; ++u)
-              if (v[u]) pending &= ~(1u << u);
-            if (!pending) break;
-            if (*(volatile int*)p.status != 0) {
-              ok = false;
-              break;
-            }
-            if (tc::globaltimer() - t0 > tc::kWaitNs) {
-              raise_status(p.status, DSPARK_ETIMEOUT);
-              ok = false;
-              break;
-            }
-            __nanosleep(32);
-          }
-          if (__any_sync(0xFFFFFFFFu, !ok) && lane == 0) *abort = 1;
-          __threadfence();
+          bx += bs * kBlk;
         }
       }
+
+      // ---- publish this set's best (block key, token) and its partials
+      // (max, sum exp, z of its token, its token)
+      if (valid && !*abort) {
+        if (bx >= 0) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bx));
+        // every set writes its slot every step (a set without blocks writes
+        // the neutral partial), so no entry of an earlier launch is combined
+        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] =
+            make_float4(M, S, bzx, __int_as_float(bx));
+      }
+      // the winner words of step k are final once every CTA has passed here
+      grid_sync(p, gctr, (unsigned)(p.G * k), leader, abort);
     }
 
     // ---- after the last step: per (row, step), one warp combines the
@@ -703,27 +596,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
         const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
         const int Pr = kSets * group_ctas(p.G, p.nG, br / kTcRows);
-        unsigned long long fx = 0ull, fp = 0ull;
-        if (lane == 0) {
-          fx = wait_flag(xw + (size_t)kk * p.rowsG + br, p.status);
-          if (kk > 0) fp = wait_flag(xw + (size_t)(kk - 1) * p.rowsG + br, p.status);
-        }
-        fx = __shfl_sync(0xFFFFFFFFu, fx, 0);
-        fp = __shfl_sync(0xFFFFFFFFu, fp, 0);
-        if (fx == 0ull || (kk > 0 && fp == 0ull)) {
+        const unsigned long long wx = __ldcg(win + (size_t)kk * p.rowsG + br);
+        int xp = kk == 0 ? p.anchor[br] : win_token(__ldcg(win + (size_t)(kk - 1) * p.rowsG + br));
+        if (wx == 0ull) {
           if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
           continue;
         }
-        const int x = (int)(uint32_t)fx - 1;
-        const float zx = __uint_as_float((uint32_t)(fx >> 32));
-        int xp = kk == 0 ? p.anchor[br] : (int)(uint32_t)fp - 1;
-        if (xp < 0 || xp >= p.V) xp = 0;  // an anchor out of range was reported by the prologue
-        const float2* pr = p.dpart + ((size_t)kk * p.rowsG + br) * p.P;
-        float2 dd[kMaxPartLanes];
+        const int x = win_token(wx);
+        if (xp < 0 || xp >= p.V) xp = 0;  // an anchor out of range was reported at the step-1 gather
+        const float4* pr = p.dpart + ((size_t)kk * p.rowsG + br) * p.P;
+        float4 dd[kMaxPartLanes];
 #pragma unroll
         for (int u = 0; u < kMaxPartLanes; ++u) {
           const int i = lane + 32 * u;
-          dd[u] = i < Pr ? __ldcg(pr + i) : make_float2(-INFINITY, 0.f);
+          dd[u] = i < Pr ? __ldcg(pr + i) : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
         }
         float cd = 0.f;
         for (int ci = lane; ci < p.r / 8; ci += 32) {
@@ -738,10 +624,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         MS ms{-INFINITY, 0.f};
+        float zx = 0.f;
+        bool mine = false;  // this lane holds the winning set's partial
 #pragma unroll
-        for (int u = 0; u < kMaxPartLanes; ++u) ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
+        for (int u = 0; u < kMaxPartLanes; ++u) {
+          ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
+          if (__float_as_int(dd[u].w) == x) {
+            zx = dd[u].z;
+            mine = true;
+          }
+        }
         ms = warp_ms(ms);
         cd = warp_sum(cd);
+        const unsigned hold = __ballot_sync(0xFFFFFFFFu, mine);
+        zx = __shfl_sync(0xFFFFFFFFu, zx, hold ? __ffs(hold) - 1 : 0);
         if (lane == 0) {
           const size_t o = (size_t)br * p.g + kk;
           const float L2 = ms_log(ms);
@@ -749,7 +645,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.pd_tok[o] = expf(zx - L2);
           p.lse[o] = L2;
           const float cf = 1.f / (1.f + expf(-(p.s_h[o] + cd) / p.T[kk]));
-          if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
+          if (!isfinite(cf) || !hold) raise_status(p.status, DSPARK_ENUMERIC);
           p.conf[o] = cf;
         }
       }
@@ -875,14 +771,10 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.conf = a.conf;
   p.dpart = ws->s.dpart;
   p.win = ws->s.dwin;
-  p.xw = ws->s.dxw;
-  p.aimg = reinterpret_cast<__nv_bfloat16*>(ws->s.aimg);
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
 
-  k_draft_prologue<<<d.B * d.gamma, 128, 0, st>>>(a.h, a.w, d.H, ws->s.s_h,
-                                                 reinterpret_cast<const __nv_bfloat16*>(a.W1), a.anchor, p.aimg,
-                                                 d.gamma, d.V, d.r, ws->s.status);
+  k_draft_prologue<<<d.B * d.gamma, 128, 0, st>>>(a.h, a.w, d.H, ws->s.s_h);
   ++*launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

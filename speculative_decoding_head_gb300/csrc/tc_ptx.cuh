@@ -250,6 +250,9 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long
 __device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 }  // namespace tc
 }  // namespace dspark

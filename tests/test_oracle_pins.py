@@ -149,6 +149,58 @@ def test_sampler_block_and_token_levels_both_matter():
     assert oracle.sample(np.full(10, -np.inf))[0] == -1
 
 
+@pytest.mark.parametrize("V", [5, 64, 200])
+def test_draft_sampler_marginal_is_softmax(V):
+    rng = np.random.default_rng(100 + V)
+    logw = rng.normal(0, 1.5, V)
+    if V > 5:
+        logw[rng.choice(V, V // 10, replace=False)] = -np.inf   # zero-weight tokens
+    N = 60000
+    counts = np.zeros(V)
+    for b in range(N):
+        v, _ = oracle.sample_draft(logw, seed=13, rnd=4, b=b, j=2)
+        counts[v] += 1
+    p = np.exp(logw - special.logsumexp(logw))
+    assert chi2_p(counts, p) > 1e-4
+
+
+def test_draft_sampler_uniform_block_is_floor_of_u():
+    """Equal weights over one full block: the inverse CDF picks token
+    lo + floor(64 u), u being the uniform of that block (never on a boundary:
+    64 u = (2m + 1) 2^-18 is not an integer)."""
+    V = 192
+    logw = np.full(V, -np.inf)
+    logw[64:128] = 0.7
+    for b in range(500):
+        v, m = oracle.sample_draft(logw, seed=21, rnd=3, b=b, j=1)
+        u = oracle.uniform(21, 3, oracle.P_DRAFT_TOKEN, b, 1, 1)   # block 1
+        assert v == 64 + int(np.floor(64 * u))
+        frac = 64 * u - np.floor(64 * u)
+        assert abs(m - min(frac, 1 - frac) / 64) < 1e-12          # distance to the nearest boundary
+
+
+def test_draft_sampler_two_tokens_threshold():
+    """Weights 1 and 3 in one block: the first token iff u < 1/4."""
+    logw = np.array([0.0, np.log(3.0)])
+    seen = [0, 0]
+    for b in range(2000):
+        v, _ = oracle.sample_draft(logw, seed=8, rnd=0, b=b, j=5)
+        u = oracle.uniform(8, 0, oracle.P_DRAFT_TOKEN, b, 5, 0)
+        assert v == (0 if u < 0.25 else 1)
+        seen[v] += 1
+    assert min(seen) > 0
+
+
+def test_draft_sampler_block_level_and_empty():
+    V = 256
+    logw = np.full(V, -np.inf)
+    logw[130:140] = np.log(np.arange(1, 11, dtype=float))
+    for b in range(500):
+        v, _ = oracle.sample_draft(logw, seed=5, b=b)
+        assert 130 <= v < 140
+    assert oracle.sample_draft(np.full(10, -np.inf))[0] == -1
+
+
 # ------------------------------------------------------------------ helpers
 def token_independent_round(qs, ps, N, seed=7, ell=None, tokens=None, rnd=0):
     """Draft + verify with zero Markov weights: position k drafts from qs[k-1],
