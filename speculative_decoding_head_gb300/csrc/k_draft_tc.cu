@@ -75,6 +75,7 @@ constexpr int kAccCols = kTileBlocks * kBlk; // 128 columns per accumulator
 constexpr int kNAcc = 4;                     // accumulators: the MMA runs up to three tiles ahead
 constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
+constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
 
 static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
@@ -510,24 +511,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               for (int e = 0; e < kBlk; ++e)
                 if (v0 + e >= p.V) z[e] = -INFINITY;
             }
-            // block max and sum of exponentials as 8-way trees (short chains)
+            // block max (three-input max, 8 chains) and sum of exponentials
+            // e^(z - mb) = 2^(z log2e - mb log2e) on fp32 pairs (FFMA2, MUFU
+            // ex2, FADD2 into 4 pair accumulators)
             float m8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(z[e], z[e + 8]);
+            for (int c8 = 0; c8 < 8; ++c8) {
+              m8[c8] = tc::max3f(z[8 * c8], z[8 * c8 + 1], z[8 * c8 + 2]);
+              m8[c8] = tc::max3f(m8[c8], z[8 * c8 + 3], z[8 * c8 + 4]);
+              m8[c8] = tc::max3f(m8[c8], z[8 * c8 + 5], z[8 * c8 + 6]);
+              m8[c8] = fmaxf(m8[c8], z[8 * c8 + 7]);
+            }
+            const float mb = tc::max3f(tc::max3f(m8[0], m8[1], m8[2]), tc::max3f(m8[3], m8[4], m8[5]),
+                                       fmaxf(m8[6], m8[7]));
+            const unsigned long long l2e = tc::f2pack(kLog2e, kLog2e);
+            const unsigned long long nml = tc::f2pack(-mb * kLog2e, -mb * kLog2e);
+            unsigned long long acc[2];
 #pragma unroll
-            for (int i = 16; i < kBlk; i += 8)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) m8[e] = fmaxf(m8[e], z[i + e]);
-            const float mb = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            float s8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s8[e] = __expf(z[e] - mb);
-#pragma unroll
-            for (int i = 8; i < kBlk; i += 8)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) s8[e] += __expf(z[i + e] - mb);
-            const float sb = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+            for (int i = 0; i < kBlk / 2; ++i) {
+              float a0, a1;
+              tc::f2unpack(tc::fma2(tc::f2pack(z[2 * i], z[2 * i + 1]), l2e, nml), a0, a1);
+              const unsigned long long e2 = tc::f2pack(tc::ex2_ftz(a0), tc::ex2_ftz(a1));
+              acc[i & 1] = i < 2 ? e2 : tc::add2(acc[i & 1], e2);
+            }
+            float sl, sh;
+            tc::f2unpack(tc::add2(acc[0], acc[1]), sl, sh);
+            const float sb = sl + sh;
             const float lm = mb + logf(sb);
             if (mb > M) {
               S = S * __expf(M - mb) + sb;
@@ -549,29 +558,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       // ---- the token inside this set's best block, by inverse CDF with one
       // uniform u of the block: e_v = exp(z_v - max) in token order, and x is
-      // the first v whose running sum exceeds u times the total. Both passes
-      // form the same running sum, so for u < 1 some v always does.
+      // the first v whose running sum exceeds u times the total. The running
+      // sum is formed chunk by chunk (8 tokens each): s_c = e_8c + .. + e_8c+7,
+      // P_c+1 = P_c + s_c; the chunk is the first with P_c+1 > u P_8, and the
+      // token the first i in it with P_c + (e_8c + .. + e_8c+i) > u P_8. The
+      // last i of the chunk reproduces P_c+1 bit for bit, so one qualifies.
       int bx = -1;
       float bzx = 0.f;
       if (valid && bs != kNoIdx && !*abort) {
-        float tot = 0.f;
+        float s8[8];
 #pragma unroll
-        for (int e = 0; e < kBlk; ++e) tot += __expf(zb[e] - bm);
-        const float thr = u01(p.rng.word(kDraftToken, b, k, bs)) * tot;
-        float cum = 0.f;
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float a = __expf(zb[8 * c8] - bm);
 #pragma unroll
-        for (int e = 0; e < kBlk; ++e) {
-          cum += __expf(zb[e] - bm);
-          if (bx < 0 && cum > thr) {
-            bx = e;
-            bzx = zb[e];
+          for (int i = 1; i < 8; ++i) a += __expf(zb[8 * c8 + i] - bm);
+          s8[c8] = a;
+        }
+        float P[9];
+        P[0] = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) P[c8 + 1] = P[c8] + s8[c8];
+        const float thr = u01(p.rng.word(kDraftToken, b, k, bs)) * P[8];
+        int cs = 7;
+#pragma unroll
+        for (int c8 = 6; c8 >= 0; --c8)
+          if (P[c8 + 1] > thr) cs = c8;
+        float base = P[7], zc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) zc[i] = zb[56 + i];
+#pragma unroll
+        for (int c8 = 6; c8 >= 0; --c8)
+          if (cs == c8) {
+            base = P[c8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) zc[i] = zb[8 * c8 + i];
+          }
+        float a = 0.f;
+        int xi = -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          a += __expf(zc[i] - bm);
+          if (xi < 0 && base + a > thr) {
+            xi = i;
+            bzx = zc[i];
           }
         }
-        if (bx < 0) {
+        if (xi < 0) {
           raise_status(p.status, DSPARK_ENUMERIC);  // non-finite logits in the block
           *abort = 1;
         } else {
-          bx += bs * kBlk;
+          bx = bs * kBlk + 8 * cs + xi;
         }
       }
 
