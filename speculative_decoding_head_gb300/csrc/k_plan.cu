@@ -25,17 +25,21 @@
 namespace dspark {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanMaxCand = 8192;  // B * gamma supported by the one-CTA planner
 
-// Padded candidate count: a power of two, at least one warp's 64-element chunk.
+constexpr int kRankMaxChunks = 16;  // up to this many 64-element chunks: rank merge, else bitonic
+
+// Padded candidate count: whole 64-element chunks; a power of two when the
+// bitonic network sorts them (more than kRankMaxChunks chunks).
 __host__ __device__ inline int plan_mp(int M) {
+  const int c = (M + 63) / 64 * 64;
+  if (c <= 64 * kRankMaxChunks) return c < 64 ? 64 : c;
   int p = 64;
   while (p < M) p <<= 1;
   return p;
 }
 
 size_t plan_smem_bytes(const dspark_dims& d) {
-  const int Mp = plan_mp(d.B * d.gamma);
+  const int Mp = d.mode == DSPARK_STATIC ? 0 : plan_mp(d.B * d.gamma);  // static: counts only
   return (size_t)Mp * (sizeof(unsigned long long) + sizeof(unsigned) + sizeof(double)) +
          sizeof(int) * (size_t)(d.B + 1) + 64;
 }
@@ -57,7 +61,7 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
   const int M = B * g;
   for (int i = threadIdx.x; i < Mp; i += blockDim.x) {
     sm.key[i] = 0ull;
-    sm.id[i] = 0xFFFFFFFFu;  // padding sorts last
+    sm.id[i] = (unsigned)i;  // padding (i >= M) sorts after every candidate, ids stay distinct
   }
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
@@ -78,7 +82,9 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
   // stride <= 32 is an in-lane swap or a shuffle with no block barrier; only
   // strides >= 64 go through shared memory, one barrier each.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  auto reg_stages = [&](int size_lo, int size_hi, int s_hi) {
+  // flat: the 64-wide stage leaves every chunk in "before" order (for the rank
+  // merge) instead of alternating directions (for the next bitonic stage)
+  auto reg_stages = [&](int size_lo, int size_hi, int s_hi, bool flat) {
     for (int c = warp; c < Mp / 64; c += nwarps) {
       const int e0 = 64 * c + lane, e1 = e0 + 32;
       unsigned long long k0 = sm.key[e0], k1 = sm.key[e1];
@@ -86,7 +92,7 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
       for (int size = size_lo; size <= size_hi; size <<= 1) {
         for (int st = min(size >> 1, s_hi); st > 0; st >>= 1) {
           if (st == 32) {  // e0 and e1 pair up inside the lane; e0 is the lower index
-            const bool up = (e0 & size) == 0;
+            const bool up = (e0 & size) == 0 || (flat && size == 64);
             if (before(k0, i0, k1, i1) != up) {
               const unsigned long long tk = k0;
               k0 = k1;
@@ -99,8 +105,10 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
             const unsigned long long p0 = __shfl_xor_sync(0xFFFFFFFFu, k0, st), p1 = __shfl_xor_sync(0xFFFFFFFFu, k1, st);
             const unsigned q0 = __shfl_xor_sync(0xFFFFFFFFu, i0, st), q1 = __shfl_xor_sync(0xFFFFFFFFu, i1, st);
             // keep the element that goes first iff (this index is the lower one) == up
-            const bool keep0 = ((e0 & st) == 0) == ((e0 & size) == 0);
-            const bool keep1 = ((e1 & st) == 0) == ((e1 & size) == 0);
+            const bool up0 = (e0 & size) == 0 || (flat && size == 64);
+            const bool up1 = (e1 & size) == 0 || (flat && size == 64);
+            const bool keep0 = ((e0 & st) == 0) == up0;
+            const bool keep1 = ((e1 & st) == 0) == up1;
             if (before(k0, i0, p0, q0) != keep0) {
               k0 = p0;
               i0 = q0;
@@ -119,7 +127,49 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
     }
     __syncthreads();
   };
-  reg_stages(2, 64, 32);
+  const int nch = Mp / 64;
+  reg_stages(2, 64, 32, nch <= kRankMaxChunks);
+  if (nch <= kRankMaxChunks) {
+    // Every element's place in the sorted whole: its index in its own sorted
+    // chunk plus, for every other chunk, how many of that chunk's elements go
+    // before it (a branchless binary search over the 64 sorted entries). The
+    // order is strict (ids are distinct), so the places are a permutation.
+    constexpr int kPer = 64 * kRankMaxChunks / kPlanThreads;
+    unsigned long long kx[kPer];
+    unsigned ix[kPer];
+    int rk[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = threadIdx.x + u * blockDim.x;
+      rk[u] = -1;
+      if (e < Mp) {
+        kx[u] = sm.key[e];
+        ix[u] = sm.id[e];
+        int r = e & 63;
+#pragma unroll 4
+        for (int c2 = 0; c2 < nch; ++c2) {
+          const unsigned long long* ck = sm.key + 64 * c2;
+          const unsigned* ci = sm.id + 64 * c2;
+          int q = 0;
+#pragma unroll
+          for (int st = 32; st > 0; st >>= 1)
+            if (before(ck[q + st - 1], ci[q + st - 1], kx[u], ix[u])) q += st;
+          if (q == 63 && before(ck[63], ci[63], kx[u], ix[u])) q = 64;
+          r += c2 == (e >> 6) ? 0 : q;  // own chunk: e & 63 above
+        }
+        rk[u] = r;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (rk[u] >= 0) {
+        sm.key[rk[u]] = kx[u];
+        sm.id[rk[u]] = ix[u];
+      }
+    __syncthreads();
+    return;
+  }
   for (int size = 128; size <= Mp; size <<= 1) {
     for (int stride = size >> 1; stride >= 64; stride >>= 1) {
       for (int t = threadIdx.x; t < Mp / 2; t += blockDim.x) {
@@ -138,44 +188,41 @@ __device__ void sort_candidates(const float* c, int B, int g, int Mp, PlanSmem s
       }
       __syncthreads();
     }
-    reg_stages(size, size, 32);
+    reg_stages(size, size, 32, false);
   }
 }
 
-// pre[m] = sum_{i<m} a_(i) for m = 0..Mp-1 (padding contributes 0)
-__device__ void prefix_sums(int Mp, PlanSmem sm, double* warp_tot) {
-  const int T = blockDim.x;
-  const int per = (Mp + T - 1) / T;
-  const int lo = threadIdx.x * per;
-  double loc = 0.0;
-  for (int i = lo; i < lo + per && i < Mp; ++i) loc += __longlong_as_double((long long)sm.key[i]);
-  // exclusive scan of the per-thread totals
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = loc;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
+// pre[m] = sum_{i<m} a_(i) for m = 0..Mp-1 (padding contributes 0). fp64
+// adds are scarce on this part, so the sum runs in 64-bit fixed point: each
+// a in [0, 1] is rounded to a multiple of 2^-50 (error <= 2^-51 each), the
+// integers are summed exactly (total < 2^63 for up to 8192 candidates), and
+// each prefix goes back to fp64. The absolute error of pre[m] is below
+// m 2^-51 < 4e-12, relative to tau = B + pre >= 1.
+__device__ void prefix_sums(int Mp, PlanSmem sm) {
+  unsigned long long* fx = reinterpret_cast<unsigned long long*>(sm.pre);
+  for (int i = threadIdx.x; i < Mp; i += blockDim.x)
+    fx[i] = __double2ull_rn(__longlong_as_double((long long)sm.key[i]) * 0x1p50);
   __syncthreads();
-  if (warp == 0) {
-    const int nw = T >> 5;
-    double x = lane < nw ? warp_tot[lane] : 0.0;
-    double inc = x;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (Mp + 31) / 32, lo = lane * per, hi = min(lo + per, Mp);
+    unsigned long long loc = 0ull;
+    for (int i = lo; i < hi; ++i) loc += fx[i];
+    unsigned long long incl = loc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-      if (lane >= o) inc += y;
+      const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
     }
-    if (lane < nw) warp_tot[lane] = inc - x;  // exclusive
+    unsigned long long run = incl - loc;
+    for (int i = lo; i < hi; ++i) {
+      const unsigned long long v = fx[i];
+      fx[i] = run;
+      run += v;
+    }
   }
   __syncthreads();
-  double run = warp_tot[warp] + (incl - loc);
-  for (int i = lo; i < lo + per && i < Mp; ++i) {
-    sm.pre[i] = run;
-    run += __longlong_as_double((long long)sm.key[i]);
-  }
+  for (int i = threadIdx.x; i < Mp; i += blockDim.x) sm.pre[i] = __ull2double_rn(fx[i]) * 0x1p-50;
   __syncthreads();
 }
 
@@ -188,14 +235,13 @@ __global__ void __launch_bounds__(kPlanThreads)
            float* __restrict__ ring, uint32_t* __restrict__ plan_round, int32_t* __restrict__ lengths,
            int32_t* __restrict__ row_off, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ double warp_tot[32];
   __shared__ double warp_bv[32];
   __shared__ int warp_bm[32];
   __shared__ int warp_int[32];
   __shared__ int s_cut;
   __shared__ int s_bestm;
   const int M = B * g;
-  const int Mp = plan_mp(M);
+  const int Mp = mode == DSPARK_STATIC ? 0 : plan_mp(M);  // the layout of plan_smem_bytes
   PlanSmem sm;
   sm.key = reinterpret_cast<unsigned long long*>(smem_raw);
   sm.pre = reinterpret_cast<double*>(sm.key + Mp);
@@ -221,7 +267,7 @@ __global__ void __launch_bounds__(kPlanThreads)
         // capacity from the confidences of round t - lag: full-path argmax
         const float* clag = ring + (size_t)((t - lag) % depth) * M;
         sort_candidates(clag, B, g, Mp, sm, status);
-        prefix_sums(Mp, sm, warp_tot);
+        prefix_sums(Mp, sm);
         // first maximum of Theta_m, m = 0..M
         double bv = -1.0;
         int bm = 0x7FFFFFFF;
@@ -271,7 +317,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     // current candidates in admission order
     sort_candidates(cnow, B, g, Mp, sm, status);
     if (!lagged) {
-      prefix_sums(Mp, sm, warp_tot);
+      prefix_sums(Mp, sm);
       if (threadIdx.x == 0) s_cut = M;
       __syncthreads();
       // Algorithm 1: stop at the first m whose admission does not raise

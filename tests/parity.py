@@ -29,9 +29,10 @@ from speculative_decoding_head_gb300 import workloads as wlmod
 
 RTOL = 1e-4
 # Planner flags. With identical fp32 confidences both sides form the same fp64
-# survival products and sort order; only the prefix sums are associated
-# differently (relative error below M * 2^-53 < 1e-12 for M <= 8192), so a
-# decision is flagged only when its relative Theta gap is below 1e-11.
+# survival products and sort order; only the prefix sums differ (the GPU sums
+# them in 2^-50 fixed point: absolute error below M * 2^-51 < 4e-12 for
+# M <= 8192, against tau >= 1), so a decision is flagged only when its
+# relative Theta gap is below 1e-11.
 PLAN_THETA_TOL_SAME_INPUT = 1e-11
 # When each side computes its own confidences (fp32 on the GPU, fp64 rounded to
 # fp32 in the oracle) they differ by ~1e-6 relative, survival products by up
