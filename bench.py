@@ -36,9 +36,9 @@ METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofli
 # the ncu capture summarised in profiles/draft_tc_prod.md, and a hash of the
 # kernel source it was taken on; the roofline's "traffic" is reported only
 # while the source is unchanged.
-DRAFT_TRAFFIC = {"sha256": "1de0532ea374c07b04b9338d084f3d60ac4712384cf5c6bfddf66bd0a0c2d580",
-                 "bytes": 418118912 + 3596032}
-NORTH_STAR_BW = 8000.0   # GB/s, the roofline constant the metric is quoted against
+DRAFT_TRAFFIC = {"sha256": "bd5d665e0fc5af505efbf446af50c2e5fb4c7dde34f1ec01b3ea0b351d075af6",
+                 "bytes": 402673664 + 3516928}
+QUOTED_HBM_GBS = 8000.0   # GB/s, the roofline constant the metric is quoted against
 
 
 def parse():
@@ -405,7 +405,7 @@ def main():
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(wl, sum_len),
             "hbm_roofline": {"alg_bytes_per_round": bts["alg"], "alg_bytes_w2_once": bts["alg_w2_once"],
-                             "frac_of_8TBs": bts["alg"] / t_round / 1e9 / NORTH_STAR_BW,
+                             "frac_of_8TBs": bts["alg"] / t_round / 1e9 / QUOTED_HBM_GBS,
                              "frac_of_measured": bts["alg"] / t_round / 1e9 / peak,
                              "frac_w2_once_of_measured": bts["alg_w2_once"] / t_round / 1e9 / peak},
             "verified_positions_per_s": value * sum_len,

@@ -75,7 +75,6 @@ constexpr int kAccCols = kTileBlocks * kBlk; // 128 columns per accumulator
 constexpr int kNAcc = 4;                     // accumulators: the MMA runs up to three tiles ahead
 constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
 
 static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
@@ -524,8 +523,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             const float mb = tc::max3f(tc::max3f(m8[0], m8[1], m8[2]), tc::max3f(m8[3], m8[4], m8[5]),
                                        fmaxf(m8[6], m8[7]));
-            const unsigned long long l2e = tc::f2pack(kLog2e, kLog2e);
-            const unsigned long long nml = tc::f2pack(-mb * kLog2e, -mb * kLog2e);
+            const unsigned long long l2e = tc::f2pack(tc::kLog2e, tc::kLog2e);
+            const unsigned long long nml = tc::f2pack(-mb * tc::kLog2e, -mb * tc::kLog2e);
             unsigned long long acc[2];
 #pragma unroll
             for (int i = 0; i < kBlk / 2; ++i) {

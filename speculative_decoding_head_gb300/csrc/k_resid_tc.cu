@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   int* col_b = reinterpret_cast<int*>(smem + L.col);
   int* col_n = col_b + kRN;
   int* col_row = col_n + kRN;
-  float* col_lsed = reinterpret_cast<float*>(col_row + kRN);
-  float* col_lset = col_lsed + kRN;
+  float* col_nld = reinterpret_cast<float*>(col_row + kRN);  // -lse_d log2(e)
+  float* col_nlt = col_nld + kRN;                              // -lse_t log2(e)
   float* part = reinterpret_cast<float*>(smem + L.part);   // [4][128]
   float* best_key = reinterpret_cast<float*>(smem + L.best);
   int* best_blk = reinterpret_cast<int*>(best_key + kRN);
@@ -311,8 +311,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
           col_b[et] = b;
           col_n[et] = n;
           col_row[et] = p.vrow[b];
-          col_lsed[et] = p.lse[(size_t)b * p.g + n];
-          col_lset[et] = p.vlset[b];
+          col_nld[et] = -p.lse[(size_t)b * p.g + n] * tc::kLog2e;
+          col_nlt[et] = -p.vlset[b] * tc::kLog2e;
           if (x < 0 || x >= p.V) {
             raise_status(p.status, DSPARK_ERANGE);
             x = 0;
@@ -387,7 +387,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             for (int j = 0; j < 16; ++j) {
               const int col = half * 16 + j;
               const int cl = min(col, ncols - 1);
-              const float w = fmaxf(0.f, __expf(pp[j] - col_lset[cl]) - __expf(a[j] + uu[j] - col_lsed[cl]));
+              // p_t - p_d = 2^(P log2e - lse_t log2e) - 2^(z_d log2e - lse_d log2e), z_d = D + U
+              const float w = fmaxf(0.f, tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[cl])) -
+                                             tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[cl])));
               a[j] = (col < ncols && v < p.V) ? w : 0.f;
             }
             const float s = transpose_sum16(a);  // this warp's 32 entries, request 16 half + (lane & 15)

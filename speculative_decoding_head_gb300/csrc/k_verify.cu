@@ -238,14 +238,32 @@ __global__ void __launch_bounds__(kBulkThreads)
       float4 x[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = blk4[(i + tid) & 15];  // rotated: conflict-free
-      float m = -INFINITY;
+      // block max (three-input max, 4 chains) and sum of e^(x - m) =
+      // 2^(x log2e - m log2e) on fp32 pairs (FFMA2, MUFU ex2, FADD2)
+      float m4[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
+      for (int i = 0; i < 4; ++i) m4[i] = tc::max3f(x[i].x, x[i].y, tc::max3f(x[i].z, x[i].w, -INFINITY));
+#pragma unroll
+      for (int i = 4; i < 16; ++i) m4[i & 3] = tc::max3f(tc::max3f(m4[i & 3], x[i].x, x[i].y), x[i].z, x[i].w);
+      const float m = tc::max3f(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
       float t = 0.f;
       if (m != -INFINITY) {
+        const unsigned long long l2e = tc::f2pack(tc::kLog2e, tc::kLog2e);
+        const unsigned long long nml = tc::f2pack(-m * tc::kLog2e, -m * tc::kLog2e);
+        unsigned long long acc0 = 0ull, acc1 = 0ull;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          t += (__expf(x[i].x - m) + __expf(x[i].y - m)) + (__expf(x[i].z - m) + __expf(x[i].w - m));
+        for (int i = 0; i < 16; ++i) {
+          float a0, a1, a2, a3;
+          tc::f2unpack(tc::fma2(tc::f2pack(x[i].x, x[i].y), l2e, nml), a0, a1);
+          tc::f2unpack(tc::fma2(tc::f2pack(x[i].z, x[i].w), l2e, nml), a2, a3);
+          const unsigned long long e01 = tc::f2pack(tc::ex2_ftz(a0), tc::ex2_ftz(a1));
+          const unsigned long long e23 = tc::f2pack(tc::ex2_ftz(a2), tc::ex2_ftz(a3));
+          acc0 = i == 0 ? e01 : tc::add2(acc0, e01);
+          acc1 = i == 0 ? e23 : tc::add2(acc1, e23);
+        }
+        float s0, s1;
+        tc::f2unpack(tc::add2(acc0, acc1), s0, s1);
+        t = s0 + s1;
         const int q = (int)(u / nblk), sblk = (int)(u - (long long)q * nblk);
         if (q != q_cur) {
           flush();

@@ -70,6 +70,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------- fp32 arithmetic
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2 e)
 // Three-input maximum (NaN inputs are ignored, as by fmaxf).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
