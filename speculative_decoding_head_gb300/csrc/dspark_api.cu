@@ -208,7 +208,7 @@ dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1,
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
   cudaError_t e;
   if (ws->use_tc && ws->geo.tc_ok) {
-    e = launch_draft_tc(ws, a, st, &launches);  // its prologue computes the hidden half of c_k
+    e = launch_draft_tc(ws, a, st, &launches);  // one launch; it forms c_k from h itself
   } else {
     e = launch_conf_hidden(ws, h, w, st, &launches);
     if (e == cudaSuccess) e = launch_draft_simt(ws, a, st, &launches);

@@ -6,9 +6,7 @@
 // and eq. (7): c_k = sigma((w^T [h_k; W1[x_{k-1}]]) / T_k) (the temperature is
 // the STS sigmoid(raw / T) of the zdszero.github.io "spec_dspark" page).
 //
-// Two launches. k_draft_prologue computes the hidden half of every confidence
-// logit.
-// k_draft_tc, one cooperative launch, runs all gamma steps. Each CTA (one per
+// One cooperative launch, k_draft_tc, runs all gamma steps. Each CTA (one per
 // SM) owns a contiguous range of 64-token sampler blocks of one 128-row group,
 // taken two at a time as MMA tiles:
 //   warp 0      TMA producer of W2, in chunks of 64 K rows x 128 tokens (two
@@ -42,7 +40,8 @@
 // keep prefetching the next step's tiles meanwhile (they do not depend on
 // the drafted token). Log-sum-exps, probabilities of the drawn tokens and
 // confidences are off that chain: per-set partials (max, sum exp) are kept
-// per step and combined after the last step, one warp per (row, step).
+// per step and combined after the last step, one warp per (row, step), which
+// also forms the confidence logit w^T [h_k; W1[x_{k-1}]] from h and W1.
 //
 // Every wait is bounded (tc_ptx.cuh); a timeout sets DSPARK_ETIMEOUT, every
 // role leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
@@ -104,7 +103,7 @@ struct TcParams {
   const void* W1;
   const float* w;
   const float* T;
-  const float* s_h;
+  const float* h;           // [B*g][H] hidden states (the hidden half of each confidence logit)
   int32_t* tokens;
   float* pd_tok;
   float* lse;
@@ -161,20 +160,6 @@ __device__ bool grid_sync(const TcParams& p, unsigned* ctr, unsigned target, boo
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
   return !*abort;
-}
-
-// The hidden half of every confidence logit, s_h[row] = w_h . h[row] (one CTA
-// per row of h).
-__global__ void __launch_bounds__(128) k_draft_prologue(const float* __restrict__ h, const float* __restrict__ w,
-                                                        int H, float* __restrict__ s_h) {
-  __shared__ float red[4];
-  const int row = blockIdx.x;
-  if (H > 0) {
-    const float d = hidden_dot128(h + (size_t)row * H, w, H, red);
-    if (threadIdx.x == 0) s_h[row] = d;
-  } else if (threadIdx.x == 0) {
-    s_h[row] = 0.f;
-  }
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -646,7 +631,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int i = lane + 32 * u;
           dd[u] = i < Pr ? __ldcg(pr + i) : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
         }
+        // w^T [h_k; W1[x_{k-1}]]: the hidden half (H floats, 16-byte loads
+        // when H allows, ten per lane in flight), then the W1 half
         float cd = 0.f;
+        const float* hr = p.h + ((size_t)br * p.g + kk) * p.H;
+        if ((p.H & 3) == 0) {
+          const float4* h4 = reinterpret_cast<const float4*>(hr);
+          const float4* w4 = reinterpret_cast<const float4*>(p.w);
+          for (int i0 = lane; i0 < p.H / 4; i0 += 10 * 32) {
+            float4 a[10], b4[10];
+#pragma unroll
+            for (int u = 0; u < 10; ++u) {
+              const int i = i0 + 32 * u;
+              a[u] = i < p.H / 4 ? __ldcs(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);  // h is read once
+              b4[u] = i < p.H / 4 ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 10; ++u) {
+              cd = fmaf(a[u].x, b4[u].x, cd);
+              cd = fmaf(a[u].y, b4[u].y, cd);
+              cd = fmaf(a[u].z, b4[u].z, cd);
+              cd = fmaf(a[u].w, b4[u].w, cd);
+            }
+          }
+        } else {
+          for (int i = lane; i < p.H; i += 32) cd = fmaf(__ldcs(hr + i), __ldg(p.w + i), cd);
+        }
         for (int ci = lane; ci < p.r / 8; ci += 32) {
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)xp * p.r) + ci);
           const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v);
@@ -679,7 +689,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.tokens[o] = x;
           p.pd_tok[o] = expf(zx - L2);
           p.lse[o] = L2;
-          const float cf = 1.f / (1.f + expf(-(p.s_h[o] + cd) / p.T[kk]));
+          const float cf = 1.f / (1.f + expf(-cd / p.T[kk]));
           if (!isfinite(cf) || !hold) raise_status(p.status, DSPARK_ENUMERIC);
           p.conf[o] = cf;
         }
@@ -799,7 +809,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.W1 = a.W1;
   p.w = a.w;
   p.T = a.T;
-  p.s_h = ws->s.s_h;
+  p.h = a.h;
   p.tokens = a.tokens;
   p.pd_tok = a.pd_tok;
   p.lse = a.lse;
@@ -809,11 +819,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
 
-  k_draft_prologue<<<d.B * d.gamma, 128, 0, st>>>(a.h, a.w, d.H, ws->s.s_h);
-  ++*launches;
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
+  cudaError_t e;
   const TcSmem L = TcSmem::make(d.r);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));

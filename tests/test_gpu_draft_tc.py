@@ -43,7 +43,7 @@ def _check(wl, rnd=0, reqs=None):
     inp = make_inputs(wl, with_target=False)
     dev, npi = to_device(inp), np_inputs(inp)
     tc, ws = _draft(wl, dev, "tcgen05", wl.seed, rnd)
-    assert ws.last_launches == 2          # hidden-state dot + one persistent kernel
+    assert ws.last_launches == 1          # one persistent kernel
     simt, _ = _draft(wl, dev, "simt", wl.seed, rnd)
     reqs = range(wl.B) if reqs is None else reqs
     od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed, rnd,
