@@ -11,9 +11,9 @@
 // taken two at a time as MMA tiles:
 //   warp 0      TMA producer of W2, in chunks of 64 K rows x 128 tokens (two
 //               128-byte-swizzled boxes; L2 evict_last: W2 is reused by every
-//               step), into a ring of 4 stages;
+//               step), into a ring of 6 stages;
 //   warp 10     TMA producer of U, one block [128 x 64] fp32 at a time
-//               (evict_first: streamed once), into a ring of 3 stages (two
+//               (evict_first: streamed once), into a ring of 2 stages (two
 //               producers, so that neither stream waits behind the other);
 //   warp 1      allocates all 512 TMEM columns and issues tcgen05.mma with
 //               M = 128 rows, N = 64 x (blocks of the tile), K = r in steps of
@@ -66,8 +66,8 @@ constexpr int kTileBlocks = 2;      // MMA N = 64 x blocks of the tile
 constexpr int kKc = 64;             // K rows of W2 per ring stage
 constexpr int kW2Box = kKc * 128;   // 8 KB: 64 K rows x 64 tokens (128-byte rows)
 constexpr int kW2Stage = kTileBlocks * kW2Box;  // 16 KB
-constexpr int kNW = 4;              // W2 ring depth (K chunks)
-constexpr int kNU = 3;              // U ring depth (blocks)
+constexpr int kNW = 6;              // W2 ring depth (K chunks): a tile and a half
+constexpr int kNU = 2;              // U ring depth (blocks)
 constexpr int kUStage = kTcRows * kBlk * 4;  // 32 KB: two 128 x 32 fp32 boxes
 constexpr int kUBox = kTcRows * 32 * 4;      // 16 KB
 constexpr int kAccCols = kTileBlocks * kBlk; // 128 columns per accumulator
