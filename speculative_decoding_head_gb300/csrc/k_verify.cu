@@ -163,7 +163,8 @@ constexpr int kBulkMaxSlots = 8;
 int sweep_bulk_max_slots() { return kBulkMaxSlots; }
 
 size_t sweep_bulk_smem_bytes() {
-  return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 128;
+  return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 64 +
+         (size_t)kBulkMaxSlots * 16;
 }
 
 __global__ void __launch_bounds__(kBulkThreads)
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kBulkThreads)
   float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
                                                (size_t)kBulkMaxSlots * kBulkThreads * 16);
+  int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [kBulkMaxSlots]
   const int R = min(max(row_off[B], 0), Rmax);
   const long long T = (long long)R * nblk;
   if (T == 0) return;
@@ -190,13 +192,6 @@ __global__ void __launch_bounds__(kBulkThreads)
   const int nchunks = (int)((hi - lo + kBulkUnits - 1) / kBulkUnits);
   const uint32_t bar0 = tc::smem_u32(bars);
   const uint32_t st0 = tc::smem_u32(stage);
-  for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
-    slot[i] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
-  if (tid == 0) {
-    for (int i = 0; i < kBulkStages; ++i) tc::mbar_init(bar0 + 8u * i, 1);
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
   auto issue = [&](int ch) {
     const long long u = lo + (long long)ch * kBulkUnits;
     const int units = (int)min((long long)kBulkUnits, hi - u);
@@ -206,8 +201,21 @@ __global__ void __launch_bounds__(kBulkThreads)
     tc::bulk_load(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, bar0 + 8u * sidx);
   };
   int issued = 0;  // chunks issued (thread 0's count)
-  if (tid == 0)
+  if (tid == 0) {  // the first copies fly while the row table is built
+    for (int i = 0; i < kBulkStages; ++i) tc::mbar_init(bar0 + 8u * i, 1);
+    tc::fence_barrier_init();
     for (; issued < kBulkStages && issued < nchunks; ++issued) issue(issued);
+  }
+  // request, position and bonus flag of each row the range touches
+  if (tid >= 32 && tid < 32 + nslots) {
+    const int q = q0 + tid - 32;
+    const int b = request_of_row(row_off, B, q);
+    const int j = q - row_off[b];
+    rowinfo[tid - 32] = make_int4(b, j, j == lengths[b] - 1 ? 1 : 0, 0);
+  }
+  for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
+    slot[i] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
+  __syncthreads();
   volatile int never = 0;
   int q_cur = -1, bcur = 0, jcur = 0;
   bool bonus = false;
@@ -268,9 +276,10 @@ __global__ void __launch_bounds__(kBulkThreads)
         if (q != q_cur) {
           flush();
           q_cur = q;
-          bcur = request_of_row(row_off, B, q);
-          jcur = q - row_off[bcur];
-          bonus = jcur == lengths[bcur] - 1;
+          const int4 ri = rowinfo[q - q0];
+          bcur = ri.x;
+          jcur = ri.y;
+          bonus = ri.z != 0;
         }
         ms = ms_combine(ms, MS{m, t});
         if (bonus) kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, bcur, jcur, sblk)), sblk});
