@@ -103,9 +103,10 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out);
 /* Free the workspace (synchronises the device first). NULL is a no-op. */
 void dspark_ws_destroy(dspark_ws* ws);
 
-/* Clear the device status word, the lagged planner's round counter and the
- * draft kernel's grid-barrier words and winner slots, on `stream`. Call it
- * after any call that left a non-zero device status. */
+/* Clear the device status word, the lagged planner's round counter, the
+ * draft kernel's grid-barrier words and winner slots, and the verify sweep's
+ * per-request completion counters, on `stream`. Call it after any call that
+ * left a non-zero device status. */
 dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream);
 
 /* Copy the device status word into *device_status (a synchronous 4-byte copy;

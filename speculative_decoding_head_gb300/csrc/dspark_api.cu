@@ -83,7 +83,6 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   geo.tc_ok = draft_tc_supported(d);
 
   const size_t BG = (size_t)d.B * d.gamma;
-  const size_t rows = (size_t)d.B * (d.gamma + 1);
   size_t off = 0;
   auto carve = [&](size_t bytes) {
     const size_t o = off;
@@ -100,6 +99,8 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
   const size_t o_vlset = carve(sizeof(float) * d.B);
+  const size_t o_vdone = carve(sizeof(int) * d.B);
+  const size_t o_vpx = carve(sizeof(float) * (size_t)d.B * (d.gamma + 1));
   geo.resid_tc_ok = resid_tc_supported(d);
   if (geo.resid_tc_ok && resid_tc_configure(ws) != cudaSuccess) geo.resid_tc_ok = 0;
   cudaGetLastError();
@@ -136,6 +137,8 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vflag = reinterpret_cast<int*>(base + o_vflag);
   s.vrow = reinterpret_cast<int*>(base + o_vrow);
   s.vlset = reinterpret_cast<float*>(base + o_vlset);
+  s.vdone = reinterpret_cast<int*>(base + o_vdone);
+  s.vpx = reinterpret_cast<float*>(base + o_vpx);
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
   s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
@@ -162,6 +165,7 @@ dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream) {
   cudaError_t e = cudaMemsetAsync(ws->s.status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.plan_round, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 8 * sizeof(unsigned), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.vdone, 0, sizeof(int) * ws->d.B, st);
   if (e == cudaSuccess && ws->s.dwin)
     e = cudaMemsetAsync(ws->s.dwin, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
   return cuda_fail(e);

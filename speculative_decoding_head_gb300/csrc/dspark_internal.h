@@ -54,6 +54,8 @@ struct Scratch {
   int* vflag;             // [B] 1 = next anchor comes from the residual
   int* vrow;              // [B] packed row of the first rejection
   float* vlset;           // [B] target log-sum-exp of that row
+  int* vdone;             // [B] sweep ranges done per request (back to 0 by the finalizing CTA)
+  float* vpx;             // [B*(gamma+1)] P at each verified row's draft token (bulk sweep)
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
   float4* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set

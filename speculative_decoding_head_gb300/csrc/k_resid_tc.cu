@@ -162,12 +162,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
   }
-  // the rejected requests, in request order (every CTA builds the same list)
+  // the rejected requests, in request order (every CTA builds the same list).
+  // The flags, positions and rows are this round's only if every stage so far
+  // left the status clear: an error leaves the list empty.
   if (warp == 2) {
+    const bool clear = __shfl_sync(0xFFFFFFFFu, *(volatile int*)p.status, 0) == 0;
     int base = 0;
     for (int b0 = 0; b0 < p.B; b0 += 32) {
       const int b = b0 + lane;
-      const bool f = b < p.B && p.vflag[b] != 0;
+      const bool f = clear && b < p.B && p.vflag[b] != 0;
       const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
       if (f) list[base + __popc(m & ((1u << lane) - 1u))] = b;
       base += __popc(m);
@@ -224,8 +227,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
       const float* prow = p.P;
       if (lane < ncols) {
         const int b = list[gq * kRN + lane];
-        urow = p.U + ((size_t)b * p.g + p.n_acc[b]) * p.V;
-        prow = p.P + (size_t)p.vrow[b] * p.V;
+        urow = p.U + ((size_t)b * p.g + min(max(p.n_acc[b], 0), p.g - 1)) * p.V;
+        prow = p.P + (size_t)min(max(p.vrow[b], 0), p.B * (p.g + 1) - 1) * p.V;
       }
       for (int i = 0; i < nt && ok; ++i) {
         const int it = gq * nt + i, us = it % kRUP, v0 = (tile_lo + i) * kRM;
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const bool valid = et < kRN && i < nrej;
         if (valid) {
           const int b = list[i];
-          const int n = p.n_acc[b];
+          const int n = min(max(p.n_acc[b], 0), p.g - 1);  // a rejection leaves n <= gamma - 1
           x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
           col_b[et] = b;
           col_n[et] = n;

@@ -21,7 +21,9 @@
 //                      for the last verified row of a request also the block
 //                      draw of the bonus token.
 //   k_verify_finalize  one warp per request, one lane per row: accept tests,
-//                      first rejection, bonus token draw inside its block.
+//                      first rejection, bonus token draw inside its block
+//                      (after the bulk sweep, the same work runs in the sweep
+//                      CTA that completes the request's partials).
 //   k_resid_blocks     grid (chunks, B): residual block masses and block draw.
 //   k_resid_pick       grid (B): residual token draw inside the drawn block.
 #include "dspark_common.cuh"
@@ -144,6 +146,169 @@ __global__ void __launch_bounds__(kSweepThreads)
   }
 }
 
+// What the accept tests and the bonus draw read, and what they write.
+struct FinArgs {
+  const float* P;
+  const int32_t* row_off;
+  const int32_t* lengths;
+  const int32_t* anchor;
+  const int32_t* tokens;
+  const float* pd_tok;
+  int B, g, V, nblk, SL, Gs;
+  Rng rng;
+  const float4* part;
+  int32_t* n_acc;
+  int32_t* next_anchor;
+  int* vflag;
+  int* vrow;
+  float* vlset;
+  int* status;
+  float* px;  // [rows] P at each row's draft token, stored by the bulk sweep (nullptr: read P)
+};
+
+// Request b, by one whole warp. Lane j handles target row j: its
+// log-sum-exp from the sweep partials, p_t of draft x_{j+1} and the accept
+// test; the first rejection is the lowest failing lane. Then the bonus token
+// draw inside its block, or the hand-over to the residual pass.
+__device__ void finalize_request(int b, const FinArgs& f) {
+  const int lane = threadIdx.x & 31;
+  const float* __restrict__ P = f.P;
+  const int32_t* __restrict__ row_off = f.row_off;
+  const int32_t* __restrict__ lengths = f.lengths;
+  const int32_t* __restrict__ anchor = f.anchor;
+  const int32_t* __restrict__ tokens = f.tokens;
+  const float* __restrict__ pd_tok = f.pd_tok;
+  const int B = f.B, g = f.g, V = f.V, nblk = f.nblk, SL = f.SL, Gs = f.Gs;
+  const Rng rng = f.rng;
+  const float4* __restrict__ part = f.part;
+  int32_t* __restrict__ n_acc = f.n_acc;
+  int32_t* __restrict__ next_anchor = f.next_anchor;
+  int* __restrict__ vflag = f.vflag;
+  int* __restrict__ vrow = f.vrow;
+  float* __restrict__ vlset = f.vlset;
+  int* __restrict__ status = f.status;
+  if (lane == 0) vflag[b] = 0;  // no residual pass unless a rejection is found below
+  const int ell = lengths[b], base = row_off[b];
+  const int Rmax = B * (g + 1);
+  const int R = min(max(row_off[B], 0), Rmax);
+  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > R || anchor[b] < 0 || anchor[b] >= V) {
+    if (lane == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  const long long T = (long long)R * nblk;
+  // partials of row q: the CTAs whose unit ranges meet [q nblk, (q+1) nblk)
+  auto row_partials = [&](int q, MS* ms_out, KeyIdx* kb_out) {
+    const long long u0 = (long long)q * nblk, u1 = u0 + nblk - 1;
+    const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
+    MS ms{-INFINITY, 0.f};
+    KeyIdx kb = key_none();
+    for (int cb = c0; cb <= c1; cb += 4) {  // four partials' loads in flight at a time
+      float4 d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int c = cb + e;
+        d[e] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
+        if (c > c1) continue;
+        const long long clo = unit_lo(c, T, Gs);
+        if (clo >= unit_lo(c + 1, T, Gs)) continue;  // an empty range wrote nothing
+        const int first = (int)(clo / nblk);
+        if (q - first >= SL) continue;
+        d[e] = __ldcg(part + (size_t)c * SL + (q - first));
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        ms = ms_combine(ms, MS{d[e].x, d[e].y});
+        kb = better(kb, KeyIdx{d[e].z, __float_as_int(d[e].w)});
+      }
+    }
+    *ms_out = ms;
+    *kb_out = kb;
+  };
+  // ---- one lane per verified row: accept tests of rows 0 .. ell-2, and the
+  // bonus block key of row ell-1; the draft token's target logit is loaded
+  // alongside the row's partials
+  bool acc = true, bad = false;
+  float Lt = 0.f;
+  KeyIdx kbonus = key_none();
+  const bool arow = lane < ell - 1;
+  int x = 0;
+  float Px = 0.f, pdx = 0.f;
+  if (arow) {
+    x = tokens[(size_t)b * g + lane];
+    pdx = pd_tok[(size_t)b * g + lane];
+    if (x >= 0 && x < V) Px = f.px ? __ldcg(f.px + base + lane) : P[(size_t)(base + lane) * V + x];
+  }
+  if (lane < ell) {
+    MS ms;
+    KeyIdx kb;
+    row_partials(base + lane, &ms, &kb);
+    Lt = ms_log(ms);
+    kbonus = kb;
+  }
+  if (arow) {
+    if (!isfinite(Lt) || x < 0 || x >= V) {
+      bad = true;
+    } else {
+      const float pt = expf(Px - Lt);
+      const float u = u01(rng.word(kAccept, b, lane, 0));
+      acc = u * pdx < pt;
+    }
+  }
+  const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
+  if (badm) {
+    if (lane == 0) raise_status(status, DSPARK_ERANGE);
+    return;
+  }
+  const unsigned rej = __ballot_sync(0xFFFFFFFFu, !acc);
+  if (rej) {
+    const int n = __ffs(rej) - 1;
+    const float lset = __shfl_sync(0xFFFFFFFFu, Lt, n);
+    if (lane == 0) {
+      n_acc[b] = n;
+      vflag[b] = 1;
+      vrow[b] = base + n;
+      vlset[b] = lset;
+    }
+    return;
+  }
+  // ---- every verified draft accepted: bonus token from row ell - 1
+  const int n = ell - 1;
+  const size_t q = (size_t)base + n;
+  KeyIdx kb = kbonus;
+  if (n >= 32) {  // gamma = 32: the bonus row has no lane of its own
+    MS unused;
+    if (lane == 0) row_partials((int)q, &unused, &kb);
+  }
+  kb.key = __shfl_sync(0xFFFFFFFFu, kb.key, n < 32 ? n : 0);
+  kb.idx = __shfl_sync(0xFFFFFFFFu, kb.idx, n < 32 ? n : 0);
+  if (kb.idx == kNoIdx) {
+    if (lane == 0) raise_status(status, DSPARK_ENUMERIC);
+    return;
+  }
+  KeyIdx kt = key_none();
+  for (int v = kb.idx * kBlockW + lane; v < min(V, (kb.idx + 1) * kBlockW); v += 32)
+    kt = better(kt, KeyIdx{P[q * V + v] + gumbel(rng.word(kBonusToken, b, n, v)), v});
+  kt = warp_best(kt);
+  if (lane == 0) {
+    n_acc[b] = n;
+    next_anchor[b] = kt.idx;
+  }
+}
+
+// log of the residual weight max(0, p_t - p_d) of one token, written as
+// log p_t + log(-expm1(log p_d - log p_t)) so that near-equal p_t and p_d keep
+// their relative precision; -inf when p_t <= p_d.
+__device__ __forceinline__ float resid_logw(float lpt, float lpd) {
+  if (!(lpt > lpd)) return -INFINITY;
+  return lpt + logf(-expm1f(lpd - lpt));
+}
+
+// One warp per request, after the register sweep.
+__global__ void __launch_bounds__(128) k_verify_finalize(const FinArgs f) {
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b < f.B) finalize_request(b, f);
+}
+
 // Bulk-copy sweep for V % 64 == 0: unit u is then tokens [64u, 64u + 64) of
 // the packed rows, so a CTA's range is one contiguous byte range of P. It is
 // streamed through a 3-deep ring of 32 KB stages by cp.async.bulk and
@@ -170,16 +335,31 @@ size_t sweep_bulk_smem_bytes() {
 __global__ void __launch_bounds__(kBulkThreads)
     k_verify_sweep_bulk(const float* __restrict__ P, const int32_t* __restrict__ row_off,
                         const int32_t* __restrict__ lengths, int B, int nblk, int Rmax, int SL, Rng rng,
-                        float4* __restrict__ part, int* __restrict__ status) {
+                        float4* __restrict__ part, int* __restrict__ status, const FinArgs fin,
+                        int* __restrict__ vdone) {
   extern __shared__ __align__(128) unsigned char smem[];
   float* stage = reinterpret_cast<float*>(smem);
   float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
                                                (size_t)kBulkMaxSlots * kBulkThreads * 16);
   int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [kBulkMaxSlots]
+  // The finalize of a request whose rows no range covers never runs, so the
+  // lengths, offsets and anchors of all requests are checked by one CTA.
+  auto check_requests = [&]() {
+    if (threadIdx.x == 0 && row_off[0] != 0) raise_status(status, DSPARK_ERANGE);
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int ell = lengths[b], base = row_off[b];
+      if (ell < 1 || ell > fin.g + 1 || base < 0 || row_off[b + 1] != base + ell || base + ell > Rmax ||
+          fin.anchor[b] < 0 || fin.anchor[b] >= fin.V)
+        raise_status(status, DSPARK_ERANGE);
+    }
+  };
   const int R = min(max(row_off[B], 0), Rmax);
   const long long T = (long long)R * nblk;
-  if (T == 0) return;
+  if (T == 0) {  // no rows at all
+    if (blockIdx.x == gridDim.x - 1) check_requests();
+    return;
+  }
   const int G = gridDim.x, c = blockIdx.x, tid = threadIdx.x;
   const long long lo = unit_lo(c, T, G), hi = unit_lo(c + 1, T, G);
   if (lo >= hi) return;
@@ -211,7 +391,11 @@ __global__ void __launch_bounds__(kBulkThreads)
     const int q = q0 + tid - 32;
     const int b = request_of_row(row_off, B, q);
     const int j = q - row_off[b];
-    rowinfo[tid - 32] = make_int4(b, j, j == lengths[b] - 1 ? 1 : 0, 0);
+    // the draft token the row tests (-1 on the last verified row; offsets
+    // and lengths are checked by CTA 0 meanwhile, so stay in bounds here)
+    const bool tested = j >= 0 && j < min(lengths[b], fin.g + 1) - 1;
+    const int xt = tested ? fin.tokens[(size_t)b * fin.g + j] : -1;
+    rowinfo[tid - 32] = make_int4(b, j, j == lengths[b] - 1 ? 1 : 0, xt >= 0 && xt < fin.V ? xt : -1);
   }
   for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
     slot[i] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
@@ -283,6 +467,8 @@ __global__ void __launch_bounds__(kBulkThreads)
         }
         ms = ms_combine(ms, MS{m, t});
         if (bonus) kb = better(kb, KeyIdx{m + logf(t) + gumbel(rng.word(kBonusBlock, bcur, jcur, sblk)), sblk});
+        const int xt = rowinfo[q - q0].w;  // the accept test's target logit, while the block is staged
+        if (xt >= 0 && (xt >> 6) == sblk) fin.px[q] = stage[(size_t)sidx * kBulkFloats + tid * kBlockW + (xt & 63)];
       }
     }
     __syncthreads();  // every thread is done with this stage
@@ -312,136 +498,34 @@ __global__ void __launch_bounds__(kBulkThreads)
     k2 = warp_best(k2);
     if (lane == 0) part[(size_t)c * SL + sl] = make_float4(m2.m, m2.s, k2.key, __int_as_float(k2.idx));
   }
-}
-
-// One warp per request. Lane j handles target row j: its log-sum-exp from the
-// sweep partials, p_t of draft x_{j+1} and the accept test; the first
-// rejection is the lowest failing lane. Then the bonus token draw inside its
-// block, or the hand-over to the residual pass.
-__global__ void __launch_bounds__(128)
-    k_verify_finalize(const float* __restrict__ P, const int32_t* __restrict__ row_off,
-                      const int32_t* __restrict__ lengths, const int32_t* __restrict__ anchor,
-                      const int32_t* __restrict__ tokens, const float* __restrict__ pd_tok, int B, int g, int V,
-                      int nblk, int SL, int Gs, Rng rng, const float4* __restrict__ part,
-                      int32_t* __restrict__ n_acc, int32_t* __restrict__ next_anchor, int* __restrict__ vflag,
-                      int* __restrict__ vrow, float* __restrict__ vlset, int* __restrict__ status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (b >= B) return;
-  if (lane == 0) vflag[b] = 0;  // no residual pass unless a rejection is found below
-  const int ell = lengths[b], base = row_off[b];
-  const int Rmax = B * (g + 1);
-  const int R = min(max(row_off[B], 0), Rmax);
-  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > R || anchor[b] < 0 || anchor[b] >= V) {
-    if (lane == 0) raise_status(status, DSPARK_ERANGE);
-    return;
-  }
-  const long long T = (long long)R * nblk;
-  // partials of row q: the CTAs whose unit ranges meet [q nblk, (q+1) nblk)
-  auto row_partials = [&](int q, MS* ms_out, KeyIdx* kb_out) {
-    const long long u0 = (long long)q * nblk, u1 = u0 + nblk - 1;
-    const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
-    MS ms{-INFINITY, 0.f};
-    KeyIdx kb = key_none();
-    for (int cb = c0; cb <= c1; cb += 4) {  // four partials' loads in flight at a time
-      float4 d[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = cb + e;
-        d[e] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
-        if (c > c1) continue;
-        const long long clo = unit_lo(c, T, Gs);
-        if (clo >= unit_lo(c + 1, T, Gs)) continue;  // an empty range wrote nothing
-        const int first = (int)(clo / nblk);
-        if (q - first >= SL) continue;
-        d[e] = part[(size_t)c * SL + (q - first)];
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        ms = ms_combine(ms, MS{d[e].x, d[e].y});
-        kb = better(kb, KeyIdx{d[e].z, __float_as_int(d[e].w)});
-      }
-    }
-    *ms_out = ms;
-    *kb_out = kb;
-  };
-  // ---- one lane per verified row: accept tests of rows 0 .. ell-2, and the
-  // bonus block key of row ell-1; the draft token's target logit is loaded
-  // alongside the row's partials
-  bool acc = true, bad = false;
-  float Lt = 0.f;
-  KeyIdx kbonus = key_none();
-  const bool arow = lane < ell - 1;
-  int x = 0;
-  float Px = 0.f, pdx = 0.f;
-  if (arow) {
-    x = tokens[(size_t)b * g + lane];
-    pdx = pd_tok[(size_t)b * g + lane];
-    if (x >= 0 && x < V) Px = P[(size_t)(base + lane) * V + x];
-  }
-  if (lane < ell) {
-    MS ms;
-    KeyIdx kb;
-    row_partials(base + lane, &ms, &kb);
-    Lt = ms_log(ms);
-    kbonus = kb;
-  }
-  if (arow) {
-    if (!isfinite(Lt) || x < 0 || x >= V) {
-      bad = true;
-    } else {
-      const float pt = expf(Px - Lt);
-      const float u = u01(rng.word(kAccept, b, lane, 0));
-      acc = u * pdx < pt;
-    }
-  }
-  const unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
-  if (badm) {
-    if (lane == 0) raise_status(status, DSPARK_ERANGE);
-    return;
-  }
-  const unsigned rej = __ballot_sync(0xFFFFFFFFu, !acc);
-  if (rej) {
-    const int n = __ffs(rej) - 1;
-    const float lset = __shfl_sync(0xFFFFFFFFu, Lt, n);
+  // the last CTA checks the requests after its own range, so that the check
+  // does not delay the stream
+  if (blockIdx.x == gridDim.x - 1) check_requests();
+  // ---- the accept tests and the bonus draw of a request run in the CTA that
+  // completes its last partial: each CTA counts itself in for every request
+  // its range touched (release), and the CTA whose count completes the
+  // request's set of covering ranges (acquire) finalizes it with one warp
+  __threadfence();
+  __syncthreads();
+  for (int i = warp; i < nslots; i += kBulkThreads / 32) {
+    const int4 ri = rowinfo[i];
+    if (i > 0 && rowinfo[i - 1].x == ri.x) continue;  // counted once per request
+    int last = 0;
     if (lane == 0) {
-      n_acc[b] = n;
-      vflag[b] = 1;
-      vrow[b] = base + n;
-      vlset[b] = lset;
+      const int b = ri.x;
+      const long long r0 = min(max(row_off[b], 0), R), r1 = min(max((long long)row_off[b] + lengths[b], r0), (long long)R);
+      int ncov = 0;  // 0 (never finalized here) when the request has no rows; CTA 0 reports it
+      if (r1 > r0)
+        for (int cc = unit_owner(r0 * nblk, T, G); cc <= unit_owner(r1 * nblk - 1, T, G); ++cc)
+          ncov += unit_lo(cc, T, G) < unit_lo(cc + 1, T, G) ? 1 : 0;
+      last = atomicAdd(vdone + b, 1) == ncov - 1;
+      if (last) {
+        __threadfence();
+        vdone[b] = 0;  // the last user: ready for the next launch
+      }
     }
-    return;
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) finalize_request(ri.x, fin);
   }
-  // ---- every verified draft accepted: bonus token from row ell - 1
-  const int n = ell - 1;
-  const size_t q = (size_t)base + n;
-  KeyIdx kb = kbonus;
-  if (n >= 32) {  // gamma = 32: the bonus row has no lane of its own
-    MS unused;
-    if (lane == 0) row_partials((int)q, &unused, &kb);
-  }
-  kb.key = __shfl_sync(0xFFFFFFFFu, kb.key, n < 32 ? n : 0);
-  kb.idx = __shfl_sync(0xFFFFFFFFu, kb.idx, n < 32 ? n : 0);
-  if (kb.idx == kNoIdx) {
-    if (lane == 0) raise_status(status, DSPARK_ENUMERIC);
-    return;
-  }
-  KeyIdx kt = key_none();
-  for (int v = kb.idx * kBlockW + lane; v < min(V, (kb.idx + 1) * kBlockW); v += 32)
-    kt = better(kt, KeyIdx{P[q * V + v] + gumbel(rng.word(kBonusToken, b, n, v)), v});
-  kt = warp_best(kt);
-  if (lane == 0) {
-    n_acc[b] = n;
-    next_anchor[b] = kt.idx;
-  }
-}
-
-// log of the residual weight max(0, p_t - p_d) of one token, written as
-// log p_t + log(-expm1(log p_d - log p_t)) so that near-equal p_t and p_d keep
-// their relative precision; -inf when p_t <= p_d.
-__device__ __forceinline__ float resid_logw(float lpt, float lpd) {
-  if (!(lpt > lpd)) return -INFINITY;
-  return lpt + logf(-expm1f(lpd - lpt));
 }
 
 template <int BF16>
@@ -451,12 +535,14 @@ __global__ void __launch_bounds__(256)
                    const int32_t* __restrict__ tokens, const float* __restrict__ lse, int g, int V, int r,
                    int nblk, const int* __restrict__ vflag, const int32_t* __restrict__ n_acc,
                    const int* __restrict__ vrow, const float* __restrict__ vlset, Rng rng,
-                   float2* __restrict__ rpart) {
+                   float2* __restrict__ rpart, const int* __restrict__ status) {
   extern __shared__ float e[];  // W1[x_n], [r]
   __shared__ KeyIdx red_k[8];
   const int b = blockIdx.y, c = blockIdx.x;
-  if (!vflag[b]) return;
-  const int n = n_acc[b];
+  // this round's flags only if every stage so far left the status clear (no
+  // kernel running now writes the status, so every thread reads the same)
+  if (!vflag[b] || *(volatile const int*)status != 0) return;
+  const int n = min(max(n_acc[b], 0), g - 1);
   const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
   for (int i = threadIdx.x; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
   __syncthreads();
@@ -502,16 +588,19 @@ __global__ void __launch_bounds__(kPickThreads)
                  const int32_t* __restrict__ tokens, const float* __restrict__ lse, int g, int V, int r,
                  int nblk, int nchunk, const int* __restrict__ vflag, const int32_t* __restrict__ n_acc,
                  const int* __restrict__ vrow, const float* __restrict__ vlset, Rng rng,
-                 const float2* __restrict__ rpart, int32_t* __restrict__ next_anchor) {
+                 const float2* __restrict__ rpart, int32_t* __restrict__ next_anchor,
+                 const int* __restrict__ status) {
   extern __shared__ float e[];  // [r]
   __shared__ KeyIdx red_k[kPickThreads / 32];
   __shared__ float zpart[kPickThreads / kBlockW][kBlockW];
   __shared__ int s_blk;
   const int b = blockIdx.x;
-  if (!vflag[b]) return;
+  // this round's flags only if every stage so far left the status clear (no
+  // kernel running now writes the status, so every thread reads the same)
+  if (!vflag[b] || *(volatile const int*)status != 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-  const int n = n_acc[b];
-  const float* Prow = P + (size_t)vrow[b] * V;
+  const int n = min(max(n_acc[b], 0), g - 1);
+  const float* Prow = P + (size_t)min(max(vrow[b], 0), (int)gridDim.x * (g + 1) - 1) * V;
   // W1[x_n] (the previous token's row) does not depend on the drawn block:
   // its load overlaps the reduction of the block keys
   {
@@ -608,16 +697,19 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
   const Rng rng = Rng::make(a.seed, a.round);
-  if (geo.sweep_bulk)
+  const FinArgs fin{a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma, d.V, geo.nblk,
+                    geo.SL, geo.sweep_grid, rng, ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
+                    ws->s.vlset, ws->s.status, geo.sweep_bulk ? ws->s.vpx : nullptr};
+  if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
     k_verify_sweep_bulk<<<geo.sweep_grid, kBulkThreads, sweep_bulk_smem_bytes(), st>>>(
-        a.P, a.row_off, a.lengths, d.B, geo.nblk, d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status);
-  else
+        a.P, a.row_off, a.lengths, d.B, geo.nblk, d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin,
+        ws->s.vdone);
+    *launches -= 1;
+  } else {
     k_verify_sweep<<<geo.sweep_grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.nblk,
                                                             d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart);
-  k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B,
-                                                   d.gamma, d.V, geo.nblk, geo.SL, geo.sweep_grid, rng,
-                                                   ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
-                                                   ws->s.vlset, ws->s.status);
+    k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(fin);
+  }
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
   if (BF16 && ws->use_tc && geo.resid_tc_ok) {
@@ -628,11 +720,11 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   } else {
     k_resid_blocks<BF16><<<dim3(kResidChunks, d.B), 256, smem, st>>>(
         a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
-        ws->s.vrow, ws->s.vlset, rng, ws->s.rpart);
+        ws->s.vrow, ws->s.vlset, rng, ws->s.rpart, ws->s.status);
   }
   k_resid_pick<BF16><<<d.B, kPickThreads, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
                                              d.r, geo.nblk, nchunk, ws->s.vflag, a.n_acc, ws->s.vrow,
-                                             ws->s.vlset, rng, ws->s.rpart, a.next_anchor);
+                                             ws->s.vlset, rng, ws->s.rpart, a.next_anchor, ws->s.status);
   *launches += 4;
   return cudaGetLastError();
 }

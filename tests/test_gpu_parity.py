@@ -226,6 +226,42 @@ def test_device_errors_are_reported_not_faulted():
         ws.plan(conf.cpu(), dev["sps"])               # host tensors are refused by the binding
 
 
+def test_verify_rejects_inconsistent_lengths():
+    """Lengths outside [1, gamma + 1] or offsets that do not add up are reported
+    as ERANGE by the sweep (bulk path: V % 64 == 0), not faulted."""
+    wl = MID["mid_ragged"].with_(B=16, V=4096, seed=23)
+    assert wl.V % 64 == 0
+    inp = make_inputs(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], 5, 1)
+    ws = Workspace.for_workload(wl)
+    L = np.full(wl.B, 2, np.int32)
+    P = pack_np(npi["P_full"], L)
+    args = (torch.from_numpy(od["tokens"]).cuda(), torch.from_numpy(od["pd_tok"].astype(np.float32)).cuda(),
+            torch.from_numpy(od["lse"].astype(np.float32)).cuda(), dev["U"], dev["W1"], dev["W2"], 5, 1)
+    for bad_L, bad_ro in ((L.copy(), None), (L.copy(), "shift")):
+        if bad_ro is None:
+            bad_L[3] = 0                                   # a request with no verified row
+        ro = row_off_np(bad_L)
+        if bad_ro == "shift":
+            ro[5] += 1                                     # offsets that do not add up
+        out = ws.verify(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(bad_L).cuda(),
+                        dev["anchor"], *args)
+        torch.cuda.synchronize()
+        assert ws.device_status() == 6, ws.device_status()
+        ws.reset()
+        torch.cuda.synchronize()
+        assert ws.device_status() == 0
+    # the workspace is usable again after the reset
+    ro = row_off_np(L)
+    out = ws.verify(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(L).cuda(),
+                    dev["anchor"], *args)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    ov = oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], 5, 1)
+    compare_verify(gpu_np(out), ov, range(wl.B)).check_rate()
+
+
 def test_gpu_losslessness_chi_square():
     """Replicated requests with token-independent rows: the first emitted token follows p_t."""
     from scipy import stats
