@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sts", action="store_true", help="skip the STS calibration-fit timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 
@@ -205,6 +206,33 @@ def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int):
     return rounds_per_s, cores, (f"oracle draft + verify (gamma+1 rows) of {done_req} requests of the "
                                  f"{wl.name} workload, plus the plan each pass: {spent:.1f} s on {cores} "
                                  f"threads, scaled to a {wl.B}-request round")
+
+
+def sts_timing(reps: int = 10):
+    """The STS calibration fit (sequential temperature scaling of the
+    confidences) on its held-out workload: device time per fit, CUDA events on
+    the launching stream after warm-up (inputs resident)."""
+    import torch
+    from speculative_decoding_head_gb300 import binding
+    from speculative_decoding_head_gb300.workloads import STS_SETS, make_sts_inputs, sts_grid
+    c = STS_SETS["sts_prod"]
+    inp = make_sts_inputs(c["N"], c["gamma"], c["seed"], device="cuda")
+    grid = sts_grid(c["G"]).cuda()
+    for _ in range(3):
+        T, ece, st = binding.sts_fit(inp["raw"], inp["cstar"], grid, c["M"])
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        binding.sts_fit(inp["raw"], inp["cstar"], grid, c["M"])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    evals = c["N"] * c["G"] * c["gamma"]
+    return {"workload": "sts_prod", "N": c["N"], "gamma": c["gamma"], "grid": c["G"], "bins": c["M"],
+            "ms_per_fit": ms, "evals_per_s": evals / (ms * 1e-3), "launches": 2 * c["gamma"],
+            "temperatures": [round(float(t), 3) for t in T.cpu().tolist()]}
 
 
 def run_reference(args):
@@ -411,6 +439,7 @@ def main():
             "verified_positions_per_s": value * sum_len,
             "emitted_tokens_per_round": emitted,
             "stage_ms": st,
+            "sts_fit": None if args.no_sts else sts_timing(),
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": e2e,

@@ -205,6 +205,28 @@ dspark_status dspark_markov_draft_noalloc(const dspark_dims* dims, const float* 
                                           int32_t* tokens, float* pd_tok, float* lse, float* conf,
                                           int32_t* device_status, dspark_stream_t stream);
 
+/*
+ * Sequential temperature scaling (STS) of the confidence head
+ * ("DeepSeek-V4.1 模型结构（6）：解码，DSpark", section "confidence head";
+ * zdszero "spec_dspark", "STS 校准"; deepseek.csdn.net §5.2). For N held-out
+ * blocks of gamma positions, raw [N, gamma] fp32 holds the confidence logits
+ * w^T [h_k; W1[x_{k-1}]] before the temperature and cstar [N, gamma] fp32 the
+ * soft labels (each position's acceptance probability 1 - ||p_d - p_t||_1 / 2).
+ * Left to right, T_out[k] becomes the first value of Tgrid [G] fp32 (> 0) that
+ * minimises the expected calibration error, over M equal-width bins of [0, 1],
+ * of a_k = prod_{i<=k} sigmoid(raw_i / T_i) against y_k = prod_{i<=k} cstar_i,
+ * the earlier positions' temperatures kept; ece_out [gamma] fp64 receives that
+ * ECE. All pointers are device pointers owned by the caller; scratch holds
+ * dspark_sts_scratch_bytes(N, G) bytes (8-byte aligned) and device_status one
+ * int32 that the call zeroes and a kernel sets to DSPARK_ERANGE for a grid
+ * value that is not positive and finite. 1 <= M <= 32, N < 2^23, G <= 65535. Returns
+ * EINVAL/EUNSUPPORTED/ECUDA on the host; asynchronous on `stream`.
+ */
+dspark_status dspark_sts_fit(const float* raw, const float* cstar, int N, int gamma, const float* Tgrid,
+                             int G, int M, float* T_out, double* ece_out, void* scratch,
+                             int32_t* device_status, dspark_stream_t stream);
+size_t dspark_sts_scratch_bytes(int N, int G);
+
 #ifdef __cplusplus
 }
 #endif

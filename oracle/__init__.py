@@ -86,6 +86,7 @@ def lib():
             l.orc_residual.argtypes = [P, P, C.c_long, u64, u64, u32, u32, P]
             l.orc_residual.restype = i32
             l.orc_markov_logits.argtypes = [P, P, P, P, i32, P]
+            l.orc_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P]
             l.orc_block_width.restype = i32
             l.orc_set_threads.argtypes = [i32]
             l.orc_get_threads.restype = i32
@@ -154,6 +155,20 @@ def sample_draft(logw, seed=0, rnd=0, b=0, j=0):
     m = np.zeros(1, np.float64)
     v = lib().orc_sample_draft(_p(a), a.size, seed, rnd, b, j, _p(m))
     return int(v), float(m[0])
+
+
+def sts_fit(raw, cstar, Tgrid, M: int = 15):
+    """Sequential temperature scaling (see ``orc_sts_fit``): raw and cstar are
+    [N, gamma]; returns (T [gamma] float32, ece [gamma], margin [gamma])."""
+    r = _c(raw, np.float32)
+    c = _c(cstar, np.float32)
+    t = _c(Tgrid, np.float32)
+    N, g = r.shape
+    T = np.zeros(g, np.float32)
+    ece = np.zeros(g, np.float64)
+    mg = np.zeros(g, np.float64)
+    lib().orc_sts_fit(N, g, _p(r), _p(c), t.size, _p(t), M, _p(T), _p(ece), _p(mg))
+    return T, ece, mg
 
 
 def residual(pt, pd, seed=0, rnd=0, b=0, j=0):

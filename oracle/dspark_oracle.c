@@ -22,6 +22,10 @@
  *              ([V4.1 blog] "目标函数", "贪心就能解"; [csdn] 5.3). The
  *              asynchronous variant takes the capacity K = argmax Theta from
  *              lagged confidences and the top-K current candidates ([csdn] 8).
+ *   sts     -- sequential temperature scaling of c_k: per position, left to
+ *              right, the grid temperature that minimises the ECE of the
+ *              cumulative product against cumulative soft labels
+ *              ([spec_dspark] "STS 校准"; [ailearn] 05; [csdn] 5.2).
  *   verify  -- accept x with probability min(1, p_t(x)/p_d(x)); at the first
  *              rejection resample from norm(max(0, p_t - p_d)); if every
  *              verified draft is accepted draw the bonus token from the
@@ -521,6 +525,66 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         resid[b] = from_resid;
         free(lt); free(z); free(lw); free(tol); free(tm);
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* STS: sequential temperature scaling of the confidence head          */
+/* ([V4.1 blog] section "confidence head" (a temperature per position, */
+/* fitted on held-out data); zdszero "spec_dspark" "STS 校准"; [ailearn] */
+/* 05; [csdn] 5.2: left to right, a one-dimensional grid search per    */
+/* position minimising the ECE of the cumulative product, earlier      */
+/* positions kept fixed).                                              */
+/*                                                                     */
+/* For n < N held-out blocks and positions k = 1..g: raw[n][k] is the  */
+/* confidence logit before the temperature and cstar[n][k] the soft    */
+/* label (the position's acceptance probability). With                 */
+/*   a_k(n) = prod_{i<=k} sigma(raw[n][i] / T_i),                      */
+/*   y_k(n) = prod_{i<=k} cstar[n][i]                                  */
+/* (the prefix's joint acceptance factorises by the chain rule), and   */
+/* M equal-width bins of [0, 1] (bin floor(a M), a = 1 in the last),   */
+/*   ECE_k(T) = (1/N) sum_m | sum_{n: a_k(n) in bin m} (a_k(n) - y_k(n)) |,
+/* T_k is the first grid value minimising ECE_k given T_1..T_{k-1}.    */
+/* margin_out[k] = second-best ECE - best ECE (INFINITY if G == 1).    */
+/* ------------------------------------------------------------------ */
+void orc_sts_fit(int N, int g, const float* raw, const float* cstar, int G, const float* Tgrid,
+                 int M, float* T_out, double* ece_out, double* margin_out)
+{
+    double* a = (double*)malloc(sizeof(double) * (size_t)N);
+    double* y = (double*)malloc(sizeof(double) * (size_t)N);
+    double* yk = (double*)malloc(sizeof(double) * (size_t)N);
+    double* S = (double*)malloc(sizeof(double) * (size_t)M);
+    for (int n = 0; n < N; ++n) { a[n] = 1.0; y[n] = 1.0; }
+    for (int k = 0; k < g; ++k) {
+        for (int n = 0; n < N; ++n) yk[n] = y[n] * (double)cstar[(size_t)n * g + k];
+        double best = INFINITY, second = INFINITY;
+        int gbest = 0;
+        for (int gi = 0; gi < G; ++gi) {
+            const double T = (double)Tgrid[gi];
+            for (int m = 0; m < M; ++m) S[m] = 0.0;
+            for (int n = 0; n < N; ++n) {
+                const double c = 1.0 / (1.0 + exp(-(double)raw[(size_t)n * g + k] / T));
+                const double an = a[n] * c;
+                int m = (int)floor(an * M);
+                if (m > M - 1) m = M - 1;
+                if (m < 0) m = 0;
+                S[m] += an - yk[n];
+            }
+            double e = 0.0;
+            for (int m = 0; m < M; ++m) e += fabs(S[m]);
+            e /= (double)N;
+            if (e < best) { second = best; best = e; gbest = gi; }
+            else if (e < second) second = e;
+        }
+        T_out[k] = Tgrid[gbest];
+        ece_out[k] = best;
+        margin_out[k] = second - best;
+        const double Tk = (double)Tgrid[gbest];
+        for (int n = 0; n < N; ++n) {
+            a[n] *= 1.0 / (1.0 + exp(-(double)raw[(size_t)n * g + k] / Tk));
+            y[n] = yk[n];
+        }
+    }
+    free(a); free(y); free(yk); free(S);
 }
 
 /* ------------------------------------------------------------------ */

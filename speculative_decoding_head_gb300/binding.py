@@ -77,6 +77,10 @@ def load() -> C.CDLL:
         lib.dspark_verify.restype = i32
         lib.dspark_round.argtypes = [P] * 10 + [u64, u64] + [P] * 9
         lib.dspark_round.restype = i32
+        lib.dspark_sts_fit.argtypes = [P, P, i32, i32, P, i32, i32, P, P, P, P, P]
+        lib.dspark_sts_fit.restype = i32
+        lib.dspark_sts_scratch_bytes.argtypes = [i32, i32]
+        lib.dspark_sts_scratch_bytes.restype = C.c_size_t
         _lib = lib
         return lib
 
@@ -106,6 +110,28 @@ def _stream(stream) -> C.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
     return C.c_void_p(stream.cuda_stream)
+
+
+def sts_fit(raw: torch.Tensor, cstar: torch.Tensor, Tgrid: torch.Tensor, M: int = 15, stream=None):
+    """Sequential temperature scaling (``dspark_sts_fit``): raw and cstar are
+    [N, gamma] fp32 CUDA tensors, Tgrid [G] fp32. Returns (T [gamma] fp32,
+    ece [gamma] fp64, device status [1] int32), all on the device."""
+    lib = load()
+    f32 = torch.float32
+    if raw.dim() != 2 or cstar.shape != raw.shape:
+        raise DsparkError("raw and cstar must be [N, gamma] of the same shape")
+    N, g = raw.shape
+    G = Tgrid.numel()
+    dev = raw.device
+    scratch = torch.empty(int(lib.dspark_sts_scratch_bytes(N, G)), dtype=torch.uint8, device=dev)
+    T = torch.empty(g, dtype=f32, device=dev)
+    ece = torch.empty(g, dtype=torch.float64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    code = lib.dspark_sts_fit(_ptr(raw, f32, "raw"), _ptr(cstar, f32, "cstar"), N, g, _ptr(Tgrid, f32, "Tgrid"), G,
+                              int(M), _ptr(T, f32, "T"), _ptr(ece, torch.float64, "ece"), _ptr(scratch, None, "scratch"),
+                              _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(code, "dspark_sts_fit")
+    return T, ece, status
 
 
 class Workspace:

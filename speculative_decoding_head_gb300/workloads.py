@@ -155,6 +155,33 @@ def make_inputs(wl: Workload, device: str = "cpu", with_target: bool = True) -> 
     return out
 
 
+# Held-out calibration sets for the STS fit: confidence logits per position
+# (mean falling along the block, as later positions are drafted with less
+# context) and soft acceptance labels in [0, 1] that rise with the logit but
+# are noisier and flatter than the logit's own sigmoid would be, so that the
+# best temperatures differ from 1 and from position to position.
+STS_SETS = {
+    "sts_small": dict(N=20000, gamma=4, G=40, M=15, seed=49),
+    "sts_prod": dict(N=262144, gamma=5, G=64, M=15, seed=41),
+}
+
+
+def sts_grid(G: int) -> torch.Tensor:
+    """G temperatures from 0.1 upwards in steps of 0.1 (fp32)."""
+    return (torch.arange(1, G + 1, dtype=torch.float64) * 0.1).to(torch.float32)
+
+
+def make_sts_inputs(N: int, gamma: int, seed: int, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    gen = torch.Generator().manual_seed(seed)
+    mu = torch.linspace(2.0, 0.5, gamma, dtype=torch.float64)
+    raw = mu + 1.5 * torch.randn(N, gamma, generator=gen, dtype=torch.float64)
+    # labels: a clipped affine function of the logit plus noise (no sigmoid)
+    slope = torch.linspace(0.12, 0.2, gamma, dtype=torch.float64)
+    lab = 0.55 + slope * raw + 0.08 * torch.randn(N, gamma, generator=gen, dtype=torch.float64)
+    cstar = lab.clamp(0.02, 0.98)
+    return {"raw": raw.to(torch.float32).to(device), "cstar": cstar.to(torch.float32).to(device)}
+
+
 def pack_rows(P_full: torch.Tensor, lengths: torch.Tensor) -> torch.Tensor:
     """Packed ragged target logits [sum(lengths), V]: rows 0..lengths[b]-1 of each request.
 

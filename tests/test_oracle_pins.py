@@ -615,3 +615,59 @@ def test_lagged_planner_takes_capacity_from_lag_and_order_from_now():
     # with no lag (same confidences) the capacity is the full-path optimum
     L0, K0, _ = oracle.plan_lagged(now, now, sps)
     assert K0 == oracle.plan_capacity(now, sps)[0]
+
+
+# ------------------------------------------------------------------ STS calibration
+def _sig(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def test_sts_recovers_the_generating_temperatures():
+    """Labels equal to sigmoid(raw / T*) with T* on the grid: every position
+    finds its T* and the ECE is zero up to the labels' fp32 rounding."""
+    rng = np.random.default_rng(3)
+    N, g = 3000, 4
+    raw = rng.normal(1.0, 1.5, (N, g)).astype(np.float32)
+    grid = (np.arange(1, 31) * 0.1).astype(np.float32)
+    Tstar = grid[[6, 12, 19, 3]]
+    cstar = _sig(raw.astype(np.float64) / Tstar.astype(np.float64)).astype(np.float32)
+    T, ece, margin = oracle.sts_fit(raw, cstar, grid)
+    assert np.array_equal(T, Tstar)
+    assert ece.max() < 1e-7
+    assert margin.min() > 1e-4
+
+
+def test_sts_single_sample_and_single_bin_closed_forms():
+    # one block, one position, one temperature: ECE = |sigmoid(r / T) - c*|
+    T, ece, margin = oracle.sts_fit(np.array([[0.8]], np.float32), np.array([[0.3]], np.float32),
+                                    np.array([2.0], np.float32))
+    assert T[0] == np.float32(2.0) and np.isinf(margin[0])
+    r, c = float(np.float32(0.8)), float(np.float32(0.3))      # the stored fp32 values
+    assert abs(ece[0] - abs(_sig(r / 2.0) - c)) < 1e-12
+    # one bin: ECE = |mean(a) - mean(y)| over the whole set (textbook definition)
+    rng = np.random.default_rng(5)
+    raw = rng.normal(0.0, 2.0, (500, 2)).astype(np.float32)
+    cstar = rng.uniform(0.0, 1.0, (500, 2)).astype(np.float32)
+    grid = np.array([0.5, 1.0, 2.0], np.float32)
+    T, ece, _ = oracle.sts_fit(raw, cstar, grid, M=1)
+    r64, c64 = raw.astype(np.float64), cstar.astype(np.float64)
+    a1 = _sig(r64[:, 0] / T[0])
+    assert abs(ece[0] - abs(a1.mean() - c64[:, 0].mean())) < 1e-12
+    best = min(abs(np.mean(_sig(r64[:, 0] / t)) - c64[:, 0].mean()) for t in grid.astype(np.float64))
+    assert abs(ece[0] - best) < 1e-12
+    a2 = a1 * _sig(r64[:, 1] / T[1])
+    assert abs(ece[1] - abs(a2.mean() - (c64[:, 0] * c64[:, 1]).mean())) < 1e-12
+
+
+def test_sts_is_left_to_right():
+    """Position 1's temperature and ECE do not depend on later positions' data."""
+    rng = np.random.default_rng(8)
+    raw = rng.normal(1.0, 1.5, (2000, 3)).astype(np.float32)
+    cstar = rng.uniform(0.1, 0.9, (2000, 3)).astype(np.float32)
+    grid = (np.arange(1, 21) * 0.2).astype(np.float32)
+    T1, e1, _ = oracle.sts_fit(raw, cstar, grid)
+    raw2, c2 = raw.copy(), cstar.copy()
+    raw2[:, 1:] = rng.normal(-1.0, 0.5, (2000, 2))
+    c2[:, 1:] = rng.uniform(0.0, 1.0, (2000, 2))
+    T2, e2, _ = oracle.sts_fit(raw2, c2, grid)
+    assert T1[0] == T2[0] and e1[0] == e2[0]
