@@ -23,6 +23,7 @@ SYMBOLS = [
     "dspark_ws_create", "dspark_ws_destroy", "dspark_ws_reset", "dspark_last_error",
     "dspark_status_string", "dspark_last_launch_count", "dspark_path",
     "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
+    "dspark_sts_fit", "dspark_sts_scratch_bytes",
 ]
 
 

@@ -819,10 +819,8 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
 
-  cudaError_t e;
   const TcSmem L = TcSmem::make(d.r);
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.G);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = L.total + 1024;
@@ -832,7 +830,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_draft_tc, tm_w2, tm_u, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_draft_tc, tm_w2, tm_u, p);
   ++*launches;
   return e;
 }

@@ -74,3 +74,20 @@ def test_binding_refuses_missing_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_lib", None)
     with pytest.raises(binding.DsparkError):
         binding.load()
+
+
+def test_sts_fit_arguments_are_checked_on_the_host(lib):
+    """Bad sizes and null pointers are EINVAL / EUNSUPPORTED before any CUDA call."""
+    fake = ctypes.c_void_p(16)   # never dereferenced: the checks come first
+    args = dict(raw=fake, cstar=fake, N=100, g=4, Tgrid=fake, G=10, M=15, T=fake, ece=fake, scratch=fake, st=fake)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return lib.dspark_sts_fit(a["raw"], a["cstar"], a["N"], a["g"], a["Tgrid"], a["G"], a["M"], a["T"], a["ece"],
+                                  a["scratch"], a["st"], None)
+
+    assert call(M=0) == 1 and call(M=33) == 1            # 1 <= M <= 32
+    assert call(N=0) == 1 and call(g=0) == 1 and call(G=0) == 1 and call(G=70000) == 1
+    assert call(raw=None) == 1 and call(scratch=None) == 1 and call(st=None) == 1
+    assert call(N=1 << 23) == 5                          # the fixed-point bin sums' range
+    assert lib.dspark_sts_scratch_bytes(1000, 10) == 8 * 10 * 8 * 32 + 8 * 10 + 16 * 1000
