@@ -68,6 +68,8 @@ def test_tc_smallest():
     (130, 2, 4104, 256),     # two row groups, the second nearly empty
     (200, 3, 2048, 192),     # two row groups, rank 192
     (256, 2, 6000, 256),     # two full row groups
+    (64, 16, 2048, 128),     # a long block: sixteen steps, sixteen grid barriers
+    (1000, 2, 1088, 64),     # eight row groups, the last one ragged
 ])
 def test_tc_shapes(B, gamma, V, r):
     _check(_wl(f"tc_{B}_{V}_{r}", B=B, gamma=gamma, V=V, r=r, seed=B + V + r))
