@@ -36,8 +36,8 @@ METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofli
 # the ncu capture summarised in profiles/draft_tc_prod.md, and a hash of the
 # kernel source it was taken on; the roofline's "traffic" is reported only
 # while the source is unchanged.
-DRAFT_TRAFFIC = {"sha256": "d7147e0a64bb887fee9e8a41c0a07a1a93d95c47dd0214d18964981fceb2f59f",
-                 "bytes": 414790656 + 3460352}
+DRAFT_TRAFFIC = {"sha256": "9c45c4ff4f517f4c5951abfe6b7c100f9e2efcf2b185cb3d035b32b5b6267bec",
+                 "bytes": 414924800 + 3521280}
 QUOTED_HBM_GBS = 8000.0   # GB/s, the roofline constant the metric is quoted against
 
 
