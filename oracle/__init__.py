@@ -87,6 +87,7 @@ def lib():
             l.orc_residual.restype = i32
             l.orc_markov_logits.argtypes = [P, P, P, P, i32, P]
             l.orc_sts_fit.argtypes = [i32, i32, P, P, i32, P, i32, P, P, P]
+            l.orc_train_loss.argtypes = [P, P, P, P, P, P, P, P, dbl, P, P, P, P]
             l.orc_block_width.restype = i32
             l.orc_set_threads.argtypes = [i32]
             l.orc_get_threads.restype = i32
@@ -155,6 +156,28 @@ def sample_draft(logw, seed=0, rnd=0, b=0, j=0):
     m = np.zeros(1, np.float64)
     v = lib().orc_sample_draft(_p(a), a.size, seed, rnd, b, j, _p(m))
     return int(v), float(m[0])
+
+
+def train_loss(U, W1, W2, anchor, xstar, P, conf, tau: float) -> Dict[str, np.ndarray]:
+    """Teacher-forced training objective (see ``orc_train_loss``): U and P are
+    [B, gamma, V] fp32, xstar [B, gamma] int32, conf [B, gamma] fp32. Returns
+    per-position ce, l1, bce [B, gamma] fp64 and the scalar loss."""
+    U = _c(U, np.float32)
+    B, g, V = U.shape
+    W1a, bf = _weights(W1)
+    W2a, _ = _weights(W2)
+    d = _dims(B, g, V, W1a.shape[1], 0, bf)
+    an = _c(anchor, np.int32)
+    xs = _c(xstar, np.int32)
+    Pa = _c(P, np.float32)
+    cf = _c(conf, np.float32)
+    ce = np.zeros((B, g), np.float64)
+    l1 = np.zeros((B, g), np.float64)
+    bce = np.zeros((B, g), np.float64)
+    loss = np.zeros(1, np.float64)
+    lib().orc_train_loss(C.byref(d), _p(U), _p(W1a), _p(W2a), _p(an), _p(xs), _p(Pa), _p(cf), float(tau),
+                         _p(ce), _p(l1), _p(bce), _p(loss))
+    return {"ce": ce, "l1": l1, "bce": bce, "loss": float(loss[0])}
 
 
 def sts_fit(raw, cstar, Tgrid, M: int = 15):

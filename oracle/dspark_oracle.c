@@ -22,6 +22,8 @@
  *              ([V4.1 blog] "目标函数", "贪心就能解"; [csdn] 5.3). The
  *              asynchronous variant takes the capacity K = argmax Theta from
  *              lagged confidences and the top-K current candidates ([csdn] 8).
+ *   loss    -- the draft head's training objective, teacher-forced, eqs.
+ *              (9)-(12) ([V4.1 blog] "训练"; [csdn] 6; [ailearn] 07).
  *   sts     -- sequential temperature scaling of c_k: per position, left to
  *              right, the grid temperature that minimises the ECE of the
  *              cumulative product against cumulative soft labels
@@ -525,6 +527,47 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         resid[b] = from_resid;
         free(lt); free(z); free(lw); free(tol); free(tm);
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* Training objective of the draft head ([V4.1 blog] "训练：直接优化接受 */
+/* 率"; [csdn] section 6, eqs. (9)-(12); [ailearn] 07), teacher-forced:   */
+/* position k (0-based) of request b drafts from x_prev = anchor[b] for   */
+/* k = 0, else xstar[b][k-1], so every position is independent.          */
+/*   z_d = U[b,k] + W1[x_prev] W2,  p_d = softmax(z_d)                    */
+/*   p_t = softmax(P[b,k])  (the target's logits at that position)        */
+/*   ce  = -log p_d(xstar[b][k])                                (9)       */
+/*   l1  = sum_v |p_d(v) - p_t(v)|                              (10)      */
+/*   c*  = 1 - l1 / 2 (the position's acceptance probability)             */
+/*   bce = -(c* log c + (1 - c*) log(1 - c)),  c = conf[b][k]   (11)      */
+/*   loss = (1/B) sum_b sum_k w_k (0.1 ce + 0.9 l1 + 1.0 bce),            */
+/*   w_k = exp(-k / tau)                                        (12)      */
+/* ------------------------------------------------------------------ */
+void orc_train_loss(const orc_dims* d, const float* U, const void* W1, const void* W2,
+                    const int32_t* anchor, const int32_t* xstar, const float* P, const float* conf,
+                    double tau, double* ce, double* l1, double* bce, double* loss)
+{
+    const long V = d->V, g = d->gamma;
+    double total = 0.0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : total)
+    for (long o = 0; o < (long)d->B * g; ++o) {
+        const long b = o / g, k = o % g;
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* zt = (double*)malloc(sizeof(double) * (size_t)V);
+        const int x_prev = k == 0 ? anchor[b] : xstar[b * g + k - 1];
+        markov_logits(d, U + o * V, W1, W2, x_prev, z);
+        for (long v = 0; v < V; ++v) zt[v] = (double)P[o * V + v];
+        const double Ld = orc_logsumexp(z, V), Lt = orc_logsumexp(zt, V);
+        double s = 0.0;
+        for (long v = 0; v < V; ++v) s += fabs(exp(z[v] - Ld) - exp(zt[v] - Lt));
+        const double c = (double)conf[o], cs = 1.0 - 0.5 * s;
+        ce[o] = Ld - z[xstar[o]];
+        l1[o] = s;
+        bce[o] = -(cs * log(c) + (1.0 - cs) * log(1.0 - c));
+        total += exp(-(double)k / tau) * (0.1 * ce[o] + 0.9 * l1[o] + 1.0 * bce[o]);
+        free(z); free(zt);
+    }
+    *loss = total / (double)d->B;
 }
 
 /* ------------------------------------------------------------------ */

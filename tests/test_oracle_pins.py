@@ -671,3 +671,54 @@ def test_sts_is_left_to_right():
     c2[:, 1:] = rng.uniform(0.0, 1.0, (2000, 2))
     T2, e2, _ = oracle.sts_fit(raw2, c2, grid)
     assert T1[0] == T2[0] and e1[0] == e2[0]
+
+
+# ------------------------------------------------------------------ training objective
+def _loss_inputs(seed, B=3, g=3, V=150, r=8, wstd=0.0):
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0.0, 1.5, (B, g, V)).astype(np.float32)
+    W1 = (rng.normal(0.0, 1.0, (V, r)) * wstd).astype(np.float32)
+    W2 = (rng.normal(0.0, 1.0, (r, V)) * wstd).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    xstar = rng.integers(0, V, (B, g)).astype(np.int32)
+    P = (U + rng.normal(0.0, 0.7, (B, g, V))).astype(np.float32)
+    conf = rng.uniform(0.1, 0.9, (B, g)).astype(np.float32)
+    return U, W1, W2, anchor, xstar, P, conf
+
+
+def test_loss_terms_match_textbook_forms():
+    """With zero Markov weights p_d = softmax(U): ce is the cross entropy of
+    x*, l1 = 2 (1 - sum_v min(p_d, p_t)) (the acceptance identity), and bce
+    uses c* = 1 - l1 / 2."""
+    U, W1, W2, anchor, xstar, P, conf = _loss_inputs(1)
+    o = oracle.train_loss(U, W1, W2, anchor, xstar, P, conf, tau=3.0)
+    u, t = U.astype(np.float64), P.astype(np.float64)
+    pd = np.exp(u - special.logsumexp(u, axis=2, keepdims=True))
+    pt = np.exp(t - special.logsumexp(t, axis=2, keepdims=True))
+    ce = -np.log(np.take_along_axis(pd, xstar[..., None].astype(np.int64), axis=2)[..., 0])
+    l1 = 2.0 * (1.0 - np.minimum(pd, pt).sum(axis=2))
+    cs, c = 1.0 - l1 / 2.0, conf.astype(np.float64)
+    bce = -(cs * np.log(c) + (1.0 - cs) * np.log(1.0 - c))
+    assert np.allclose(o["ce"], ce, rtol=1e-12, atol=1e-12)
+    assert np.allclose(o["l1"], l1, rtol=1e-10, atol=1e-12)
+    assert np.allclose(o["bce"], bce, rtol=1e-10, atol=1e-12)
+    w = np.exp(-np.arange(U.shape[1]) / 3.0)
+    assert abs(o["loss"] - (w * (0.1 * ce + 0.9 * l1 + bce)).sum(axis=1).mean()) < 1e-10
+
+
+def test_loss_identical_distributions_and_teacher_forcing():
+    U, W1, W2, anchor, xstar, P, conf = _loss_inputs(2, wstd=0.3)
+    o = oracle.train_loss(U, W1, W2, anchor, xstar, P, conf, tau=2.0)
+    # the target equal to the draft's own logits (fp64 bias rounded to fp32 is
+    # close, not equal: l1 small, c* near 1, bce near -log c)
+    z = np.stack([[oracle.markov_logits(U[b, k], W1, W2, anchor[b] if k == 0 else xstar[b, k - 1])
+                   for k in range(U.shape[1])] for b in range(U.shape[0])])
+    o2 = oracle.train_loss(U, W1, W2, anchor, xstar, z.astype(np.float32), conf, tau=2.0)
+    assert o2["l1"].max() < 1e-5
+    assert np.allclose(o2["bce"], -np.log(conf.astype(np.float64)), atol=1e-5)
+    # teacher forcing: x*_k moves position k + 1's draft logits, not position k's
+    xs2 = xstar.copy()
+    xs2[:, 0] = (xs2[:, 0] + 17) % U.shape[2]
+    o3 = oracle.train_loss(U, W1, W2, anchor, xs2, P, conf, tau=2.0)
+    assert np.array_equal(o3["l1"][:, 0], o["l1"][:, 0])
+    assert not np.allclose(o3["l1"][:, 1], o["l1"][:, 1])
