@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sts", action="store_true", help="skip the STS calibration-fit timing")
+    ap.add_argument("--no-loss", action="store_true", help="skip the training-objective timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 
@@ -233,6 +234,40 @@ def sts_timing(reps: int = 10):
     return {"workload": "sts_prod", "N": c["N"], "gamma": c["gamma"], "grid": c["G"], "bins": c["M"],
             "ms_per_fit": ms, "evals_per_s": evals / (ms * 1e-3), "launches": 2 * c["gamma"],
             "temperatures": [round(float(t), 3) for t in T.cpu().tolist()]}
+
+
+def loss_timing(peak_gbs: float, reps: int = 10):
+    """The draft head's teacher-forced training objective on the prod shape:
+    device time per call (five launches), CUDA events on the launching stream
+    after warm-up, inputs resident (U and P, 0.66 GB, exceed the L2). The
+    algorithmic bytes are two passes over U and P plus W2 once per pass."""
+    import torch
+    from speculative_decoding_head_gb300.binding import Workspace
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_loss_inputs
+    wl = WORKLOADS["prod"]
+    tau = 4.0
+    inp = {k: v.cuda() for k, v in make_loss_inputs(wl).items()}
+    ws = Workspace.for_workload(wl)
+    out = ws.new_loss_outputs()
+    args = (inp["U"], inp["W1"], inp["W2"], inp["anchor"], inp["xstar"], inp["P"], inp["conf"], tau)
+    for _ in range(3):
+        ws.train_loss(*args, out=out)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        ws.train_loss(*args, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    n = wl.B * wl.gamma
+    alg = 2 * (2 * n * wl.V * 4 + wl.r * wl.V * 2)
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"workload": "prod", "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "ms_per_call": ms,
+            "positions_per_s": n / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches,
+            "loss": float(out["loss"].item())}
 
 
 def run_reference(args):
@@ -440,6 +475,7 @@ def main():
             "emitted_tokens_per_round": emitted,
             "stage_ms": st,
             "sts_fit": None if args.no_sts else sts_timing(),
+            "train_loss": None if args.no_loss else loss_timing(peak),
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": e2e,

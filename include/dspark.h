@@ -227,6 +227,35 @@ dspark_status dspark_sts_fit(const float* raw, const float* cstar, int N, int ga
                              int32_t* device_status, dspark_stream_t stream);
 size_t dspark_sts_scratch_bytes(int N, int G);
 
+/*
+ * The draft head's teacher-forced training objective
+ * ("DeepSeek-V4.1 模型结构（6）：解码，DSpark", section on training the head for
+ * the acceptance rate; deepseek.csdn.net §6, eqs. (9)-(12)). Position k of
+ * request b drafts from x_prev = anchor[b] (k = 0) or xstar[b][k-1]; with
+ * z_d = U[b][k] + W1[x_prev] W2, p_d = softmax(z_d), p_t = softmax(P[b][k]):
+ *   ce[b][k]  = logsumexp(z_d) - z_d[xstar[b][k]]
+ *   l1[b][k]  = sum_v |p_d(v) - p_t(v)|
+ *   bce[b][k] = -(c* log c + (1 - c*) log(1 - c)),  c* = 1 - l1 / 2, c = conf[b][k]
+ *   *loss     = (1/B) sum_{b,k} exp(-k / tau) (0.1 ce + 0.9 l1 + bce)
+ * The workspace's dims give B, gamma, V, r; the call needs bf16 weights,
+ * r a multiple of 64 up to 256, V % 8 == 0 and B <= 1024 (else
+ * DSPARK_EUNSUPPORTED). U and P are [B][gamma][V] fp32 (P: the target's logits
+ * at the teacher-forced positions), W1 [V][r] and W2 [r][V] bf16, anchor [B]
+ * and xstar [B][gamma] int32, conf [B][gamma] fp32 in (0, 1); ce, l1, bce
+ * [B][gamma] fp32 and loss [1] fp64 receive the results. Every pointer is a
+ * 16-byte aligned device pointer owned by the caller (loss: 8-byte);
+ * scratch holds dspark_train_loss_scratch_bytes(ws) bytes, 256-byte aligned.
+ * tau must be positive and finite (else DSPARK_EINVAL). A token id out of
+ * [0, V) raises DSPARK_ERANGE and a confidence outside (0, 1) DSPARK_ENUMERIC
+ * in the workspace's device status (dspark_last_error). Five launches,
+ * asynchronous on `stream`; W2 is read through the L2 by every 32 positions.
+ */
+dspark_status dspark_train_loss(dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                const int32_t* anchor, const int32_t* xstar, const float* P, const float* conf,
+                                double tau, float* ce, float* l1, float* bce, double* loss, void* scratch,
+                                dspark_stream_t stream);
+size_t dspark_train_loss_scratch_bytes(const dspark_ws* ws);
+
 #ifdef __cplusplus
 }
 #endif

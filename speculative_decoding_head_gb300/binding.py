@@ -23,7 +23,7 @@ SYMBOLS = [
     "dspark_ws_create", "dspark_ws_destroy", "dspark_ws_reset", "dspark_last_error",
     "dspark_status_string", "dspark_last_launch_count", "dspark_path",
     "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
-    "dspark_sts_fit", "dspark_sts_scratch_bytes",
+    "dspark_sts_fit", "dspark_sts_scratch_bytes", "dspark_train_loss", "dspark_train_loss_scratch_bytes",
 ]
 
 
@@ -82,6 +82,10 @@ def load() -> C.CDLL:
         lib.dspark_sts_fit.restype = i32
         lib.dspark_sts_scratch_bytes.argtypes = [i32, i32]
         lib.dspark_sts_scratch_bytes.restype = C.c_size_t
+        lib.dspark_train_loss.argtypes = [P] * 8 + [C.c_double] + [P] * 6
+        lib.dspark_train_loss.restype = i32
+        lib.dspark_train_loss_scratch_bytes.argtypes = [P]
+        lib.dspark_train_loss_scratch_bytes.restype = C.c_size_t
         _lib = lib
         return lib
 
@@ -238,6 +242,29 @@ class Workspace:
             _ptr(W2, self.wdtype, "W2"), int(seed), int(rnd), _ptr(out["n_acc"], i32, "n_acc"),
             _ptr(out["next_anchor"], i32, "next_anchor"), _stream(stream))
         _check(code, "dspark_verify")
+        return out
+
+    def new_loss_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:
+        B, g = self.dims.B, self.dims.gamma
+        return {"ce": torch.empty(B, g, dtype=torch.float32, device=device),
+                "l1": torch.empty(B, g, dtype=torch.float32, device=device),
+                "bce": torch.empty(B, g, dtype=torch.float32, device=device),
+                "loss": torch.empty(1, dtype=torch.float64, device=device),
+                "scratch": torch.empty(int(self.lib.dspark_train_loss_scratch_bytes(self._h)), dtype=torch.uint8,
+                                       device=device)}
+
+    def train_loss(self, U, W1, W2, anchor, xstar, P, conf, tau: float, out=None, stream=None):
+        """Teacher-forced training objective (``dspark_train_loss``): U and P
+        [B, gamma, V] fp32, xstar and conf [B, gamma]; per-position ce, l1,
+        bce and the scalar loss stay on the device."""
+        out = out or self.new_loss_outputs(U.device)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_train_loss(
+            self._h, _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"), _ptr(W2, self.wdtype, "W2"),
+            _ptr(anchor, i32, "anchor"), _ptr(xstar, i32, "xstar"), _ptr(P, f32, "P"), _ptr(conf, f32, "conf"),
+            float(tau), _ptr(out["ce"], f32, "ce"), _ptr(out["l1"], f32, "l1"), _ptr(out["bce"], f32, "bce"),
+            _ptr(out["loss"], torch.float64, "loss"), _ptr(out["scratch"], None, "scratch"), _stream(stream))
+        _check(code, "dspark_train_loss")
         return out
 
     def round(self, U, W1, W2, anchor, h, w, T, sps, P, seed: int, rnd: int, out=None, stream=None):

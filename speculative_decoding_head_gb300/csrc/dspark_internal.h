@@ -43,6 +43,29 @@ struct VerifyArgs {
   int32_t* next_anchor;
 };
 
+// The draft head's teacher-forced training objective: inputs, outputs and the
+// caller's scratch (column i = b * gamma + k, G = ws->geo.num_sms partials).
+struct LossArgs {
+  const float* U;
+  const void* W1;
+  const void* W2;
+  const int32_t* anchor;
+  const int32_t* xstar;
+  const float* P;
+  const float* conf;
+  double tau;
+  float* ce;
+  float* l1;
+  float* bce;
+  double* loss;
+  float4* lpart;   // [B*gamma][G] (max, sum exp) of z_d and of z_t per CTA
+  float* l1part;   // [B*gamma][G] sum |p_d - p_t| per CTA
+  float* zx;       // [B*gamma] z_d at x*
+  float* lse_d;    // [B*gamma]
+  float* lse_t;    // [B*gamma]
+  double* term;    // [B*gamma] w_k (0.1 ce + 0.9 l1 + bce)
+};
+
 // Device scratch carved out of one arena by dspark_ws_create.
 struct Scratch {
   int* status;            // [1] first device error, 0 = none
@@ -113,6 +136,9 @@ size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch
 int resid_tc_supported(const dspark_dims& d);
 cudaError_t resid_tc_configure(dspark_ws* ws);
 cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st);
+// pass 0: per-CTA (max, sum exp) of z_d and z_t and z_d at x*; pass 1: per-CTA
+// sum |p_d - p_t| (needs lse_d, lse_t). Grid = ws->geo.num_sms.
+cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);
 
 size_t plan_smem_bytes(const dspark_dims& d);
 cudaError_t sweep_bulk_configure();

@@ -47,6 +47,13 @@ static_assert(kRN == 32, "one 32-request chunk per tile, 16 requests for each wa
 constexpr int kRGMax = 16;        // block Gumbels of a group kept in shared memory (blocks per CTA)
 constexpr int kRMaxB = 1024;
 
+// What a launch computes over its columns (MMA N): the residual block draw of
+// the rejected requests, or one of the two passes of the draft head's
+// teacher-forced training objective over every position (b, k).
+constexpr int kModeResid = 0;      // per block: residual mass and Gumbel key; the best block per CTA
+constexpr int kModeLossStats = 1;  // per column: (max, sum exp) of z_d and of z_t over the CTA's tiles, z_d at x*
+constexpr int kModeLossL1 = 2;     // per column: sum |p_d - p_t| over the CTA's tiles
+
 struct RSmem {
   uint32_t bop, w2, up, col, part, best, gum, list, bars, misc, total;
   __host__ __device__ static RSmem make(int r) {
@@ -55,8 +62,8 @@ struct RSmem {
     s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r x 64] bf16)
     s.up = s.w2 + kRNW * 2 * r * 128;       // kRUP x [request][U slice | P slice] fp32
     s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row (int), lse_d, lse_t (float)
-    s.part = s.col + 5 * 4 * kRN;           // [4 warps][128] block partial sums
-    s.best = s.part + 4 * 4 * kRN;          // [128] best key, [128] best block
+    s.part = s.col + 5 * 4 * kRN;           // [4 quarters][32 columns] partials (float4 for the loss statistics)
+    s.best = s.part + 4 * 16 * kRN;         // [128] best key, [128] best block
     s.gum = s.best + 2 * 4 * kRN;           // [kRN][kRGMax] block Gumbels of this CTA's blocks
     s.list = s.gum + 4 * kRN * kRGMax;      // [kRMaxB] rejected requests
     s.bars = s.list + 4 * kRMaxB;
@@ -82,6 +89,13 @@ struct RParams {
   const float* vlset;
   float2* rpart;  // [B][G] (key, block) of each CTA
   int* status;
+  // the training objective's passes: column i = b * g + k (teacher-forced)
+  const int32_t* xstar;  // [B][g] the reference tokens x*
+  float4* lpart;         // [B*g][G] (max, sum exp) of z_d, then of z_t, over the CTA's tiles
+  float* zx;             // [B*g] z_d at x*
+  float* l1part;         // [B*g][G] sum |p_d - p_t| over the CTA's tiles
+  const float* lse_d;    // [B*g]
+  const float* lse_t;    // [B*g]
 };
 
 // Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
@@ -103,6 +117,23 @@ __device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
   return a[0] + __shfl_xor_sync(0xFFFFFFFFu, a[0], 16);
 }
 
+// The same transpose over 32 lanes with a maximum instead of a sum.
+__device__ __forceinline__ float transpose_max16(float (&a)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? a[k] : a[k + o];
+      const float keep = upper ? a[k + o] : a[k];
+      a[k] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+    }
+  }
+  return fmaxf(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 16));
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kRThreads, 1)
     k_resid_tc(const __grid_constant__ CUtensorMap tm_w2, const RParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -166,16 +197,20 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // The flags, positions and rows are this round's only if every stage so far
   // left the status clear: an error leaves the list empty.
   if (warp == 2) {
-    const bool clear = __shfl_sync(0xFFFFFFFFu, *(volatile int*)p.status, 0) == 0;
-    int base = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-      const int b = b0 + lane;
-      const bool f = clear && b < p.B && p.vflag[b] != 0;
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
-      if (f) list[base + __popc(m & ((1u << lane) - 1u))] = b;
-      base += __popc(m);
+    if constexpr (MODE == kModeResid) {
+      const bool clear = __shfl_sync(0xFFFFFFFFu, *(volatile int*)p.status, 0) == 0;
+      int base = 0;
+      for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        const bool f = clear && b < p.B && p.vflag[b] != 0;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+        if (f) list[base + __popc(m & ((1u << lane) - 1u))] = b;
+        base += __popc(m);
+      }
+      if (lane == 0) *s_nrej = base;
+    } else {
+      if (lane == 0) *s_nrej = p.B * p.g;  // every position is a column
     }
-    if (lane == 0) *s_nrej = base;
   }
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(tmem_holder), kRTmemCols);
@@ -226,9 +261,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
       const float* urow = p.U;
       const float* prow = p.P;
       if (lane < ncols) {
-        const int b = list[gq * kRN + lane];
-        urow = p.U + ((size_t)b * p.g + min(max(p.n_acc[b], 0), p.g - 1)) * p.V;
-        prow = p.P + (size_t)min(max(p.vrow[b], 0), p.B * (p.g + 1) - 1) * p.V;
+        if constexpr (MODE == kModeResid) {
+          const int b = list[gq * kRN + lane];
+          urow = p.U + ((size_t)b * p.g + min(max(p.n_acc[b], 0), p.g - 1)) * p.V;
+          prow = p.P + (size_t)min(max(p.vrow[b], 0), p.B * (p.g + 1) - 1) * p.V;
+        } else {  // position i of the objective: U row i, target logits row i
+          urow = p.U + (size_t)(gq * kRN + lane) * p.V;
+          prow = p.P + (size_t)(gq * kRN + lane) * p.V;
+        }
       }
       for (int i = 0; i < nt && ok; ++i) {
         const int it = gq * nt + i, us = it % kRUP, v0 = (tile_lo + i) * kRM;
@@ -308,14 +348,31 @@ __global__ void __launch_bounds__(kRThreads, 1)
         int x = 0;
         const bool valid = et < kRN && i < nrej;
         if (valid) {
-          const int b = list[i];
-          const int n = min(max(p.n_acc[b], 0), p.g - 1);  // a rejection leaves n <= gamma - 1
-          x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
-          col_b[et] = b;
-          col_n[et] = n;
-          col_row[et] = p.vrow[b];
-          col_nld[et] = -p.lse[(size_t)b * p.g + n] * tc::kLog2e;
-          col_nlt[et] = -p.vlset[b] * tc::kLog2e;
+          if constexpr (MODE == kModeResid) {
+            const int b = list[i];
+            const int n = min(max(p.n_acc[b], 0), p.g - 1);  // a rejection leaves n <= gamma - 1
+            x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
+            col_b[et] = b;
+            col_n[et] = n;
+            col_row[et] = p.vrow[b];
+            col_nld[et] = -p.lse[(size_t)b * p.g + n] * tc::kLog2e;
+            col_nlt[et] = -p.vlset[b] * tc::kLog2e;
+          } else {  // teacher forcing: position k drafts from x*_{k-1} (the anchor at k = 0)
+            const int b = i / p.g, k = i - b * p.g;
+            x = k == 0 ? p.anchor[b] : p.xstar[i - 1];
+            col_b[et] = i;
+            col_n[et] = k;
+            int xt = p.xstar[i];
+            if (xt < 0 || xt >= p.V) {
+              raise_status(p.status, DSPARK_ERANGE);
+              xt = 0;
+            }
+            col_row[et] = xt;  // the reference token, whose z_d the cross entropy needs
+            if constexpr (MODE == kModeLossL1) {
+              col_nld[et] = -p.lse_d[i] * tc::kLog2e;
+              col_nlt[et] = -p.lse_t[i] * tc::kLog2e;
+            }
+          }
           if (x < 0 || x >= p.V) {
             raise_status(p.status, DSPARK_ERANGE);
             x = 0;
@@ -324,6 +381,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
         if (et < kRN) {
           best_key[et] = -INFINITY;
           best_blk[et] = kNoIdx;
+          // running (max, sum exp) of z_d and of z_t, or the running |p_d - p_t| sum
+          if constexpr (MODE == kModeLossStats)
+            reinterpret_cast<float4*>(gsm)[et] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+          else if constexpr (MODE == kModeLossL1)
+            reinterpret_cast<float4*>(gsm)[et] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const int m = et;
         for (int kb = 0; kb < p.r / 64 && et < kRN; ++kb) {
@@ -348,7 +410,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       // computed once up front (visible to the combining warp after the first
       // tile's barrier) instead of on the per-tile critical path
       const int nbl = 2 * nt;
-      const bool gpre = nbl <= kRGMax;
+      const bool gpre = MODE == kModeResid && nbl <= kRGMax;
       if (gpre)
         for (int idx = et; idx < ncols * nbl; idx += 32 * kREpi) {
           const int col = idx / nbl, lb = idx - col * nbl;
@@ -386,17 +448,50 @@ __global__ void __launch_bounds__(kRThreads, 1)
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * (2 * kRM * 4)));
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * (2 * kRM * 4) + kRM * 4));
             }
+            if constexpr (MODE == kModeLossStats) {
+              // per column, over this warp's 32 entries: max and sum exp of
+              // z_d = D + U and of z_t = P (a transpose-max, every lane takes
+              // its columns' maxima, then a transpose-sum)
+              float zd[16], zt[16], e[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = half * 16 + j;
-              const int cl = min(col, ncols - 1);
-              // p_t - p_d = 2^(P log2e - lse_t log2e) - 2^(z_d log2e - lse_d log2e), z_d = D + U
-              const float w = fmaxf(0.f, tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[cl])) -
-                                             tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[cl])));
-              a[j] = (col < ncols && v < p.V) ? w : 0.f;
+              for (int j = 0; j < 16; ++j) {
+                const int col = half * 16 + j;
+                const bool ok = col < ncols && v < p.V;
+                zd[j] = ok ? a[j] + uu[j] : -INFINITY;
+                zt[j] = ok ? pp[j] : -INFINITY;
+                if (ok && v == col_row[col]) p.zx[col_b[col]] = zd[j];  // z_d at x*: one entry of the grid
+              }
+              float m4[4];
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                float* z = w == 0 ? zd : zt;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) e[j] = z[j];
+                const float mx = transpose_max16(e);  // lane l: column l & 15
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const float mj = __shfl_sync(0xFFFFFFFFu, mx, j);
+                  e[j] = z[j] == -INFINITY ? 0.f : tc::ex2_ftz((z[j] - mj) * tc::kLog2e);
+                }
+                m4[2 * w] = mx;
+                m4[2 * w + 1] = transpose_sum16(e);
+              }
+              if (lane < 16)
+                reinterpret_cast<float4*>(part)[q * kRN + half * 16 + lane] = make_float4(m4[0], m4[1], m4[2], m4[3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int col = half * 16 + j;
+                const int cl = min(col, ncols - 1);
+                // p_t - p_d = 2^(P log2e - lse_t log2e) - 2^(z_d log2e - lse_d log2e), z_d = D + U
+                const float d = tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[cl])) -
+                                tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[cl]));
+                const float w = MODE == kModeResid ? fmaxf(0.f, d) : fabsf(d);
+                a[j] = (col < ncols && v < p.V) ? w : 0.f;
+              }
+              const float s = transpose_sum16(a);  // this warp's 32 entries, column 16 half + (lane & 15)
+              if (lane < 16) part[q * kRN + half * 16 + lane] = s;
             }
-            const float s = transpose_sum16(a);  // this warp's 32 entries, request 16 half + (lane & 15)
-            if (lane < 16) part[q * kRN + half * 16 + lane] = s;
           }
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(up_empty(us));
@@ -405,7 +500,24 @@ __global__ void __launch_bounds__(kRThreads, 1)
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
         }
         asm volatile("bar.sync 2, 256;" ::: "memory");
-        if (live && warp == 4) {
+        if constexpr (MODE == kModeLossStats) {
+          if (live && warp == 4)
+            for (int col = lane; col < ncols; col += 32) {
+              float4 r = reinterpret_cast<float4*>(gsm)[col];
+              MS md{r.x, r.y}, mt{r.z, r.w};
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                const float4 pq = reinterpret_cast<const float4*>(part)[qq * kRN + col];
+                md = ms_combine(md, MS{pq.x, pq.y});
+                mt = ms_combine(mt, MS{pq.z, pq.w});
+              }
+              reinterpret_cast<float4*>(gsm)[col] = make_float4(md.m, md.s, mt.m, mt.s);
+            }
+        } else if constexpr (MODE == kModeLossL1) {
+          if (live && warp == 4)
+            for (int col = lane; col < ncols; col += 32)
+              gsm[4 * col] += (part[col] + part[kRN + col]) + (part[2 * kRN + col] + part[3 * kRN + col]);
+        } else if (live && warp == 4) {
           // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
           for (int col = lane; col < ncols; col += 32) {
             const int b = col_b[col], n = col_n[col];
@@ -426,8 +538,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
         asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
       }
       if (warp == 4 && !aborted()) {
-        for (int col = lane; col < ncols; col += 32)
-          p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
+        for (int col = lane; col < ncols; col += 32) {
+          if constexpr (MODE == kModeResid)
+            p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
+          else if constexpr (MODE == kModeLossStats)
+            p.lpart[(size_t)col_b[col] * p.G + c] = reinterpret_cast<const float4*>(gsm)[col];
+          else
+            p.l1part[(size_t)col_b[col] * p.G + c] = gsm[4 * col];
+        }
       }
       asm volatile("bar.sync 2, 256;" ::: "memory");  // constants are rewritten by the next group
     }
@@ -462,10 +580,14 @@ int resid_tc_supported(const dspark_dims& d) {
 cudaError_t resid_tc_configure(dspark_ws* ws) {
   const RSmem L = RSmem::make(ws->d.r);
   const size_t smem = L.total + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_resid_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_resid_tc<kModeResid>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_resid_tc<kModeLossStats>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_resid_tc<kModeLossL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_resid_tc, kRThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_resid_tc<kModeResid>, kRThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1 || !encode_fn()) return cudaErrorNotSupported;
   return cudaSuccess;
@@ -474,19 +596,25 @@ cudaError_t resid_tc_configure(dspark_ws* ws) {
 // The residual block draw for the requests verify flagged; writes
 // rpart[b * grid + cta]. Grid = one CTA per SM (no grid-wide barrier, so no
 // co-residency requirement).
-cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st) {
-  const dspark_dims& d = ws->d;
+namespace {
+
+// W2 as [r rows x V] bf16, boxes of [r x 64] with the 128-byte swizzle.
+cudaError_t w2_tensor_map(const dspark_dims& d, const void* W2, CUtensorMap* tm) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap tm;
   const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
   const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)d.r};
   const cuuint32_t es[2] = {1, 1};
-  if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, strides, box, es,
+  if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+RParams base_params(const dspark_ws* ws, int grid) {
+  const dspark_dims& d = ws->d;
   RParams p;
   memset(&p, 0, sizeof(p));
   p.B = d.B;
@@ -495,6 +623,18 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.r = d.r;
   p.ntiles = (d.V + kRM - 1) / kRM;
   p.G = grid;
+  p.status = ws->s.status;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  CUtensorMap tm;
+  cudaError_t e = w2_tensor_map(d, a.W2, &tm);
+  if (e != cudaSuccess) return e;
+  RParams p = base_params(ws, grid);
   p.rng = Rng::make(a.seed, a.round);
   p.P = a.P;
   p.U = a.U;
@@ -507,9 +647,32 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.vrow = ws->s.vrow;
   p.vlset = ws->s.vlset;
   p.rpart = rpart;
-  p.status = ws->s.status;
   const RSmem L = RSmem::make(d.r);
-  k_resid_tc<<<grid, kRThreads, L.total + 1024, st>>>(tm, p);
+  k_resid_tc<kModeResid><<<grid, kRThreads, L.total + 1024, st>>>(tm, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  CUtensorMap tm;
+  cudaError_t e = w2_tensor_map(d, a.W2, &tm);
+  if (e != cudaSuccess) return e;
+  RParams p = base_params(ws, ws->geo.num_sms);
+  p.P = a.P;
+  p.U = a.U;
+  p.W1 = a.W1;
+  p.anchor = a.anchor;
+  p.xstar = a.xstar;
+  p.lpart = a.lpart;
+  p.zx = a.zx;
+  p.l1part = a.l1part;
+  p.lse_d = a.lse_d;
+  p.lse_t = a.lse_t;
+  const RSmem L = RSmem::make(d.r);
+  if (pass == 0)
+    k_resid_tc<kModeLossStats><<<p.G, kRThreads, L.total + 1024, st>>>(tm, p);
+  else
+    k_resid_tc<kModeLossL1><<<p.G, kRThreads, L.total + 1024, st>>>(tm, p);
   return cudaGetLastError();
 }
 

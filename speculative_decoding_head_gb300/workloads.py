@@ -182,6 +182,23 @@ def make_sts_inputs(N: int, gamma: int, seed: int, device: str = "cpu") -> Dict[
     return {"raw": raw.to(torch.float32).to(device), "cstar": cstar.to(torch.float32).to(device)}
 
 
+def make_loss_inputs(wl: Workload, seed_offset: int = 104729) -> Dict[str, torch.Tensor]:
+    """Inputs of the teacher-forced training objective for workload ``wl`` (CPU).
+
+    U, W1, W2 and the anchors are the round's; P [B, gamma, V] is the target's
+    logits at the gamma drafted positions (rows 0..gamma-1 of the round's
+    target rows); the reference tokens x* are uniform over the vocabulary and
+    the confidences uniform in [0.02, 0.98].
+    """
+    base = make_inputs(wl)
+    gen = torch.Generator().manual_seed(wl.seed + seed_offset)
+    B, g, V = wl.B, wl.gamma, wl.V
+    return {"U": base["U"], "W1": base["W1"], "W2": base["W2"], "anchor": base["anchor"],
+            "P": base["P_full"][:, :g].contiguous(),
+            "xstar": torch.randint(0, V, (B, g), generator=gen, dtype=torch.int64).to(torch.int32),
+            "conf": (0.02 + 0.96 * torch.rand(B, g, generator=gen)).to(torch.float32)}
+
+
 def pack_rows(P_full: torch.Tensor, lengths: torch.Tensor) -> torch.Tensor:
     """Packed ragged target logits [sum(lengths), V]: rows 0..lengths[b]-1 of each request.
 

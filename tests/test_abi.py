@@ -91,3 +91,10 @@ def test_sts_fit_arguments_are_checked_on_the_host(lib):
     assert call(raw=None) == 1 and call(scratch=None) == 1 and call(st=None) == 1
     assert call(N=1 << 23) == 5                          # the fixed-point bin sums' range
     assert lib.dspark_sts_scratch_bytes(1000, 10) == 8 * 10 * 8 * 32 + 8 * 10 + 16 * 1000
+
+
+def test_train_loss_arguments_are_checked_on_the_host(lib):
+    """No workspace or a null pointer is EINVAL before any CUDA call."""
+    fake = ctypes.c_void_p(256)
+    assert lib.dspark_train_loss(None, *([fake] * 7), 4.0, *([fake] * 5), None) == 1
+    assert lib.dspark_train_loss_scratch_bytes(None) == 0
