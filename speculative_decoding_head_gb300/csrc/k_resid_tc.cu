@@ -117,20 +117,42 @@ __device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
   return a[0] + __shfl_xor_sync(0xFFFFFFFFu, a[0], 16);
 }
 
-// The same transpose over 32 lanes with a maximum instead of a sum.
-__device__ __forceinline__ float transpose_max16(float (&a)[16]) {
+constexpr float kNegBig = -1e30f;  // "no entry yet" of a running maximum (finite: no inf - inf)
+constexpr float kLn2 = 0.693147180559945309f;
+
+// y joins a running (m, s = sum 2^(y_i - m)) pair: one ex2 per entry.
+__device__ __forceinline__ void online_add(float& m, float& s, float y) {
+  const float d = y - m;
+  const float e = tc::ex2_ftz(-fabsf(d));
+  s = d > 0.f ? fmaf(s, e, 1.f) : s + e;
+  m = fmaxf(m, y);
+}
+
+// Two (m, s) pairs in base 2 combined.
+__device__ __forceinline__ float2 ms2_combine(float2 a, float2 b) {
+  const float m = fmaxf(a.x, b.x);
+  return make_float2(m, fmaf(a.y, tc::ex2_ftz(a.x - m), b.y * tc::ex2_ftz(b.x - m)));
+}
+
+// The transpose of transpose_sum16 over (m, s) pairs: afterwards lane L holds
+// the combination of every lane's pair L & 15.
+__device__ __forceinline__ float2 transpose_ms16(float (&m)[16], float (&s)[16]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 8; o >= 1; o >>= 1) {
     const bool upper = (lane & o) != 0;
 #pragma unroll
     for (int k = 0; k < o; ++k) {
-      const float send = upper ? a[k] : a[k + o];
-      const float keep = upper ? a[k + o] : a[k];
-      a[k] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+      const float sm = upper ? m[k] : m[k + o], ss = upper ? s[k] : s[k + o];
+      const float km = upper ? m[k + o] : m[k], ks = upper ? s[k + o] : s[k];
+      const float2 r = ms2_combine(make_float2(km, ks), make_float2(__shfl_xor_sync(0xFFFFFFFFu, sm, o),
+                                                                   __shfl_xor_sync(0xFFFFFFFFu, ss, o)));
+      m[k] = r.x;
+      s[k] = r.y;
     }
   }
-  return fmaxf(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 16));
+  return ms2_combine(make_float2(m[0], s[0]),
+                     make_float2(__shfl_xor_sync(0xFFFFFFFFu, m[0], 16), __shfl_xor_sync(0xFFFFFFFFu, s[0], 16)));
 }
 
 template <int MODE>
@@ -171,6 +193,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int tile_lo = (int)((long long)c * p.ntiles / p.G);
   const int tile_hi = (int)((long long)(c + 1) * p.ntiles / p.G);
   const int nt = tile_hi - tile_lo;
+  // The loss modes walk the CTA's tiles forwards in even groups and backwards
+  // in odd ones, so the W2 tiles used last are the first reused (from L2).
+  auto tile_of = [&](int gq, int i) { return tile_lo + ((MODE != kModeResid && (gq & 1)) ? nt - 1 - i : i); };
   const uint32_t box_bytes = (uint32_t)p.r * 128u;  // one [r x 64] bf16 box
   const uint32_t w2_bytes = 2u * box_bytes;
 
@@ -231,7 +256,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       bool ok = true;
       for (int gq = 0; gq < ngroups && ok; ++gq) {
         for (int i = 0; i < nt && ok; ++i) {
-          const int it = gq * nt + i, t = tile_lo + i, ws = it % kRNW;
+          const int it = gq * nt + i, t = tile_of(gq, i), ws = it % kRNW;
           ok = tc::mbar_wait(w2_empty(ws), ((it / kRNW) & 1) ^ 1, abort);
           if (!ok) break;
           tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
@@ -271,7 +296,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
       }
       for (int i = 0; i < nt && ok; ++i) {
-        const int it = gq * nt + i, us = it % kRUP, v0 = (tile_lo + i) * kRM;
+        const int it = gq * nt + i, us = it % kRUP, v0 = tile_of(gq, i) * kRM;
         const uint32_t bytes = (uint32_t)min(kRM, p.V - v0) * 4u;  // a multiple of 32 (V % 8 == 0)
         int got = 1;
         if (lane == 0) got = tc::mbar_wait(up_empty(us), ((it / kRUP) & 1) ^ 1, abort) ? 1 : 0;
@@ -381,11 +406,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
         if (et < kRN) {
           best_key[et] = -INFINITY;
           best_blk[et] = kNoIdx;
-          // running (max, sum exp) of z_d and of z_t, or the running |p_d - p_t| sum
-          if constexpr (MODE == kModeLossStats)
-            reinterpret_cast<float4*>(gsm)[et] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-          else if constexpr (MODE == kModeLossL1)
-            reinterpret_cast<float4*>(gsm)[et] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const int m = et;
         for (int kb = 0; kb < p.r / 64 && et < kRN; ++kb) {
@@ -416,8 +436,18 @@ __global__ void __launch_bounds__(kRThreads, 1)
           const int col = idx / nbl, lb = idx - col * nbl;
           gsm[col * kRGMax + lb] = gumbel(p.rng.word(kResidBlock, col_b[col], col_n[col], 2 * tile_lo + lb));
         }
+      // the loss modes' running values of this thread's entries, per column of
+      // its half: (max, sum) of z_d and of z_t in base 2, or sum |p_d - p_t|
+      float ra[16], rb[16], rc[16], rd[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        ra[j] = MODE == kModeLossStats ? kNegBig : 0.f;
+        rb[j] = 0.f;
+        rc[j] = kNegBig;
+        rd[j] = 0.f;
+      }
       for (int i = 0; i < nt; ++i) {
-        const int it = gq * nt + i, t = tile_lo + i, ab = it & 1, us = it % kRUP;
+        const int it = gq * nt + i, t = tile_of(gq, i), ab = it & 1, us = it % kRUP;
         bool live = !aborted();
         if (live) {
           bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
@@ -449,47 +479,36 @@ __global__ void __launch_bounds__(kRThreads, 1)
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * (2 * kRM * 4) + kRM * 4));
             }
             if constexpr (MODE == kModeLossStats) {
-              // per column, over this warp's 32 entries: max and sum exp of
-              // z_d = D + U and of z_t = P (a transpose-max, every lane takes
-              // its columns' maxima, then a transpose-sum)
-              float zd[16], zt[16], e[16];
+              // running (max, sum 2^(y - max)) of y = z log2(e) per column,
+              // for z_d = D + U and z_t = P; the entry of x* records z_d
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int col = half * 16 + j;
                 const bool ok = col < ncols && v < p.V;
-                zd[j] = ok ? a[j] + uu[j] : -INFINITY;
-                zt[j] = ok ? pp[j] : -INFINITY;
-                if (ok && v == col_row[col]) p.zx[col_b[col]] = zd[j];  // z_d at x*: one entry of the grid
+                const float zd = a[j] + uu[j];
+                if (ok && v == col_row[col]) p.zx[col_b[col]] = zd;  // z_d at x*: one entry of the grid
+                online_add(ra[j], rb[j], ok ? zd * tc::kLog2e : -INFINITY);
+                online_add(rc[j], rd[j], ok ? pp[j] * tc::kLog2e : -INFINITY);
               }
-              float m4[4];
+            } else if constexpr (MODE == kModeLossL1) {
 #pragma unroll
-              for (int w = 0; w < 2; ++w) {
-                float* z = w == 0 ? zd : zt;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) e[j] = z[j];
-                const float mx = transpose_max16(e);  // lane l: column l & 15
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const float mj = __shfl_sync(0xFFFFFFFFu, mx, j);
-                  e[j] = z[j] == -INFINITY ? 0.f : tc::ex2_ftz((z[j] - mj) * tc::kLog2e);
-                }
-                m4[2 * w] = mx;
-                m4[2 * w + 1] = transpose_sum16(e);
+              for (int j = 0; j < 16; ++j) {
+                const int col = half * 16 + j;
+                const float d = tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[col])) -
+                                tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[col]));
+                ra[j] += (col < ncols && v < p.V) ? fabsf(d) : 0.f;
               }
-              if (lane < 16)
-                reinterpret_cast<float4*>(part)[q * kRN + half * 16 + lane] = make_float4(m4[0], m4[1], m4[2], m4[3]);
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int col = half * 16 + j;
                 const int cl = min(col, ncols - 1);
                 // p_t - p_d = 2^(P log2e - lse_t log2e) - 2^(z_d log2e - lse_d log2e), z_d = D + U
-                const float d = tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[cl])) -
-                                tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[cl]));
-                const float w = MODE == kModeResid ? fmaxf(0.f, d) : fabsf(d);
+                const float w = fmaxf(0.f, tc::ex2_ftz(fmaf(pp[j], tc::kLog2e, col_nlt[cl])) -
+                                               tc::ex2_ftz(fmaf(a[j] + uu[j], tc::kLog2e, col_nld[cl])));
                 a[j] = (col < ncols && v < p.V) ? w : 0.f;
               }
-              const float s = transpose_sum16(a);  // this warp's 32 entries, column 16 half + (lane & 15)
+              const float s = transpose_sum16(a);  // this warp's 32 entries, request 16 half + (lane & 15)
               if (lane < 16) part[q * kRN + half * 16 + lane] = s;
             }
           }
@@ -499,53 +518,63 @@ __global__ void __launch_bounds__(kRThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
         }
-        asm volatile("bar.sync 2, 256;" ::: "memory");
-        if constexpr (MODE == kModeLossStats) {
-          if (live && warp == 4)
+        if constexpr (MODE == kModeResid) {
+          asm volatile("bar.sync 2, 256;" ::: "memory");
+          if (live && warp == 4) {
+            // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
             for (int col = lane; col < ncols; col += 32) {
-              float4 r = reinterpret_cast<float4*>(gsm)[col];
-              MS md{r.x, r.y}, mt{r.z, r.w};
+              const int b = col_b[col], n = col_n[col];
 #pragma unroll
-              for (int qq = 0; qq < 4; ++qq) {
-                const float4 pq = reinterpret_cast<const float4*>(part)[qq * kRN + col];
-                md = ms_combine(md, MS{pq.x, pq.y});
-                mt = ms_combine(mt, MS{pq.z, pq.w});
-              }
-              reinterpret_cast<float4*>(gsm)[col] = make_float4(md.m, md.s, mt.m, mt.s);
-            }
-        } else if constexpr (MODE == kModeLossL1) {
-          if (live && warp == 4)
-            for (int col = lane; col < ncols; col += 32)
-              gsm[4 * col] += (part[col] + part[kRN + col]) + (part[2 * kRN + col] + part[3 * kRN + col]);
-        } else if (live && warp == 4) {
-          // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
-          for (int col = lane; col < ncols; col += 32) {
-            const int b = col_b[col], n = col_n[col];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int s = 2 * t + h;
-              if (s * 64 >= p.V) continue;
-              const float W = part[(2 * h) * kRN + col] + part[(2 * h + 1) * kRN + col];
-              if (!(W > 0.f)) continue;
-              const float key = logf(W) + (gpre ? gsm[col * kRGMax + 2 * i + h] : gumbel(p.rng.word(kResidBlock, b, n, s)));
-              if (key > best_key[col]) {  // blocks arrive in increasing order: ties keep the first
-                best_key[col] = key;
-                best_blk[col] = s;
+              for (int h = 0; h < 2; ++h) {
+                const int s = 2 * t + h;
+                if (s * 64 >= p.V) continue;
+                const float W = part[(2 * h) * kRN + col] + part[(2 * h + 1) * kRN + col];
+                if (!(W > 0.f)) continue;
+                const float key =
+                    logf(W) + (gpre ? gsm[col * kRGMax + 2 * i + h] : gumbel(p.rng.word(kResidBlock, b, n, s)));
+                if (key > best_key[col]) {  // blocks arrive in increasing order: ties keep the first
+                  best_key[col] = key;
+                  best_blk[col] = s;
+                }
               }
             }
           }
+          asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
         }
-        asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
       }
-      if (warp == 4 && !aborted()) {
-        for (int col = lane; col < ncols; col += 32) {
-          if constexpr (MODE == kModeResid)
+      // the group's per-CTA results: the loss modes reduce each thread's
+      // running values over the lanes and the four lane quarters once here
+      if constexpr (MODE == kModeLossStats) {
+        float2 d2 = transpose_ms16(ra, rb), t2 = transpose_ms16(rc, rd);  // lane l: column 16 half + (l & 15)
+        if (lane < 16)
+          reinterpret_cast<float4*>(part)[q * kRN + half * 16 + lane] = make_float4(d2.x, d2.y, t2.x, t2.y);
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (warp == 4 && !aborted())
+          for (int col = lane; col < ncols; col += 32) {
+            float4 r = reinterpret_cast<const float4*>(part)[col];
+#pragma unroll
+            for (int qq = 1; qq < 4; ++qq) {
+              const float4 o = reinterpret_cast<const float4*>(part)[qq * kRN + col];
+              const float2 x = ms2_combine(make_float2(r.x, r.y), make_float2(o.x, o.y));
+              const float2 y = ms2_combine(make_float2(r.z, r.w), make_float2(o.z, o.w));
+              r = make_float4(x.x, x.y, y.x, y.y);
+            }
+            // back to natural-log units; a column with no finite entry is (-inf, 0)
+            p.lpart[(size_t)col_b[col] * p.G + c] =
+                make_float4(r.y > 0.f ? r.x * kLn2 : -INFINITY, r.y, r.w > 0.f ? r.z * kLn2 : -INFINITY, r.w);
+          }
+      } else if constexpr (MODE == kModeLossL1) {
+        const float s = transpose_sum16(ra);
+        if (lane < 16) part[q * kRN + half * 16 + lane] = s;
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (warp == 4 && !aborted())
+          for (int col = lane; col < ncols; col += 32)
+            p.l1part[(size_t)col_b[col] * p.G + c] =
+                (part[col] + part[kRN + col]) + (part[2 * kRN + col] + part[3 * kRN + col]);
+      } else {
+        if (warp == 4 && !aborted())
+          for (int col = lane; col < ncols; col += 32)
             p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
-          else if constexpr (MODE == kModeLossStats)
-            p.lpart[(size_t)col_b[col] * p.G + c] = reinterpret_cast<const float4*>(gsm)[col];
-          else
-            p.l1part[(size_t)col_b[col] * p.G + c] = gsm[4 * col];
-        }
       }
       asm volatile("bar.sync 2, 256;" ::: "memory");  // constants are rewritten by the next group
     }
