@@ -14,15 +14,15 @@
 // entries (A = W2 tile, N-major in memory, 128-byte swizzle, two 64-wide
 // boxes) and N = 32 rejected requests (B = gathered W1 rows, K-major). A
 // producer warp stages, per tile, each request's 512-byte slices of U and P in
-// shared memory with bulk copies (a two-stage ring), so each epilogue thread
+// shared memory with bulk copies (a three-stage ring), so each epilogue thread
 // owns one vocabulary entry and reads U and P of every request from shared
 // memory; a block's mass is a sum over two warps' lanes (a 31-shuffle
 // transpose-reduce per 32 requests, then shared memory). Requests are taken in
 // groups of 32 (the list of rejected requests is compacted in each CTA from
 // the verify flags); more groups re-read W2, which the draft left in L2.
 // Persistent, one CTA per SM over 128-wide vocabulary tiles; W2 is read with
-// the L2 evict_last policy (the draft kept it there), U and P with evict-first
-// streaming loads. Every wait is bounded.
+// the L2 evict_last policy (the draft kept it there), in K-halves through a
+// three-stage ring; U and P with plain bulk copies. Every wait is bounded.
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -39,13 +39,14 @@ constexpr int kREpi = 8;
 constexpr int kRUPWarp = 10;
 constexpr int kRM = 128;          // vocabulary entries per tile (MMA M)
 constexpr int kRN = 32;           // requests per group (MMA N)
-constexpr int kRNW = 2;           // W2 ring depth
-constexpr int kRUP = 2;           // U/P ring depth (tiles)
+constexpr int kRNW = 3;           // W2 ring depth in K-halves of a tile (1.5 tiles)
+constexpr int kRUP = 3;           // U/P ring depth (tiles)
 constexpr int kRUPStage = kRN * 2 * kRM * 4;  // 32 KB: per request a 512-byte slice of U and of P
 constexpr int kRTmemCols = 64;    // two 32-column accumulators
 static_assert(kRN == 32, "one 32-request chunk per tile, 16 requests for each warp of a TMEM lane quarter");
 constexpr int kRGMax = 16;        // block Gumbels of a group kept in shared memory (blocks per CTA)
 constexpr int kRMaxB = 1024;
+constexpr int kRGather = kRN * (256 / 8) / (32 * 8);  // 16-byte W1 chunks per epilogue thread (r <= 256)
 
 // What a launch computes over its columns (MMA N): the residual block draw of
 // the rejected requests, or one of the two passes of the draft head's
@@ -59,10 +60,10 @@ struct RSmem {
   __host__ __device__ static RSmem make(int r) {
     RSmem s;
     s.bop = 0;                              // [128 requests x r] bf16, K-major swizzled
-    s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r x 64] bf16)
-    s.up = s.w2 + kRNW * 2 * r * 128;       // kRUP x [request][U slice | P slice] fp32
-    s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row (int), lse_d, lse_t (float)
-    s.part = s.col + 5 * 4 * kRN;           // [4 quarters][32 columns] partials (float4 for the loss statistics)
+    s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r/2 x 64] bf16: one K-half of a tile)
+    s.up = s.w2 + kRNW * r * 128;           // kRUP x [request][U slice | P slice] fp32
+    s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row, x (int), lse_d, lse_t (float)
+    s.part = s.col + 6 * 4 * kRN;           // [4 quarters][32 columns] partials (float4 for the loss statistics)
     s.best = s.part + 4 * 16 * kRN;         // [128] best key, [128] best block
     s.gum = s.best + 2 * 4 * kRN;           // [kRN][kRGMax] block Gumbels of this CTA's blocks
     s.list = s.gum + 4 * kRN * kRGMax;      // [kRMaxB] rejected requests
@@ -157,7 +158,8 @@ __device__ __forceinline__ float2 transpose_ms16(float (&m)[16], float (&s)[16])
 
 template <int MODE>
 __global__ void __launch_bounds__(kRThreads, 1)
-    k_resid_tc(const __grid_constant__ CUtensorMap tm_w2, const RParams p) {
+    k_resid_tc(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
+               const __grid_constant__ CUtensorMap tm_p, const RParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -167,7 +169,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   int* col_b = reinterpret_cast<int*>(smem + L.col);
   int* col_n = col_b + kRN;
   int* col_row = col_n + kRN;
-  float* col_nld = reinterpret_cast<float*>(col_row + kRN);  // -lse_d log2(e)
+  int* col_x = col_row + kRN;                                 // the row of W1 gathered into B
+  float* col_nld = reinterpret_cast<float*>(col_x + kRN);    // -lse_d log2(e)
   float* col_nlt = col_nld + kRN;                              // -lse_t log2(e)
   float* part = reinterpret_cast<float*>(smem + L.part);   // [4][128]
   float* best_key = reinterpret_cast<float*>(smem + L.best);
@@ -196,8 +199,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // The loss modes walk the CTA's tiles forwards in even groups and backwards
   // in odd ones, so the W2 tiles used last are the first reused (from L2).
   auto tile_of = [&](int gq, int i) { return tile_lo + ((MODE != kModeResid && (gq & 1)) ? nt - 1 - i : i); };
-  const uint32_t box_bytes = (uint32_t)p.r * 128u;  // one [r x 64] bf16 box
-  const uint32_t w2_bytes = 2u * box_bytes;
+  const uint32_t box_bytes = (uint32_t)p.r * 64u;  // one [r/2 x 64] bf16 box
+  const uint32_t w2_bytes = 2u * box_bytes;         // one K-half of a tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRNW; ++i) {
@@ -217,6 +220,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
+    if constexpr (MODE != kModeResid) {
+      tc::prefetch_tmap(&tm_u);
+      tc::prefetch_tmap(&tm_p);
+    }
   }
   // the rejected requests, in request order (every CTA builds the same list).
   // The flags, positions and rows are this round's only if every stage so far
@@ -256,13 +263,16 @@ __global__ void __launch_bounds__(kRThreads, 1)
       bool ok = true;
       for (int gq = 0; gq < ngroups && ok; ++gq) {
         for (int i = 0; i < nt && ok; ++i) {
-          const int it = gq * nt + i, t = tile_of(gq, i), ws = it % kRNW;
-          ok = tc::mbar_wait(w2_empty(ws), ((it / kRNW) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
-          tc::tma_load_2d(sW2 + ws * w2_bytes, &tm_w2, t * kRM, 0, w2_full(ws), keep);
-          tc::tma_load_2d(sW2 + ws * w2_bytes + box_bytes, &tm_w2, t * kRM + 64, 0, w2_full(ws), keep);
-          issued = it + 1;
+          const int t = tile_of(gq, i);
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int hs = 2 * (gq * nt + i) + h, ws = hs % kRNW;
+            ok = tc::mbar_wait(w2_empty(ws), ((hs / kRNW) & 1) ^ 1, abort);
+            if (!ok) break;
+            tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
+            tc::tma_load_2d(sW2 + ws * w2_bytes, &tm_w2, t * kRM, h * (p.r / 2), w2_full(ws), keep);
+            tc::tma_load_2d(sW2 + ws * w2_bytes + box_bytes, &tm_w2, t * kRM + 64, h * (p.r / 2), w2_full(ws), keep);
+            issued = hs + 1;
+          }
         }
       }
       if (!ok) {
@@ -281,6 +291,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     // bulk copies, so the epilogue reads them from shared memory
     bool ok = true;
     int issued = 0;
+    const uint64_t stream_pol = tc::policy_evict_first();
     for (int gq = 0; gq < ngroups && ok; ++gq) {
       const int ncols = min(kRN, nrej - gq * kRN);
       const float* urow = p.U;
@@ -302,12 +313,21 @@ __global__ void __launch_bounds__(kRThreads, 1)
         if (lane == 0) got = tc::mbar_wait(up_empty(us), ((it / kRUP) & 1) ^ 1, abort) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
         if (!ok) break;
-        if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), 2u * bytes * (uint32_t)ncols);
-        __syncwarp();
-        if (lane < ncols) {
-          const uint32_t dst = sUP + us * kRUPStage + lane * (2 * kRM * 4);
-          tc::bulk_load(dst, urow + v0, bytes, up_full(us));
-          tc::bulk_load(dst + kRM * 4, prow + v0, bytes, up_full(us));
+        if constexpr (MODE == kModeResid) {
+          if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), 2u * bytes * (uint32_t)ncols);
+          __syncwarp();
+          if (lane < ncols) {
+            const uint32_t dst = sUP + us * kRUPStage + lane * (2 * kRM * 4);
+            tc::bulk_load(dst, urow + v0, bytes, up_full(us));
+            tc::bulk_load(dst + kRM * 4, prow + v0, bytes, up_full(us));
+          }
+        } else if (lane == 0) {
+          // the group's 32 consecutive rows of U and of P: one [32 x 128] box
+          // each (rows past B*gamma and entries past V read as zeros)
+          tc::mbar_arrive_expect_tx(up_full(us), (uint32_t)kRUPStage);
+          const uint32_t dst = sUP + us * kRUPStage;
+          tc::tma_load_2d(dst, &tm_u, v0, gq * kRN, up_full(us), stream_pol);
+          tc::tma_load_2d(dst + kRN * kRM * 4, &tm_p, v0, gq * kRN, up_full(us), stream_pol);
         }
         issued = it + 1;
       }
@@ -331,20 +351,25 @@ __global__ void __launch_bounds__(kRThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();
         for (int i = 0; i < nt && ok; ++i) {
-          const int it = gq * nt + i, ws = it % kRNW, ab = it & 1;
-          ok = tc::mbar_wait(w2_full(ws), (it / kRNW) & 1, abort) &&
-               tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
-          if (!ok) break;
-          tc::tc_fence_after();
+          const int it = gq * nt + i, ab = it & 1;
+          ok = tc::mbar_wait(t_empty(ab), ((it >> 1) & 1) ^ 1, abort);
           const uint32_t d = tmem + (uint32_t)(ab * kRN);
-          const uint32_t astage = sW2 + ws * w2_bytes;
-          for (int ks = 0; ks < p.r / 16; ++ks) {
-            // A: two 64-wide M atoms (LBO apart), 8 K rows per 1 KB atom (SBO)
-            const uint64_t ad = tc::smem_desc(astage + ks * 2048, box_bytes, 1024);
-            const uint64_t bd = tc::smem_desc(sB + (ks >> 2) * (kRN * 128) + (ks & 3) * 32, 16, 1024);
-            tc::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          for (int h = 0; h < 2 && ok; ++h) {
+            const int hs = 2 * it + h, ws = hs % kRNW;
+            ok = tc::mbar_wait(w2_full(ws), (hs / kRNW) & 1, abort);
+            if (!ok) break;
+            tc::tc_fence_after();
+            const uint32_t astage = sW2 + ws * w2_bytes;
+            for (int kh = 0; kh < p.r / 32; ++kh) {
+              const int ks = h * (p.r / 32) + kh;
+              // A: two 64-wide M atoms (LBO apart), 8 K rows per 1 KB atom (SBO)
+              const uint64_t ad = tc::smem_desc(astage + kh * 2048, box_bytes, 1024);
+              const uint64_t bd = tc::smem_desc(sB + (ks >> 2) * (kRN * 128) + (ks & 3) * 32, 16, 1024);
+              tc::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(w2_empty(ws));
           }
-          tc::mma_commit(w2_empty(ws));
+          if (!ok) break;
           tc::mma_commit(t_full(ab));
         }
       }
@@ -406,17 +431,34 @@ __global__ void __launch_bounds__(kRThreads, 1)
         if (et < kRN) {
           best_key[et] = -INFINITY;
           best_blk[et] = kNoIdx;
+          col_x[et] = valid ? x : -1;
         }
-        const int m = et;
-        for (int kb = 0; kb < p.r / 64 && et < kRN; ++kb) {
-          const uint4* src = reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r + kb * 64);
+      }
+      asm volatile("bar.sync 2, 256;" ::: "memory");  // column constants visible to all epilogue warps
+      if (!aborted()) {
+        // B = the columns' W1 rows, K-major with the 128-byte swizzle: every
+        // epilogue thread loads up to kRGather 16-byte chunks (consecutive
+        // threads take consecutive chunks of a row), all in flight at once
+        const int cpr = p.r / 8;  // 16-byte chunks per row
+        uint4 v[kRGather];
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const uint4 v = valid ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kRGather; ++j) {
+          const int idx = et + j * 32 * kREpi;
+          v[j] = make_uint4(0, 0, 0, 0);
+          if (idx < kRN * cpr) {
+            const int m = idx / cpr, x = col_x[m];
+            if (x >= 0) v[j] = __ldg(reinterpret_cast<const uint4*>(W1 + (size_t)x * p.r) + (idx - m * cpr));
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kRGather; ++j) {
+          const int idx = et + j * 32 * kREpi;
+          if (idx < kRN * cpr) {
+            const int m = idx / cpr, cc = idx - m * cpr, kb = cc >> 3, ch = cc & 7;
             const uint32_t dst = sB + kb * (kRN * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
                                  ((uint32_t)(ch ^ (m & 7)) << 4);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z),
-                         "r"(v.w)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v[j].x), "r"(v[j].y),
+                         "r"(v[j].z), "r"(v[j].w)
                          : "memory");
           }
         }
@@ -424,7 +466,6 @@ __global__ void __launch_bounds__(kRThreads, 1)
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(a_full);
       }
-      asm volatile("bar.sync 2, 256;" ::: "memory");  // column constants visible to all epilogue warps
       const int ncols = min(kRN, nrej - gq * kRN);
       // the block draw's Gumbel noise of every (request, block) of this CTA,
       // computed once up front (visible to the combining warp after the first
@@ -472,11 +513,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
             // U and P of request j at this entry, from the staged slices
             // (consecutive lanes read consecutive words)
             float uu[16], pp[16];
-            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(half * 16) * (2 * kRM * 4) + (uint32_t)(q * 32 + lane) * 4u;
+            // stage layout: per request [U slice | P slice] (residual), or
+            // [32 rows of U][32 rows of P] (the loss modes' two boxes)
+            constexpr uint32_t kRow = MODE == kModeResid ? 2 * kRM * 4 : kRM * 4;
+            constexpr uint32_t kPOff = MODE == kModeResid ? kRM * 4 : kRN * kRM * 4;
+            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(half * 16) * kRow + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * (2 * kRM * 4)));
-              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * (2 * kRM * 4) + kRM * 4));
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * kRow));
+              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * kRow + kPOff));
             }
             if constexpr (MODE == kModeLossStats) {
               // running (max, sum 2^(y - max)) of y = z log2(e) per column,
@@ -627,16 +672,32 @@ cudaError_t resid_tc_configure(dspark_ws* ws) {
 // co-residency requirement).
 namespace {
 
-// W2 as [r rows x V] bf16, boxes of [r x 64] with the 128-byte swizzle.
+// W2 as [r rows x V] bf16, boxes of [r/2 x 64] (a K-half of a tile) with the
+// 128-byte swizzle.
 cudaError_t w2_tensor_map(const dspark_dims& d, const void* W2, CUtensorMap* tm) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
   const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)d.r};
+  const cuuint32_t box[2] = {64, (cuuint32_t)d.r / 2};
   const cuuint32_t es[2] = {1, 1};
   if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+// A [rows x V] fp32 matrix as boxes of [32 rows x 128 entries], no swizzle.
+cudaError_t rows_tensor_map(const float* X, int rows, int V, CUtensorMap* tm) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)V * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)kRM, (cuuint32_t)kRN};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;
@@ -677,7 +738,7 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.vlset = ws->s.vlset;
   p.rpart = rpart;
   const RSmem L = RSmem::make(d.r);
-  k_resid_tc<kModeResid><<<grid, kRThreads, L.total + 1024, st>>>(tm, p);
+  k_resid_tc<kModeResid><<<grid, kRThreads, L.total + 1024, st>>>(tm, tm, tm, p);
   return cudaGetLastError();
 }
 
@@ -685,6 +746,11 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
   const dspark_dims& d = ws->d;
   CUtensorMap tm;
   cudaError_t e = w2_tensor_map(d, a.W2, &tm);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tu, tp;
+  const int rows = d.B * d.gamma;
+  e = rows_tensor_map(a.U, rows, d.V, &tu);
+  if (e == cudaSuccess) e = rows_tensor_map(a.P, rows, d.V, &tp);
   if (e != cudaSuccess) return e;
   RParams p = base_params(ws, ws->geo.num_sms);
   p.P = a.P;
@@ -699,9 +765,9 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
   p.lse_t = a.lse_t;
   const RSmem L = RSmem::make(d.r);
   if (pass == 0)
-    k_resid_tc<kModeLossStats><<<p.G, kRThreads, L.total + 1024, st>>>(tm, p);
+    k_resid_tc<kModeLossStats><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tp, p);
   else
-    k_resid_tc<kModeLossL1><<<p.G, kRThreads, L.total + 1024, st>>>(tm, p);
+    k_resid_tc<kModeLossL1><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tp, p);
   return cudaGetLastError();
 }
 
