@@ -71,6 +71,7 @@ def lib():
             l.orc_logsumexp.argtypes = [P, C.c_long]
             l.orc_logsumexp.restype = dbl
             l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P]
+            l.orc_rnn_draft.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P]
             l.orc_plan_sync.argtypes = [i32, i32, P, P, P, P]
             l.orc_plan_sync.restype = i32
             l.orc_plan_capacity.argtypes = [i32, i32, P, P, P]
@@ -241,6 +242,40 @@ def draft(U, W1, W2, anchor, h, w, T, seed: int, rnd: int,
     lib().orc_draft(C.byref(d), _p(U), _p(w1), _p(w2), _p(anchor), _p(h), _p(w), _p(T),
                     seed, rnd, _p(rq), rq.size, _p(out["tokens"]), _p(out["pd_tok"]),
                     _p(out["lse"]), _p(out["conf"]), _p(out["margin"]))
+    return out
+
+
+def rnn_draft(U, W1, W2, Wr, anchor, h, w, T, seed: int, rnd: int,
+              reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+    """Draft tail with the RNN head, eq. (6) (see ``orc_rnn_draft``).
+
+    As ``draft``, plus Wr [3, r, 2r + H] (W_g, W_c, W_o; same storage as W1)
+    and the output ``ovec`` [B, gamma, r]: the head's vector o_k with
+    z_k = U_k + o_k W2.
+    """
+    U = _c(U, np.float32)
+    B, g, V = U.shape
+    w1, bf = _weights(W1)
+    w2, _ = _weights(W2)
+    wr, bf_r = _weights(Wr)
+    if bf_r != bf:
+        raise ValueError("Wr must be stored like W1 and W2")
+    r = w1.shape[1]
+    h = _c(h, np.float32)
+    H = h.shape[2]
+    if wr.shape != (3, r, 2 * r + H):
+        raise ValueError(f"Wr must be [3, {r}, {2 * r + H}], got {wr.shape}")
+    anchor = _c(anchor, np.int32)
+    w = _c(w, np.float32)
+    T = _c(T, np.float32)
+    rq = _c(range(B) if reqs is None else reqs, np.int32)
+    d = _dims(B, g, V, r, H, bf)
+    out = {"tokens": np.full((B, g), -1, np.int32), "pd_tok": np.full((B, g), np.nan),
+           "lse": np.full((B, g), np.nan), "conf": np.full((B, g), np.nan),
+           "margin": np.full((B, g), np.inf), "ovec": np.full((B, g, r), np.nan)}
+    lib().orc_rnn_draft(C.byref(d), _p(U), _p(w1), _p(w2), _p(wr), _p(anchor), _p(h), _p(w), _p(T),
+                        seed, rnd, _p(rq), rq.size, _p(out["tokens"]), _p(out["pd_tok"]),
+                        _p(out["lse"]), _p(out["conf"]), _p(out["margin"]), _p(out["ovec"]))
     return out
 
 

@@ -311,6 +311,76 @@ void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2
 }
 
 /* ------------------------------------------------------------------ */
+/* RNN head ([V4.1 blog] section on the Markov head (the RNN variant    */
+/* the paper also tried); [ailearn] "RNN 头（可选）"; [csdn] §4.2,       */
+/* eq. (6)). A gated recurrent state s_k in R^r summarises the block's  */
+/* prefix: with z_k = [s_{k-1}; W1[x_{k-1}]; h_k] (length 2r + H),       */
+/*   g_k = sigma(W_g z_k),  s_k = g_k * s_{k-1} + (1 - g_k) * tanh(W_c z_k),
+/*   o_k = tanh(W_o z_k),   z = U_k + o_k W2  (the bias B_k = W2^T o_k), */
+/* s_0 = 0, x_0 = the anchor; W_g, W_c, W_o are [r][2r + H] (no bias,   */
+/* as the equation shows none), stored one after the other in Wr in the */
+/* weights' dtype. Sampling and the confidence head (eq. (7), with      */
+/* W1[x_{k-1}]) are the Markov draft's. ovec [B][gamma][r] receives o_k. */
+/* ------------------------------------------------------------------ */
+void orc_rnn_draft(const orc_dims* d, const float* U, const void* W1, const void* W2, const void* Wr,
+                   const int32_t* anchor, const float* h, const float* w, const float* T,
+                   uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                   int32_t* tokens, double* pd_tok, double* lse, double* conf, double* margin,
+                   double* ovec)
+{
+    const long V = d->V, g = d->gamma, r = d->r, H = d->H, Z = 2 * r + H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int q = 0; q < n_req; ++q) {
+        const long b = reqs[q];
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* zin = (double*)malloc(sizeof(double) * (size_t)Z);
+        double* st = (double*)calloc((size_t)r, sizeof(double));     /* s_0 = 0 */
+        double* ov = (double*)malloc(sizeof(double) * (size_t)r);
+        int x_prev = anchor[b];
+        for (long k = 1; k <= g; ++k) {
+            const long o = b * g + (k - 1);
+            /* z_k = [s_{k-1}; W1[x_{k-1}]; h_k] */
+            for (long i = 0; i < r; ++i) zin[i] = st[i];
+            for (long i = 0; i < r; ++i) zin[r + i] = wget(W1, d->w_bf16, x_prev, r, i);
+            for (long i = 0; i < H; ++i) zin[2 * r + i] = (double)h[o * H + i];
+            /* gate, candidate and output of every state entry (all from z_k) */
+            for (long j = 0; j < r; ++j) {
+                double ag = 0.0, ac = 0.0, ao = 0.0;
+                for (long i = 0; i < Z; ++i) {
+                    ag += wget(Wr, d->w_bf16, j, Z, i) * zin[i];
+                    ac += wget(Wr, d->w_bf16, r + j, Z, i) * zin[i];
+                    ao += wget(Wr, d->w_bf16, 2 * r + j, Z, i) * zin[i];
+                }
+                const double gk = 1.0 / (1.0 + exp(-ag));
+                st[j] = gk * zin[j] + (1.0 - gk) * tanh(ac);
+                ov[j] = tanh(ao);
+                ovec[o * r + j] = ov[j];
+            }
+            /* eq. (7) as for the Markov head */
+            double s = 0.0;
+            for (long i = 0; i < H; ++i) s += (double)w[i] * (double)h[o * H + i];
+            for (long i = 0; i < r; ++i) s += (double)w[H + i] * zin[r + i];
+            conf[o] = 1.0 / (1.0 + exp(-s / (double)T[k - 1]));
+            /* z = U_k + o_k W2 */
+            for (long v = 0; v < V; ++v) z[v] = 0.0;
+            for (long i = 0; i < r; ++i)
+                for (long v = 0; v < V; ++v) z[v] += ov[i] * wget(W2, d->w_bf16, i, V, v);
+            for (long v = 0; v < V; ++v) z[v] += (double)U[o * V + v];
+            const double L = orc_logsumexp(z, V);
+            double m = 0.0;
+            const int x = sample_two_level_icdf(z, V, seed, round, ORC_P_DRAFT_BLOCK,
+                                                ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            tokens[o] = x;
+            pd_tok[o] = exp(z[x] - L);
+            lse[o] = L;
+            margin[o] = m;
+            x_prev = x;
+        }
+        free(z); free(zin); free(st); free(ov);
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* Planner                                                             */
 /* ------------------------------------------------------------------ */
 typedef struct { double a; int j; int b; } orc_cand;

@@ -722,3 +722,119 @@ def test_loss_identical_distributions_and_teacher_forcing():
     o3 = oracle.train_loss(U, W1, W2, anchor, xs2, P, conf, tau=2.0)
     assert np.array_equal(o3["l1"][:, 0], o["l1"][:, 0])
     assert not np.allclose(o3["l1"][:, 1], o["l1"][:, 1])
+
+
+# ---------------------------------------------------------------- RNN head, eq. (6)
+def _rnn_inputs(seed, B=3, g=4, V=200, r=8, H=6):
+    rng = np.random.default_rng(seed)
+    return dict(U=rng.normal(0.0, 2.0, (B, g, V)).astype(np.float32),
+                W1=rng.normal(0.0, 0.7, (V, r)).astype(np.float32),
+                W2=rng.normal(0.0, 0.7, (r, V)).astype(np.float32),
+                anchor=rng.integers(0, V, B).astype(np.int32),
+                h=rng.normal(0.0, 1.0, (B, g, H)).astype(np.float32),
+                w=rng.normal(0.0, 0.3, H + r).astype(np.float32),
+                T=np.full(g, 1.0, np.float32), C=rng.normal(0.0, 0.8, (r, H)).astype(np.float32))
+
+
+def _rnn_weights(r, H, Wg=None, Wc=None, Wo=None):
+    Z = 2 * r + H
+    Wr = np.zeros((3, r, Z), np.float32)
+    for i, m in enumerate((Wg, Wc, Wo)):
+        if m is not None:
+            Wr[i] = m
+    return Wr
+
+
+def test_rnn_head_reduces_to_the_markov_head():
+    """W_o = [0 | I | 0] and W_g = W_c = 0: o_k = tanh(W1[x_{k-1}]), so the
+    draft equals the Markov draft with W1 replaced by tanh(W1) (w_r = 0 so
+    that the confidences agree too)."""
+    a = _rnn_inputs(3)
+    r, H = a["W1"].shape[1], a["h"].shape[2]
+    Wo = np.zeros((r, 2 * r + H), np.float32)
+    Wo[:, r:2 * r] = np.eye(r)
+    Wr = _rnn_weights(r, H, Wo=Wo)
+    w = a["w"].copy()
+    w[H:] = 0.0
+    o = oracle.rnn_draft(a["U"], a["W1"], a["W2"], Wr, a["anchor"], a["h"], w, a["T"], 9, 2)
+    m = oracle.draft(a["U"], np.tanh(a["W1"].astype(np.float64)).astype(np.float32), a["W2"], a["anchor"], a["h"], w,
+                     a["T"], 9, 2)
+    assert np.all(o["margin"] > 1e-6)
+    assert np.array_equal(o["tokens"], m["tokens"])
+    assert np.allclose(o["lse"], m["lse"], rtol=1e-7, atol=0)
+    assert np.allclose(o["pd_tok"], m["pd_tok"], rtol=1e-6, atol=0)
+    assert np.allclose(o["conf"], m["conf"], rtol=1e-12, atol=0)
+    # o_k is tanh of the previous token's W1 row
+    prev = np.concatenate([a["anchor"][:, None], o["tokens"][:, :-1]], axis=1)
+    assert np.allclose(o["ovec"], np.tanh(a["W1"].astype(np.float64)[prev]), rtol=0, atol=1e-15)
+
+
+def test_rnn_state_recursion_closed_form():
+    """W_g = 0 (gate 1/2), W_c reads h only, W_o reads s only:
+    s_k = s_{k-1}/2 + tanh(C h_k)/2 and o_k = tanh(s_{k-1}), so o_1 = 0 and the
+    first position's logits are U_1."""
+    a = _rnn_inputs(4)
+    r, H = a["W1"].shape[1], a["h"].shape[2]
+    Wc = np.zeros((r, 2 * r + H), np.float32)
+    Wc[:, 2 * r:] = a["C"]
+    Wo = np.zeros((r, 2 * r + H), np.float32)
+    Wo[:, :r] = np.eye(r)
+    o = oracle.rnn_draft(a["U"], a["W1"], a["W2"], _rnn_weights(r, H, Wc=Wc, Wo=Wo), a["anchor"], a["h"], a["w"],
+                         a["T"], 5, 0)
+    B, g = a["U"].shape[:2]
+    s = np.zeros((B, r))
+    for k in range(g):
+        assert np.allclose(o["ovec"][:, k], np.tanh(s), rtol=0, atol=1e-14), k
+        s = 0.5 * s + 0.5 * np.tanh(a["h"][:, k].astype(np.float64) @ a["C"].astype(np.float64).T)
+    z = a["U"].astype(np.float64) + np.einsum("bkr,rv->bkv", o["ovec"], a["W2"].astype(np.float64))
+    assert np.allclose(o["lse"], special.logsumexp(z, axis=2), rtol=1e-13, atol=0)
+    assert np.allclose(o["lse"][:, 0], special.logsumexp(a["U"][:, 0].astype(np.float64), axis=1), rtol=1e-13)
+
+
+def test_rnn_gate_saturation():
+    """A gate saturated at 1 keeps s_0 = 0 for ever (o_k = tanh(0) = 0, the
+    logits are U_k); saturated at 0 it makes s_k = tanh(C h_k), so
+    o_k = tanh(tanh(C h_{k-1}))."""
+    a = _rnn_inputs(5)
+    r, H = a["W1"].shape[1], a["h"].shape[2]
+    h = np.abs(a["h"]) + 1.0                       # positive: the gate's sign is known
+    Wc = np.zeros((r, 2 * r + H), np.float32)
+    Wc[:, 2 * r:] = a["C"]
+    Wo = np.zeros((r, 2 * r + H), np.float32)
+    Wo[:, :r] = np.eye(r)
+    for sign in (+1.0, -1.0):
+        Wg = np.zeros((r, 2 * r + H), np.float32)
+        Wg[:, 2 * r:] = 100.0 * sign
+        o = oracle.rnn_draft(a["U"], a["W1"], a["W2"], _rnn_weights(r, H, Wg, Wc, Wo), a["anchor"], h, a["w"],
+                             a["T"], 6, 1)
+        if sign > 0:
+            assert np.all(o["ovec"] == 0.0)
+            assert np.allclose(o["lse"], special.logsumexp(a["U"].astype(np.float64), axis=2), rtol=1e-13)
+        else:
+            cand = np.tanh(np.einsum("bkh,rh->bkr", h.astype(np.float64), a["C"].astype(np.float64)))
+            assert np.all(o["ovec"][:, 0] == 0.0)
+            assert np.allclose(o["ovec"][:, 1:], np.tanh(cand[:, :-1]), rtol=0, atol=1e-14)
+
+
+def test_rnn_head_is_non_anticipating_and_carries_the_prefix():
+    """Position k's outputs do not depend on U at later positions; the state
+    makes o_k depend on tokens before x_{k-1} (unlike the Markov head)."""
+    a = _rnn_inputs(6)
+    rng = np.random.default_rng(60)
+    r, H = a["W1"].shape[1], a["h"].shape[2]
+    Wr = (rng.normal(0.0, 0.4, (3, r, 2 * r + H))).astype(np.float32)
+    o = oracle.rnn_draft(a["U"], a["W1"], a["W2"], Wr, a["anchor"], a["h"], a["w"], a["T"], 7, 3)
+    U2 = a["U"].copy()
+    U2[:, 2:] += rng.normal(0.0, 3.0, U2[:, 2:].shape).astype(np.float32)
+    o2 = oracle.rnn_draft(U2, a["W1"], a["W2"], Wr, a["anchor"], a["h"], a["w"], a["T"], 7, 3)
+    assert np.array_equal(o["tokens"][:, :2], o2["tokens"][:, :2])
+    assert np.array_equal(o["ovec"][:, :3], o2["ovec"][:, :3])   # o_3 uses x_2, not U_3
+    # a different anchor changes s_1 and so o_2 even where x_1 is the same token
+    an2 = (a["anchor"] + 1) % a["U"].shape[2]
+    U3 = a["U"].copy()
+    U3[:, 0] = -1e4
+    U3[:, 0, 7] = 0.0                                  # x_1 = 7 whatever the anchor
+    o3 = oracle.rnn_draft(U3, a["W1"], a["W2"], Wr, a["anchor"], a["h"], a["w"], a["T"], 7, 3)
+    o4 = oracle.rnn_draft(U3, a["W1"], a["W2"], Wr, an2, a["h"], a["w"], a["T"], 7, 3)
+    assert np.all(o3["tokens"][:, 0] == 7) and np.all(o4["tokens"][:, 0] == 7)
+    assert not np.allclose(o3["ovec"][:, 1], o4["ovec"][:, 1])
