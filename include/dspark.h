@@ -256,6 +256,28 @@ dspark_status dspark_train_loss(dspark_ws* ws, const float* U, const void* W1, c
                                 dspark_stream_t stream);
 size_t dspark_train_loss_scratch_bytes(const dspark_ws* ws);
 
+/*
+ * The draft tail with the RNN head instead of the Markov head
+ * ("DeepSeek-V4.1 模型结构（6）：解码，DSpark", section on the Markov head, the
+ * RNN variant; deepseek.csdn.net §4.2, eq. (6)). With s_0 = 0, x_0 = anchor[b]
+ * and z_k = [s_{k-1}; W1[x_{k-1}]; h_k] (length 2r + H):
+ *   s_k = sigma(W_g z_k) * s_{k-1} + (1 - sigma(W_g z_k)) * tanh(W_c z_k),
+ *   o_k = tanh(W_o z_k),  logits_k = U_k + o_k W2,
+ * and x_k, pd_tok, lse and conf exactly as dspark_markov_draft (the
+ * confidence takes W1[x_{k-1}], eq. (7)). Wr is [3][r][2r + H] (W_g, W_c, W_o,
+ * row-major, no bias) in the workspace's weight dtype; ovec [B][gamma][r] fp32
+ * receives o_k. The other arguments are those of dspark_markov_draft. Every
+ * pointer is a 16-byte aligned device pointer owned by the caller; scratch
+ * holds dspark_rnn_draft_scratch_bytes(ws) bytes, 256-byte aligned. Runs on
+ * CUDA cores (SIMT kernels): 2 + 3 gamma launches. Asynchronous on `stream`;
+ * device errors go to the workspace's status word.
+ */
+dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2, const void* Wr,
+                               const int32_t* anchor, const float* h, const float* w, const float* T,
+                               uint64_t seed, uint64_t round, int32_t* tokens, float* pd_tok, float* lse,
+                               float* conf, float* ovec, void* scratch, dspark_stream_t stream);
+size_t dspark_rnn_draft_scratch_bytes(const dspark_ws* ws);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,6 +24,7 @@ SYMBOLS = [
     "dspark_status_string", "dspark_last_launch_count", "dspark_path",
     "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
     "dspark_sts_fit", "dspark_sts_scratch_bytes", "dspark_train_loss", "dspark_train_loss_scratch_bytes",
+    "dspark_rnn_draft", "dspark_rnn_draft_scratch_bytes",
 ]
 
 
@@ -86,6 +87,10 @@ def load() -> C.CDLL:
         lib.dspark_train_loss.restype = i32
         lib.dspark_train_loss_scratch_bytes.argtypes = [P]
         lib.dspark_train_loss_scratch_bytes.restype = C.c_size_t
+        lib.dspark_rnn_draft.argtypes = [P] * 9 + [u64, u64] + [P] * 7
+        lib.dspark_rnn_draft.restype = i32
+        lib.dspark_rnn_draft_scratch_bytes.argtypes = [P]
+        lib.dspark_rnn_draft_scratch_bytes.restype = C.c_size_t
         _lib = lib
         return lib
 
@@ -242,6 +247,26 @@ class Workspace:
             _ptr(W2, self.wdtype, "W2"), int(seed), int(rnd), _ptr(out["n_acc"], i32, "n_acc"),
             _ptr(out["next_anchor"], i32, "next_anchor"), _stream(stream))
         _check(code, "dspark_verify")
+        return out
+
+    def rnn_draft(self, U, W1, W2, Wr, anchor, h, w, T, seed: int, rnd: int, out=None, stream=None):
+        """Draft tail with the RNN head (``dspark_rnn_draft``): as ``draft``,
+        plus Wr [3, r, 2r + H]; ``out`` also holds ovec [B, gamma, r] fp32."""
+        if out is None:
+            out = self.new_draft_outputs(U.device)
+            B, g, r = self.dims.B, self.dims.gamma, self.dims.r
+            out["ovec"] = torch.empty(B, g, r, dtype=torch.float32, device=U.device)
+            out["scratch"] = torch.empty(int(self.lib.dspark_rnn_draft_scratch_bytes(self._h)), dtype=torch.uint8,
+                                         device=U.device)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_rnn_draft(
+            self._h, _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"), _ptr(W2, self.wdtype, "W2"),
+            _ptr(Wr, self.wdtype, "Wr"), _ptr(anchor, i32, "anchor"),
+            _ptr(h, f32, "h") if self.dims.H > 0 else C.c_void_p(0), _ptr(w, f32, "w"), _ptr(T, f32, "T"),
+            int(seed), int(rnd), _ptr(out["tokens"], i32, "tokens"), _ptr(out["pd_tok"], f32, "pd_tok"),
+            _ptr(out["lse"], f32, "lse"), _ptr(out["conf"], f32, "conf"), _ptr(out["ovec"], f32, "ovec"),
+            _ptr(out["scratch"], None, "scratch"), _stream(stream))
+        _check(code, "dspark_rnn_draft")
         return out
 
     def new_loss_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:

@@ -123,6 +123,15 @@ cudaError_t launch_conf_hidden(const dspark_ws* ws, const float* h, const float*
                                int* launches);
 cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches);
 cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches);
+// The RNN head (eq. (6)): Hp[row][3r] = the h_k part of W_g, W_c, W_o z_k for
+// every position; the cell of step k (S [B][r] the state, updated in place;
+// ovec [B*gamma][r] receives o_k); the whole draft tail on the SIMT path.
+cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr, float* Hp, cudaStream_t st,
+                             int* launches);
+cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void* Wr, const float* Hp, float* S,
+                            float* ovec, int k, cudaStream_t st, int* launches);
+cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
+                             float* ovec, cudaStream_t st, int* launches);
 cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
                         int32_t* row_off, cudaStream_t st, int* launches);
 cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t st, int* launches);

@@ -13,6 +13,9 @@
 //                   argmax_s(log mass_s + G_s), then z of the 64 tokens of the
 //                   drawn block recomputed and the token inside it drawn by
 //                   inverse CDF with one uniform of the block; also c_k.
+// With the RNN head (eq. (6)) the r-vector that multiplies W2 is the head's
+// o_k, which k_rnn_cell writes before each step (ovec); the confidence still
+// takes W1[x_{k-1}].
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -49,16 +52,18 @@ __device__ __forceinline__ float markov_dot(const float* __restrict__ e, const v
 template <int BF16>
 __global__ void __launch_bounds__(kSimtThreads)
     k_draft_blocks(const float* __restrict__ U, const void* __restrict__ W1, const void* __restrict__ W2,
-                   const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens, int g, int V,
-                   int r, int k, int nblk, float* __restrict__ blk, int* __restrict__ status) {
-  extern __shared__ float e[];  // W1[x_{k-1}] as fp32, [r]
+                   const int32_t* __restrict__ anchor, const int32_t* __restrict__ tokens,
+                   const float* __restrict__ ovec, int g, int V, int r, int k, int nblk, float* __restrict__ blk,
+                   int* __restrict__ status) {
+  extern __shared__ float e[];  // W1[x_{k-1}] (Markov head) or o_k (RNN head) as fp32, [r]
   const int b = blockIdx.y;
   const int x = prev_token(anchor, tokens, b, g, k);
   if (x < 0 || x >= V) {
     if (threadIdx.x == 0) raise_status(status, DSPARK_ERANGE);
     return;
   }
-  for (int i = threadIdx.x; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+  for (int i = threadIdx.x; i < r; i += blockDim.x)
+    e[i] = ovec ? ovec[((size_t)b * g + (k - 1)) * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
   __syncthreads();
   const float* Urow = U + ((size_t)b * g + (k - 1)) * V;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,8 +84,9 @@ template <int BF16>
 __global__ void __launch_bounds__(kSimtThreads)
     k_draft_pick(const float* __restrict__ U, const void* __restrict__ W1, const void* __restrict__ W2,
                  const int32_t* __restrict__ anchor, const float* __restrict__ w,
-                 const float* __restrict__ T, const float* __restrict__ s_h, int g, int V, int r, int H,
-                 int k, int nblk, const float* __restrict__ blk, Rng rng, int32_t* __restrict__ tokens,
+                 const float* __restrict__ T, const float* __restrict__ s_h, const float* __restrict__ ovec, int g,
+                 int V, int r, int H, int k, int nblk, const float* __restrict__ blk, Rng rng,
+                 int32_t* __restrict__ tokens,
                  float* __restrict__ pd_tok, float* __restrict__ lse_out, float* __restrict__ conf,
                  int* __restrict__ status) {
   extern __shared__ float e[];  // [r]
@@ -96,13 +102,14 @@ __global__ void __launch_bounds__(kSimtThreads)
     if (tid == 0) raise_status(status, DSPARK_ERANGE);
     return;
   }
-  for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
-  __syncthreads();
   const size_t o = (size_t)b * g + (k - 1);
+  for (int i = tid; i < r; i += blockDim.x) e[i] = ovec ? ovec[o * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
+  __syncthreads();
 
   // eq. (7): c_k = sigma((s_h + w_r . W1[x_{k-1}]) / T_k)
   float cr = 0.f;
-  for (int i = tid; i < r; i += blockDim.x) cr = fmaf(w[H + i], e[i], cr);
+  for (int i = tid; i < r; i += blockDim.x)
+    cr = fmaf(w[H + i], ovec ? ld_w(W1, BF16, (size_t)x * r + i) : e[i], cr);
   cr = warp_sum(cr);
   if (lane == 0) red_f[warp] = cr;
   // log-sum-exp over the block log-masses
@@ -195,9 +202,18 @@ cudaError_t launch_conf_hidden(const dspark_ws* ws, const float* h, const float*
   return cudaGetLastError();
 }
 
+// rnn: the RNN head's cell runs before each step (Hp, S, ovec: its scratch
+// and output); null for the Markov head.
+struct RnnStep {
+  const void* Wr;
+  float* Hp;
+  float* S;
+  float* ovec;
+};
+
 template <int BF16>
 static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st,
-                                   int* launches) {
+                                   int* launches, const RnnStep* rnn = nullptr) {
   const dspark_dims& d = ws->d;
   const int nblk = ws->geo.nblk;
   const size_t smem = sizeof(float) * d.r;
@@ -205,10 +221,15 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
   int chunks = (nblk + 4 * wpc - 1) / (4 * wpc);  // about 4 blocks per warp
   if (chunks < 1) chunks = 1;
   const Rng rng = Rng::make(a.seed, a.round);
+  const float* ovec = rnn ? rnn->ovec : nullptr;
   for (int k = 1; k <= d.gamma; ++k) {
+    if (rnn) {
+      const cudaError_t e = launch_rnn_cell(ws, a, rnn->Wr, rnn->Hp, rnn->S, rnn->ovec, k, st, launches);
+      if (e != cudaSuccess) return e;
+    }
     k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
-        a.U, a.W1, a.W2, a.anchor, a.tokens, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
-    k_draft_pick<BF16><<<d.B, kSimtThreads, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h,
+        a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+    k_draft_pick<BF16><<<d.B, kSimtThreads, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec,
                                                        d.gamma, d.V, d.r, d.H, k, nblk, ws->s.blk, rng,
                                                        a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
     *launches += 2;
@@ -219,6 +240,17 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
 cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches) {
   if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches);
   return draft_simt_impl<0>(ws, a, st, launches);
+}
+
+cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
+                             float* ovec, cudaStream_t st, int* launches) {
+  cudaError_t e = launch_conf_hidden(ws, a.h, a.w, st, launches);
+  if (e == cudaSuccess) e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
+  if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0
+  if (e != cudaSuccess) return e;
+  const RnnStep rnn{Wr, Hp, S, ovec};
+  if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches, &rnn);
+  return draft_simt_impl<0>(ws, a, st, launches, &rnn);
 }
 
 }  // namespace dspark

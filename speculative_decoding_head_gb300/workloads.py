@@ -182,6 +182,16 @@ def make_sts_inputs(N: int, gamma: int, seed: int, device: str = "cpu") -> Dict[
     return {"raw": raw.to(torch.float32).to(device), "cstar": cstar.to(torch.float32).to(device)}
 
 
+def make_rnn_weights(wl: Workload, seed_offset: int = 31337) -> torch.Tensor:
+    """The RNN head's stacked weights Wr [3, r, 2r + H] (W_g, W_c, W_o) for
+    workload ``wl`` (CPU), in the workload's weight dtype: entries
+    N(0, 1 / (2r + H)), so that each pre-activation is of order one."""
+    gen = torch.Generator().manual_seed(wl.seed + seed_offset)
+    Z = 2 * wl.r + wl.H
+    Wr = torch.randn((3, wl.r, Z), generator=gen, dtype=torch.float32) / Z ** 0.5
+    return Wr.to(torch.bfloat16).contiguous() if wl.wdtype == "bf16" else Wr.contiguous()
+
+
 def make_loss_inputs(wl: Workload, seed_offset: int = 104729) -> Dict[str, torch.Tensor]:
     """Inputs of the teacher-forced training objective for workload ``wl`` (CPU).
 

@@ -1,0 +1,83 @@
+"""The RNN head's draft tail (eq. (6)) on the GPU against the oracle.
+
+Tokens are bit-exact up to the first position the oracle flags (the same
+margins as the Markov draft); pd_tok, lse and conf within 1e-4 relative; the
+head vector o_k within 2e-5 absolute (|o| < 1; its pre-activations are fp32
+sums of 2r + H terms) up to and including that position, since o_k depends on
+x_{k-1} and the state of the earlier positions only.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_head_gb300 import build
+from speculative_decoding_head_gb300.binding import Workspace
+from speculative_decoding_head_gb300.workloads import WORKLOADS, Workload, make_inputs, make_rnn_weights
+
+from parity import compare_draft, gpu_np, np_inputs, to_device
+
+pytestmark = pytest.mark.gpu
+
+OVEC_ATOL = 2e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def _run(wl, rnd=0, reqs=None):
+    inp = make_inputs(wl, with_target=False)
+    inp["Wr"] = make_rnn_weights(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    ws = Workspace.for_workload(wl)
+    out = ws.rnn_draft(dev["U"], dev["W1"], dev["W2"], dev["Wr"], dev["anchor"], dev["h"], dev["w"], dev["T"],
+                       wl.seed, rnd)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    assert ws.last_launches == (2 if wl.H > 0 else 0) + 3 * wl.gamma
+    g = gpu_np({k: v for k, v in out.items() if k != "scratch"})
+    reqs = list(range(wl.B)) if reqs is None else list(reqs)
+    o = oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
+                         wl.seed, rnd, reqs=reqs)
+    t, _ = compare_draft(g, o, reqs)
+    t.check_rate()
+    for b in reqs:
+        for k in range(wl.gamma):
+            d = np.abs(g["ovec"][b, k] - o["ovec"][b, k]).max()
+            assert d <= OVEC_ATOL, (b, k, d)
+            if o["margin"][b, k] < oracle.MARGIN:
+                break
+    return g, o, t
+
+
+def _wl(name, B, gamma, V, r, H, wdtype="bf16", seed=41):
+    return Workload(name, B=B, gamma=gamma, V=V, r=r, H=H, wdtype=wdtype, mode="static", seed=seed, u_std=2.0,
+                    w_std=0.05 if wdtype == "bf16" else 0.3)
+
+
+@pytest.mark.parametrize("wl", [
+    _wl("rnn_tiny", 2, 3, 1024, 16, 64, wdtype="f32"),
+    _wl("rnn_small", 6, 4, 4104, 64, 96),            # a vocabulary ending inside a 64-token block
+    _wl("rnn_noh", 5, 6, 2048, 32, 0, wdtype="f32"),  # no hidden states: z = [s; W1[x]]
+    _wl("rnn_mid", 40, 5, 32000, 256, 1024),
+], ids=lambda w: w.name)
+def test_rnn_draft_parity(wl):
+    _run(wl, rnd=1)
+
+
+def test_rnn_draft_full_size_sampled():
+    """The prod shape (B=128, gamma=5, V=129280, r=256, H=5120) on eight requests."""
+    _run(WORKLOADS["prod"], rnd=3, reqs=[0, 9, 31, 64, 77, 100, 126, 127])
+
+
+def test_rnn_head_differs_from_markov_head():
+    """Same inputs: the RNN head's tokens follow its own bias, not W1[x] W2."""
+    wl = _wl("rnn_vs_markov", 8, 5, 4096, 64, 32)
+    g, o, _ = _run(wl)
+    inp = make_inputs(wl, with_target=False)
+    npi = np_inputs(inp)
+    m = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed, 0)
+    assert not np.allclose(m["lse"], o["lse"])
