@@ -209,6 +209,7 @@ struct RnnStep {
   float* Hp;
   float* S;
   float* ovec;
+  bool tc;  // block pass on tcgen05
 };
 
 template <int BF16>
@@ -227,8 +228,13 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
       const cudaError_t e = launch_rnn_cell(ws, a, rnn->Wr, rnn->Hp, rnn->S, rnn->ovec, k, st, launches);
       if (e != cudaSuccess) return e;
     }
-    k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
-        a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+    if (rnn && rnn->tc) {  // the block pass on tcgen05
+      const cudaError_t e = launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
+      if (e != cudaSuccess) return e;
+    } else {
+      k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
+          a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+    }
     k_draft_pick<BF16><<<d.B, kSimtThreads, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec,
                                                        d.gamma, d.V, d.r, d.H, k, nblk, ws->s.blk, rng,
                                                        a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
@@ -248,7 +254,7 @@ cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void
   if (e == cudaSuccess) e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
   if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0
   if (e != cudaSuccess) return e;
-  const RnnStep rnn{Wr, Hp, S, ovec};
+  const RnnStep rnn{Wr, Hp, S, ovec, ws->use_tc && ws->geo.resid_tc_ok && ws->d.r <= 256};
   if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches, &rnn);
   return draft_simt_impl<0>(ws, a, st, launches, &rnn);
 }

@@ -54,15 +54,18 @@ constexpr int kRGather = kRN * (256 / 8) / (32 * 8);  // 16-byte W1 chunks per e
 constexpr int kModeResid = 0;      // per block: residual mass and Gumbel key; the best block per CTA
 constexpr int kModeLossStats = 1;  // per column: (max, sum exp) of z_d and of z_t over the CTA's tiles, z_d at x*
 constexpr int kModeLossL1 = 2;     // per column: sum |p_d - p_t| over the CTA's tiles
+constexpr int kModeDraft = 3;      // per column (request) and 64-token block: log sum exp z of one draft step
+                                   // of the RNN head, z = U_k + o_k W2 with o_k split into bf16 hi + lo parts
 
 struct RSmem {
-  uint32_t bop, w2, up, col, part, best, gum, list, bars, misc, total;
-  __host__ __device__ static RSmem make(int r) {
+  uint32_t bop, w2, up, stage, col, part, best, gum, list, bars, misc, total;
+  __host__ __device__ static RSmem make(int r, bool draft) {
     RSmem s;
-    s.bop = 0;                              // [128 requests x r] bf16, K-major swizzled
-    s.w2 = s.bop + kRN * r * 2;             // kRNW x (two boxes of [r/2 x 64] bf16: one K-half of a tile)
-    s.up = s.w2 + kRNW * r * 128;           // kRUP x [request][U slice | P slice] fp32
-    s.col = s.up + kRUP * kRUPStage;        // per-request: b, n, row, x (int), lse_d, lse_t (float)
+    s.bop = 0;                              // [32 columns x r] bf16, K-major swizzled (draft: hi, then lo)
+    s.w2 = s.bop + (draft ? 2 : 1) * kRN * r * 2;  // kRNW x (two boxes of [r/2 x 64] bf16: one K-half of a tile)
+    s.up = s.w2 + kRNW * r * 128;           // kRUP x [request][U slice | P slice] fp32 (draft: U rows only)
+    s.stage = draft ? kRN * kRM * 4 : kRUPStage;
+    s.col = s.up + kRUP * s.stage;          // per-request: b, n, row, x (int), lse_d, lse_t (float)
     s.part = s.col + 6 * 4 * kRN;           // [4 quarters][32 columns] partials (float4 for the loss statistics)
     s.best = s.part + 4 * 16 * kRN;         // [128] best key, [128] best block
     s.gum = s.best + 2 * 4 * kRN;           // [kRN][kRGMax] block Gumbels of this CTA's blocks
@@ -97,6 +100,11 @@ struct RParams {
   float* l1part;         // [B*g][G] sum |p_d - p_t| over the CTA's tiles
   const float* lse_d;    // [B*g]
   const float* lse_t;    // [B*g]
+  // one draft step of the RNN head: column b takes o_k of request b
+  const float* ovec;     // [B][g][r] fp32
+  int step;              // k (1-based)
+  float* blk;            // [B][nblk] block log-masses
+  int nblk;
 };
 
 // Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
@@ -116,6 +124,22 @@ __device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
     }
   }
   return a[0] + __shfl_xor_sync(0xFFFFFFFFu, a[0], 16);
+}
+
+// The same transpose over 32 lanes with a maximum instead of a sum.
+__device__ __forceinline__ float transpose_max16(float (&a)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? a[k] : a[k + o];
+      const float keep = upper ? a[k + o] : a[k];
+      a[k] = fmaxf(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+    }
+  }
+  return fmaxf(a[0], __shfl_xor_sync(0xFFFFFFFFu, a[0], 16));
 }
 
 constexpr float kNegBig = -1e30f;  // "no entry yet" of a running maximum (finite: no inf - inf)
@@ -163,7 +187,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const RSmem L = RSmem::make(p.r);
+  const RSmem L = RSmem::make(p.r, MODE == kModeDraft);
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sB = sbase + L.bop, sW2 = sbase + L.w2;
   int* col_b = reinterpret_cast<int*>(smem + L.col);
@@ -240,6 +264,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         base += __popc(m);
       }
       if (lane == 0) *s_nrej = base;
+    } else if constexpr (MODE == kModeDraft) {
+      if (lane == 0) *s_nrej = p.B;  // every request is a column
     } else {
       if (lane == 0) *s_nrej = p.B * p.g;  // every position is a column
     }
@@ -317,15 +343,20 @@ __global__ void __launch_bounds__(kRThreads, 1)
           if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), 2u * bytes * (uint32_t)ncols);
           __syncwarp();
           if (lane < ncols) {
-            const uint32_t dst = sUP + us * kRUPStage + lane * (2 * kRM * 4);
+            const uint32_t dst = sUP + us * L.stage + lane * (2 * kRM * 4);
             tc::bulk_load(dst, urow + v0, bytes, up_full(us));
             tc::bulk_load(dst + kRM * 4, prow + v0, bytes, up_full(us));
           }
-        } else if (lane == 0) {
+        } else if (MODE == kModeDraft && lane == 0) {
+          // U_k of the group's 32 requests: one [32 x 128] box of the
+          // tensor map whose rows are the requests (stride gamma V)
+          tc::mbar_arrive_expect_tx(up_full(us), (uint32_t)(kRN * kRM * 4));
+          tc::tma_load_2d(sUP + us * L.stage, &tm_u, v0, gq * kRN, up_full(us), stream_pol);
+        } else if (MODE != kModeDraft && lane == 0) {
           // the group's 32 consecutive rows of U and of P: one [32 x 128] box
           // each (rows past B*gamma and entries past V read as zeros)
           tc::mbar_arrive_expect_tx(up_full(us), (uint32_t)kRUPStage);
-          const uint32_t dst = sUP + us * kRUPStage;
+          const uint32_t dst = sUP + us * L.stage;
           tc::tma_load_2d(dst, &tm_u, v0, gq * kRN, up_full(us), stream_pol);
           tc::tma_load_2d(dst + kRN * kRM * 4, &tm_p, v0, gq * kRN, up_full(us), stream_pol);
         }
@@ -364,8 +395,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
               const int ks = h * (p.r / 32) + kh;
               // A: two 64-wide M atoms (LBO apart), 8 K rows per 1 KB atom (SBO)
               const uint64_t ad = tc::smem_desc(astage + kh * 2048, box_bytes, 1024);
-              const uint64_t bd = tc::smem_desc(sB + (ks >> 2) * (kRN * 128) + (ks & 3) * 32, 16, 1024);
-              tc::mma_bf16(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+              const uint32_t boff = (ks >> 2) * (kRN * 128) + (ks & 3) * 32;
+              tc::mma_bf16(d, ad, tc::smem_desc(sB + boff, 16, 1024), idesc, ks > 0 ? 1u : 0u);
+              if constexpr (MODE == kModeDraft)  // the lo part of o_k against the same W2 rows
+                tc::mma_bf16(d, ad, tc::smem_desc(sB + kRN * p.r * 2 + boff, 16, 1024), idesc, 1u);
             }
             tc::mma_commit(w2_empty(ws));
           }
@@ -407,6 +440,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             col_row[et] = p.vrow[b];
             col_nld[et] = -p.lse[(size_t)b * p.g + n] * tc::kLog2e;
             col_nlt[et] = -p.vlset[b] * tc::kLog2e;
+          } else if constexpr (MODE == kModeDraft) {
+            col_b[et] = i;  // request i; its B row is o_k, not a W1 row
+            x = i;
           } else {  // teacher forcing: position k drafts from x*_{k-1} (the anchor at k = 0)
             const int b = i / p.g, k = i - b * p.g;
             x = k == 0 ? p.anchor[b] : p.xstar[i - 1];
@@ -423,7 +459,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
               col_nlt[et] = -p.lse_t[i] * tc::kLog2e;
             }
           }
-          if (x < 0 || x >= p.V) {
+          if (MODE != kModeDraft && (x < 0 || x >= p.V)) {
             raise_status(p.status, DSPARK_ERANGE);
             x = 0;
           }
@@ -440,6 +476,50 @@ __global__ void __launch_bounds__(kRThreads, 1)
         // epilogue thread loads up to kRGather 16-byte chunks (consecutive
         // threads take consecutive chunks of a row), all in flight at once
         const int cpr = p.r / 8;  // 16-byte chunks per row
+        if constexpr (MODE == kModeDraft) {
+          // o_k rows in fp32 -> hi = bf16(o), lo = bf16(o - hi), eight values per chunk
+          float4 f[kRGather][2];
+#pragma unroll
+          for (int j = 0; j < kRGather; ++j) {
+            const int idx = et + j * 32 * kREpi;
+            f[j][0] = f[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (idx < kRN * cpr) {
+              const int m = idx / cpr, b = col_x[m];
+              if (b >= 0) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.ovec + ((size_t)b * p.g + (p.step - 1)) * p.r + (size_t)(idx - m * cpr) * 8);
+                f[j][0] = __ldg(src);
+                f[j][1] = __ldg(src + 1);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kRGather; ++j) {
+            const int idx = et + j * 32 * kREpi;
+            if (idx < kRN * cpr) {
+              const int m = idx / cpr, cc = idx - m * cpr, kb = cc >> 3, ch = cc & 7;
+              const float x8[8] = {f[j][0].x, f[j][0].y, f[j][0].z, f[j][0].w,
+                                   f[j][1].x, f[j][1].y, f[j][1].z, f[j][1].w};
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int t2 = 0; t2 < 4; ++t2) {
+                const __nv_bfloat16 h0 = __float2bfloat16_rn(x8[2 * t2]), h1 = __float2bfloat16_rn(x8[2 * t2 + 1]);
+                const __nv_bfloat16 l0 = __float2bfloat16_rn(x8[2 * t2] - __bfloat162float(h0));
+                const __nv_bfloat16 l1 = __float2bfloat16_rn(x8[2 * t2 + 1] - __bfloat162float(h1));
+                hi[t2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                lo[t2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+              }
+              const uint32_t dst = sB + kb * (kRN * 128) + (m >> 3) * 1024 + (m & 7) * 128 +
+                                   ((uint32_t)(ch ^ (m & 7)) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(hi[0]), "r"(hi[1]),
+                           "r"(hi[2]), "r"(hi[3])
+                           : "memory");
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + kRN * p.r * 2), "r"(lo[0]),
+                           "r"(lo[1]), "r"(lo[2]), "r"(lo[3])
+                           : "memory");
+            }
+          }
+        } else {
         uint4 v[kRGather];
 #pragma unroll
         for (int j = 0; j < kRGather; ++j) {
@@ -461,6 +541,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                          "r"(v[j].z), "r"(v[j].w)
                          : "memory");
           }
+        }
         }
         tc::fence_proxy_async_smem();
         __syncwarp();
@@ -517,11 +598,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
             // [32 rows of U][32 rows of P] (the loss modes' two boxes)
             constexpr uint32_t kRow = MODE == kModeResid ? 2 * kRM * 4 : kRM * 4;
             constexpr uint32_t kPOff = MODE == kModeResid ? kRM * 4 : kRN * kRM * 4;
-            const uint32_t su = sUP + us * kRUPStage + (uint32_t)(half * 16) * kRow + (uint32_t)(q * 32 + lane) * 4u;
+            const uint32_t su = sUP + us * L.stage + (uint32_t)(half * 16) * kRow + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * kRow));
-              asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * kRow + kPOff));
+              if constexpr (MODE != kModeDraft)
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * kRow + kPOff));
             }
             if constexpr (MODE == kModeLossStats) {
               // running (max, sum 2^(y - max)) of y = z log2(e) per column,
@@ -535,6 +617,25 @@ __global__ void __launch_bounds__(kRThreads, 1)
                 online_add(ra[j], rb[j], ok ? zd * tc::kLog2e : -INFINITY);
                 online_add(rc[j], rd[j], ok ? pp[j] * tc::kLog2e : -INFINITY);
               }
+            } else if constexpr (MODE == kModeDraft) {
+              // per column, over this warp's 32 entries (half of a 64-token
+              // block): max and sum exp of z = D + U (a transpose-max, the
+              // columns' maxima broadcast, then a transpose-sum)
+              float zd[16], e[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int col = half * 16 + j;
+                zd[j] = (col < ncols && v < p.V) ? a[j] + uu[j] : -INFINITY;
+                e[j] = zd[j];
+              }
+              const float mx = transpose_max16(e);  // lane l: column 16 half + (l & 15)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float mj = __shfl_sync(0xFFFFFFFFu, mx, j);
+                e[j] = zd[j] == -INFINITY ? 0.f : tc::ex2_ftz((zd[j] - mj) * tc::kLog2e);
+              }
+              const float sm = transpose_sum16(e);
+              if (lane < 16) reinterpret_cast<float2*>(part)[q * kRN + half * 16 + lane] = make_float2(mx, sm);
             } else if constexpr (MODE == kModeLossL1) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -562,6 +663,22 @@ __global__ void __launch_bounds__(kRThreads, 1)
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
+        }
+        if constexpr (MODE == kModeDraft) {
+          asm volatile("bar.sync 2, 256;" ::: "memory");
+          // block 2t from quarters 0, 1 and block 2t + 1 from quarters 2, 3
+          if (live && et < 2 * ncols) {
+            const int col = et >> 1, hh = et & 1, sblk = 2 * t + hh;
+            if (sblk * 64 < p.V) {
+              const float2 p0 = reinterpret_cast<const float2*>(part)[(2 * hh) * kRN + col];
+              const float2 p1 = reinterpret_cast<const float2*>(part)[(2 * hh + 1) * kRN + col];
+              const float m = fmaxf(p0.x, p1.x);
+              float lm = -INFINITY;
+              if (m > -INFINITY) lm = m + logf(p0.y * __expf(p0.x - m) + p1.y * __expf(p1.x - m));
+              p.blk[(size_t)col_b[col] * p.nblk + sblk] = lm;
+            }
+          }
+          asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
         }
         if constexpr (MODE == kModeResid) {
           asm volatile("bar.sync 2, 256;" ::: "memory");
@@ -616,7 +733,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           for (int col = lane; col < ncols; col += 32)
             p.l1part[(size_t)col_b[col] * p.G + c] =
                 (part[col] + part[kRN + col]) + (part[2 * kRN + col] + part[3 * kRN + col]);
-      } else {
+      } else if constexpr (MODE == kModeResid) {
         if (warp == 4 && !aborted())
           for (int col = lane; col < ncols; col += 32)
             p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
@@ -652,13 +769,16 @@ int resid_tc_supported(const dspark_dims& d) {
 }
 
 cudaError_t resid_tc_configure(dspark_ws* ws) {
-  const RSmem L = RSmem::make(ws->d.r);
+  const RSmem L = RSmem::make(ws->d.r, false);
   const size_t smem = L.total + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_resid_tc<kModeResid>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_resid_tc<kModeLossStats>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_resid_tc<kModeLossL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_resid_tc<kModeDraft>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(RSmem::make(ws->d.r, true).total + 1024));
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_resid_tc<kModeResid>, kRThreads, smem);
@@ -688,12 +808,13 @@ cudaError_t w2_tensor_map(const dspark_dims& d, const void* W2, CUtensorMap* tm)
   return cudaSuccess;
 }
 
-// A [rows x V] fp32 matrix as boxes of [32 rows x 128 entries], no swizzle.
-cudaError_t rows_tensor_map(const float* X, int rows, int V, CUtensorMap* tm) {
+// A [rows x V] fp32 matrix (rows `stride` floats apart) as boxes of
+// [32 rows x 128 entries], no swizzle.
+cudaError_t rows_tensor_map(const float* X, int rows, int V, size_t stride, CUtensorMap* tm) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)V * 4};
+  const cuuint64_t strides[1] = {(cuuint64_t)stride * 4};
   const cuuint32_t box[2] = {(cuuint32_t)kRM, (cuuint32_t)kRN};
   const cuuint32_t es[2] = {1, 1};
   if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides, box, es,
@@ -737,7 +858,7 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.vrow = ws->s.vrow;
   p.vlset = ws->s.vlset;
   p.rpart = rpart;
-  const RSmem L = RSmem::make(d.r);
+  const RSmem L = RSmem::make(d.r, false);
   k_resid_tc<kModeResid><<<grid, kRThreads, L.total + 1024, st>>>(tm, tm, tm, p);
   return cudaGetLastError();
 }
@@ -749,8 +870,8 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
   if (e != cudaSuccess) return e;
   CUtensorMap tu, tp;
   const int rows = d.B * d.gamma;
-  e = rows_tensor_map(a.U, rows, d.V, &tu);
-  if (e == cudaSuccess) e = rows_tensor_map(a.P, rows, d.V, &tp);
+  e = rows_tensor_map(a.U, rows, d.V, (size_t)d.V, &tu);
+  if (e == cudaSuccess) e = rows_tensor_map(a.P, rows, d.V, (size_t)d.V, &tp);
   if (e != cudaSuccess) return e;
   RParams p = base_params(ws, ws->geo.num_sms);
   p.P = a.P;
@@ -763,11 +884,30 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
   p.l1part = a.l1part;
   p.lse_d = a.lse_d;
   p.lse_t = a.lse_t;
-  const RSmem L = RSmem::make(d.r);
+  const RSmem L = RSmem::make(d.r, false);
   if (pass == 0)
     k_resid_tc<kModeLossStats><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tp, p);
   else
     k_resid_tc<kModeLossL1><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tp, p);
+  return cudaGetLastError();
+}
+
+// One draft step k of the RNN head: blk[b][s] = log sum_{v in block s} exp z_v
+// with z = U_k + o_k W2 for every request. Grid = one CTA per SM.
+cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
+                                 cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  CUtensorMap tm, tu;
+  cudaError_t e = w2_tensor_map(d, W2, &tm);
+  if (e == cudaSuccess) e = rows_tensor_map(U + (size_t)(k - 1) * d.V, d.B, d.V, (size_t)d.gamma * d.V, &tu);
+  if (e != cudaSuccess) return e;
+  RParams p = base_params(ws, ws->geo.num_sms);
+  p.ovec = ovec;
+  p.step = k;
+  p.blk = ws->s.blk;
+  p.nblk = ws->geo.nblk;
+  const RSmem L = RSmem::make(d.r, true);
+  k_resid_tc<kModeDraft><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tu, p);
   return cudaGetLastError();
 }
 

@@ -28,11 +28,11 @@ def _built():
     build.build()
 
 
-def _run(wl, rnd=0, reqs=None):
+def _run(wl, rnd=0, reqs=None, path=None):
     inp = make_inputs(wl, with_target=False)
     inp["Wr"] = make_rnn_weights(wl)
     dev, npi = to_device(inp), np_inputs(inp)
-    ws = Workspace.for_workload(wl)
+    ws = Workspace.for_workload(wl, path=path)
     out = ws.rnn_draft(dev["U"], dev["W1"], dev["W2"], dev["Wr"], dev["anchor"], dev["h"], dev["w"], dev["T"],
                        wl.seed, rnd)
     torch.cuda.synchronize()
@@ -66,6 +66,12 @@ def _wl(name, B, gamma, V, r, H, wdtype="bf16", seed=41):
 ], ids=lambda w: w.name)
 def test_rnn_draft_parity(wl):
     _run(wl, rnd=1)
+
+
+def test_rnn_draft_simt_block_pass():
+    """The SIMT block pass (the fallback for shapes tcgen05 does not take) on
+    a bf16 shape the tcgen05 pass also takes."""
+    _run(_wl("rnn_small_simt", 6, 4, 4104, 64, 96), rnd=2, path="simt")
 
 
 def test_rnn_draft_full_size_sampled():
