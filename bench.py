@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sts", action="store_true", help="skip the STS calibration-fit timing")
     ap.add_argument("--no-loss", action="store_true", help="skip the training-objective timing")
+    ap.add_argument("--no-rnn", action="store_true", help="skip the RNN-head draft timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 
@@ -270,6 +271,40 @@ def loss_timing(peak_gbs: float, reps: int = 10):
             "loss": float(out["loss"].item())}
 
 
+def rnn_timing(peak_gbs: float, reps: int = 10):
+    """The draft tail with the RNN head on the prod shape: device time per
+    call, CUDA events on the launching stream after warm-up, inputs resident.
+    The algorithmic bytes are the Markov draft's (U once, W2 once per step,
+    h once) plus the three gate matrices once."""
+    import torch
+    from speculative_decoding_head_gb300.binding import Workspace
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_rnn_weights
+    wl = WORKLOADS["prod"]
+    inp = {k: v.cuda() for k, v in make_inputs(wl, with_target=False).items()}
+    Wr = make_rnn_weights(wl).cuda()
+    ws = Workspace.for_workload(wl)
+    out = None
+    for _ in range(3):
+        out = ws.rnn_draft(inp["U"], inp["W1"], inp["W2"], Wr, inp["anchor"], inp["h"], inp["w"], inp["T"], 1, 0,
+                           out=out)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        ws.rnn_draft(inp["U"], inp["W1"], inp["W2"], Wr, inp["anchor"], inp["h"], inp["w"], inp["T"], 1, i + 1,
+                     out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    B, g, V, r, H = wl.B, wl.gamma, wl.V, wl.r, wl.H
+    alg = B * g * V * 4 + g * r * V * 2 + B * g * H * 4 + 3 * r * (2 * r + H) * 2
+    gbs = alg / (ms * 1e-3) / 1e9
+    return {"workload": "prod", "B": B, "gamma": g, "V": V, "r": r, "H": H, "ms_per_call": ms,
+            "drafted_tokens_per_s": B * g / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches, "path": "tcgen05 block pass"}
+
+
 def run_reference(args):
     """The oracle itself as the reference arm (rank 0 only)."""
     import torch
@@ -476,6 +511,7 @@ def main():
             "stage_ms": st,
             "sts_fit": None if args.no_sts else sts_timing(),
             "train_loss": None if args.no_loss else loss_timing(peak),
+            "rnn_draft": None if args.no_rnn else rnn_timing(peak),
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": e2e,

@@ -252,7 +252,7 @@ cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void
                              float* ovec, cudaStream_t st, int* launches) {
   cudaError_t e = launch_conf_hidden(ws, a.h, a.w, st, launches);
   if (e == cudaSuccess) e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
-  if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0
+  if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0 (buffer 0)
   if (e != cudaSuccess) return e;
   const RnnStep rnn{Wr, Hp, S, ovec, ws->use_tc && ws->geo.resid_tc_ok && ws->d.r <= 256};
   if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches, &rnn);

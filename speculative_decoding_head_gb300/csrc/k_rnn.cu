@@ -8,15 +8,16 @@
 //   s_k = sigma(W_g z_k) * s_{k-1} + (1 - sigma(W_g z_k)) * tanh(W_c z_k),
 //   B_k = W2^T tanh(W_o z_k),
 // s_0 = 0 and x_0 = the anchor. The weights are stacked as Wr [3][r][2r + H]
-// (W_g, W_c, W_o) in the dtype of W1 and W2. The draft tail then runs the
-// Markov draft's SIMT kernels with o_k = tanh(W_o z_k) in place of W1[x_{k-1}]
-// (k_draft_simt.cu).
+// (W_g, W_c, W_o) in the dtype of W1 and W2. The draft tail then takes
+// o_k = tanh(W_o z_k) in place of W1[x_{k-1}]: the vocabulary pass on tcgen05
+// (k_resid_tc.cu, o_k as bf16 hi + lo operands) or on CUDA cores, then the
+// SIMT pick (k_draft_simt.cu).
 //
 // Two kernels: k_rnn_hproj, once per round, the h_k part of all three
 // projections for every position (a [B*gamma x H] x [H x 3r] product, the
 // bulk of the cell's arithmetic, which does not depend on drafted tokens);
-// k_rnn_cell, before each draft step, one CTA per request: the [s; W1[x]]
-// part (a warp per output row), then the gate, the state update and o_k.
+// k_rnn_cell, before each draft step, one CTA per 16 state entries and 16
+// requests: the [s; W1[x]] part, then the gate, the state update and o_k.
 #include <stdio.h>
 
 #include "dspark_common.cuh"
@@ -28,11 +29,36 @@ namespace {
 
 constexpr int kHpTile = 64;     // output tile of k_rnn_hproj (rows x columns)
 constexpr int kHpK = 32;        // K step
+constexpr int kHpSplit = 4;     // K is split over 4 CTAs; each writes its own partial product
 constexpr int kCellThreads = 256;
+constexpr int kCellJ = 16;  // state entries per CTA of k_rnn_cell
+constexpr int kCellB = 16;  // requests per CTA of k_rnn_cell (kCellJ x kCellB = threads)
+static_assert(kCellJ * kCellB == kCellThreads, "one (entry, request) per thread in the update");
+static_assert(kHpSplit == 4, "k_rnn_cell adds four slices of the h projection");
 
-// Hp[m][n] = sum_{i<H} h[m][i] Wr[n][2r + i] for m < M = B*gamma, n < 3r:
-// 64 x 64 output tiles, 256 threads with 4 x 4 outputs each, K in steps of 32
-// staged in shared memory (fp32 accumulation).
+// Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
+// sum of every lane's a[L & 15] (each step keeps the half whose index bit
+// matches the lane's bit and adds the partner's other half).
+__device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int q = 0; q < o; ++q) {
+      const float send = upper ? a[q] : a[q + o];
+      const float keep = upper ? a[q + o] : a[q];
+      a[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+  return a[0] + __shfl_xor_sync(0xFFFFFFFFu, a[0], 16);
+}
+
+// Hp[p][m][n] = sum_{i in slice p of H} h[m][i] Wr[n][2r + i] for m < M =
+// B*gamma, n < 3r and the kHpSplit slices p of the H inputs (the cell adds the
+// slices in order): 64 x 64 output tiles, 256 threads with 4 x 4 outputs each,
+// K in steps of 32 staged in shared memory (fp32 accumulation), the next
+// step's operands loaded into registers while one step computes.
 template <int BF16>
 __global__ void __launch_bounds__(256)
     k_rnn_hproj(const float* __restrict__ h, const void* __restrict__ Wr, int M, int H, int r,
@@ -41,17 +67,32 @@ __global__ void __launch_bounds__(256)
   __shared__ float Bs[kHpK][kHpTile + 4];
   const int N = 3 * r, Z = 2 * r + H;
   const int m0 = blockIdx.y * kHpTile, n0 = blockIdx.x * kHpTile;
+  const int ksl = (H + kHpSplit - 1) / kHpSplit;
+  const int kbeg = blockIdx.z * ksl, kend = min(H, kbeg + ksl);
+  Hp += (size_t)blockIdx.z * M * N;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += kHpK) {
+  constexpr int kPer = (kHpTile * kHpK) / 256;
+  // the next K step's operands are loaded into registers while this one computes
+  float ra[kPer], rw[kPer];
+  auto gload = [&](int k0) {
 #pragma unroll
-    for (int q = 0; q < (kHpTile * kHpK) / 256; ++q) {
+    for (int q = 0; q < kPer; ++q) {
+      const int idx = tid + q * 256, row = idx / kHpK, kg = k0 + idx % kHpK;
+      ra[q] = (m0 + row < M && kg < kend) ? h[(size_t)(m0 + row) * H + kg] : 0.f;
+      rw[q] = (n0 + row < N && kg < kend) ? ld_w(Wr, BF16, (size_t)(n0 + row) * Z + 2 * r + kg) : 0.f;
+    }
+  };
+  gload(kbeg);
+  for (int k0 = kbeg; k0 < kend; k0 += kHpK) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
       const int idx = tid + q * 256, row = idx / kHpK, kk = idx % kHpK;
-      const int kg = k0 + kk;
-      As[kk][row] = (m0 + row < M && kg < H) ? h[(size_t)(m0 + row) * H + kg] : 0.f;
-      Bs[kk][row] = (n0 + row < N && kg < H) ? ld_w(Wr, BF16, (size_t)(n0 + row) * Z + 2 * r + kg) : 0.f;
+      As[kk][row] = ra[q];
+      Bs[kk][row] = rw[q];
     }
     __syncthreads();
+    if (k0 + kHpK < kend) gload(k0 + kHpK);
 #pragma unroll 8
     for (int kk = 0; kk < kHpK; ++kk) {
       float a[4], b[4];
@@ -76,49 +117,94 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Step k of request b = blockIdx.x: pre = W_{g,c,o}[:, :2r] [s_{k-1}; W1[x_{k-1}]]
-// + Hp (a warp per output row, lanes across the 2r inputs), then the gate, the
-// state update (S in place: this CTA alone owns row b) and o_k.
+// Step k for requests b0 .. b0 + 15 and state entries j0 .. j0 + 15 (one CTA):
+// pre = W_{g,c,o}[:, :2r] [s_{k-1}; W1[x_{k-1}]] + Hp. Warp w takes entries
+// j0 + w and j0 + w + 8; for each it runs the three rows (g, c, o) over the
+// 2r inputs with the 16 requests' inputs from shared memory (lanes across the
+// inputs), then one transpose-reduce per row. The gate, the state update and
+// o_k follow per (entry, request). The state is double-buffered by step
+// parity (every CTA reads the whole s_{k-1} of its requests).
 template <int BF16>
 __global__ void __launch_bounds__(kCellThreads)
     k_rnn_cell(const void* __restrict__ W1, const void* __restrict__ Wr, const int32_t* __restrict__ anchor,
-               const int32_t* __restrict__ tokens, const float* __restrict__ Hp, float* __restrict__ S,
-               float* __restrict__ ovec, int g, int V, int r, int H, int k, int* __restrict__ status) {
-  extern __shared__ float sm[];
-  float* zin = sm;          // [2r]: s_{k-1}, W1[x_{k-1}]
-  float* pre = sm + 2 * r;  // [3r]: the three pre-activations
-  const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x = k == 1 ? anchor[b] : tokens[(size_t)b * g + (k - 2)];
-  if (x < 0 || x >= V) {
-    if (tid == 0) raise_status(status, DSPARK_ERANGE);
-    return;
-  }
-  for (int i = tid; i < r; i += kCellThreads) {
-    zin[i] = S[(size_t)b * r + i];
-    zin[r + i] = ld_w(W1, BF16, (size_t)x * r + i);
+               const int32_t* __restrict__ tokens, const float* __restrict__ Hp, const float* __restrict__ S_in,
+               float* __restrict__ S_out, float* __restrict__ ovec, int B, int g, int V, int r, int H, int k,
+               int* __restrict__ status) {
+  extern __shared__ float zin[];  // [kCellB][2r]: s_{k-1}, W1[x_{k-1}] of each request
+  __shared__ float pre[3][kCellJ][kCellB];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j0 = blockIdx.x * kCellJ, b0 = blockIdx.y * kCellB;
+  const int r2 = 2 * r, Z = r2 + H;
+  for (int rb = 0; rb < kCellB; ++rb) {
+    const int b = b0 + rb;
+    int x = 0;
+    if (b < B) {
+      x = k == 1 ? anchor[b] : tokens[(size_t)b * g + (k - 2)];
+      if (x < 0 || x >= V) {
+        if (tid == 0) raise_status(status, DSPARK_ERANGE);
+        x = 0;
+      }
+    }
+    for (int i = tid; i < r; i += kCellThreads) {
+      zin[rb * r2 + i] = b < B ? S_in[(size_t)b * r + i] : 0.f;
+      zin[rb * r2 + r + i] = b < B ? ld_w(W1, BF16, (size_t)x * r + i) : 0.f;
+    }
   }
   __syncthreads();
-  const int Z = 2 * r + H;
-  const size_t row = (size_t)b * g + (k - 1);
-  for (int n = warp; n < 3 * r; n += kCellThreads / 32) {
-    float acc = 0.f;
-    for (int i = lane; i < 2 * r; i += 32) acc = fmaf(ld_w(Wr, BF16, (size_t)n * Z + i), zin[i], acc);
-    acc = warp_sum(acc);
-    if (lane == 0) pre[n] = acc + Hp[row * 3 * r + n];
+  for (int jj = warp; jj < kCellJ; jj += kCellThreads / 32) {
+    const int j = j0 + jj;
+    if (j >= r) break;  // warp-uniform
+    float acc[3][kCellB];
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int rb = 0; rb < kCellB; ++rb) acc[q][rb] = 0.f;
+    for (int i = lane; i < r2; i += 32) {
+      const float wg = ld_w(Wr, BF16, (size_t)j * Z + i);
+      const float wc = ld_w(Wr, BF16, (size_t)(r + j) * Z + i);
+      const float wo = ld_w(Wr, BF16, (size_t)(2 * r + j) * Z + i);
+#pragma unroll
+      for (int rb = 0; rb < kCellB; ++rb) {
+        const float zv = zin[rb * r2 + i];
+        acc[0][rb] = fmaf(wg, zv, acc[0][rb]);
+        acc[1][rb] = fmaf(wc, zv, acc[1][rb]);
+        acc[2][rb] = fmaf(wo, zv, acc[2][rb]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const float sum = transpose_sum16(acc[q]);  // lane l: request l & 15
+      if (lane < kCellB) pre[q][jj][lane] = sum;
+    }
   }
   __syncthreads();
-  for (int j = tid; j < r; j += kCellThreads) {
-    const float gk = 1.f / (1.f + expf(-pre[j]));
-    S[(size_t)b * r + j] = gk * zin[j] + (1.f - gk) * tanhf(pre[r + j]);
-    ovec[row * r + j] = tanhf(pre[2 * r + j]);
+  {
+    const int jj = tid % kCellJ, rb = tid / kCellJ, j = j0 + jj, b = b0 + rb;
+    if (j < r && b < B) {
+      const size_t row = (size_t)b * g + (k - 1);
+      const size_t slice = (size_t)B * g * 3 * r;  // the h projection's K slices, added in order
+      float hq[3];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const float* hp = Hp + row * 3 * r + q * r + j;
+        hq[q] = ((hp[0] + hp[slice]) + hp[2 * slice]) + hp[3 * slice];
+      }
+      const float gk = 1.f / (1.f + expf(-(pre[0][jj][rb] + hq[0])));
+      S_out[(size_t)b * r + j] = gk * zin[rb * r2 + j] + (1.f - gk) * tanhf(pre[1][jj][rb] + hq[1]);
+      ovec[row * r + j] = tanhf(pre[2][jj][rb] + hq[2]);
+    }
   }
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Scratch: Hp [B*gamma][3r] fp32, then S [B][r] fp32 (256-byte aligned).
-size_t hp_bytes(const dspark_dims& d) { return round_up(sizeof(float) * (size_t)d.B * d.gamma * 3 * d.r, 256); }
-size_t state_bytes(const dspark_dims& d) { return round_up(sizeof(float) * (size_t)d.B * d.r, 256); }
+// Scratch: Hp [4][B*gamma][3r] fp32 (the h projection's K slices), then the
+// state S [2][B][r] fp32 (two buffers alternating by step parity; 256-byte
+// aligned).
+size_t hp_bytes(const dspark_dims& d) {
+  return round_up(sizeof(float) * kHpSplit * (size_t)d.B * d.gamma * 3 * d.r, 256);
+}
+size_t state_bytes(const dspark_dims& d) { return round_up(2 * sizeof(float) * (size_t)d.B * d.r, 256); }
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -128,8 +214,8 @@ cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr
                              int* launches) {
   const dspark_dims& d = ws->d;
   const int M = d.B * d.gamma, N = 3 * d.r;
-  if (d.H == 0) return cudaMemsetAsync(Hp, 0, sizeof(float) * (size_t)M * N, st);
-  const dim3 grid((N + kHpTile - 1) / kHpTile, (M + kHpTile - 1) / kHpTile);
+  if (d.H == 0) return cudaMemsetAsync(Hp, 0, sizeof(float) * kHpSplit * (size_t)M * N, st);
+  const dim3 grid((N + kHpTile - 1) / kHpTile, (M + kHpTile - 1) / kHpTile, kHpSplit);
   if (d.wdtype == DSPARK_BF16)
     k_rnn_hproj<1><<<grid, 256, 0, st>>>(h, Wr, M, d.H, d.r, Hp);
   else
@@ -141,13 +227,28 @@ cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr
 cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void* Wr, const float* Hp, float* S,
                             float* ovec, int k, cudaStream_t st, int* launches) {
   const dspark_dims& d = ws->d;
-  const size_t smem = sizeof(float) * 5 * (size_t)d.r;
+  const size_t smem = sizeof(float) * kCellB * 2 * (size_t)d.r;  // 128 KB at r = 1024
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_rnn_cell<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(float) * kCellB * 2 * 1024));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_rnn_cell<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(sizeof(float) * kCellB * 2 * 1024));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  // step k reads the state of step k - 1 from buffer (k - 1) % 2, writes buffer k % 2
+  const size_t BR = (size_t)d.B * d.r;
+  const float* S_in = S + ((k - 1) & 1) * BR;
+  float* S_out = S + (k & 1) * BR;
+  const dim3 grid((d.r + kCellJ - 1) / kCellJ, (d.B + kCellB - 1) / kCellB);
   if (d.wdtype == DSPARK_BF16)
-    k_rnn_cell<1><<<d.B, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S, ovec, d.gamma, d.V, d.r,
-                                                   d.H, k, ws->s.status);
+    k_rnn_cell<1><<<grid, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S_in, S_out, ovec, d.B,
+                                                    d.gamma, d.V, d.r, d.H, k, ws->s.status);
   else
-    k_rnn_cell<0><<<d.B, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S, ovec, d.gamma, d.V, d.r,
-                                                   d.H, k, ws->s.status);
+    k_rnn_cell<0><<<grid, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S_in, S_out, ovec, d.B,
+                                                    d.gamma, d.V, d.r, d.H, k, ws->s.status);
   ++*launches;
   return cudaGetLastError();
 }
@@ -173,7 +274,6 @@ extern "C" dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const v
       !aligned16(ovec) || !scratch || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
     return DSPARK_EINVAL;
   if (d.H > 0 && !aligned16(h)) return DSPARK_EINVAL;
-  if (5 * (size_t)d.r * sizeof(float) > 48 * 1024) return DSPARK_EUNSUPPORTED;  // the cell's shared memory
   char* base = static_cast<char*>(scratch);
   float* Hp = reinterpret_cast<float*>(base);
   float* S = reinterpret_cast<float*>(base + hp_bytes(d));
