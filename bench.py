@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--no-sts", action="store_true", help="skip the STS calibration-fit timing")
     ap.add_argument("--no-loss", action="store_true", help="skip the training-objective timing")
     ap.add_argument("--no-rnn", action="store_true", help="skip the RNN-head draft timing")
+    ap.add_argument("--only", choices=["loss", "rnn", "sts"], default=None,
+                    help="run one of the secondary timings alone and print its JSON (for profiling)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="with --only loss / rnn: the number of requests (default: the prod workload's)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 
@@ -237,7 +241,7 @@ def sts_timing(reps: int = 10):
             "temperatures": [round(float(t), 3) for t in T.cpu().tolist()]}
 
 
-def loss_timing(peak_gbs: float, reps: int = 10):
+def loss_timing(peak_gbs: float, reps: int = 10, batch=None):
     """The draft head's teacher-forced training objective on the prod shape:
     device time per call (five launches), CUDA events on the launching stream
     after warm-up, inputs resident (U and P, 0.66 GB, exceed the L2). The
@@ -245,7 +249,7 @@ def loss_timing(peak_gbs: float, reps: int = 10):
     import torch
     from speculative_decoding_head_gb300.binding import Workspace
     from speculative_decoding_head_gb300.workloads import WORKLOADS, make_loss_inputs
-    wl = WORKLOADS["prod"]
+    wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
     tau = 4.0
     inp = {k: v.cuda() for k, v in make_loss_inputs(wl).items()}
     ws = Workspace.for_workload(wl)
@@ -265,13 +269,14 @@ def loss_timing(peak_gbs: float, reps: int = 10):
     n = wl.B * wl.gamma
     alg = 2 * (2 * n * wl.V * 4 + wl.r * wl.V * 2)
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"workload": "prod", "B": wl.B, "gamma": wl.gamma, "V": wl.V, "r": wl.r, "ms_per_call": ms,
+    return {"workload": "prod" if batch is None else f"prod with B={batch}", "B": wl.B, "gamma": wl.gamma,
+            "V": wl.V, "r": wl.r, "ms_per_call": ms,
             "positions_per_s": n / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches,
             "loss": float(out["loss"].item())}
 
 
-def rnn_timing(peak_gbs: float, reps: int = 10):
+def rnn_timing(peak_gbs: float, reps: int = 10, batch=None):
     """The draft tail with the RNN head on the prod shape: device time per
     call, CUDA events on the launching stream after warm-up, inputs resident.
     The algorithmic bytes are the Markov draft's (U once, W2 once per step,
@@ -279,7 +284,7 @@ def rnn_timing(peak_gbs: float, reps: int = 10):
     import torch
     from speculative_decoding_head_gb300.binding import Workspace
     from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_rnn_weights
-    wl = WORKLOADS["prod"]
+    wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
     inp = {k: v.cuda() for k, v in make_inputs(wl, with_target=False).items()}
     Wr = make_rnn_weights(wl).cuda()
     ws = Workspace.for_workload(wl)
@@ -300,7 +305,8 @@ def rnn_timing(peak_gbs: float, reps: int = 10):
     B, g, V, r, H = wl.B, wl.gamma, wl.V, wl.r, wl.H
     alg = B * g * V * 4 + g * r * V * 2 + B * g * H * 4 + 3 * r * (2 * r + H) * 2
     gbs = alg / (ms * 1e-3) / 1e9
-    return {"workload": "prod", "B": B, "gamma": g, "V": V, "r": r, "H": H, "ms_per_call": ms,
+    return {"workload": "prod" if batch is None else f"prod with B={batch}", "B": B, "gamma": g, "V": V, "r": r,
+            "H": H, "ms_per_call": ms,
             "drafted_tokens_per_s": B * g / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches, "path": "tcgen05 block pass"}
 
@@ -337,6 +343,14 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.only is not None:
+        from speculative_decoding_head_gb300 import build as bmod
+        bmod.build()
+        peak, _ = peaks()
+        fn = {"loss": lambda: loss_timing(peak, batch=args.batch), "rnn": lambda: rnn_timing(peak, batch=args.batch),
+              "sts": sts_timing}[args.only]
+        print(json.dumps({"only": args.only, **fn()}), flush=True)
+        return
     import numpy as np
     import torch
     from speculative_decoding_head_gb300 import build as bmod
