@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kSimtThreads)
     if (q < 4) {
       float acc = 0.f;
       if (v < V)
+#pragma unroll 16  // the W2 loads of 16 rows in flight together (the FMA order is unchanged)
         for (int i = q; i < r; i += 4) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
       zpart[q][vl] = acc;
     }

@@ -27,14 +27,13 @@ namespace dspark {
 
 namespace {
 
-constexpr int kHpTile = 64;     // output tile of k_rnn_hproj (rows x columns)
-constexpr int kHpK = 32;        // K step
-constexpr int kHpSplit = 4;     // K is split over 4 CTAs; each writes its own partial product
+constexpr int kHpTile = 128;    // output tile of k_rnn_hproj (rows x columns)
+constexpr int kHpK = 16;        // K step
+constexpr int kHpSplit = 10;    // K is split over 10 CTAs (two per SM at prod); each writes its own partial product
 constexpr int kCellThreads = 256;
 constexpr int kCellJ = 16;  // state entries per CTA of k_rnn_cell
 constexpr int kCellB = 16;  // requests per CTA of k_rnn_cell (kCellJ x kCellB = threads)
 static_assert(kCellJ * kCellB == kCellThreads, "one (entry, request) per thread in the update");
-static_assert(kHpSplit == 4, "k_rnn_cell adds four slices of the h projection");
 
 // Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
 // sum of every lane's a[L & 15] (each step keeps the half whose index bit
@@ -56,24 +55,24 @@ __device__ __forceinline__ float transpose_sum16(float (&a)[16]) {
 
 // Hp[p][m][n] = sum_{i in slice p of H} h[m][i] Wr[n][2r + i] for m < M =
 // B*gamma, n < 3r and the kHpSplit slices p of the H inputs (the cell adds the
-// slices in order): 64 x 64 output tiles, 256 threads with 4 x 4 outputs each,
-// K in steps of 32 staged in shared memory (fp32 accumulation), the next
+// slices in order): 128 x 128 output tiles, 256 threads with 8 x 8 outputs
+// each (two 4-wide strips per dimension, read as float4 from shared memory),
+// K in steps of 16 staged in shared memory (fp32 accumulation), the next
 // step's operands loaded into registers while one step computes.
 template <int BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     k_rnn_hproj(const float* __restrict__ h, const void* __restrict__ Wr, int M, int H, int r,
                 float* __restrict__ Hp) {
-  __shared__ float As[kHpK][kHpTile + 4];
-  __shared__ float Bs[kHpK][kHpTile + 4];
+  __shared__ __align__(16) float As[kHpK][kHpTile];
+  __shared__ __align__(16) float Bs[kHpK][kHpTile];
   const int N = 3 * r, Z = 2 * r + H;
   const int m0 = blockIdx.y * kHpTile, n0 = blockIdx.x * kHpTile;
   const int ksl = (H + kHpSplit - 1) / kHpSplit;
   const int kbeg = blockIdx.z * ksl, kend = min(H, kbeg + ksl);
   Hp += (size_t)blockIdx.z * M * N;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  float acc[4][4] = {};
-  constexpr int kPer = (kHpTile * kHpK) / 256;
-  // the next K step's operands are loaded into registers while this one computes
+  float acc[8][8] = {};
+  constexpr int kPer = (kHpTile * kHpK) / 256;  // 8 elements of each operand per thread
   float ra[kPer], rw[kPer];
   auto gload = [&](int k0) {
 #pragma unroll
@@ -93,27 +92,27 @@ __global__ void __launch_bounds__(256)
     }
     __syncthreads();
     if (k0 + kHpK < kend) gload(k0 + kHpK);
-#pragma unroll 8
+#pragma unroll
     for (int kk = 0; kk < kHpK; ++kk) {
-      float a[4], b[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = As[kk][ty * 4 + i];
-        b[i] = Bs[kk][tx * 4 + i];
-      }
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j2 = 0; j2 < 8; ++j2) acc[i][j2] = fmaf(a[i], b[j2], acc[i][j2]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
-      if (m < M && n < N) Hp[(size_t)m * N + n] = acc[i][j];
+    for (int j2 = 0; j2 < 8; ++j2) {
+      const int m = m0 + (i >> 2) * 64 + ty * 4 + (i & 3), n = n0 + (j2 >> 2) * 64 + tx * 4 + (j2 & 3);
+      if (m < M && n < N) Hp[(size_t)m * N + n] = acc[i][j2];
     }
 }
 
@@ -187,7 +186,10 @@ __global__ void __launch_bounds__(kCellThreads)
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
         const float* hp = Hp + row * 3 * r + q * r + j;
-        hq[q] = ((hp[0] + hp[slice]) + hp[2 * slice]) + hp[3 * slice];
+        float t = hp[0];
+#pragma unroll
+        for (int sl = 1; sl < kHpSplit; ++sl) t += hp[sl * slice];
+        hq[q] = t;
       }
       const float gk = 1.f / (1.f + expf(-(pre[0][jj][rb] + hq[0])));
       S_out[(size_t)b * r + j] = gk * zin[rb * r2 + j] + (1.f - gk) * tanhf(pre[1][jj][rb] + hq[1]);
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kCellThreads)
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Scratch: Hp [4][B*gamma][3r] fp32 (the h projection's K slices), then the
+// Scratch: Hp [10][B*gamma][3r] fp32 (the h projection's K slices), then the
 // state S [2][B][r] fp32 (two buffers alternating by step parity; 256-byte
 // aligned).
 size_t hp_bytes(const dspark_dims& d) {
