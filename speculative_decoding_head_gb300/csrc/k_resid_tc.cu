@@ -23,6 +23,20 @@
 // Persistent, one CTA per SM over 128-wide vocabulary tiles; W2 is read with
 // the L2 evict_last policy (the draft kept it there), in K-halves through a
 // three-stage ring; U and P with plain bulk copies. Every wait is bounded.
+//
+// The same vocabulary pass serves three other computations (template MODE),
+// each with every position or request as an MMA column:
+//   - the draft head's teacher-forced training objective (eqs. (9)-(12) of the
+//     deepseek.csdn.net reading, §6): pass kModeLossStats keeps per thread a
+//     running (max, sum 2^(y - max)) of z_d and of z_t per column and reduces
+//     it once per column group; pass kModeLossL1 sums |p_d - p_t|. A group's
+//     U and P rows are consecutive, so they arrive as two TMA boxes; the tiles
+//     are walked in alternating directions per group so that W2 is reused
+//     from L2;
+//   - one draft step of the RNN head (eq. (6), same reading §4.2),
+//     kModeDraft: z = U_k + o_k W2 with o_k split into bf16 hi and lo
+//     operands that both accumulate into the tile, and the log-mass of every
+//     64-token block for the SIMT pick.
 #include <cudaTypedefs.h>
 #include <string.h>
 
