@@ -71,6 +71,8 @@ def lib():
             l.orc_logsumexp.argtypes = [P, C.c_long]
             l.orc_logsumexp.restype = dbl
             l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P]
+            l.orc_verify_head.argtypes = [P, P, P, P, P, P, P, P, P, P, u64, u64, P, i32,
+                                          P, P, P, P, P]
             l.orc_rnn_draft.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P]
             l.orc_plan_sync.argtypes = [i32, i32, P, P, P, P]
             l.orc_plan_sync.restype = i32
@@ -351,8 +353,10 @@ def plan_lagged(conf_now, conf_lagged, sps):
 
 
 def verify(P_packed, row_off, lengths, anchor, tokens, U, W1, W2, seed: int, rnd: int,
-           reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
-    """Lossless ragged verify. Returns n_acc, next_anchor, margins, resid flag."""
+           reqs: Optional[Sequence[int]] = None, ovec=None) -> Dict[str, np.ndarray]:
+    """Lossless ragged verify. Returns n_acc, next_anchor, margins, resid flag.
+    ``ovec`` [B, gamma, r]: the RNN head's vectors o_k (p_d from U + o W2)
+    instead of the Markov head's W1[x_{k-1}]."""
     P = _c(P_packed, np.float32)
     U = _c(U, np.float32)
     B, g, V = U.shape
@@ -368,10 +372,13 @@ def verify(P_packed, row_off, lengths, anchor, tokens, U, W1, W2, seed: int, rnd
     out = {"n_acc": np.full(B, -1, np.int32), "next_anchor": np.full(B, -1, np.int32),
            "acc_margin": np.full(B, np.inf), "smp_margin": np.full(B, np.inf),
            "resid": np.zeros(B, np.int32)}
-    lib().orc_verify(C.byref(d), _p(P), _p(ro), _p(L), _p(anchor), _p(tokens), _p(U),
-                     _p(w1), _p(w2), seed, rnd, _p(rq), rq.size, _p(out["n_acc"]),
-                     _p(out["next_anchor"]), _p(out["acc_margin"]), _p(out["smp_margin"]),
-                     _p(out["resid"]))
+    ov = None if ovec is None else _c(ovec, np.float64)
+    if ov is not None and ov.shape != (B, g, r):
+        raise ValueError(f"ovec must be [{B}, {g}, {r}], got {ov.shape}")
+    lib().orc_verify_head(C.byref(d), _p(P), _p(ro), _p(L), _p(anchor), _p(tokens), _p(U),
+                          _p(w1), _p(w2), None if ov is None else _p(ov), seed, rnd, _p(rq), rq.size,
+                          _p(out["n_acc"]), _p(out["next_anchor"]), _p(out["acc_margin"]),
+                          _p(out["smp_margin"]), _p(out["resid"]))
     return out
 
 

@@ -270,6 +270,17 @@ static void markov_logits(const orc_dims* d, const float* Urow, const void* W1,
     for (long v = 0; v < V; ++v) z[v] += (double)Urow[v];
 }
 
+/* z_v = U_k(v) + sum_i o_i W2[i, v]: the draft logits of a head whose bias is
+ * an r-vector o times W2 (the RNN head's o_k, eq. (6)), fp64 */
+static void head_logits(const orc_dims* d, const float* Urow, const void* W2, const double* o, double* z)
+{
+    long V = d->V, r = d->r;
+    for (long v = 0; v < V; ++v) z[v] = 0.0;
+    for (long i = 0; i < r; ++i)
+        for (long v = 0; v < V; ++v) z[v] += o[i] * wget(W2, d->w_bf16, i, V, v);
+    for (long v = 0; v < V; ++v) z[v] += (double)Urow[v];
+}
+
 /*
  * For each request b in reqs[0..n_req): draft x_1..x_gamma.
  * Outputs (indexed [b][k-1], full-size arrays, only listed rows written):
@@ -315,7 +326,8 @@ void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2
 /* the paper also tried); [ailearn] "RNN 头（可选）"; [csdn] §4.2,       */
 /* eq. (6)). A gated recurrent state s_k in R^r summarises the block's  */
 /* prefix: with z_k = [s_{k-1}; W1[x_{k-1}]; h_k] (length 2r + H),       */
-/*   g_k = sigma(W_g z_k),  s_k = g_k * s_{k-1} + (1 - g_k) * tanh(W_c z_k),
+/*   g_k = sigma(W_g z_k),                                              */
+/*   s_k = g_k * s_{k-1} + (1 - g_k) * tanh(W_c z_k),                   */
 /*   o_k = tanh(W_o z_k),   z = U_k + o_k W2  (the bias B_k = W2^T o_k), */
 /* s_0 = 0, x_0 = the anchor; W_g, W_c, W_o are [r][2r + H] (no bias,   */
 /* as the equation shows none), stored one after the other in Wr in the */
@@ -362,10 +374,7 @@ void orc_rnn_draft(const orc_dims* d, const float* U, const void* W1, const void
             for (long i = 0; i < r; ++i) s += (double)w[H + i] * zin[r + i];
             conf[o] = 1.0 / (1.0 + exp(-s / (double)T[k - 1]));
             /* z = U_k + o_k W2 */
-            for (long v = 0; v < V; ++v) z[v] = 0.0;
-            for (long i = 0; i < r; ++i)
-                for (long v = 0; v < V; ++v) z[v] += ov[i] * wget(W2, d->w_bf16, i, V, v);
-            for (long v = 0; v < V; ++v) z[v] += (double)U[o * V + v];
+            head_logits(d, U + o * V, W2, ov, z);
             const double L = orc_logsumexp(z, V);
             double m = 0.0;
             const int x = sample_two_level_icdf(z, V, seed, round, ORC_P_DRAFT_BLOCK,
@@ -516,18 +525,20 @@ void orc_plan_topk(int B, int g, const float* conf, int K, int32_t* lengths, dou
  * For each request b in reqs: rows P + row_off[b] .. + lengths[b]-1 of the
  * packed target logits (row j = target distribution after x_j, x_0 = anchor).
  * Draft tokens tokens[b][0..g) are x_1..x_g. The draft distribution p_d at
- * position j+1 is recomputed here in fp64 from (U, W1, W2, x_j).
+ * position j+1 is recomputed here in fp64 from (U, W1, W2, x_j) for the
+ * Markov head, or from (U, ovec[b][j], W2) for the RNN head (ovec non-NULL:
+ * the head vectors o_{j+1} of the draft).
  * Outputs: n_acc[b] (leading accepted drafts), next_anchor[b],
  *   acc_margin[b] = min |u - p_t/p_d| over the tests taken,
  *   smp_margin[b] = key-gap margin of the final draw (residual or bonus),
  *   resid[b] = 1 if the next anchor came from the residual distribution.
  */
-void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
-                const int32_t* lengths, const int32_t* anchor, const int32_t* tokens,
-                const float* U, const void* W1, const void* W2,
-                uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
-                int32_t* n_acc, int32_t* next_anchor, double* acc_margin,
-                double* smp_margin, int32_t* resid)
+void orc_verify_head(const orc_dims* d, const float* P, const int32_t* row_off,
+                     const int32_t* lengths, const int32_t* anchor, const int32_t* tokens,
+                     const float* U, const void* W1, const void* W2, const double* ovec,
+                     uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                     int32_t* n_acc, int32_t* next_anchor, double* acc_margin,
+                     double* smp_margin, int32_t* resid)
 {
     const long V = d->V, g = d->gamma;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -548,7 +559,10 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
             for (long v = 0; v < V; ++v) lt[v] -= Lt;
             const int x_prev = j == 0 ? anchor[b] : tokens[b * g + (j - 1)];
             const int x = tokens[b * g + j];
-            markov_logits(d, U + (b * g + j) * V, W1, W2, x_prev, z);
+            if (ovec)
+                head_logits(d, U + (b * g + j) * V, W2, ovec + (b * g + j) * d->r, z);
+            else
+                markov_logits(d, U + (b * g + j) * V, W1, W2, x_prev, z);
             double Ld = orc_logsumexp(z, V);
             double pt = exp(lt[x]), pd = exp(z[x] - Ld);
             double u = orc_uniform(seed, round, ORC_P_ACCEPT, (uint32_t)b, (uint32_t)j, 0u);
@@ -597,6 +611,17 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
         resid[b] = from_resid;
         free(lt); free(z); free(lw); free(tol); free(tm);
     }
+}
+
+void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
+                const int32_t* lengths, const int32_t* anchor, const int32_t* tokens,
+                const float* U, const void* W1, const void* W2,
+                uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                int32_t* n_acc, int32_t* next_anchor, double* acc_margin,
+                double* smp_margin, int32_t* resid)
+{
+    orc_verify_head(d, P, row_off, lengths, anchor, tokens, U, W1, W2, NULL, seed, round, reqs, n_req,
+                    n_acc, next_anchor, acc_margin, smp_margin, resid);
 }
 
 /* ------------------------------------------------------------------ */

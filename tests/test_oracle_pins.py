@@ -838,3 +838,27 @@ def test_rnn_head_is_non_anticipating_and_carries_the_prefix():
     o4 = oracle.rnn_draft(U3, a["W1"], a["W2"], Wr, an2, a["h"], a["w"], a["T"], 7, 3)
     assert np.all(o3["tokens"][:, 0] == 7) and np.all(o4["tokens"][:, 0] == 7)
     assert not np.allclose(o3["ovec"][:, 1], o4["ovec"][:, 1])
+
+
+def test_verify_with_head_vectors_equal_to_w1_rows_is_the_markov_verify():
+    """p_d recomputed from o = W1[x_{j}] rows (the Markov head's own bias
+    vectors) gives the Markov verify exactly; other vectors change p_d."""
+    rng = np.random.default_rng(71)
+    B, g, V, r = 4, 3, 120, 6
+    U = rng.normal(0.0, 1.0, (B, g, V)).astype(np.float32)
+    W1 = rng.normal(0.0, 0.8, (V, r)).astype(np.float32)
+    W2 = rng.normal(0.0, 0.8, (r, V)).astype(np.float32)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    tokens = rng.integers(0, V, (B, g)).astype(np.int32)
+    L = np.full(B, g + 1, np.int32)
+    ro = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    P = rng.normal(0.0, 1.0, (int(L.sum()), V)).astype(np.float32)
+    prev = np.concatenate([anchor[:, None], tokens[:, :-1]], axis=1)
+    ovec = W1.astype(np.float64)[prev]
+    m = oracle.verify(P, ro, L, anchor, tokens, U, W1, W2, 5, 1)
+    o = oracle.verify(P, ro, L, anchor, tokens, U, W1, W2, 5, 1, ovec=ovec)
+    for k in ("n_acc", "next_anchor", "resid"):
+        assert np.array_equal(m[k], o[k]), k
+    assert np.array_equal(m["acc_margin"], o["acc_margin"])
+    o2 = oracle.verify(P, ro, L, anchor, tokens, U, W1, W2, 5, 1, ovec=ovec * 3.0)
+    assert not np.array_equal(m["acc_margin"], o2["acc_margin"])
