@@ -24,7 +24,7 @@ SYMBOLS = [
     "dspark_status_string", "dspark_last_launch_count", "dspark_path",
     "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
     "dspark_sts_fit", "dspark_sts_scratch_bytes", "dspark_train_loss", "dspark_train_loss_scratch_bytes",
-    "dspark_rnn_draft", "dspark_rnn_draft_scratch_bytes",
+    "dspark_rnn_draft", "dspark_rnn_draft_scratch_bytes", "dspark_verify_rnn",
 ]
 
 
@@ -89,6 +89,8 @@ def load() -> C.CDLL:
         lib.dspark_train_loss_scratch_bytes.restype = C.c_size_t
         lib.dspark_rnn_draft.argtypes = [P] * 9 + [u64, u64] + [P] * 7
         lib.dspark_rnn_draft.restype = i32
+        lib.dspark_verify_rnn.argtypes = [P] * 11 + [u64, u64] + [P] * 3
+        lib.dspark_verify_rnn.restype = i32
         lib.dspark_rnn_draft_scratch_bytes.argtypes = [P]
         lib.dspark_rnn_draft_scratch_bytes.restype = C.c_size_t
         _lib = lib
@@ -267,6 +269,21 @@ class Workspace:
             _ptr(out["lse"], f32, "lse"), _ptr(out["conf"], f32, "conf"), _ptr(out["ovec"], f32, "ovec"),
             _ptr(out["scratch"], None, "scratch"), _stream(stream))
         _check(code, "dspark_rnn_draft")
+        return out
+
+    def verify_rnn(self, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, ovec, W2, seed: int, rnd: int,
+                   out=None, stream=None):
+        """Verify of RNN-head drafts (``dspark_verify_rnn``): p_d of a rejected
+        position from U + o W2 with ovec [B, gamma, r] fp32."""
+        out = out or self.new_verify_outputs(P.device)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_verify_rnn(
+            self._h, _ptr(P, f32, "P"), _ptr(row_off, i32, "row_off"), _ptr(lengths, i32, "lengths"),
+            _ptr(anchor, i32, "anchor"), _ptr(tokens, i32, "tokens"), _ptr(pd_tok, f32, "pd_tok"),
+            _ptr(lse, f32, "lse"), _ptr(U, f32, "U"), _ptr(ovec, f32, "ovec"), _ptr(W2, self.wdtype, "W2"),
+            int(seed), int(rnd), _ptr(out["n_acc"], i32, "n_acc"), _ptr(out["next_anchor"], i32, "next_anchor"),
+            _stream(stream))
+        _check(code, "dspark_verify_rnn")
         return out
 
     def new_loss_outputs(self, device="cuda") -> Dict[str, torch.Tensor]:

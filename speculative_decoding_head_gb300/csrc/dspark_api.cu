@@ -241,7 +241,25 @@ dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_of
       !aligned16(pd_tok) || !aligned16(lse) || !aligned16(U) || !aligned16(W1) || !aligned16(W2) ||
       !aligned16(n_accepted) || !aligned16(next_anchor))
     return DSPARK_EINVAL;
-  VerifyArgs a{P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted, next_anchor};
+  VerifyArgs a{P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted, next_anchor,
+               nullptr};
+  int launches = 0;
+  cudaError_t e = launch_verify(ws, a, reinterpret_cast<cudaStream_t>(stream), &launches);
+  ws->last_launches = launches;
+  return cuda_fail(e);
+}
+
+dspark_status dspark_verify_rnn(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
+                                const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
+                                const float* U, const float* ovec, const void* W2, uint64_t seed, uint64_t round,
+                                int32_t* n_accepted, int32_t* next_anchor, dspark_stream_t stream) {
+  if (!ws) return DSPARK_EINVAL;
+  if (!aligned16(P) || !aligned16(row_off) || !aligned16(lengths) || !aligned16(anchor) || !aligned16(tokens) ||
+      !aligned16(pd_tok) || !aligned16(lse) || !aligned16(U) || !aligned16(ovec) || !aligned16(W2) ||
+      !aligned16(n_accepted) || !aligned16(next_anchor))
+    return DSPARK_EINVAL;
+  VerifyArgs a{P, row_off, lengths, anchor, tokens, pd_tok, lse, U, nullptr, W2, seed, round, n_accepted,
+               next_anchor, ovec};
   int launches = 0;
   cudaError_t e = launch_verify(ws, a, reinterpret_cast<cudaStream_t>(stream), &launches);
   ws->last_launches = launches;

@@ -41,6 +41,7 @@ struct VerifyArgs {
   uint64_t seed, round;
   int32_t* n_acc;
   int32_t* next_anchor;
+  const float* ovec;  // [B][gamma][r] the RNN head's o_k (p_d from U + o W2), or null (Markov head)
 };
 
 // The draft head's teacher-forced training objective: inputs, outputs and the

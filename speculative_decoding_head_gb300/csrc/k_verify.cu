@@ -534,9 +534,9 @@ __global__ void __launch_bounds__(256)
                    const void* __restrict__ W2, const int32_t* __restrict__ anchor,
                    const int32_t* __restrict__ tokens, const float* __restrict__ lse, int g, int V, int r,
                    int nblk, const int* __restrict__ vflag, const int32_t* __restrict__ n_acc,
-                   const int* __restrict__ vrow, const float* __restrict__ vlset, Rng rng,
-                   float2* __restrict__ rpart, const int* __restrict__ status) {
-  extern __shared__ float e[];  // W1[x_n], [r]
+                   const int* __restrict__ vrow, const float* __restrict__ vlset, const float* __restrict__ ovec,
+                   Rng rng, float2* __restrict__ rpart, const int* __restrict__ status) {
+  extern __shared__ float e[];  // W1[x_n] (Markov head) or o_{n+1} (RNN head), [r]
   __shared__ KeyIdx red_k[8];
   const int b = blockIdx.y, c = blockIdx.x;
   // this round's flags only if every stage so far left the status clear (no
@@ -544,7 +544,8 @@ __global__ void __launch_bounds__(256)
   if (!vflag[b] || *(volatile const int*)status != 0) return;
   const int n = min(max(n_acc[b], 0), g - 1);
   const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
-  for (int i = threadIdx.x; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+  for (int i = threadIdx.x; i < r; i += blockDim.x)
+    e[i] = ovec ? ovec[((size_t)b * g + n) * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
   __syncthreads();
   const float Ld = lse[(size_t)b * g + n];  // draft position n + 1
   const float Lt = vlset[b];
@@ -587,8 +588,8 @@ __global__ void __launch_bounds__(kPickThreads)
                  const void* __restrict__ W2, const int32_t* __restrict__ anchor,
                  const int32_t* __restrict__ tokens, const float* __restrict__ lse, int g, int V, int r,
                  int nblk, int nchunk, const int* __restrict__ vflag, const int32_t* __restrict__ n_acc,
-                 const int* __restrict__ vrow, const float* __restrict__ vlset, Rng rng,
-                 const float2* __restrict__ rpart, int32_t* __restrict__ next_anchor,
+                 const int* __restrict__ vrow, const float* __restrict__ vlset, const float* __restrict__ ovec,
+                 Rng rng, const float2* __restrict__ rpart, int32_t* __restrict__ next_anchor,
                  const int* __restrict__ status) {
   extern __shared__ float e[];  // [r]
   __shared__ KeyIdx red_k[kPickThreads / 32];
@@ -605,7 +606,8 @@ __global__ void __launch_bounds__(kPickThreads)
   // its load overlaps the reduction of the block keys
   {
     const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
-    for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
+    for (int i = tid; i < r; i += blockDim.x)
+      e[i] = ovec ? ovec[((size_t)b * g + n) * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
   }
   if (warp == 0) {
     KeyIdx k2 = key_none();
@@ -712,7 +714,7 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   }
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
-  if (BF16 && ws->use_tc && geo.resid_tc_ok) {
+  if (BF16 && ws->use_tc && geo.resid_tc_ok && !a.ovec) {
     // residual block draw on tensor cores: one CTA per SM
     nchunk = geo.num_sms;
     cudaError_t e = launch_resid_tc(ws, a, ws->s.rpart, nchunk, st);
@@ -720,11 +722,11 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   } else {
     k_resid_blocks<BF16><<<dim3(kResidChunks, d.B), 256, smem, st>>>(
         a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
-        ws->s.vrow, ws->s.vlset, rng, ws->s.rpart, ws->s.status);
+        ws->s.vrow, ws->s.vlset, a.ovec, rng, ws->s.rpart, ws->s.status);
   }
   k_resid_pick<BF16><<<d.B, kPickThreads, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
                                              d.r, geo.nblk, nchunk, ws->s.vflag, a.n_acc, ws->s.vrow,
-                                             ws->s.vlset, rng, ws->s.rpart, a.next_anchor, ws->s.status);
+                                             ws->s.vlset, a.ovec, rng, ws->s.rpart, a.next_anchor, ws->s.status);
   *launches += 4;
   return cudaGetLastError();
 }

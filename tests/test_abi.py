@@ -104,3 +104,8 @@ def test_rnn_draft_arguments_are_checked_on_the_host(lib):
     fake = ctypes.c_void_p(256)
     assert lib.dspark_rnn_draft(None, *([fake] * 8), 0, 0, *([fake] * 6), None) == 1
     assert lib.dspark_rnn_draft_scratch_bytes(None) == 0
+
+
+def test_rnn_verify_arguments_are_checked_on_the_host(lib):
+    fake = ctypes.c_void_p(256)
+    assert lib.dspark_verify_rnn(None, *([fake] * 10), 0, 0, fake, fake, None) == 1

@@ -87,3 +87,59 @@ def test_rnn_head_differs_from_markov_head():
     npi = np_inputs(inp)
     m = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed, 0)
     assert not np.allclose(m["lse"], o["lse"])
+
+
+def test_rnn_verify_stagewise_on_oracle_drafts():
+    """Both sides verify the oracle's RNN-head drafts: p_d of a rejected
+    position from U + o W2 (the oracle's o_k, rounded to fp32 for the GPU),
+    under several length patterns; most requests take a residual draw."""
+    from parity import Tally, compare_verify, pack_np, row_off_np
+    wl = _wl("rnn_verify", 24, 4, 4104, 64, 96, seed=43)
+    inp = make_inputs(wl)
+    inp["Wr"] = make_rnn_weights(wl)
+    dev, npi = to_device(inp), np_inputs(inp)
+    od = oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
+                          6, 4)
+    ws = Workspace.for_workload(wl)
+    rng = np.random.default_rng(8)
+    tally = Tally()
+    resid = 0
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).astype(np.float32)).cuda()
+    for trial in range(3):
+        L = rng.integers(1, wl.gamma + 2, wl.B).astype(np.int32)
+        ro = row_off_np(L)
+        P = pack_np(npi["P_full"], L)
+        out = ws.verify_rnn(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(L).cuda(),
+                            dev["anchor"], torch.from_numpy(od["tokens"]).cuda(), f32(od["pd_tok"]), f32(od["lse"]),
+                            dev["U"], f32(od["ovec"]), dev["W2"], 6, 10 + trial)
+        torch.cuda.synchronize()
+        assert ws.device_status() == 0
+        ov = oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], 6, 10 + trial,
+                           ovec=od["ovec"])
+        tally = tally.add(compare_verify(gpu_np(out), ov, range(wl.B)))
+        resid += int(ov["resid"].sum())
+        assert (out["n_acc"].cpu().numpy() <= L - 1).all()
+    tally.check_rate()
+    assert tally.compared > 0 and resid > 0
+
+
+def test_rnn_round_on_the_gpu_is_consistent():
+    """The GPU's own RNN drafts through the planner and the RNN verify."""
+    wl = _wl("rnn_round", 16, 5, 4096, 64, 32, seed=45).with_(mode="compact", sps_knee=32.0)
+    inp = make_inputs(wl)
+    Wr = make_rnn_weights(wl).cuda()
+    dev = to_device(inp)
+    ws = Workspace.for_workload(wl)
+    d = ws.rnn_draft(dev["U"], dev["W1"], dev["W2"], Wr, dev["anchor"], dev["h"], dev["w"], dev["T"], 2, 0)
+    p = ws.plan(d["conf"], dev["sps"])
+    from speculative_decoding_head_gb300.workloads import pack_rows
+    P = pack_rows(dev["P_full"], p["lengths"])
+    v = ws.verify_rnn(P, p["row_off"], p["lengths"], dev["anchor"], d["tokens"], d["pd_tok"], d["lse"], dev["U"],
+                      d["ovec"], dev["W2"], 2, 0)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    L = p["lengths"].cpu().numpy()
+    n = v["n_acc"].cpu().numpy()
+    assert ((n >= 0) & (n <= L - 1)).all()
+    na = v["next_anchor"].cpu().numpy()
+    assert ((na >= 0) & (na < wl.V)).all()
