@@ -67,7 +67,10 @@ enum {
     ORC_P_BONUS_BLOCK = 4,
     ORC_P_BONUS_TOKEN = 5,
     ORC_P_RESID_BLOCK = 6,
-    ORC_P_RESID_TOKEN = 7
+    ORC_P_RESID_TOKEN = 7,
+    ORC_P_TREE_ACCEPT = 8,
+    ORC_P_TREE_BLOCK = 9,
+    ORC_P_TREE_TOKEN = 10
 };
 
 /* ------------------------------------------------------------------ */
@@ -622,6 +625,173 @@ void orc_verify(const orc_dims* d, const float* P, const int32_t* row_off,
 {
     orc_verify_head(d, P, row_off, lengths, anchor, tokens, U, W1, W2, NULL, seed, round, reqs, n_req,
                     n_acc, next_anchor, acc_margin, smp_margin, resid);
+}
+
+/* ------------------------------------------------------------------ */
+/* PCTree: the chain made a tree ([V4.1 blog] "后续工作": the Markov     */
+/* head already scores every child token under a parent token, so it   */
+/* picks candidate children per parent node, and the most probable     */
+/* paths are kept within a fixed verify budget; no retraining, no extra */
+/* backbone pass). The pages only summarise it; the steps below are the */
+/* plainest reading:                                                   */
+/*  build: node 0 is the anchor (depth 0, log-probability 0). A node x  */
+/*   at depth k < gamma proposes its c most probable children under    */
+/*   p_d(. | x) = softmax(U_{k+1} + W1[x] W2) (U of the position, shared */
+/*   by every node of that depth: no extra backbone pass), each with    */
+/*   the path log-probability of its parent plus log p_d(child). Nodes  */
+/*   are admitted best first (highest path log-probability; ties to the */
+/*   smaller depth, parent index, token) until N nodes besides the root */
+/*   are in: the N most probable paths' nodes. Children are kept in     */
+/*   admission order, so siblings come in decreasing probability.       */
+/*  verify (lossless): at a node with target p = softmax(P[node]), the  */
+/*   children are tried in order; child i is accepted with the current  */
+/*   (renormalised) p of its token, u < p(t_i) with u = uniform(purpose */
+/*   8, b, node, i); a rejected child's token is removed from p and p is */
+/*   renormalised. An accepted child becomes the node. When no child is */
+/*   accepted (or there is none), the next anchor is drawn from p (the   */
+/*   target with the rejected tokens removed) by the two-level sampler  */
+/*   (purposes 9, 10; j = node). Each emitted token is then an exact    */
+/*   draw from the target given its prefix.                             */
+/* ------------------------------------------------------------------ */
+typedef struct { double lp; int depth, parent, token; } orc_tcand;
+
+/* a better than b: higher log-probability, then smaller depth, parent, token */
+static int tcand_better(const orc_tcand* a, const orc_tcand* b)
+{
+    if (a->lp != b->lp) return a->lp > b->lp;
+    if (a->depth != b->depth) return a->depth < b->depth;
+    if (a->parent != b->parent) return a->parent < b->parent;
+    return a->token < b->token;
+}
+
+/*
+ * Per request b: tok, par, dep [b][N+1] (node 0 the root; -1 past the last
+ * node), lp [b][N+1] the path log-probabilities; n_nodes[b] the nodes besides
+ * the root (< N only when every path reaches depth gamma); margin[b] = the
+ * smallest log-probability gap that decided an admission or a top-c choice.
+ */
+void orc_pctree_build(const orc_dims* d, const float* U, const void* W1, const void* W2,
+                      const int32_t* anchor, int c, int N, int32_t* tok, int32_t* par, int32_t* dep,
+                      double* lp, int32_t* n_nodes, double* margin)
+{
+    const long V = d->V, g = d->gamma;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < d->B; ++b) {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        orc_tcand* fr = (orc_tcand*)malloc(sizeof(orc_tcand) * (size_t)(N + 1) * (size_t)(c > 0 ? c : 1));
+        int nf = 0;
+        double mg = INFINITY;
+        int32_t* tk = tok + (long)b * (N + 1);
+        int32_t* pa = par + (long)b * (N + 1);
+        int32_t* de = dep + (long)b * (N + 1);
+        double* l = lp + (long)b * (N + 1);
+        for (int i = 0; i <= N; ++i) { tk[i] = -1; pa[i] = -1; de[i] = -1; l[i] = -INFINITY; }
+        tk[0] = anchor[b]; de[0] = 0; l[0] = 0.0;
+        int n = 0, last = 0;
+        for (;;) {
+            /* expand the node just admitted */
+            if (de[last] < g && c > 0) {
+                markov_logits(d, U + ((long)b * g + de[last]) * V, W1, W2, tk[last], z);
+                const double L = orc_logsumexp(z, V);
+                for (int t = 0; t < c && t < V; ++t) {
+                    long best = -1;
+                    for (long v = 0; v < V; ++v) {
+                        if (z[v] == -INFINITY) continue;
+                        if (best < 0 || z[v] > z[best]) best = v;
+                    }
+                    if (best < 0) break;
+                    fr[nf].lp = l[last] + (z[best] - L);
+                    fr[nf].depth = de[last] + 1;
+                    fr[nf].parent = last;
+                    fr[nf].token = (int)best;
+                    ++nf;
+                    z[best] = -INFINITY;
+                    /* the gap to the next child decided this top-c choice */
+                    if (t == c - 1) {
+                        double nxt = -INFINITY;
+                        for (long v = 0; v < V; ++v) if (z[v] > nxt) nxt = z[v];
+                        if (nxt > -INFINITY) {
+                            const double gap = (fr[nf - 1].lp - l[last]) - (nxt - L);
+                            if (gap < mg) mg = gap;
+                        }
+                    }
+                }
+            }
+            if (n == N || nf == 0) break;
+            /* admit the best frontier candidate */
+            int bi = 0;
+            for (int i = 1; i < nf; ++i) if (tcand_better(&fr[i], &fr[bi])) bi = i;
+            for (int i = 0; i < nf; ++i)
+                if (i != bi && fr[bi].lp - fr[i].lp < mg) mg = fr[bi].lp - fr[i].lp;
+            ++n;
+            tk[n] = fr[bi].token; pa[n] = fr[bi].parent; de[n] = fr[bi].depth; l[n] = fr[bi].lp;
+            last = n;
+            fr[bi] = fr[nf - 1];
+            --nf;
+        }
+        n_nodes[b] = n;
+        margin[b] = mg;
+        free(z); free(fr);
+    }
+}
+
+/*
+ * P holds [B][N+1][V] target logits, row i the target's distribution of the
+ * token after node i's path. Outputs: path [b][gamma+1] the accepted nodes
+ * (root first, -1 after the last), n_acc[b] the accepted draft tokens,
+ * next_anchor[b], margin[b] = min |u - p| over the tests taken and the final
+ * draw's key margin.
+ */
+void orc_pctree_verify(const orc_dims* d, int N, const int32_t* tok, const int32_t* par, const float* P,
+                       uint64_t seed, uint64_t round, int32_t* path, int32_t* n_acc, int32_t* next_anchor,
+                       double* margin)
+{
+    const long V = d->V, g = d->gamma;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int b = 0; b < d->B; ++b) {
+        double* lt = (double*)malloc(sizeof(double) * (size_t)V);
+        double* pr = (double*)malloc(sizeof(double) * (size_t)V);
+        const int32_t* tk = tok + (long)b * (N + 1);
+        const int32_t* pa = par + (long)b * (N + 1);
+        int32_t* ph = path + (long)b * (g + 1);
+        for (long i = 0; i <= g; ++i) ph[i] = -1;
+        int node = 0, n = 0;
+        double mg = INFINITY;
+        ph[0] = 0;
+        for (;;) {
+            const float* row = P + ((long)b * (N + 1) + node) * V;
+            for (long v = 0; v < V; ++v) lt[v] = (double)row[v];
+            const double L = orc_logsumexp(lt, V);
+            for (long v = 0; v < V; ++v) pr[v] = exp(lt[v] - L);
+            int next = -1, i = 0;
+            for (int ch = node + 1; ch <= N && tk[ch] >= 0; ++ch) {
+                if (pa[ch] != node) continue;
+                const double q = pr[tk[ch]];
+                const double u = orc_uniform(seed, round, ORC_P_TREE_ACCEPT, (uint32_t)b, (uint32_t)node,
+                                             (uint32_t)i);
+                if (fabs(u - q) < mg) mg = fabs(u - q);
+                ++i;
+                if (u < q) { next = ch; break; }
+                pr[tk[ch]] = 0.0;                        /* removed, the rest renormalised */
+                const double keep = 1.0 - q;
+                for (long v = 0; v < V; ++v) pr[v] /= keep;
+            }
+            if (next >= 0) {
+                node = next;
+                ph[++n] = node;
+                continue;
+            }
+            for (long v = 0; v < V; ++v) lt[v] = pr[v] > 0.0 ? log(pr[v]) : -INFINITY;
+            double sm = INFINITY;
+            next_anchor[b] = sample_two_level(lt, NULL, NULL, V, seed, round, ORC_P_TREE_BLOCK,
+                                              ORC_P_TREE_TOKEN, (uint32_t)b, (uint32_t)node, &sm);
+            if (sm < mg) mg = sm;
+            break;
+        }
+        n_acc[b] = n;
+        margin[b] = mg;
+        free(lt); free(pr);
+    }
 }
 
 /* ------------------------------------------------------------------ */

@@ -862,3 +862,127 @@ def test_verify_with_head_vectors_equal_to_w1_rows_is_the_markov_verify():
     assert np.array_equal(m["acc_margin"], o["acc_margin"])
     o2 = oracle.verify(P, ro, L, anchor, tokens, U, W1, W2, 5, 1, ovec=ovec * 3.0)
     assert not np.array_equal(m["acc_margin"], o2["acc_margin"])
+
+
+# ---------------------------------------------------------------- PCTree (tree draft + tree verify)
+def _tree_inputs(seed, B=1, g=3, V=30, r=4):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(0.0, 1.5, (B, g, V)).astype(np.float32), rng.normal(0.0, 0.7, (V, r)).astype(np.float32),
+            rng.normal(0.0, 0.7, (r, V)).astype(np.float32), rng.integers(0, V, B).astype(np.int32))
+
+
+def test_pctree_build_keeps_the_n_most_probable_paths():
+    """Brute force over the full c-ary tree of depth gamma (children scored by
+    a numpy softmax of U_k + W1[x] W2): the built nodes are the N with the
+    highest path probability, each after its parent, siblings in decreasing
+    probability."""
+    U, W1, W2, anchor = _tree_inputs(1)
+    g, c, N = U.shape[1], 2, 6
+    t = oracle.pctree_build(U, W1, W2, anchor, c, N)
+    assert t["n_nodes"][0] == N and t["margin"][0] > 1e-9
+
+    def children(x, k):
+        z = U[0, k].astype(np.float64) + W1[x].astype(np.float64) @ W2.astype(np.float64)
+        lp = z - special.logsumexp(z)
+        top = np.argsort(-lp, kind="stable")[:c]
+        return [(int(v), float(lp[v])) for v in top]
+
+    allnodes = []                      # (path log-prob, token path)
+    frontier = [((int(anchor[0]),), 0.0)]
+    for k in range(g):
+        nxt = []
+        for path, lp in frontier:
+            for v, l in children(path[-1], k):
+                nxt.append((path + (v,), lp + l))
+        allnodes += nxt
+        frontier = nxt
+    best = sorted(allnodes, key=lambda e: -e[1])[:N]
+    tok, par, lp = t["tok"][0], t["par"][0], t["lp"][0]
+
+    def path_of(i):
+        p = []
+        while i >= 0:
+            p.append(int(tok[i]))
+            i = par[i]
+        return tuple(reversed(p))
+
+    built = sorted(((path_of(i), lp[i]) for i in range(1, N + 1)), key=lambda e: -e[1])
+    assert [p for p, _ in built] == [p for p, _ in best]
+    assert np.allclose([l for _, l in built], [l for _, l in best], rtol=0, atol=1e-12)
+    for i in range(1, N + 1):
+        assert par[i] < i
+        sib = [j for j in range(1, N + 1) if par[j] == par[i]]
+        assert all(lp[a] >= lp[b] for a, b in zip(sib, sib[1:]))
+
+
+def _tree_mc(seed, reps=20000, V=12, c=3, N=7, g=3):
+    U, W1, W2, anchor = _tree_inputs(seed, B=1, g=g, V=V)
+    t = oracle.pctree_build(U, W1, W2, anchor, c, N)
+    rng = np.random.default_rng(seed + 100)
+    P1 = rng.normal(0.0, 1.2, (1, N + 1, V)).astype(np.float32)
+    rep = lambda a: np.repeat(a, reps, axis=0)
+    o = oracle.pctree_verify(rep(t["tok"]), rep(t["par"]), rep(P1), g, 17, 3)
+    return t, P1[0], o
+
+
+def test_pctree_verify_is_lossless():
+    """Over many independent draws (one request per draw), the first emitted
+    token (the first accepted child, or the next anchor) is distributed as
+    softmax(P[root]) (chi-square), whatever the tree proposes."""
+    t, P, o = _tree_mc(2)
+    tok = t["tok"][0]
+    first = np.where(o["n_acc"] > 0, tok[np.maximum(o["path"][:, 1], 0)], o["next_anchor"])
+    V = P.shape[1]
+    p = np.exp(P[0].astype(np.float64) - special.logsumexp(P[0].astype(np.float64)))
+    counts = np.bincount(first, minlength=V)
+    keep = p * len(first) >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp_ = np.append(p[keep], p[~keep].sum()) * len(first)
+    if exp_[-1] == 0:
+        obs, exp_ = obs[:-1], exp_[:-1]
+    assert stats.chisquare(obs, exp_).pvalue > 1e-3
+
+
+def test_pctree_expected_accepted_length_closed_form():
+    """A node is reached with probability prod over its path of p_t(token |
+    parent row): E[n_acc] is the sum of these over the nodes."""
+    t, P, o = _tree_mc(3)
+    tok, par = t["tok"][0], t["par"][0]
+    pt = np.exp(P.astype(np.float64) - special.logsumexp(P.astype(np.float64), axis=1, keepdims=True))
+    reach = np.zeros(len(tok))
+    reach[0] = 1.0
+    for i in range(1, len(tok)):
+        reach[i] = reach[par[i]] * pt[par[i], tok[i]]
+    expected = reach[1:].sum()
+    n = o["n_acc"].astype(np.float64)
+    assert abs(n.mean() - expected) < 4 * n.std() / np.sqrt(len(n)) + 1e-9
+    # the accepted path always follows parent links from the root
+    for row in o["path"][:200]:
+        for a, b in zip(row, row[1:]):
+            if b < 0:
+                break
+            assert par[b] == a
+
+
+def test_pctree_certain_targets_accept_the_first_children():
+    """Target rows that put all their mass on a node's first child accept it:
+    the path follows first children to the deepest one, and the next anchor
+    is then the bonus draw from the last row."""
+    U, W1, W2, anchor = _tree_inputs(4, g=3)
+    N = 7
+    t = oracle.pctree_build(U, W1, W2, anchor, 2, N)
+    tok, par = t["tok"][0], t["par"][0]
+    V = U.shape[2]
+    P = np.full((1, N + 1, V), -30.0, np.float32)
+    first = {}
+    for i in range(1, N + 1):
+        first.setdefault(par[i], i)
+    for node, ch in first.items():
+        P[0, node, tok[ch]] = 30.0
+    o = oracle.pctree_verify(t["tok"], t["par"], P, 3, 5, 0)
+    node, path = 0, [0]
+    while node in first:
+        node = first[node]
+        path.append(node)
+    assert o["n_acc"][0] == len(path) - 1
+    assert list(o["path"][0][:len(path)]) == path
