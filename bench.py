@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-sts", action="store_true", help="skip the STS calibration-fit timing")
     ap.add_argument("--no-loss", action="store_true", help="skip the training-objective timing")
     ap.add_argument("--no-rnn", action="store_true", help="skip the RNN-head draft timing")
-    ap.add_argument("--only", choices=["loss", "rnn", "sts"], default=None,
+    ap.add_argument("--only", choices=["draft", "loss", "rnn", "sts"], default=None,
                     help="run one of the secondary timings alone and print its JSON (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --only loss / rnn: the number of requests (default: the prod workload's)")
@@ -241,6 +241,32 @@ def sts_timing(reps: int = 10):
             "temperatures": [round(float(t), 3) for t in T.cpu().tolist()]}
 
 
+def draft_timing(peak_gbs: float, calls: int = 4, batch=None):
+    """The Markov draft alone on the prod shape (inputs drawn on the device),
+    for kernel captures: `calls` direct calls, the last `calls - 1` timed with
+    CUDA events (U, 0.33 GB, exceeds the L2)."""
+    import torch
+    from speculative_decoding_head_gb300.binding import Workspace
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
+    dev = make_inputs(wl, device="cuda", with_target=False)
+    ws = Workspace.for_workload(wl)
+    args = (dev["U"], dev["W1"], dev["W2"], dev["anchor"], dev["h"], dev["w"], dev["T"], wl.seed, 0)
+    out = ws.draft(*args)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls - 1):
+        ws.draft(*args, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    ms = e0.elapsed_time(e1) / max(1, calls - 1)
+    alg = wl.B * wl.gamma * wl.V * 4 + wl.gamma * wl.r * wl.V * 2
+    return {"workload": "prod" if batch is None else f"prod with B={batch}", "path": ws.path, "ms_per_call": ms,
+            "alg_bytes": alg, "achieved_gbs": alg / (ms * 1e-3) / 1e9,
+            "frac_of_measured_hbm": alg / (ms * 1e-3) / 1e9 / peak_gbs, "launches": ws.last_launches}
+
+
 def _graphed(fn):
     """fn captured in a CUDA graph (replayed by the returned callable), as the
     round is timed; direct calls if the capture fails. Returns (call, graph?)."""
@@ -368,7 +394,8 @@ def main():
         from speculative_decoding_head_gb300 import build as bmod
         bmod.build()
         peak, _ = peaks()
-        fn = {"loss": lambda: loss_timing(peak, batch=args.batch), "rnn": lambda: rnn_timing(peak, batch=args.batch),
+        fn = {"draft": lambda: draft_timing(peak, batch=args.batch),
+              "loss": lambda: loss_timing(peak, batch=args.batch), "rnn": lambda: rnn_timing(peak, batch=args.batch),
               "sts": sts_timing}[args.only]
         print(json.dumps({"only": args.only, **fn()}), flush=True)
         return
