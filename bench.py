@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--only", choices=["draft", "loss", "rnn", "sts"], default=None,
                     help="run one of the secondary timings alone and print its JSON (for profiling)")
     ap.add_argument("--batch", type=int, default=None,
-                    help="with --only loss / rnn: the number of requests (default: the prod workload's)")
+                    help="with --only draft / loss / rnn: the number of requests (default: the prod workload's)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle sample")
     return ap.parse_args()
 

@@ -850,7 +850,8 @@ void orc_train_loss(const orc_dims* d, const float* U, const void* W1, const voi
 /*   y_k(n) = prod_{i<=k} cstar[n][i]                                  */
 /* (the prefix's joint acceptance factorises by the chain rule), and   */
 /* M equal-width bins of [0, 1] (bin floor(a M), a = 1 in the last),   */
-/*   ECE_k(T) = (1/N) sum_m | sum_{n: a_k(n) in bin m} (a_k(n) - y_k(n)) |,
+/*   ECE_k(T) = (1/N) sum_m | sum_{n: a_k(n) in bin m}                   */
+/*                             (a_k(n) - y_k(n)) |,                     */
 /* T_k is the first grid value minimising ECE_k given T_1..T_{k-1}.    */
 /* margin_out[k] = second-best ECE - best ECE (INFINITY if G == 1).    */
 /* ------------------------------------------------------------------ */
