@@ -241,6 +241,62 @@ def sts_timing(reps: int = 10):
             "temperatures": [round(float(t), 3) for t in T.cpu().tolist()]}
 
 
+def _np_inputs(inp_cpu):
+    import torch
+    return {k: (v.contiguous().view(torch.int16).numpy() if v.dtype == torch.bfloat16 else v.numpy())
+            for k, v in inp_cpu.items()}
+
+
+def oracle_loss_sample(wl, inp_cpu, budget_s: float, tau: float = 4.0):
+    """The oracle's training objective on a bounded sample of requests (its
+    positions are independent), scaled to one call of B requests: returns
+    the cpu_baseline dict (calls/s), or None for no budget."""
+    if budget_s <= 0:
+        return None
+    import oracle
+    oracle.set_threads(os.cpu_count() or 1)
+    cores = oracle.get_threads()
+    npi = _np_inputs(inp_cpu)
+    n = max(1, min(cores, wl.B))
+    done, spent = 0, 0.0
+    while spent < budget_s and done < wl.B:
+        rows = [(done + i) % wl.B for i in range(n)]
+        t0 = time.perf_counter()
+        oracle.train_loss(npi["U"][rows], npi["W1"], npi["W2"], npi["anchor"][rows], npi["xstar"][rows],
+                          npi["P"][rows], npi["conf"][rows], tau)
+        spent += time.perf_counter() - t0
+        done += n
+    per_call = spent / done * wl.B
+    return {"value": 1.0 / per_call, "unit": "calls/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle training objective of {done} of the {wl.B} requests ({done * wl.gamma} positions): "
+                      f"{spent:.1f} s on {cores} threads, scaled to a {wl.B}-request call"}
+
+
+def oracle_rnn_sample(wl, inp_cpu, Wr_cpu, budget_s: float):
+    """The oracle's RNN-head draft on a bounded sample of requests, scaled to
+    one call of B requests: returns the cpu_baseline dict (calls/s), or None
+    for no budget."""
+    if budget_s <= 0:
+        return None
+    import oracle
+    oracle.set_threads(os.cpu_count() or 1)
+    cores = oracle.get_threads()
+    npi = _np_inputs({**inp_cpu, "Wr": Wr_cpu})
+    n = max(1, min(cores, wl.B))
+    done, spent = 0, 0.0
+    while spent < budget_s and done < wl.B:
+        reqs = [(done + i) % wl.B for i in range(n)]
+        t0 = time.perf_counter()
+        oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
+                         1, 0, reqs=reqs)
+        spent += time.perf_counter() - t0
+        done += n
+    per_call = spent / done * wl.B
+    return {"value": 1.0 / per_call, "unit": "calls/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle RNN-head draft of {done} of the {wl.B} requests: {spent:.1f} s on {cores} threads, "
+                      f"scaled to a {wl.B}-request call"}
+
+
 def draft_timing(peak_gbs: float, calls: int = 4, batch=None):
     """The Markov draft alone on the prod shape (inputs drawn on the device),
     for kernel captures: `calls` direct calls, the last `calls - 1` timed with
@@ -267,6 +323,17 @@ def draft_timing(peak_gbs: float, calls: int = 4, batch=None):
             "frac_of_measured_hbm": alg / (ms * 1e-3) / 1e9 / peak_gbs, "launches": ws.last_launches}
 
 
+def _secondary(fn, *a, **kw):
+    """A secondary timing (STS fit, training objective, RNN draft): its dict,
+    or {"error": ...} so that a failure there is reported in the line without
+    losing the round's own measurement."""
+    try:
+        return fn(*a, **kw)
+    except Exception as e:  # noqa: BLE001 - recorded in the JSON line
+        print(f"# {fn.__name__} failed: {e!r}", file=sys.stderr)
+        return {"error": repr(e)}
+
+
 def _graphed(fn):
     """fn captured in a CUDA graph (replayed by the returned callable), as the
     round is timed; direct calls if the capture fails. Returns (call, graph?)."""
@@ -283,7 +350,7 @@ def _graphed(fn):
         return fn, False
 
 
-def loss_timing(peak_gbs: float, reps: int = 10, batch=None):
+def loss_timing(peak_gbs: float, reps: int = 10, batch=None, cpu_budget_s: float = 3.0):
     """The draft head's teacher-forced training objective on the prod shape:
     device time per call (five launches), CUDA events on the launching stream
     after warm-up, inputs resident (U and P, 0.66 GB, exceed the L2). The
@@ -293,7 +360,8 @@ def loss_timing(peak_gbs: float, reps: int = 10, batch=None):
     from speculative_decoding_head_gb300.workloads import WORKLOADS, make_loss_inputs
     wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
     tau = 4.0
-    inp = {k: v.cuda() for k, v in make_loss_inputs(wl).items()}
+    inp_cpu = make_loss_inputs(wl)
+    inp = {k: v.cuda() for k, v in inp_cpu.items()}
     ws = Workspace.for_workload(wl)
     out = ws.new_loss_outputs()
     args = (inp["U"], inp["W1"], inp["W2"], inp["anchor"], inp["xstar"], inp["P"], inp["conf"], tau)
@@ -317,10 +385,10 @@ def loss_timing(peak_gbs: float, reps: int = 10, batch=None):
             "V": wl.V, "r": wl.r, "ms_per_call": ms,
             "positions_per_s": n / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches, "graph": graphed,
-            "loss": float(out["loss"].item())}
+            "loss": float(out["loss"].item()), "cpu_baseline": oracle_loss_sample(wl, inp_cpu, cpu_budget_s)}
 
 
-def rnn_timing(peak_gbs: float, reps: int = 10, batch=None):
+def rnn_timing(peak_gbs: float, reps: int = 10, batch=None, cpu_budget_s: float = 3.0):
     """The draft tail with the RNN head on the prod shape: device time per
     call, CUDA events on the launching stream after warm-up, inputs resident.
     The algorithmic bytes are the Markov draft's (U once, W2 once per step,
@@ -329,8 +397,10 @@ def rnn_timing(peak_gbs: float, reps: int = 10, batch=None):
     from speculative_decoding_head_gb300.binding import Workspace
     from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_rnn_weights
     wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
-    inp = {k: v.cuda() for k, v in make_inputs(wl, with_target=False).items()}
-    Wr = make_rnn_weights(wl).cuda()
+    inp_cpu = make_inputs(wl, with_target=False)
+    Wr_cpu = make_rnn_weights(wl)
+    inp = {k: v.cuda() for k, v in inp_cpu.items()}
+    Wr = Wr_cpu.cuda()
     ws = Workspace.for_workload(wl)
     out = None
     for _ in range(3):
@@ -355,7 +425,7 @@ def rnn_timing(peak_gbs: float, reps: int = 10, batch=None):
             "H": H, "ms_per_call": ms,
             "drafted_tokens_per_s": B * g / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches, "graph": graphed,
-            "path": "tcgen05 block pass"}
+            "path": "tcgen05 block pass", "cpu_baseline": oracle_rnn_sample(wl, inp_cpu, Wr_cpu, cpu_budget_s)}
 
 
 def run_reference(args):
@@ -559,6 +629,7 @@ def main():
     if rank == 0:
         value = world / t_round
         emitted = int((out["n_acc"].to(torch.int64) + 1).sum().item())
+        cpu_s = 0.0 if args.no_cpu_baseline else 3.0  # oracle seconds beside each secondary timing
         line = {
             "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -571,9 +642,9 @@ def main():
             "verified_positions_per_s": value * sum_len,
             "emitted_tokens_per_round": emitted,
             "stage_ms": st,
-            "sts_fit": None if args.no_sts else sts_timing(),
-            "train_loss": None if args.no_loss else loss_timing(peak),
-            "rnn_draft": None if args.no_rnn else rnn_timing(peak),
+            "sts_fit": None if args.no_sts else _secondary(sts_timing),
+            "train_loss": None if args.no_loss else _secondary(loss_timing, peak, cpu_budget_s=cpu_s),
+            "rnn_draft": None if args.no_rnn else _secondary(rnn_timing, peak, cpu_budget_s=cpu_s),
             "roofline": roofline,
             "cpu_baseline": cpu_base,
             "e2e": e2e,

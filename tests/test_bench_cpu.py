@@ -24,3 +24,17 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"].startswith("tiny")
+
+
+def test_secondary_oracle_samples_run_on_cpu():
+    """The oracle legs that sit beside the training-objective and RNN-draft
+    timings (bench.py's cpu_baseline entries), on a small shape."""
+    import sys as _s
+    _s.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_loss_inputs, make_rnn_weights
+    wl = WORKLOADS["small"].with_(B=4, gamma=3, V=1024, r=64, H=32)
+    c = bench.oracle_loss_sample(wl, make_loss_inputs(wl), 0.2)
+    assert c["value"] > 0 and c["kind"] == "oracle" and c["unit"] == "calls/s" and c["cores"] >= 1
+    c = bench.oracle_rnn_sample(wl, make_inputs(wl, with_target=False), make_rnn_weights(wl), 0.2)
+    assert c["value"] > 0 and c["kind"] == "oracle" and "RNN" in c["sample"]
