@@ -38,3 +38,13 @@ def test_secondary_oracle_samples_run_on_cpu():
     assert c["value"] > 0 and c["kind"] == "oracle" and c["unit"] == "calls/s" and c["cores"] >= 1
     c = bench.oracle_rnn_sample(wl, make_inputs(wl, with_target=False), make_rnn_weights(wl), 0.2)
     assert c["value"] > 0 and c["kind"] == "oracle" and "RNN" in c["sample"]
+
+
+def test_sts_oracle_sample_runs_on_cpu():
+    import sys as _s
+    _s.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_head_gb300.workloads import make_sts_inputs, sts_grid
+    c = bench.oracle_sts_sample(make_sts_inputs(5000, 3, 1), sts_grid(8), 15, 0.1)
+    assert c["value"] > 0 and c["unit"] == "fits/s" and c["kind"] == "oracle"
+    assert bench.oracle_sts_sample(make_sts_inputs(100, 2, 1), sts_grid(4), 15, 0.0) is None
