@@ -71,12 +71,12 @@ def lib():
             l.orc_gumbel.restype = dbl
             l.orc_logsumexp.argtypes = [P, C.c_long]
             l.orc_logsumexp.restype = dbl
-            l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P]
+            l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P]
             l.orc_verify_head.argtypes = [P, P, P, P, P, P, P, P, P, P, u64, u64, P, i32,
                                           P, P, P, P, P]
             l.orc_pctree_build.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, P]
             l.orc_pctree_verify.argtypes = [P, i32, P, P, P, u64, u64, P, P, P, P]
-            l.orc_rnn_draft.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P]
+            l.orc_rnn_draft.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P, P]
             l.orc_plan_sync.argtypes = [i32, i32, P, P, P, P]
             l.orc_plan_sync.restype = i32
             l.orc_plan_capacity.argtypes = [i32, i32, P, P, P]
@@ -156,8 +156,9 @@ def sample(logw, seed=0, rnd=0, pblk=P_DRAFT_BLOCK, ptok=P_DRAFT_TOKEN, b=0, j=0
 
 
 def sample_draft(logw, seed=0, rnd=0, b=0, j=0):
-    """One draw with the draft's sampler (block by Gumbel-max, token inside the
-    block by inverse CDF). Returns (v, margin)."""
+    """One draw with the draft's random stream (block by Gumbel-max, token
+    inside the block by Gumbel-max; purposes draft block / draft token).
+    Returns (v, margin)."""
     a = _c(logw, np.float64)
     m = np.zeros(1, np.float64)
     v = lib().orc_sample_draft(_p(a), a.size, seed, rnd, b, j, _p(m))
@@ -221,13 +222,24 @@ def _weights(W) -> (np.ndarray, bool):
     return _c(a, np.float32), False
 
 
+def _force(force, B, g):
+    if force is None:
+        return None
+    f = _c(force, np.int32)
+    if f.shape != (B, g):
+        raise ValueError(f"force must be [{B}, {g}], got {f.shape}")
+    return f
+
+
 def draft(U, W1, W2, anchor, h, w, T, seed: int, rnd: int,
-          reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+          reqs: Optional[Sequence[int]] = None, force=None) -> Dict[str, np.ndarray]:
     """Markov-head draft tail + confidence head, eq. (4), (5), (7).
 
     U [B, gamma, V] fp32, W1 [V, r], W2 [r, V] (fp32 or bf16 bits), anchor [B],
     h [B, gamma, H], w [H + r], T [gamma]. ``reqs`` restricts the work to a
-    subset of requests (global indices keep their random streams).
+    subset of requests (global indices keep their random streams). ``force``
+    [B, gamma] int32 (optional): entries >= 0 are adopted in place of the
+    draw at that position (teacher forcing at flagged positions).
     """
     U = _c(U, np.float32)
     B, g, V = U.shape
@@ -244,14 +256,15 @@ def draft(U, W1, W2, anchor, h, w, T, seed: int, rnd: int,
     out = {"tokens": np.full((B, g), -1, np.int32), "pd_tok": np.full((B, g), np.nan),
            "lse": np.full((B, g), np.nan), "conf": np.full((B, g), np.nan),
            "margin": np.full((B, g), np.inf)}
+    f = _force(force, B, g)
     lib().orc_draft(C.byref(d), _p(U), _p(w1), _p(w2), _p(anchor), _p(h), _p(w), _p(T),
-                    seed, rnd, _p(rq), rq.size, _p(out["tokens"]), _p(out["pd_tok"]),
+                    seed, rnd, _p(rq), rq.size, None if f is None else _p(f), _p(out["tokens"]), _p(out["pd_tok"]),
                     _p(out["lse"]), _p(out["conf"]), _p(out["margin"]))
     return out
 
 
 def rnn_draft(U, W1, W2, Wr, anchor, h, w, T, seed: int, rnd: int,
-              reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
+              reqs: Optional[Sequence[int]] = None, force=None) -> Dict[str, np.ndarray]:
     """Draft tail with the RNN head, eq. (6) (see ``orc_rnn_draft``).
 
     As ``draft``, plus Wr [3, r, 2r + H] (W_g, W_c, W_o; same storage as W1)
@@ -278,8 +291,10 @@ def rnn_draft(U, W1, W2, Wr, anchor, h, w, T, seed: int, rnd: int,
     out = {"tokens": np.full((B, g), -1, np.int32), "pd_tok": np.full((B, g), np.nan),
            "lse": np.full((B, g), np.nan), "conf": np.full((B, g), np.nan),
            "margin": np.full((B, g), np.inf), "ovec": np.full((B, g, r), np.nan)}
+    f = _force(force, B, g)
     lib().orc_rnn_draft(C.byref(d), _p(U), _p(w1), _p(w2), _p(wr), _p(anchor), _p(h), _p(w), _p(T),
-                        seed, rnd, _p(rq), rq.size, _p(out["tokens"]), _p(out["pd_tok"]),
+                        seed, rnd, _p(rq), rq.size, None if f is None else _p(f), _p(out["tokens"]),
+                        _p(out["pd_tok"]),
                         _p(out["lse"]), _p(out["conf"]), _p(out["margin"]), _p(out["ovec"]))
     return out
 

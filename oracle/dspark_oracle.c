@@ -34,15 +34,19 @@
  *              target ([V4.1 blog] "投机解码"; [ailearn] 02; [csdn] 2.1).
  *
  * Readings where the pages are silent (each also listed in the design notes):
- *   * sampler: the pages only write sample(logits). Every sample here is an
- *     exact two-level draw over vocabulary blocks of 64 tokens: a block is
- *     drawn with probability (block mass / total mass) by a Gumbel-max,
- *     argmax_s (log mass_s + G_s), then a token inside it with probability
- *     (weight / block mass). The draft takes that token by inverse CDF with
- *     one uniform u of the block: the first v (in token order) whose
- *     cumulative block weight exceeds u times the block mass. The verify
- *     draws (bonus, residual) take it by argmax_v (log weight_v + G_v).
- *     Temperature is 1.
+ *   * sampler: the pages only write sample(logits). Every sample here (the
+ *     draft, the bonus and the residual draw) is an exact two-level draw over
+ *     vocabulary blocks of 64 tokens: a block is drawn with probability
+ *     (block mass / total mass) by a Gumbel-max, argmax_s (log mass_s + G_s),
+ *     then a token inside it with probability (weight / block mass) by a
+ *     second Gumbel-max, argmax_v (log weight_v + G_v) over the block's
+ *     tokens. Each level is an exact categorical draw, so the pair is an
+ *     exact draw from the softmax, and each level's decision has a key gap
+ *     as its margin. Temperature is 1.
+ *   * teacher forcing (for parity checks only): the draft may be handed a
+ *     token to adopt at a position whose draw was too close to call; the
+ *     position's logits, margin and probability are still computed, and the
+ *     chain continues from the adopted token.
  *   * random stream: Philox4x32-10 (Salmon et al., SC'11), key = seed,
  *     counter = (v >> 2, b, j, purpose << 24 | round mod 2^24), word v & 3,
  *     u = (2 * (word >> 9) + 1) * 2^-24, G = -log(-log u).
@@ -190,7 +194,7 @@ static long pick_block(const double* logw, const double* tol_mass, long V, uint6
     return bs;
 }
 
-/* Two-level draw, token level by Gumbel-max (verify draws). The margin is the
+/* Two-level draw, token level by Gumbel-max (every draw). The margin is the
  * smaller of the block and token key gaps; tol/tol_mass (may be NULL) are
  * per-token absolute error bounds of exp(logw) that widen the gaps.
  * Returns -1 if no token has positive weight. */
@@ -212,42 +216,6 @@ static int sample_two_level(const double* logw, const double* tol, const double*
         else if (key > k2) { k2 = key; t2 = t; }
     }
     double m2 = (k2 == -INFINITY) ? INFINITY : (kb - k2) - (t1 + t2);
-    *margin = m1 < m2 ? m1 : m2;
-    return (int)vb;
-}
-
-/* Two-level draw, token level by inverse CDF (the draft): with
- * u = U(ptok, b, j, block) and e_v = exp(logw_v - max of the block),
- * the first v of the block with e_lo + ... + e_v > u * (sum of the block's e).
- * The token margin is the distance of u * sum to the nearest cumulative
- * boundary of the drawn token, relative to the sum; the margin reported is
- * the smaller of it and the block key gap. Returns -1 if no positive weight. */
-static int sample_two_level_icdf(const double* logw, long V, uint64_t seed, uint64_t round,
-                                 uint32_t pblk, uint32_t ptok, uint32_t b, uint32_t j,
-                                 double* margin)
-{
-    double m1;
-    long bs = pick_block(logw, NULL, V, seed, round, pblk, b, j, &m1);
-    if (bs < 0) { *margin = INFINITY; return -1; }
-    long lo = bs * ORC_BLOCK, hi = lo + ORC_BLOCK < V ? lo + ORC_BLOCK : V;
-    double mx = -INFINITY;
-    for (long v = lo; v < hi; ++v) if (logw[v] > mx) mx = logw[v];
-    double e[ORC_BLOCK], sum = 0.0;
-    for (long v = lo; v < hi; ++v) { e[v - lo] = exp(logw[v] - mx); sum += e[v - lo]; }
-    double t = orc_uniform(seed, round, ptok, b, j, (uint32_t)bs) * sum;
-    double c = 0.0, below = 0.0;
-    long vb = -1;
-    for (long v = lo; v < hi; ++v) {
-        below = c;
-        c += e[v - lo];
-        if (e[v - lo] > 0.0 && c > t) { vb = v; break; }
-    }
-    if (vb < 0) {  /* not reached for u < 1; keep the last positive weight */
-        for (long v = hi - 1; v >= lo; --v) if (e[v - lo] > 0.0) { vb = v; break; }
-        *margin = 0.0;
-        return (int)vb;
-    }
-    double m2 = fmin(t - below, c - t) / sum;
     *margin = m1 < m2 ? m1 : m2;
     return (int)vb;
 }
@@ -288,11 +256,13 @@ static void head_logits(const orc_dims* d, const float* Urow, const void* W2, co
  * For each request b in reqs[0..n_req): draft x_1..x_gamma.
  * Outputs (indexed [b][k-1], full-size arrays, only listed rows written):
  *   tokens, pd_tok = p_k(x_k), lse = log sum exp(z_k), conf = c_k,
- *   margin = the draw's margin (see sample_two_level_icdf).
+ *   margin = the draw's margin (see sample_two_level).
+ * force (may be NULL): force[b][k-1] >= 0 replaces the drawn x_k by that token
+ * (teacher forcing at a flagged position); the margin is still the draw's.
  */
 void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2,
                const int32_t* anchor, const float* h, const float* w, const float* T,
-               uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+               uint64_t seed, uint64_t round, const int32_t* reqs, int n_req, const int32_t* force,
                int32_t* tokens, double* pd_tok, double* lse, double* conf, double* margin)
 {
     const long V = d->V, g = d->gamma, r = d->r, H = d->H;
@@ -312,8 +282,9 @@ void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2
             markov_logits(d, U + o * V, W1, W2, x_prev, z);
             double L = orc_logsumexp(z, V);
             double m = 0.0;
-            int x = sample_two_level_icdf(z, V, seed, round, ORC_P_DRAFT_BLOCK,
-                                          ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            int x = sample_two_level(z, NULL, NULL, V, seed, round, ORC_P_DRAFT_BLOCK,
+                                     ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            if (force && force[o] >= 0) x = force[o];
             tokens[o] = x;
             pd_tok[o] = exp(z[x] - L);
             lse[o] = L;
@@ -339,7 +310,7 @@ void orc_draft(const orc_dims* d, const float* U, const void* W1, const void* W2
 /* ------------------------------------------------------------------ */
 void orc_rnn_draft(const orc_dims* d, const float* U, const void* W1, const void* W2, const void* Wr,
                    const int32_t* anchor, const float* h, const float* w, const float* T,
-                   uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                   uint64_t seed, uint64_t round, const int32_t* reqs, int n_req, const int32_t* force,
                    int32_t* tokens, double* pd_tok, double* lse, double* conf, double* margin,
                    double* ovec)
 {
@@ -380,8 +351,9 @@ void orc_rnn_draft(const orc_dims* d, const float* U, const void* W1, const void
             head_logits(d, U + o * V, W2, ov, z);
             const double L = orc_logsumexp(z, V);
             double m = 0.0;
-            const int x = sample_two_level_icdf(z, V, seed, round, ORC_P_DRAFT_BLOCK,
-                                                ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            int x = sample_two_level(z, NULL, NULL, V, seed, round, ORC_P_DRAFT_BLOCK,
+                                     ORC_P_DRAFT_TOKEN, (uint32_t)b, (uint32_t)k, &m);
+            if (force && force[o] >= 0) x = force[o];
             tokens[o] = x;
             pd_tok[o] = exp(z[x] - L);
             lse[o] = L;
@@ -906,12 +878,12 @@ int orc_sample(const double* logw, long V, uint64_t seed, uint64_t round,
     return sample_two_level(logw, NULL, NULL, V, seed, round, pblk, ptok, b, j, margin);
 }
 
-/* one exact draw with the draft's sampler (token level by inverse CDF) */
+/* one exact draw with the draft's stream (purposes draft block / draft token) */
 int orc_sample_draft(const double* logw, long V, uint64_t seed, uint64_t round,
                      uint32_t b, uint32_t j, double* margin)
 {
-    return sample_two_level_icdf(logw, V, seed, round, ORC_P_DRAFT_BLOCK, ORC_P_DRAFT_TOKEN,
-                                 b, j, margin);
+    return sample_two_level(logw, NULL, NULL, V, seed, round, ORC_P_DRAFT_BLOCK, ORC_P_DRAFT_TOKEN,
+                            b, j, margin);
 }
 
 /* residual draw for explicit p_t, p_d (pin tests); returns -1 if no mass */
