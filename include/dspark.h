@@ -135,8 +135,11 @@ dspark_status dspark_ws_set_path(dspark_ws* ws, const char* path);
  *   pd_tok  fp32    p_k(x_k), the draft probability of the drafted token
  *   lse     fp32    log sum_v exp(U_k(v) + W1[x_{k-1}] . W2[:, v])
  *   conf    fp32    c_k
- * anchor [B] int32 in [0, V). Sampling: two-level Gumbel-max (vocabulary
- * blocks of 64 tokens), temperature 1.
+ * anchor [B] int32 in [0, V). Sampling, temperature 1: a two-level Gumbel-max
+ * over vocabulary blocks of 64 tokens, the block s by argmax (log mass_s + G)
+ * and the token inside it by argmax (z_v + G), each G = -log(-log u) with u
+ * from Philox4x32-10 (key = seed, counter (index >> 2, b, k, purpose << 24 |
+ * round mod 2^24), word index & 3; purpose 1 for blocks, 2 for tokens).
  */
 dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2,
                                   const int32_t* anchor, const float* h, const float* w,

@@ -12,7 +12,7 @@
 //   k_draft_pick    grid (B): log-sum-exp over blocks, the block draw
 //                   argmax_s(log mass_s + G_s), then z of the 64 tokens of the
 //                   drawn block recomputed and the token inside it drawn by
-//                   inverse CDF with one uniform of the block; also c_k.
+//                   argmax_v (z_v + G_v); also c_k.
 // With the RNN head (eq. (6)) the r-vector that multiplies W2 is the head's
 // o_k, which k_rnn_cell writes before each step (ovec); the confidence still
 // takes W1[x_{k-1}].
@@ -162,29 +162,23 @@ __global__ void __launch_bounds__(kSimtThreads)
     }
   }
   __syncthreads();
+  // token draw inside block sb: argmax_v (z_v + G_v) over its 64 tokens, one
+  // thread per token, then across the two warps
   if (tid < kBlockW) {
     const int v = sb * kBlockW + tid;
     float z = -INFINITY;
     if (v < V) z = U[o * V + v] + ((zpart[0][tid] + zpart[1][tid]) + (zpart[2][tid] + zpart[3][tid]));
     zblk[tid] = z;
+    KeyIdx kt = key_none();
+    if (z > -INFINITY) kt = KeyIdx{z + gumbel(rng.word(kDraftToken, b, k, v)), tid};
+    kt = warp_best(kt);
+    if (lane == 0) red_k[warp] = kt;
   }
   __syncthreads();
   if (tid == 0) {
-    // inverse CDF with one uniform u of the block: e_v = exp(z_v - max) in
-    // token order, x = the first v whose running sum exceeds u times the
-    // total (the same running sum, so for u < 1 some v always does)
-    float mx = -INFINITY;
-    for (int i = 0; i < kBlockW; ++i) mx = fmaxf(mx, zblk[i]);
-    float tot = 0.f;
-    for (int i = 0; i < kBlockW; ++i) tot += __expf(zblk[i] - mx);
-    const float thr = u01(rng.word(kDraftToken, b, k, sb)) * tot;
-    float cum = 0.f;
-    int xl = -1;
-    for (int i = 0; i < kBlockW && xl < 0; ++i) {
-      cum += __expf(zblk[i] - mx);
-      if (cum > thr) xl = i;
-    }
-    if (xl < 0) {  // only non-finite logits get here
+    const KeyIdx kt = better(red_k[0], red_k[1]);
+    int xl = kt.idx;
+    if (xl == kNoIdx) {  // only non-finite logits get here
       raise_status(status, DSPARK_ENUMERIC);
       xl = 0;
     }

@@ -29,16 +29,16 @@
 //               z = TMEM, the block's log-mass (max, sum exp), the block
 //               draw key log mass + G_s, the row's online log-sum-exp, and a
 //               register copy of z for the set's best block so far.
-// Step boundary. The block draw is a grid-wide argmax: each set publishes its
-// best (key, block) per row with a 64-bit atomic max, then all CTAs meet at
-// one grid barrier. The token draw inside the winning block needs only that
-// block's z, which the set that found it recorded: that set's warp draws the
-// token (lanes split the 64 tokens) and stores a per-row flag carrying x_k.
-// In every CTA of the group, the epilogue thread of each row waits for that
-// flag and gathers W1[x_k] straight into the swizzled A operand in shared
-// memory (the anchors' rows at step 1). The producers
-// keep prefetching the next step's tiles meanwhile (they do not depend on
-// the drafted token). Log-sum-exps, probabilities of the drawn tokens and
+// Step boundary. The block draw is a grid-wide argmax of the block keys. Each
+// set first draws the token inside its own best block (the token level of the
+// two-level sampler, argmax_v (z_v + G_v) over the block's 64 tokens, from the
+// register copy of that block's z), so that its candidate is complete, then
+// publishes (block key, token) per row with a 64-bit atomic max; all CTAs
+// meet at one grid barrier, after which the winner words are final. In every
+// CTA of the group the epilogue warps read the 128 rows' tokens and gather
+// W1[x_k] straight into the swizzled A operand in shared memory (the anchors'
+// rows at step 1). The producers keep prefetching the next step's tiles
+// meanwhile (they do not depend on the drafted token). Log-sum-exps, probabilities of the drawn tokens and
 // confidences are off that chain: per-set partials (max, sum exp) are kept
 // per step and combined after the last step, one warp per (row, step), which
 // also forms the confidence logit w^T [h_k; W1[x_{k-1}]] from h and W1.
@@ -84,13 +84,17 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
   __host__ __device__ static TcSmem make(int r) {
     TcSmem s;
     s.a = 0;
-    s.w2 = s.a + kTcRows * r * 2;
+    // the A operand; between the last tile of a step and the next gather it
+    // holds every epilogue thread's best block of z (64 fp32 each)
+    s.w2 = s.a + max(kTcRows * r * 2, kEpiThreads * kBlk * 4);
     s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
     // w2 full/empty, u full, u empty, t full/empty, a_full, drain, acc_u
     // (accumulator holds U), the copier's drain
     s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 2 + kNAcc + 1);
-    s.total = s.misc + 64;
+    // misc: TMEM address and abort word (64 B), then the step-end exchange of
+    // each set's best block per row: key [kSets][128] fp32, block [kSets][128] u16
+    s.total = s.misc + 64 + kEpiThreads * 4 + kEpiThreads * 2;
     return s;
   }
 };
@@ -133,6 +137,73 @@ __device__ __forceinline__ int win_token(unsigned long long w) {
 // 64 elements 16 KB apart.
 __device__ __forceinline__ size_t a_piece(int m, int kb, int ch) {
   return (size_t)kb * (kTcRows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
+}
+
+// The token level of the draft's two-level sampler over one 64-token block
+// whose z sits in shared memory (chunk c of 4 tokens at c ^ sw): argmax_i
+// (z[i] + G(kDraftToken, b, k, v0 + i)), first maximum on ties. The two
+// threads of a row each screen half of the tokens, ranking
+// z log2(e) + gumbel2_screen(u) (error about 1e-5); when the best two screened
+// keys of the block lie within kScreenGap, the keys are recomputed exactly
+// (z + gumbel(u)) and the argmax taken on those, so the result is the
+// exact-key argmax.
+struct DrawPart {
+  float k1, k2, z1;  // best and second screened key, z of the best
+  int i1;            // its token in the block, -1 if none is finite
+};
+
+constexpr int kDrawUnroll = 4;  // independent Philox chains in flight per thread
+__device__ __noinline__ DrawPart draw_screen(const float4* zs, int sw, const Rng& rng, int b, int k, int v0,
+                                             int c_lo) {
+  DrawPart d{-INFINITY, -INFINITY, 0.f, -1};
+#pragma unroll(kDrawUnroll)
+  for (int c4 = c_lo; c4 < c_lo + kBlk / 8; ++c4) {
+    const float4 zz = zs[c4 ^ sw];
+    const uint4 o = rng.block4(kDraftToken, b, k, v0 + 4 * c4);
+    const float zv[4] = {zz.x, zz.y, zz.z, zz.w};
+    const uint32_t wv[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float key = fmaf(zv[i], tc::kLog2e, gumbel2_screen(wv[i]));
+      d.k2 = fmaxf(d.k2, fminf(d.k1, key));
+      if (key > d.k1) {
+        d.k1 = key;
+        d.z1 = zv[i];
+        d.i1 = 4 * c4 + i;
+      }
+    }
+  }
+  return d;
+}
+
+// the two halves combined: the lower half's tokens come first on ties
+__device__ __forceinline__ DrawPart draw_join(const DrawPart& a, const DrawPart& b) {
+  DrawPart r = b.k1 > a.k1 ? b : a;
+  r.k2 = fmaxf(fminf(a.k1, b.k1), fmaxf(a.k2, b.k2));
+  return r;
+}
+
+__device__ __noinline__ int draw_exact(const float4* zs, int sw, const Rng& rng, int b, int k, int v0, float* zx) {
+  float best = -INFINITY, z1 = 0.f;
+  int i1 = -1;
+#pragma unroll 1
+  for (int c4 = 0; c4 < kBlk / 4; ++c4) {
+    const float4 zz = zs[c4 ^ sw];
+    const uint4 o = rng.block4(kDraftToken, b, k, v0 + 4 * c4);
+    const float zv[4] = {zz.x, zz.y, zz.z, zz.w};
+    const uint32_t wv[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float key = zv[i] + gumbel(wv[i]);
+      if (key > best) {
+        best = key;
+        z1 = zv[i];
+        i1 = 4 * c4 + i;
+      }
+    }
+  }
+  *zx = z1;
+  return i1;
 }
 
 // Grid barrier among the epilogue warps (named barrier 1) of all CTAs: the
@@ -445,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
       // ---- this CTA's tiles; set s takes the blocks whose running index gb
       // has gb % kSets == s (so the sets share the tiles and the U ring evenly)
-      float M = -INFINITY, S = 0.f, bk = -INFINITY, bm = 0.f;
+      float M = -INFINITY, S = 0.f, bk = -INFINITY;
       int bs = kNoIdx;
       float zb[kBlk];  // z of this set's best block so far
 #pragma unroll
@@ -532,7 +603,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (key > bk) {  // this set sees its blocks in increasing order: ties keep the first
               bk = key;
               bs = t;
-              bm = mb;
 #pragma unroll
               for (int e = 0; e < kBlk; ++e) zb[e] = z[e];
             }
@@ -540,63 +610,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
-      // ---- the token inside this set's best block, by inverse CDF with one
-      // uniform u of the block: e_v = exp(z_v - max) in token order, and x is
-      // the first v whose running sum exceeds u times the total. The running
-      // sum is formed chunk by chunk (8 tokens each): s_c = e_8c + .. + e_8c+7,
-      // P_c+1 = P_c + s_c; the chunk is the first with P_c+1 > u P_8, and the
-      // token the first i in it with P_c + (e_8c + .. + e_8c+i) > u P_8. The
-      // last i of the chunk reproduces P_c+1 bit for bit, so one qualifies.
+      // ---- the token inside this CTA's best block of the row: argmax_v
+      // (z_v + G_v) over its 64 tokens, G_v from the draft-token stream at
+      // (b, k, v). Every MMA of this step has completed once both sets are
+      // here (each waited for all of its tiles), so the A operand is free
+      // until the next gather: each thread parks its best block's z there
+      // (its slot), the two sets' keys are compared per row, and the two
+      // threads of the row each screen half of the better block's tokens
+      // with rolled loops (straight-line code for 64 Gumbels would not fit
+      // the instruction cache); the partial results meet in the other slot.
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      const bool cand = valid && bs != kNoIdx && !*abort;
+      float* keyx = reinterpret_cast<float*>(smem + L.misc + 64);
+      uint16_t* blkx = reinterpret_cast<uint16_t*>(smem + L.misc + 64 + kEpiThreads * 4);
+      float4* slot0 = reinterpret_cast<float4*>(smem + L.a) + (size_t)m * (kBlk / 4);  // set 0's slot of row m
+      float4* slot1 = slot0 + (size_t)kTcRows * (kBlk / 4);
+      const int sw = lane & 7;  // chunk swizzle: a quarter-warp's 16-byte accesses hit distinct banks
+      keyx[set * kTcRows + m] = cand ? bk : -INFINITY;
+      blkx[set * kTcRows + m] = (uint16_t)(cand ? bs : 0);
+      if (cand) {
+        float4* zs = set ? slot1 : slot0;
+#pragma unroll
+        for (int c4 = 0; c4 < kBlk / 4; ++c4)
+          zs[c4 ^ sw] = make_float4(zb[4 * c4], zb[4 * c4 + 1], zb[4 * c4 + 2], zb[4 * c4 + 3]);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      const float kA = keyx[m], kB = keyx[kTcRows + m];
+      const int wset = kB > kA ? 1 : 0;  // the row's better candidate of this CTA (set 0 on ties)
+      const bool any = valid && (kA > -INFINITY || kB > -INFINITY) && !*abort;
+      const int wbs = blkx[wset * kTcRows + m];
+      const float4* zw = wset ? slot1 : slot0;
+      float4* zl = wset ? slot0 : slot1;  // the other slot carries the two halves' results
+      if (any) {
+        const DrawPart d = draw_screen(zw, sw, p.rng, b, k, wbs * kBlk, set * (kBlk / 8));
+        zl[set] = make_float4(d.k1, d.k2, d.z1, __int_as_float(d.i1));
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       int bx = -1;
       float bzx = 0.f;
-      if (valid && bs != kNoIdx && !*abort) {
-        float s8[8];
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float a = __expf(zb[8 * c8] - bm);
-#pragma unroll
-          for (int i = 1; i < 8; ++i) a += __expf(zb[8 * c8 + i] - bm);
-          s8[c8] = a;
-        }
-        float P[9];
-        P[0] = 0.f;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) P[c8 + 1] = P[c8] + s8[c8];
-        const float thr = u01(p.rng.word(kDraftToken, b, k, bs)) * P[8];
-        int cs = 7;
-#pragma unroll
-        for (int c8 = 6; c8 >= 0; --c8)
-          if (P[c8 + 1] > thr) cs = c8;
-        float base = P[7], zc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) zc[i] = zb[56 + i];
-#pragma unroll
-        for (int c8 = 6; c8 >= 0; --c8)
-          if (cs == c8) {
-            base = P[c8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) zc[i] = zb[8 * c8 + i];
-          }
-        float a = 0.f;
-        int xi = -1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          a += __expf(zc[i] - bm);
-          if (xi < 0 && base + a > thr) {
-            xi = i;
-            bzx = zc[i];
-          }
-        }
+      if (any && set == wset) {
+        const float4 h0 = zl[0], h1 = zl[1];
+        const DrawPart d = draw_join(DrawPart{h0.x, h0.y, h0.z, __float_as_int(h0.w)},
+                                     DrawPart{h1.x, h1.y, h1.z, __float_as_int(h1.w)});
+        int xi = d.i1;
+        bzx = d.z1;
+        if (xi >= 0 && !(d.k1 - d.k2 > kScreenGap)) xi = draw_exact(zw, sw, p.rng, b, k, wbs * kBlk, &bzx);
         if (xi < 0) {
           raise_status(p.status, DSPARK_ENUMERIC);  // non-finite logits in the block
           *abort = 1;
         } else {
-          bx = bs * kBlk + 8 * cs + xi;
+          bx = wbs * kBlk + xi;
         }
       }
 
-      // ---- publish this set's best (block key, token) and its partials
-      // (max, sum exp, z of its token, its token)
+      // ---- publish the row's candidate (block key, token) and each set's
+      // partials (max, sum exp, z of its token, its token)
       if (valid && !*abort) {
         if (bx >= 0) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bx));
         // every set writes its slot every step (a set without blocks writes
@@ -730,6 +798,7 @@ int draft_tc_supported(const dspark_dims& d) {
   if (d.r % 64 != 0 || d.r > 256) return 0;
   if (d.V % 8 != 0) return 0;
   if (d.B > kTcRows * kMaxGroups) return 0;
+  if ((d.V + kBlk - 1) / kBlk > 65535) return 0;  // block indices are exchanged as 16-bit words
   return 1;
 }
 

@@ -2,23 +2,28 @@
 
 Parity rule: token ids, lengths, accepted counts and next anchors must be
 bit-exact, except at decisions the fp64 oracle calls too close to take in
-fp32 (margin < oracle.MARGIN); such "flagged" decisions are counted, and
-everything downstream of one in the same request is not compared. Draft
-probabilities, log-sum-exps and confidences must agree within 1e-4 relative.
+fp32 (margin < oracle.MARGIN); such "flagged" decisions are counted and must
+stay below 1e-4 of the decisions compared. At a flagged position whose
+outcome differs, the oracle adopts the GPU's choice and continues from it
+(teacher forcing), so one flag does not end the comparison of a request or a
+chained round. Draft probabilities, log-sum-exps and confidences must agree
+within 1e-4 relative.
 
-Expected flag rates. A Gumbel-max decision is flagged when its top two keys
-lie within MARGIN, about MARGIN per draw. The draft's token level is an
-inverse CDF: it is flagged when u times the block mass lies within MARGIN
-(relative) of either cumulative boundary of the drawn token, about
-2 * MARGIN per boundary that carries mass, i.e. up to ~1e-3 per draw for a
-block of 64 tokens (the oracle flags 2 of 260 draws on the 130 x 2 rows,
-V = 4104 shape). The checks allow a multiple of these rates, enough to
-catch a degenerate margin (everything flagged), not a statistical test.
+Expected flag rates. Every sample of the library is a two-level Gumbel-max
+(block, then token inside the block); a level's decision is flagged when its
+top two keys lie within MARGIN, which happens with probability about MARGIN
+per level (the gap has density near 1 at zero: for 64 equal weights the law
+is P(gap > t) = 64 / (1 + 63 e^t)), so about 2e-5 per draw. Accept tests are
+flagged within MARGIN of the ratio, about 1e-5 per test. Each test allows
+1e-4 of its decisions plus one stray flag (a sample of a few hundred draws
+shows one flag in about 1% of runs); the session's totals are printed at the
+end of the run.
 """
 
 from __future__ import annotations
 
 import dataclasses
+import os
 from typing import Dict, Optional, Sequence
 
 import numpy as np
@@ -42,8 +47,16 @@ PLAN_THETA_TOL_OWN_INPUT = 1e-5
 PLAN_CUT_TOL_OWN_INPUT = 1e-5
 
 
-DRAFT_FLAG_RATE = 1e-2     # per draft draw (inverse-CDF token level)
+DRAFT_FLAG_RATE = 1e-4     # per draft draw (two Gumbel-max levels)
 VERIFY_FLAG_RATE = 1e-4    # per verify decision (Gumbel keys, accept ratios)
+
+# per test: (kind, compared, flagged), collected for the end-of-run summary
+SESSION = []
+
+
+def _record(kind: str, compared: int, flagged: int) -> None:
+    name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    SESSION.append((name, kind, compared, flagged))
 
 
 @dataclasses.dataclass
@@ -84,30 +97,66 @@ def rel_close(a, b, rtol=RTOL) -> np.ndarray:
 
 
 def compare_draft(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Sequence[int]):
-    """Compare draft outputs request by request; returns (tally, set of clean requests)."""
+    """Compare draft outputs of the listed requests, position by position.
+
+    ``o`` should come from ``forced_draft`` (the oracle already adopted the
+    GPU's token at every flagged position where they differ); a flagged
+    position is counted, an unflagged one must match bit for bit. Returns
+    (tally, set of requests compared)."""
     t = Tally()
-    clean = set()
     for b in reqs:
-        ok = True
         for k in range(o["tokens"].shape[1]):
-            # lse_k and c_k depend on x_{k-1} only, which matched so far
+            # lse_k and c_k depend on x_{k-1} only, which both sides share
             assert rel_close(g["lse"][b, k], o["lse"][b, k]), ("lse", b, k, g["lse"][b, k], o["lse"][b, k])
             assert rel_close(g["conf"][b, k], o["conf"][b, k]), ("conf", b, k, g["conf"][b, k], o["conf"][b, k])
             if o["margin"][b, k] < oracle.MARGIN:
                 t.flagged += 1
-                ok = False
-                break
             assert g["tokens"][b, k] == o["tokens"][b, k], ("token", b, k, g["tokens"][b, k], o["tokens"][b, k],
                                                              o["margin"][b, k])
             assert rel_close(g["pd_tok"][b, k], o["pd_tok"][b, k]), ("pd", b, k, g["pd_tok"][b, k], o["pd_tok"][b, k])
             t.compared += 1
-        if ok:
-            clean.add(b)
-        else:
-            t.excluded_requests += 1
-    t.budget = DRAFT_FLAG_RATE * (t.compared + t.flagged)
-    t.slack = 3
-    return t, clean
+    t.budget = DRAFT_FLAG_RATE * t.compared
+    t.slack = 1
+    _record("draft", t.compared, t.flagged)
+    return t, set(reqs)
+
+
+def forced_draft(g: Dict[str, np.ndarray], draft_fn, reqs: Sequence[int]) -> Dict[str, np.ndarray]:
+    """The oracle's draft of ``reqs`` under teacher forcing.
+
+    ``draft_fn(reqs, force)`` runs the oracle (force: [B, gamma] int32, -1 =
+    draw). Wherever the oracle flags a position and its token differs from the
+    GPU's, it adopts the GPU's token there and drafts the rest of that
+    request again from it. A difference at an unflagged position is left in
+    place for ``compare_draft`` to report."""
+    reqs = list(reqs)
+    B, gamma = g["tokens"].shape
+    force = np.full((B, gamma), -1, np.int32)
+    od = draft_fn(reqs, None)
+    todo = reqs
+    while todo:
+        redo = []
+        for b in todo:
+            for k in range(gamma):
+                if od["tokens"][b, k] == g["tokens"][b, k]:
+                    continue
+                if od["margin"][b, k] < oracle.MARGIN and force[b, k] < 0:
+                    force[b, k] = g["tokens"][b, k]
+                    redo.append(b)
+                break
+        if redo:
+            o2 = draft_fn(redo, force)
+            for key in od:
+                od[key][redo] = o2[key][redo]
+        todo = redo
+    return od
+
+
+def check_draft(g: Dict[str, np.ndarray], draft_fn, reqs: Sequence[int]):
+    """forced_draft, then compare_draft; returns (tally, oracle outputs)."""
+    od = forced_draft(g, draft_fn, reqs)
+    t, _ = compare_draft(g, od, reqs)
+    return t, od
 
 
 def compare_verify(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Sequence[int]) -> Tally:
@@ -122,6 +171,7 @@ def compare_verify(g: Dict[str, np.ndarray], o: Dict[str, np.ndarray], reqs: Seq
             "next_anchor", b, g["next_anchor"][b], o["next_anchor"][b], o["resid"][b], o["smp_margin"][b])
         t.compared += 2
     t.budget = VERIFY_FLAG_RATE * (t.compared + t.flagged)
+    _record("verify", t.compared, t.flagged)
     return t
 
 

@@ -14,7 +14,7 @@ from speculative_decoding_head_gb300 import build
 from speculative_decoding_head_gb300.binding import Workspace
 from speculative_decoding_head_gb300.workloads import WORKLOADS, Workload, make_inputs
 
-from parity import compare_draft, gpu_np, np_inputs, rel_close, to_device
+from parity import check_draft, gpu_np, np_inputs, rel_close, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -46,10 +46,13 @@ def _check(wl, rnd=0, reqs=None):
     assert ws.last_launches == 1          # one persistent kernel
     simt, _ = _draft(wl, dev, "simt", wl.seed, rnd)
     reqs = range(wl.B) if reqs is None else reqs
-    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed, rnd,
-                      reqs=list(reqs))
+
+    def draft_fn(rq, force):
+        return oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed,
+                            rnd, reqs=rq, force=force)
+
     for name, g in (("tcgen05", tc), ("simt", simt)):
-        t, _ = compare_draft(g, od, reqs)
+        t, od = check_draft(g, draft_fn, reqs)
         t.check_rate()
     # the two GPU paths agree on every value the oracle compared
     rr = list(reqs)
@@ -80,11 +83,13 @@ def test_tc_prod_full_size_sampled():
     inp = make_inputs(wl, with_target=False)
     dev = to_device(inp)
     tc, _ = _draft(wl, dev, "tcgen05", wl.seed, 2)
-    reqs = [0, 1, 63, 64, 127]
     sub = np_inputs({k: inp[k] for k in ("W1", "W2")})
-    od = oracle.draft(inp["U"].numpy(), sub["W1"], sub["W2"], inp["anchor"].numpy(), inp["h"].numpy(),
-                      inp["w"].numpy(), inp["T"].numpy(), wl.seed, 2, reqs=reqs)
-    t, _ = compare_draft(tc, od, reqs)
+
+    def draft_fn(rq, force):
+        return oracle.draft(inp["U"].numpy(), sub["W1"], sub["W2"], inp["anchor"].numpy(), inp["h"].numpy(),
+                            inp["w"].numpy(), inp["T"].numpy(), wl.seed, 2, reqs=rq, force=force)
+
+    t, _ = check_draft(tc, draft_fn, range(wl.B))     # every request of the batch
     t.check_rate()
 
 

@@ -1,10 +1,10 @@
 """The RNN head's draft tail (eq. (6)) on the GPU against the oracle.
 
-Tokens are bit-exact up to the first position the oracle flags (the same
-margins as the Markov draft); pd_tok, lse and conf within 1e-4 relative; the
-head vector o_k within 2e-5 absolute (|o| < 1; its pre-activations are fp32
-sums of 2r + H terms) up to and including that position, since o_k depends on
-x_{k-1} and the state of the earlier positions only.
+Tokens are bit-exact except at positions the oracle flags (the same margins
+as the Markov draft), where it adopts the GPU's token and continues (teacher
+forcing); pd_tok, lse and conf within 1e-4 relative; the head vector o_k
+within 2e-5 absolute (|o| < 1; its pre-activations are fp32 sums of 2r + H
+terms) at every position.
 """
 
 import numpy as np
@@ -16,7 +16,7 @@ from speculative_decoding_head_gb300 import build
 from speculative_decoding_head_gb300.binding import Workspace
 from speculative_decoding_head_gb300.workloads import WORKLOADS, Workload, make_inputs, make_rnn_weights
 
-from parity import compare_draft, gpu_np, np_inputs, to_device
+from parity import check_draft, gpu_np, np_inputs, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -40,16 +40,16 @@ def _run(wl, rnd=0, reqs=None, path=None):
     assert ws.last_launches == (2 if wl.H > 0 else 0) + 3 * wl.gamma
     g = gpu_np({k: v for k, v in out.items() if k != "scratch"})
     reqs = list(range(wl.B)) if reqs is None else list(reqs)
-    o = oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
-                         wl.seed, rnd, reqs=reqs)
-    t, _ = compare_draft(g, o, reqs)
+
+    def draft_fn(rq, force):
+        return oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"],
+                                npi["T"], wl.seed, rnd, reqs=rq, force=force)
+
+    t, o = check_draft(g, draft_fn, reqs)
     t.check_rate()
     for b in reqs:
-        for k in range(wl.gamma):
-            d = np.abs(g["ovec"][b, k] - o["ovec"][b, k]).max()
-            assert d <= OVEC_ATOL, (b, k, d)
-            if o["margin"][b, k] < oracle.MARGIN:
-                break
+        d = np.abs(g["ovec"][b] - o["ovec"][b]).max()
+        assert d <= OVEC_ATOL, (b, d)
     return g, o, t
 
 
@@ -74,9 +74,9 @@ def test_rnn_draft_simt_block_pass():
     _run(_wl("rnn_small_simt", 6, 4, 4104, 64, 96), rnd=2, path="simt")
 
 
-def test_rnn_draft_full_size_sampled():
-    """The prod shape (B=128, gamma=5, V=129280, r=256, H=5120) on eight requests."""
-    _run(WORKLOADS["prod"], rnd=3, reqs=[0, 9, 31, 64, 77, 100, 126, 127])
+def test_rnn_draft_full_size():
+    """The prod shape (B=128, gamma=5, V=129280, r=256, H=5120), every request."""
+    _run(WORKLOADS["prod"], rnd=3)
 
 
 def test_rnn_head_differs_from_markov_head():
