@@ -82,6 +82,7 @@ def lib():
             l.orc_plan_capacity.argtypes = [i32, i32, P, P, P]
             l.orc_plan_capacity.restype = i32
             l.orc_plan_topk.argtypes = [i32, i32, P, i32, P, P]
+            l.orc_plan_theta_path.argtypes = [i32, i32, P, P, P]
             l.orc_survival.argtypes = [i32, i32, P, P]
             l.orc_verify.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32,
                                      P, P, P, P, P]
@@ -382,6 +383,17 @@ def plan_capacity(conf, sps):
     m = np.zeros(1, np.float64)
     K = lib().orc_plan_capacity(B, g, _p(c), _p(s), _p(m))
     return int(K), float(m[0])
+
+
+def plan_theta_path(conf, sps) -> np.ndarray:
+    """Theta_m = (B + sum of the m largest survival values) * SPS(B + m) for
+    m = 0 .. B*gamma: the path whose first maximum is the lagged capacity."""
+    c = _c(conf, np.float32)
+    B, g = c.shape
+    s = _c(sps, np.float64)
+    th = np.zeros(B * g + 1, np.float64)
+    lib().orc_plan_theta_path(B, g, _p(c), _p(s), _p(th))
+    return th
 
 
 def plan_topk(conf, K: int):

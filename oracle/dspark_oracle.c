@@ -480,6 +480,21 @@ int orc_plan_capacity(int B, int g, const float* conf, const double* sps, double
     return K;
 }
 
+/* Theta_m = (B + sum of the m largest a) * SPS(B + m) for m = 0 .. B*g, the
+   path the capacity search maximises (theta[B*g + 1]) */
+void orc_plan_theta_path(int B, int g, const float* conf, const double* sps, double* theta)
+{
+    orc_cand* c = sorted_candidates(B, g, conf);
+    const int M = B * g;
+    double tau = (double)B;
+    theta[0] = tau * sps[B];
+    for (int m = 1; m <= M; ++m) {
+        tau += c[m - 1].a;
+        theta[m] = tau * sps[B + m];
+    }
+    free(c);
+}
+
 /* lengths from the K best current candidates; margin = relative a gap at the cut
    (the Theta margin does not apply: the capacity K is given) */
 void orc_plan_topk(int B, int g, const float* conf, int K, int32_t* lengths, double* margin)

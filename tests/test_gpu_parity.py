@@ -2,8 +2,13 @@
 
 Sizes: small enough for the oracle to finish in seconds yet spanning many
 64-token blocks, a ragged last block, several 128-row groups; plus the
-benchmark workloads at full size on sampled requests (requests are
-independent in draft and verify, and keep their global random streams).
+benchmark workloads at full size, every request, each in its own planner mode
+(prod compact, long static, loaded lagged over chained rounds).
+
+Rounds are chained under teacher forcing: where the oracle flags a decision
+(a draw, a plan or a verify outcome too close to call in fp32) and the two
+sides differ, the oracle adopts the GPU's outcome and both continue from it,
+so every round of a chain is compared.
 """
 
 import numpy as np
@@ -16,7 +21,7 @@ from speculative_decoding_head_gb300.binding import Workspace
 from speculative_decoding_head_gb300.workloads import WORKLOADS, Workload, make_inputs, pack_rows
 
 from parity import (PLAN_CUT_TOL_OWN_INPUT, PLAN_THETA_TOL_OWN_INPUT, PLAN_THETA_TOL_SAME_INPUT, Tally,
-                    compare_draft, compare_verify, gpu_np, np_inputs, oracle_plan, pack_np, row_off_np,
+                    _record, check_draft, compare_verify, gpu_np, np_inputs, oracle_plan, pack_np, row_off_np,
                     run_gpu_round, to_device)
 
 pytestmark = pytest.mark.gpu
@@ -47,51 +52,87 @@ def _built():
     build.build()
 
 
-def _oracle_round(wl, npi, seed, rnd, anchor, lag_conf=None):
-    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], anchor, npi["h"], npi["w"], npi["T"], seed, rnd)
-    oL, pm = oracle_plan(wl, od["conf"].astype(np.float32), npi["sps"], lag_conf)
-    oP = pack_np(npi["P_full"], oL)
-    ov = oracle.verify(oP, row_off_np(oL), oL, anchor, od["tokens"], npi["U"], npi["W1"], npi["W2"], seed, rnd)
-    return od, oL, pm, ov
-
-
-@pytest.mark.parametrize("name", list(MID))
-def test_round_parity(name):
-    """End to end: each side drafts, plans and verifies on its own outputs."""
-    wl = MID[name]
+def chained_rounds(wl, rounds=None):
+    """Draft -> plan -> verify on both sides for ``rounds`` chained rounds of
+    every request. Each round starts from the previous round's next anchors;
+    the lagged planner's ring carries confidences across rounds on both
+    sides. Returns (tally, rounds compared, plans compared, plans flagged)."""
+    rounds = wl.rounds if rounds is None else rounds
     inp = make_inputs(wl)
     dev, npi = to_device(inp), np_inputs(inp)
     ws = Workspace.for_workload(wl)
     tally = Tally()
-    plan_checked = plan_flagged = 0
-    anchor_gpu = dev["anchor"].clone()
-    anchor_np = npi["anchor"].copy()
+    plan_checked = plan_flagged = done = 0
+    anchor = npi["anchor"].copy()
     confs = []
-    for rnd in range(wl.rounds):
-        g = run_gpu_round(ws, dev, wl.seed, rnd, anchor_gpu)
-        lag_conf = confs[rnd - wl.lag] if (wl.mode == "lagged" and rnd >= wl.lag) else None
-        od, oL, pm, ov = _oracle_round(wl, npi, wl.seed, rnd, anchor_np, lag_conf)
-        t, clean = compare_draft(g, od, range(wl.B))
+    for rnd in range(rounds):
+        g = run_gpu_round(ws, dev, wl.seed, rnd, torch.from_numpy(anchor).cuda())
+
+        def draft_fn(rq, force, anchor=anchor, rnd=rnd):
+            return oracle.draft(npi["U"], npi["W1"], npi["W2"], anchor, npi["h"], npi["w"], npi["T"], wl.seed, rnd,
+                                reqs=rq, force=force)
+
+        t, od = check_draft(g, draft_fn, range(wl.B))
         tally = tally.add(t)
-        if len(clean) == wl.B and not pm.flagged(PLAN_THETA_TOL_OWN_INPUT, PLAN_CUT_TOL_OWN_INPUT):
-            assert (g["lengths"] == oL).all(), (g["lengths"], oL, pm)
-            assert (g["row_off"] == row_off_np(oL)).all()
-            plan_checked += 1
-        else:
+        conf32 = od["conf"].astype(np.float32)
+        lag_conf = confs[rnd - wl.lag] if (wl.mode == "lagged" and rnd >= wl.lag) else None
+        oL, pm = oracle_plan(wl, conf32, npi["sps"], lag_conf)
+        if lag_conf is not None and pm.theta < PLAN_THETA_TOL_OWN_INPUT:
+            # The lagged capacity K = argmax Theta_m sits on a flat top: its
+            # best and runner-up Theta differ by less than the confidences'
+            # fp32 differences can move them. The GPU's K (its admitted
+            # count) must lie on that top; the oracle then adopts it and the
+            # top-K selection on the current confidences is compared exactly.
+            K_gpu = int((g["lengths"] - 1).sum())
+            th = oracle.plan_theta_path(lag_conf, npi["sps"])
+            assert th[K_gpu] >= th.max() * (1 - PLAN_THETA_TOL_OWN_INPUT), (rnd, K_gpu, int(th.argmax()))
+            oL, cut = oracle.plan_topk(conf32, K_gpu)
+            pm = oracle.PlanMargin(np.inf, cut)
+        if pm.flagged(PLAN_THETA_TOL_OWN_INPUT, PLAN_CUT_TOL_OWN_INPUT):
             plan_flagged += 1
-        # verify is per request given its rows: compare every clean request
-        # whose length both sides agree on
-        same = [b for b in sorted(clean) if g["lengths"][b] == oL[b]]
-        tally = tally.add(compare_verify(g, ov, same))
-        confs.append(od["conf"].astype(np.float32))
-        if len(same) < wl.B or not (g["next_anchor"] == ov["next_anchor"]).all():
-            break
-        # chain rounds: both sides continue from their (equal) next anchors
-        anchor_np = ov["next_anchor"].astype(np.int32)
-        anchor_gpu = torch.from_numpy(anchor_np).cuda()
+            L = g["lengths"]          # teacher forcing: the oracle adopts the GPU's lengths
+        else:
+            assert (g["lengths"] == oL).all(), (rnd, g["lengths"], oL, pm)
+            plan_checked += 1
+            L = oL
+        assert (g["row_off"] == row_off_np(L)).all()
+        _record("plan", 1, int(pm.flagged(PLAN_THETA_TOL_OWN_INPUT, PLAN_CUT_TOL_OWN_INPUT)))
+        ov = oracle.verify(pack_np(npi["P_full"], L), row_off_np(L), L, anchor, od["tokens"], npi["U"], npi["W1"],
+                           npi["W2"], wl.seed, rnd)
+        tally = tally.add(compare_verify(g, ov, range(wl.B)))
+        confs.append(conf32)
+        # both sides continue from the GPU's next anchors, which are the
+        # oracle's wherever its verify decisions were not flagged
+        anchor = g["next_anchor"].astype(np.int32)
+        done += 1
     tally.check_rate()
     assert tally.compared > 0
-    assert plan_checked + plan_flagged > 0
+    return tally, done, plan_checked, plan_flagged
+
+
+@pytest.mark.parametrize("name", list(MID))
+def test_round_parity(name):
+    """End to end: each side drafts, plans and verifies on its own outputs,
+    every round of the chain compared (for mid_lagged, rounds t >= lag use
+    the lagged capacity)."""
+    wl = MID[name]
+    _, done, checked, flagged = chained_rounds(wl)
+    assert done == wl.rounds
+    if wl.mode == "lagged":
+        assert done >= wl.lag + 2
+    assert checked + flagged == wl.rounds and checked >= wl.rounds - 1
+
+
+@pytest.mark.parametrize("name,rounds", [("prod", 1), ("long", 1), ("loaded", 4)])
+def test_full_size_rounds_in_own_mode(name, rounds):
+    """The benchmark workloads at full size in their own planner modes, every
+    request: prod compact (the planner on the head's own confidences, the
+    ragged verify packed by the GPU's lengths), long static (16 verify rows),
+    loaded lagged over four chained rounds (rounds 2 and 3 use the capacity
+    of the confidences two rounds back), with per-request target noise."""
+    wl = WORKLOADS[name]
+    _, done, checked, flagged = chained_rounds(wl, rounds)
+    assert done == rounds and checked >= rounds - 1
 
 
 def _rand_conf(B, g, seed):
@@ -135,34 +176,6 @@ def test_plan_static_and_flat():
     out = ws.plan(c, torch.full((21,), 400.0, dtype=torch.float64, device="cuda"))
     torch.cuda.synchronize()
     assert (out["lengths"].cpu() == 4).all()   # flat SPS table: full verify
-
-
-@pytest.mark.parametrize("name", ["prod", "long", "loaded"])
-def test_draft_and_verify_full_size_sampled(name):
-    """Full-size workload in the benchmark's launch configuration; the oracle
-    checks a few requests (static verify lengths so that both sides agree on
-    them without the oracle drafting every request)."""
-    wl = WORKLOADS[name].with_(mode="static")
-    inp = make_inputs(wl)
-    dev = to_device(inp)
-    ws = Workspace.for_workload(wl)
-    rnd = 3
-    g = run_gpu_round(ws, dev, wl.seed, rnd)
-    reqs = [0, wl.B // 2 + 1, wl.B - 1]
-    sub = {k: v for k, v in np_inputs({k: inp[k] for k in ("W1", "W2", "w", "T")}).items()}
-    U = inp["U"].numpy()
-    h = inp["h"].numpy()
-    anchor = inp["anchor"].numpy()
-    od = oracle.draft(U, sub["W1"], sub["W2"], anchor, h, sub["w"], sub["T"], wl.seed, rnd, reqs=reqs)
-    t, clean = compare_draft(g, od, reqs)
-    t.check_rate()
-    L = np.full(wl.B, wl.gamma + 1, np.int32)
-    ro = row_off_np(L)
-    P = inp["P_full"].numpy().reshape(-1, wl.V)
-    ok = sorted(clean)
-    ov = oracle.verify(P, ro, L, anchor, od["tokens"], U, sub["W1"], sub["W2"], wl.seed, rnd, reqs=ok)
-    compare_verify(g, ov, ok).check_rate()
-    del dev, inp
 
 
 def test_verify_stagewise_on_oracle_drafts():

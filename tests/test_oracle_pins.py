@@ -501,6 +501,10 @@ def test_appendix_a_planner_numbers():
         # the retrospective global argmax does look at c_2
         K, _ = oracle.plan_capacity(c, sps)
         assert K == g[case]["retrospective_drafts_verified"]
+        # the Theta path the capacity search maximises: the pages' Theta_0..2
+        path = oracle.plan_theta_path(c, sps)
+        assert np.allclose(path, [g["theta0"], g["theta1"], g[case]["theta2"]], atol=1e-6)
+        assert int(np.argmax(path)) == K
 
 
 def appendix_a_pipeline(N, planner, seed):
