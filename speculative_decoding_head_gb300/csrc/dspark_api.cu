@@ -94,7 +94,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_bar = carve(8 * sizeof(unsigned));
   const size_t o_sh = carve(sizeof(float) * BG);
   const size_t o_blk = carve(sizeof(float) * (size_t)d.B * geo.nblk);
-  const size_t o_ring = carve(d.mode == DSPARK_COMPACT_LAGGED ? sizeof(float) * (d.lag + 1) * BG : 0);
+  const size_t o_ring = carve(d.mode == DSPARK_COMPACT_LAGGED ? sizeof(int32_t) * (d.lag + 1) : 0);
   const size_t o_vpart = carve(sizeof(float4) * (size_t)geo.sweep_grid * geo.SL);
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
@@ -132,7 +132,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.barrier = reinterpret_cast<unsigned*>(base + o_bar);
   s.s_h = reinterpret_cast<float*>(base + o_sh);
   s.blk = reinterpret_cast<float*>(base + o_blk);
-  s.ring = reinterpret_cast<float*>(base + o_ring);
+  s.kring = reinterpret_cast<int32_t*>(base + o_ring);
   s.vpart = reinterpret_cast<float4*>(base + o_vpart);
   s.vflag = reinterpret_cast<int*>(base + o_vflag);
   s.vrow = reinterpret_cast<int*>(base + o_vrow);

@@ -72,7 +72,7 @@ struct Scratch {
   int* status;            // [1] first device error, 0 = none
   float* s_h;             // [B*gamma] hidden half of the confidence logit
   float* blk;             // [B*nblk] block log-masses of one draft step (SIMT path)
-  float* ring;            // [(lag+1)*B*gamma] confidence ring of the lagged planner
+  int32_t* kring;         // [lag+1] capacities of the lagged planner, by round mod (lag+1)
   uint32_t* plan_round;   // [1] rounds planned since the last reset
   float4* vpart;          // [sweep_grid*SL] verify-sweep partials (m, s, key, block)
   int* vflag;             // [B] 1 = next anchor comes from the residual
