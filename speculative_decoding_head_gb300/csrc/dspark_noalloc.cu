@@ -13,11 +13,15 @@
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds it (4 MiB) until the process exits. Host code may not pass
 // the array's name to a kernel (that name is only a host-side stand-in): the
-// device address is fetched with cudaGetSymbolAddress, once per device, with
-// that device current, by the first call made on that device, so make that
-// first call before any stream capture begins. All calls share the array and
-// it keeps the last call's contents: two calls whose kernels overlap on the
-// GPU race on it, so never issue calls on concurrent streams.
+// device address is fetched with cudaGetSymbolAddress, once per device and
+// context, with that device current, by the first call made there, so make
+// that first call before any stream capture begins. The address is cached
+// with the context it belongs to: after the device's primary context is
+// destroyed and recreated (cudaDeviceReset), the module is loaded again and
+// the next call fetches the new address. All calls share the array and it
+// keeps the last call's contents: two calls whose kernels overlap on the GPU
+// race on it, so never issue calls on concurrent streams.
+#include <cudaTypedefs.h>
 #include <mutex>
 #include <stdio.h>
 #include <string.h>
@@ -34,19 +38,42 @@ __device__ __align__(256) float g_noalloc_scratch[kNoAllocFloats];
 
 std::mutex g_mu;
 float* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library links
+// only the runtime)
+PFN_cuCtxGetCurrent_v4000 ctx_get_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  }
+  return fn;
+}
 
 float* scratch_for_current_device(int* dev_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   *dev_out = dev;
+  PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_get_current_fn();
+  if (!get_ctx) return nullptr;
+  CUcontext ctx = nullptr;  // null while this thread has no current context yet
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (ctx == nullptr || !g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
+    // the lookup also makes the device's primary context current
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      g_scratch_addr[dev] = nullptr;
       return nullptr;
     }
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
     g_scratch_addr[dev] = static_cast<float*>(p);
+    g_scratch_ctx[dev] = ctx;
   }
   return g_scratch_addr[dev];
 }
