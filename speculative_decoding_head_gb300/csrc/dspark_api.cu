@@ -275,11 +275,16 @@ dspark_status dspark_round(dspark_ws* ws, const float* U, const void* W1, const 
       dspark_markov_draft(ws, U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf, stream);
   if (s != DSPARK_OK) return s;
   const int l1 = ws->last_launches;
+  // within the round each kernel after the draft may start while the one
+  // before it drains: every input it reads before its in-kernel wait was
+  // written before the draft began
+  ws->pdl = 1;
   s = dspark_plan(ws, conf, sps, lengths, row_off, stream);
-  if (s != DSPARK_OK) return s;
   const int l2 = ws->last_launches;
-  s = dspark_verify(ws, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted,
-                    next_anchor, stream);
+  if (s == DSPARK_OK)
+    s = dspark_verify(ws, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted,
+                      next_anchor, stream);
+  ws->pdl = 0;
   ws->last_launches += l1 + l2;
   return s;
 }

@@ -200,6 +200,17 @@ __device__ __forceinline__ float hidden_dot128(const float* __restrict__ hr, con
   return (red[0] + red[1]) + (red[2] + red[3]);
 }
 
+// Programmatic dependent launch. Inside dspark_round the planner, the sweep
+// and the residual kernels are launched so that each may start while the
+// kernel before it drains (CUDA's programmatic stream serialization); such a
+// kernel calls pdl_wait() before it touches anything an earlier kernel of the
+// round writes, which returns once those kernels have completed and their
+// writes are visible. Launched without that attribute, pdl_wait() returns at
+// once. pdl_trigger() lets the next kernel of the round be scheduled as soon
+// as every CTA of this one has issued it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // First error wins; kernels poll it to stop early.
 __device__ __forceinline__ void raise_status(int* st, int code) { atomicCAS(st, 0, code); }
 

@@ -114,9 +114,28 @@ struct dspark_ws {
   dspark::Geometry geo;
   int use_tc;  // tensor-core draft and residual where geo.tc_ok / geo.resid_tc_ok hold
   int last_launches;
+  int pdl;     // set by dspark_round: the plan and verify kernels wait on the previous kernel in-kernel
 };
 
 namespace dspark {
+
+// Launch with programmatic stream serialization when `pdl` is set (the kernel
+// must call pdl_wait() before it reads what earlier kernels write).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Launchers: return cudaGetLastError() of their launches; add their launch
 // count to *launches.
@@ -145,7 +164,8 @@ size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch
 
 int resid_tc_supported(const dspark_dims& d);
 cudaError_t resid_tc_configure(dspark_ws* ws);
-cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st);
+cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st,
+                            bool pdl);
 // pass 0: per-CTA (max, sum exp) of z_d and z_t and z_d at x*; pass 1: per-CTA
 // sum |p_d - p_t| (needs lse_d, lse_t). Grid = ws->geo.num_sms.
 cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);

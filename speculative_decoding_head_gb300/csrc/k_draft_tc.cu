@@ -660,6 +660,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           *abort = 1;
         } else {
           bx = wbs * kBlk + xi;
+          // whichever CTA's candidate wins the row, its W1 row is gathered by
+          // every CTA after the barrier: start bringing it into L2 now
+          const char* w1row = reinterpret_cast<const char*>(W1 + (size_t)bx * p.r);
+          for (int o = 0; o < p.r * 2; o += 128) tc::prefetch_l2(w1row + o);
         }
       }
 
@@ -679,6 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- after the last step: per (row, step), one warp combines the
     // partials into the log-sum-exp, the drawn token's probability, and the
     // confidence c_k from W1[x_{k-1}]
+    pdl_trigger();  // the planner may be scheduled while this tail runs
     if (!aborted()) {
       const int nw = p.G * (kEpiThreads / 32);
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {

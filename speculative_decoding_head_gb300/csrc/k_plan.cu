@@ -324,6 +324,7 @@ __device__ __forceinline__ void plan_compact(const float* __restrict__ conf, con
   for (int n = 1 + t; n <= B + M; n += kPlanThreads)
     if (!(sps[n] > 0.0) || !isfinite(sps[n])) raise_status(status, DSPARK_ENUMERIC);
   const double sB = t == 0 ? __ldg(sps + B + M) : 0.0;  // Theta at m = M uses SPS(B + M)
+  pdl_wait();  // the confidences are the draft's
 
   const uint32_t rt = *plan_round;
   const bool lagged = mode == DSPARK_COMPACT_LAGGED;
@@ -415,6 +416,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   int* cnt = reinterpret_cast<int*>(smem_raw + (compact ? plan_cnt_offset(M) : 0));
   for (int b = threadIdx.x; b < B; b += blockDim.x) cnt[b] = 0;
   __syncthreads();
+  if (!compact) pdl_wait();  // lengths are written below
   if (compact) {
     switch (plan_mp(M) / kPlanThreads) {
       case 1: plan_compact<1>(conf, sps, B, g, mode, lag, kring, plan_round, cnt, smem_raw, status); break;
@@ -424,6 +426,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     }
   }
   // lengths and their exclusive scan row_off
+  pdl_trigger();  // the sweep may be scheduled while this tail runs
   {
     const int T = blockDim.x, per = (B + T - 1) / T, lo = threadIdx.x * per;
     int loc = 0;
@@ -469,11 +472,11 @@ cudaError_t plan_configure() {
 cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
                         int32_t* row_off, cudaStream_t st, int* launches) {
   const dspark_dims& d = ws->d;
-  k_plan<<<1, kPlanThreads, plan_smem_bytes(d), st>>>(conf, sps, d.B, d.gamma, (int)d.mode, d.lag,
-                                                     ws->s.kring, ws->s.plan_round, lengths, row_off,
-                                                     ws->s.status);
+  const cudaError_t e = launch_ex(k_plan, dim3(1), dim3(kPlanThreads), plan_smem_bytes(d), st, ws->pdl != 0, conf,
+                                  sps, d.B, d.gamma, (int)d.mode, d.lag, ws->s.kring, ws->s.plan_round, lengths,
+                                  row_off, ws->s.status);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace dspark

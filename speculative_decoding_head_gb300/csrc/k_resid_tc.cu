@@ -266,6 +266,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // the rejected requests, in request order (every CTA builds the same list).
   // The flags, positions and rows are this round's only if every stage so far
   // left the status clear: an error leaves the list empty.
+  pdl_wait();  // the verify flags are the sweep's
   if (warp == 2) {
     if constexpr (MODE == kModeResid) {
       const bool clear = __shfl_sync(0xFFFFFFFFu, *(volatile int*)p.status, 0) == 0;
@@ -854,7 +855,8 @@ RParams base_params(const dspark_ws* ws, int grid) {
 
 }  // namespace
 
-cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st) {
+cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rpart, int grid, cudaStream_t st,
+                            bool pdl) {
   const dspark_dims& d = ws->d;
   CUtensorMap tm;
   cudaError_t e = w2_tensor_map(d, a.W2, &tm);
@@ -873,8 +875,7 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.vlset = ws->s.vlset;
   p.rpart = rpart;
   const RSmem L = RSmem::make(d.r, false);
-  k_resid_tc<kModeResid><<<grid, kRThreads, L.total + 1024, st>>>(tm, tm, tm, p);
-  return cudaGetLastError();
+  return launch_ex(k_resid_tc<kModeResid>, dim3(grid), dim3(kRThreads), L.total + 1024, st, pdl, tm, tm, tm, p);
 }
 
 cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st) {

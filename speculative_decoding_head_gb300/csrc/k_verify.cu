@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(kBulkThreads)
                         float4* __restrict__ part, int* __restrict__ status, const FinArgs fin,
                         int* __restrict__ vdone) {
   extern __shared__ __align__(128) unsigned char smem[];
+  pdl_wait();  // row offsets and lengths are the planner's
   float* stage = reinterpret_cast<float*>(smem);
   float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
@@ -386,16 +387,45 @@ __global__ void __launch_bounds__(kBulkThreads)
     tc::fence_barrier_init();
     for (; issued < kBulkStages && issued < nchunks; ++issued) issue(issued);
   }
-  // request, position and bonus flag of each row the range touches
-  if (tid >= 32 && tid < 32 + nslots) {
-    const int q = q0 + tid - 32;
-    const int b = request_of_row(row_off, B, q);
-    const int j = q - row_off[b];
-    // the draft token the row tests (-1 on the last verified row; offsets
-    // and lengths are checked by CTA 0 meanwhile, so stay in bounds here)
-    const bool tested = j >= 0 && j < min(lengths[b], fin.g + 1) - 1;
-    const int xt = tested ? fin.tokens[(size_t)b * fin.g + j] : -1;
-    rowinfo[tid - 32] = make_int4(b, j, j == lengths[b] - 1 ? 1 : 0, xt >= 0 && xt < fin.V ? xt : -1);
+  // request, position and bonus flag of each row the range touches. Warp 1
+  // finds the requests by 32-way sampling of row_off (each round of loads
+  // narrows the request of row q0 to a 32nd of its interval) instead of a
+  // binary search's log2(B) dependent loads; the range's rows then belong to
+  // the next few requests, read in one more round.
+  if (tid >= 32 && tid < 64) {
+    const int lane = tid - 32;
+    int lo = 0, hi = B;  // the request of row q0 lies in [lo, hi)
+    while (hi - lo > 16) {
+      const int stride = (hi - lo + 31) / 32;
+      const int sidx = lo + lane * stride;
+      const int v = sidx < hi ? row_off[sidx] : INT_MAX;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, v <= q0);
+      const int L = m ? 31 - __clz((int)m) : 0;  // offsets that do not add up are reported by the last CTA
+      lo += L * stride;
+      hi = min(hi, lo + stride);
+    }
+    const int sidx = lo + lane;
+    const int v = sidx < B ? row_off[sidx] : INT_MAX;
+    int my_b = lo, my_ro = 0;
+    for (int i = 0; i < nslots; ++i) {
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, v <= q0 + i);
+      const int b = lo + (m ? 31 - __clz((int)m) : 0);
+      const int ro = __shfl_sync(0xFFFFFFFFu, v, b - lo);
+      if (lane == i) {
+        my_b = b;
+        my_ro = ro;
+      }
+    }
+    if (lane < nslots) {
+      const int b = min(max(my_b, 0), B - 1);
+      const int j = q0 + lane - my_ro;
+      // the draft token the row tests (-1 on the last verified row; offsets
+      // and lengths are checked by the last CTA meanwhile, so stay in bounds here)
+      const int ell = lengths[b];
+      const bool tested = j >= 0 && j < min(ell, fin.g + 1) - 1;
+      const int xt = tested ? fin.tokens[(size_t)b * fin.g + j] : -1;
+      rowinfo[lane] = make_int4(b, j, j == ell - 1 ? 1 : 0, xt >= 0 && xt < fin.V ? xt : -1);
+    }
   }
   for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
     slot[i] = make_float4(-INFINITY, 0.f, -INFINITY, __int_as_float(kNoIdx));
@@ -483,6 +513,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     return;
   }
   flush();
+  pdl_trigger();  // the residual pass may be scheduled while this tail runs
   __syncthreads();
   // reduce each row slot over the CTA's threads: warp w takes slots w, w + 4, ...
   const int warp = tid >> 5, lane = tid & 31;
@@ -595,6 +626,7 @@ __global__ void __launch_bounds__(kPickThreads)
   __shared__ KeyIdx red_k[kPickThreads / 32];
   __shared__ float zpart[kPickThreads / kBlockW][kBlockW];
   __shared__ int s_blk;
+  pdl_wait();  // the residual block keys are the previous kernel's
   const int b = blockIdx.x;
   // this round's flags only if every stage so far left the status clear (no
   // kernel running now writes the status, so every thread reads the same)
@@ -702,32 +734,39 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const FinArgs fin{a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma, d.V, geo.nblk,
                     geo.SL, geo.sweep_grid, rng, ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
                     ws->s.vlset, ws->s.status, geo.sweep_bulk ? ws->s.vpx : nullptr};
+  const bool pdl = ws->pdl != 0;
   if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
-    k_verify_sweep_bulk<<<geo.sweep_grid, kBulkThreads, sweep_bulk_smem_bytes(), st>>>(
-        a.P, a.row_off, a.lengths, d.B, geo.nblk, d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin,
-        ws->s.vdone);
+    const cudaError_t e = launch_ex(k_verify_sweep_bulk, dim3(geo.sweep_grid), dim3(kBulkThreads),
+                                    sweep_bulk_smem_bytes(), st, pdl, a.P, a.row_off, a.lengths, d.B, geo.nblk,
+                                    d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin, ws->s.vdone);
+    if (e != cudaSuccess) return e;
     *launches -= 1;
-  } else {
+  } else {  // ordinary launches (these kernels do not wait in-kernel)
     k_verify_sweep<<<geo.sweep_grid, kSweepThreads, 0, st>>>(a.P, a.row_off, a.lengths, d.B, d.V, geo.nblk,
                                                             d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart);
     k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(fin);
   }
+  const bool pdl_resid = pdl && geo.sweep_bulk;  // the residual kernels follow the bulk sweep
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
   if (BF16 && ws->use_tc && geo.resid_tc_ok && !a.ovec) {
     // residual block draw on tensor cores: one CTA per SM
     nchunk = geo.num_sms;
-    cudaError_t e = launch_resid_tc(ws, a, ws->s.rpart, nchunk, st);
+    cudaError_t e = launch_resid_tc(ws, a, ws->s.rpart, nchunk, st, pdl_resid);
     if (e != cudaSuccess) return e;
   } else {
     k_resid_blocks<BF16><<<dim3(kResidChunks, d.B), 256, smem, st>>>(
         a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, ws->s.vflag, a.n_acc,
         ws->s.vrow, ws->s.vlset, a.ovec, rng, ws->s.rpart, ws->s.status);
   }
-  k_resid_pick<BF16><<<d.B, kPickThreads, smem, st>>>(a.P, a.U, a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V,
-                                             d.r, geo.nblk, nchunk, ws->s.vflag, a.n_acc, ws->s.vrow,
-                                             ws->s.vlset, a.ovec, rng, ws->s.rpart, a.next_anchor, ws->s.status);
+  // after the SIMT block pass (an ordinary launch) the pick may still start
+  // early: it waits in-kernel
+  const cudaError_t e = launch_ex(k_resid_pick<BF16>, dim3(d.B), dim3(kPickThreads), smem, st, pdl_resid, a.P, a.U,
+                                  a.W1, a.W2, a.anchor, a.tokens, a.lse, d.gamma, d.V, d.r, geo.nblk, nchunk,
+                                  ws->s.vflag, a.n_acc, ws->s.vrow, ws->s.vlset, a.ovec, rng, ws->s.rpart,
+                                  a.next_anchor, ws->s.status);
   *launches += 4;
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
