@@ -101,6 +101,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_vlset = carve(sizeof(float) * d.B);
   const size_t o_vdone = carve(sizeof(int) * d.B);
   const size_t o_vpx = carve(sizeof(float) * (size_t)d.B * (d.gamma + 1));
+  const size_t o_rowtab = carve(sizeof(int4) * (size_t)d.B * (d.gamma + 1));
   geo.resid_tc_ok = resid_tc_supported(d);
   if (geo.resid_tc_ok && resid_tc_configure(ws) != cudaSuccess) geo.resid_tc_ok = 0;
   cudaGetLastError();
@@ -139,6 +140,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vlset = reinterpret_cast<float*>(base + o_vlset);
   s.vdone = reinterpret_cast<int*>(base + o_vdone);
   s.vpx = reinterpret_cast<float*>(base + o_vpx);
+  s.rowtab = reinterpret_cast<int4*>(base + o_rowtab);
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
   s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
@@ -221,32 +223,50 @@ dspark_status dspark_markov_draft(dspark_ws* ws, const float* U, const void* W1,
   return cuda_fail(e);
 }
 
-dspark_status dspark_plan(dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
-                          int32_t* row_off, dspark_stream_t stream) {
+namespace {
+
+dspark_status plan_call(dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths, int32_t* row_off,
+                        int4* rowtab, dspark_stream_t stream) {
   if (!ws) return DSPARK_EINVAL;
   if (!aligned16(lengths) || !aligned16(row_off)) return DSPARK_EINVAL;
   if (ws->d.mode != DSPARK_STATIC && (!aligned16(conf) || !aligned16(sps))) return DSPARK_EINVAL;
   int launches = 0;
-  cudaError_t e = launch_plan(ws, conf, sps, lengths, row_off, reinterpret_cast<cudaStream_t>(stream), &launches);
+  cudaError_t e =
+      launch_plan(ws, conf, sps, lengths, row_off, rowtab, reinterpret_cast<cudaStream_t>(stream), &launches);
   ws->last_launches = launches;
   return cuda_fail(e);
 }
 
-dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
-                            const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
-                            const float* U, const void* W1, const void* W2, uint64_t seed, uint64_t round,
-                            int32_t* n_accepted, int32_t* next_anchor, dspark_stream_t stream) {
+dspark_status verify_call(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
+                          const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
+                          const float* U, const void* W1, const void* W2, uint64_t seed, uint64_t round,
+                          int32_t* n_accepted, int32_t* next_anchor, const int4* rowtab, dspark_stream_t stream) {
   if (!ws) return DSPARK_EINVAL;
   if (!aligned16(P) || !aligned16(row_off) || !aligned16(lengths) || !aligned16(anchor) || !aligned16(tokens) ||
       !aligned16(pd_tok) || !aligned16(lse) || !aligned16(U) || !aligned16(W1) || !aligned16(W2) ||
       !aligned16(n_accepted) || !aligned16(next_anchor))
     return DSPARK_EINVAL;
   VerifyArgs a{P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted, next_anchor,
-               nullptr};
+               nullptr, rowtab};
   int launches = 0;
   cudaError_t e = launch_verify(ws, a, reinterpret_cast<cudaStream_t>(stream), &launches);
   ws->last_launches = launches;
   return cuda_fail(e);
+}
+
+}  // namespace
+
+dspark_status dspark_plan(dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
+                          int32_t* row_off, dspark_stream_t stream) {
+  return plan_call(ws, conf, sps, lengths, row_off, nullptr, stream);
+}
+
+dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
+                            const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
+                            const float* U, const void* W1, const void* W2, uint64_t seed, uint64_t round,
+                            int32_t* n_accepted, int32_t* next_anchor, dspark_stream_t stream) {
+  return verify_call(ws, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted,
+                     next_anchor, nullptr, stream);
 }
 
 dspark_status dspark_verify_rnn(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
@@ -259,7 +279,7 @@ dspark_status dspark_verify_rnn(dspark_ws* ws, const float* P, const int32_t* ro
       !aligned16(n_accepted) || !aligned16(next_anchor))
     return DSPARK_EINVAL;
   VerifyArgs a{P, row_off, lengths, anchor, tokens, pd_tok, lse, U, nullptr, W2, seed, round, n_accepted,
-               next_anchor, ovec};
+               next_anchor, ovec, nullptr};
   int launches = 0;
   cudaError_t e = launch_verify(ws, a, reinterpret_cast<cudaStream_t>(stream), &launches);
   ws->last_launches = launches;
@@ -279,11 +299,13 @@ dspark_status dspark_round(dspark_ws* ws, const float* U, const void* W1, const 
   // before it drains: every input it reads before its in-kernel wait was
   // written before the draft began
   ws->pdl = 1;
-  s = dspark_plan(ws, conf, sps, lengths, row_off, stream);
+  // the planner also writes each packed row's request and position, so the
+  // sweep reads them instead of searching the offsets
+  s = plan_call(ws, conf, sps, lengths, row_off, ws->s.rowtab, stream);
   const int l2 = ws->last_launches;
   if (s == DSPARK_OK)
-    s = dspark_verify(ws, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted,
-                      next_anchor, stream);
+    s = verify_call(ws, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed, round, n_accepted,
+                    next_anchor, ws->s.rowtab, stream);
   ws->pdl = 0;
   ws->last_launches += l1 + l2;
   return s;

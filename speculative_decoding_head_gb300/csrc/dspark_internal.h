@@ -42,6 +42,8 @@ struct VerifyArgs {
   int32_t* n_acc;
   int32_t* next_anchor;
   const float* ovec;  // [B][gamma][r] the RNN head's o_k (p_d from U + o W2), or null (Markov head)
+  const int4* rowtab;  // [rows] (b, j, lengths[b], row_off[b]) per packed row, written by this
+                       // round's planner (dspark_round), or null: the sweep looks the rows up
 };
 
 // The draft head's teacher-forced training objective: inputs, outputs and the
@@ -80,6 +82,7 @@ struct Scratch {
   float* vlset;           // [B] target log-sum-exp of that row
   int* vdone;             // [B] sweep ranges done per request (back to 0 by the finalizing CTA)
   float* vpx;             // [B*(gamma+1)] P at each verified row's draft token (bulk sweep)
+  int4* rowtab;           // [B*(gamma+1)] (b, j, lengths[b], row_off[b]) per packed row (dspark_round)
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
   float4* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
@@ -152,8 +155,9 @@ cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void*
                             float* ovec, int k, cudaStream_t st, int* launches);
 cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
                              float* ovec, cudaStream_t st, int* launches);
+// rowtab (may be null): also write each packed row's (b, j, lengths[b], row_off[b])
 cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
-                        int32_t* row_off, cudaStream_t st, int* launches);
+                        int32_t* row_off, int4* rowtab, cudaStream_t st, int* launches);
 cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t st, int* launches);
 
 // Whether the tcgen05 draft kernel supports these dims, and its launch shape.

@@ -407,7 +407,7 @@ __device__ __forceinline__ void plan_compact(const float* __restrict__ conf, con
 __global__ void __launch_bounds__(kPlanThreads)
     k_plan(const float* __restrict__ conf, const double* __restrict__ sps, int B, int g, int mode, int lag,
            int32_t* __restrict__ kring, uint32_t* __restrict__ plan_round, int32_t* __restrict__ lengths,
-           int32_t* __restrict__ row_off, int* __restrict__ status) {
+           int32_t* __restrict__ row_off, int4* __restrict__ rowtab, int* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int warp_int[32];
   const int M = B * g;
@@ -459,8 +459,11 @@ __global__ void __launch_bounds__(kPlanThreads)
     __syncthreads();
     int run = warp_int[warp] + (incl - loc);
     for (int b = lo; b < lo + per && b < B; ++b) {
+      const int l = mode == DSPARK_STATIC ? g + 1 : 1 + cnt[b];
       row_off[b] = run;
-      run += mode == DSPARK_STATIC ? g + 1 : 1 + cnt[b];
+      if (rowtab)
+        for (int j = 0; j < l; ++j) rowtab[run + j] = make_int4(b, j, l, run);
+      run += l;
     }
   }
 }
@@ -470,11 +473,11 @@ cudaError_t plan_configure() {
 }
 
 cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
-                        int32_t* row_off, cudaStream_t st, int* launches) {
+                        int32_t* row_off, int4* rowtab, cudaStream_t st, int* launches) {
   const dspark_dims& d = ws->d;
   const cudaError_t e = launch_ex(k_plan, dim3(1), dim3(kPlanThreads), plan_smem_bytes(d), st, ws->pdl != 0, conf,
                                   sps, d.B, d.gamma, (int)d.mode, d.lag, ws->s.kring, ws->s.plan_round, lengths,
-                                  row_off, ws->s.status);
+                                  row_off, rowtab, ws->s.status);
   ++*launches;
   return e;
 }

@@ -756,6 +756,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       asm volatile("bar.sync 2, 256;" ::: "memory");  // constants are rewritten by the next group
     }
   }
+  pdl_trigger();  // the token pick may be scheduled while this CTA finishes
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {

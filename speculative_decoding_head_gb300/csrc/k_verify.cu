@@ -170,7 +170,9 @@ struct FinArgs {
 // log-sum-exp from the sweep partials, p_t of draft x_{j+1} and the accept
 // test; the first rejection is the lowest failing lane. Then the bonus token
 // draw inside its block, or the hand-over to the residual pass.
-__device__ void finalize_request(int b, const FinArgs& f) {
+// ell = lengths[b], base = row_off[b], R = row_off[B] (clamped to the row
+// capacity), as the caller read them.
+__device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R) {
   const int lane = threadIdx.x & 31;
   const float* __restrict__ P = f.P;
   const int32_t* __restrict__ row_off = f.row_off;
@@ -188,10 +190,7 @@ __device__ void finalize_request(int b, const FinArgs& f) {
   float* __restrict__ vlset = f.vlset;
   int* __restrict__ status = f.status;
   if (lane == 0) vflag[b] = 0;  // no residual pass unless a rejection is found below
-  const int ell = lengths[b], base = row_off[b];
-  const int Rmax = B * (g + 1);
-  const int R = min(max(row_off[B], 0), Rmax);
-  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > R || anchor[b] < 0 || anchor[b] >= V) {
+  if (ell < 1 || ell > g + 1 || base < 0 || base + ell > R) {
     if (lane == 0) raise_status(status, DSPARK_ERANGE);
     return;
   }
@@ -306,7 +305,13 @@ __device__ __forceinline__ float resid_logw(float lpt, float lpd) {
 // One warp per request, after the register sweep.
 __global__ void __launch_bounds__(128) k_verify_finalize(const FinArgs f) {
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (b < f.B) finalize_request(b, f);
+  if (b >= f.B) return;
+  const int R = min(max(f.row_off[f.B], 0), f.B * (f.g + 1));
+  if (f.anchor[b] < 0 || f.anchor[b] >= f.V) {
+    if ((threadIdx.x & 31) == 0) raise_status(f.status, DSPARK_ERANGE);
+    return;
+  }
+  finalize_core(b, f, f.lengths[b], f.row_off[b], R);
 }
 
 // Bulk-copy sweep for V % 64 == 0: unit u is then tokens [64u, 64u + 64) of
@@ -329,21 +334,22 @@ int sweep_bulk_max_slots() { return kBulkMaxSlots; }
 
 size_t sweep_bulk_smem_bytes() {
   return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 64 +
-         (size_t)kBulkMaxSlots * 16;
+         (size_t)kBulkMaxSlots * (16 + 8);
 }
 
 __global__ void __launch_bounds__(kBulkThreads)
     k_verify_sweep_bulk(const float* __restrict__ P, const int32_t* __restrict__ row_off,
                         const int32_t* __restrict__ lengths, int B, int nblk, int Rmax, int SL, Rng rng,
                         float4* __restrict__ part, int* __restrict__ status, const FinArgs fin,
-                        int* __restrict__ vdone) {
+                        int* __restrict__ vdone, const int4* __restrict__ rowtab) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_wait();  // row offsets and lengths are the planner's
   float* stage = reinterpret_cast<float*>(smem);
   float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
                                                (size_t)kBulkMaxSlots * kBulkThreads * 16);
-  int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [kBulkMaxSlots]
+  int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [kBulkMaxSlots] (b, j, last row?, tested token)
+  int2* rowlen = reinterpret_cast<int2*>(rowinfo + kBulkMaxSlots);  // [kBulkMaxSlots] (lengths[b], row_off[b])
   // The finalize of a request whose rows no range covers never runs, so the
   // lengths, offsets and anchors of all requests are checked by one CTA.
   auto check_requests = [&]() {
@@ -387,12 +393,20 @@ __global__ void __launch_bounds__(kBulkThreads)
     tc::fence_barrier_init();
     for (; issued < kBulkStages && issued < nchunks; ++issued) issue(issued);
   }
-  // request, position and bonus flag of each row the range touches. Warp 1
-  // finds the requests by 32-way sampling of row_off (each round of loads
-  // narrows the request of row q0 to a 32nd of its interval) instead of a
-  // binary search's log2(B) dependent loads; the range's rows then belong to
-  // the next few requests, read in one more round.
-  if (tid >= 32 && tid < 64) {
+  // request, position and bonus flag of each row the range touches: from the
+  // planner's row table when it wrote one for this round; else warp 1 finds
+  // the requests by 32-way sampling of row_off (each round of loads narrows
+  // the request of row q0 to a 32nd of its interval) instead of a binary
+  // search's log2(B) dependent loads; the range's rows then belong to the
+  // next few requests, read in one more round.
+  if (rowtab && tid >= 32 && tid < 32 + nslots) {
+    const int4 t4 = rowtab[q0 + tid - 32];
+    const int b = min(max(t4.x, 0), B - 1), j = t4.y, ell = t4.z;
+    const bool tested = j >= 0 && j < min(ell, fin.g + 1) - 1;
+    const int xt = tested ? fin.tokens[(size_t)b * fin.g + j] : -1;
+    rowinfo[tid - 32] = make_int4(b, j, j == ell - 1 ? 1 : 0, xt >= 0 && xt < fin.V ? xt : -1);
+    rowlen[tid - 32] = make_int2(ell, t4.w);
+  } else if (!rowtab && tid >= 32 && tid < 64) {
     const int lane = tid - 32;
     int lo = 0, hi = B;  // the request of row q0 lies in [lo, hi)
     while (hi - lo > 16) {
@@ -425,6 +439,7 @@ __global__ void __launch_bounds__(kBulkThreads)
       const bool tested = j >= 0 && j < min(ell, fin.g + 1) - 1;
       const int xt = tested ? fin.tokens[(size_t)b * fin.g + j] : -1;
       rowinfo[lane] = make_int4(b, j, j == ell - 1 ? 1 : 0, xt >= 0 && xt < fin.V ? xt : -1);
+      rowlen[lane] = make_int2(ell, my_ro);
     }
   }
   for (int i = tid; i < nslots * kBulkThreads; i += kBulkThreads)
@@ -555,7 +570,7 @@ __global__ void __launch_bounds__(kBulkThreads)
         vdone[b] = 0;  // the last user: ready for the next launch
       }
     }
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) finalize_request(ri.x, fin);
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) finalize_core(ri.x, fin, rowlen[i].x, rowlen[i].y, R);
   }
 }
 
@@ -738,7 +753,8 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
     const cudaError_t e = launch_ex(k_verify_sweep_bulk, dim3(geo.sweep_grid), dim3(kBulkThreads),
                                     sweep_bulk_smem_bytes(), st, pdl, a.P, a.row_off, a.lengths, d.B, geo.nblk,
-                                    d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin, ws->s.vdone);
+                                    d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin, ws->s.vdone,
+                                    a.rowtab);
     if (e != cudaSuccess) return e;
     *launches -= 1;
   } else {  // ordinary launches (these kernels do not wait in-kernel)
