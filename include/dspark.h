@@ -294,6 +294,49 @@ dspark_status dspark_verify_rnn(dspark_ws* ws, const float* P, const int32_t* ro
                                 const float* U, const float* ovec, const void* W2, uint64_t seed, uint64_t round,
                                 int32_t* n_accepted, int32_t* next_anchor, dspark_stream_t stream);
 
+/*
+ * PCTree: the Markov head's draft made a tree ("DeepSeek-V4.1 模型结构（6）：
+ * 解码，DSpark", follow-up note "后续工作": the Markov head scores every child
+ * token under a parent, so candidate children are proposed per parent node
+ * and the most probable paths are kept within a fixed verify budget, with no
+ * retraining and no extra backbone pass).
+ *
+ * dspark_pctree_build grows, for every request b, a tree of N nodes besides
+ * the root best first: node 0 is anchor[b] (depth 0, log-probability 0);
+ * expanding a node with token x at depth k < gamma proposes its c most
+ * probable children under softmax(U[b, k] + W1[x] W2) (ties to the smaller
+ * token); the next node admitted is the best candidate so far (the higher path
+ * log-probability, then the smaller depth, parent index, token), and it is
+ * expanded in turn, until N nodes are in or no candidate is left. Outputs,
+ * each [B][N+1] with node i in admission order: tok int32, par int32 (parent
+ * node index, -1 for the root), dep int32, lp fp32 (path log-probability:
+ * the sum of log p_d along the path); slots past the last node hold -1 (lp:
+ * -inf). n_nodes [B] int32. 1 <= c <= 8, 1 <= N <= 64, V < 2^24, c <= V.
+ * scratch holds dspark_pctree_scratch_bytes(ws, c, N) bytes, 256-byte aligned
+ * (0 means unsupported dims). An anchor out of range sets DSPARK_ERANGE.
+ *
+ * dspark_pctree_verify walks each request's tree: P [B][N+1][V] fp32 holds
+ * the target's logits after each node's path (row i for node i). At a node,
+ * its children (par == node, in index order) are tried in turn, child i
+ * accepted when u < p(t_i) / (1 - the target probability of the children
+ * rejected before it), u uniform from the stream (purpose 8, j = node, index
+ * i); an accepted child becomes the node. With no child accepted the next
+ * anchor is drawn from the target with the tried children removed: the
+ * two-level Gumbel-max (purposes 9 and 10, j = node). Outputs: path
+ * [B][gamma+1] int32 (the accepted nodes, root first, -1 after the last),
+ * n_accepted [B] (accepted draft tokens), next_anchor [B]. V % 4 == 0 and
+ * ceil(V/64) * 4 + 128 KiB of shared memory must fit one CTA, else
+ * EUNSUPPORTED. Both calls are asynchronous on `stream`; all pointers are
+ * device pointers owned by the caller.
+ */
+size_t dspark_pctree_scratch_bytes(const dspark_ws* ws, int c, int N);
+dspark_status dspark_pctree_build(dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                  const int32_t* anchor, int c, int N, int32_t* tok, int32_t* par, int32_t* dep,
+                                  float* lp, int32_t* n_nodes, void* scratch, dspark_stream_t stream);
+dspark_status dspark_pctree_verify(dspark_ws* ws, const float* P, const int32_t* tok, const int32_t* par, int N,
+                                   uint64_t seed, uint64_t round, int32_t* path, int32_t* n_accepted,
+                                   int32_t* next_anchor, dspark_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -74,8 +74,8 @@ def lib():
             l.orc_draft.argtypes = [P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P]
             l.orc_verify_head.argtypes = [P, P, P, P, P, P, P, P, P, P, u64, u64, P, i32,
                                           P, P, P, P, P]
-            l.orc_pctree_build.argtypes = [P, P, P, P, P, i32, i32, P, P, P, P, P, P]
-            l.orc_pctree_verify.argtypes = [P, i32, P, P, P, u64, u64, P, P, P, P]
+            l.orc_pctree_build.argtypes = [P, P, P, P, P, i32, i32, P, i32, P, P, P, P, P, P]
+            l.orc_pctree_verify.argtypes = [P, i32, P, P, P, u64, u64, P, i32, P, P, P, P]
             l.orc_rnn_draft.argtypes = [P, P, P, P, P, P, P, P, P, u64, u64, P, i32, P, P, P, P, P, P, P]
             l.orc_plan_sync.argtypes = [i32, i32, P, P, P, P]
             l.orc_plan_sync.restype = i32
@@ -300,37 +300,43 @@ def rnn_draft(U, W1, W2, Wr, anchor, h, w, T, seed: int, rnd: int,
     return out
 
 
-def pctree_build(U, W1, W2, anchor, c: int, N: int) -> Dict[str, np.ndarray]:
+def pctree_build(U, W1, W2, anchor, c: int, N: int, reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """PCTree's draft tree (see ``orc_pctree_build``): U [B, gamma, V], W1, W2
     as for ``draft``; c children per parent, N nodes besides the root. Returns
-    tok, par, dep [B, N+1] int32, lp [B, N+1], n_nodes [B], margin [B]."""
+    tok, par, dep [B, N+1] int32, lp [B, N+1], n_nodes [B], margin [B] (only
+    the rows of ``reqs`` are written when it is given)."""
     U = _c(U, np.float32)
     B, g, V = U.shape
     w1, bf = _weights(W1)
     w2, _ = _weights(W2)
     d = _dims(B, g, V, w1.shape[1], 0, bf)
     an = _c(anchor, np.int32)
-    out = {"tok": np.zeros((B, N + 1), np.int32), "par": np.zeros((B, N + 1), np.int32),
-           "dep": np.zeros((B, N + 1), np.int32), "lp": np.zeros((B, N + 1)),
-           "n_nodes": np.zeros(B, np.int32), "margin": np.zeros(B)}
-    lib().orc_pctree_build(C.byref(d), _p(U), _p(w1), _p(w2), _p(an), int(c), int(N), _p(out["tok"]),
-                           _p(out["par"]), _p(out["dep"]), _p(out["lp"]), _p(out["n_nodes"]), _p(out["margin"]))
+    rq = _c(range(B) if reqs is None else reqs, np.int32)
+    out = {"tok": np.full((B, N + 1), -1, np.int32), "par": np.full((B, N + 1), -1, np.int32),
+           "dep": np.full((B, N + 1), -1, np.int32), "lp": np.full((B, N + 1), -np.inf),
+           "n_nodes": np.zeros(B, np.int32), "margin": np.full(B, np.inf)}
+    lib().orc_pctree_build(C.byref(d), _p(U), _p(w1), _p(w2), _p(an), int(c), int(N), _p(rq), rq.size,
+                           _p(out["tok"]), _p(out["par"]), _p(out["dep"]), _p(out["lp"]), _p(out["n_nodes"]),
+                           _p(out["margin"]))
     return out
 
 
-def pctree_verify(tok, par, P, gamma: int, seed: int, rnd: int) -> Dict[str, np.ndarray]:
+def pctree_verify(tok, par, P, gamma: int, seed: int, rnd: int,
+                  reqs: Optional[Sequence[int]] = None) -> Dict[str, np.ndarray]:
     """PCTree's lossless tree verify (see ``orc_pctree_verify``): tok, par
     [B, N+1] from ``pctree_build``, P [B, N+1, V] the target logits after each
-    node's path. Returns path [B, gamma+1], n_acc, next_anchor, margin [B]."""
+    node's path. Returns path [B, gamma+1], n_acc, next_anchor, margin [B]
+    (only the rows of ``reqs`` when it is given)."""
     tok = _c(tok, np.int32)
     par = _c(par, np.int32)
     P = _c(P, np.float32)
     B, N1, V = P.shape
     d = _dims(B, gamma, V, 0, 0, False)
-    out = {"path": np.zeros((B, gamma + 1), np.int32), "n_acc": np.zeros(B, np.int32),
-           "next_anchor": np.zeros(B, np.int32), "margin": np.zeros(B)}
-    lib().orc_pctree_verify(C.byref(d), N1 - 1, _p(tok), _p(par), _p(P), seed, rnd, _p(out["path"]),
-                            _p(out["n_acc"]), _p(out["next_anchor"]), _p(out["margin"]))
+    rq = _c(range(B) if reqs is None else reqs, np.int32)
+    out = {"path": np.full((B, gamma + 1), -1, np.int32), "n_acc": np.full(B, -1, np.int32),
+           "next_anchor": np.full(B, -1, np.int32), "margin": np.full(B, np.inf)}
+    lib().orc_pctree_verify(C.byref(d), N1 - 1, _p(tok), _p(par), _p(P), seed, rnd, _p(rq), rq.size,
+                            _p(out["path"]), _p(out["n_acc"]), _p(out["next_anchor"]), _p(out["margin"]))
     return out
 
 

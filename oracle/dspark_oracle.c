@@ -652,18 +652,21 @@ static int tcand_better(const orc_tcand* a, const orc_tcand* b)
 }
 
 /*
- * Per request b: tok, par, dep [b][N+1] (node 0 the root; -1 past the last
- * node), lp [b][N+1] the path log-probabilities; n_nodes[b] the nodes besides
- * the root (< N only when every path reaches depth gamma); margin[b] = the
- * smallest log-probability gap that decided an admission or a top-c choice.
+ * Per request b in reqs[0..n_req): tok, par, dep [b][N+1] (node 0 the root;
+ * -1 past the last node), lp [b][N+1] the path log-probabilities; n_nodes[b]
+ * the nodes besides the root (< N only when every path reaches depth gamma);
+ * margin[b] = the smallest log-probability gap that decided an admission or a
+ * top-c choice.
  */
 void orc_pctree_build(const orc_dims* d, const float* U, const void* W1, const void* W2,
-                      const int32_t* anchor, int c, int N, int32_t* tok, int32_t* par, int32_t* dep,
+                      const int32_t* anchor, int c, int N, const int32_t* reqs, int n_req,
+                      int32_t* tok, int32_t* par, int32_t* dep,
                       double* lp, int32_t* n_nodes, double* margin)
 {
     const long V = d->V, g = d->gamma;
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int b = 0; b < d->B; ++b) {
+    for (int q = 0; q < n_req; ++q) {
+        const int b = reqs[q];
         double* z = (double*)malloc(sizeof(double) * (size_t)V);
         orc_tcand* fr = (orc_tcand*)malloc(sizeof(orc_tcand) * (size_t)(N + 1) * (size_t)(c > 0 ? c : 1));
         int nf = 0;
@@ -724,18 +727,20 @@ void orc_pctree_build(const orc_dims* d, const float* U, const void* W1, const v
 
 /*
  * P holds [B][N+1][V] target logits, row i the target's distribution of the
- * token after node i's path. Outputs: path [b][gamma+1] the accepted nodes
+ * token after node i's path; the requests in reqs[0..n_req) are walked (their
+ * global indices keep their random streams). Outputs: path [b][gamma+1] the accepted nodes
  * (root first, -1 after the last), n_acc[b] the accepted draft tokens,
  * next_anchor[b], margin[b] = min |u - p| over the tests taken and the final
  * draw's key margin.
  */
 void orc_pctree_verify(const orc_dims* d, int N, const int32_t* tok, const int32_t* par, const float* P,
-                       uint64_t seed, uint64_t round, int32_t* path, int32_t* n_acc, int32_t* next_anchor,
-                       double* margin)
+                       uint64_t seed, uint64_t round, const int32_t* reqs, int n_req,
+                       int32_t* path, int32_t* n_acc, int32_t* next_anchor, double* margin)
 {
     const long V = d->V, g = d->gamma;
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int b = 0; b < d->B; ++b) {
+    for (int q = 0; q < n_req; ++q) {
+        const int b = reqs[q];
         double* lt = (double*)malloc(sizeof(double) * (size_t)V);
         double* pr = (double*)malloc(sizeof(double) * (size_t)V);
         const int32_t* tk = tok + (long)b * (N + 1);

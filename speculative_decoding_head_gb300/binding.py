@@ -25,6 +25,7 @@ SYMBOLS = [
     "dspark_markov_draft", "dspark_plan", "dspark_verify", "dspark_round", "dspark_ws_set_path",
     "dspark_sts_fit", "dspark_sts_scratch_bytes", "dspark_train_loss", "dspark_train_loss_scratch_bytes",
     "dspark_rnn_draft", "dspark_rnn_draft_scratch_bytes", "dspark_verify_rnn",
+    "dspark_pctree_scratch_bytes", "dspark_pctree_build", "dspark_pctree_verify",
 ]
 
 
@@ -93,6 +94,12 @@ def load() -> C.CDLL:
         lib.dspark_verify_rnn.restype = i32
         lib.dspark_rnn_draft_scratch_bytes.argtypes = [P]
         lib.dspark_rnn_draft_scratch_bytes.restype = C.c_size_t
+        lib.dspark_pctree_scratch_bytes.argtypes = [P, i32, i32]
+        lib.dspark_pctree_scratch_bytes.restype = C.c_size_t
+        lib.dspark_pctree_build.argtypes = [P] * 5 + [i32, i32] + [P] * 7
+        lib.dspark_pctree_build.restype = i32
+        lib.dspark_pctree_verify.argtypes = [P] * 4 + [i32, u64, u64] + [P] * 4
+        lib.dspark_pctree_verify.restype = i32
         _lib = lib
         return lib
 
@@ -269,6 +276,45 @@ class Workspace:
             _ptr(out["lse"], f32, "lse"), _ptr(out["conf"], f32, "conf"), _ptr(out["ovec"], f32, "ovec"),
             _ptr(out["scratch"], None, "scratch"), _stream(stream))
         _check(code, "dspark_rnn_draft")
+        return out
+
+    def pctree_build(self, U, W1, W2, anchor, c: int, N: int, out=None, stream=None):
+        """PCTree's draft tree (``dspark_pctree_build``): tok, par, dep [B, N+1]
+        int32, lp [B, N+1] fp32, n_nodes [B] int32."""
+        B = self.dims.B
+        if out is None:
+            dev = U.device
+            nbytes = int(self.lib.dspark_pctree_scratch_bytes(self._h, int(c), int(N)))
+            if nbytes == 0:
+                raise DsparkError(f"dspark_pctree_build: unsupported c={c}, N={N}")
+            out = {k: torch.empty(B, N + 1, dtype=torch.int32, device=dev) for k in ("tok", "par", "dep")}
+            out["lp"] = torch.empty(B, N + 1, dtype=torch.float32, device=dev)
+            out["n_nodes"] = torch.empty(B, dtype=torch.int32, device=dev)
+            out["scratch"] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        f32, i32 = torch.float32, torch.int32
+        code = self.lib.dspark_pctree_build(
+            self._h, _ptr(U, f32, "U"), _ptr(W1, self.wdtype, "W1"), _ptr(W2, self.wdtype, "W2"),
+            _ptr(anchor, i32, "anchor"), int(c), int(N), _ptr(out["tok"], i32, "tok"), _ptr(out["par"], i32, "par"),
+            _ptr(out["dep"], i32, "dep"), _ptr(out["lp"], f32, "lp"), _ptr(out["n_nodes"], i32, "n_nodes"),
+            _ptr(out["scratch"], None, "scratch"), _stream(stream))
+        _check(code, "dspark_pctree_build")
+        return out
+
+    def pctree_verify(self, P, tok, par, N: int, seed: int, rnd: int, out=None, stream=None):
+        """PCTree's lossless tree verify (``dspark_pctree_verify``): P [B, N+1, V]
+        fp32. Returns path [B, gamma+1], n_acc [B], next_anchor [B] (int32)."""
+        B, g = self.dims.B, self.dims.gamma
+        if out is None:
+            dev = P.device
+            out = {"path": torch.empty(B, g + 1, dtype=torch.int32, device=dev),
+                   "n_acc": torch.empty(B, dtype=torch.int32, device=dev),
+                   "next_anchor": torch.empty(B, dtype=torch.int32, device=dev)}
+        i32 = torch.int32
+        code = self.lib.dspark_pctree_verify(
+            self._h, _ptr(P, torch.float32, "P"), _ptr(tok, i32, "tok"), _ptr(par, i32, "par"), int(N), int(seed),
+            int(rnd), _ptr(out["path"], i32, "path"), _ptr(out["n_acc"], i32, "n_acc"),
+            _ptr(out["next_anchor"], i32, "next_anchor"), _stream(stream))
+        _check(code, "dspark_pctree_verify")
         return out
 
     def verify_rnn(self, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, ovec, W2, seed: int, rnd: int,

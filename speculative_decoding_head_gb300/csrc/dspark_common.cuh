@@ -26,6 +26,9 @@ enum : uint32_t {
   kBonusToken = 5,
   kResidBlock = 6,
   kResidToken = 7,
+  kTreeAccept = 8,  // PCTree: accept test of child i at a node (j = node, v = i)
+  kTreeBlock = 9,   // PCTree: the next anchor's block and token draws (j = node)
+  kTreeToken = 10,
 };
 
 // Width of the vocabulary blocks of the two-level sampler: a block is drawn

@@ -178,6 +178,22 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
 cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
                                  cudaStream_t st);
 
+// PCTree (k_pctree.cu): the best-first draft tree of N nodes with c children
+// per expansion, and its lossless verify.
+constexpr int kTreeMaxChildren = 8;
+constexpr int kTreeMaxNodes = 64;
+size_t tree_scratch_bytes(const dspark_dims& d, int nblk, int c, int N);
+size_t tree_verify_smem_bytes(int nblk);
+cudaError_t launch_pctree_build(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                const int32_t* anchor, int c, int N, int32_t* tok, int32_t* par, int32_t* dep,
+                                float* lp, int32_t* n_nodes, void* scratch, cudaStream_t st, int* launches);
+cudaError_t launch_pctree_verify(const dspark_ws* ws, const float* P, const int32_t* tok, const int32_t* par, int N,
+                                 uint64_t seed, uint64_t round, int32_t* path, int32_t* n_acc, int32_t* next_anchor,
+                                 cudaStream_t st, int* launches);
+cudaError_t launch_tree_blocks_tc(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                  const int32_t* tok, const int32_t* dep, const int4* state, int N, float* blk,
+                                  float* bmax, cudaStream_t st);
+
 size_t plan_smem_bytes(const dspark_dims& d);
 cudaError_t sweep_bulk_configure();
 int sweep_bulk_max_slots();  // rows one CTA range of the bulk sweep may span

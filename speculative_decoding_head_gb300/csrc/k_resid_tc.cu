@@ -70,6 +70,8 @@ constexpr int kModeLossStats = 1;  // per column: (max, sum exp) of z_d and of z
 constexpr int kModeLossL1 = 2;     // per column: sum |p_d - p_t| over the CTA's tiles
 constexpr int kModeDraft = 3;      // per column (request) and 64-token block: log sum exp z of one draft step
                                    // of the RNN head, z = U_k + o_k W2 with o_k split into bf16 hi + lo parts
+constexpr int kModeTree = 4;       // per column (request) and 64-token block: log sum exp z and max z of the
+                                   // expansion of a PCTree node, z = U[b, depth] + W1[token] W2
 
 struct RSmem {
   uint32_t bop, w2, up, stage, col, part, best, gum, list, bars, misc, total;
@@ -119,6 +121,12 @@ struct RParams {
   int step;              // k (1-based)
   float* blk;            // [B][nblk] block log-masses
   int nblk;
+  // one expansion step of PCTree: column b expands node state[b].y of its tree
+  const int32_t* tree_tok;  // [B][N+1] node tokens
+  const int32_t* tree_dep;  // [B][N+1] node depths
+  const int4* tree_state;   // [B] (nodes admitted, node to expand, frontier size, done)
+  int tree_N;
+  float* bmax;              // [B][nblk] block maxima of z
 };
 
 // Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         base += __popc(m);
       }
       if (lane == 0) *s_nrej = base;
-    } else if constexpr (MODE == kModeDraft) {
+    } else if constexpr (MODE == kModeDraft || MODE == kModeTree) {
       if (lane == 0) *s_nrej = p.B;  // every request is a column
     } else {
       if (lane == 0) *s_nrej = p.B * p.g;  // every position is a column
@@ -342,6 +350,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
           const int b = list[gq * kRN + lane];
           urow = p.U + ((size_t)b * p.g + min(max(p.n_acc[b], 0), p.g - 1)) * p.V;
           prow = p.P + (size_t)min(max(p.vrow[b], 0), p.B * (p.g + 1) - 1) * p.V;
+        } else if constexpr (MODE == kModeTree) {  // U of the expanded node's depth
+          const int b = gq * kRN + lane;
+          const int node = min(max(p.tree_state[b].y, 0), p.tree_N);
+          const int d = min(max(p.tree_dep[(size_t)b * (p.tree_N + 1) + node], 0), p.g - 1);
+          urow = p.U + ((size_t)b * p.g + d) * p.V;
         } else {  // position i of the objective: U row i, target logits row i
           urow = p.U + (size_t)(gq * kRN + lane) * p.V;
           prow = p.P + (size_t)(gq * kRN + lane) * p.V;
@@ -362,6 +375,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
             tc::bulk_load(dst, urow + v0, bytes, up_full(us));
             tc::bulk_load(dst + kRM * 4, prow + v0, bytes, up_full(us));
           }
+        } else if constexpr (MODE == kModeTree) {  // the residual's layout, U slices only
+          if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), bytes * (uint32_t)ncols);
+          __syncwarp();
+          if (lane < ncols) tc::bulk_load(sUP + us * L.stage + lane * (2 * kRM * 4), urow + v0, bytes, up_full(us));
         } else if (MODE == kModeDraft && lane == 0) {
           // U_k of the group's 32 requests: one [32 x 128] box of the
           // tensor map whose rows are the requests (stride gamma V)
@@ -458,6 +475,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
           } else if constexpr (MODE == kModeDraft) {
             col_b[et] = i;  // request i; its B row is o_k, not a W1 row
             x = i;
+          } else if constexpr (MODE == kModeTree) {  // request i expands its node state.y
+            const int node = min(max(p.tree_state[i].y, 0), p.tree_N);
+            x = p.tree_tok[(size_t)i * (p.tree_N + 1) + node];
+            col_b[et] = i;
           } else {  // teacher forcing: position k drafts from x*_{k-1} (the anchor at k = 0)
             const int b = i / p.g, k = i - b * p.g;
             x = k == 0 ? p.anchor[b] : p.xstar[i - 1];
@@ -611,13 +632,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
             float uu[16], pp[16];
             // stage layout: per request [U slice | P slice] (residual), or
             // [32 rows of U][32 rows of P] (the loss modes' two boxes)
-            constexpr uint32_t kRow = MODE == kModeResid ? 2 * kRM * 4 : kRM * 4;
+            constexpr uint32_t kRow = (MODE == kModeResid || MODE == kModeTree) ? 2 * kRM * 4 : kRM * 4;
             constexpr uint32_t kPOff = MODE == kModeResid ? kRM * 4 : kRN * kRM * 4;
             const uint32_t su = sUP + us * L.stage + (uint32_t)(half * 16) * kRow + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               asm volatile("ld.shared.f32 %0, [%1];" : "=f"(uu[j]) : "r"(su + j * kRow));
-              if constexpr (MODE != kModeDraft)
+              if constexpr (MODE != kModeDraft && MODE != kModeTree)
                 asm volatile("ld.shared.f32 %0, [%1];" : "=f"(pp[j]) : "r"(su + j * kRow + kPOff));
             }
             if constexpr (MODE == kModeLossStats) {
@@ -632,7 +653,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
                 online_add(ra[j], rb[j], ok ? zd * tc::kLog2e : -INFINITY);
                 online_add(rc[j], rd[j], ok ? pp[j] * tc::kLog2e : -INFINITY);
               }
-            } else if constexpr (MODE == kModeDraft) {
+            } else if constexpr (MODE == kModeDraft || MODE == kModeTree) {
               // per column, over this warp's 32 entries (half of a 64-token
               // block): max and sum exp of z = D + U (a transpose-max, the
               // columns' maxima broadcast, then a transpose-sum)
@@ -679,7 +700,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(t_empty(ab));
         }
-        if constexpr (MODE == kModeDraft) {
+        if constexpr (MODE == kModeDraft || MODE == kModeTree) {
           asm volatile("bar.sync 2, 256;" ::: "memory");
           // block 2t from quarters 0, 1 and block 2t + 1 from quarters 2, 3
           if (live && et < 2 * ncols) {
@@ -691,6 +712,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
               float lm = -INFINITY;
               if (m > -INFINITY) lm = m + logf(p0.y * __expf(p0.x - m) + p1.y * __expf(p1.x - m));
               p.blk[(size_t)col_b[col] * p.nblk + sblk] = lm;
+              if constexpr (MODE == kModeTree) p.bmax[(size_t)col_b[col] * p.nblk + sblk] = m;
             }
           }
           asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
@@ -795,6 +817,8 @@ cudaError_t resid_tc_configure(dspark_ws* ws) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_resid_tc<kModeDraft>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(RSmem::make(ws->d.r, true).total + 1024));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_resid_tc<kModeTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_resid_tc<kModeResid>, kRThreads, smem);
@@ -924,6 +948,32 @@ cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void
   p.nblk = ws->geo.nblk;
   const RSmem L = RSmem::make(d.r, true);
   k_resid_tc<kModeDraft><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tu, p);
+  return cudaGetLastError();
+}
+
+// One expansion step of PCTree: for every request b, blk[b][s] and bmax[b][s]
+// are the log-mass and the maximum of z = U[b, depth] + W1[token] W2 over
+// 64-token block s, (token, depth) those of node state[b].y. Grid = one CTA
+// per SM.
+cudaError_t launch_tree_blocks_tc(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                  const int32_t* tok, const int32_t* dep, const int4* state, int N, float* blk,
+                                  float* bmax, cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  CUtensorMap tm;
+  cudaError_t e = w2_tensor_map(d, W2, &tm);
+  if (e != cudaSuccess) return e;
+  RParams p = base_params(ws, ws->geo.num_sms);
+  p.U = U;
+  p.W1 = W1;
+  p.tree_tok = tok;
+  p.tree_dep = dep;
+  p.tree_state = state;
+  p.tree_N = N;
+  p.blk = blk;
+  p.bmax = bmax;
+  p.nblk = ws->geo.nblk;
+  const RSmem L = RSmem::make(d.r, false);
+  k_resid_tc<kModeTree><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tm, tm, p);
   return cudaGetLastError();
 }
 

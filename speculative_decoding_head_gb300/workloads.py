@@ -209,6 +209,32 @@ def make_loss_inputs(wl: Workload, seed_offset: int = 104729) -> Dict[str, torch
             "conf": (0.02 + 0.96 * torch.rand(B, g, generator=gen)).to(torch.float32)}
 
 
+def make_tree_targets(wl: Workload, U: torch.Tensor, dep: torch.Tensor, sigma: float = 0.5,
+                      seed_offset: int = 7727) -> torch.Tensor:
+    """Target logits of a draft tree's nodes, P [B, N+1, V] fp32 (CPU).
+
+    Row i of request b is the target's distribution of the token after node
+    i's path. As for the chain (module docstring), it is drawn as the base
+    logits of the position that token takes, U[b, dep[b, i]], plus
+    N(0, sigma^2) noise; a node at depth gamma is followed by the bonus
+    position, a fresh U-distributed draw plus noise; empty node slots
+    (dep < 0) are zeros.
+    """
+    gen = torch.Generator().manual_seed(wl.seed + seed_offset)
+    B, N1 = dep.shape
+    g, V = wl.gamma, wl.V
+    P = torch.zeros(B, N1, V, dtype=torch.float32)
+    d = dep.to(torch.int64).cpu()
+    for b in range(B):
+        for i in range(N1):
+            k = int(d[b, i])
+            if k < 0:
+                continue
+            base = U[b, k] if k < g else torch.randn(V, generator=gen) * wl.u_std
+            P[b, i] = base + torch.randn(V, generator=gen) * sigma
+    return P
+
+
 def pack_rows(P_full: torch.Tensor, lengths: torch.Tensor) -> torch.Tensor:
     """Packed ragged target logits [sum(lengths), V]: rows 0..lengths[b]-1 of each request.
 
