@@ -73,13 +73,20 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   geo.nblk = (d.V + kBlockW - 1) / kBlockW;
   geo.sweep_bulk = (d.V % kBlockW) == 0 && sweep_bulk_configure() == cudaSuccess;
   cudaGetLastError();
-  // the bulk sweep keeps a fixed number of row slots per CTA: rounds with more
-  // verified rows per CTA range take the register sweep
-  if (geo.sweep_bulk && (d.B * (d.gamma + 1) + 2 * geo.num_sms - 1) / (2 * geo.num_sms) + 2 > sweep_bulk_max_slots())
+  // The bulk sweep keeps per-thread partials of every row its range touches
+  // (a range of ceil(R nblk / grid) blocks touches at most ceil(R / grid) + 1
+  // rows). Two CTAs per SM (a 96 KB ring each) while that is at most 8 rows;
+  // else one CTA per SM with up to 32 rows; beyond, the register sweep.
+  const int Rmax = d.B * (d.gamma + 1);
+  if (geo.sweep_bulk && (Rmax + 2 * geo.num_sms - 1) / (2 * geo.num_sms) + 2 <= 8) {
+    geo.sweep_grid = 2 * geo.num_sms;
+  } else if (geo.sweep_bulk && (Rmax + geo.num_sms - 1) / geo.num_sms + 2 <= sweep_bulk_max_slots()) {
+    geo.sweep_grid = geo.num_sms;
+  } else {
     geo.sweep_bulk = 0;
-  geo.sweep_grid = geo.num_sms * (geo.sweep_bulk ? 2 : 4);  // bulk: 2 x 96 KB ring per SM
-  // a range of ceil(R*nblk/grid) blocks touches at most ceil(R/grid) + 1 rows
-  geo.SL = (d.B * (d.gamma + 1) + geo.sweep_grid - 1) / geo.sweep_grid + 2;
+    geo.sweep_grid = 4 * geo.num_sms;
+  }
+  geo.SL = (Rmax + geo.sweep_grid - 1) / geo.sweep_grid + 2;
   geo.tc_ok = draft_tc_supported(d);
 
   const size_t BG = (size_t)d.B * d.gamma;

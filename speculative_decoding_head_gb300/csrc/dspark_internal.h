@@ -197,6 +197,7 @@ cudaError_t launch_tree_blocks_tc(const dspark_ws* ws, const float* U, const voi
 size_t plan_smem_bytes(const dspark_dims& d);
 cudaError_t sweep_bulk_configure();
 int sweep_bulk_max_slots();  // rows one CTA range of the bulk sweep may span
+size_t sweep_bulk_smem_bytes(int SL);
 cudaError_t plan_configure();
 
 }  // namespace dspark

@@ -40,7 +40,8 @@
 namespace dspark {
 
 constexpr int kTreeMaxC = kTreeMaxChildren;  // children per expanded node
-constexpr int kPickT = 256;    // k_tree_pick threads
+constexpr int kPickT = 1024;   // k_tree_pick threads
+constexpr int kPickKG = kPickT / kBlockW;  // K slices of the z recompute (16)
 
 struct TreeScratch {
   int4* state;       // [B] (nodes admitted n, node to expand, frontier size, done)
@@ -213,6 +214,9 @@ __global__ void __launch_bounds__(kPickT)
   __shared__ int s_blk[kTreeMaxC];
   __shared__ float cz[kTreeMaxC * kBlockW];  // z of the candidate tokens
   __shared__ int cv[kTreeMaxC * kBlockW];
+  __shared__ float zp[kPickKG][kTreeMaxC * kBlockW];  // K-slice partial sums of the recompute
+  __shared__ float wl_v[kPickT / 32][kTreeMaxC];        // each warp's best blocks
+  __shared__ int wl_i[kPickT / 32][kTreeMaxC];
   __shared__ float4 red_c[kPickT / 32];
   __shared__ int red_i[kPickT / 32];
   __shared__ float s_L;
@@ -232,8 +236,9 @@ __global__ void __launch_bounds__(kPickT)
     for (int s = tid; s < nblk; s += kPickT) ms = ms_combine(ms, MS{blk[(size_t)b * nblk + s], 1.f});
     ms = warp_ms(ms);
     if (lane == 0) red_ms[warp] = ms;
-    // the c blocks with the largest maxima (warp 0)
-    if (warp == 0) {
+    // the c blocks with the largest maxima: every warp its own best c, then
+    // warp 0 merges the warps' lists (each lane one warp's)
+    {
       float lv[kTreeMaxC];
       int li[kTreeMaxC];
 #pragma unroll
@@ -241,9 +246,28 @@ __global__ void __launch_bounds__(kPickT)
         lv[j] = -INFINITY;
         li[j] = -1;
       }
-      for (int s = lane; s < nblk; s += 32) {
+      for (int s = tid; s < nblk; s += kPickT) {
         const float m = bmax[(size_t)b * nblk + s];
         if (m > -INFINITY) list_insert(lv, li, m, s);
+      }
+      float ov[kTreeMaxC];
+      int oi[kTreeMaxC];
+      warp_merge_top(lv, li, c, ov, oi);
+      if (lane == 0)
+#pragma unroll
+        for (int t = 0; t < kTreeMaxC; ++t) {
+          wl_v[warp][t] = ov[t];
+          wl_i[warp][t] = oi[t];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float lv[kTreeMaxC];
+      int li[kTreeMaxC];
+#pragma unroll
+      for (int t = 0; t < kTreeMaxC; ++t) {
+        lv[t] = wl_v[lane][t];
+        li[t] = wl_i[lane][t];
       }
       float ov[kTreeMaxC];
       int oi[kTreeMaxC];
@@ -255,28 +279,41 @@ __global__ void __launch_bounds__(kPickT)
           if (t == lane) pick = oi[t];
         s_blk[lane] = pick;
       }
+      if (lane == 0) {
+        MS m2 = red_ms[0];
+        for (int i = 1; i < kPickT / 32; ++i) m2 = ms_combine(m2, red_ms[i]);
+        s_L = ms_log(m2);
+      }
     }
     __syncthreads();
-    if (tid == 0) {
-      MS m2 = red_ms[0];
-      for (int i = 1; i < kPickT / 32; ++i) m2 = ms_combine(m2, red_ms[i]);
-      s_L = ms_log(m2);
+    // z of the chosen blocks' tokens, recomputed in fp32: thread t takes token
+    // t % 64 of every chosen block over K rows t / 64, t / 64 + 16, ... (all
+    // of its W2 loads in flight), then the slices are added in a fixed order
+    const int vl = tid & (kBlockW - 1), kg = tid / kBlockW;
+    for (int j = 0; j < c; ++j) {
+      const int sb = s_blk[j];
+      const int v = sb * kBlockW + vl;
+      float acc = 0.f;
+      if (sb >= 0 && v < V) {
+#pragma unroll 16
+        for (int i = kg; i < r; i += kPickKG) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
+      }
+      zp[kg][j * kBlockW + vl] = acc;
     }
-    // z of the chosen blocks' tokens, recomputed in full fp32 (W2 loads of
-    // each thread's tokens all in flight)
+    __syncthreads();
     const float* Urow = U + ((size_t)b * g + d) * V;
-    for (int q = tid; q < kTreeMaxC * kBlockW; q += kPickT) {
-      const int sb = s_blk[q / kBlockW];
-      const int v = sb * kBlockW + (q % kBlockW);
+    if (tid < c * kBlockW) {
+      const int sb = s_blk[tid / kBlockW];
+      const int v = sb * kBlockW + vl;
       float z = -INFINITY;
       if (sb >= 0 && v < V) {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < r; ++i) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
-        z = Urow[v] + acc;
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kPickKG; ++q) sum += zp[q][tid];
+        z = Urow[v] + sum;
       }
-      cz[q] = z;
-      cv[q] = sb >= 0 ? v : -1;
+      cz[tid] = z;
+      cv[tid] = (sb >= 0 && v < V) ? v : -1;
     }
     __syncthreads();
     // the c largest z among them (warp 0), children in decreasing z
@@ -288,7 +325,7 @@ __global__ void __launch_bounds__(kPickT)
         lv[j] = -INFINITY;
         li[j] = -1;
       }
-      for (int q = lane; q < kTreeMaxC * kBlockW; q += 32)
+      for (int q = lane; q < c * kBlockW; q += 32)
         if (cv[q] >= 0 && cz[q] > -INFINITY) list_insert(lv, li, cz[q], cv[q]);
       float ov[kTreeMaxC];
       int oi[kTreeMaxC];
@@ -357,9 +394,9 @@ __global__ void __launch_bounds__(kPickT)
 }
 
 // ---------------------------------------------------------------- verify
-constexpr int kTvThreads = 128;
+constexpr int kTvThreads = 512;
 constexpr int kTvStages = 4;
-constexpr int kTvChunk = kTvThreads * kBlockW;  // floats per stage: one 64-token block per thread
+constexpr int kTvChunk = 128 * kBlockW;  // floats per stage (32 KB): 128 blocks, four threads each
 
 size_t tree_verify_smem_bytes(int nblk) {
   return (size_t)kTvStages * kTvChunk * 4 + (size_t)nblk * 4 + 64;
@@ -376,6 +413,9 @@ __global__ void __launch_bounds__(kTvThreads)
   uint64_t* bars = reinterpret_cast<uint64_t*>(blkm + nblk + (nblk & 1));
   __shared__ int ch_node[kTreeMaxC];  // children of the current node, in admission order
   __shared__ int ch_tok[kTreeMaxC];
+  __shared__ float ch_logit[kTreeMaxC];     // their target logits in the node's row
+  __shared__ int t_tok[kTreeMaxNodes + 1];  // the request's tree
+  __shared__ int t_par[kTreeMaxNodes + 1];
   __shared__ int s_nch, s_next;
   __shared__ MS red_ms[kTvThreads / 32];
   __shared__ KeyIdx red_k[kTvThreads / 32];
@@ -387,6 +427,10 @@ __global__ void __launch_bounds__(kTvThreads)
     tc::fence_barrier_init();
   }
   for (int i = tid; i <= g; i += kTvThreads) path[(size_t)b * (g + 1) + i] = i == 0 ? 0 : -1;
+  for (int i = tid; i <= N; i += kTvThreads) {
+    t_tok[i] = tok[nb + i];
+    t_par[i] = par[nb + i];
+  }
   __syncthreads();
   const int nchunks = (V + kTvChunk - 1) / kTvChunk;
   volatile int never = 0;
@@ -396,10 +440,10 @@ __global__ void __launch_bounds__(kTvThreads)
     // first empty slot), in admission order
     if (tid == 0) {
       int k = 0;
-      for (int ch = node + 1; ch <= N && tok[nb + ch] >= 0; ++ch)
-        if (par[nb + ch] == node && k < kTreeMaxC) {
+      for (int ch = node + 1; ch <= N && t_tok[ch] >= 0; ++ch)
+        if (t_par[ch] == node && k < kTreeMaxC) {
           ch_node[k] = ch;
-          ch_tok[k] = tok[nb + ch];
+          ch_tok[k] = t_tok[ch];
           ++k;
         }
       s_nch = k;
@@ -407,6 +451,10 @@ __global__ void __launch_bounds__(kTvThreads)
     __syncthreads();
     const int nch = s_nch;
     const float* row = P + (nb + node) * (size_t)V;
+    if (tid < nch) {  // the children's target logits, loaded while the row streams
+      const int t = ch_tok[tid];
+      ch_logit[tid] = (t >= 0 && t < V) ? row[t] : -INFINITY;
+    }
     // stream the row: thread t takes block t of each chunk; per block the
     // log-mass without the children's tokens, and the running total of all
     auto issue = [&](int ch) {
@@ -437,52 +485,65 @@ __global__ void __launch_bounds__(kTvThreads)
         failed = true;
         break;
       }
-      const int s = ch * kTvThreads + tid;
-      if (s < nblk) {
-        // this thread's block from the stage, 16-byte pieces in a rotated
-        // order (conflict-free across the warp); the children's tokens masked
-        const float4* xb4 = reinterpret_cast<const float4*>(stage + (size_t)sidx * kTvChunk) + tid * (kBlockW / 4);
-        unsigned long long rem = 0ull;
+      // four threads per 64-token block (a quarter of 16 tokens each); the
+      // quarters' 16-byte pieces are read in a rotated order (fewer bank
+      // conflicts across the warp); the children's tokens are masked
+      const int qb = tid >> 2, qq = tid & 3;
+      const int s = ch * (kTvChunk / kBlockW) + qb;
+      {
+        const float4* xb4 = reinterpret_cast<const float4*>(stage + (size_t)sidx * kTvChunk + qb * kBlockW + qq * 16);
+        unsigned rem = 0u;  // the quarter's 16 tokens
         for (int k = 0; k < nch; ++k) {
-          const int t = ch_tok[k] - s * kBlockW;
-          if (t >= 0 && t < kBlockW) rem |= 1ull << t;
+          const int t = ch_tok[k] - s * kBlockW - qq * 16;
+          if (t >= 0 && t < 16) rem |= 1u << t;
         }
-        const int vlim = V - s * kBlockW;  // tokens of the block inside the vocabulary
-        float4 x4[kBlockW / 4];
-        int jj[kBlockW / 4];
+        const int vlim = V - s * kBlockW - qq * 16;  // tokens of the quarter inside the vocabulary
+        float4 x4[4];
+        int jj[4];
 #pragma unroll
-        for (int i = 0; i < kBlockW / 4; ++i) {
-          jj[i] = (i + tid) & (kBlockW / 4 - 1);
+        for (int i = 0; i < 4; ++i) {
+          jj[i] = (i + qb) & 3;
           x4[i] = xb4[jj[i]];
         }
         float mall = -INFINITY, m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kBlockW / 4; ++i) {
+        for (int i = 0; i < 4; ++i) {
           const float xv[4] = {x4[i].x, x4[i].y, x4[i].z, x4[i].w};
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const int e = 4 * jj[i] + c4;
-            const float val = e < vlim ? xv[c4] : -INFINITY;
+            const float val = (s < nblk && e < vlim) ? xv[c4] : -INFINITY;
             mall = fmaxf(mall, val);
-            if (!((rem >> e) & 1ull)) m = fmaxf(m, val);
+            if (!((rem >> e) & 1u)) m = fmaxf(m, val);
           }
         }
+        // the block's maxima over its four quarters (consecutive lanes)
+        mall = fmaxf(mall, __shfl_xor_sync(0xFFFFFFFFu, mall, 1));
+        mall = fmaxf(mall, __shfl_xor_sync(0xFFFFFFFFu, mall, 2));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
         float sall = 0.f, sm = 0.f;
         if (mall > -INFINITY) {
 #pragma unroll
-          for (int i = 0; i < kBlockW / 4; ++i) {
+          for (int i = 0; i < 4; ++i) {
             const float xv[4] = {x4[i].x, x4[i].y, x4[i].z, x4[i].w};
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               const int e = 4 * jj[i] + c4;
-              const float ev = (e < vlim && xv[c4] > -INFINITY) ? __expf(xv[c4] - mall) : 0.f;
+              const float ev = (s < nblk && e < vlim && xv[c4] > -INFINITY) ? __expf(xv[c4] - mall) : 0.f;
               sall += ev;
-              if (!((rem >> e) & 1ull)) sm += ev;
+              if (!((rem >> e) & 1u)) sm += ev;
             }
           }
         }
-        blkm[s] = (m > -INFINITY && sm > 0.f) ? mall + logf(sm) : -INFINITY;
-        tot = ms_combine(tot, MS{mall, sall});
+        sall += __shfl_xor_sync(0xFFFFFFFFu, sall, 1);
+        sall += __shfl_xor_sync(0xFFFFFFFFu, sall, 2);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 1);
+        sm += __shfl_xor_sync(0xFFFFFFFFu, sm, 2);
+        if (s < nblk && qq == 0) {
+          blkm[s] = (m > -INFINITY && sm > 0.f) ? mall + logf(sm) : -INFINITY;
+          tot = ms_combine(tot, MS{mall, sall});
+        }
       }
       __syncthreads();  // the stage is consumed
       if (tid == 0 && issued < nchunks) issue(issued++);
@@ -500,8 +561,7 @@ __global__ void __launch_bounds__(kTvThreads)
       int next = -1;
       float gone = 0.f;  // probability of the children rejected so far
       for (int k = 0; k < nch; ++k) {
-        const int t = ch_tok[k];
-        const float pt = (t >= 0 && t < V) ? expf(row[t] - L) : 0.f;
+        const float pt = expf(ch_logit[k] - L);
         const float q = pt / (1.f - gone);
         const float u = u01(rng.word(kTreeAccept, b, node, k));
         if (u < q) {

@@ -328,13 +328,14 @@ constexpr int kBulkThreads = 128;
 constexpr int kBulkStages = 3;
 constexpr int kBulkUnits = kBulkThreads;             // one block per thread per stage
 constexpr int kBulkFloats = kBulkUnits * kBlockW;   // 8192 fp32 = 32 KB
-constexpr int kBulkMaxSlots = 8;
+constexpr int kBulkMaxSlots = 32;  // rows one CTA range may touch (per-row partials of every thread)
 
 int sweep_bulk_max_slots() { return kBulkMaxSlots; }
 
-size_t sweep_bulk_smem_bytes() {
-  return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)kBulkMaxSlots * kBulkThreads * 16 + 64 +
-         (size_t)kBulkMaxSlots * (16 + 8);
+// ring stages, then SL rows of per-thread partials, the ring barriers, and
+// the rows' (request, position, ...) and (length, offset)
+size_t sweep_bulk_smem_bytes(int SL) {
+  return (size_t)kBulkStages * kBulkFloats * 4 + (size_t)SL * kBulkThreads * 16 + 64 + (size_t)SL * (16 + 8);
 }
 
 __global__ void __launch_bounds__(kBulkThreads)
@@ -347,9 +348,9 @@ __global__ void __launch_bounds__(kBulkThreads)
   float* stage = reinterpret_cast<float*>(smem);
   float4* slot = reinterpret_cast<float4*>(smem + (size_t)kBulkStages * kBulkFloats * 4);  // [SL][threads]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kBulkStages * kBulkFloats * 4 +
-                                               (size_t)kBulkMaxSlots * kBulkThreads * 16);
-  int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [kBulkMaxSlots] (b, j, last row?, tested token)
-  int2* rowlen = reinterpret_cast<int2*>(rowinfo + kBulkMaxSlots);  // [kBulkMaxSlots] (lengths[b], row_off[b])
+                                               (size_t)SL * kBulkThreads * 16);
+  int4* rowinfo = reinterpret_cast<int4*>(bars + 8);  // [SL] (b, j, last row?, tested token)
+  int2* rowlen = reinterpret_cast<int2*>(rowinfo + SL);  // [SL] (lengths[b], row_off[b])
   // The finalize of a request whose rows no range covers never runs, so the
   // lengths, offsets and anchors of all requests are checked by one CTA.
   auto check_requests = [&]() {
@@ -752,7 +753,7 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const bool pdl = ws->pdl != 0;
   if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
     const cudaError_t e = launch_ex(k_verify_sweep_bulk, dim3(geo.sweep_grid), dim3(kBulkThreads),
-                                    sweep_bulk_smem_bytes(), st, pdl, a.P, a.row_off, a.lengths, d.B, geo.nblk,
+                                    sweep_bulk_smem_bytes(geo.SL), st, pdl, a.P, a.row_off, a.lengths, d.B, geo.nblk,
                                     d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin, ws->s.vdone,
                                     a.rowtab);
     if (e != cudaSuccess) return e;
@@ -796,6 +797,6 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 namespace dspark {
 cudaError_t sweep_bulk_configure() {
   return cudaFuncSetAttribute(k_verify_sweep_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)sweep_bulk_smem_bytes());
+                              (int)sweep_bulk_smem_bytes(kBulkMaxSlots));
 }
 }  // namespace dspark

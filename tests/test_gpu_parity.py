@@ -40,8 +40,8 @@ MID = {
     "mid_oddV": Workload("mid_oddV", B=6, gamma=3, V=1001, r=16, H=24, wdtype="f32", mode="compact",
                          seed=15, u_std=2.0, w_std=0.1, sps_knee=8.0),
     "small": WORKLOADS["small"],
-    # static rounds with more verified rows than the bulk sweep's row slots
-    # hold per CTA range (256 x 8 rows): the register sweep takes them
+    # static rounds with more verified rows than two CTAs per SM can hold
+    # partials for (256 x 8 rows): the bulk sweep runs one CTA per SM
     "mid_static_many_rows": Workload("mid_static_many_rows", B=256, gamma=7, V=2048, r=64, H=16, wdtype="bf16",
                                      mode="static", seed=16, u_std=2.0, w_std=0.05),
 }
