@@ -32,12 +32,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofline"
 
-# DRAM bytes (read + write) of one k_draft_tc launch on the prod workload, from
-# the ncu capture summarised in profiles/draft_tc_prod.md, and a hash of the
-# kernel source it was taken on; the roofline's "traffic" is reported only
-# while the source is unchanged.
-DRAFT_TRAFFIC = {"sha256": "9c45c4ff4f517f4c5951abfe6b7c100f9e2efcf2b185cb3d035b32b5b6267bec",
-                 "bytes": 414924800 + 3521280}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_draft_tc
+# launch on the prod workload, from one ncu capture of this bench (caches
+# flushed before the launch), and a hash of the kernel source it was taken on;
+# the roofline's "traffic" is reported only while the source is unchanged.
+DRAFT_TRAFFIC = {"sha256": "030149f0fa04e75cba9e6d03dcc1cabc05b437da13218de6ea419ebd3b2d8b05",
+                 "bytes": 459661312 + 1618944}
 QUOTED_HBM_GBS = 8000.0   # GB/s, the roofline constant the metric is quoted against
 
 

@@ -160,6 +160,37 @@ dspark_status dspark_plan(dspark_ws* ws, const float* conf, const double* sps,
                           int32_t* lengths, int32_t* row_off, dspark_stream_t stream);
 
 /*
+ * A batch split by request across devices. The planner's objective
+ * Theta = tau * SPS(B_tot) ("spec_dspark", section "目标函数": the SPS table
+ * is a property of the target engine's whole verify batch) couples every
+ * request of the batch, while draft and verify are independent per request.
+ * So each device drafts and verifies its own contiguous range of requests
+ * with a workspace of that range's size, every device plans the whole batch
+ * from the confidences of all devices (the caller all-gathers them: B * gamma
+ * fp32), and each keeps its own range's lengths.
+ *
+ * dspark_ws_set_shard: the workspace holds requests b_offset .. b_offset +
+ * B - 1 of the batch. The request word b of every Philox counter becomes
+ * b_offset + b, so each request draws the same numbers as in an unsplit
+ * batch. Default 0. EINVAL if b_offset < 0 or b_offset + B > 2^31 - 1.
+ *
+ * dspark_plan_shard: dspark_plan on a workspace made for the WHOLE batch
+ * (dims.B = every device's requests; conf [B, gamma] gathered in batch
+ * order; lengths [B], row_off [B + 1] as dspark_plan writes them), then
+ * lengths_local[i] = lengths[b_begin + i] for i < b_count and
+ * row_off_local[i] = row_off[b_begin + i] - row_off[b_begin] for i <= b_count:
+ * the range's lengths and its own packed-row offsets, ready for that device's
+ * dspark_verify. All buffers are the caller's device memory, 16-byte aligned.
+ * EINVAL unless 0 <= b_begin, 1 <= b_count and b_begin + b_count <= B. Every
+ * device that runs it on the same gathered confidences (and, for
+ * COMPACT_LAGGED, the same history) gets the same whole-batch plan.
+ */
+dspark_status dspark_ws_set_shard(dspark_ws* ws, int b_offset);
+dspark_status dspark_plan_shard(dspark_ws* ws, const float* conf, const double* sps, int b_begin, int b_count,
+                                int32_t* lengths, int32_t* row_off, int32_t* lengths_local,
+                                int32_t* row_off_local, dspark_stream_t stream);
+
+/*
  * Verify. P packed [row_off[B], V] fp32 target logits; row_off and lengths as
  * written by dspark_plan; anchor [B]; tokens, pd_tok, lse [B, gamma] as written
  * by dspark_markov_draft; U, W1, W2 as given to it (the draft distribution at

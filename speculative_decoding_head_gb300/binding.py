@@ -26,6 +26,7 @@ SYMBOLS = [
     "dspark_sts_fit", "dspark_sts_scratch_bytes", "dspark_train_loss", "dspark_train_loss_scratch_bytes",
     "dspark_rnn_draft", "dspark_rnn_draft_scratch_bytes", "dspark_verify_rnn",
     "dspark_pctree_scratch_bytes", "dspark_pctree_build", "dspark_pctree_verify",
+    "dspark_ws_set_shard", "dspark_plan_shard",
 ]
 
 
@@ -100,6 +101,10 @@ def load() -> C.CDLL:
         lib.dspark_pctree_build.restype = i32
         lib.dspark_pctree_verify.argtypes = [P] * 4 + [i32, u64, u64] + [P] * 4
         lib.dspark_pctree_verify.restype = i32
+        lib.dspark_ws_set_shard.argtypes = [P, i32]
+        lib.dspark_ws_set_shard.restype = i32
+        lib.dspark_plan_shard.argtypes = [P, P, P, i32, i32, P, P, P, P, P]
+        lib.dspark_plan_shard.restype = i32
         _lib = lib
         return lib
 
@@ -243,6 +248,30 @@ class Workspace:
                                     _ptr(out["lengths"], torch.int32, "lengths"),
                                     _ptr(out["row_off"], torch.int32, "row_off"), _stream(stream))
         _check(code, "dspark_plan")
+        return out
+
+    def set_shard(self, b_offset: int):
+        """This workspace holds requests b_offset .. b_offset + B - 1 of a
+        batch split across devices (``dspark_ws_set_shard``)."""
+        _check(self.lib.dspark_ws_set_shard(self._h, int(b_offset)), "dspark_ws_set_shard")
+
+    def plan_shard(self, conf, sps, b_begin: int, b_count: int, out=None, stream=None):
+        """Plan the whole batch (this workspace's B) from the gathered
+        confidences and keep requests b_begin .. b_begin + b_count - 1
+        (``dspark_plan_shard``). ``out`` gains lengths_local [b_count] and
+        row_off_local [b_count + 1]."""
+        dev = conf.device
+        out = out or self.new_plan_outputs(dev)
+        if "lengths_local" not in out:
+            out["lengths_local"] = torch.zeros(b_count, dtype=torch.int32, device=dev)
+            out["row_off_local"] = torch.zeros(b_count + 1, dtype=torch.int32, device=dev)
+        i32 = torch.int32
+        code = self.lib.dspark_plan_shard(self._h, _ptr(conf, torch.float32, "conf"),
+                                          _ptr(sps, torch.float64, "sps"), int(b_begin), int(b_count),
+                                          _ptr(out["lengths"], i32, "lengths"), _ptr(out["row_off"], i32, "row_off"),
+                                          _ptr(out["lengths_local"], i32, "lengths_local"),
+                                          _ptr(out["row_off_local"], i32, "row_off_local"), _stream(stream))
+        _check(code, "dspark_plan_shard")
         return out
 
     def verify(self, P, row_off, lengths, anchor, tokens, pd_tok, lse, U, W1, W2, seed: int, rnd: int,

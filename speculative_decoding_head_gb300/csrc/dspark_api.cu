@@ -268,6 +268,26 @@ dspark_status dspark_plan(dspark_ws* ws, const float* conf, const double* sps, i
   return plan_call(ws, conf, sps, lengths, row_off, nullptr, stream);
 }
 
+dspark_status dspark_ws_set_shard(dspark_ws* ws, int b_offset) {
+  if (!ws || b_offset < 0 || (long long)b_offset + ws->d.B > 0x7FFFFFFFLL) return DSPARK_EINVAL;
+  ws->b0 = b_offset;
+  return DSPARK_OK;
+}
+
+dspark_status dspark_plan_shard(dspark_ws* ws, const float* conf, const double* sps, int b_begin, int b_count,
+                                int32_t* lengths, int32_t* row_off, int32_t* lengths_local, int32_t* row_off_local,
+                                dspark_stream_t stream) {
+  if (!ws || b_begin < 0 || b_count < 1 || b_count > ws->d.B - b_begin) return DSPARK_EINVAL;
+  if (!aligned16(lengths_local) || !aligned16(row_off_local)) return DSPARK_EINVAL;
+  const dspark_status s = plan_call(ws, conf, sps, lengths, row_off, nullptr, stream);
+  if (s != DSPARK_OK) return s;
+  int launches = ws->last_launches;
+  cudaError_t e = launch_plan_slice(lengths, row_off, b_begin, b_count, lengths_local, row_off_local,
+                                    reinterpret_cast<cudaStream_t>(stream), &launches);
+  ws->last_launches = launches;
+  return cuda_fail(e);
+}
+
 dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
                             const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
                             const float* U, const void* W1, const void* W2, uint64_t seed, uint64_t round,

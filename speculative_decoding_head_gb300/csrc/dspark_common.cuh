@@ -52,18 +52,23 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The counter's request word is the request's index in the whole batch: a
+// workspace that holds requests b0 .. b0 + B - 1 of a batch split across
+// devices passes b0, so every request draws the same numbers wherever it runs.
 struct Rng {
   uint32_t k0, k1, tag;  // tag = purpose << 24 | round mod 2^24 (without purpose)
-  __host__ __device__ static Rng make(uint64_t seed, uint64_t round) {
+  uint32_t b0;           // batch index of the workspace's request 0
+  __host__ __device__ static Rng make(uint64_t seed, uint64_t round, uint32_t b0 = 0) {
     Rng r;
     r.k0 = (uint32_t)(seed & 0xFFFFFFFFull);
     r.k1 = (uint32_t)(seed >> 32);
     r.tag = (uint32_t)(round & 0xFFFFFFull);
+    r.b0 = b0;
     return r;
   }
-  // all four words of the counter block that holds token v
+  // all four words of the counter block that holds token v (b: index in the workspace)
   __device__ __forceinline__ uint4 block4(uint32_t purpose, uint32_t b, uint32_t j, uint32_t v) const {
-    return philox4x32_10(make_uint4(v >> 2, b, j, (purpose << 24) | tag), k0, k1);
+    return philox4x32_10(make_uint4(v >> 2, b0 + b, j, (purpose << 24) | tag), k0, k1);
   }
   __device__ __forceinline__ uint32_t word(uint32_t purpose, uint32_t b, uint32_t j, uint32_t v) const {
     const uint4 o = block4(purpose, b, j, v);

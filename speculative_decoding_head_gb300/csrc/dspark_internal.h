@@ -118,6 +118,7 @@ struct dspark_ws {
   int use_tc;  // tensor-core draft and residual where geo.tc_ok / geo.resid_tc_ok hold
   int last_launches;
   int pdl;     // set by dspark_round: the plan and verify kernels wait on the previous kernel in-kernel
+  int b0;      // batch index of request 0 (dspark_ws_set_shard): the request word of every random draw
 };
 
 namespace dspark {
@@ -195,6 +196,10 @@ cudaError_t launch_tree_blocks_tc(const dspark_ws* ws, const float* U, const voi
                                   float* bmax, cudaStream_t st);
 
 size_t plan_smem_bytes(const dspark_dims& d);
+// lengths_l[i] = lengths[b_begin + i] and row_off_l[i] = row_off[b_begin + i] - row_off[b_begin]
+// (i <= n for row_off_l): one device's share of a plan made for the whole batch.
+cudaError_t launch_plan_slice(const int32_t* lengths, const int32_t* row_off, int b_begin, int n, int32_t* lengths_l,
+                              int32_t* row_off_l, cudaStream_t st, int* launches);
 cudaError_t sweep_bulk_configure();
 int sweep_bulk_max_slots();  // rows one CTA range of the bulk sweep may span
 size_t sweep_bulk_smem_bytes(int SL);

@@ -216,7 +216,7 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
   const int wpc = kSimtThreads / 32;
   int chunks = (nblk + 4 * wpc - 1) / (4 * wpc);  // about 4 blocks per warp
   if (chunks < 1) chunks = 1;
-  const Rng rng = Rng::make(a.seed, a.round);
+  const Rng rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
   const float* ovec = rnn ? rnn->ovec : nullptr;
   for (int k = 1; k <= d.gamma; ++k) {
     if (rnn) {

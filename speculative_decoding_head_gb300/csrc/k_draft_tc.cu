@@ -878,7 +878,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.Ggmax = (p.G + p.nG - 1) / p.nG;
   p.P = kSets * p.Ggmax;
   p.rowsG = p.nG * kTcRows;
-  p.rng = Rng::make(a.seed, a.round);
+  p.rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
   p.anchor = a.anchor;
   p.W1 = a.W1;
   p.w = a.w;

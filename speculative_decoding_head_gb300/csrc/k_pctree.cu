@@ -625,7 +625,7 @@ cudaError_t launch_pctree_verify(const dspark_ws* ws, const float* P, const int3
   const size_t smem = tree_verify_smem_bytes(ws->geo.nblk);
   cudaError_t e = cudaFuncSetAttribute(k_tree_verify, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_tree_verify<<<d.B, kTvThreads, smem, st>>>(P, tok, par, N, d.gamma, d.V, ws->geo.nblk, Rng::make(seed, round),
+  k_tree_verify<<<d.B, kTvThreads, smem, st>>>(P, tok, par, N, d.gamma, d.V, ws->geo.nblk, Rng::make(seed, round, (uint32_t)ws->b0),
                                                path, n_acc, next_anchor, ws->s.status);
   ++*launches;
   return cudaGetLastError();

@@ -482,4 +482,20 @@ cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sp
   return e;
 }
 
+__global__ void k_plan_slice(const int32_t* __restrict__ lengths, const int32_t* __restrict__ row_off, int b_begin,
+                             int n, int32_t* __restrict__ lengths_l, int32_t* __restrict__ row_off_l) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i > n) return;
+  const int32_t base = row_off[b_begin];
+  row_off_l[i] = row_off[b_begin + i] - base;
+  if (i < n) lengths_l[i] = lengths[b_begin + i];
+}
+
+cudaError_t launch_plan_slice(const int32_t* lengths, const int32_t* row_off, int b_begin, int n, int32_t* lengths_l,
+                              int32_t* row_off_l, cudaStream_t st, int* launches) {
+  k_plan_slice<<<(n + 1 + 255) / 256, 256, 0, st>>>(lengths, row_off, b_begin, n, lengths_l, row_off_l);
+  ++*launches;
+  return cudaGetLastError();
+}
+
 }  // namespace dspark

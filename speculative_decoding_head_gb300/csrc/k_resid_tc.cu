@@ -887,7 +887,7 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   cudaError_t e = w2_tensor_map(d, a.W2, &tm);
   if (e != cudaSuccess) return e;
   RParams p = base_params(ws, grid);
-  p.rng = Rng::make(a.seed, a.round);
+  p.rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
   p.P = a.P;
   p.U = a.U;
   p.W1 = a.W1;

@@ -746,7 +746,7 @@ template <int BF16>
 static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t st, int* launches) {
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
-  const Rng rng = Rng::make(a.seed, a.round);
+  const Rng rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
   const FinArgs fin{a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma, d.V, geo.nblk,
                     geo.SL, geo.sweep_grid, rng, ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
                     ws->s.vlset, ws->s.status, geo.sweep_bulk ? ws->s.vpx : nullptr};
