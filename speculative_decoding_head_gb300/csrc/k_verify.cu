@@ -175,12 +175,9 @@ struct FinArgs {
 __device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R) {
   const int lane = threadIdx.x & 31;
   const float* __restrict__ P = f.P;
-  const int32_t* __restrict__ row_off = f.row_off;
-  const int32_t* __restrict__ lengths = f.lengths;
-  const int32_t* __restrict__ anchor = f.anchor;
   const int32_t* __restrict__ tokens = f.tokens;
   const float* __restrict__ pd_tok = f.pd_tok;
-  const int B = f.B, g = f.g, V = f.V, nblk = f.nblk, SL = f.SL, Gs = f.Gs;
+  const int g = f.g, V = f.V, nblk = f.nblk, SL = f.SL, Gs = f.Gs;
   const Rng rng = f.rng;
   const float4* __restrict__ part = f.part;
   int32_t* __restrict__ n_acc = f.n_acc;
@@ -380,13 +377,16 @@ __global__ void __launch_bounds__(kBulkThreads)
   const int nchunks = (int)((hi - lo + kBulkUnits - 1) / kBulkUnits);
   const uint32_t bar0 = tc::smem_u32(bars);
   const uint32_t st0 = tc::smem_u32(stage);
+  // P is read once: evict it first, so that W2 (kept with evict_last by the
+  // draft and the residual pass) stays in L2 across the sweep
+  const uint64_t pol = tc::policy_evict_first();
   auto issue = [&](int ch) {
     const long long u = lo + (long long)ch * kBulkUnits;
     const int units = (int)min((long long)kBulkUnits, hi - u);
     const uint32_t bytes = (uint32_t)units * kBlockW * 4u;
     const int sidx = ch % kBulkStages;
     tc::mbar_arrive_expect_tx(bar0 + 8u * sidx, bytes);
-    tc::bulk_load(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, bar0 + 8u * sidx);
+    tc::bulk_load_hint(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, bar0 + 8u * sidx, pol);
   };
   int issued = 0;  // chunks issued (thread 0's count)
   if (tid == 0) {  // the first copies fly while the row table is built

@@ -156,6 +156,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// The same copy with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Tensor-memory allocation (one warp executes; writes the base address to *dst).
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
