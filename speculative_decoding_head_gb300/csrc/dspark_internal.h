@@ -87,7 +87,7 @@ struct Scratch {
   // persistent tcgen05 draft kernel
   float4* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
                           // (max, sum exp) of a row's blocks
-  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, token) winners; the
+  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, token) winners, 16 words apart; the
                              // two halves alternate between launches
   unsigned* barrier;      // [8] draft kernel words: [2] launch count, [4 + launch parity] barrier arrivals
 };

@@ -75,6 +75,9 @@ constexpr int kNAcc = 4;                     // accumulators: the MMA runs up to
 constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
+// Winner words are kWinPad words apart (one 128-byte line per row), so that
+// the CTAs' atomic maxima on different rows do not queue on shared lines.
+constexpr int kWinPad = 16;
 
 static_assert(kBlk == kBlockW, "an accumulator slice is one sampler block");
 static_assert(kSets == 2, "the A gather splits a lane quarter's rows into even and odd");
@@ -113,7 +116,7 @@ struct TcParams {
   float* lse;
   float* conf;
   float4* dpart;            // [g][rowsG][P]: (max, sum exp, z of its token, its token) per CTA and set
-  unsigned long long* win;  // [2][g][rowsG]: packed (block key, token), 0 = none
+  unsigned long long* win;  // [2][g][rowsG] x kWinPad: packed (block key, token), 0 = none
   unsigned* bar;            // [2] launches (parity of win and counters), [4 + parity] grid-barrier arrivals
   int* status;
 };
@@ -457,12 +460,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int par = (int)(__ldcg(p.bar + 2) & 1u);
     unsigned* gctr = p.bar + 4 + par;
     const size_t half = (size_t)p.g * p.rowsG;
-    unsigned long long* win = p.win + par * half;
+    unsigned long long* win = p.win + par * half * kWinPad;
     {
       const int et = threadIdx.x - 64;
       if (c == 0 && et == 0) p.bar[4 + (par ^ 1)] = 0u;
       for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads)
-        p.win[(par ^ 1) * half + i] = 0ull;
+        p.win[((par ^ 1) * half + i) * kWinPad] = 0ull;
     }
     for (int k = 1; k <= p.g; ++k) {
       // ---- A = W1[x_{k-1}], gathered by the epilogue warps into the swizzled
@@ -476,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (k == 1) {
             x = p.anchor[b];
           } else {
-            const unsigned long long wv = __ldcg(win + (size_t)(k - 2) * p.rowsG + b);
+            const unsigned long long wv = __ldcg(win + ((size_t)(k - 2) * p.rowsG + b) * kWinPad);
             x = wv ? win_token(wv) : -1;
           }
           if (x < 0 || x >= p.V) {
@@ -670,7 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---- publish the row's candidate (block key, token) and each set's
       // partials (max, sum exp, z of its token, its token)
       if (valid && !*abort) {
-        if (bx >= 0) atomicMax(win + (size_t)(k - 1) * p.rowsG + b, pack_win(bk, bx));
+        if (bx >= 0) atomicMax(win + ((size_t)(k - 1) * p.rowsG + b) * kWinPad, pack_win(bk, bx));
         // every set writes its slot every step (a set without blocks writes
         // the neutral partial), so no entry of an earlier launch is combined
         p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] =
@@ -689,8 +692,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
         const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
         const int Pr = kSets * group_ctas(p.G, p.nG, br / kTcRows);
-        const unsigned long long wx = __ldcg(win + (size_t)kk * p.rowsG + br);
-        int xp = kk == 0 ? p.anchor[br] : win_token(__ldcg(win + (size_t)(kk - 1) * p.rowsG + br));
+        const unsigned long long wx = __ldcg(win + ((size_t)kk * p.rowsG + br) * kWinPad);
+        int xp = kk == 0 ? p.anchor[br] : win_token(__ldcg(win + ((size_t)(kk - 1) * p.rowsG + br) * kWinPad));
         if (wx == 0ull) {
           if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
           continue;
@@ -837,7 +840,7 @@ size_t draft_tc_partials(const dspark_dims& d, int grid) {
 
 size_t draft_tc_winners(const dspark_dims& d) {
   const int nG = (d.B + kTcRows - 1) / kTcRows;
-  return (size_t)2 * d.gamma * nG * kTcRows;
+  return (size_t)2 * d.gamma * nG * kTcRows * kWinPad;
 }
 
 cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_t st, int* launches) {
