@@ -119,7 +119,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
     if (draft_tc_configure(ws) != cudaSuccess) geo.tc_ok = 0;
   }
   if (geo.tc_ok) {
-    o_dpart = carve(sizeof(float4) * draft_tc_partials(d, geo.tc_grid));
+    o_dpart = carve(sizeof(float2) * draft_tc_partials(d, geo.tc_grid));
     o_dwin = carve(sizeof(unsigned long long) * draft_tc_winners(d));
   }
   if (plan_configure() != cudaSuccess) {
@@ -149,7 +149,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vpx = reinterpret_cast<float*>(base + o_vpx);
   s.rowtab = reinterpret_cast<int4*>(base + o_rowtab);
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
-  s.dpart = geo.tc_ok ? reinterpret_cast<float4*>(base + o_dpart) : nullptr;
+  s.dpart = geo.tc_ok ? reinterpret_cast<float2*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
   ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {

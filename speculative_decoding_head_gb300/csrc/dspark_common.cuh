@@ -83,34 +83,6 @@ __device__ __forceinline__ float u01(uint32_t x) {
 
 __device__ __forceinline__ float gumbel(uint32_t x) { return -logf(-logf(u01(x))); }
 
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Gumbel noise in log2 units for a screening pass: -log2(-log2 u) =
-// log2(e) G - log2(log2 e) with G = -log(-log u), so z log2(e) plus it orders
-// tokens as z + G does. The inner logarithm of u > 1 - 2^-5 comes from the
-// series -log(1 - t) = t + t^2/2 + t^3/3 + t^4/4 with t = 1 - u (exact: u
-// lies on the 2^-24 grid), truncated at 2e-7 relative, so that it keeps its
-// relative accuracy where -log u is small; elsewhere -log2 u >= 0.045 and
-// lg2.approx (absolute error about 2^-22) costs at most 6e-6 relative. The
-// result is within about 1e-5 of the exact value.
-__device__ __forceinline__ float gumbel2_screen(uint32_t x) {
-  constexpr float kL2e = 1.4426950408889634f;
-  const float u = u01(x);
-  const float t = 1.f - u;
-  const float ser = t * (kL2e * fmaf(t, fmaf(t, fmaf(t, 0.25f, 1.f / 3.f), 0.5f), 1.f));
-  const float e2 = t < 0x1p-5f ? ser : -lg2_approx(u);
-  return -lg2_approx(e2);
-}
-
-// A screening pass ranks token keys with gumbel2_screen; keys whose screened
-// values lie within kScreenGap (log2 units) of each other are a close call,
-// and the caller recomputes them with the exact map (gumbel).
-constexpr float kScreenGap = 1e-4f;
-
 __device__ __forceinline__ float ld_w(const void* W, int bf16, size_t i) {
   if (bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(W)[i]);
   return reinterpret_cast<const float*>(W)[i];

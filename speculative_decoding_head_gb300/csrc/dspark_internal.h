@@ -85,10 +85,11 @@ struct Scratch {
   int4* rowtab;           // [B*(gamma+1)] (b, j, lengths[b], row_off[b]) per packed row (dspark_round)
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
-  float4* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
+  float2* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
                           // (max, sum exp) of a row's blocks
-  unsigned long long* dwin;  // [2][gamma][groups*128] packed (block key, token) winners, 16 words apart; the
-                             // two halves alternate between launches
+  unsigned long long* dwin;  // [2][gamma][groups*128] lines of 16 words: word 0 the packed (block key,
+                             // block) winner, word 1 the token drawn in it; the two halves alternate
+                             // between launches
   unsigned* barrier;      // [8] draft kernel words: [2] launch count, [4 + launch parity] barrier arrivals
 };
 
@@ -164,7 +165,7 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 // Whether the tcgen05 draft kernel supports these dims, and its launch shape.
 int draft_tc_supported(const dspark_dims& d);
 cudaError_t draft_tc_configure(dspark_ws* ws);
-size_t draft_tc_partials(const dspark_dims& d, int grid);  // float4 entries of Scratch::dpart
+size_t draft_tc_partials(const dspark_dims& d, int grid);  // float2 entries of Scratch::dpart
 size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch::dwin
 
 int resid_tc_supported(const dspark_dims& d);

@@ -29,19 +29,25 @@
 //               z = TMEM, the block's log-mass (max, sum exp), the block
 //               draw key log mass + G_s, the row's online log-sum-exp, and a
 //               register copy of z for the set's best block so far.
-// Step boundary. The block draw is a grid-wide argmax of the block keys. Each
-// set first draws the token inside its own best block (the token level of the
-// two-level sampler, argmax_v (z_v + G_v) over the block's 64 tokens, from the
-// register copy of that block's z), so that its candidate is complete, then
-// publishes (block key, token) per row with a 64-bit atomic max; all CTAs
-// meet at one grid barrier, after which the winner words are final. In every
-// CTA of the group the epilogue warps read the 128 rows' tokens and gather
-// W1[x_k] straight into the swizzled A operand in shared memory (the anchors'
-// rows at step 1). The producers keep prefetching the next step's tiles
-// meanwhile (they do not depend on the drafted token). Log-sum-exps, probabilities of the drawn tokens and
-// confidences are off that chain: per-set partials (max, sum exp) are kept
-// per step and combined after the last step, one warp per (row, step), which
-// also forms the confidence logit w^T [h_k; W1[x_{k-1}]] from h and W1.
+// Step boundary. The block draw is a grid-wide argmax of the block keys:
+// per row, each CTA publishes its best (block key, block) with a 64-bit
+// atomic max into the row's winner word, and the thread holding that block
+// parks its z in shared memory; all CTAs meet at a grid barrier. Only then is
+// the token inside the block drawn (the token level of the two-level sampler,
+// argmax_v (z_v + G_v) over the block's 64 tokens with exact Gumbel keys), by
+// the one CTA that owns the winning block, one warp per row it owns; it
+// writes the token and its z beside the winner word, and a second grid
+// barrier makes every token of the step final. (Drawing every CTA's
+// candidate token before a single barrier costs each CTA the draw of all its
+// rows, of which it wins about 1 in G.) In every CTA of the group the
+// epilogue warps then read the 128 rows' tokens and gather W1[x_k] straight
+// into the swizzled A operand in shared memory (the anchors' rows at step 1).
+// The producers keep prefetching the next step's tiles meanwhile (they do not
+// depend on the drafted token). Log-sum-exps, probabilities of the drawn
+// tokens and confidences are off that chain: per-set partials (max, sum exp)
+// are kept per step and combined after the last step, one warp per (row,
+// step), which also forms the confidence logit w^T [h_k; W1[x_{k-1}]] from h
+// and W1.
 //
 // Every wait is bounded (tc_ptx.cuh); a timeout sets DSPARK_ETIMEOUT, every
 // role leaves its loop, in-flight copies and MMAs are drained, TMEM is freed.
@@ -115,7 +121,7 @@ struct TcParams {
   float* pd_tok;
   float* lse;
   float* conf;
-  float4* dpart;            // [g][rowsG][P]: (max, sum exp, z of its token, its token) per CTA and set
+  float2* dpart;            // [g][rowsG][P]: (max, sum exp) of a row's blocks per CTA and set
   unsigned long long* win;  // [2][g][rowsG] x kWinPad: packed (block key, token), 0 = none
   unsigned* bar;            // [2] launches (parity of win and counters), [4 + parity] grid-barrier arrivals
   int* status;
@@ -123,15 +129,14 @@ struct TcParams {
 
 __device__ __forceinline__ int group_ctas(int G, int nG, int g) { return (G - g + nG - 1) / nG; }
 
-// (block key, token drawn in the block) as one unsigned 64-bit word whose
-// unsigned order is: larger key first, then the smaller token (blocks are
-// token ranges, so the smaller block). Never 0.
+// (block key, block) as one unsigned 64-bit word whose unsigned order is:
+// larger key first, then the smaller block. Never 0.
 __device__ __forceinline__ unsigned long long pack_win(float key, int x) {
   uint32_t u = __float_as_uint(key);
   u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
   return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)x);
 }
-__device__ __forceinline__ int win_token(unsigned long long w) {
+__device__ __forceinline__ int win_block(unsigned long long w) {
   return (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
 }
 
@@ -142,72 +147,16 @@ __device__ __forceinline__ size_t a_piece(int m, int kb, int ch) {
   return (size_t)kb * (kTcRows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
 }
 
-// The token level of the draft's two-level sampler over one 64-token block
-// whose z sits in shared memory (chunk c of 4 tokens at c ^ sw): argmax_i
-// (z[i] + G(kDraftToken, b, k, v0 + i)), first maximum on ties. The two
-// threads of a row each screen half of the tokens, ranking
-// z log2(e) + gumbel2_screen(u) (error about 1e-5); when the best two screened
-// keys of the block lie within kScreenGap, the keys are recomputed exactly
-// (z + gumbel(u)) and the argmax taken on those, so the result is the
-// exact-key argmax.
-struct DrawPart {
-  float k1, k2, z1;  // best and second screened key, z of the best
-  int i1;            // its token in the block, -1 if none is finite
-};
-
-constexpr int kDrawUnroll = 4;  // independent Philox chains in flight per thread
-__device__ __noinline__ DrawPart draw_screen(const float4* zs, int sw, const Rng& rng, int b, int k, int v0,
-                                             int c_lo) {
-  DrawPart d{-INFINITY, -INFINITY, 0.f, -1};
-#pragma unroll(kDrawUnroll)
-  for (int c4 = c_lo; c4 < c_lo + kBlk / 8; ++c4) {
-    const float4 zz = zs[c4 ^ sw];
-    const uint4 o = rng.block4(kDraftToken, b, k, v0 + 4 * c4);
-    const float zv[4] = {zz.x, zz.y, zz.z, zz.w};
-    const uint32_t wv[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float key = fmaf(zv[i], tc::kLog2e, gumbel2_screen(wv[i]));
-      d.k2 = fmaxf(d.k2, fminf(d.k1, key));
-      if (key > d.k1) {
-        d.k1 = key;
-        d.z1 = zv[i];
-        d.i1 = 4 * c4 + i;
-      }
-    }
-  }
-  return d;
+// The set whose best block is this CTA's candidate for row m (larger key,
+// then the smaller block), from the step-end exchange in shared memory.
+__device__ __forceinline__ int cta_best_set(const float* keyx, const uint16_t* blkx, int m) {
+  const float kA = keyx[m], kB = keyx[kTcRows + m];
+  return (kB > kA || (kB == kA && blkx[kTcRows + m] < blkx[m])) ? 1 : 0;
 }
 
-// the two halves combined: the lower half's tokens come first on ties
-__device__ __forceinline__ DrawPart draw_join(const DrawPart& a, const DrawPart& b) {
-  DrawPart r = b.k1 > a.k1 ? b : a;
-  r.k2 = fmaxf(fminf(a.k1, b.k1), fmaxf(a.k2, b.k2));
-  return r;
-}
-
-__device__ __noinline__ int draw_exact(const float4* zs, int sw, const Rng& rng, int b, int k, int v0, float* zx) {
-  float best = -INFINITY, z1 = 0.f;
-  int i1 = -1;
-#pragma unroll 1
-  for (int c4 = 0; c4 < kBlk / 4; ++c4) {
-    const float4 zz = zs[c4 ^ sw];
-    const uint4 o = rng.block4(kDraftToken, b, k, v0 + 4 * c4);
-    const float zv[4] = {zz.x, zz.y, zz.z, zz.w};
-    const uint32_t wv[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float key = zv[i] + gumbel(wv[i]);
-      if (key > best) {
-        best = key;
-        z1 = zv[i];
-        i1 = 4 * c4 + i;
-      }
-    }
-  }
-  *zx = z1;
-  return i1;
-}
+// The token word beside a row's winner word: (z of the token) << 32 | token + 1,
+// 0 while no token is written. Returns the token, -1 if none.
+__device__ __forceinline__ int drawn_token(unsigned long long w) { return (int)(uint32_t)(w & 0xFFFFFFFFull) - 1; }
 
 // Grid barrier among the epilogue warps (named barrier 1) of all CTAs: the
 // leader of each CTA adds one to this launch's arrival counter (release) and
@@ -464,8 +413,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     {
       const int et = threadIdx.x - 64;
       if (c == 0 && et == 0) p.bar[4 + (par ^ 1)] = 0u;
-      for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads)
+      for (size_t i = (size_t)c * kEpiThreads + et; i < half; i += (size_t)p.G * kEpiThreads) {
         p.win[((par ^ 1) * half + i) * kWinPad] = 0ull;
+        p.win[((par ^ 1) * half + i) * kWinPad + 1] = 0ull;
+      }
     }
     for (int k = 1; k <= p.g; ++k) {
       // ---- A = W1[x_{k-1}], gathered by the epilogue warps into the swizzled
@@ -479,8 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (k == 1) {
             x = p.anchor[b];
           } else {
-            const unsigned long long wv = __ldcg(win + ((size_t)(k - 2) * p.rowsG + b) * kWinPad);
-            x = wv ? win_token(wv) : -1;
+            x = drawn_token(__ldcg(win + ((size_t)(k - 2) * p.rowsG + b) * kWinPad + 1));
           }
           if (x < 0 || x >= p.V) {
             if (k == 1) {
@@ -613,74 +563,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 
-      // ---- the token inside this CTA's best block of the row: argmax_v
-      // (z_v + G_v) over its 64 tokens, G_v from the draft-token stream at
-      // (b, k, v). Every MMA of this step has completed once both sets are
-      // here (each waited for all of its tiles), so the A operand is free
-      // until the next gather: each thread parks its best block's z there
-      // (its slot), the two sets' keys are compared per row, and the two
-      // threads of the row each screen half of the better block's tokens
-      // with rolled loops (straight-line code for 64 Gumbels would not fit
-      // the instruction cache); the partial results meet in the other slot.
+      // ---- step end. Every MMA of this step has completed once both sets
+      // are here (each waited for all of its tiles), so the A operand is free
+      // until the next gather.
+      // (1) Per row, this CTA's candidate is the better of the two sets' best
+      // blocks (larger key, then the smaller block). Its (block key, block)
+      // goes into the row's winner word by atomic max, and the thread that
+      // holds it parks the block's z in the A region.
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
       const bool cand = valid && bs != kNoIdx && !*abort;
       float* keyx = reinterpret_cast<float*>(smem + L.misc + 64);
       uint16_t* blkx = reinterpret_cast<uint16_t*>(smem + L.misc + 64 + kEpiThreads * 4);
-      float4* slot0 = reinterpret_cast<float4*>(smem + L.a) + (size_t)m * (kBlk / 4);  // set 0's slot of row m
-      float4* slot1 = slot0 + (size_t)kTcRows * (kBlk / 4);
-      const int sw = lane & 7;  // chunk swizzle: a quarter-warp's 16-byte accesses hit distinct banks
+      unsigned* own = reinterpret_cast<unsigned*>(smem + L.misc + 32);  // [4] rows whose token this CTA draws
       keyx[set * kTcRows + m] = cand ? bk : -INFINITY;
-      blkx[set * kTcRows + m] = (uint16_t)(cand ? bs : 0);
-      if (cand) {
-        float4* zs = set ? slot1 : slot0;
+      blkx[set * kTcRows + m] = (uint16_t)(cand ? bs : 0xFFFF);
+      if (ew == 0 && lane < kTcRows / 32) own[lane] = 0u;
+      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+      const bool mine = cand && set == cta_best_set(keyx, blkx, m);
+      if (mine) {
+        unsigned long long* wrow = win + ((size_t)(k - 1) * p.rowsG + b) * kWinPad;
+        float4* zs = reinterpret_cast<float4*>(smem + L.a) + (size_t)m * (kBlk / 4);
 #pragma unroll
-        for (int c4 = 0; c4 < kBlk / 4; ++c4)
-          zs[c4 ^ sw] = make_float4(zb[4 * c4], zb[4 * c4 + 1], zb[4 * c4 + 2], zb[4 * c4 + 3]);
+        for (int c4 = 0; c4 < kBlk / 4; ++c4)  // chunk swizzle: a quarter-warp's stores hit distinct banks
+          zs[c4 ^ (m & 7)] = make_float4(zb[4 * c4], zb[4 * c4 + 1], zb[4 * c4 + 2], zb[4 * c4 + 3]);
+        atomicMax(wrow, pack_win(bk, bs));
       }
+      // every set writes its slot every step (a set without blocks writes the
+      // neutral partial), so no entry of an earlier launch is combined
+      if (valid && !*abort)
+        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] = make_float2(M, S);
+      // (2) the winner words of step k are final once every CTA has passed here
+      grid_sync(p, gctr, (unsigned)(p.G * (2 * k - 1)), leader, abort);
+      if (mine && !*abort && win_block(__ldcg(win + ((size_t)(k - 1) * p.rowsG + b) * kWinPad)) == bs)
+        atomicOr(own + (m >> 5), 1u << (m & 31));
       asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      const float kA = keyx[m], kB = keyx[kTcRows + m];
-      const int wset = kB > kA ? 1 : 0;  // the row's better candidate of this CTA (set 0 on ties)
-      const bool any = valid && (kA > -INFINITY || kB > -INFINITY) && !*abort;
-      const int wbs = blkx[wset * kTcRows + m];
-      const float4* zw = wset ? slot1 : slot0;
-      float4* zl = wset ? slot0 : slot1;  // the other slot carries the two halves' results
-      if (any) {
-        const DrawPart d = draw_screen(zw, sw, p.rng, b, k, wbs * kBlk, set * (kBlk / 8));
-        zl[set] = make_float4(d.k1, d.k2, d.z1, __int_as_float(d.i1));
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
-      int bx = -1;
-      float bzx = 0.f;
-      if (any && set == wset) {
-        const float4 h0 = zl[0], h1 = zl[1];
-        const DrawPart d = draw_join(DrawPart{h0.x, h0.y, h0.z, __float_as_int(h0.w)},
-                                     DrawPart{h1.x, h1.y, h1.z, __float_as_int(h1.w)});
-        int xi = d.i1;
-        bzx = d.z1;
-        if (xi >= 0 && !(d.k1 - d.k2 > kScreenGap)) xi = draw_exact(zw, sw, p.rng, b, k, wbs * kBlk, &bzx);
-        if (xi < 0) {
-          raise_status(p.status, DSPARK_ENUMERIC);  // non-finite logits in the block
-          *abort = 1;
-        } else {
-          bx = wbs * kBlk + xi;
-          // whichever CTA's candidate wins the row, its W1 row is gathered by
-          // every CTA after the barrier: start bringing it into L2 now
-          const char* w1row = reinterpret_cast<const char*>(W1 + (size_t)bx * p.r);
-          for (int o = 0; o < p.r * 2; o += 128) tc::prefetch_l2(w1row + o);
+      // (3) the token inside the winning block, drawn by the CTA that owns the
+      // block: one warp per owned row, two tokens per lane, exact keys
+      // z_v + G_v with G_v from the draft-token stream at (b, k, v); the token
+      // and its z go into the second word of the row's winner line
+      if (!aborted()) {
+        for (int rr = ew; rr < kTcRows; rr += 4 * kSets) {
+          if (!((own[rr >> 5] >> (rr & 31)) & 1u)) continue;  // the same smem word for the whole warp
+          const int br = grp * kTcRows + rr;
+          const int v0 = (int)blkx[cta_best_set(keyx, blkx, rr) * kTcRows + rr] * kBlk;
+          const float4 zz = reinterpret_cast<const float4*>(smem + L.a)[(size_t)rr * (kBlk / 4) + ((lane >> 1) ^ (rr & 7))];
+          const int i0 = 2 * lane;  // tokens i0 and i0 + 1 of the block: half of chunk lane / 2
+          const float za = (lane & 1) ? zz.z : zz.x, zb1 = (lane & 1) ? zz.w : zz.y;
+          const uint4 o = p.rng.block4(kDraftToken, br, k, v0 + i0);
+          const uint32_t ua = (lane & 1) ? o.z : o.x, ub = (lane & 1) ? o.w : o.y;
+          KeyIdx kb = better(KeyIdx{za + gumbel(ua), i0}, KeyIdx{zb1 + gumbel(ub), i0 + 1});
+          kb = warp_best(kb);
+          const int src = kb.idx >> 1;
+          const float zsel = __shfl_sync(0xFFFFFFFFu, (kb.idx & 1) ? zb1 : za, src);
+          if (lane == 0) {
+            if (!(kb.key > -INFINITY)) {
+              raise_status(p.status, DSPARK_ENUMERIC);  // no finite logit in the block
+              *abort = 1;
+            } else {
+              const int x = v0 + kb.idx;
+              __stcg(win + ((size_t)(k - 1) * p.rowsG + br) * kWinPad + 1,
+                     ((unsigned long long)__float_as_uint(zsel) << 32) | (unsigned long long)(uint32_t)(x + 1));
+              // every CTA gathers this row after the next barrier: bring it into L2 now
+              const char* w1row = reinterpret_cast<const char*>(W1 + (size_t)x * p.r);
+              for (int o2 = 0; o2 < p.r * 2; o2 += 128) tc::prefetch_l2(w1row + o2);
+            }
+          }
         }
       }
-
-      // ---- publish the row's candidate (block key, token) and each set's
-      // partials (max, sum exp, z of its token, its token)
-      if (valid && !*abort) {
-        if (bx >= 0) atomicMax(win + ((size_t)(k - 1) * p.rowsG + b) * kWinPad, pack_win(bk, bx));
-        // every set writes its slot every step (a set without blocks writes
-        // the neutral partial), so no entry of an earlier launch is combined
-        p.dpart[((size_t)(k - 1) * p.rowsG + b) * p.P + kSets * cg + set] =
-            make_float4(M, S, bzx, __int_as_float(bx));
-      }
-      // the winner words of step k are final once every CTA has passed here
-      grid_sync(p, gctr, (unsigned)(p.G * k), leader, abort);
+      // (4) the step's tokens are final once every CTA has passed here
+      grid_sync(p, gctr, (unsigned)(p.G * 2 * k), leader, abort);
     }
 
     // ---- after the last step: per (row, step), one warp combines the
@@ -692,20 +643,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
         const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
         const int Pr = kSets * group_ctas(p.G, p.nG, br / kTcRows);
-        const unsigned long long wx = __ldcg(win + ((size_t)kk * p.rowsG + br) * kWinPad);
-        int xp = kk == 0 ? p.anchor[br] : win_token(__ldcg(win + ((size_t)(kk - 1) * p.rowsG + br) * kWinPad));
-        if (wx == 0ull) {
+        const unsigned long long tw = __ldcg(win + ((size_t)kk * p.rowsG + br) * kWinPad + 1);
+        int xp = kk == 0 ? p.anchor[br] : drawn_token(__ldcg(win + ((size_t)(kk - 1) * p.rowsG + br) * kWinPad + 1));
+        const int x = drawn_token(tw);
+        if (x < 0 || x >= p.V) {
           if (lane == 0) raise_status(p.status, DSPARK_ENUMERIC);
           continue;
         }
-        const int x = win_token(wx);
+        const float zx = __uint_as_float((uint32_t)(tw >> 32));
         if (xp < 0 || xp >= p.V) xp = 0;  // an anchor out of range was reported at the step-1 gather
-        const float4* pr = p.dpart + ((size_t)kk * p.rowsG + br) * p.P;
-        float4 dd[kMaxPartLanes];
+        const float2* pr = p.dpart + ((size_t)kk * p.rowsG + br) * p.P;
+        float2 dd[kMaxPartLanes];
 #pragma unroll
         for (int u = 0; u < kMaxPartLanes; ++u) {
           const int i = lane + 32 * u;
-          dd[u] = i < Pr ? __ldcg(pr + i) : make_float4(-INFINITY, 0.f, 0.f, __int_as_float(-1));
+          dd[u] = i < Pr ? __ldcg(pr + i) : make_float2(-INFINITY, 0.f);
         }
         // w^T [h_k; W1[x_{k-1}]]: the hidden half (H floats, 16-byte loads
         // when H allows, ten per lane in flight), then the W1 half
@@ -745,20 +697,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         MS ms{-INFINITY, 0.f};
-        float zx = 0.f;
-        bool mine = false;  // this lane holds the winning set's partial
 #pragma unroll
-        for (int u = 0; u < kMaxPartLanes; ++u) {
-          ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
-          if (__float_as_int(dd[u].w) == x) {
-            zx = dd[u].z;
-            mine = true;
-          }
-        }
+        for (int u = 0; u < kMaxPartLanes; ++u) ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
         ms = warp_ms(ms);
         cd = warp_sum(cd);
-        const unsigned hold = __ballot_sync(0xFFFFFFFFu, mine);
-        zx = __shfl_sync(0xFFFFFFFFu, zx, hold ? __ffs(hold) - 1 : 0);
         if (lane == 0) {
           const size_t o = (size_t)br * p.g + kk;
           const float L2 = ms_log(ms);
@@ -766,7 +708,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.pd_tok[o] = expf(zx - L2);
           p.lse[o] = L2;
           const float cf = 1.f / (1.f + expf(-cd / p.T[kk]));
-          if (!isfinite(cf) || !hold) raise_status(p.status, DSPARK_ENUMERIC);
+          if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
           p.conf[o] = cf;
         }
       }
