@@ -78,6 +78,10 @@ constexpr int kUStage = kTcRows * kBlk * 4;  // 32 KB: two 128 x 32 fp32 boxes
 constexpr int kUBox = kTcRows * 32 * 4;      // 16 KB
 constexpr int kAccCols = kTileBlocks * kBlk; // 128 columns per accumulator
 constexpr int kNAcc = 4;                     // accumulators: the MMA runs up to three tiles ahead
+// U blocks of step k + 1 the producer may load before the tokens of step k are
+// final: more would keep HBM busy across the step boundary, but they queue
+// ahead of the boundary's latency-bound traffic (barrier atomics, W1 rows).
+constexpr int kUEarly = 6;
 constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
@@ -99,8 +103,8 @@ struct TcSmem {  // byte offsets into dynamic shared memory (1024-aligned base)
     s.u = s.w2 + kNW * kW2Stage;
     s.bars = s.u + kNU * kUStage;
     // w2 full/empty, u full, u empty, t full/empty, a_full, drain, acc_u
-    // (accumulator holds U), the copier's drain
-    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 2 + kNAcc + 1);
+    // (accumulator holds U), the copier's drain, u_go
+    s.misc = s.bars + 8 * (2 * kNW + 2 * kNU + 2 * kNAcc + 2 + kNAcc + 2);
     // misc: TMEM address and abort word (64 B), then the step-end exchange of
     // each set's best block per row: key [kSets][128] fp32, block [kSets][128] u16
     s.total = s.misc + 64 + kEpiThreads * 4 + kEpiThreads * 2;
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t drain = a_full + 8u;
   auto acc_u = [&](int i) { return a_full + 16u + 8u * i; };
   const uint32_t drain_c = a_full + 16u + 8u * kNAcc;
+  const uint32_t u_go = drain_c + 8u;  // completes once per step: that step's tokens are final
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
 
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::mbar_init(drain, 1);
     for (int i = 0; i < kNAcc; ++i) tc::mbar_init(acc_u(i), 1);
     tc::mbar_init(drain_c, 1);
+    tc::mbar_init(u_go, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -289,6 +295,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int k = 1; k <= p.g && ok; ++k) {
         for (int i = 0; i < nbc && ok; ++i) {
           const int gb = (k - 1) * nbc + i, us = gb % kNU, v = (blo + i) * kBlk;
+          if (k > 1 && i == kUEarly) ok = tc::mbar_wait(u_go, (k - 2) & 1, abort);
+          if (!ok) break;
           ok = tc::mbar_wait(u_empty(us), ((gb / kNU) & 1) ^ 1, abort);
           if (!ok) break;
           tc::mbar_arrive_expect_tx(u_full(gb), kUStage);
@@ -625,13 +633,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      ((unsigned long long)__float_as_uint(zsel) << 32) | (unsigned long long)(uint32_t)(x + 1));
               // every CTA gathers this row after the next barrier: bring it into L2 now
               const char* w1row = reinterpret_cast<const char*>(W1 + (size_t)x * p.r);
-              for (int o2 = 0; o2 < p.r * 2; o2 += 128) tc::prefetch_l2(w1row + o2);
+              tc::bulk_prefetch_l2(w1row, (uint32_t)(p.r * 2));
             }
           }
         }
       }
       // (4) the step's tokens are final once every CTA has passed here
       grid_sync(p, gctr, (unsigned)(p.G * 2 * k), leader, abort);
+      if (leader) tc::mbar_arrive(u_go);  // the U producer may run ahead into step k + 1
     }
 
     // ---- after the last step: per (row, step), one warp combines the

@@ -127,6 +127,13 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 }
 
 // ---------------------------------------------------------------- TMA
+// Bulk prefetch of [p, p + bytes) into L2 by the copy engine (p 16-byte
+// aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
