@@ -114,13 +114,14 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   cudaGetLastError();
   geo.rchunks = geo.num_sms > kResidChunks ? geo.num_sms : kResidChunks;
   const size_t o_rpart = carve(sizeof(float2) * (size_t)d.B * geo.rchunks);
-  size_t o_dpart = 0, o_dwin = 0;
+  size_t o_dpart = 0, o_dwin = 0, o_hpart = 0;
   if (geo.tc_ok) {
     if (draft_tc_configure(ws) != cudaSuccess) geo.tc_ok = 0;
   }
   if (geo.tc_ok) {
     o_dpart = carve(sizeof(float2) * draft_tc_partials(d, geo.tc_grid));
     o_dwin = carve(sizeof(unsigned long long) * draft_tc_winners(d));
+    o_hpart = carve(sizeof(float) * draft_tc_hidden_partials(d));
   }
   if (plan_configure() != cudaSuccess) {
     delete ws;
@@ -151,6 +152,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
   s.dpart = geo.tc_ok ? reinterpret_cast<float2*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
+  s.hpart = geo.tc_ok ? reinterpret_cast<float*>(base + o_hpart) : nullptr;
   ws->use_tc = geo.tc_ok;
   if (cudaMemset(ws->arena, 0, off) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(ws->arena);

@@ -90,6 +90,7 @@ struct Scratch {
   unsigned long long* dwin;  // [2][gamma][groups*128] lines of 16 words: word 0 the packed (block key,
                              // block) winner, word 1 the token drawn in it; the two halves alternate
                              // between launches
+  float* hpart;           // [B*gamma][ceil(H/1024)] partial sums of w_h . h_k over 1024-float chunks
   unsigned* barrier;      // [8] draft kernel words: [2] launch count, [4 + launch parity] barrier arrivals
 };
 
@@ -167,6 +168,7 @@ int draft_tc_supported(const dspark_dims& d);
 cudaError_t draft_tc_configure(dspark_ws* ws);
 size_t draft_tc_partials(const dspark_dims& d, int grid);  // float2 entries of Scratch::dpart
 size_t draft_tc_winners(const dspark_dims& d);             // entries of Scratch::dwin
+size_t draft_tc_hidden_partials(const dspark_dims& d);     // floats of Scratch::hpart
 
 int resid_tc_supported(const dspark_dims& d);
 cudaError_t resid_tc_configure(dspark_ws* ws);

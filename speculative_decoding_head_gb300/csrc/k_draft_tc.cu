@@ -85,6 +85,7 @@ constexpr int kUEarly = 6;
 constexpr int kTmemCols = kNAcc * kAccCols;  // all of TMEM
 constexpr int kMaxGroups = 8;       // B <= 1024
 constexpr int kMaxPartLanes = 16;   // partials per lane in the finalize (kSets per CTA)
+constexpr int kHChunk = 32 * 8;      // float4 of h per warp task of the hidden pass (eight per lane in flight)
 // Winner words are kWinPad words apart (one 128-byte line per row), so that
 // the CTAs' atomic maxima on different rows do not queue on shared lines.
 constexpr int kWinPad = 16;
@@ -126,6 +127,7 @@ struct TcParams {
   float* lse;
   float* conf;
   float2* dpart;            // [g][rowsG][P]: (max, sum exp) of a row's blocks per CTA and set
+  float* hpart;             // [B*g][nhc]: w_h . h over chunks of kHChunk float4 (H % 4 == 0)
   unsigned long long* win;  // [2][g][rowsG] x kWinPad: packed (block key, token), 0 = none
   unsigned* bar;            // [2] launches (parity of win and counters), [4 + parity] grid-barrier arrivals
   int* status;
@@ -638,6 +640,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      // the hidden halves of the confidence logits, w_h . h_k for every row
+      // and step, do not depend on the draws: before the last barrier every
+      // warp sums whole chunks of h (eight 16-byte loads per lane in flight)
+      // into per-chunk partials, which the combine below adds in order
+      if (k == p.g && (p.H & 3) == 0 && p.H > 0 && !aborted()) {
+        const int nq = p.H / 4, nhc = (nq + kHChunk - 1) / kHChunk;
+        const int ntask = p.B * p.g * nhc, nw = p.G * (kEpiThreads / 32);
+        const float4* w4 = reinterpret_cast<const float4*>(p.w);
+        for (int ti = c * (kEpiThreads / 32) + ew; ti < ntask; ti += nw) {
+          const int it = ti / nhc, ch = ti - it * nhc;
+          const float4* h4 = reinterpret_cast<const float4*>(p.h + (size_t)it * p.H);
+          float4 a[8], b4[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = ch * kHChunk + 32 * u + lane;
+            a[u] = i < nq ? __ldcs(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);  // h is read once
+            b4[u] = i < nq ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          float hs = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            hs = fmaf(a[u].x, b4[u].x, hs);
+            hs = fmaf(a[u].y, b4[u].y, hs);
+            hs = fmaf(a[u].z, b4[u].z, hs);
+            hs = fmaf(a[u].w, b4[u].w, hs);
+          }
+          hs = warp_sum(hs);
+          if (lane == 0) p.hpart[ti] = hs;
+        }
+      }
       // (4) the step's tokens are final once every CTA has passed here
       grid_sync(p, gctr, (unsigned)(p.G * 2 * k), leader, abort);
       if (leader) tc::mbar_arrive(u_go);  // the U producer may run ahead into step k + 1
@@ -652,6 +684,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int pi = c * (kEpiThreads / 32) + ew; pi < p.B * p.g; pi += nw) {
         const int br = pi / p.g, kk = pi - br * p.g;  // step kk + 1
         const int Pr = kSets * group_ctas(p.G, p.nG, br / kTcRows);
+        const float Tk = __ldg(p.T + kk);
         const unsigned long long tw = __ldcg(win + ((size_t)kk * p.rowsG + br) * kWinPad + 1);
         int xp = kk == 0 ? p.anchor[br] : drawn_token(__ldcg(win + ((size_t)(kk - 1) * p.rowsG + br) * kWinPad + 1));
         const int x = drawn_token(tw);
@@ -668,29 +701,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int i = lane + 32 * u;
           dd[u] = i < Pr ? __ldcg(pr + i) : make_float2(-INFINITY, 0.f);
         }
-        // w^T [h_k; W1[x_{k-1}]]: the hidden half (H floats, 16-byte loads
-        // when H allows, ten per lane in flight), then the W1 half
+        // w^T [h_k; W1[x_{k-1}]]: the hidden half from the chunk partials
+        // (lane j holds chunk j, chunks beyond 32 folded in order) or, when
+        // H % 4 != 0, from h directly; then the W1 half
         float cd = 0.f;
         const float* hr = p.h + ((size_t)br * p.g + kk) * p.H;
         if ((p.H & 3) == 0) {
-          const float4* h4 = reinterpret_cast<const float4*>(hr);
-          const float4* w4 = reinterpret_cast<const float4*>(p.w);
-          for (int i0 = lane; i0 < p.H / 4; i0 += 10 * 32) {
-            float4 a[10], b4[10];
-#pragma unroll
-            for (int u = 0; u < 10; ++u) {
-              const int i = i0 + 32 * u;
-              a[u] = i < p.H / 4 ? __ldcs(h4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);  // h is read once
-              b4[u] = i < p.H / 4 ? __ldg(w4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int u = 0; u < 10; ++u) {
-              cd = fmaf(a[u].x, b4[u].x, cd);
-              cd = fmaf(a[u].y, b4[u].y, cd);
-              cd = fmaf(a[u].z, b4[u].z, cd);
-              cd = fmaf(a[u].w, b4[u].w, cd);
-            }
-          }
+          const int nhc = (p.H / 4 + kHChunk - 1) / kHChunk;
+          for (int j = lane; j < nhc; j += 32) cd += __ldcg(p.hpart + (size_t)pi * nhc + j);
         } else {
           for (int i = lane; i < p.H; i += 32) cd = fmaf(__ldcs(hr + i), __ldg(p.w + i), cd);
         }
@@ -705,10 +723,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             cd = fmaf(f.y, wr[2 * e + 1], cd);
           }
         }
-        MS ms{-INFINITY, 0.f};
+        // this lane's partials: the largest max first, then the scaled sums
+        // (independent exponentials rather than a chain of pairwise combines)
+        float mx = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kMaxPartLanes; ++u) ms = ms_combine(ms, MS{dd[u].x, dd[u].y});
-        ms = warp_ms(ms);
+        for (int u = 0; u < kMaxPartLanes; ++u) mx = fmaxf(mx, dd[u].x);
+        float sx = 0.f;
+        if (mx > -INFINITY) {
+#pragma unroll
+          for (int u = 0; u < kMaxPartLanes; ++u)
+            if (dd[u].x > -INFINITY) sx += dd[u].y * __expf(dd[u].x - mx);
+        }
+        MS ms = warp_ms(MS{mx, sx});
         cd = warp_sum(cd);
         if (lane == 0) {
           const size_t o = (size_t)br * p.g + kk;
@@ -716,7 +742,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           p.tokens[o] = x;
           p.pd_tok[o] = expf(zx - L2);
           p.lse[o] = L2;
-          const float cf = 1.f / (1.f + expf(-cd / p.T[kk]));
+          const float cf = 1.f / (1.f + expf(-cd / Tk));
           if (!isfinite(cf)) raise_status(p.status, DSPARK_ENUMERIC);
           p.conf[o] = cf;
         }
@@ -789,6 +815,11 @@ size_t draft_tc_partials(const dspark_dims& d, int grid) {
   return (size_t)d.gamma * nG * kTcRows * kSets * Ggmax;
 }
 
+size_t draft_tc_hidden_partials(const dspark_dims& d) {
+  const int nq = d.H / 4;
+  return (size_t)d.B * d.gamma * (size_t)((nq + kHChunk - 1) / kHChunk + 1);
+}
+
 size_t draft_tc_winners(const dspark_dims& d) {
   const int nG = (d.B + kTcRows - 1) / kTcRows;
   return (size_t)2 * d.gamma * nG * kTcRows * kWinPad;
@@ -843,6 +874,7 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
   p.lse = a.lse;
   p.conf = a.conf;
   p.dpart = ws->s.dpart;
+  p.hpart = ws->s.hpart;
   p.win = ws->s.dwin;
   p.bar = ws->s.barrier;
   p.status = ws->s.status;
