@@ -64,16 +64,6 @@ __device__ __forceinline__ bool before(unsigned long long ka, unsigned ia, unsig
   return ka > kb || (ka == kb && ia < ib);
 }
 
-// One compare-exchange seen from index i: keep the element that goes first
-// iff (i is the lower index of its pair) == (its bitonic block ascends).
-__device__ __forceinline__ void keep(unsigned long long& k, unsigned& id, unsigned long long pk, unsigned pid,
-                                     bool keep_first) {
-  if (before(pk, pid, k, id) == keep_first) {
-    k = pk;
-    id = pid;
-  }
-}
-
 // Sort the M candidates of confidences c [B, g] into admission order and
 // load ranks e * 1024 + t into (k, id). (k0, i0), (k1, i1): two buffers of M
 // (value, id).
