@@ -11,6 +11,7 @@ namespace dspark {
 
 // Tunables of the launch shapes (none of them changes a result).
 constexpr int kResidChunks = 32;    // CTAs per rejected request in the SIMT residual pass
+constexpr int kRnnHpSlices = 10;    // K slices of the RNN head's h projection (partial products the cell adds)
 
 struct DraftArgs {
   const float* U;
@@ -156,8 +157,19 @@ cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr
                              int* launches);
 cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void* Wr, const float* Hp, float* S,
                             float* ovec, int k, cudaStream_t st, int* launches);
+// hl: scratch for h split into bf16 hi | lo (rnn_hsplit_bytes), or null: the
+// h projection then runs on CUDA cores
 cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
-                             float* ovec, cudaStream_t st, int* launches);
+                             float* ovec, void* hl, cudaStream_t st, int* launches);
+// The h projection on tcgen05 (k_rnn_tc.cu): shapes it takes (bf16 weights,
+// H % 64 == 0, r % 64 == 0, r <= 256), whether this workspace runs it, the
+// bytes of its hi | lo copy of h, and its launch (same Hp layout as
+// launch_rnn_hproj).
+bool rnn_hproj_tc_shape(const dspark_dims& d);
+bool rnn_hproj_tc_supported(const dspark_ws* ws);
+size_t rnn_hsplit_bytes(const dspark_dims& d);
+cudaError_t launch_rnn_hproj_tc(const dspark_ws* ws, const float* h, const void* Wr, float* Hp, void* hl_scratch,
+                                cudaStream_t st, int* launches);
 // rowtab (may be null): also write each packed row's (b, j, lengths[b], row_off[b])
 cudaError_t launch_plan(const dspark_ws* ws, const float* conf, const double* sps, int32_t* lengths,
                         int32_t* row_off, int4* rowtab, cudaStream_t st, int* launches);

@@ -244,9 +244,14 @@ cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStrea
 }
 
 cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
-                             float* ovec, cudaStream_t st, int* launches) {
+                             float* ovec, void* hl, cudaStream_t st, int* launches) {
   cudaError_t e = launch_conf_hidden(ws, a.h, a.w, st, launches);
-  if (e == cudaSuccess) e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
+  if (e == cudaSuccess) {
+    if (hl && rnn_hproj_tc_supported(ws))
+      e = launch_rnn_hproj_tc(ws, a.h, Wr, Hp, hl, st, launches);
+    else
+      e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
+  }
   if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0 (buffer 0)
   if (e != cudaSuccess) return e;
   const RnnStep rnn{Wr, Hp, S, ovec, ws->use_tc && ws->geo.resid_tc_ok && ws->d.r <= 256};

@@ -29,7 +29,7 @@ namespace {
 
 constexpr int kHpTile = 128;    // output tile of k_rnn_hproj (rows x columns)
 constexpr int kHpK = 16;        // K step
-constexpr int kHpSplit = 10;    // K is split over 10 CTAs (two per SM at prod); each writes its own partial product
+constexpr int kHpSplit = kRnnHpSlices;  // K is split over 10 CTAs (two per SM at prod); each writes its own partial product
 constexpr int kCellThreads = 256;
 constexpr int kCellJ = 16;  // state entries per CTA of k_rnn_cell
 constexpr int kCellB = 16;  // requests per CTA of k_rnn_cell (kCellJ x kCellB = threads)
@@ -261,7 +261,9 @@ using namespace dspark;
 
 extern "C" size_t dspark_rnn_draft_scratch_bytes(const dspark_ws* ws) {
   if (!ws) return 0;
-  return hp_bytes(ws->d) + state_bytes(ws->d);
+  // the hi | lo copy of h for the tcgen05 h projection, wherever the shape allows it
+  // (whichever compute path the workspace is set to when the call runs)
+  return hp_bytes(ws->d) + state_bytes(ws->d) + (rnn_hproj_tc_shape(ws->d) ? rnn_hsplit_bytes(ws->d) : 0);
 }
 
 extern "C" dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2,
@@ -279,9 +281,11 @@ extern "C" dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const v
   char* base = static_cast<char*>(scratch);
   float* Hp = reinterpret_cast<float*>(base);
   float* S = reinterpret_cast<float*>(base + hp_bytes(d));
+  void* hl = rnn_hproj_tc_shape(d) ? static_cast<void*>(base + hp_bytes(d) + state_bytes(d)) : nullptr;
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
   int launches = 0;
-  const cudaError_t e = launch_rnn_draft(ws, a, Wr, Hp, S, ovec, reinterpret_cast<cudaStream_t>(stream), &launches);
+  const cudaError_t e =
+      launch_rnn_draft(ws, a, Wr, Hp, S, ovec, hl, reinterpret_cast<cudaStream_t>(stream), &launches);
   ws->last_launches = launches;
   if (e == cudaSuccess) return DSPARK_OK;
   fprintf(stderr, "dspark: CUDA error %s\n", cudaGetErrorString(e));
