@@ -189,6 +189,11 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
 // pass 0: per-CTA (max, sum exp) of z_d and z_t and z_d at x*; pass 1: per-CTA
 // sum |p_d - p_t| (needs lse_d, lse_t). Grid = ws->geo.num_sms.
 cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);
+// The same two passes with the positions as MMA rows (k_rowpass.cu), where
+// rowpass_supported: the same partial layout ([n][num_sms], neutral values in
+// the slots no CTA fills).
+bool rowpass_supported(const dspark_ws* ws);
+cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);
 // One draft step of the RNN head on tcgen05: Scratch::blk = the block
 // log-masses of z = U_k + o_k W2 (o_k from ovec, split into bf16 hi + lo).
 cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,

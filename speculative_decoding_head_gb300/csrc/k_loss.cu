@@ -138,7 +138,8 @@ extern "C" dspark_status dspark_train_loss(dspark_ws* ws, const float* U, const 
       (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
     return DSPARK_EINVAL;
   if (!(tau > 0.0) || !(tau < INFINITY)) return DSPARK_EINVAL;
-  if (!ws->geo.resid_tc_ok) return DSPARK_EUNSUPPORTED;
+  const bool rows = rowpass_supported(ws);
+  if (!rows && !ws->geo.resid_tc_ok) return DSPARK_EUNSUPPORTED;
   const dspark_dims& d = ws->d;
   const int n = d.B * d.gamma, G = ws->geo.num_sms;
   const LossScratch L = LossScratch::make((size_t)n, (size_t)G);
@@ -149,12 +150,13 @@ extern "C" dspark_status dspark_train_loss(dspark_ws* ws, const float* U, const 
              reinterpret_cast<float*>(base + L.lse_t), reinterpret_cast<double*>(base + L.term)};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int blocks = (n + kLossWarps - 1) / kLossWarps;
-  cudaError_t e = launch_loss_tc(ws, a, 0, st);
+  auto pass = [&](int ps) { return rows ? launch_loss_rowpass(ws, a, ps, st) : launch_loss_tc(ws, a, ps, st); };
+  cudaError_t e = pass(0);
   if (e == cudaSuccess) {
     k_loss_lse<<<blocks, 32 * kLossWarps, 0, st>>>(a.lpart, n, G, a.lse_d, a.lse_t);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess) e = launch_loss_tc(ws, a, 1, st);
+  if (e == cudaSuccess) e = pass(1);
   if (e == cudaSuccess) {
     k_loss_pos<<<blocks, 32 * kLossWarps, 0, st>>>(a.l1part, a.zx, a.lse_d, conf, n, d.gamma, G, tau, ce, l1, bce,
                                                    a.term, ws->s.status);
