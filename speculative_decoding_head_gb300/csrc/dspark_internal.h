@@ -192,8 +192,16 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
 // The same two passes with the positions as MMA rows (k_rowpass.cu), where
 // rowpass_supported: the same partial layout ([n][num_sms], neutral values in
 // the slots no CTA fills).
-bool rowpass_supported(const dspark_ws* ws);
+// n: the rows (positions for the loss, requests for the RNN and PCTree passes).
+bool rowpass_supported(const dspark_ws* ws, int n);
 cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);
+// One RNN draft step's block log-masses into Scratch::blk (as launch_rnn_blocks_tc),
+// and one PCTree expansion's block log-masses and maxima (as launch_tree_blocks_tc).
+cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
+                                      cudaStream_t st);
+cudaError_t launch_tree_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                       const int32_t* tok, const int32_t* dep, const int4* state, int N, float* blk,
+                                       float* bmax, cudaStream_t st);
 // One draft step of the RNN head on tcgen05: Scratch::blk = the block
 // log-masses of z = U_k + o_k W2 (o_k from ovec, split into bf16 hi + lo).
 cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,

@@ -223,8 +223,9 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
       const cudaError_t e = launch_rnn_cell(ws, a, rnn->Wr, rnn->Hp, rnn->S, rnn->ovec, k, st, launches);
       if (e != cudaSuccess) return e;
     }
-    if (rnn && rnn->tc) {  // the block pass on tcgen05
-      const cudaError_t e = launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
+    if (rnn && rnn->tc) {  // the block pass on tcgen05 (requests as MMA rows where the shape allows)
+      const cudaError_t e = rowpass_supported(ws, d.B) ? launch_rnn_blocks_rowpass(ws, a.U, a.W2, ovec, k, st)
+                                                       : launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
       if (e != cudaSuccess) return e;
     } else {
       k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(

@@ -138,7 +138,7 @@ extern "C" dspark_status dspark_train_loss(dspark_ws* ws, const float* U, const 
       (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0)
     return DSPARK_EINVAL;
   if (!(tau > 0.0) || !(tau < INFINITY)) return DSPARK_EINVAL;
-  const bool rows = rowpass_supported(ws);
+  const bool rows = rowpass_supported(ws, ws->d.B * ws->d.gamma);
   if (!rows && !ws->geo.resid_tc_ok) return DSPARK_EUNSUPPORTED;
   const dspark_dims& d = ws->d;
   const int n = d.B * d.gamma, G = ws->geo.num_sms;

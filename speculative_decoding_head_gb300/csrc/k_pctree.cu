@@ -643,7 +643,9 @@ cudaError_t launch_pctree_build(const dspark_ws* ws, const float* U, const void*
   const size_t esm = sizeof(float) * d.r;
   for (int step = 0; step < N; ++step) {
     if (tc) {
-      const cudaError_t e = launch_tree_blocks_tc(ws, U, W1, W2, tok, dep, ts.state, N, ws->s.blk, ts.bmax, st);
+      const cudaError_t e = rowpass_supported(ws, d.B)
+                                ? launch_tree_blocks_rowpass(ws, U, W1, W2, tok, dep, ts.state, N, ws->s.blk, ts.bmax, st)
+                                : launch_tree_blocks_tc(ws, U, W1, W2, tok, dep, ts.state, N, ws->s.blk, ts.bmax, st);
       if (e != cudaSuccess) return e;
     } else {
       const int chunks = max(1, (nblk + 31) / 32);

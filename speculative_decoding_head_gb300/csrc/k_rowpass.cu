@@ -1,4 +1,6 @@
-// k_rowpass.cu -- the training objective's vocabulary passes, row-oriented on tcgen05.
+// k_rowpass.cu -- row-oriented vocabulary passes on tcgen05: the training
+// objective's two passes, the RNN head's per-step block masses, and the
+// PCTree expansion's block masses and maxima.
 //
 // deepseek.csdn.net reading §6, eqs. (9)-(12): every teacher-forced position
 // i = (b, k) has draft logits z_d = U[b, k] + W1[x*_{k-1}] W2 (x*_{-1} = the
@@ -28,6 +30,19 @@
 // partial per position into slot cg (its index in the group) of the
 // [n][G] partial arrays, and neutral values into the slots no CTA of the
 // group owns, so the combine kernels read G slots as before.
+//
+// The same pass with requests as rows serves two more computations:
+//   - one draft step of the RNN head (eq. (6), same reading §4.2): rows are
+//     requests, A = o_k split into bf16 hi and lo, both images copied into
+//     tensor memory (they do not fit beside the rings in shared memory) and
+//     both MMAs accumulate into the tile (A read from TMEM); U_k arrives by
+//     a 3-D box; per row and 64-token block the log-mass log sum exp z goes
+//     to blk [B][nblk] for the pick;
+//   - one PCTree expansion (zdszero "spec_dspark", section "后续工作"): rows
+//     are requests, A = W1[token of the node being expanded], and U of the
+//     node's depth differs per row, so the epilogue adds it from global
+//     memory (the accumulator starts at zero); per block the log-mass and
+//     the maximum of z.
 // Every wait is bounded; a timeout sets DSPARK_ETIMEOUT and every role ends.
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -60,6 +75,12 @@ constexpr int kRpNAcc = 2;                     // accumulators (and as many P bu
 constexpr int kRpTmemCols = 512;
 constexpr int kRpMaxGroups = 64;               // n <= 8192 positions
 
+// What a launch computes (template MODE)
+constexpr int kRowLoss0 = 0;  // per position: (max, sum exp) of z_d and z_t, z_d at x*
+constexpr int kRowLoss1 = 1;  // per position: sum |p_d - p_t|
+constexpr int kRowRnn = 2;    // per request and block: log-mass of U_k + o_k W2 (o_k as bf16 hi + lo)
+constexpr int kRowTree = 3;   // per request and block: log-mass and max of U[b, depth] + W1[token] W2
+
 struct RpSmem {
   uint32_t a, w2, u, bars, misc, total;
   __host__ __device__ static RpSmem make(int r) {
@@ -68,8 +89,9 @@ struct RpSmem {
     s.w2 = s.a + kRpRows * r * 2;
     s.u = s.w2 + kRpNW * kRpW2Stage;
     s.bars = s.u + kRpNU * kRpUStage;
-    // w2 full/empty, u full/empty, acc_u, t_full, t_empty, p_full, p_empty, a_full, drains
-    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAcc + 3);
+    // w2 full/empty, u full/empty, acc_u, t_full, t_empty, p_full, p_empty, a_full, drains,
+    // a_cp_hi, a_cp_lo
+    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAcc + 5);
     // misc: TMEM address, abort word
     s.total = s.misc + 64;
     return s;
@@ -78,6 +100,15 @@ struct RpSmem {
 
 struct RpParams {
   int n, g, V, r, nblk, nG, G;
+  int step;            // RNN: draft step k (1-based)
+  const float* ovec;   // RNN: [B][g][r] o_k
+  const float* U;      // PCTree: U [B][g][V], read by the epilogue
+  const int32_t* tree_tok;   // PCTree: [B][N+1] nodes' tokens, depths; state[b].y = the node to expand
+  const int32_t* tree_dep;
+  const int4* tree_state;
+  int tree_N;
+  float* blk;          // RNN, PCTree: [B][nblk] block log-masses
+  float* bmax;         // PCTree: [B][nblk] block maxima
   const int32_t* anchor;
   const int32_t* xstar;
   const void* W1;
@@ -153,7 +184,7 @@ __device__ __forceinline__ void ms_merge(float& M, float& S, float mb, float sb)
   }
 }
 
-template <int PASS>
+template <int MODE>
 __global__ void __launch_bounds__(kRpThreads, 1)
     k_rowpass(const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_u,
               const __grid_constant__ CUtensorMap tm_p, const RpParams p) {
@@ -176,6 +207,11 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   auto p_empty = [&](int i) { return b5 + 8u * (4 * kRpNAcc + i); };  // (unused slot: keeps the layout even)
   const uint32_t a_full = b5 + 8u * (5 * kRpNAcc);
   const uint32_t drain = a_full + 8u, drain_c = a_full + 16u;
+  const uint32_t a_cp_hi = a_full + 24u, a_cp_lo = a_full + 32u;  // RNN: the A images are in TMEM
+  constexpr bool kLoss = MODE == kRowLoss0 || MODE == kRowLoss1;
+  // TMEM: accumulators at columns 0 and 128; then the P buffers (loss) or
+  // the A images hi and lo (RNN), r / 2 columns each
+  const uint32_t tm_hi = (uint32_t)(kRpNAcc * kRpAccCols), tm_lo = tm_hi + (uint32_t)(p.r / 2);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
   // [128] set 1's results per row, at the end: the A region is free once the
@@ -212,6 +248,8 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     tc::mbar_init(a_full, kRpEpi / 32);
     tc::mbar_init(drain, 1);
     tc::mbar_init(drain_c, 1);
+    tc::mbar_init(a_cp_hi, 1);
+    tc::mbar_init(a_cp_lo, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -257,20 +295,27 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   } else if (warp == kRpUWarp) {
     // ------------------------------------------------------------ U and P producer
     // per tile: its U blocks, then its P blocks, each one ring stage
-    if (lane == 0) {
+    if (lane == 0 && MODE != kRowTree) {
       const uint64_t stream = tc::policy_evict_first();
       int iss = 0;
       bool ok = true;
+      const int per_tile = kLoss ? 2 : 1;  // U blocks, then (loss) P blocks
       for (int tj = 0; tj < ntl && ok; ++tj) {
         const int nbt = tile_blocks(tj);
-        for (int e = 0; e < 2 * nbt && ok; ++e) {
+        for (int e = 0; e < per_tile * nbt && ok; ++e) {
           const int j = e % nbt, us = iss % kRpNU, v = (blo + tj * kRpTileBlocks + j) * kRpBlk;
           ok = tc::mbar_wait(u_empty(us), ((iss / kRpNU) & 1) ^ 1, abort);
           if (!ok) break;
-          const CUtensorMap* tm = e < nbt ? &tm_u : &tm_p;
           tc::mbar_arrive_expect_tx(u_full(us), kRpUStage);
-          tc::tma_load_2d(sU + us * kRpUStage, tm, v, grp * kRpRows, u_full(us), stream);
-          tc::tma_load_2d(sU + us * kRpUStage + kRpUBox, tm, v + 32, grp * kRpRows, u_full(us), stream);
+          if constexpr (MODE == kRowRnn) {  // U_k of the group's requests: a 3-D box (V, g, B) at step k
+            tc::tma_load_3d(sU + us * kRpUStage, &tm_u, v, p.step - 1, grp * kRpRows, u_full(us), stream);
+            tc::tma_load_3d(sU + us * kRpUStage + kRpUBox, &tm_u, v + 32, p.step - 1, grp * kRpRows, u_full(us),
+                            stream);
+          } else {
+            const CUtensorMap* tm = e < nbt ? &tm_u : &tm_p;
+            tc::tma_load_2d(sU + us * kRpUStage, tm, v, grp * kRpRows, u_full(us), stream);
+            tc::tma_load_2d(sU + us * kRpUStage + kRpUBox, tm, v + 32, grp * kRpRows, u_full(us), stream);
+          }
           ++iss;
         }
       }
@@ -289,10 +334,25 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     if (lane == 0) {
       bool ok = true;
       int iss = 0;
+      if constexpr (MODE == kRowRnn) {
+        // the epilogue leaves o_k's hi image, then its lo image, in the A
+        // region; each goes to its TMEM columns (16 bf16 of K per 8 columns)
+        for (int img = 0; img < 2 && ok; ++img) {
+          ok = tc::mbar_wait(a_full, img, abort);
+          if (!ok) break;
+          tc::tc_fence_after();
+          for (int ks = 0; ks < p.r / 16; ++ks)
+            tc::cp_128x256b(tmem + (img ? tm_lo : tm_hi) + (uint32_t)(ks * 8),
+                            tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024));
+          tc::mma_commit(img ? a_cp_lo : a_cp_hi);
+        }
+      }
+      const int per_tile = MODE == kRowTree ? 0 : kLoss ? 2 : 1;
       for (int tj = 0; tj < ntl && ok; ++tj) {
         const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
         ok = tc::mbar_wait(t_empty(ab), ((tj / kRpNAcc) & 1) ^ 1, abort);  // accumulator and P buffer free
-        for (int e = 0; e < 2 * nbt && ok; ++e) {
+        if (ok && per_tile == 0) tc::mma_commit(acc_u(ab));  // PCTree: the MMAs start from zero
+        for (int e = 0; e < per_tile * nbt && ok; ++e) {
           const int j = e % nbt, us = iss % kRpNU;
           ok = tc::mbar_wait(u_full(us), (iss / kRpNU) & 1, abort);
           if (!ok) break;
@@ -308,7 +368,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           ++iss;
           if (e == nbt - 1) tc::mma_commit(acc_u(ab));
         }
-        if (ok) tc::mma_commit(p_full(ab));
+        if (ok && kLoss) tc::mma_commit(p_full(ab));
       }
       if (!ok) {
         if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
@@ -321,7 +381,8 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      bool ok = tc::mbar_wait(a_full, 0, abort);
+      bool ok = MODE == kRowRnn ? (tc::mbar_wait(a_cp_hi, 0, abort) && tc::mbar_wait(a_cp_lo, 0, abort))
+                                : tc::mbar_wait(a_full, 0, abort);
       if (ok) tc::tc_fence_after();
       for (int tj = 0; tj < ntl && ok; ++tj) {
         const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
@@ -336,9 +397,15 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           tc::tc_fence_after();
           for (int kk = 0; kk < kRpKc / 16; ++kk) {
             const int ks = ch * (kRpKc / 16) + kk;
-            const uint64_t ad = tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024);
             const uint64_t bd = tc::smem_desc(sW2 + ws * kRpW2Stage + kk * 2048, kRpW2Box, 1024);
-            tc::mma_bf16(d, ad, bd, idesc, 1u);  // the accumulator starts as U
+            if constexpr (MODE == kRowRnn) {  // o_k hi, then lo, against the same W2 rows
+              tc::mma_bf16_ta(d, tmem + tm_hi + (uint32_t)(ks * 8), bd, idesc, 1u);
+              tc::mma_bf16_ta(d, tmem + tm_lo + (uint32_t)(ks * 8), bd, idesc, 1u);
+            } else {
+              const uint64_t ad = tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024);
+              // the accumulator starts as U (PCTree: from zero, U is added by the epilogue)
+              tc::mma_bf16(d, ad, bd, idesc, (MODE != kRowTree || ks > 0) ? 1u : 0u);
+            }
           }
           tc::mma_commit(w2_empty(ws));
         }
@@ -361,10 +428,81 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     auto aborted = [&]() { return __any_sync(0xFFFFFFFFu, *abort != 0); };
     int xs = -1;  // x*_k of this row (pass 0)
     float ld2 = 0.f, lt2 = 0.f;  // lse_d, lse_t in log2 units (pass 1)
-    // ---- A = W1[x*_{k-1}] of the group's rows (the anchor at k = 0)
-    {
+    bool live = valid;           // RNN, PCTree: the row's request has a node to expand / is drafted
+    const float* urow = nullptr;  // PCTree: U of the expanded node's depth
+    if constexpr (MODE == kRowRnn) {
+      // ---- A = o_k of the group's rows, as bf16 hi (then lo) images; the
+      // copier moves each into tensor memory before the next is written
+      uint4 lo[16];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float4 f[8][2];
+#pragma unroll
+        for (int i8 = 0; i8 < 8; ++i8) {
+          const int rl = 2 * (half * 8 + i8) + set, mr = q * 32 + rl, br = grp * kRpRows + mr;
+          f[i8][0] = f[i8][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (br < p.n && lane < p.r / 8) {
+            const float4* src = reinterpret_cast<const float4*>(
+                p.ovec + ((size_t)br * p.g + (p.step - 1)) * p.r + (size_t)lane * 8);
+            f[i8][0] = __ldg(src);
+            f[i8][1] = __ldg(src + 1);
+          }
+        }
+#pragma unroll
+        for (int i8 = 0; i8 < 8; ++i8) {
+          const float o8[8] = {f[i8][0].x, f[i8][0].y, f[i8][0].z, f[i8][0].w,
+                               f[i8][1].x, f[i8][1].y, f[i8][1].z, f[i8][1].w};
+          __nv_bfloat16 h8[8], l8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            h8[e] = __float2bfloat16_rn(o8[e]);
+            l8[e] = __float2bfloat16_rn(o8[e] - __bfloat162float(h8[e]));
+          }
+          const uint4 hv = *reinterpret_cast<const uint4*>(h8);
+          lo[half * 8 + i8] = *reinterpret_cast<const uint4*>(l8);
+          const int rl = 2 * (half * 8 + i8) + set;
+          if (lane < p.r / 8)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             sA + 2u * (uint32_t)rp_a_piece(q * 32 + rl, lane >> 3, lane & 7)),
+                         "r"(hv.x), "r"(hv.y), "r"(hv.z), "r"(hv.w)
+                         : "memory");
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(a_full);
+      const bool okc = __all_sync(0xFFFFFFFFu, tc::mbar_wait(a_cp_hi, 0, abort));  // the hi image has moved
+      if (okc && lane < p.r / 8) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           sA + 2u * (uint32_t)rp_a_piece(q * 32 + 2 * i + set, lane >> 3, lane & 7)),
+                       "r"(lo[i].x), "r"(lo[i].y), "r"(lo[i].z), "r"(lo[i].w)
+                       : "memory");
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(a_full);
+    } else {
+      // ---- A = the rows' W1 row: W1[x*_{k-1}] (loss; the anchor at k = 0)
+      // or W1[token of the node to expand] (PCTree)
       int x = 0;
-      if (valid) {
+      if constexpr (MODE == kRowTree) {
+        if (valid) {
+          const int4 st = p.tree_state[row];
+          const int node = min(max(st.y, 0), p.tree_N);
+          const size_t nb = (size_t)row * (p.tree_N + 1) + node;
+          const int d = p.tree_dep[nb];
+          live = st.w == 0 && d >= 0 && d < p.g;
+          x = live ? p.tree_tok[nb] : 0;
+          if (x < 0 || x >= p.V) {
+            raise_status(p.status, DSPARK_ERANGE);
+            x = 0;
+            live = false;
+          }
+          if (live) urow = p.U + ((size_t)row * p.g + d) * p.V;
+        }
+      } else if (valid) {
         const int b = row / p.g, k = row - b * p.g;
         x = k == 0 ? p.anchor[b] : p.xstar[(size_t)b * p.g + k - 1];
         xs = p.xstar[row];
@@ -373,7 +511,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           x = 0;
           xs = -1;
         }
-        if (PASS == 1) {
+        if (MODE == kRowLoss1) {
           ld2 = p.lse_d[row] * tc::kLog2e;
           lt2 = p.lse_t[row] * tc::kLog2e;
         }
@@ -406,7 +544,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       const int gb0 = tj * kRpTileBlocks;
       const int j0 = (set - gb0 % kRpSets + kRpSets) % kRpSets;
       bool ok = tc::mbar_wait(t_full(ab), (tj / kRpNAcc) & 1, abort) &&
-                tc::mbar_wait(p_full(ab), (tj / kRpNAcc) & 1, abort);
+                (!kLoss || tc::mbar_wait(p_full(ab), (tj / kRpNAcc) & 1, abort));
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
         if (lane == 0 && !*abort) {
@@ -419,6 +557,47 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       for (int j = j0; j < nbt; j += kRpSets) {
         const int t = blo + gb0 + j;
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        if constexpr (!kLoss) {
+          // RNN, PCTree: the block's log-mass (and maximum), from two halves
+          float mb = -INFINITY, sb = 0.f;
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {
+            const int v0 = t * kRpBlk + hh * 32;
+            float z[32];
+            float4 u4[8];
+            if (MODE == kRowTree && live) {  // U of the node's depth, this row's 32 entries
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                u4[e] = v0 + 4 * e + 3 < p.V ? __ldg(reinterpret_cast<const float4*>(urow + v0) + e)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            tc::tmem_ld32(tmem + lanes + (uint32_t)(ab * kRpAccCols + j * kRpBlk + hh * 32), z);
+            tc::tmem_wait_ld();
+            if (!live) continue;
+            if constexpr (MODE == kRowTree) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                z[4 * e] += u4[e].x;
+                z[4 * e + 1] += u4[e].y;
+                z[4 * e + 2] += u4[e].z;
+                z[4 * e + 3] += u4[e].w;
+              }
+            }
+            if (v0 + 32 > p.V) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (v0 + e >= p.V) z[e] = -INFINITY;
+            }
+            float mh, sh;
+            half_ms(z, mh, sh);
+            ms_merge(mb, sb, mh, sh);
+          }
+          if (live && t * kRpBlk < p.V) {
+            p.blk[(size_t)row * p.nblk + t] = mb > -INFINITY ? mb + logf(sb) : -INFINITY;
+            if (MODE == kRowTree) p.bmax[(size_t)row * p.nblk + t] = mb;
+          }
+          continue;
+        }
         // the block in two halves of 32 columns (z_d from the accumulator, z_t
         // from the P buffer), which keeps 64 values live instead of 128
 #pragma unroll 1
@@ -437,7 +616,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
                 y[e] = -INFINITY;
               }
           }
-          if (PASS == 0) {
+          if (MODE == kRowLoss0) {
             float mb, sb;
             half_ms(z, mb, sb);
             ms_merge(Md, Sd, mb, sb);
@@ -469,14 +648,15 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       if (lane == 0) tc::mbar_arrive(t_empty(ab));
     }
     // ---- the two sets of a row meet; set 0 writes the CTA's partial
+    if constexpr (kLoss) {
     asm volatile("bar.sync 1, %0;" ::"n"(kRpEpi) : "memory");
-    if (set == 1) xchg[m] = PASS == 0 ? make_float4(Md, Sd, Mt, St) : make_float4(l1, 0.f, 0.f, 0.f);
-    if (PASS == 0 && valid && have_zx && !*abort) p.zx[row] = zxv;
+    if (set == 1) xchg[m] = MODE == kRowLoss0 ? make_float4(Md, Sd, Mt, St) : make_float4(l1, 0.f, 0.f, 0.f);
+    if (MODE == kRowLoss0 && valid && have_zx && !*abort) p.zx[row] = zxv;
     asm volatile("bar.sync 1, %0;" ::"n"(kRpEpi) : "memory");
     if (set == 0 && valid && !*abort) {
       const float4 o = xchg[m];
       float4 w;
-      if (PASS == 0) {
+      if (MODE == kRowLoss0) {
         ms_merge(Md, Sd, o.x, o.y);
         ms_merge(Mt, St, o.z, o.w);
         w = make_float4(Md, Sd, Mt, St);
@@ -485,11 +665,12 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       }
       // slot cg holds this CTA's partial; the slots no CTA of the group owns get neutral values
       for (int s = cg; s < p.G; s += Gg) {
-        if (PASS == 0)
+        if (MODE == kRowLoss0)
           p.lpart[(size_t)row * p.G + s] = s == cg ? w : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         else
           p.l1part[(size_t)row * p.G + s] = s == cg ? w.x : 0.f;
       }
+    }
     }
   }
   tc::tc_fence_before();
@@ -515,42 +696,120 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool rowpass_supported(const dspark_ws* ws) {
+bool rowpass_supported(const dspark_ws* ws, int n) {
   const dspark_dims& d = ws->d;
   if (!ws->use_tc || d.wdtype != DSPARK_BF16) return false;
-  if (d.r % 64 != 0 || d.r > 256 || d.V % 8 != 0) return false;
-  const int n = d.B * d.gamma, nG = (n + kRpRows - 1) / kRpRows;
+  if (d.r % 64 != 0 || d.r > 256 || d.V % 8 != 0 || n < 1) return false;
+  const int nG = (n + kRpRows - 1) / kRpRows;
   if (nG > kRpMaxGroups || nG > ws->geo.num_sms) return false;
   if ((d.V + kRpBlk - 1) / kRpBlk < (ws->geo.num_sms + nG - 1) / nG) return false;  // a CTA per block at least
   return encode_fn() != nullptr;
 }
 
+namespace {
+
+cudaError_t rowpass_configure() {
+  static bool configured = false;
+  if (configured) return cudaSuccess;
+  const int mx = (int)(RpSmem::make(256).total + 1024);  // the largest operand (r = 256)
+  cudaError_t e = cudaFuncSetAttribute(k_rowpass<kRowLoss0>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_rowpass<kRowLoss1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_rowpass<kRowRnn>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_rowpass<kRowTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess) configured = true;
+  return e;
+}
+
+cudaError_t w2_map(const dspark_dims& d, const void* W2, CUtensorMap* tm) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
+  const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kRpBlk, (cuuint32_t)kRpKc};
+  const cuuint32_t es[2] = {1, 1};
+  if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W2), dims, strides, box, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+RpParams base_params(const dspark_ws* ws, int n) {
+  RpParams p;
+  memset(&p, 0, sizeof(p));
+  p.n = n;
+  p.g = ws->d.gamma;
+  p.V = ws->d.V;
+  p.r = ws->d.r;
+  p.nblk = ws->geo.nblk;
+  p.nG = (n + kRpRows - 1) / kRpRows;
+  p.G = ws->geo.num_sms;
+  p.status = ws->s.status;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
+                                      cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  cudaError_t e = rowpass_configure();
+  CUtensorMap tm_w2, tm_u;
+  if (e == cudaSuccess) e = w2_map(d, W2, &tm_w2);
+  if (e != cudaSuccess) return e;
+  {
+    // U as (V, gamma, B): the rows of one step are a 3-D box
+    const cuuint64_t dims[3] = {(cuuint64_t)d.V, (cuuint64_t)d.gamma, (cuuint64_t)d.B};
+    const cuuint64_t strides[2] = {(cuuint64_t)d.V * 4, (cuuint64_t)d.gamma * d.V * 4};
+    const cuuint32_t box[3] = {32, 1, (cuuint32_t)kRpRows};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (encode_fn()(&tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(U), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  RpParams p = base_params(ws, d.B);
+  p.step = k;
+  p.ovec = ovec;
+  p.blk = ws->s.blk;
+  const size_t smem = RpSmem::make(d.r).total + 1024;
+  k_rowpass<kRowRnn><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_u, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
+                                       const int32_t* tok, const int32_t* dep, const int4* state, int N, float* blk,
+                                       float* bmax, cudaStream_t st) {
+  const dspark_dims& d = ws->d;
+  cudaError_t e = rowpass_configure();
+  CUtensorMap tm_w2;
+  if (e == cudaSuccess) e = w2_map(d, W2, &tm_w2);
+  if (e != cudaSuccess) return e;
+  RpParams p = base_params(ws, d.B);
+  p.W1 = W1;
+  p.U = U;
+  p.tree_tok = tok;
+  p.tree_dep = dep;
+  p.tree_state = state;
+  p.tree_N = N;
+  p.blk = blk;
+  p.bmax = bmax;
+  const size_t smem = RpSmem::make(d.r).total + 1024;
+  k_rowpass<kRowTree><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_w2, tm_w2, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st) {
   const dspark_dims& d = ws->d;
-  const RpSmem L = RpSmem::make(d.r);
-  const size_t smem = L.total + 1024;
-  static bool configured = false;
-  if (!configured) {  // once, for the largest operand (r = 256)
-    const int mx = (int)(RpSmem::make(256).total + 1024);
-    cudaError_t e = cudaFuncSetAttribute(k_rowpass<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_rowpass<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const size_t smem = RpSmem::make(d.r).total + 1024;
+  cudaError_t e0 = rowpass_configure();
+  if (e0 != cudaSuccess) return e0;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int n = d.B * d.gamma;
   CUtensorMap tm_w2, tm_u, tm_p;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)d.r};
-    const cuuint64_t strides[1] = {(cuuint64_t)d.V * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kRpBlk, (cuuint32_t)kRpKc};
-    const cuuint32_t es[2] = {1, 1};
-    if (enc(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W2), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  e0 = w2_map(d, a.W2, &tm_w2);
+  if (e0 != cudaSuccess) return e0;
   for (int w = 0; w < 2; ++w) {
     // U and P as [n positions][V] fp32
     const cuuint64_t dims[2] = {(cuuint64_t)d.V, (cuuint64_t)n};
@@ -562,15 +821,7 @@ cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  RpParams p;
-  memset(&p, 0, sizeof(p));
-  p.n = n;
-  p.g = d.gamma;
-  p.V = d.V;
-  p.r = d.r;
-  p.nblk = ws->geo.nblk;
-  p.nG = (n + kRpRows - 1) / kRpRows;
-  p.G = ws->geo.num_sms;
+  RpParams p = base_params(ws, n);
   p.anchor = a.anchor;
   p.xstar = a.xstar;
   p.W1 = a.W1;
@@ -579,11 +830,10 @@ cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass
   p.lpart = a.lpart;
   p.zx = a.zx;
   p.l1part = a.l1part;
-  p.status = ws->s.status;
   if (pass == 0)
-    k_rowpass<0><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_p, p);
+    k_rowpass<kRowLoss0><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_p, p);
   else
-    k_rowpass<1><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_p, p);
+    k_rowpass<kRowLoss1><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_p, p);
   return cudaGetLastError();
 }
 
