@@ -22,6 +22,8 @@
 namespace dspark {
 
 constexpr int kSimtThreads = 256;
+constexpr int kPickThreadsS = 1024;             // k_draft_pick: 16 K slices of the 64-token recompute
+constexpr int kPickKs = kPickThreadsS / kBlockW;
 
 // s_h[row] = sum_{i<H} w[i] h[row, i]: the part of the confidence logit that
 // does not depend on drafted tokens (one CTA of 128 threads per row of h, all
@@ -81,7 +83,7 @@ __global__ void __launch_bounds__(kSimtThreads)
 }
 
 template <int BF16>
-__global__ void __launch_bounds__(kSimtThreads)
+__global__ void __launch_bounds__(kPickThreadsS)
     k_draft_pick(const float* __restrict__ U, const void* __restrict__ W1, const void* __restrict__ W2,
                  const int32_t* __restrict__ anchor, const float* __restrict__ w,
                  const float* __restrict__ T, const float* __restrict__ s_h, const float* __restrict__ ovec, int g,
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kSimtThreads)
   __shared__ float red_f[32];
   __shared__ MS red_ms[32];
   __shared__ KeyIdx red_k[32];
-  __shared__ float zpart[4][kBlockW];
+  __shared__ float zpart[kPickKs][kBlockW];
   __shared__ float zblk[kBlockW];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
@@ -149,17 +151,17 @@ __global__ void __launch_bounds__(kSimtThreads)
     if (tid == 0) raise_status(status, DSPARK_ENUMERIC);
     return;
   }
-  // token draw inside block sb: recompute z for its 64 tokens (4 partial dots)
+  // token draw inside block sb: recompute z for its 64 tokens, each over
+  // 16 K slices (a thread's slice of rows i = q, q + 16, ... with all of its
+  // W2 loads in flight), the slices added in a fixed order
   {
-    const int vl = tid & (kBlockW - 1), q = tid >> 6;
+    const int vl = tid & (kBlockW - 1), q = tid / kBlockW;
     const int v = sb * kBlockW + vl;
-    if (q < 4) {
-      float acc = 0.f;
-      if (v < V)
-#pragma unroll 16  // the W2 loads of 16 rows in flight together (the FMA order is unchanged)
-        for (int i = q; i < r; i += 4) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
-      zpart[q][vl] = acc;
-    }
+    float acc = 0.f;
+    if (v < V)
+#pragma unroll 16
+      for (int i = q; i < r; i += kPickKs) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
+    zpart[q][vl] = acc;
   }
   __syncthreads();
   // token draw inside block sb: argmax_v (z_v + G_v) over its 64 tokens, one
@@ -167,7 +169,12 @@ __global__ void __launch_bounds__(kSimtThreads)
   if (tid < kBlockW) {
     const int v = sb * kBlockW + tid;
     float z = -INFINITY;
-    if (v < V) z = U[o * V + v] + ((zpart[0][tid] + zpart[1][tid]) + (zpart[2][tid] + zpart[3][tid]));
+    if (v < V) {
+      float zs = 0.f;
+#pragma unroll
+      for (int q = 0; q < kPickKs; ++q) zs += zpart[q][tid];
+      z = U[o * V + v] + zs;
+    }
     zblk[tid] = z;
     KeyIdx kt = key_none();
     if (z > -INFINITY) kt = KeyIdx{z + gumbel(rng.word(kDraftToken, b, k, v)), tid};
@@ -231,7 +238,7 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
       k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
           a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
     }
-    k_draft_pick<BF16><<<d.B, kSimtThreads, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec,
+    k_draft_pick<BF16><<<d.B, kPickThreadsS, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec,
                                                        d.gamma, d.V, d.r, d.H, k, nblk, ws->s.blk, rng,
                                                        a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
     *launches += 2;

@@ -31,9 +31,10 @@ constexpr int kHpTile = 128;    // output tile of k_rnn_hproj (rows x columns)
 constexpr int kHpK = 16;        // K step
 constexpr int kHpSplit = kRnnHpSlices;  // K is split over 10 CTAs (two per SM at prod); each writes its own partial product
 constexpr int kCellThreads = 256;
-constexpr int kCellJ = 16;  // state entries per CTA of k_rnn_cell
-constexpr int kCellB = 16;  // requests per CTA of k_rnn_cell (kCellJ x kCellB = threads)
-static_assert(kCellJ * kCellB == kCellThreads, "one (entry, request) per thread in the update");
+constexpr int kCellJ = 8;   // state entries per CTA of k_rnn_cell: one per warp
+constexpr int kCellB = 16;  // requests per CTA of k_rnn_cell
+static_assert(kCellJ * kCellB <= kCellThreads, "one (entry, request) per thread in the update");
+static_assert(kCellJ == kCellThreads / 32, "one warp per state entry");
 
 // Sum over the 32 lanes of 16 per-lane values: afterwards lane L holds the
 // sum of every lane's a[L & 15] (each step keeps the half whose index bit
@@ -117,10 +118,10 @@ __global__ void __launch_bounds__(256, 2)
 }
 
 // Step k for requests b0 .. b0 + 15 and state entries j0 .. j0 + 15 (one CTA):
-// pre = W_{g,c,o}[:, :2r] [s_{k-1}; W1[x_{k-1}]] + Hp. Warp w takes entries
-// j0 + w and j0 + w + 8; for each it runs the three rows (g, c, o) over the
-// 2r inputs with the 16 requests' inputs from shared memory (lanes across the
-// inputs), then one transpose-reduce per row. The gate, the state update and
+// pre = W_{g,c,o}[:, :2r] [s_{k-1}; W1[x_{k-1}]] + Hp. Warp w takes entry
+// j0 + w: it runs the three rows (g, c, o) over the 2r inputs with the 16
+// requests' inputs from shared memory (lanes across the inputs, the rows'
+// loads of four steps in flight), then one transpose-reduce per row. The gate, the state update and
 // o_k follow per (entry, request). The state is double-buffered by step
 // parity (every CTA reads the whole s_{k-1} of its requests).
 template <int BF16>
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kCellThreads)
     for (int q = 0; q < 3; ++q)
 #pragma unroll
       for (int rb = 0; rb < kCellB; ++rb) acc[q][rb] = 0.f;
+#pragma unroll 4
     for (int i = lane; i < r2; i += 32) {
       const float wg = ld_w(Wr, BF16, (size_t)j * Z + i);
       const float wc = ld_w(Wr, BF16, (size_t)(r + j) * Z + i);
@@ -177,7 +179,7 @@ __global__ void __launch_bounds__(kCellThreads)
     }
   }
   __syncthreads();
-  {
+  if (tid < kCellJ * kCellB) {
     const int jj = tid % kCellJ, rb = tid / kCellJ, j = j0 + jj, b = b0 + rb;
     if (j < r && b < B) {
       const size_t row = (size_t)b * g + (k - 1);
