@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 
@@ -87,6 +89,8 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
     geo.sweep_grid = 4 * geo.num_sms;
   }
   geo.SL = (Rmax + geo.sweep_grid - 1) / geo.sweep_grid + 2;
+  geo.sweep_dyn = (d.V % kBlockW) == 0 && geo.nblk >= sweep_dyn_min_blocks() && sweep_dyn_configure() == cudaSuccess;
+  cudaGetLastError();
   geo.tc_ok = draft_tc_supported(d);
 
   const size_t BG = (size_t)d.B * d.gamma;
@@ -102,7 +106,10 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t o_sh = carve(sizeof(float) * BG);
   const size_t o_blk = carve(sizeof(float) * (size_t)d.B * geo.nblk);
   const size_t o_ring = carve(d.mode == DSPARK_COMPACT_LAGGED ? sizeof(int32_t) * (d.lag + 1) : 0);
-  const size_t o_vpart = carve(sizeof(float4) * (size_t)geo.sweep_grid * geo.SL);
+  const size_t vparts = geo.sweep_dyn ? sweep_dyn_parts((long long)Rmax * geo.nblk) : 0;
+  const size_t o_vpart = carve(sizeof(float4) * std::max((size_t)geo.sweep_grid * geo.SL, vparts));
+  const size_t o_vsched = carve(sizeof(int));
+  const size_t o_vlse = carve(geo.sweep_dyn ? sizeof(float) * (size_t)d.B * geo.nblk : 0);
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
   const size_t o_vlset = carve(sizeof(float) * d.B);
@@ -149,6 +156,8 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   s.vdone = reinterpret_cast<int*>(base + o_vdone);
   s.vpx = reinterpret_cast<float*>(base + o_vpx);
   s.rowtab = reinterpret_cast<int4*>(base + o_rowtab);
+  s.vsched = reinterpret_cast<int*>(base + o_vsched);
+  s.vlse = geo.sweep_dyn ? reinterpret_cast<float*>(base + o_vlse) : nullptr;
   s.rpart = reinterpret_cast<float2*>(base + o_rpart);
   s.dpart = geo.tc_ok ? reinterpret_cast<float2*>(base + o_dpart) : nullptr;
   s.dwin = geo.tc_ok ? reinterpret_cast<unsigned long long*>(base + o_dwin) : nullptr;
@@ -177,6 +186,7 @@ dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream) {
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.plan_round, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.barrier, 0, 8 * sizeof(unsigned), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.vdone, 0, sizeof(int) * ws->d.B, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws->s.vsched, 0, sizeof(int), st);
   if (e == cudaSuccess && ws->s.dwin)
     e = cudaMemsetAsync(ws->s.dwin, 0, sizeof(unsigned long long) * draft_tc_winners(ws->d), st);
   return cuda_fail(e);

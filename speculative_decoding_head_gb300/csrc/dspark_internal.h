@@ -84,6 +84,8 @@ struct Scratch {
   int* vdone;             // [B] sweep ranges done per request (back to 0 by the finalizing CTA)
   float* vpx;             // [B*(gamma+1)] P at each verified row's draft token (bulk sweep)
   int4* rowtab;           // [B*(gamma+1)] (b, j, lengths[b], row_off[b]) per packed row (dspark_round)
+  int* vsched;            // [1] the dynamic sweep's chunk counter (cleared by its finalize kernel)
+  float* vlse;            // [B*nblk] block log-sum-exps of each request's bonus row (dynamic sweep)
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
   float2* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
@@ -99,6 +101,7 @@ struct Geometry {
   int nblk;        // ceil(V / 64)
   int sweep_grid;  // CTAs of the verify sweep
   int sweep_bulk;  // bulk-copy sweep (V % 64 == 0)
+  int sweep_dyn;   // the bulk sweep with chunks taken from a counter (rounds with a row table)
   int SL;          // sweep partial slots per CTA (rows one range can touch)
   int num_sms;
   // persistent draft kernel
@@ -231,6 +234,11 @@ cudaError_t launch_plan_slice(const int32_t* lengths, const int32_t* row_off, in
 cudaError_t sweep_bulk_configure();
 int sweep_bulk_max_slots();  // rows one CTA range of the bulk sweep may span
 size_t sweep_bulk_smem_bytes(int SL);
+// The dynamic sweep: rows of at least sweep_dyn_min_blocks() blocks, the
+// partial count for a number of units (two float2, one float4, per group of 32), its configuration.
+int sweep_dyn_min_blocks();
+size_t sweep_dyn_parts(long long units);
+cudaError_t sweep_dyn_configure();
 cudaError_t plan_configure();
 
 }  // namespace dspark

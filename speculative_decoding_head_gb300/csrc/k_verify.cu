@@ -164,6 +164,7 @@ struct FinArgs {
   float* vlset;
   int* status;
   float* px;  // [rows] P at each row's draft token, stored by the bulk sweep (nullptr: read P)
+  const float4* rowstat;  // non-null: (max, sum, bonus key, block) of each of the request's rows, from row_off[b]
 };
 
 // Request b, by one whole warp. Lane j handles target row j: its
@@ -172,11 +173,22 @@ struct FinArgs {
 // draw inside its block, or the hand-over to the residual pass.
 // ell = lengths[b], base = row_off[b], R = row_off[B] (clamped to the row
 // capacity), as the caller read them.
-__device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R) {
+struct FinIn {  // lane j's draft token x_{j+1}, its draft probability and P at it (rows 0 .. ell-2)
+  int x;
+  float pdx, Px;
+};
+__device__ __forceinline__ FinIn finalize_inputs(int b, const FinArgs& f, int ell, int base, int R) {
+  const int lane = threadIdx.x & 31;
+  FinIn in{0, 0.f, 0.f};
+  if (ell < 1 || ell > f.g + 1 || base < 0 || base + ell > R || lane >= ell - 1) return in;
+  in.x = f.tokens[(size_t)b * f.g + lane];
+  in.pdx = f.pd_tok[(size_t)b * f.g + lane];
+  if (in.x >= 0 && in.x < f.V) in.Px = f.px ? __ldcg(f.px + base + lane) : f.P[(size_t)(base + lane) * f.V + in.x];
+  return in;
+}
+__device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R, const FinIn& in) {
   const int lane = threadIdx.x & 31;
   const float* __restrict__ P = f.P;
-  const int32_t* __restrict__ tokens = f.tokens;
-  const float* __restrict__ pd_tok = f.pd_tok;
   const int g = f.g, V = f.V, nblk = f.nblk, SL = f.SL, Gs = f.Gs;
   const Rng rng = f.rng;
   const float4* __restrict__ part = f.part;
@@ -192,12 +204,19 @@ __device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R)
     return;
   }
   const long long T = (long long)R * nblk;
-  // partials of row q: the CTAs whose unit ranges meet [q nblk, (q+1) nblk)
+  // partials of row q: the CTAs whose unit ranges meet [q nblk, (q+1) nblk),
+  // or the row's statistics already combined by the caller
   auto row_partials = [&](int q, MS* ms_out, KeyIdx* kb_out) {
+    if (f.rowstat) {
+      const float4 d = f.rowstat[q - base];
+      *ms_out = MS{d.x, d.y};
+      *kb_out = KeyIdx{d.z, __float_as_int(d.w)};
+      return;
+    }
     const long long u0 = (long long)q * nblk, u1 = u0 + nblk - 1;
-    const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
     MS ms{-INFINITY, 0.f};
     KeyIdx kb = key_none();
+    const int c0 = unit_owner(u0, T, Gs), c1 = unit_owner(u1, T, Gs);
     for (int cb = c0; cb <= c1; cb += 4) {  // four partials' loads in flight at a time
       float4 d[4];
 #pragma unroll
@@ -227,13 +246,8 @@ __device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R)
   float Lt = 0.f;
   KeyIdx kbonus = key_none();
   const bool arow = lane < ell - 1;
-  int x = 0;
-  float Px = 0.f, pdx = 0.f;
-  if (arow) {
-    x = tokens[(size_t)b * g + lane];
-    pdx = pd_tok[(size_t)b * g + lane];
-    if (x >= 0 && x < V) Px = f.px ? __ldcg(f.px + base + lane) : P[(size_t)(base + lane) * V + x];
-  }
+  const int x = in.x;
+  const float Px = in.Px, pdx = in.pdx;
   if (lane < ell) {
     MS ms;
     KeyIdx kb;
@@ -282,13 +296,22 @@ __device__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R)
     return;
   }
   KeyIdx kt = key_none();
-  for (int v = kb.idx * kBlockW + lane; v < min(V, (kb.idx + 1) * kBlockW); v += 32)
-    kt = better(kt, KeyIdx{P[q * V + v] + gumbel(rng.word(kBonusToken, b, n, v)), v});
+  {  // lane: tokens v and v + 1 of the block, which share one counter draw
+    const int v = kb.idx * kBlockW + 2 * lane;
+    const uint4 w = rng.block4(kBonusToken, b, n, v);
+    const uint32_t w0 = (v & 3) ? w.z : w.x, w1 = (v & 3) ? w.w : w.y;
+    if (v < V) kt = better(kt, KeyIdx{P[q * V + v] + gumbel(w0), v});
+    if (v + 1 < V) kt = better(kt, KeyIdx{P[q * V + v + 1] + gumbel(w1), v + 1});
+  }
   kt = warp_best(kt);
   if (lane == 0) {
     n_acc[b] = n;
     next_anchor[b] = kt.idx;
   }
+}
+
+__device__ __forceinline__ void finalize_core(int b, const FinArgs& f, int ell, int base, int R) {
+  finalize_core(b, f, ell, base, R, finalize_inputs(b, f, ell, base, R));
 }
 
 // log of the residual weight max(0, p_t - p_d) of one token, written as
@@ -575,6 +598,264 @@ __global__ void __launch_bounds__(kBulkThreads)
   }
 }
 
+// Dynamic bulk sweep (the rounds of dspark_round, whose planner wrote the
+// packed-row table; V % 64 == 0 and at least 128 blocks per row): the packed
+// rows' units are cut into chunks of kBulkUnits (32 KB of P) that the CTAs
+// take from a global counter, so a CTA that starts late or streams slowly
+// takes fewer chunks and every CTA ends within about a chunk of the others.
+// Warp 4 is the producer: it refills a stage as soon as the four consumer
+// warps have its data in registers, with the chunk its previous take
+// returned (one take ahead, so the counter's round trip hides behind the
+// ring), and brings the rowtab entries of the chunk's (at most two) rows
+// with it. The consumer warps never wait for one another: per chunk each
+// thread reduces one block and each warp writes, for its 32 blocks (a
+// "group", g = unit / 32), the per-row (max, sum) to part[2 g + slot]; a
+// thread whose block lies in a request's last verified row (the bonus row)
+// also stores the block's log-sum-exp to vlse[b][block]. No fence, no
+// random draw and no per-row counting sits on the stream: the bonus block's
+// Gumbel keys and the accept tests run in the next kernel
+// (k_verify_fin_dyn), one CTA per request, which also clears the counter
+// for the next launch.
+constexpr int kDynStages = kBulkStages;
+constexpr int kDynConsumers = kBulkThreads / 32;
+constexpr int kDynThreads = kBulkThreads + 32;
+constexpr int kDynGroup = 32;  // units per partial
+constexpr int kFinWarps = 16;  // warps per request in k_verify_fin_dyn
+constexpr int kFinRows = 33;   // verified rows a request can have (gamma <= 32, checked when a workspace is made)
+
+size_t sweep_dyn_smem_bytes() { return (size_t)kDynStages * (kBulkFloats * 4 + 2 * 16 + 2 * 8); }
+
+// (max, sum of exp(x - max)) of one row over the warp: the maximum first,
+// then every lane's sum rescaled to it and added (one exponential per lane
+// rather than two per combining step).
+__device__ __forceinline__ MS warp_ms_maxfirst(MS x) {
+  float M = x.m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  float t = x.m == -INFINITY ? 0.f : x.s * __expf(x.m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+  return MS{M, M == -INFINITY ? 0.f : t};
+}
+
+__global__ void __launch_bounds__(kDynThreads)
+    k_verify_sweep_dyn(const float* __restrict__ P, const int32_t* __restrict__ row_off, int B, int nblk, int Rmax,
+                       float2* __restrict__ part, float* __restrict__ vlse, int* __restrict__ status,
+                       const int4* __restrict__ rowtab, int* __restrict__ sched) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_wait();     // row offsets and the row table are the planner's
+  pdl_trigger();  // the finalize's CTAs may become resident and wait for this grid's end
+  float* stage = reinterpret_cast<float*>(smem);
+  int4* s_rows = reinterpret_cast<int4*>(smem + (size_t)kDynStages * kBulkFloats * 4);  // [stage][2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s_rows + 2 * kDynStages);            // full[S], empty[S]
+  __shared__ int s_chunk[kDynStages];  // chunk in each stage, -1: none (the consumers stop there)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = min(max(row_off[B], 0), Rmax);
+  const long long T = (long long)R * nblk;
+  if (T == 0) return;  // no rows: the counter is not touched
+  const int NC = (int)((T + kBulkUnits - 1) / kBulkUnits);
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8u * kDynStages;
+  if (tid == 0) {
+    for (int i = 0; i < kDynStages; ++i) {
+      tc::mbar_init(full0 + 8u * i, 1);
+      tc::mbar_init(empty0 + 8u * i, kDynConsumers);
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int never = 0;
+  if (warp == kDynConsumers) {  // ---- producer
+    if (lane != 0) return;
+    const uint32_t st0 = tc::smem_u32(stage), sr0 = tc::smem_u32(s_rows);
+    const uint64_t pol = tc::policy_evict_first();  // P is read once: W2 stays in L2 for the residual pass
+    const int first = atomicAdd(sched, kDynStages);  // the first stages' chunks in one take
+    int pending = atomicAdd(sched, 1);
+    int it = 0;  // stage fills so far
+    for (;; ++it) {
+      const int sidx = it % kDynStages;
+      const uint32_t fb = full0 + 8u * sidx;
+      if (it >= kDynStages && !tc::mbar_wait(empty0 + 8u * sidx, (it / kDynStages - 1) & 1, &never)) {
+        raise_status(status, DSPARK_ETIMEOUT);
+        break;
+      }
+      int c = first + it;
+      if (it >= kDynStages) {
+        c = pending;
+        pending = atomicAdd(sched, 1);
+      }
+      if (c >= NC) {  // no work left: the consumers stop at this stage
+        s_chunk[sidx] = -1;
+        tc::mbar_arrive(fb);
+        ++it;
+        break;
+      }
+      s_chunk[sidx] = c;
+      const long long u = (long long)c * kBulkUnits;
+      const int units = (int)min((long long)kBulkUnits, T - u);
+      const int q0 = (int)(u / nblk), nrows = (int)((u + units - 1) / nblk) - q0 + 1;  // 1 or 2
+      const uint32_t bytes = (uint32_t)units * kBlockW * 4u, rb = (uint32_t)nrows * 16u;
+      tc::mbar_arrive_expect_tx(fb, bytes + rb);
+      tc::bulk_load_hint(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, fb, pol);
+      tc::bulk_load(sr0 + (uint32_t)sidx * 32u, rowtab + q0, rb, fb);
+    }
+    // the copies of the last fill of each stage have landed before the CTA
+    // exits (at once when the consumers took them)
+    volatile int nv = 0;
+    for (int i = max(it - kDynStages, 0); i < it; ++i)
+      tc::mbar_wait(full0 + 8u * (i % kDynStages), (i / kDynStages) & 1, &nv);
+    return;
+  }
+  // ---- consumers: each warp on its own
+  for (int it = 0;; ++it) {
+    const int sidx = it % kDynStages;
+    if (!tc::mbar_wait(full0 + 8u * sidx, (it / kDynStages) & 1, &never)) {
+      if (lane == 0) raise_status(status, DSPARK_ETIMEOUT);
+      break;  // this warp releases no more stages: the producer gives up too
+    }
+    const int c = s_chunk[sidx];
+    if (c < 0) break;
+    const long long uw = (long long)c * kBulkUnits + (warp << 5), u = uw + lane;  // the warp's group, the lane's unit
+    if (uw >= T) {  // the ragged last chunk: a group past the end
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(empty0 + 8u * sidx);
+      continue;
+    }
+    const bool live = u < T;
+    const int qa = (int)(uw / nblk);  // the group's first row
+    MS ms{-INFINITY, 0.f};
+    int slot = 0, sblk = 0;
+    int4 ri = make_int4(0, 0, 0, 0);
+    float4 x[16];
+    if (live) {
+      const float4* blk4 = reinterpret_cast<const float4*>(stage + (size_t)sidx * kBulkFloats) + tid * 16;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x[i] = blk4[(i + tid) & 15];  // rotated: conflict-free
+      const int q = (int)(u / nblk);
+      sblk = (int)(u - (long long)q * nblk);
+      slot = q - qa;
+      ri = s_rows[sidx * 2 + q - (int)((long long)c * kBulkUnits / nblk)];  // (b, j, lengths[b], row_off[b])
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(empty0 + 8u * sidx);  // this warp is done with the stage
+    if (live) {
+      float m4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m4[i] = tc::max3f(x[i].x, x[i].y, tc::max3f(x[i].z, x[i].w, -INFINITY));
+#pragma unroll
+      for (int i = 4; i < 16; ++i) m4[i & 3] = tc::max3f(tc::max3f(m4[i & 3], x[i].x, x[i].y), x[i].z, x[i].w);
+      const float m = tc::max3f(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
+      if (m != -INFINITY) {
+        const unsigned long long l2e = tc::f2pack(tc::kLog2e, tc::kLog2e);
+        const unsigned long long nml = tc::f2pack(-m * tc::kLog2e, -m * tc::kLog2e);
+        unsigned long long acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a0, a1, a2, a3;
+          tc::f2unpack(tc::fma2(tc::f2pack(x[i].x, x[i].y), l2e, nml), a0, a1);
+          tc::f2unpack(tc::fma2(tc::f2pack(x[i].z, x[i].w), l2e, nml), a2, a3);
+          const unsigned long long e01 = tc::f2pack(tc::ex2_ftz(a0), tc::ex2_ftz(a1));
+          const unsigned long long e23 = tc::f2pack(tc::ex2_ftz(a2), tc::ex2_ftz(a3));
+          acc0 = i == 0 ? e01 : tc::add2(acc0, e01);
+          acc1 = i == 0 ? e23 : tc::add2(acc1, e23);
+        }
+        float s0, s1;
+        tc::f2unpack(tc::add2(acc0, acc1), s0, s1);
+        const float t = s0 + s1;
+        ms = MS{m, t};
+      }
+      if (ri.y == ri.z - 1)  // the request's last verified row: the block's log-sum-exp
+        vlse[(size_t)min(max(ri.x, 0), B - 1) * nblk + sblk] = ms.m == -INFINITY ? -INFINITY : ms.m + logf(ms.s);
+    }
+    // the group's rows (one, or two where a row ends inside the group)
+    const int nslot = (int)(min(uw + 31, T - 1) / nblk) - qa + 1;
+    for (int rr = 0; rr < nslot; ++rr) {
+      const MS mr = warp_ms_maxfirst(slot == rr ? ms : MS{-INFINITY, 0.f});
+      if (lane == 0) part[(size_t)(uw / kDynGroup) * 2 + rr] = make_float2(mr.m, mr.s);
+    }
+  }
+}
+
+// After the dynamic sweep: one CTA per request. The row layout, the draft
+// tokens and P at them were final before the sweep began, so they are read
+// before the wait, while the sweep still streams. Then the warps combine the
+// group partials of the accept rows 0 .. ell-2 (row j by warp j mod 16) and,
+// together, draw the bonus row's block: every block's key is its
+// log-sum-exp from the sweep plus its Gumbel draw. Warp 0 runs the accept
+// tests and the bonus token draw on these. Block 0 also checks the row
+// layout's start and clears the sweep's chunk counter for the next launch.
+__global__ void __launch_bounds__(kFinWarps * 32)
+    k_verify_fin_dyn(const FinArgs f, int Rmax, int* __restrict__ sched, const float* __restrict__ vlse) {
+  __shared__ float4 s_stat[kFinRows];
+  __shared__ KeyIdx s_key[kFinWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, b = blockIdx.x;
+  const int R = min(max(f.row_off[f.B], 0), Rmax);
+  const int ell = f.lengths[b], base = f.row_off[b];
+  const bool bad = f.anchor[b] < 0 || f.anchor[b] >= f.V || f.row_off[b + 1] != base + ell || ell < 1 ||
+                   ell > f.g + 1 || base < 0 || base + ell > R;  // the same for every thread
+  FinIn in{0, 0.f, 0.f};
+  if (!bad && warp == 0) in = finalize_inputs(b, f, ell, base, R);
+  pdl_wait();  // the sweep's partials and block log-sum-exps
+  pdl_trigger();
+  if (b == 0 && tid == 0) {
+    sched[0] = 0;
+    if (f.row_off[0] != 0) raise_status(f.status, DSPARK_ERANGE);
+  }
+  if (bad) {
+    if (tid == 0) {
+      f.vflag[b] = 0;
+      raise_status(f.status, DSPARK_ERANGE);
+    }
+    return;
+  }
+  const long long nb = f.nblk;
+  const float2* __restrict__ part = reinterpret_cast<const float2*>(f.part);
+  for (int j = warp; j < ell - 1; j += kFinWarps) {
+    const long long q = base + j;
+    const long long g0 = q * nb / kDynGroup, g1 = (q * nb + nb - 1) / kDynGroup;
+    MS ms{-INFINITY, 0.f};
+    for (long long gb = g0 + lane; gb <= g1; gb += 4 * 32) {  // four partials' loads in flight per lane
+      float2 d[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const long long gi = gb + 32 * e;
+        d[e] = make_float2(-INFINITY, 0.f);
+        if (gi <= g1) d[e] = __ldcg(part + (size_t)gi * 2 + (size_t)(q - gi * kDynGroup / nb));
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ms = ms_combine(ms, MS{d[e].x, d[e].y});
+    }
+    ms = warp_ms(ms);
+    if (lane == 0) s_stat[j] = make_float4(ms.m, ms.s, -INFINITY, __int_as_float(kNoIdx));
+  }
+  KeyIdx kb = key_none();
+  const float* __restrict__ L = vlse + (size_t)b * nb;
+  for (int k4 = tid; 4 * k4 < (int)nb; k4 += kFinWarps * 32) {  // four blocks per counter draw
+    float l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) l[e] = 4 * k4 + e < (int)nb ? __ldcg(L + 4 * k4 + e) : -INFINITY;
+    const uint4 w = f.rng.block4(kBonusBlock, b, ell - 1, 4 * k4);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (l[e] > -INFINITY) kb = better(kb, KeyIdx{l[e] + gumbel(wv[e]), 4 * k4 + e});
+  }
+  kb = warp_best(kb);
+  if (lane == 0) s_key[warp] = kb;
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) {
+      KeyIdx best = key_none();
+#pragma unroll
+      for (int w = 0; w < kFinWarps; ++w) best = better(best, s_key[w]);
+      s_stat[ell - 1] = make_float4(-INFINITY, 0.f, best.key, __int_as_float(best.idx));
+    }
+    __syncwarp();
+    FinArgs fr = f;
+    fr.rowstat = s_stat;
+    finalize_core(b, fr, ell, base, R, in);
+  }
+}
+
 template <int BF16>
 __global__ void __launch_bounds__(256)
     k_resid_blocks(const float* __restrict__ P, const float* __restrict__ U, const void* __restrict__ W1,
@@ -747,11 +1028,21 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
   const Rng rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
+  const bool dyn = geo.sweep_dyn && a.rowtab != nullptr;
   const FinArgs fin{a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma, d.V, geo.nblk,
                     geo.SL, geo.sweep_grid, rng, ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
-                    ws->s.vlset, ws->s.status, geo.sweep_bulk ? ws->s.vpx : nullptr};
+                    ws->s.vlset, ws->s.status, (geo.sweep_bulk && !dyn) ? ws->s.vpx : nullptr, nullptr};
   const bool pdl = ws->pdl != 0;
-  if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
+  if (dyn) {  // chunks taken from a counter; the accept tests in a kernel of their own
+    cudaError_t e = launch_ex(k_verify_sweep_dyn, dim3(2 * geo.num_sms), dim3(kDynThreads), sweep_dyn_smem_bytes(),
+                              st, pdl, a.P, a.row_off, d.B, geo.nblk, d.B * (d.gamma + 1),
+                              reinterpret_cast<float2*>(ws->s.vpart), ws->s.vlse, ws->s.status, a.rowtab,
+                              ws->s.vsched);
+    if (e != cudaSuccess) return e;
+    e = launch_ex(k_verify_fin_dyn, dim3(d.B), dim3(kFinWarps * 32), 0, st, pdl, fin, d.B * (d.gamma + 1),
+                  ws->s.vsched, ws->s.vlse);
+    if (e != cudaSuccess) return e;
+  } else if (geo.sweep_bulk) {  // the finalize runs in the sweep's CTAs
     const cudaError_t e = launch_ex(k_verify_sweep_bulk, dim3(geo.sweep_grid), dim3(kBulkThreads),
                                     sweep_bulk_smem_bytes(geo.SL), st, pdl, a.P, a.row_off, a.lengths, d.B, geo.nblk,
                                     d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart, ws->s.status, fin, ws->s.vdone,
@@ -763,7 +1054,7 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
                                                             d.B * (d.gamma + 1), geo.SL, rng, ws->s.vpart);
     k_verify_finalize<<<(d.B + 3) / 4, 128, 0, st>>>(fin);
   }
-  const bool pdl_resid = pdl && geo.sweep_bulk;  // the residual kernels follow the bulk sweep
+  const bool pdl_resid = pdl && (geo.sweep_bulk || dyn);  // the residual kernels follow a bulk sweep
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
   if (BF16 && ws->use_tc && geo.resid_tc_ok && !a.ovec) {
@@ -795,6 +1086,12 @@ cudaError_t launch_verify(const dspark_ws* ws, const VerifyArgs& a, cudaStream_t
 }  // namespace dspark
 
 namespace dspark {
+int sweep_dyn_min_blocks() { return kBulkUnits; }
+size_t sweep_dyn_parts(long long units) { return (size_t)((units + kDynGroup - 1) / kDynGroup); }
+cudaError_t sweep_dyn_configure() {
+  return cudaFuncSetAttribute(k_verify_sweep_dyn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sweep_dyn_smem_bytes());
+}
 cudaError_t sweep_bulk_configure() {
   return cudaFuncSetAttribute(k_verify_sweep_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)sweep_bulk_smem_bytes(kBulkMaxSlots));
