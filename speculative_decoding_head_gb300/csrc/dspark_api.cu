@@ -109,7 +109,7 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   const size_t vparts = geo.sweep_dyn ? sweep_dyn_parts((long long)Rmax * geo.nblk) : 0;
   const size_t o_vpart = carve(sizeof(float4) * std::max((size_t)geo.sweep_grid * geo.SL, vparts));
   const size_t o_vsched = carve(sizeof(int));
-  const size_t o_vlse = carve(geo.sweep_dyn ? sizeof(float) * (size_t)d.B * geo.nblk : 0);
+  const size_t o_vlse = carve(geo.sweep_dyn ? sizeof(float) * (size_t)Rmax * geo.nblk : 0);
   const size_t o_vflag = carve(sizeof(int) * d.B);
   const size_t o_vrow = carve(sizeof(int) * d.B);
   const size_t o_vlset = carve(sizeof(float) * d.B);

@@ -85,7 +85,7 @@ struct Scratch {
   float* vpx;             // [B*(gamma+1)] P at each verified row's draft token (bulk sweep)
   int4* rowtab;           // [B*(gamma+1)] (b, j, lengths[b], row_off[b]) per packed row (dspark_round)
   int* vsched;            // [1] the dynamic sweep's chunk counter (cleared by its finalize kernel)
-  float* vlse;            // [B*nblk] block log-sum-exps of each request's bonus row (dynamic sweep)
+  float* vlse;            // [B*(gamma+1)*nblk] block log-sum-exps of the packed rows (dynamic sweep)
   float2* rpart;          // [B*kResidChunks] residual (key, block) per CTA
   // persistent tcgen05 draft kernel
   float2* dpart;          // [gamma][groups*128][sets*ceil(grid/groups)] per-CTA, per-epilogue-set
@@ -101,7 +101,7 @@ struct Geometry {
   int nblk;        // ceil(V / 64)
   int sweep_grid;  // CTAs of the verify sweep
   int sweep_bulk;  // bulk-copy sweep (V % 64 == 0)
-  int sweep_dyn;   // the bulk sweep with chunks taken from a counter (rounds with a row table)
+  int sweep_dyn;   // the bulk sweep with chunks taken from a counter (at least 128 blocks a row)
   int SL;          // sweep partial slots per CTA (rows one range can touch)
   int num_sms;
   // persistent draft kernel

@@ -598,24 +598,21 @@ __global__ void __launch_bounds__(kBulkThreads)
   }
 }
 
-// Dynamic bulk sweep (the rounds of dspark_round, whose planner wrote the
-// packed-row table; V % 64 == 0 and at least 128 blocks per row): the packed
-// rows' units are cut into chunks of kBulkUnits (32 KB of P) that the CTAs
-// take from a global counter, so a CTA that starts late or streams slowly
-// takes fewer chunks and every CTA ends within about a chunk of the others.
-// Warp 4 is the producer: it refills a stage as soon as the four consumer
-// warps have its data in registers, with the chunk its previous take
-// returned (one take ahead, so the counter's round trip hides behind the
-// ring), and brings the rowtab entries of the chunk's (at most two) rows
-// with it. The consumer warps never wait for one another: per chunk each
-// thread reduces one block and each warp writes, for its 32 blocks (a
-// "group", g = unit / 32), the per-row (max, sum) to part[2 g + slot]; a
-// thread whose block lies in a request's last verified row (the bonus row)
-// also stores the block's log-sum-exp to vlse[b][block]. No fence, no
-// random draw and no per-row counting sits on the stream: the bonus block's
-// Gumbel keys and the accept tests run in the next kernel
-// (k_verify_fin_dyn), one CTA per request, which also clears the counter
-// for the next launch.
+// Dynamic bulk sweep (V % 64 == 0 and at least 128 blocks per row): the
+// packed rows' units are cut into chunks of kBulkUnits (32 KB of P) that the
+// CTAs take from a global counter, so a CTA that starts late or streams
+// slowly takes fewer chunks and every CTA ends within about a chunk of the
+// others. Warp 4 is the producer: it refills a stage as soon as the four
+// consumer warps have its data in registers, with the chunk its previous
+// take returned (one take ahead, so the counter's round trip hides behind
+// the ring). The consumer warps never wait for one another: per chunk each
+// thread reduces one block, stores the block's log-sum-exp at its unit
+// index (vlse, [rows][nblk] in packed-row order) and each warp writes, for
+// its 32 blocks (a "group", g = unit / 32), the per-row (max, sum) to
+// part[2 g + slot]. No fence, no random draw and no per-row counting sits
+// on the stream, and the stream needs no row table: the bonus row's Gumbel
+// keys and the accept tests run in the next kernel (k_verify_fin_dyn), one
+// CTA per request, which also clears the counter for the next launch.
 constexpr int kDynStages = kBulkStages;
 constexpr int kDynConsumers = kBulkThreads / 32;
 constexpr int kDynThreads = kBulkThreads + 32;
@@ -623,7 +620,7 @@ constexpr int kDynGroup = 32;  // units per partial
 constexpr int kFinWarps = 16;  // warps per request in k_verify_fin_dyn
 constexpr int kFinRows = 33;   // verified rows a request can have (gamma <= 32, checked when a workspace is made)
 
-size_t sweep_dyn_smem_bytes() { return (size_t)kDynStages * (kBulkFloats * 4 + 2 * 16 + 2 * 8); }
+size_t sweep_dyn_smem_bytes() { return (size_t)kDynStages * (kBulkFloats * 4 + 2 * 8); }
 
 // (max, sum of exp(x - max)) of one row over the warp: the maximum first,
 // then every lane's sum rescaled to it and added (one exponential per lane
@@ -641,13 +638,12 @@ __device__ __forceinline__ MS warp_ms_maxfirst(MS x) {
 __global__ void __launch_bounds__(kDynThreads)
     k_verify_sweep_dyn(const float* __restrict__ P, const int32_t* __restrict__ row_off, int B, int nblk, int Rmax,
                        float2* __restrict__ part, float* __restrict__ vlse, int* __restrict__ status,
-                       const int4* __restrict__ rowtab, int* __restrict__ sched) {
+                       int* __restrict__ sched) {
   extern __shared__ __align__(128) unsigned char smem[];
-  pdl_wait();     // row offsets and the row table are the planner's
+  pdl_wait();     // the row offsets may be the planner's
   pdl_trigger();  // the finalize's CTAs may become resident and wait for this grid's end
   float* stage = reinterpret_cast<float*>(smem);
-  int4* s_rows = reinterpret_cast<int4*>(smem + (size_t)kDynStages * kBulkFloats * 4);  // [stage][2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s_rows + 2 * kDynStages);            // full[S], empty[S]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kDynStages * kBulkFloats * 4);  // full[S], empty[S]
   __shared__ int s_chunk[kDynStages];  // chunk in each stage, -1: none (the consumers stop there)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = min(max(row_off[B], 0), Rmax);
@@ -666,7 +662,7 @@ __global__ void __launch_bounds__(kDynThreads)
   volatile int never = 0;
   if (warp == kDynConsumers) {  // ---- producer
     if (lane != 0) return;
-    const uint32_t st0 = tc::smem_u32(stage), sr0 = tc::smem_u32(s_rows);
+    const uint32_t st0 = tc::smem_u32(stage);
     const uint64_t pol = tc::policy_evict_first();  // P is read once: W2 stays in L2 for the residual pass
     const int first = atomicAdd(sched, kDynStages);  // the first stages' chunks in one take
     int pending = atomicAdd(sched, 1);
@@ -692,11 +688,9 @@ __global__ void __launch_bounds__(kDynThreads)
       s_chunk[sidx] = c;
       const long long u = (long long)c * kBulkUnits;
       const int units = (int)min((long long)kBulkUnits, T - u);
-      const int q0 = (int)(u / nblk), nrows = (int)((u + units - 1) / nblk) - q0 + 1;  // 1 or 2
-      const uint32_t bytes = (uint32_t)units * kBlockW * 4u, rb = (uint32_t)nrows * 16u;
-      tc::mbar_arrive_expect_tx(fb, bytes + rb);
+      const uint32_t bytes = (uint32_t)units * kBlockW * 4u;
+      tc::mbar_arrive_expect_tx(fb, bytes);
       tc::bulk_load_hint(st0 + (uint32_t)sidx * kBulkFloats * 4u, P + u * kBlockW, bytes, fb, pol);
-      tc::bulk_load(sr0 + (uint32_t)sidx * 32u, rowtab + q0, rb, fb);
     }
     // the copies of the last fill of each stage have landed before the CTA
     // exits (at once when the consumers took them)
@@ -723,17 +717,13 @@ __global__ void __launch_bounds__(kDynThreads)
     const bool live = u < T;
     const int qa = (int)(uw / nblk);  // the group's first row
     MS ms{-INFINITY, 0.f};
-    int slot = 0, sblk = 0;
-    int4 ri = make_int4(0, 0, 0, 0);
+    int slot = 0;
     float4 x[16];
     if (live) {
       const float4* blk4 = reinterpret_cast<const float4*>(stage + (size_t)sidx * kBulkFloats) + tid * 16;
 #pragma unroll
       for (int i = 0; i < 16; ++i) x[i] = blk4[(i + tid) & 15];  // rotated: conflict-free
-      const int q = (int)(u / nblk);
-      sblk = (int)(u - (long long)q * nblk);
-      slot = q - qa;
-      ri = s_rows[sidx * 2 + q - (int)((long long)c * kBulkUnits / nblk)];  // (b, j, lengths[b], row_off[b])
+      slot = (int)(u / nblk) - qa;
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(empty0 + 8u * sidx);  // this warp is done with the stage
@@ -763,8 +753,7 @@ __global__ void __launch_bounds__(kDynThreads)
         const float t = s0 + s1;
         ms = MS{m, t};
       }
-      if (ri.y == ri.z - 1)  // the request's last verified row: the block's log-sum-exp
-        vlse[(size_t)min(max(ri.x, 0), B - 1) * nblk + sblk] = ms.m == -INFINITY ? -INFINITY : ms.m + logf(ms.s);
+      vlse[u] = ms.m == -INFINITY ? -INFINITY : ms.m + logf(ms.s);  // the block's log-sum-exp
     }
     // the group's rows (one, or two where a row ends inside the group)
     const int nslot = (int)(min(uw + 31, T - 1) / nblk) - qa + 1;
@@ -776,8 +765,9 @@ __global__ void __launch_bounds__(kDynThreads)
 }
 
 // After the dynamic sweep: one CTA per request. The row layout, the draft
-// tokens and P at them were final before the sweep began, so they are read
-// before the wait, while the sweep still streams. Then the warps combine the
+// tokens and P at them were final before the sweep began (the sweep waited
+// for the kernel before it), so they are read before the wait, while the
+// sweep still streams. Then the warps combine the
 // group partials of the accept rows 0 .. ell-2 (row j by warp j mod 16) and,
 // together, draw the bonus row's block: every block's key is its
 // log-sum-exp from the sweep plus its Gumbel draw. Warp 0 runs the accept
@@ -828,7 +818,7 @@ __global__ void __launch_bounds__(kFinWarps * 32)
     if (lane == 0) s_stat[j] = make_float4(ms.m, ms.s, -INFINITY, __int_as_float(kNoIdx));
   }
   KeyIdx kb = key_none();
-  const float* __restrict__ L = vlse + (size_t)b * nb;
+  const float* __restrict__ L = vlse + (size_t)(base + ell - 1) * nb;  // the bonus row's blocks
   for (int k4 = tid; 4 * k4 < (int)nb; k4 += kFinWarps * 32) {  // four blocks per counter draw
     float l[4];
 #pragma unroll
@@ -1028,16 +1018,15 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const dspark_dims& d = ws->d;
   const Geometry& geo = ws->geo;
   const Rng rng = Rng::make(a.seed, a.round, (uint32_t)ws->b0);
-  const bool dyn = geo.sweep_dyn && a.rowtab != nullptr;
+  const bool pdl = ws->pdl != 0;
+  const bool dyn = geo.sweep_dyn != 0;
   const FinArgs fin{a.P, a.row_off, a.lengths, a.anchor, a.tokens, a.pd_tok, d.B, d.gamma, d.V, geo.nblk,
                     geo.SL, geo.sweep_grid, rng, ws->s.vpart, a.n_acc, a.next_anchor, ws->s.vflag, ws->s.vrow,
                     ws->s.vlset, ws->s.status, (geo.sweep_bulk && !dyn) ? ws->s.vpx : nullptr, nullptr};
-  const bool pdl = ws->pdl != 0;
   if (dyn) {  // chunks taken from a counter; the accept tests in a kernel of their own
     cudaError_t e = launch_ex(k_verify_sweep_dyn, dim3(2 * geo.num_sms), dim3(kDynThreads), sweep_dyn_smem_bytes(),
                               st, pdl, a.P, a.row_off, d.B, geo.nblk, d.B * (d.gamma + 1),
-                              reinterpret_cast<float2*>(ws->s.vpart), ws->s.vlse, ws->s.status, a.rowtab,
-                              ws->s.vsched);
+                              reinterpret_cast<float2*>(ws->s.vpart), ws->s.vlse, ws->s.status, ws->s.vsched);
     if (e != cudaSuccess) return e;
     e = launch_ex(k_verify_fin_dyn, dim3(d.B), dim3(kFinWarps * 32), 0, st, pdl, fin, d.B * (d.gamma + 1),
                   ws->s.vsched, ws->s.vlse);
