@@ -132,23 +132,30 @@ __global__ void __launch_bounds__(kCellThreads)
                int* __restrict__ status) {
   extern __shared__ float zin[];  // [kCellB][2r]: s_{k-1}, W1[x_{k-1}] of each request
   __shared__ float pre[3][kCellJ][kCellB];
+  __shared__ int xs[kCellB];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j0 = blockIdx.x * kCellJ, b0 = blockIdx.y * kCellB;
   const int r2 = 2 * r, Z = r2 + H;
-  for (int rb = 0; rb < kCellB; ++rb) {
-    const int b = b0 + rb;
+  if (tid < kCellB) {  // the requests' previous tokens first, so the row loads below are independent
+    const int b = b0 + tid;
     int x = 0;
     if (b < B) {
       x = k == 1 ? anchor[b] : tokens[(size_t)b * g + (k - 2)];
       if (x < 0 || x >= V) {
-        if (tid == 0) raise_status(status, DSPARK_ERANGE);
+        raise_status(status, DSPARK_ERANGE);
         x = 0;
       }
     }
-    for (int i = tid; i < r; i += kCellThreads) {
-      zin[rb * r2 + i] = b < B ? S_in[(size_t)b * r + i] : 0.f;
-      zin[rb * r2 + r + i] = b < B ? ld_w(W1, BF16, (size_t)x * r + i) : 0.f;
-    }
+    xs[tid] = x;
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int e = tid; e < kCellB * r; e += kCellThreads) {
+    const int rb = e / r, i = e - rb * r, b = b0 + rb;
+    const float sv = b < B ? S_in[(size_t)b * r + i] : 0.f;
+    const float wv = b < B ? ld_w(W1, BF16, (size_t)xs[rb] * r + i) : 0.f;
+    zin[rb * r2 + i] = sv;
+    zin[rb * r2 + r + i] = wv;
   }
   __syncthreads();
   for (int jj = warp; jj < kCellJ; jj += kCellThreads / 32) {
@@ -159,7 +166,7 @@ __global__ void __launch_bounds__(kCellThreads)
     for (int q = 0; q < 3; ++q)
 #pragma unroll
       for (int rb = 0; rb < kCellB; ++rb) acc[q][rb] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int i = lane; i < r2; i += 32) {
       const float wg = ld_w(Wr, BF16, (size_t)j * Z + i);
       const float wc = ld_w(Wr, BF16, (size_t)(r + j) * Z + i);
