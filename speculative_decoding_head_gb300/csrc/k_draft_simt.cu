@@ -97,6 +97,8 @@ __global__ void __launch_bounds__(kPickThreadsS)
   __shared__ KeyIdx red_k[32];
   __shared__ float zpart[kPickKs][kBlockW];
   __shared__ float zblk[kBlockW];
+  pdl_wait();  // the block pass (and the previous step's pick) of this step
+  pdl_trigger();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
   const int x = prev_token(anchor, tokens, b, g, k);
@@ -238,9 +240,12 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
       k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
           a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
     }
-    k_draft_pick<BF16><<<d.B, kPickThreadsS, smem, st>>>(a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec,
-                                                       d.gamma, d.V, d.r, d.H, k, nblk, ws->s.blk, rng,
-                                                       a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
+    // the RNN head's steps are chained by programmatic dependent launch (the
+    // cell and the pick wait in-kernel); the Markov SIMT steps launch plainly
+    const cudaError_t e = launch_ex(k_draft_pick<BF16>, dim3(d.B), dim3(kPickThreadsS), smem, st, rnn != nullptr,
+                                    a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec, d.gamma, d.V, d.r, d.H, k,
+                                    nblk, ws->s.blk, rng, a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
+    if (e != cudaSuccess) return e;
     *launches += 2;
   }
   return cudaGetLastError();

@@ -117,93 +117,181 @@ __global__ void __launch_bounds__(256, 2)
     }
 }
 
-// Step k for requests b0 .. b0 + 15 and state entries j0 .. j0 + 15 (one CTA):
+// Step k for requests b0 .. b0 + 15 and state entries j0 .. j0 + 7 (one CTA):
 // pre = W_{g,c,o}[:, :2r] [s_{k-1}; W1[x_{k-1}]] + Hp. Warp w takes entry
 // j0 + w: it runs the three rows (g, c, o) over the 2r inputs with the 16
-// requests' inputs from shared memory (lanes across the inputs, the rows'
-// loads of four steps in flight), then one transpose-reduce per row. The gate, the state update and
-// o_k follow per (entry, request). The state is double-buffered by step
-// parity (every CTA reads the whole s_{k-1} of its requests).
+// requests' inputs from shared memory, lane l on inputs 2l + 64 i and the next
+// one, then one transpose-reduce per row. The gate, the state update and o_k
+// follow per (entry, request). The state is double-buffered by step parity
+// (every CTA reads the whole s_{k-1} of its requests).
+// Before its wait on the previous kernel (programmatic dependent launch) the
+// CTA loads what does not depend on the previous step: the three weight rows
+// of each warp (bf16 pairs in registers, for 2r <= 512) and the h
+// projection's sums of its (entry, request) pairs. After it, the state rows
+// go out while the tokens come back, and all staging loads are 16 bytes wide
+// and in flight together.
+constexpr int kCellWp = 8;  // bf16 pairs of a weight row per lane (2r <= 64 * kCellWp)
+
 template <int BF16>
 __global__ void __launch_bounds__(kCellThreads)
     k_rnn_cell(const void* __restrict__ W1, const void* __restrict__ Wr, const int32_t* __restrict__ anchor,
                const int32_t* __restrict__ tokens, const float* __restrict__ Hp, const float* __restrict__ S_in,
                float* __restrict__ S_out, float* __restrict__ ovec, int B, int g, int V, int r, int H, int k,
                int* __restrict__ status) {
-  extern __shared__ float zin[];  // [kCellB][2r]: s_{k-1}, W1[x_{k-1}] of each request
+  extern __shared__ __align__(16) float zin[];  // [kCellB][2r]: s_{k-1}, W1[x_{k-1}] of each request
   __shared__ float pre[3][kCellJ][kCellB];
   __shared__ int xs[kCellB];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j0 = blockIdx.x * kCellJ, b0 = blockIdx.y * kCellB;
   const int r2 = 2 * r, Z = r2 + H;
-  if (tid < kCellB) {  // the requests' previous tokens first, so the row loads below are independent
-    const int b = b0 + tid;
-    int x = 0;
-    if (b < B) {
-      x = k == 1 ? anchor[b] : tokens[(size_t)b * g + (k - 2)];
-      if (x < 0 || x >= V) {
-        raise_status(status, DSPARK_ERANGE);
-        x = 0;
+  const int jw = j0 + warp;  // this warp's state entry
+  // ---- before the wait
+  const bool wreg = BF16 && r2 <= 64 * kCellWp && (Z & 1) == 0;  // the same for every thread
+  uint32_t wv[3][kCellWp];
+  if (wreg) {
+    const __nv_bfloat16* wr = reinterpret_cast<const __nv_bfloat16*>(Wr);
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+      for (int t = 0; t < kCellWp; ++t) {
+        const int i = 2 * lane + 64 * t;
+        wv[q][t] = jw < r && i < r2 ? __ldg(reinterpret_cast<const uint32_t*>(wr + (size_t)(q * r + jw) * Z + i)) : 0u;
       }
+  }
+  const int ejj = tid % kCellJ, erb = tid / kCellJ, ej = j0 + ejj, eb = b0 + erb;  // the update's (entry, request)
+  const bool eact = tid < kCellJ * kCellB && ej < r && eb < B;
+  float hq[3] = {0.f, 0.f, 0.f};
+  if (eact) {
+    const size_t row = (size_t)eb * g + (k - 1);
+    const size_t slice = (size_t)B * g * 3 * r;  // the h projection's K slices, added in order
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const float* hp = Hp + row * 3 * r + q * r + ej;
+      float t = hp[0];
+#pragma unroll
+      for (int sl = 1; sl < kHpSplit; ++sl) t += hp[sl * slice];
+      hq[q] = t;
+    }
+  }
+  // ---- the previous step's pick (tokens) and cell (state). No early
+  // trigger: the row pass launched during the cell slowed the step down
+  pdl_wait();
+  int x = 0;
+  if (tid < kCellB && b0 + tid < B) x = k == 1 ? anchor[b0 + tid] : tokens[(size_t)(b0 + tid) * g + (k - 2)];
+  const bool v16 = (r & 7) == 0;  // rows in 16-byte pieces
+  if (v16) {  // s_{k-1}: kCellB rows of r/4 float4, four a thread in flight
+    const int r4 = r >> 2, n4 = kCellB * r4;
+    for (int e0 = tid; e0 < n4; e0 += 4 * kCellThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kCellThreads, rb = e / r4, b = b0 + rb;
+        v[u] = e < n4 && b < B ? __ldg(reinterpret_cast<const float4*>(S_in + (size_t)b * r) + (e - rb * r4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kCellThreads, rb = e / r4;
+        if (e < n4) *reinterpret_cast<float4*>(zin + rb * r2 + 4 * (e - rb * r4)) = v[u];
+      }
+    }
+  } else {
+    for (int e = tid; e < kCellB * r; e += kCellThreads) {
+      const int rb = e / r, i = e - rb * r, b = b0 + rb;
+      zin[rb * r2 + i] = b < B ? S_in[(size_t)b * r + i] : 0.f;
+    }
+  }
+  if (tid < kCellB) {
+    if (x < 0 || x >= V) {
+      raise_status(status, DSPARK_ERANGE);
+      x = 0;
     }
     xs[tid] = x;
   }
   __syncthreads();
-#pragma unroll 4
-  for (int e = tid; e < kCellB * r; e += kCellThreads) {
-    const int rb = e / r, i = e - rb * r, b = b0 + rb;
-    const float sv = b < B ? S_in[(size_t)b * r + i] : 0.f;
-    const float wv = b < B ? ld_w(W1, BF16, (size_t)xs[rb] * r + i) : 0.f;
-    zin[rb * r2 + i] = sv;
-    zin[rb * r2 + r + i] = wv;
+  if (v16) {  // W1[x_{k-1}]: kCellB rows of 16-byte pieces (8 bf16 or 4 fp32), four a thread in flight
+    constexpr int per = BF16 ? 8 : 4;
+    const int rp = r / per, np = kCellB * rp;
+    for (int e0 = tid; e0 < np; e0 += 4 * kCellThreads) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kCellThreads, rb = e / rp, b = b0 + rb;
+        const char* wrow = reinterpret_cast<const char*>(W1) + (size_t)xs[rb < kCellB ? rb : 0] * r * (BF16 ? 2 : 4);
+        v[u] = e < np && b < B ? __ldg(reinterpret_cast<const uint4*>(wrow) + (e - rb * rp)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kCellThreads, rb = e / rp;
+        if (e >= np) continue;
+        float* dst = zin + rb * r2 + r + per * (e - rb * rp);
+        if (BF16) {
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+          float2 f[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) f[t] = __bfloat1622float2(h2[t]);
+          reinterpret_cast<float4*>(dst)[0] = make_float4(f[0].x, f[0].y, f[1].x, f[1].y);
+          reinterpret_cast<float4*>(dst)[1] = make_float4(f[2].x, f[2].y, f[3].x, f[3].y);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = v[u];
+        }
+      }
+    }
+  } else {
+    for (int e = tid; e < kCellB * r; e += kCellThreads) {
+      const int rb = e / r, i = e - rb * r, b = b0 + rb;
+      zin[rb * r2 + r + i] = b < B ? ld_w(W1, BF16, (size_t)xs[rb] * r + i) : 0.f;
+    }
   }
   __syncthreads();
-  for (int jj = warp; jj < kCellJ; jj += kCellThreads / 32) {
-    const int j = j0 + jj;
-    if (j >= r) break;  // warp-uniform
+  if (jw < r) {  // warp-uniform
     float acc[3][kCellB];
 #pragma unroll
     for (int q = 0; q < 3; ++q)
 #pragma unroll
       for (int rb = 0; rb < kCellB; ++rb) acc[q][rb] = 0.f;
-#pragma unroll 8
-    for (int i = lane; i < r2; i += 32) {
-      const float wg = ld_w(Wr, BF16, (size_t)j * Z + i);
-      const float wc = ld_w(Wr, BF16, (size_t)(r + j) * Z + i);
-      const float wo = ld_w(Wr, BF16, (size_t)(2 * r + j) * Z + i);
+    if (wreg) {
 #pragma unroll
-      for (int rb = 0; rb < kCellB; ++rb) {
-        const float zv = zin[rb * r2 + i];
-        acc[0][rb] = fmaf(wg, zv, acc[0][rb]);
-        acc[1][rb] = fmaf(wc, zv, acc[1][rb]);
-        acc[2][rb] = fmaf(wo, zv, acc[2][rb]);
+      for (int t = 0; t < kCellWp; ++t) {
+        const int i = 2 * lane + 64 * t;
+        if (i >= r2) break;
+        float2 w2[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) w2[q] = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q][t]));
+#pragma unroll
+        for (int rb = 0; rb < kCellB; ++rb) {
+          const float2 zv = *reinterpret_cast<const float2*>(zin + rb * r2 + i);
+#pragma unroll
+          for (int q = 0; q < 3; ++q) acc[q][rb] = fmaf(w2[q].y, zv.y, fmaf(w2[q].x, zv.x, acc[q][rb]));
+        }
+      }
+    } else {
+#pragma unroll 8
+      for (int i = lane; i < r2; i += 32) {
+        const float wg = ld_w(Wr, BF16, (size_t)jw * Z + i);
+        const float wc = ld_w(Wr, BF16, (size_t)(r + jw) * Z + i);
+        const float wo = ld_w(Wr, BF16, (size_t)(2 * r + jw) * Z + i);
+#pragma unroll
+        for (int rb = 0; rb < kCellB; ++rb) {
+          const float zv = zin[rb * r2 + i];
+          acc[0][rb] = fmaf(wg, zv, acc[0][rb]);
+          acc[1][rb] = fmaf(wc, zv, acc[1][rb]);
+          acc[2][rb] = fmaf(wo, zv, acc[2][rb]);
+        }
       }
     }
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
       const float sum = transpose_sum16(acc[q]);  // lane l: request l & 15
-      if (lane < kCellB) pre[q][jj][lane] = sum;
+      if (lane < kCellB) pre[q][warp][lane] = sum;
     }
   }
   __syncthreads();
-  if (tid < kCellJ * kCellB) {
-    const int jj = tid % kCellJ, rb = tid / kCellJ, j = j0 + jj, b = b0 + rb;
-    if (j < r && b < B) {
-      const size_t row = (size_t)b * g + (k - 1);
-      const size_t slice = (size_t)B * g * 3 * r;  // the h projection's K slices, added in order
-      float hq[3];
-#pragma unroll
-      for (int q = 0; q < 3; ++q) {
-        const float* hp = Hp + row * 3 * r + q * r + j;
-        float t = hp[0];
-#pragma unroll
-        for (int sl = 1; sl < kHpSplit; ++sl) t += hp[sl * slice];
-        hq[q] = t;
-      }
-      const float gk = 1.f / (1.f + expf(-(pre[0][jj][rb] + hq[0])));
-      S_out[(size_t)b * r + j] = gk * zin[rb * r2 + j] + (1.f - gk) * tanhf(pre[1][jj][rb] + hq[1]);
-      ovec[row * r + j] = tanhf(pre[2][jj][rb] + hq[2]);
-    }
+  if (eact) {
+    const size_t row = (size_t)eb * g + (k - 1);
+    const float gk = 1.f / (1.f + expf(-(pre[0][ejj][erb] + hq[0])));
+    S_out[(size_t)eb * r + ej] = gk * zin[erb * r2 + ej] + (1.f - gk) * tanhf(pre[1][ejj][erb] + hq[1]);
+    ovec[row * r + ej] = tanhf(pre[2][ejj][erb] + hq[2]);
   }
 }
 
@@ -254,14 +342,15 @@ cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void*
   const float* S_in = S + ((k - 1) & 1) * BR;
   float* S_out = S + (k & 1) * BR;
   const dim3 grid((d.r + kCellJ - 1) / kCellJ, (d.B + kCellB - 1) / kCellB);
-  if (d.wdtype == DSPARK_BF16)
-    k_rnn_cell<1><<<grid, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S_in, S_out, ovec, d.B,
-                                                    d.gamma, d.V, d.r, d.H, k, ws->s.status);
-  else
-    k_rnn_cell<0><<<grid, kCellThreads, smem, st>>>(a.W1, Wr, a.anchor, a.tokens, Hp, S_in, S_out, ovec, d.B,
-                                                    d.gamma, d.V, d.r, d.H, k, ws->s.status);
+  // programmatic dependent launch: the step's kernels wait in-kernel for the one before
+  const cudaError_t e =
+      d.wdtype == DSPARK_BF16
+          ? launch_ex(k_rnn_cell<1>, grid, dim3(kCellThreads), smem, st, true, a.W1, Wr, a.anchor, a.tokens, Hp,
+                      S_in, S_out, ovec, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status)
+          : launch_ex(k_rnn_cell<0>, grid, dim3(kCellThreads), smem, st, true, a.W1, Wr, a.anchor, a.tokens, Hp,
+                      S_in, S_out, ovec, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status);
   ++*launches;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dspark

@@ -421,6 +421,11 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // (launched as a dependent kernel, only the epilogue waits for the kernel
+    // before: the producers stream W2 and U, inputs, meanwhile; the pick
+    // that follows launches when this grid ends, which measured faster than
+    // an early trigger)
+    pdl_wait();
     const int ew = warp - 2, set = ew >> 2, q = warp & 3, m = q * 32 + lane;
     const int row = grp * kRpRows + m;
     const bool valid = row < p.n;
@@ -773,8 +778,9 @@ cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const
   p.ovec = ovec;
   p.blk = ws->s.blk;
   const size_t smem = RpSmem::make(d.r).total + 1024;
-  k_rowpass<kRowRnn><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_u, tm_u, p);
-  return cudaGetLastError();
+  const cudaError_t el = launch_ex(k_rowpass<kRowRnn>, dim3(p.G), dim3(kRpThreads), smem, st, true, tm_w2, tm_u,
+                                   tm_u, p);
+  return el != cudaSuccess ? el : cudaGetLastError();
 }
 
 cudaError_t launch_tree_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
