@@ -88,6 +88,13 @@ __device__ __forceinline__ float ld_w(const void* W, int bf16, size_t i) {
   return reinterpret_cast<const float*>(W)[i];
 }
 
+// Offset (bf16 elements) of the 16-byte piece ch of K-block kb of row m in a
+// K-major MMA operand of `rows` rows with the 128-byte swizzle: 8-row atoms
+// of 1 KB, K-blocks of 64 elements rows x 128 bytes apart.
+__device__ __forceinline__ size_t kmajor_sw128_piece(int m, int kb, int ch, int rows) {
+  return (size_t)kb * (rows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
+}
+
 // Largest key wins; equal keys go to the smaller index (the first maximum).
 // "Nothing yet" is {-inf, kNoIdx}.
 constexpr int kNoIdx = 0x7FFFFFFF;

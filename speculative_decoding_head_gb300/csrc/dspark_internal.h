@@ -2,6 +2,7 @@
 // translation units of libdspark.so (not part of the public C-ABI).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -158,12 +159,15 @@ cudaError_t launch_draft_tc(const dspark_ws* ws, const DraftArgs& a, cudaStream_
 // ovec [B*gamma][r] receives o_k); the whole draft tail on the SIMT path.
 cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr, float* Hp, cudaStream_t st,
                              int* launches);
+// oimg: o_k's bf16 hi and lo images in the row pass's operand layout (null: not written)
 cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void* Wr, const float* Hp, float* S,
-                            float* ovec, int k, cudaStream_t st, int* launches);
+                            float* ovec, __nv_bfloat16* oimg, int k, cudaStream_t st, int* launches);
 // hl: scratch for h split into bf16 hi | lo (rnn_hsplit_bytes), or null: the
-// h projection then runs on CUDA cores
+// h projection then runs on CUDA cores; oimg: scratch of oimg_len bytes for
+// o_k's images, which the cell writes when the row pass runs the block pass
 cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
-                             float* ovec, void* hl, cudaStream_t st, int* launches);
+                             float* ovec, void* hl, __nv_bfloat16* oimg, size_t oimg_len, cudaStream_t st,
+                             int* launches);
 // The h projection on tcgen05 (k_rnn_tc.cu): shapes it takes (bf16 weights,
 // H % 64 == 0, r % 64 == 0, r <= 256), whether this workspace runs it, the
 // bytes of its hi | lo copy of h, and its launch (same Hp layout as
@@ -200,8 +204,8 @@ bool rowpass_supported(const dspark_ws* ws, int n);
 cudaError_t launch_loss_rowpass(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st);
 // One RNN draft step's block log-masses into Scratch::blk (as launch_rnn_blocks_tc),
 // and one PCTree expansion's block log-masses and maxima (as launch_tree_blocks_tc).
-cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
-                                      cudaStream_t st);
+cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec,
+                                      const __nv_bfloat16* oimg, int k, cudaStream_t st);
 cudaError_t launch_tree_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W1, const void* W2,
                                        const int32_t* tok, const int32_t* dep, const int4* state, int N, float* blk,
                                        float* bmax, cudaStream_t st);

@@ -213,7 +213,8 @@ struct RnnStep {
   float* Hp;
   float* S;
   float* ovec;
-  bool tc;  // block pass on tcgen05
+  bool tc;              // block pass on tcgen05
+  __nv_bfloat16* oimg;  // o_k's images for the row pass (when it runs the block pass)
 };
 
 template <int BF16>
@@ -229,12 +230,15 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
   const float* ovec = rnn ? rnn->ovec : nullptr;
   for (int k = 1; k <= d.gamma; ++k) {
     if (rnn) {
-      const cudaError_t e = launch_rnn_cell(ws, a, rnn->Wr, rnn->Hp, rnn->S, rnn->ovec, k, st, launches);
+      const bool rowpass = rnn->tc && rowpass_supported(ws, d.B);
+      const cudaError_t e =
+          launch_rnn_cell(ws, a, rnn->Wr, rnn->Hp, rnn->S, rnn->ovec, rowpass ? rnn->oimg : nullptr, k, st, launches);
       if (e != cudaSuccess) return e;
     }
     if (rnn && rnn->tc) {  // the block pass on tcgen05 (requests as MMA rows where the shape allows)
-      const cudaError_t e = rowpass_supported(ws, d.B) ? launch_rnn_blocks_rowpass(ws, a.U, a.W2, ovec, k, st)
-                                                       : launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
+      const cudaError_t e = rowpass_supported(ws, d.B)
+                                ? launch_rnn_blocks_rowpass(ws, a.U, a.W2, ovec, rnn->oimg, k, st)
+                                : launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
       if (e != cudaSuccess) return e;
     } else {
       k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
@@ -257,7 +261,8 @@ cudaError_t launch_draft_simt(const dspark_ws* ws, const DraftArgs& a, cudaStrea
 }
 
 cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void* Wr, float* Hp, float* S,
-                             float* ovec, void* hl, cudaStream_t st, int* launches) {
+                             float* ovec, void* hl, __nv_bfloat16* oimg, size_t oimg_len, cudaStream_t st,
+                             int* launches) {
   cudaError_t e = launch_conf_hidden(ws, a.h, a.w, st, launches);
   if (e == cudaSuccess) {
     if (hl && rnn_hproj_tc_supported(ws))
@@ -266,8 +271,10 @@ cudaError_t launch_rnn_draft(const dspark_ws* ws, const DraftArgs& a, const void
       e = launch_rnn_hproj(ws, a.h, Wr, Hp, st, launches);
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)ws->d.B * ws->d.r, st);  // s_0 = 0 (buffer 0)
+  // the images' rows past the last request stay zero (the cell writes the others every step)
+  if (e == cudaSuccess && ws->d.B % 128 != 0) e = cudaMemsetAsync(oimg, 0, oimg_len, st);
   if (e != cudaSuccess) return e;
-  const RnnStep rnn{Wr, Hp, S, ovec, ws->use_tc && ws->geo.resid_tc_ok && ws->d.r <= 256};
+  const RnnStep rnn{Wr, Hp, S, ovec, ws->use_tc && ws->geo.resid_tc_ok && ws->d.r <= 256, oimg};
   if (ws->d.wdtype == DSPARK_BF16) return draft_simt_impl<1>(ws, a, st, launches, &rnn);
   return draft_simt_impl<0>(ws, a, st, launches, &rnn);
 }

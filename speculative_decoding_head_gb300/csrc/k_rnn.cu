@@ -136,8 +136,8 @@ template <int BF16>
 __global__ void __launch_bounds__(kCellThreads)
     k_rnn_cell(const void* __restrict__ W1, const void* __restrict__ Wr, const int32_t* __restrict__ anchor,
                const int32_t* __restrict__ tokens, const float* __restrict__ Hp, const float* __restrict__ S_in,
-               float* __restrict__ S_out, float* __restrict__ ovec, int B, int g, int V, int r, int H, int k,
-               int* __restrict__ status) {
+               float* __restrict__ S_out, float* __restrict__ ovec, __nv_bfloat16* __restrict__ oimg, int B, int g,
+               int V, int r, int H, int k, int* __restrict__ status) {
   extern __shared__ __align__(16) float zin[];  // [kCellB][2r]: s_{k-1}, W1[x_{k-1}] of each request
   __shared__ float pre[3][kCellJ][kCellB];
   __shared__ int xs[kCellB];
@@ -291,7 +291,15 @@ __global__ void __launch_bounds__(kCellThreads)
     const size_t row = (size_t)eb * g + (k - 1);
     const float gk = 1.f / (1.f + expf(-(pre[0][ejj][erb] + hq[0])));
     S_out[(size_t)eb * r + ej] = gk * zin[erb * r2 + ej] + (1.f - gk) * tanhf(pre[1][ejj][erb] + hq[1]);
-    ovec[row * r + ej] = tanhf(pre[2][ejj][erb] + hq[2]);
+    const float o = tanhf(pre[2][ejj][erb] + hq[2]);
+    ovec[row * r + ej] = o;
+    if (oimg) {  // o_k as bf16 hi and lo, each in the layout of the row pass's A operand (128 rows a group)
+      const __nv_bfloat16 hi = __float2bfloat16_rn(o), lo = __float2bfloat16_rn(o - __bfloat162float(hi));
+      __nv_bfloat16* im = oimg + (size_t)(eb >> 7) * 2 * 128 * r;
+      const size_t off = kmajor_sw128_piece(eb & 127, ej >> 6, (ej >> 3) & 7, 128) + (ej & 7);
+      im[off] = hi;
+      im[(size_t)128 * r + off] = lo;
+    }
   }
 }
 
@@ -304,6 +312,10 @@ size_t hp_bytes(const dspark_dims& d) {
   return round_up(sizeof(float) * kHpSplit * (size_t)d.B * d.gamma * 3 * d.r, 256);
 }
 size_t state_bytes(const dspark_dims& d) { return round_up(2 * sizeof(float) * (size_t)d.B * d.r, 256); }
+// o_k's bf16 hi and lo images for the row pass, per group of 128 requests
+size_t oimg_bytes(const dspark_dims& d) {
+  return round_up(sizeof(__nv_bfloat16) * 2 * 128 * (size_t)((d.B + 127) / 128) * d.r, 256);
+}
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -324,7 +336,7 @@ cudaError_t launch_rnn_hproj(const dspark_ws* ws, const float* h, const void* Wr
 }
 
 cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void* Wr, const float* Hp, float* S,
-                            float* ovec, int k, cudaStream_t st, int* launches) {
+                            float* ovec, __nv_bfloat16* oimg, int k, cudaStream_t st, int* launches) {
   const dspark_dims& d = ws->d;
   const size_t smem = sizeof(float) * kCellB * 2 * (size_t)d.r;  // 128 KB at r = 1024
   static bool configured = false;
@@ -346,9 +358,9 @@ cudaError_t launch_rnn_cell(const dspark_ws* ws, const DraftArgs& a, const void*
   const cudaError_t e =
       d.wdtype == DSPARK_BF16
           ? launch_ex(k_rnn_cell<1>, grid, dim3(kCellThreads), smem, st, true, a.W1, Wr, a.anchor, a.tokens, Hp,
-                      S_in, S_out, ovec, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status)
+                      S_in, S_out, ovec, oimg, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status)
           : launch_ex(k_rnn_cell<0>, grid, dim3(kCellThreads), smem, st, true, a.W1, Wr, a.anchor, a.tokens, Hp,
-                      S_in, S_out, ovec, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status);
+                      S_in, S_out, ovec, oimg, d.B, d.gamma, d.V, d.r, d.H, k, ws->s.status);
   ++*launches;
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -361,7 +373,8 @@ extern "C" size_t dspark_rnn_draft_scratch_bytes(const dspark_ws* ws) {
   if (!ws) return 0;
   // the hi | lo copy of h for the tcgen05 h projection, wherever the shape allows it
   // (whichever compute path the workspace is set to when the call runs)
-  return hp_bytes(ws->d) + state_bytes(ws->d) + (rnn_hproj_tc_shape(ws->d) ? rnn_hsplit_bytes(ws->d) : 0);
+  return hp_bytes(ws->d) + state_bytes(ws->d) + oimg_bytes(ws->d) +
+         (rnn_hproj_tc_shape(ws->d) ? rnn_hsplit_bytes(ws->d) : 0);
 }
 
 extern "C" dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2,
@@ -379,11 +392,13 @@ extern "C" dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const v
   char* base = static_cast<char*>(scratch);
   float* Hp = reinterpret_cast<float*>(base);
   float* S = reinterpret_cast<float*>(base + hp_bytes(d));
-  void* hl = rnn_hproj_tc_shape(d) ? static_cast<void*>(base + hp_bytes(d) + state_bytes(d)) : nullptr;
+  __nv_bfloat16* oimg = reinterpret_cast<__nv_bfloat16*>(base + hp_bytes(d) + state_bytes(d));
+  void* hl = rnn_hproj_tc_shape(d) ? static_cast<void*>(base + hp_bytes(d) + state_bytes(d) + oimg_bytes(d)) : nullptr;
   DraftArgs a{U, W1, W2, anchor, h, w, T, seed, round, tokens, pd_tok, lse, conf};
   int launches = 0;
   const cudaError_t e =
-      launch_rnn_draft(ws, a, Wr, Hp, S, ovec, hl, reinterpret_cast<cudaStream_t>(stream), &launches);
+      launch_rnn_draft(ws, a, Wr, Hp, S, ovec, hl, oimg, oimg_bytes(d), reinterpret_cast<cudaStream_t>(stream),
+                       &launches);
   ws->last_launches = launches;
   if (e == cudaSuccess) return DSPARK_OK;
   fprintf(stderr, "dspark: CUDA error %s\n", cudaGetErrorString(e));

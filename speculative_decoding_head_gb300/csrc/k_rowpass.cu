@@ -90,8 +90,8 @@ struct RpSmem {
     s.u = s.w2 + kRpNW * kRpW2Stage;
     s.bars = s.u + kRpNU * kRpUStage;
     // w2 full/empty, u full/empty, acc_u, t_full, t_empty, p_full, p_empty, a_full, drains,
-    // a_cp_hi, a_cp_lo
-    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAcc + 5);
+    // a_cp_hi, a_cp_lo, a_ld
+    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAcc + 6);
     // misc: TMEM address, abort word
     s.total = s.misc + 64;
     return s;
@@ -102,6 +102,7 @@ struct RpParams {
   int n, g, V, r, nblk, nG, G;
   int step;            // RNN: draft step k (1-based)
   const float* ovec;   // RNN: [B][g][r] o_k
+  const __nv_bfloat16* oimg;  // RNN: per row group, o_k's bf16 hi then lo image in the A operand's layout
   const float* U;      // PCTree: U [B][g][V], read by the epilogue
   const int32_t* tree_tok;   // PCTree: [B][N+1] nodes' tokens, depths; state[b].y = the node to expand
   const int32_t* tree_dep;
@@ -125,9 +126,7 @@ __device__ __forceinline__ int rp_group_ctas(int G, int nG, int g) { return (G -
 // Offset (bf16 elements) of the 16-byte piece ch of K-block kb of row m in the
 // A operand: K-major, 128-byte swizzle, 8-row atoms of 1 KB, K-blocks of 64
 // elements 16 KB apart.
-__device__ __forceinline__ size_t rp_a_piece(int m, int kb, int ch) {
-  return (size_t)kb * (kRpRows * 64) + (m >> 3) * 512 + (m & 7) * 64 + ((ch ^ (m & 7)) << 3);
-}
+__device__ __forceinline__ size_t rp_a_piece(int m, int kb, int ch) { return kmajor_sw128_piece(m, kb, ch, kRpRows); }
 
 // (max, sum 2^(y log2e - max log2e)) of 32 values on fp32 pairs.
 __device__ __forceinline__ void half_ms(const float (&y)[32], float& mb, float& sb) {
@@ -208,6 +207,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   const uint32_t a_full = b5 + 8u * (5 * kRpNAcc);
   const uint32_t drain = a_full + 8u, drain_c = a_full + 16u;
   const uint32_t a_cp_hi = a_full + 24u, a_cp_lo = a_full + 32u;  // RNN: the A images are in TMEM
+  const uint32_t a_ld = a_full + 40u;                              // RNN: an A image has landed in shared memory
   constexpr bool kLoss = MODE == kRowLoss0 || MODE == kRowLoss1;
   // TMEM: accumulators at columns 0 and 128; then the P buffers (loss) or
   // the A images hi and lo (RNN), r / 2 columns each
@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     tc::mbar_init(drain_c, 1);
     tc::mbar_init(a_cp_hi, 1);
     tc::mbar_init(a_cp_lo, 1);
+    tc::mbar_init(a_ld, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
@@ -334,28 +335,15 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     if (lane == 0) {
       bool ok = true;
       int iss = 0;
-      if constexpr (MODE == kRowRnn) {
-        // the epilogue leaves o_k's hi image, then its lo image, in the A
-        // region; each goes to its TMEM columns (16 bf16 of K per 8 columns)
-        for (int img = 0; img < 2 && ok; ++img) {
-          ok = tc::mbar_wait(a_full, img, abort);
-          if (!ok) break;
-          tc::tc_fence_after();
-          for (int ks = 0; ks < p.r / 16; ++ks)
-            tc::cp_128x256b(tmem + (img ? tm_lo : tm_hi) + (uint32_t)(ks * 8),
-                            tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024));
-          tc::mma_commit(img ? a_cp_lo : a_cp_hi);
-        }
-      }
       const int per_tile = MODE == kRowTree ? 0 : kLoss ? 2 : 1;
-      for (int tj = 0; tj < ntl && ok; ++tj) {
+      auto copy_tile = [&](int tj) {
         const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
-        ok = tc::mbar_wait(t_empty(ab), ((tj / kRpNAcc) & 1) ^ 1, abort);  // accumulator and P buffer free
-        if (ok && per_tile == 0) tc::mma_commit(acc_u(ab));  // PCTree: the MMAs start from zero
-        for (int e = 0; e < per_tile * nbt && ok; ++e) {
+        bool okt = tc::mbar_wait(t_empty(ab), ((tj / kRpNAcc) & 1) ^ 1, abort);  // accumulator and P buffer free
+        if (okt && per_tile == 0) tc::mma_commit(acc_u(ab));  // PCTree: the MMAs start from zero
+        for (int e = 0; e < per_tile * nbt && okt; ++e) {
           const int j = e % nbt, us = iss % kRpNU;
-          ok = tc::mbar_wait(u_full(us), (iss / kRpNU) & 1, abort);
-          if (!ok) break;
+          okt = tc::mbar_wait(u_full(us), (iss / kRpNU) & 1, abort);
+          if (!okt) break;
           tc::tc_fence_after();
           const uint32_t d = tmem + (uint32_t)((e < nbt ? 0 : kRpNAcc * kRpAccCols) + ab * kRpAccCols + j * kRpBlk);
 #pragma unroll
@@ -368,7 +356,45 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           ++iss;
           if (e == nbt - 1) tc::mma_commit(acc_u(ab));
         }
-        if (ok && kLoss) tc::mma_commit(p_full(ab));
+        if (okt && kLoss) tc::mma_commit(p_full(ab));
+        return okt;
+      };
+      if constexpr (MODE == kRowRnn) {
+        // o_k's hi image, then its lo image, written by the cell in the
+        // operand's layout: each comes into the A region by one bulk copy and
+        // goes to its TMEM columns (16 bf16 of K per 8 columns). The first
+        // tiles' U goes into the accumulators while the hi image is in flight.
+        pdl_wait();  // the images are the cell's
+        const uint32_t abytes = (uint32_t)(kRpRows * p.r * 2);
+        const __nv_bfloat16* img = p.oimg + (size_t)grp * 2 * kRpRows * p.r;
+        int lds = 0;  // image loads issued
+        tc::mbar_arrive_expect_tx(a_ld, abytes);
+        tc::bulk_load(sA, img, abytes, a_ld);
+        ++lds;
+        const int pre = min(ntl, kRpNAcc);
+        for (int tj = 0; tj < pre && ok; ++tj) ok = copy_tile(tj);
+        for (int im = 0; im < 2 && ok; ++im) {
+          ok = tc::mbar_wait(a_ld, im, abort);
+          if (!ok) break;
+          for (int ks = 0; ks < p.r / 16; ++ks)
+            tc::cp_128x256b(tmem + (im ? tm_lo : tm_hi) + (uint32_t)(ks * 8),
+                            tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024));
+          tc::mma_commit(im ? a_cp_lo : a_cp_hi);
+          if (im == 0) {  // the lo image takes the region once the copies have read the hi image
+            ok = tc::mbar_wait(a_cp_hi, 0, abort);
+            if (!ok) break;
+            tc::mbar_arrive_expect_tx(a_ld, abytes);
+            tc::bulk_load(sA, img + (size_t)kRpRows * p.r, abytes, a_ld);
+            ++lds;
+          }
+        }
+        if (!ok) {  // an image copy still in flight lands before the CTA ends
+          volatile int never = 0;
+          tc::mbar_wait(a_ld, lds - 1, &never);
+        }
+        for (int tj = pre; tj < ntl && ok; ++tj) ok = copy_tile(tj);
+      } else {
+        for (int tj = 0; tj < ntl && ok; ++tj) ok = copy_tile(tj);
       }
       if (!ok) {
         if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
@@ -436,58 +462,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     bool live = valid;           // RNN, PCTree: the row's request has a node to expand / is drafted
     const float* urow = nullptr;  // PCTree: U of the expanded node's depth
     if constexpr (MODE == kRowRnn) {
-      // ---- A = o_k of the group's rows, as bf16 hi (then lo) images; the
-      // copier moves each into tensor memory before the next is written
-      uint4 lo[16];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float4 f[8][2];
-#pragma unroll
-        for (int i8 = 0; i8 < 8; ++i8) {
-          const int rl = 2 * (half * 8 + i8) + set, mr = q * 32 + rl, br = grp * kRpRows + mr;
-          f[i8][0] = f[i8][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (br < p.n && lane < p.r / 8) {
-            const float4* src = reinterpret_cast<const float4*>(
-                p.ovec + ((size_t)br * p.g + (p.step - 1)) * p.r + (size_t)lane * 8);
-            f[i8][0] = __ldg(src);
-            f[i8][1] = __ldg(src + 1);
-          }
-        }
-#pragma unroll
-        for (int i8 = 0; i8 < 8; ++i8) {
-          const float o8[8] = {f[i8][0].x, f[i8][0].y, f[i8][0].z, f[i8][0].w,
-                               f[i8][1].x, f[i8][1].y, f[i8][1].z, f[i8][1].w};
-          __nv_bfloat16 h8[8], l8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            h8[e] = __float2bfloat16_rn(o8[e]);
-            l8[e] = __float2bfloat16_rn(o8[e] - __bfloat162float(h8[e]));
-          }
-          const uint4 hv = *reinterpret_cast<const uint4*>(h8);
-          lo[half * 8 + i8] = *reinterpret_cast<const uint4*>(l8);
-          const int rl = 2 * (half * 8 + i8) + set;
-          if (lane < p.r / 8)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                             sA + 2u * (uint32_t)rp_a_piece(q * 32 + rl, lane >> 3, lane & 7)),
-                         "r"(hv.x), "r"(hv.y), "r"(hv.z), "r"(hv.w)
-                         : "memory");
-        }
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(a_full);
-      const bool okc = __all_sync(0xFFFFFFFFu, tc::mbar_wait(a_cp_hi, 0, abort));  // the hi image has moved
-      if (okc && lane < p.r / 8) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           sA + 2u * (uint32_t)rp_a_piece(q * 32 + 2 * i + set, lane >> 3, lane & 7)),
-                       "r"(lo[i].x), "r"(lo[i].y), "r"(lo[i].z), "r"(lo[i].w)
-                       : "memory");
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(a_full);
+      // ---- A = o_k's hi and lo images: the copier brings them ready-made
     } else {
       // ---- A = the rows' W1 row: W1[x*_{k-1}] (loss; the anchor at k = 0)
       // or W1[token of the node to expand] (PCTree)
@@ -755,8 +730,8 @@ RpParams base_params(const dspark_ws* ws, int n) {
 
 }  // namespace
 
-cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec, int k,
-                                      cudaStream_t st) {
+cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const void* W2, const float* ovec,
+                                      const __nv_bfloat16* oimg, int k, cudaStream_t st) {
   const dspark_dims& d = ws->d;
   cudaError_t e = rowpass_configure();
   CUtensorMap tm_w2, tm_u;
@@ -776,6 +751,7 @@ cudaError_t launch_rnn_blocks_rowpass(const dspark_ws* ws, const float* U, const
   RpParams p = base_params(ws, d.B);
   p.step = k;
   p.ovec = ovec;
+  p.oimg = oimg;
   p.blk = ws->s.blk;
   const size_t smem = RpSmem::make(d.r).total + 1024;
   const cudaError_t el = launch_ex(k_rowpass<kRowRnn>, dim3(p.G), dim3(kRpThreads), smem, st, true, tm_w2, tm_u,
