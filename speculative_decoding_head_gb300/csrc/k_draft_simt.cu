@@ -101,13 +101,38 @@ __global__ void __launch_bounds__(kPickThreadsS)
   pdl_trigger();
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  const size_t o = (size_t)b * g + (k - 1);
+  // the loads that do not depend on the previous token go out with it
   const int x = prev_token(anchor, tokens, b, g, k);
+  if (ovec)
+    for (int i = tid; i < r; i += blockDim.x) e[i] = ovec[o * r + i];
+  // the block log-masses, four consecutive blocks a thread (one counter draw
+  // serves four blocks): the thread's (max, sum) and its best block key
+  MS ms{-INFINITY, 0.f};
+  KeyIdx kb = key_none();
+  for (int s4 = 4 * tid; s4 < nblk; s4 += 4 * blockDim.x) {
+    float lm[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) lm[u] = s4 + u < nblk ? blk[(size_t)b * nblk + s4 + u] : -INFINITY;
+    const uint4 wq = rng.block4(kDraftBlock, b, k, s4);
+    const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+    const float m4 = fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]));
+    if (m4 > -INFINITY) {
+      float t4 = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) t4 += __expf(lm[u] - m4);
+      ms = ms_combine(ms, MS{m4, t4});
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (lm[u] > -INFINITY) kb = better(kb, KeyIdx{lm[u] + gumbel(wv[u]), s4 + u});
+  }
   if (x < 0 || x >= V) {
     if (tid == 0) raise_status(status, DSPARK_ERANGE);
     return;
   }
-  const size_t o = (size_t)b * g + (k - 1);
-  for (int i = tid; i < r; i += blockDim.x) e[i] = ovec ? ovec[o * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
+  if (!ovec)
+    for (int i = tid; i < r; i += blockDim.x) e[i] = ld_w(W1, BF16, (size_t)x * r + i);
   __syncthreads();
 
   // eq. (7): c_k = sigma((s_h + w_r . W1[x_{k-1}]) / T_k)
@@ -116,17 +141,17 @@ __global__ void __launch_bounds__(kPickThreadsS)
     cr = fmaf(w[H + i], ovec ? ld_w(W1, BF16, (size_t)x * r + i) : e[i], cr);
   cr = warp_sum(cr);
   if (lane == 0) red_f[warp] = cr;
-  // log-sum-exp over the block log-masses
-  MS ms{-INFINITY, 0.f};
-  for (int s = tid; s < nblk; s += blockDim.x) ms = ms_combine(ms, MS{blk[(size_t)b * nblk + s], 1.f});
-  ms = warp_ms(ms);
-  if (lane == 0) red_ms[warp] = ms;
-  // block draw: argmax_s (log mass_s + G_s)
-  KeyIdx kb = key_none();
-  for (int s = tid; s < nblk; s += blockDim.x) {
-    const float lm = blk[(size_t)b * nblk + s];
-    if (lm > -INFINITY) kb = better(kb, KeyIdx{lm + gumbel(rng.word(kDraftBlock, b, k, s)), s});
+  // log-sum-exp over the block log-masses: the warp's maximum first, then the
+  // rescaled sums (one exponential a lane)
+  {
+    float M = ms.m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+    float t = ms.m == -INFINITY ? 0.f : ms.s * __expf(ms.m - M);
+    t = warp_sum(t);
+    if (lane == 0) red_ms[warp] = MS{M, M == -INFINITY ? 0.f : t};
   }
+  // block draw: argmax_s (log mass_s + G_s)
   kb = warp_best(kb);
   if (lane == 0) red_k[warp] = kb;
   __syncthreads();
@@ -153,6 +178,9 @@ __global__ void __launch_bounds__(kPickThreadsS)
     if (tid == 0) raise_status(status, DSPARK_ENUMERIC);
     return;
   }
+  // U of the block's tokens, loaded beside the W2 columns below
+  float ublk = 0.f;
+  if (tid < kBlockW && sb * kBlockW + tid < V) ublk = U[o * V + sb * kBlockW + tid];
   // token draw inside block sb: recompute z for its 64 tokens, each over
   // 16 K slices (a thread's slice of rows i = q, q + 16, ... with all of its
   // W2 loads in flight), the slices added in a fixed order
@@ -175,7 +203,7 @@ __global__ void __launch_bounds__(kPickThreadsS)
       float zs = 0.f;
 #pragma unroll
       for (int q = 0; q < kPickKs; ++q) zs += zpart[q][tid];
-      z = U[o * V + v] + zs;
+      z = ublk + zs;
     }
     zblk[tid] = z;
     KeyIdx kt = key_none();
