@@ -971,6 +971,11 @@ __global__ void __launch_bounds__(kPickThreads)
     }
     return;
   }
+  float uz = 0.f, pz = 0.f;
+  if (tid < kBlockW && sb * kBlockW + tid < V) {  // issued ahead of the W2 columns, used after the barrier
+    uz = U[((size_t)b * g + n) * V + sb * kBlockW + tid];
+    pz = Prow[sb * kBlockW + tid];
+  }
   {
     // z_v - U = sum_i e_i W2[i, v] for the 64 tokens of the block: 16 groups
     // of K rows, each thread's loads (r / 16 of them) all in flight together
@@ -983,11 +988,6 @@ __global__ void __launch_bounds__(kPickThreads)
       for (int i = q; i < r; i += kQ) acc = fmaf(e[i], ld_w(W2, BF16, (size_t)i * V + v), acc);
     }
     zpart[q][vl] = acc;
-  }
-  float uz = 0.f, pz = 0.f;
-  if (tid < kBlockW && sb * kBlockW + tid < V) {  // issued before the barrier, used after it
-    uz = U[((size_t)b * g + n) * V + sb * kBlockW + tid];
-    pz = Prow[sb * kBlockW + tid];
   }
   __syncthreads();
   if (tid < kBlockW) {
