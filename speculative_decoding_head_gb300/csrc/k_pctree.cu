@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(kPickT)
   __shared__ float4 red_c[kPickT / 32];
   __shared__ int red_i[kPickT / 32];
   __shared__ float s_L;
+  pdl_wait();  // the expansion's block masses (launched as a dependent kernel)
+  pdl_trigger();
   const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int4 st = state[b];
   if (st.w) return;
@@ -656,12 +658,15 @@ cudaError_t launch_pctree_build(const dspark_ws* ws, const float* U, const void*
         k_tree_blocks<0><<<dim3(chunks, d.B), 256, esm, st>>>(U, W1, W2, tok, dep, ts.state, N, d.gamma, d.V, d.r,
                                                               nblk, ws->s.blk, ts.bmax);
     }
-    if (d.wdtype == DSPARK_BF16)
-      k_tree_pick<1><<<d.B, kPickT, esm, st>>>(U, W1, W2, d.gamma, d.V, d.r, nblk, c, N, ws->s.blk, ts.bmax, tok, par,
-                                             dep, lp, ts.state, ts.frontier, ws->s.status);
-    else
-      k_tree_pick<0><<<d.B, kPickT, esm, st>>>(U, W1, W2, d.gamma, d.V, d.r, nblk, c, N, ws->s.blk, ts.bmax, tok, par,
-                                             dep, lp, ts.state, ts.frontier, ws->s.status);
+    // the expansion and the pick are chained by programmatic dependent launch
+    // (each waits in-kernel for the one before)
+    const cudaError_t ep =
+        d.wdtype == DSPARK_BF16
+            ? launch_ex(k_tree_pick<1>, dim3(d.B), dim3(kPickT), esm, st, true, U, W1, W2, d.gamma, d.V, d.r, nblk, c,
+                        N, ws->s.blk, ts.bmax, tok, par, dep, lp, ts.state, ts.frontier, ws->s.status)
+            : launch_ex(k_tree_pick<0>, dim3(d.B), dim3(kPickT), esm, st, true, U, W1, W2, d.gamma, d.V, d.r, nblk, c,
+                        N, ws->s.blk, ts.bmax, tok, par, dep, lp, ts.state, ts.frontier, ws->s.status);
+    if (ep != cudaSuccess) return ep;
     *launches += 2;
   }
   k_tree_count<<<(d.B + 127) / 128, 128, 0, st>>>(ts.state, d.B, n_nodes);

@@ -777,7 +777,10 @@ cudaError_t launch_tree_blocks_rowpass(const dspark_ws* ws, const float* U, cons
   p.blk = blk;
   p.bmax = bmax;
   const size_t smem = RpSmem::make(d.r).total + 1024;
-  k_rowpass<kRowTree><<<p.G, kRpThreads, smem, st>>>(tm_w2, tm_w2, tm_w2, p);
+  // a dependent launch: only the epilogue reads what the pick before wrote
+  const cudaError_t el = launch_ex(k_rowpass<kRowTree>, dim3(p.G), dim3(kRpThreads), smem, st, true, tm_w2, tm_w2,
+                                   tm_w2, p);
+  if (el != cudaSuccess) return el;
   return cudaGetLastError();
 }
 
