@@ -10,14 +10,16 @@
 // s_0 = 0 and x_0 = the anchor. The weights are stacked as Wr [3][r][2r + H]
 // (W_g, W_c, W_o) in the dtype of W1 and W2. The draft tail then takes
 // o_k = tanh(W_o z_k) in place of W1[x_{k-1}]: the vocabulary pass on tcgen05
-// (k_resid_tc.cu, o_k as bf16 hi + lo operands) or on CUDA cores, then the
+// (k_rowpass.cu, o_k as bf16 hi + lo operands that the cell writes in its
+// operand layout; k_resid_tc.cu for other shapes) or on CUDA cores, then the
 // SIMT pick (k_draft_simt.cu).
 //
 // Two kernels: k_rnn_hproj, once per round, the h_k part of all three
 // projections for every position (a [B*gamma x H] x [H x 3r] product, the
-// bulk of the cell's arithmetic, which does not depend on drafted tokens);
-// k_rnn_cell, before each draft step, one CTA per 16 state entries and 16
-// requests: the [s; W1[x]] part, then the gate, the state update and o_k.
+// bulk of the cell's arithmetic, which does not depend on drafted tokens; on
+// tcgen05 in k_rnn_tc.cu where the shape allows); k_rnn_cell, before each
+// draft step, one CTA per 8 state entries and 16 requests: the [s; W1[x]]
+// part, then the gate, the state update and o_k.
 #include <stdio.h>
 
 #include "dspark_common.cuh"

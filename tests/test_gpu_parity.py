@@ -239,10 +239,13 @@ def test_device_errors_are_reported_not_faulted():
         ws.plan(conf.cpu(), dev["sps"])               # host tensors are refused by the binding
 
 
-def test_verify_rejects_inconsistent_lengths():
+@pytest.mark.parametrize("V", [4096, 16384], ids=["bulk", "dynamic"])
+def test_verify_rejects_inconsistent_lengths(V):
     """Lengths outside [1, gamma + 1] or offsets that do not add up are reported
-    as ERANGE by the sweep (bulk path: V % 64 == 0), not faulted."""
-    wl = MID["mid_ragged"].with_(B=16, V=4096, seed=23)
+    as ERANGE, not faulted: by the bulk sweep (V % 64 == 0, 64 blocks a row)
+    and by the dynamic sweep's finalize (256 blocks a row), which also leaves
+    its chunk counter ready for the next call."""
+    wl = MID["mid_ragged"].with_(B=16, V=V, seed=23)
     assert wl.V % 64 == 0
     inp = make_inputs(wl)
     dev, npi = to_device(inp), np_inputs(inp)
