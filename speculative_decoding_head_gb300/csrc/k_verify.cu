@@ -638,19 +638,13 @@ __device__ __forceinline__ MS warp_ms_maxfirst(MS x) {
 __global__ void __launch_bounds__(kDynThreads)
     k_verify_sweep_dyn(const float* __restrict__ P, const int32_t* __restrict__ row_off, int B, int nblk, int Rmax,
                        float2* __restrict__ part, float* __restrict__ vlse, int* __restrict__ status,
-                       int* __restrict__ sched) {
+                       int* __restrict__ sched, int pre_nc) {
   extern __shared__ __align__(128) unsigned char smem[];
-  pdl_wait();     // the row offsets may be the planner's
-  pdl_trigger();  // the finalize's CTAs may become resident and wait for this grid's end
   float* stage = reinterpret_cast<float*>(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kDynStages * kBulkFloats * 4);  // full[S], empty[S]
   __shared__ int s_chunk[kDynStages];  // chunk in each stage, -1: none (the consumers stop there)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int R = min(max(row_off[B], 0), Rmax);
-  const long long T = (long long)R * nblk;
-  if (T == 0) return;  // no rows: the counter is not touched
-  const int NC = (int)((T + kBulkUnits - 1) / kBulkUnits);
-  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8u * kDynStages;
+  const uint32_t full0 = tc::smem_u32(bars), empty0 = full0 + 8u * kDynStages, st0 = tc::smem_u32(stage);
   if (tid == 0) {
     for (int i = 0; i < kDynStages; ++i) {
       tc::mbar_init(full0 + 8u * i, 1);
@@ -659,15 +653,40 @@ __global__ void __launch_bounds__(kDynThreads)
     tc::fence_barrier_init();
   }
   __syncthreads();
+  const bool prod = warp == kDynConsumers && lane == 0;
+  const uint64_t pol = tc::policy_evict_first();  // P is read once: W2 stays in L2 for the residual pass
+  // ---- before the wait: inside a round (pre_nc > 0) the producer takes its
+  // first chunks and starts the copies of those below pre_nc, blocks that
+  // exist whatever the plan (the planner gives every request a row)
+  int first = 0, pending = 0, npre = 0;
+  if (prod && pre_nc > 0) {
+    first = atomicAdd(sched, kDynStages);  // the first stages' chunks in one take
+    pending = atomicAdd(sched, 1);
+    for (; npre < kDynStages && first + npre < pre_nc; ++npre) {
+      const uint32_t fb = full0 + 8u * npre;
+      s_chunk[npre] = first + npre;
+      tc::mbar_arrive_expect_tx(fb, (uint32_t)kBulkFloats * 4u);
+      tc::bulk_load_hint(st0 + (uint32_t)npre * kBulkFloats * 4u, P + (size_t)(first + npre) * kBulkFloats,
+                         (uint32_t)kBulkFloats * 4u, fb, pol);
+    }
+  }
+  pdl_wait();     // the row offsets may be the planner's
+  pdl_trigger();  // the finalize's CTAs may become resident and wait for this grid's end
   volatile int never = 0;
+  const int R = min(max(row_off[B], 0), Rmax);
+  const long long T = (long long)R * nblk;
+  const int NC = (int)((T + kBulkUnits - 1) / kBulkUnits);
   if (warp == kDynConsumers) {  // ---- producer
     if (lane != 0) return;
-    const uint32_t st0 = tc::smem_u32(stage);
-    const uint64_t pol = tc::policy_evict_first();  // P is read once: W2 stays in L2 for the residual pass
-    const int first = atomicAdd(sched, kDynStages);  // the first stages' chunks in one take
-    int pending = atomicAdd(sched, 1);
-    int it = 0;  // stage fills so far
-    for (;; ++it) {
+    if (pre_nc <= 0) {
+      first = atomicAdd(sched, kDynStages);
+      pending = atomicAdd(sched, 1);
+    }
+    int it = npre;  // stage fills so far
+    // (a chunk taken before the wait at or past the end: the consumers stop
+    // there, so nothing more is filled)
+    const bool stop = npre > 0 && first + npre - 1 >= NC;
+    for (; !stop; ++it) {
       const int sidx = it % kDynStages;
       const uint32_t fb = full0 + 8u * sidx;
       if (it >= kDynStages && !tc::mbar_wait(empty0 + 8u * sidx, (it / kDynStages - 1) & 1, &never)) {
@@ -699,6 +718,7 @@ __global__ void __launch_bounds__(kDynThreads)
       tc::mbar_wait(full0 + 8u * (i % kDynStages), (i / kDynStages) & 1, &nv);
     return;
   }
+  if (T == 0) return;  // no rows
   // ---- consumers: each warp on its own
   for (int it = 0;; ++it) {
     const int sidx = it % kDynStages;
@@ -707,7 +727,7 @@ __global__ void __launch_bounds__(kDynThreads)
       break;  // this warp releases no more stages: the producer gives up too
     }
     const int c = s_chunk[sidx];
-    if (c < 0) break;
+    if (c < 0 || c >= NC) break;  // (a chunk taken before the wait may lie past the end)
     const long long uw = (long long)c * kBulkUnits + (warp << 5), u = uw + lane;  // the warp's group, the lane's unit
     if (uw >= T) {  // the ragged last chunk: a group past the end
       __syncwarp();
@@ -1026,7 +1046,8 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   if (dyn) {  // chunks taken from a counter; the accept tests in a kernel of their own
     cudaError_t e = launch_ex(k_verify_sweep_dyn, dim3(2 * geo.num_sms), dim3(kDynThreads), sweep_dyn_smem_bytes(),
                               st, pdl, a.P, a.row_off, d.B, geo.nblk, d.B * (d.gamma + 1),
-                              reinterpret_cast<float2*>(ws->s.vpart), ws->s.vlse, ws->s.status, ws->s.vsched);
+                              reinterpret_cast<float2*>(ws->s.vpart), ws->s.vlse, ws->s.status, ws->s.vsched,
+                              a.rowtab ? (int)((long long)d.B * geo.nblk / kBulkUnits) : 0);
     if (e != cudaSuccess) return e;
     e = launch_ex(k_verify_fin_dyn, dim3(d.B), dim3(kFinWarps * 32), 0, st, pdl, fin, d.B * (d.gamma + 1),
                   ws->s.vsched, ws->s.vlse);
