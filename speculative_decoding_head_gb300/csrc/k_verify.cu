@@ -933,21 +933,24 @@ __global__ void __launch_bounds__(kPickThreads)
   __shared__ KeyIdx red_k[kPickThreads / 32];
   __shared__ float zpart[kPickThreads / kBlockW][kBlockW];
   __shared__ int s_blk;
-  pdl_wait();  // the residual block keys are the previous kernel's
   const int b = blockIdx.x;
-  // this round's flags only if every stage so far left the status clear (no
-  // kernel running now writes the status, so every thread reads the same)
-  if (!vflag[b] || *(volatile const int*)status != 0) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+  // the flag, the first rejection and its row are the finalize's, which ended
+  // before the block pass began (the block pass waited for it), so they and
+  // W1[x_n] (the previous token's row, which does not depend on the drawn
+  // block) load before the wait on the block pass
+  const int flag = vflag[b];
   const int n = min(max(n_acc[b], 0), g - 1);
   const float* Prow = P + (size_t)min(max(vrow[b], 0), (int)gridDim.x * (g + 1) - 1) * V;
-  // W1[x_n] (the previous token's row) does not depend on the drawn block:
-  // its load overlaps the reduction of the block keys
-  {
+  if (flag) {
     const int x = n == 0 ? anchor[b] : tokens[(size_t)b * g + (n - 1)];
     for (int i = tid; i < r; i += blockDim.x)
       e[i] = ovec ? ovec[((size_t)b * g + n) * r + i] : ld_w(W1, BF16, (size_t)x * r + i);
   }
+  pdl_wait();  // the residual block keys are the previous kernel's
+  // this round's flags only if every stage so far left the status clear (no
+  // kernel running now writes the status, so every thread reads the same)
+  if (!flag || *(volatile const int*)status != 0) return;
   if (warp == 0) {
     KeyIdx k2 = key_none();
     for (int i = lane; i < nchunk; i += 32) {
