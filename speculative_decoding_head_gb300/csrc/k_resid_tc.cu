@@ -271,6 +271,19 @@ __global__ void __launch_bounds__(kRThreads, 1)
       tc::prefetch_tmap(&tm_p);
     }
   }
+  // W2 is an input: the first ring stages of the first group's tiles are
+  // filled before the wait on the previous kernel (thread 0, which initialised
+  // the barriers, is the W2 producer)
+  const int npre = min(kRNW, 2 * nt);
+  if (threadIdx.x == 0) {
+    const uint64_t keep = tc::policy_evict_last();
+    for (int hs = 0; hs < npre; ++hs) {
+      const int t = tile_of(0, hs >> 1), h = hs & 1;
+      tc::mbar_arrive_expect_tx(w2_full(hs), w2_bytes);
+      tc::tma_load_2d(sW2 + hs * w2_bytes, &tm_w2, t * kRM, h * (p.r / 2), w2_full(hs), keep);
+      tc::tma_load_2d(sW2 + hs * w2_bytes + box_bytes, &tm_w2, t * kRM + 64, h * (p.r / 2), w2_full(hs), keep);
+    }
+  }
   // the rejected requests, in request order (every CTA builds the same list).
   // The flags, positions and rows are this round's only if every stage so far
   // left the status clear: an error leaves the list empty.
@@ -306,15 +319,22 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (W2 tiles)
+    if (lane == 0 && ngroups == 0) {  // nothing to do: the stages filled before the wait land first
+      for (int hs = 0; hs < npre; ++hs) {
+        volatile int never = 0;
+        tc::mbar_wait(w2_full(hs), 0, &never);
+      }
+    }
     if (lane == 0 && ngroups > 0) {
       const uint64_t keep = tc::policy_evict_last();
-      int issued = 0;
+      int issued = npre;
       bool ok = true;
       for (int gq = 0; gq < ngroups && ok; ++gq) {
         for (int i = 0; i < nt && ok; ++i) {
           const int t = tile_of(gq, i);
           for (int h = 0; h < 2 && ok; ++h) {
             const int hs = 2 * (gq * nt + i) + h, ws = hs % kRNW;
+            if (hs < npre) continue;  // filled before the wait
             ok = tc::mbar_wait(w2_empty(ws), ((hs / kRNW) & 1) ^ 1, abort);
             if (!ok) break;
             tc::mbar_arrive_expect_tx(w2_full(ws), w2_bytes);
