@@ -104,9 +104,9 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out);
 void dspark_ws_destroy(dspark_ws* ws);
 
 /* Clear the device status word, the lagged planner's round counter, the
- * draft kernel's grid-barrier words and winner slots, and the verify sweep's
- * per-request completion counters, on `stream`. Call it after any call that
- * left a non-zero device status. */
+ * draft kernel's grid-barrier words and winner slots, and the verify sweeps'
+ * counters (per-request completion counts, the chunk counter), on `stream`.
+ * Call it after any call that left a non-zero device status. */
 dspark_status dspark_ws_reset(dspark_ws* ws, dspark_stream_t stream);
 
 /* Copy the device status word into *device_status (a synchronous 4-byte copy;
@@ -302,9 +302,11 @@ size_t dspark_train_loss_scratch_bytes(const dspark_ws* ws);
  * row-major, no bias) in the workspace's weight dtype; ovec [B][gamma][r] fp32
  * receives o_k. The other arguments are those of dspark_markov_draft. Every
  * pointer is a 16-byte aligned device pointer owned by the caller; scratch
- * holds dspark_rnn_draft_scratch_bytes(ws) bytes, 256-byte aligned. Runs on
- * CUDA cores (SIMT kernels): 2 + 3 gamma launches. Asynchronous on `stream`;
- * device errors go to the workspace's status word.
+ * holds dspark_rnn_draft_scratch_bytes(ws) bytes, 256-byte aligned. Where the
+ * shape allows (bf16 weights, r a multiple of 64 up to 256, H a multiple of
+ * 64) the h projection and each step's vocabulary pass run on tcgen05, else
+ * on CUDA cores: 2 or 3 launches, then 3 per draft step. Asynchronous on
+ * `stream`; device errors go to the workspace's status word.
  */
 dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2, const void* Wr,
                                const int32_t* anchor, const float* h, const float* w, const float* T,
