@@ -302,11 +302,11 @@ size_t dspark_train_loss_scratch_bytes(const dspark_ws* ws);
  * row-major, no bias) in the workspace's weight dtype; ovec [B][gamma][r] fp32
  * receives o_k. The other arguments are those of dspark_markov_draft. Every
  * pointer is a 16-byte aligned device pointer owned by the caller; scratch
- * holds dspark_rnn_draft_scratch_bytes(ws) bytes, 256-byte aligned. Where the
- * shape allows (bf16 weights, r a multiple of 64 up to 256, H a multiple of
- * 64) the h projection and each step's vocabulary pass run on tcgen05, else
- * on CUDA cores: 2 or 3 launches, then 3 per draft step. Asynchronous on
- * `stream`; device errors go to the workspace's status word.
+ * holds dspark_rnn_draft_scratch_bytes(ws) bytes, 256-byte aligned. With
+ * bf16 weights and r a multiple of 64 up to 256, each step's vocabulary pass
+ * runs on tcgen05, and so does the h projection when H is a multiple of 64;
+ * otherwise they run on CUDA cores. 2 or 3 launches, then 3 per draft step.
+ * Asynchronous on `stream`; device errors go to the workspace's status word.
  */
 dspark_status dspark_rnn_draft(dspark_ws* ws, const float* U, const void* W1, const void* W2, const void* Wr,
                                const int32_t* anchor, const float* h, const float* w, const float* T,
