@@ -44,6 +44,10 @@ MID = {
     # partials for (256 x 8 rows): the bulk sweep runs one CTA per SM
     "mid_static_many_rows": Workload("mid_static_many_rows", B=256, gamma=7, V=2048, r=64, H=16, wdtype="bf16",
                                      mode="static", seed=16, u_std=2.0, w_std=0.05),
+    # 129 blocks a row: the dynamic sweep, whose 128-block chunks and
+    # 32-block groups then never line up with the rows
+    "mid_dyn": Workload("mid_dyn", B=24, gamma=4, V=8256, r=128, H=64, wdtype="bf16", mode="compact",
+                        seed=17, u_std=2.0, w_std=0.05, sps_knee=24.0),
 }
 
 
@@ -178,9 +182,12 @@ def test_plan_static_and_flat():
     assert (out["lengths"].cpu() == 4).all()   # flat SPS table: full verify
 
 
-def test_verify_stagewise_on_oracle_drafts():
-    """Both sides verify the oracle's drafts (rounded to fp32) under many length patterns."""
-    wl = MID["mid_ragged"].with_(B=48, seed=21)
+@pytest.mark.parametrize("V", [4104, 8192], ids=["register_sweep", "dynamic_sweep"])
+def test_verify_stagewise_on_oracle_drafts(V):
+    """Both sides verify the oracle's drafts (rounded to fp32) under many length
+    patterns: V % 64 != 0 takes the register sweep, 128 blocks a row (the
+    smallest row the dynamic sweep takes) the dynamic sweep."""
+    wl = MID["mid_ragged"].with_(B=48, V=V, seed=21)
     inp = make_inputs(wl)
     dev, npi = to_device(inp), np_inputs(inp)
     od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], 5, 9)
