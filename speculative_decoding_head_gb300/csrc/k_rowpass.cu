@@ -72,6 +72,7 @@ constexpr int kRpUStage = kRpRows * kRpBlk * 4;  // 32 KB: two 128 x 32 fp32 box
 constexpr int kRpUBox = kRpRows * 32 * 4;        // 16 KB
 constexpr int kRpAccCols = kRpTileBlocks * kRpBlk;  // 128
 constexpr int kRpNAcc = 2;                     // accumulators (and as many P buffers)
+constexpr int kRpNAccMax = 3;                  // RNN: three accumulators (o_k's hi image stays in shared memory)
 constexpr int kRpTmemCols = 512;
 constexpr int kRpMaxGroups = 64;               // n <= 8192 positions
 
@@ -91,7 +92,7 @@ struct RpSmem {
     s.bars = s.u + kRpNU * kRpUStage;
     // w2 full/empty, u full/empty, acc_u, t_full, t_empty, p_full, p_empty, a_full, drains,
     // a_cp_hi, a_cp_lo, a_ld
-    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAcc + 6);
+    s.misc = s.bars + 8 * (2 * kRpNW + 2 * kRpNU + 5 * kRpNAccMax + 6);
     // misc: TMEM address, abort word
     s.total = s.misc + 64;
     return s;
@@ -200,18 +201,20 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   auto u_empty = [&](int i) { return bars + 8u * (2 * kRpNW + kRpNU + i); };
   const uint32_t b5 = bars + 8u * (2 * kRpNW + 2 * kRpNU);
   auto acc_u = [&](int i) { return b5 + 8u * i; };                 // the accumulator holds U
-  auto t_full = [&](int i) { return b5 + 8u * (kRpNAcc + i); };    // the MMAs of the tile are done
-  auto t_empty = [&](int i) { return b5 + 8u * (2 * kRpNAcc + i); };  // the epilogue read acc and P buffer
-  auto p_full = [&](int i) { return b5 + 8u * (3 * kRpNAcc + i); };   // the P buffer holds the tile's P
-  auto p_empty = [&](int i) { return b5 + 8u * (4 * kRpNAcc + i); };  // (unused slot: keeps the layout even)
-  const uint32_t a_full = b5 + 8u * (5 * kRpNAcc);
+  auto t_full = [&](int i) { return b5 + 8u * (kRpNAccMax + i); };    // the MMAs of the tile are done
+  auto t_empty = [&](int i) { return b5 + 8u * (2 * kRpNAccMax + i); };  // the epilogue read acc and P buffer
+  auto p_full = [&](int i) { return b5 + 8u * (3 * kRpNAccMax + i); };   // the P buffer holds the tile's P
+  auto p_empty = [&](int i) { return b5 + 8u * (4 * kRpNAccMax + i); };  // (unused slot: keeps the layout even)
+  const uint32_t a_full = b5 + 8u * (5 * kRpNAccMax);
   const uint32_t drain = a_full + 8u, drain_c = a_full + 16u;
-  const uint32_t a_cp_hi = a_full + 24u, a_cp_lo = a_full + 32u;  // RNN: the A images are in TMEM
+  // RNN: o_k's lo image is in TMEM (a_cp_lo), its hi image in the A region (a_cp_hi)
+  const uint32_t a_cp_hi = a_full + 24u, a_cp_lo = a_full + 32u;
   const uint32_t a_ld = a_full + 40u;                              // RNN: an A image has landed in shared memory
   constexpr bool kLoss = MODE == kRowLoss0 || MODE == kRowLoss1;
-  // TMEM: accumulators at columns 0 and 128; then the P buffers (loss) or
-  // the A images hi and lo (RNN), r / 2 columns each
-  const uint32_t tm_hi = (uint32_t)(kRpNAcc * kRpAccCols), tm_lo = tm_hi + (uint32_t)(p.r / 2);
+  // TMEM: accumulators at columns 0 and 128, then the P buffers (loss); RNN:
+  // accumulators at 0, 128 and 256, then o_k's lo image (r / 2 columns)
+  const int NACC = MODE == kRowRnn ? kRpNAccMax : kRpNAcc;
+  const uint32_t tm_lo = (uint32_t)(NACC * kRpAccCols);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
   // [128] set 1's results per row, at the end: the A region is free once the
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       tc::mbar_init(u_full(i), 1);
       tc::mbar_init(u_empty(i), 1);
     }
-    for (int i = 0; i < kRpNAcc; ++i) {
+    for (int i = 0; i < kRpNAccMax; ++i) {
       tc::mbar_init(acc_u(i), 1);
       tc::mbar_init(t_full(i), 1);
       tc::mbar_init(t_empty(i), kRpEpi / 32);
@@ -337,15 +340,15 @@ __global__ void __launch_bounds__(kRpThreads, 1)
       int iss = 0;
       const int per_tile = MODE == kRowTree ? 0 : kLoss ? 2 : 1;
       auto copy_tile = [&](int tj) {
-        const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
-        bool okt = tc::mbar_wait(t_empty(ab), ((tj / kRpNAcc) & 1) ^ 1, abort);  // accumulator and P buffer free
+        const int nbt = tile_blocks(tj), ab = tj % NACC;
+        bool okt = tc::mbar_wait(t_empty(ab), ((tj / NACC) & 1) ^ 1, abort);  // accumulator and P buffer free
         if (okt && per_tile == 0) tc::mma_commit(acc_u(ab));  // PCTree: the MMAs start from zero
         for (int e = 0; e < per_tile * nbt && okt; ++e) {
           const int j = e % nbt, us = iss % kRpNU;
           okt = tc::mbar_wait(u_full(us), (iss / kRpNU) & 1, abort);
           if (!okt) break;
           tc::tc_fence_after();
-          const uint32_t d = tmem + (uint32_t)((e < nbt ? 0 : kRpNAcc * kRpAccCols) + ab * kRpAccCols + j * kRpBlk);
+          const uint32_t d = tmem + (uint32_t)((e < nbt ? 0 : NACC * kRpAccCols) + ab * kRpAccCols + j * kRpBlk);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -360,39 +363,42 @@ __global__ void __launch_bounds__(kRpThreads, 1)
         return okt;
       };
       if constexpr (MODE == kRowRnn) {
-        // o_k's hi image, then its lo image, written by the cell in the
-        // operand's layout: each comes into the A region by one bulk copy and
-        // goes to its TMEM columns (16 bf16 of K per 8 columns). The first
-        // tiles' U goes into the accumulators while the hi image is in flight.
+        // o_k's images, written by the cell in the operand's layout, each
+        // come into the A region by one bulk copy: the lo image first, which
+        // goes on to its TMEM columns (16 bf16 of K per 8 columns), then the
+        // hi image, which stays there as the MMAs' shared-memory A operand
+        // (a_cp_hi completes when it has landed). The first tiles' U goes
+        // into the accumulators while the lo image is in flight.
         pdl_wait();  // the images are the cell's
         const uint32_t abytes = (uint32_t)(kRpRows * p.r * 2);
-        const __nv_bfloat16* img = p.oimg + (size_t)grp * 2 * kRpRows * p.r;
-        int lds = 0;  // image loads issued
+        const __nv_bfloat16* img = p.oimg + (size_t)grp * 2 * kRpRows * p.r;  // [hi | lo]
+        bool hi_issued = false;
         tc::mbar_arrive_expect_tx(a_ld, abytes);
-        tc::bulk_load(sA, img, abytes, a_ld);
-        ++lds;
+        tc::bulk_load(sA, img + (size_t)kRpRows * p.r, abytes, a_ld);
         const int pre = min(ntl, kRpNAcc);
         for (int tj = 0; tj < pre && ok; ++tj) ok = copy_tile(tj);
-        for (int im = 0; im < 2 && ok; ++im) {
-          ok = tc::mbar_wait(a_ld, im, abort);
-          if (!ok) break;
+        if (ok) ok = tc::mbar_wait(a_ld, 0, abort);
+        if (ok) {
           for (int ks = 0; ks < p.r / 16; ++ks)
-            tc::cp_128x256b(tmem + (im ? tm_lo : tm_hi) + (uint32_t)(ks * 8),
+            tc::cp_128x256b(tmem + tm_lo + (uint32_t)(ks * 8),
                             tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024));
-          tc::mma_commit(im ? a_cp_lo : a_cp_hi);
-          if (im == 0) {  // the lo image takes the region once the copies have read the hi image
-            ok = tc::mbar_wait(a_cp_hi, 0, abort);
-            if (!ok) break;
-            tc::mbar_arrive_expect_tx(a_ld, abytes);
-            tc::bulk_load(sA, img + (size_t)kRpRows * p.r, abytes, a_ld);
-            ++lds;
-          }
+          tc::mma_commit(a_cp_lo);
+          ok = tc::mbar_wait(a_cp_lo, 0, abort);  // the copies have read the lo image: the region takes hi
+        }
+        if (ok) {
+          tc::mbar_arrive_expect_tx(a_cp_hi, abytes);
+          tc::bulk_load(sA, img, abytes, a_cp_hi);
+          hi_issued = true;
         }
         if (!ok) {  // an image copy still in flight lands before the CTA ends
           volatile int never = 0;
-          tc::mbar_wait(a_ld, lds - 1, &never);
+          tc::mbar_wait(a_ld, 0, &never);
         }
         for (int tj = pre; tj < ntl && ok; ++tj) ok = copy_tile(tj);
+        if (hi_issued) {  // the hi image has landed before the CTA ends (at once unless a wait gave up)
+          volatile int never = 0;
+          tc::mbar_wait(a_cp_hi, 0, &never);
+        }
       } else {
         for (int tj = 0; tj < ntl && ok; ++tj) ok = copy_tile(tj);
       }
@@ -411,10 +417,10 @@ __global__ void __launch_bounds__(kRpThreads, 1)
                                 : tc::mbar_wait(a_full, 0, abort);
       if (ok) tc::tc_fence_after();
       for (int tj = 0; tj < ntl && ok; ++tj) {
-        const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
+        const int nbt = tile_blocks(tj), ab = tj % NACC;
         const uint32_t idesc = tc::idesc_bf16_f32(kRpRows, nbt * kRpBlk, true);
         const uint32_t d = tmem + (uint32_t)(ab * kRpAccCols);
-        ok = tc::mbar_wait(acc_u(ab), (tj / kRpNAcc) & 1, abort);
+        ok = tc::mbar_wait(acc_u(ab), (tj / NACC) & 1, abort);
         if (ok) tc::tc_fence_after();
         for (int ch = 0; ch < nkc && ok; ++ch) {
           const int wc = tj * nkc + ch, ws = wc % kRpNW;
@@ -424,8 +430,9 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           for (int kk = 0; kk < kRpKc / 16; ++kk) {
             const int ks = ch * (kRpKc / 16) + kk;
             const uint64_t bd = tc::smem_desc(sW2 + ws * kRpW2Stage + kk * 2048, kRpW2Box, 1024);
-            if constexpr (MODE == kRowRnn) {  // o_k hi, then lo, against the same W2 rows
-              tc::mma_bf16_ta(d, tmem + tm_hi + (uint32_t)(ks * 8), bd, idesc, 1u);
+            if constexpr (MODE == kRowRnn) {  // o_k hi (shared memory), then lo (TMEM), against the same W2 rows
+              const uint64_t ah = tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024);
+              tc::mma_bf16(d, ah, bd, idesc, 1u);
               tc::mma_bf16_ta(d, tmem + tm_lo + (uint32_t)(ks * 8), bd, idesc, 1u);
             } else {
               const uint64_t ad = tc::smem_desc(sA + (ks >> 2) * (kRpRows * 128) + (ks & 3) * 32, 16, 1024);
@@ -520,11 +527,11 @@ __global__ void __launch_bounds__(kRpThreads, 1)
     float Md = -INFINITY, Sd = 0.f, Mt = -INFINITY, St = 0.f, zxv = 0.f, l1 = 0.f;
     bool have_zx = false;
     for (int tj = 0; tj < ntl && !aborted(); ++tj) {
-      const int nbt = tile_blocks(tj), ab = tj % kRpNAcc;
+      const int nbt = tile_blocks(tj), ab = tj % NACC;
       const int gb0 = tj * kRpTileBlocks;
       const int j0 = (set - gb0 % kRpSets + kRpSets) % kRpSets;
-      bool ok = tc::mbar_wait(t_full(ab), (tj / kRpNAcc) & 1, abort) &&
-                (!kLoss || tc::mbar_wait(p_full(ab), (tj / kRpNAcc) & 1, abort));
+      bool ok = tc::mbar_wait(t_full(ab), (tj / NACC) & 1, abort) &&
+                (!kLoss || tc::mbar_wait(p_full(ab), (tj / NACC) & 1, abort));
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
         if (lane == 0 && !*abort) {
@@ -585,7 +592,7 @@ __global__ void __launch_bounds__(kRpThreads, 1)
           const int v0 = t * kRpBlk + hh * 32;
           float z[32], y[32];
           tc::tmem_ld32(tmem + lanes + (uint32_t)(ab * kRpAccCols + j * kRpBlk + hh * 32), z);
-          tc::tmem_ld32(tmem + lanes + (uint32_t)(kRpNAcc * kRpAccCols + ab * kRpAccCols + j * kRpBlk + hh * 32), y);
+          tc::tmem_ld32(tmem + lanes + (uint32_t)(NACC * kRpAccCols + ab * kRpAccCols + j * kRpBlk + hh * 32), y);
           tc::tmem_wait_ld();
           if (!valid) continue;
           if (v0 + 32 > p.V) {
