@@ -72,7 +72,7 @@ constexpr int kRpUStage = kRpRows * kRpBlk * 4;  // 32 KB: two 128 x 32 fp32 box
 constexpr int kRpUBox = kRpRows * 32 * 4;        // 16 KB
 constexpr int kRpAccCols = kRpTileBlocks * kRpBlk;  // 128
 constexpr int kRpNAcc = 2;                     // accumulators (and as many P buffers)
-constexpr int kRpNAccMax = 3;                  // RNN: three accumulators (o_k's hi image stays in shared memory)
+constexpr int kRpNAccMax = 4;                  // RNN: three accumulators (o_k's hi image stays in shared memory); PCTree: four
 constexpr int kRpTmemCols = 512;
 constexpr int kRpMaxGroups = 64;               // n <= 8192 positions
 
@@ -212,8 +212,9 @@ __global__ void __launch_bounds__(kRpThreads, 1)
   const uint32_t a_ld = a_full + 40u;                              // RNN: an A image has landed in shared memory
   constexpr bool kLoss = MODE == kRowLoss0 || MODE == kRowLoss1;
   // TMEM: accumulators at columns 0 and 128, then the P buffers (loss); RNN:
-  // accumulators at 0, 128 and 256, then o_k's lo image (r / 2 columns)
-  const int NACC = MODE == kRowRnn ? kRpNAccMax : kRpNAcc;
+  // accumulators at 0, 128 and 256, then o_k's lo image (r / 2 columns);
+  // PCTree (no P, A in shared memory): four accumulators
+  const int NACC = MODE == kRowRnn ? 3 : MODE == kRowTree ? 4 : kRpNAcc;
   const uint32_t tm_lo = (uint32_t)(NACC * kRpAccCols);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L.misc + 16);
