@@ -206,7 +206,9 @@ dspark_status dspark_verify(dspark_ws* ws, const float* P, const int32_t* row_of
 /*
  * A whole round: draft, plan, then verify on P, which the caller has packed
  * for the lengths this round produces (benchmark use: with fixed inputs and
- * round the lengths are deterministic). Same arguments as the three calls.
+ * round the lengths are deterministic), so P holds at least B rows (every
+ * request verifies at least one); the verify may start reading those first B
+ * rows before the planner has finished. Same arguments as the three calls.
  */
 dspark_status dspark_round(dspark_ws* ws, const float* U, const void* W1, const void* W2,
                            const int32_t* anchor, const float* h, const float* w, const float* T,
