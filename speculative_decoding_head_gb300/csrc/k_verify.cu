@@ -16,16 +16,20 @@
 // Every draw is the library's two-level Gumbel-max (64-token blocks).
 //
 // Kernels (all launched with grids that do not depend on device-side sizes):
-//   k_verify_sweep     the verified rows split into equal contiguous ranges of
-//                      64-token blocks, one per CTA: online log-sum-exp of P;
-//                      for the last verified row of a request also the block
-//                      draw of the bonus token.
-//   k_verify_finalize  one warp per request, one lane per row: accept tests,
-//                      first rejection, bonus token draw inside its block
-//                      (after the bulk sweep, the same work runs in the sweep
-//                      CTA that completes the request's partials).
-//   k_resid_blocks     grid (chunks, B): residual block masses and block draw.
-//   k_resid_pick       grid (B): residual token draw inside the drawn block.
+//   k_verify_sweep_dyn  V % 64 == 0 and at least 128 blocks a row: the packed
+//                       rows' blocks in 32 KB chunks taken from a counter;
+//                       per block its log-sum-exp, per 32 blocks each row's
+//                       (max, sum).
+//   k_verify_fin_dyn    after it, one CTA per request: the accept tests, the
+//                       first rejection, the bonus block and token draws.
+//   k_verify_sweep_bulk V % 64 == 0 and fewer blocks: equal contiguous ranges
+//                       of blocks, one per CTA, with the finalize of each
+//                       request in the CTA that completes its partials.
+//   k_verify_sweep      otherwise: equal ranges, then k_verify_finalize (one
+//                       warp per request, one lane per row).
+//   k_resid_blocks      grid (chunks, B): residual block masses and block draw
+//                       on CUDA cores (k_resid_tc.cu: the tcgen05 version).
+//   k_resid_pick        grid (B): residual token draw inside the drawn block.
 #include "dspark_common.cuh"
 #include "dspark_internal.h"
 #include "tc_ptx.cuh"
