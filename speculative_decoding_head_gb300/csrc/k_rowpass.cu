@@ -20,8 +20,9 @@
 //               blocks into a P buffer in tensor memory (tcgen05.cp), so an
 //               epilogue thread reads z_d and z_t of its row from TMEM;
 //   warp 1      allocates all 512 TMEM columns (two 128-column accumulators,
-//               two 128-column P buffers) and issues tcgen05.mma (M = 128,
-//               N = 128, K = r) onto the accumulator that holds U: z_d;
+//               two 128-column P buffers; see below for the other modes) and
+//               issues tcgen05.mma (M = 128, N = 128, K = r) onto the
+//               accumulator that holds U: z_d;
 //   warps 2-9   epilogue, two sets of four warps (blocks of even and odd
 //               index), one thread per row: pass 0 keeps a running
 //               (max, sum 2^(y - max)) of z_d and of z_t and picks z_d at x*;
@@ -33,16 +34,22 @@
 //
 // The same pass with requests as rows serves two more computations:
 //   - one draft step of the RNN head (eq. (6), same reading §4.2): rows are
-//     requests, A = o_k split into bf16 hi and lo, both images copied into
-//     tensor memory (they do not fit beside the rings in shared memory) and
-//     both MMAs accumulate into the tile (A read from TMEM); U_k arrives by
-//     a 3-D box; per row and 64-token block the log-mass log sum exp z goes
-//     to blk [B][nblk] for the pick;
+//     requests, A = o_k split into bf16 hi and lo images, which the cell
+//     wrote in this operand's layout: the copier brings the lo image in by
+//     one bulk copy and moves it to TMEM, then the hi image, which stays in
+//     the A region as the shared-memory operand; per K step both MMAs
+//     accumulate into the tile (hi from shared memory, lo from TMEM), and
+//     TMEM holds three accumulators beside the lo image; U_k arrives by a 3-D
+//     box; per row and 64-token block the log-mass log sum exp z goes to blk
+//     [B][nblk] for the pick;
 //   - one PCTree expansion (zdszero "spec_dspark", section "后续工作"): rows
 //     are requests, A = W1[token of the node being expanded], and U of the
 //     node's depth differs per row, so the epilogue adds it from global
-//     memory (the accumulator starts at zero); per block the log-mass and
-//     the maximum of z.
+//     memory (the accumulator starts at zero); four accumulators (no P
+//     buffers); per block the log-mass and the maximum of z.
+// The RNN and PCTree launches are dependent launches (programmatic stream
+// serialization): only the epilogue (and, for RNN, the copier's image loads)
+// waits for the kernel before, so the W2 and U streams start meanwhile.
 // Every wait is bounded; a timeout sets DSPARK_ETIMEOUT and every role ends.
 #include <cudaTypedefs.h>
 #include <string.h>
