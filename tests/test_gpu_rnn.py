@@ -71,6 +71,9 @@ def _wl(name, B, gamma, V, r, H, wdtype="bf16", seed=41):
     # last 128-row tile
     _wl("rnn_tc_r128", 12, 3, 4104, 128, 128),
     _wl("rnn_tc_r64", 9, 4, 2048, 64, 192),
+    # two row groups in the row pass (o_k's images per group of 128
+    # requests; the second group's rows past B stay zero)
+    _wl("rnn_two_groups", 160, 3, 8192, 64, 64),
 ], ids=lambda w: w.name)
 def test_rnn_draft_parity(wl):
     _run(wl, rnd=1)
