@@ -588,10 +588,14 @@ __global__ void __launch_bounds__(kBulkThreads)
     if (lane == 0) {
       const int b = ri.x;
       const long long r0 = min(max(row_off[b], 0), R), r1 = min(max((long long)row_off[b] + lengths[b], r0), (long long)R);
+      // the CTA ranges [c T / G, (c + 1) T / G) that cover the request's
+      // units: with T >= G every range holds at least one unit, so they are
+      // the owners of its first through its last unit; with T < G a range
+      // holds at most one, so there is one per unit
       int ncov = 0;  // 0 (never finalized here) when the request has no rows; CTA 0 reports it
       if (r1 > r0)
-        for (int cc = unit_owner(r0 * nblk, T, G); cc <= unit_owner(r1 * nblk - 1, T, G); ++cc)
-          ncov += unit_lo(cc, T, G) < unit_lo(cc + 1, T, G) ? 1 : 0;
+        ncov = T >= G ? unit_owner(r1 * nblk - 1, T, G) - unit_owner(r0 * nblk, T, G) + 1
+                      : (int)((r1 - r0) * nblk);
       last = atomicAdd(vdone + b, 1) == ncov - 1;
       if (last) {
         __threadfence();
