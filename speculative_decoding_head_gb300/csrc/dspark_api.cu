@@ -80,10 +80,17 @@ dspark_status dspark_ws_create(const dspark_dims* dims, dspark_ws** out) {
   // rows). Two CTAs per SM (a 96 KB ring each) while that is at most 8 rows;
   // else one CTA per SM with up to 32 rows; beyond, the register sweep.
   const int Rmax = d.B * (d.gamma + 1);
+  // no more CTAs than ranges of 32 blocks of the row capacity (a small round
+  // would leave most CTAs idle, and every working CTA counts itself in for
+  // each request it touches), nor so few that a range spans more than 6 rows
+  const long long units_max = (long long)Rmax * geo.nblk;
+  auto capped = [&](int grid) {
+    return (int)std::min<long long>(grid, std::max<long long>((units_max + 31) / 32, (Rmax + 5) / 6));
+  };
   if (geo.sweep_bulk && (Rmax + 2 * geo.num_sms - 1) / (2 * geo.num_sms) + 2 <= 8) {
-    geo.sweep_grid = 2 * geo.num_sms;
+    geo.sweep_grid = capped(2 * geo.num_sms);
   } else if (geo.sweep_bulk && (Rmax + geo.num_sms - 1) / geo.num_sms + 2 <= sweep_bulk_max_slots()) {
-    geo.sweep_grid = geo.num_sms;
+    geo.sweep_grid = capped(geo.num_sms);
   } else {
     geo.sweep_bulk = 0;
     geo.sweep_grid = 4 * geo.num_sms;
