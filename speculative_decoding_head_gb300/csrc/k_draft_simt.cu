@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kSimtThreads)
                    const float* __restrict__ ovec, int g, int V, int r, int k, int nblk, float* __restrict__ blk,
                    int* __restrict__ status) {
   extern __shared__ float e[];  // W1[x_{k-1}] (Markov head) or o_k (RNN head) as fp32, [r]
+  pdl_wait();  // the previous step's pick (launched as a dependent kernel)
   const int b = blockIdx.y;
   const int x = prev_token(anchor, tokens, b, g, k);
   if (x < 0 || x >= V) {
@@ -269,12 +270,14 @@ static cudaError_t draft_simt_impl(const dspark_ws* ws, const DraftArgs& a, cuda
                                 : launch_rnn_blocks_tc(ws, a.U, a.W2, ovec, k, st);
       if (e != cudaSuccess) return e;
     } else {
-      k_draft_blocks<BF16><<<dim3(chunks, d.B), kSimtThreads, smem, st>>>(
-          a.U, a.W1, a.W2, a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+      const cudaError_t e =
+          launch_ex(k_draft_blocks<BF16>, dim3(chunks, d.B), dim3(kSimtThreads), smem, st, true, a.U, a.W1, a.W2,
+                    a.anchor, a.tokens, ovec, d.gamma, d.V, d.r, k, nblk, ws->s.blk, ws->s.status);
+      if (e != cudaSuccess) return e;
     }
-    // the RNN head's steps are chained by programmatic dependent launch (the
-    // cell and the pick wait in-kernel); the Markov SIMT steps launch plainly
-    const cudaError_t e = launch_ex(k_draft_pick<BF16>, dim3(d.B), dim3(kPickThreadsS), smem, st, rnn != nullptr,
+    // the steps are chained by programmatic dependent launch (the block
+    // pass, the cell and the pick wait in-kernel for the kernel before)
+    const cudaError_t e = launch_ex(k_draft_pick<BF16>, dim3(d.B), dim3(kPickThreadsS), smem, st, true,
                                     a.U, a.W1, a.W2, a.anchor, a.w, a.T, ws->s.s_h, ovec, d.gamma, d.V, d.r, d.H, k,
                                     nblk, ws->s.blk, rng, a.tokens, a.pd_tok, a.lse, a.conf, ws->s.status);
     if (e != cudaSuccess) return e;
