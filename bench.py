@@ -35,7 +35,8 @@ METRIC = "DSpark draft+verify rounds/s at B=128, γ=5, V=129280; % of HBM roofli
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one k_draft_tc
 # launch on the prod workload, from one ncu capture of this bench (caches
 # flushed before the launch), and a hash of the kernel source it was taken on;
-# the roofline's "traffic" is reported only while the source is unchanged.
+# the roofline's "traffic" is reported only for that kernel on that workload
+# and only while the source is unchanged.
 DRAFT_TRAFFIC = {"sha256": "cda2fba98bf2ff4af1606f0ec018edde7e2f4e9f0bb70c88c639c56f6d5e4d7c",
                  "bytes": 414144512 + 115712}
 QUOTED_HBM_GBS = 8000.0   # GB/s, the roofline constant the metric is quoted against
@@ -784,7 +785,8 @@ def main():
     draft_gbs = draft_bytes / (st["draft"] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": f"draft stage ({ws.path})", "achieved": draft_gbs,
                 "peak": peak, "unit": "GB/s", "frac": draft_gbs / peak, "peak_kind": peak_kind,
-                "traffic": draft_traffic(), "alg_bytes_per_launch": draft_bytes,
+                "traffic": draft_traffic() if (args.workload == "prod" and ws.path == "tcgen05") else None,
+                "alg_bytes_per_launch": draft_bytes,
                 "launch_ms": st["draft"]}
 
     # end to end through the same C-ABI with host buffers: H2D of the round's
