@@ -508,14 +508,17 @@ def rnn_timing(peak_gbs: float, reps: int = 10, batch=None, cpu_budget_s: float 
     """The draft tail with the RNN head on the prod shape: device time per
     call, CUDA events on the launching stream after warm-up, inputs resident.
     The algorithmic bytes are the Markov draft's (U once, W2 once per step,
-    h once) plus the three gate matrices once."""
+    h once) plus the three gate matrices once. Then the RNN head's verify
+    (`dspark_verify_rnn`) of those drafts on the planner's lengths for their
+    confidences, timed the same way; its algorithmic bytes are the verified
+    rows of P."""
     import torch
     from speculative_decoding_head_gb300.binding import Workspace
-    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_rnn_weights
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs, make_rnn_weights, pack_rows
     wl = WORKLOADS["prod"] if batch is None else WORKLOADS["prod"].with_(B=batch)
-    inp_cpu = make_inputs(wl, with_target=False)
+    inp_cpu = make_inputs(wl)  # with the target's logits, for the verify
     Wr_cpu = make_rnn_weights(wl)
-    inp = {k: v.cuda() for k, v in inp_cpu.items()}
+    inp = {k: v.cuda() for k, v in inp_cpu.items() if k != "P_full"}
     Wr = Wr_cpu.cuda()
     ws = Workspace.for_workload(wl)
     out = None
@@ -537,11 +540,73 @@ def rnn_timing(peak_gbs: float, reps: int = 10, batch=None, cpu_budget_s: float 
     B, g, V, r, H = wl.B, wl.gamma, wl.V, wl.r, wl.H
     alg = B * g * V * 4 + g * r * V * 2 + B * g * H * 4 + 3 * r * (2 * r + H) * 2
     gbs = alg / (ms * 1e-3) / 1e9
+    launches = ws.last_launches
+    verify = rnn_verify_timing(ws, wl, inp, inp_cpu, Wr, peak_gbs, reps, cpu_budget_s)
     return {"workload": "prod" if batch is None else f"prod with B={batch}", "B": B, "gamma": g, "V": V, "r": r,
             "H": H, "ms_per_call": ms,
             "drafted_tokens_per_s": B * g / (ms * 1e-3), "alg_bytes": alg, "achieved_gbs": gbs,
-            "frac_of_measured_hbm": gbs / peak_gbs, "launches": ws.last_launches, "graph": graphed,
-            "path": "tcgen05 block pass", "cpu_baseline": oracle_rnn_sample(wl, inp_cpu, Wr_cpu, cpu_budget_s)}
+            "frac_of_measured_hbm": gbs / peak_gbs, "launches": launches, "graph": graphed,
+            "path": "tcgen05 block pass", "cpu_baseline": oracle_rnn_sample(wl, inp_cpu, Wr_cpu, cpu_budget_s),
+            "verify": verify}
+
+
+def rnn_verify_timing(ws, wl, inp, inp_cpu, Wr, peak_gbs: float, reps: int, cpu_budget_s: float):
+    """The RNN head's verify on the prod shape: one draft (round 0), the
+    planner on its confidences, P packed for those lengths, then
+    `dspark_verify_rnn` captured in a CUDA graph and timed with CUDA events;
+    the oracle's verify of the same drafts (with the same head vectors) on a
+    bounded sample of requests beside it."""
+    import torch
+    from speculative_decoding_head_gb300.workloads import pack_rows
+    d = ws.rnn_draft(inp["U"], inp["W1"], inp["W2"], Wr, inp["anchor"], inp["h"], inp["w"], inp["T"], 1, 0)
+    p = ws.plan(d["conf"], inp["sps"])
+    torch.cuda.synchronize()
+    lengths = p["lengths"].clone()
+    P = pack_rows(inp_cpu["P_full"], lengths).contiguous()
+    Pd = P.cuda()
+    args = (Pd, p["row_off"], lengths, inp["anchor"], d["tokens"], d["pd_tok"], d["lse"], inp["U"], d["ovec"],
+            inp["W2"], 1, 0)
+    vout = ws.verify_rnn(*args)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    launches = ws.last_launches
+    call, graphed = _graphed(lambda: ws.verify_rnn(*args, out=vout))
+    call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    sum_len = int(lengths.sum().item())
+    alg = sum_len * wl.V * 4
+    gbs = alg / (ms * 1e-3) / 1e9
+    cpu = None
+    if cpu_budget_s > 0:
+        import numpy as np
+        import oracle
+        oracle.set_threads(os.cpu_count() or 1)
+        cores = oracle.get_threads()
+        npi = _np_inputs({k: v for k, v in inp_cpu.items() if k != "P_full"})
+        L = lengths.cpu().numpy().astype(np.int32)
+        ro = np.zeros(wl.B + 1, np.int32)
+        ro[1:] = np.cumsum(L)
+        Pn, tok, ov = P.numpy(), d["tokens"].cpu().numpy(), d["ovec"].cpu().numpy()
+        n = max(1, min(cores, wl.B))
+        done, spent = 0, 0.0
+        while spent < cpu_budget_s and done < wl.B:
+            reqs = [(done + i) % wl.B for i in range(n)]
+            t0 = time.perf_counter()
+            oracle.verify(Pn, ro, L, npi["anchor"], tok, npi["U"], npi["W1"], npi["W2"], 1, 0, reqs=reqs, ovec=ov)
+            spent += time.perf_counter() - t0
+            done += n
+        per_call = spent / done * wl.B
+        cpu = {"value": 1.0 / per_call, "unit": "calls/s", "cores": cores, "kind": "oracle",
+               "sample": f"oracle RNN-head verify of {done} of the {wl.B} requests: {spent:.1f} s on {cores} "
+                         f"threads, scaled to a {wl.B}-request call"}
+    return {"ms_per_call": ms, "verified_rows": sum_len, "alg_bytes": alg, "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / peak_gbs, "launches": launches, "graph": graphed, "cpu_baseline": cpu}
 
 
 def pctree_timing(peak_gbs: float, reps: int = 10, c: int = 4, N: int = 16, cpu_budget_s: float = 3.0):
