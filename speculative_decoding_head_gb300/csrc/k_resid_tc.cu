@@ -36,7 +36,11 @@
 //   - one draft step of the RNN head (eq. (6), same reading §4.2),
 //     kModeDraft: z = U_k + o_k W2 with o_k split into bf16 hi and lo
 //     operands that both accumulate into the tile, and the log-mass of every
-//     64-token block for the SIMT pick.
+//     64-token block for the SIMT pick;
+//   - the residual block draw of a round drafted by the RNN head,
+//     kModeResidRnn: kModeResid with p_d from U + o_{n+1} W2, the head vector
+//     of the rejected position as the hi and lo operands of kModeDraft (its
+//     U/P ring is two tiles deep so that both operands fit beside it).
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -72,16 +76,23 @@ constexpr int kModeDraft = 3;      // per column (request) and 64-token block: l
                                    // of the RNN head, z = U_k + o_k W2 with o_k split into bf16 hi + lo parts
 constexpr int kModeTree = 4;       // per column (request) and 64-token block: log sum exp z and max z of the
                                    // expansion of a PCTree node, z = U[b, depth] + W1[token] W2
+constexpr int kModeResidRnn = 5;   // kModeResid with the RNN head's o_{n+1} (hi + lo) in place of W1[x_n]
+
+// the residual block draw (either head); B as bf16 hi + lo parts of an fp32
+// vector; U/P ring depth
+__host__ __device__ constexpr bool mode_resid(int m) { return m == kModeResid || m == kModeResidRnn; }
+__host__ __device__ constexpr bool mode_hilo(int m) { return m == kModeDraft || m == kModeResidRnn; }
+__host__ __device__ constexpr int mode_up(int m) { return m == kModeResidRnn ? 2 : kRUP; }
 
 struct RSmem {
   uint32_t bop, w2, up, stage, col, part, best, gum, list, bars, misc, total;
-  __host__ __device__ static RSmem make(int r, bool draft) {
+  __host__ __device__ static RSmem make(int r, int mode) {
     RSmem s;
-    s.bop = 0;                              // [32 columns x r] bf16, K-major swizzled (draft: hi, then lo)
-    s.w2 = s.bop + (draft ? 2 : 1) * kRN * r * 2;  // kRNW x (two boxes of [r/2 x 64] bf16: one K-half of a tile)
-    s.up = s.w2 + kRNW * r * 128;           // kRUP x [request][U slice | P slice] fp32 (draft: U rows only)
-    s.stage = draft ? kRN * kRM * 4 : kRUPStage;
-    s.col = s.up + kRUP * s.stage;          // per-request: b, n, row, x (int), lse_d, lse_t (float)
+    s.bop = 0;                              // [32 columns x r] bf16, K-major swizzled (hi + lo modes: hi, then lo)
+    s.w2 = s.bop + (mode_hilo(mode) ? 2 : 1) * kRN * r * 2;  // kRNW x (two boxes of [r/2 x 64] bf16: a K-half)
+    s.up = s.w2 + kRNW * r * 128;           // mode_up x [request][U slice | P slice] fp32 (draft: U rows only)
+    s.stage = mode == kModeDraft ? kRN * kRM * 4 : kRUPStage;
+    s.col = s.up + mode_up(mode) * s.stage;  // per-request: b, n, row, x (int), lse_d, lse_t (float)
     s.part = s.col + 6 * 4 * kRN;           // [4 quarters][32 columns] partials (float4 for the loss statistics)
     s.best = s.part + 4 * 16 * kRN;         // [128] best key, [128] best block
     s.gum = s.best + 2 * 4 * kRN;           // [kRN][kRGMax] block Gumbels of this CTA's blocks
@@ -209,7 +220,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const RSmem L = RSmem::make(p.r, MODE == kModeDraft);
+  constexpr bool kRes = mode_resid(MODE);
+  constexpr int kUP = mode_up(MODE);
+  const RSmem L = RSmem::make(p.r, MODE);
   const uint32_t sbase = tc::smem_u32(smem);
   const uint32_t sB = sbase + L.bop, sW2 = sbase + L.w2;
   int* col_b = reinterpret_cast<int*>(smem + L.col);
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int nt = tile_hi - tile_lo;
   // The loss modes walk the CTA's tiles forwards in even groups and backwards
   // in odd ones, so the W2 tiles used last are the first reused (from L2).
-  auto tile_of = [&](int gq, int i) { return tile_lo + ((MODE != kModeResid && (gq & 1)) ? nt - 1 - i : i); };
+  auto tile_of = [&](int gq, int i) { return tile_lo + ((!kRes && (gq & 1)) ? nt - 1 - i : i); };
   const uint32_t box_bytes = (uint32_t)p.r * 64u;  // one [r/2 x 64] bf16 box
   const uint32_t w2_bytes = 2u * box_bytes;         // one K-half of a tile
 
@@ -259,14 +272,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     tc::mbar_init(a_full, kREpi);
     tc::mbar_init(drain, 1);
-    for (int i = 0; i < kRUP; ++i) {
+    for (int i = 0; i < kUP; ++i) {
       tc::mbar_init(up_full(i), 1);
       tc::mbar_init(up_empty(i), kREpi);  // every epilogue warp reads the stage
     }
     *abort = 0;
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tm_w2);
-    if constexpr (MODE != kModeResid) {
+    if constexpr (!kRes) {
       tc::prefetch_tmap(&tm_u);
       tc::prefetch_tmap(&tm_p);
     }
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // left the status clear: an error leaves the list empty.
   pdl_wait();  // the verify flags are the sweep's
   if (warp == 2) {
-    if constexpr (MODE == kModeResid) {
+    if constexpr (kRes) {
       const bool clear = __shfl_sync(0xFFFFFFFFu, *(volatile int*)p.status, 0) == 0;
       int base = 0;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -366,7 +379,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       const float* urow = p.U;
       const float* prow = p.P;
       if (lane < ncols) {
-        if constexpr (MODE == kModeResid) {
+        if constexpr (kRes) {
           const int b = list[gq * kRN + lane];
           urow = p.U + ((size_t)b * p.g + min(max(p.n_acc[b], 0), p.g - 1)) * p.V;
           prow = p.P + (size_t)min(max(p.vrow[b], 0), p.B * (p.g + 1) - 1) * p.V;
@@ -381,13 +394,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
       }
       for (int i = 0; i < nt && ok; ++i) {
-        const int it = gq * nt + i, us = it % kRUP, v0 = tile_of(gq, i) * kRM;
+        const int it = gq * nt + i, us = it % kUP, v0 = tile_of(gq, i) * kRM;
         const uint32_t bytes = (uint32_t)min(kRM, p.V - v0) * 4u;  // a multiple of 32 (V % 8 == 0)
         int got = 1;
-        if (lane == 0) got = tc::mbar_wait(up_empty(us), ((it / kRUP) & 1) ^ 1, abort) ? 1 : 0;
+        if (lane == 0) got = tc::mbar_wait(up_empty(us), ((it / kUP) & 1) ^ 1, abort) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
         if (!ok) break;
-        if constexpr (MODE == kModeResid) {
+        if constexpr (kRes) {
           if (lane == 0) tc::mbar_arrive_expect_tx(up_full(us), 2u * bytes * (uint32_t)ncols);
           __syncwarp();
           if (lane < ncols) {
@@ -419,8 +432,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
       if (!*abort) raise_status(p.status, DSPARK_ETIMEOUT);
       *abort = 1;
       volatile int never = 0;  // let the copies already issued land before the CTA can exit
-      for (int it = issued - 1; it >= 0 && it >= issued - kRUP; --it)
-        tc::mbar_wait(up_full(it % kRUP), (it / kRUP) & 1, &never);
+      for (int it = issued - 1; it >= 0 && it >= issued - kUP; --it)
+        tc::mbar_wait(up_full(it % kUP), (it / kUP) & 1, &never);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -449,7 +462,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
               const uint64_t ad = tc::smem_desc(astage + kh * 2048, box_bytes, 1024);
               const uint32_t boff = (ks >> 2) * (kRN * 128) + (ks & 3) * 32;
               tc::mma_bf16(d, ad, tc::smem_desc(sB + boff, 16, 1024), idesc, ks > 0 ? 1u : 0u);
-              if constexpr (MODE == kModeDraft)  // the lo part of o_k against the same W2 rows
+              if constexpr (mode_hilo(MODE))  // the lo part of o_k against the same W2 rows
                 tc::mma_bf16(d, ad, tc::smem_desc(sB + kRN * p.r * 2 + boff, 16, 1024), idesc, 1u);
             }
             tc::mma_commit(w2_empty(ws));
@@ -483,10 +496,13 @@ __global__ void __launch_bounds__(kRThreads, 1)
         int x = 0;
         const bool valid = et < kRN && i < nrej;
         if (valid) {
-          if constexpr (MODE == kModeResid) {
+          if constexpr (kRes) {
             const int b = list[i];
             const int n = min(max(p.n_acc[b], 0), p.g - 1);  // a rejection leaves n <= gamma - 1
-            x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
+            if constexpr (MODE == kModeResid)
+              x = n == 0 ? p.anchor[b] : p.tokens[(size_t)b * p.g + (n - 1)];
+            else
+              x = b * p.g + n;  // the row of o_{n+1}, the head vector of draft position n + 1
             col_b[et] = b;
             col_n[et] = n;
             col_row[et] = p.vrow[b];
@@ -515,7 +531,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
               col_nlt[et] = -p.lse_t[i] * tc::kLog2e;
             }
           }
-          if (MODE != kModeDraft && (x < 0 || x >= p.V)) {
+          if (!mode_hilo(MODE) && (x < 0 || x >= p.V)) {
             raise_status(p.status, DSPARK_ERANGE);
             x = 0;
           }
@@ -532,7 +548,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
         // epilogue thread loads up to kRGather 16-byte chunks (consecutive
         // threads take consecutive chunks of a row), all in flight at once
         const int cpr = p.r / 8;  // 16-byte chunks per row
-        if constexpr (MODE == kModeDraft) {
+        if constexpr (mode_hilo(MODE)) {
           // o_k rows in fp32 -> hi = bf16(o), lo = bf16(o - hi), eight values per chunk
           float4 f[kRGather][2];
 #pragma unroll
@@ -542,8 +558,9 @@ __global__ void __launch_bounds__(kRThreads, 1)
             if (idx < kRN * cpr) {
               const int m = idx / cpr, b = col_x[m];
               if (b >= 0) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    p.ovec + ((size_t)b * p.g + (p.step - 1)) * p.r + (size_t)(idx - m * cpr) * 8);
+                const size_t orow = MODE == kModeDraft ? (size_t)b * p.g + (p.step - 1) : (size_t)b;
+                const float4* src =
+                    reinterpret_cast<const float4*>(p.ovec + orow * p.r + (size_t)(idx - m * cpr) * 8);
                 f[j][0] = __ldg(src);
                 f[j][1] = __ldg(src + 1);
               }
@@ -608,7 +625,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
       // computed once up front (visible to the combining warp after the first
       // tile's barrier) instead of on the per-tile critical path
       const int nbl = 2 * nt;
-      const bool gpre = MODE == kModeResid && nbl <= kRGMax;
+      const bool gpre = kRes && nbl <= kRGMax;
       if (gpre)
         for (int idx = et; idx < ncols * nbl; idx += 32 * kREpi) {
           const int col = idx / nbl, lb = idx - col * nbl;
@@ -625,11 +642,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
         rd[j] = 0.f;
       }
       for (int i = 0; i < nt; ++i) {
-        const int it = gq * nt + i, t = tile_of(gq, i), ab = it & 1, us = it % kRUP;
+        const int it = gq * nt + i, t = tile_of(gq, i), ab = it & 1, us = it % kUP;
         bool live = !aborted();
         if (live) {
           bool ok = tc::mbar_wait(t_full(ab), (it >> 1) & 1, abort);
-          ok = ok && tc::mbar_wait(up_full(us), (it / kRUP) & 1, abort);
+          ok = ok && tc::mbar_wait(up_full(us), (it / kUP) & 1, abort);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) {
             if (lane == 0 && !*abort) {
@@ -652,8 +669,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
             float uu[16], pp[16];
             // stage layout: per request [U slice | P slice] (residual), or
             // [32 rows of U][32 rows of P] (the loss modes' two boxes)
-            constexpr uint32_t kRow = (MODE == kModeResid || MODE == kModeTree) ? 2 * kRM * 4 : kRM * 4;
-            constexpr uint32_t kPOff = MODE == kModeResid ? kRM * 4 : kRN * kRM * 4;
+            constexpr uint32_t kRow = (kRes || MODE == kModeTree) ? 2 * kRM * 4 : kRM * 4;
+            constexpr uint32_t kPOff = kRes ? kRM * 4 : kRN * kRM * 4;
             const uint32_t su = sUP + us * L.stage + (uint32_t)(half * 16) * kRow + (uint32_t)(q * 32 + lane) * 4u;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -737,7 +754,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
           asm volatile("bar.sync 2, 256;" ::: "memory");  // part[] is rewritten by the next tile
         }
-        if constexpr (MODE == kModeResid) {
+        if constexpr (kRes) {
           asm volatile("bar.sync 2, 256;" ::: "memory");
           if (live && warp == 4) {
             // blocks 2t (entries 0..63: quarters 0, 1) and 2t+1 (quarters 2, 3)
@@ -790,7 +807,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
           for (int col = lane; col < ncols; col += 32)
             p.l1part[(size_t)col_b[col] * p.G + c] =
                 (part[col] + part[kRN + col]) + (part[2 * kRN + col] + part[3 * kRN + col]);
-      } else if constexpr (MODE == kModeResid) {
+      } else if constexpr (kRes) {
         if (warp == 4 && !aborted())
           for (int col = lane; col < ncols; col += 32)
             p.rpart[(size_t)col_b[col] * p.G + c] = make_float2(best_key[col], __int_as_float(best_blk[col]));
@@ -827,7 +844,7 @@ int resid_tc_supported(const dspark_dims& d) {
 }
 
 cudaError_t resid_tc_configure(dspark_ws* ws) {
-  const RSmem L = RSmem::make(ws->d.r, false);
+  const RSmem L = RSmem::make(ws->d.r, kModeResid);
   const size_t smem = L.total + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_resid_tc<kModeResid>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
@@ -836,7 +853,10 @@ cudaError_t resid_tc_configure(dspark_ws* ws) {
     e = cudaFuncSetAttribute(k_resid_tc<kModeLossL1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_resid_tc<kModeDraft>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(RSmem::make(ws->d.r, true).total + 1024));
+                             (int)(RSmem::make(ws->d.r, kModeDraft).total + 1024));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_resid_tc<kModeResidRnn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(RSmem::make(ws->d.r, kModeResidRnn).total + 1024));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(k_resid_tc<kModeTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -919,8 +939,12 @@ cudaError_t launch_resid_tc(const dspark_ws* ws, const VerifyArgs& a, float2* rp
   p.vrow = ws->s.vrow;
   p.vlset = ws->s.vlset;
   p.rpart = rpart;
-  const RSmem L = RSmem::make(d.r, false);
-  return launch_ex(k_resid_tc<kModeResid>, dim3(grid), dim3(kRThreads), L.total + 1024, st, pdl, tm, tm, tm, p);
+  p.ovec = a.ovec;
+  if (a.ovec)  // the RNN head: B = o_{n+1} as bf16 hi + lo
+    return launch_ex(k_resid_tc<kModeResidRnn>, dim3(grid), dim3(kRThreads),
+                     RSmem::make(d.r, kModeResidRnn).total + 1024, st, pdl, tm, tm, tm, p);
+  return launch_ex(k_resid_tc<kModeResid>, dim3(grid), dim3(kRThreads), RSmem::make(d.r, kModeResid).total + 1024,
+                   st, pdl, tm, tm, tm, p);
 }
 
 cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cudaStream_t st) {
@@ -944,7 +968,7 @@ cudaError_t launch_loss_tc(const dspark_ws* ws, const LossArgs& a, int pass, cud
   p.l1part = a.l1part;
   p.lse_d = a.lse_d;
   p.lse_t = a.lse_t;
-  const RSmem L = RSmem::make(d.r, false);
+  const RSmem L = RSmem::make(d.r, kModeResid);
   if (pass == 0)
     k_resid_tc<kModeLossStats><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tp, p);
   else
@@ -966,7 +990,7 @@ cudaError_t launch_rnn_blocks_tc(const dspark_ws* ws, const float* U, const void
   p.step = k;
   p.blk = ws->s.blk;
   p.nblk = ws->geo.nblk;
-  const RSmem L = RSmem::make(d.r, true);
+  const RSmem L = RSmem::make(d.r, kModeDraft);
   k_resid_tc<kModeDraft><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tu, tu, p);
   return cudaGetLastError();
 }
@@ -992,7 +1016,7 @@ cudaError_t launch_tree_blocks_tc(const dspark_ws* ws, const float* U, const voi
   p.blk = blk;
   p.bmax = bmax;
   p.nblk = ws->geo.nblk;
-  const RSmem L = RSmem::make(d.r, false);
+  const RSmem L = RSmem::make(d.r, kModeResid);
   k_resid_tc<kModeTree><<<p.G, kRThreads, L.total + 1024, st>>>(tm, tm, tm, p);
   return cudaGetLastError();
 }

@@ -1078,8 +1078,8 @@ static cudaError_t verify_impl(const dspark_ws* ws, const VerifyArgs& a, cudaStr
   const bool pdl_resid = pdl && (geo.sweep_bulk || dyn);  // the residual kernels follow a bulk sweep
   const size_t smem = sizeof(float) * d.r;
   int nchunk = kResidChunks;
-  if (BF16 && ws->use_tc && geo.resid_tc_ok && !a.ovec) {
-    // residual block draw on tensor cores: one CTA per SM
+  if (BF16 && ws->use_tc && geo.resid_tc_ok) {
+    // residual block draw on tensor cores (either head): one CTA per SM
     nchunk = geo.num_sms;
     cudaError_t e = launch_resid_tc(ws, a, ws->s.rpart, nchunk, st, pdl_resid);
     if (e != cudaSuccess) return e;

@@ -125,10 +125,13 @@ def test_rnn_head_differs_from_markov_head():
     assert not np.allclose(m["lse"], o["lse"])
 
 
-def test_rnn_verify_stagewise_on_oracle_drafts():
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+def test_rnn_verify_stagewise_on_oracle_drafts(path):
     """Both sides verify the oracle's RNN-head drafts: p_d of a rejected
     position from U + o W2 (the oracle's o_k, rounded to fp32 for the GPU),
-    under several length patterns; most requests take a residual draw."""
+    under several length patterns; most requests take a residual draw. The
+    residual block pass runs on tcgen05 (o as bf16 hi + lo operands; the
+    vocabulary ends 8 entries into its last tile) or on CUDA cores."""
     from parity import Tally, compare_verify, pack_np, row_off_np
     wl = _wl("rnn_verify", 24, 4, 4104, 64, 96, seed=43)
     inp = make_inputs(wl)
@@ -137,6 +140,7 @@ def test_rnn_verify_stagewise_on_oracle_drafts():
     od = oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
                           6, 4)
     ws = Workspace.for_workload(wl)
+    ws.set_path(path)
     rng = np.random.default_rng(8)
     tally = Tally()
     resid = 0
@@ -157,6 +161,42 @@ def test_rnn_verify_stagewise_on_oracle_drafts():
         assert (out["n_acc"].cpu().numpy() <= L - 1).all()
     tally.check_rate()
     assert tally.compared > 0 and resid > 0
+
+
+def test_rnn_verify_full_size():
+    """The RNN verify at the prod shape (B=128, gamma=5, V=129280, r=256) on
+    the oracle's drafts of sixteen sampled requests, each verifying two to
+    gamma + 1 rows (most take a residual draw on tcgen05, whose CTAs then
+    hold several requests each); the other requests verify their bonus row
+    only."""
+    from parity import compare_verify, pack_np, row_off_np
+    wl = WORKLOADS["prod"]
+    inp = make_inputs(wl)
+    inp["Wr"] = make_rnn_weights(wl)
+    npi = np_inputs(inp)
+    reqs = [0, 1, 9, 23, 37, 42, 50, 64, 71, 88, 95, 101, 110, 117, 126, 127]
+    od = oracle.rnn_draft(npi["U"], npi["W1"], npi["W2"], npi["Wr"], npi["anchor"], npi["h"], npi["w"], npi["T"],
+                          7, 2, reqs=reqs)
+    tokens = np.where(od["tokens"] < 0, 0, od["tokens"]).astype(np.int32)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.nan_to_num(a)).astype(np.float32)).cuda()
+    L = np.ones(wl.B, np.int32)
+    L[reqs] = np.random.default_rng(9).integers(2, wl.gamma + 2, len(reqs))
+    ro = row_off_np(L)
+    P = pack_np(npi["P_full"], L)
+    ws = Workspace.for_workload(wl)
+    assert ws.path == "tcgen05"
+    out = ws.verify_rnn(torch.from_numpy(P).cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(L).cuda(),
+                        inp["anchor"].cuda(), torch.from_numpy(tokens).cuda(), f32(od["pd_tok"]), f32(od["lse"]),
+                        inp["U"].cuda(), f32(od["ovec"]), inp["W2"].cuda(), 7, 2)
+    torch.cuda.synchronize()
+    assert ws.device_status() == 0
+    ov = oracle.verify(P, ro, L, npi["anchor"], tokens, npi["U"], npi["W1"], npi["W2"], 7, 2, reqs=reqs,
+                       ovec=np.nan_to_num(od["ovec"]))
+    tally = compare_verify(gpu_np(out), ov, reqs)
+    tally.check_rate()
+    assert tally.compared > 0 and int(ov["resid"][reqs].sum()) > 0
+    n = out["n_acc"].cpu().numpy()
+    assert (n[L == 1] == 0).all()
 
 
 def test_rnn_round_on_the_gpu_is_consistent():
