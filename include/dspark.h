@@ -320,9 +320,11 @@ size_t dspark_rnn_draft_scratch_bytes(const dspark_ws* ws);
  * The verify of drafts made with the RNN head: as dspark_verify, but the draft
  * distribution of a rejected position n+1 is recomputed from ovec[b][n] (the
  * head vector o_{n+1} that dspark_rnn_draft wrote, fp32 [B][gamma][r]) as
- * softmax(U_{n+1} + o_{n+1} W2) instead of from W1[x_n]; W1 is not read. The
- * residual block pass then runs on CUDA cores. Same pointer rules, outputs
- * and errors as dspark_verify.
+ * softmax(U_{n+1} + o_{n+1} W2) instead of from W1[x_n]; W1 is not read. On
+ * the tcgen05 path (bf16 weights, r a multiple of 64 up to 256, V % 8 == 0)
+ * the residual block pass takes o_{n+1} as bf16 hi + lo operands (about 16
+ * significant bits of o); otherwise it runs on CUDA cores in fp32. Same
+ * pointer rules, outputs and errors as dspark_verify.
  */
 dspark_status dspark_verify_rnn(dspark_ws* ws, const float* P, const int32_t* row_off, const int32_t* lengths,
                                 const int32_t* anchor, const int32_t* tokens, const float* pd_tok, const float* lse,
