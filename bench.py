@@ -238,23 +238,24 @@ def workload_config(wl, sum_len):
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def oracle_plan_lengths(wl, npi, seed: int, rnd: int):
+def oracle_plan_lengths(wl, npi, seed: int, rnd: int, od=None):
     """The oracle's own verify lengths for the workload's round: it drafts every
-    request once (untimed) and plans on those confidences in the workload's
-    mode (lagged: the capacity from the same confidences, as in a steady
-    sequence of identical rounds)."""
+    request once (untimed; or takes that draft as `od`) and plans on those
+    confidences in the workload's mode (lagged: the capacity from the same
+    confidences, as in a steady sequence of identical rounds)."""
     import numpy as np
     import oracle
     if wl.mode == "static":
         return np.full(wl.B, wl.gamma + 1, np.int32)
-    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], seed, rnd)
+    if od is None:
+        od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], seed, rnd)
     conf = od["conf"].astype(np.float32)
     if wl.mode == "lagged":
         return oracle.plan_lagged(conf, conf, npi["sps"])[0]
     return oracle.plan_sync(conf, npi["sps"])[0]
 
 
-def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int, lengths=None):
+def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int, lengths=None, od=None):
     """Time the oracle (draft + plan + verify) on a bounded sample of requests.
 
     Returns (rounds_per_s, cores, sample description). The verify lengths are
@@ -271,7 +272,7 @@ def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int, lengths=Non
     cores = oracle.get_threads()
     npi = {k: (v.contiguous().view(torch.int16).numpy() if v.dtype == torch.bfloat16 else v.numpy())
            for k, v in inp_cpu.items()}
-    L = oracle_plan_lengths(wl, npi, seed, rnd) if lengths is None else np.asarray(lengths, np.int32)
+    L = oracle_plan_lengths(wl, npi, seed, rnd, od) if lengths is None else np.asarray(lengths, np.int32)
     ro = np.zeros(wl.B + 1, np.int32)
     ro[1:] = np.cumsum(L)
     P = np.concatenate([npi["P_full"][b, :L[b]] for b in range(wl.B)]).reshape(-1, wl.V)
@@ -301,6 +302,62 @@ def oracle_sample(wl, inp_cpu, budget_s: float, seed: int, rnd: int, lengths=Non
                                  f"({int(L.sum())} for the batch) on a sample of {done_req} requests of the "
                                  f"{wl.name} workload: {spent:.1f} s on {cores} threads, scaled to a "
                                  f"{wl.B}-request round")
+
+
+def oracle_round_parity(wl, npi, od, gpu, seed: int, rnd: int):
+    """The timed round's outputs (`gpu`: tokens, lengths, n_acc, next_anchor)
+    against the oracle's on the same inputs, by the tests' parity rule: each
+    request's draft tokens up to its first flagged draw (a Gumbel-key gap
+    below the oracle's margin) or first difference; the plan's lengths, which
+    may differ only where the oracle flags its admission path; and, on the
+    GPU's lengths, the verify of every request whose draft agrees, except
+    where an accept test or a draw is flagged. `od` is the oracle's draft of
+    every request. Returns the counts and the observed flag rates."""
+    import numpy as np
+    import oracle
+    B, g = wl.B, wl.gamma
+    gt = gpu["tokens"]
+    pos = flagged = mism = 0
+    same = np.ones(B, bool)
+    for b in range(B):
+        for k in range(g):
+            differs = gt[b, k] != od["tokens"][b, k]
+            if od["margin"][b, k] < oracle.MARGIN:
+                flagged += 1
+            else:
+                pos += 1
+                mism += int(differs)
+            if differs:  # later draws condition on another token
+                same[b] = False
+                break
+    conf = od["conf"].astype(np.float32)
+    if wl.mode == "static":
+        L, pm = np.full(B, g + 1, np.int32), oracle.PlanMargin()
+    elif wl.mode == "lagged":
+        L, _, pm = oracle.plan_lagged(conf, conf, npi["sps"])
+    else:
+        L, _, pm = oracle.plan_sync(conf, npi["sps"])
+    Lg = np.asarray(gpu["lengths"], np.int32)
+    ro = np.zeros(B + 1, np.int32)
+    ro[1:] = np.cumsum(Lg)
+    P = np.concatenate([npi["P_full"][b, :Lg[b]] for b in range(B)]).reshape(-1, wl.V)
+    reqs = [b for b in range(B) if same[b]]
+    vf = vm = vc = 0
+    if reqs:
+        ov = oracle.verify(P, ro, Lg, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], seed, rnd,
+                           reqs=reqs)
+        for b in reqs:
+            if ov["acc_margin"][b] < oracle.MARGIN or ov["smp_margin"][b] < oracle.MARGIN:
+                vf += 1
+                continue
+            vc += 1
+            vm += int(gpu["n_acc"][b] != ov["n_acc"][b] or gpu["next_anchor"][b] != ov["next_anchor"][b])
+    return {"rule": "bit-exact except decisions whose oracle margin is below " + f"{oracle.MARGIN:g}",
+            "draft": {"draws_compared": pos, "flagged": flagged, "mismatched": mism,
+                      "flag_rate": flagged / max(1, pos + flagged)},
+            "plan": {"lengths_equal": bool((L == Lg).all()), "flagged": bool(pm.flagged(1e-5, 1e-5))},
+            "verify": {"requests_compared": vc, "flagged": vf, "mismatched": vm,
+                       "requests_skipped_draft_differs": int(B - len(reqs))}}
 
 
 def sts_timing(reps: int = 10, cpu_budget_s: float = 3.0):
@@ -808,6 +865,9 @@ def main():
     ms = e0.elapsed_time(e1) / args.steps
     ms = max_over_ranks(ms, world)
     assert ws.device_status() == 0
+    # the timed rounds' outputs (identical inputs, seed and round every step)
+    gpu_out = ({k: out[k].cpu().numpy() for k in ("tokens", "lengths", "n_acc", "next_anchor")}
+               if rank == 0 and not args.no_cpu_baseline else None)
 
     # stage times: each stage captured alone in a CUDA graph and replayed back
     # to back between events on the launching stream (no host launch gaps)
@@ -889,11 +949,16 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": ms2}
         del host, dstage
 
-    cpu_base = None
+    cpu_base = parity = None
     if rank == 0 and not args.no_cpu_baseline:
         inp_cpu = {k: dev_inp[k].cpu() for k in ("U", "W1", "W2", "anchor", "h", "w", "T", "sps")}
         inp_cpu["P_full"] = P_full_cpu
-        v, cores, sample = oracle_sample(wl, inp_cpu, args.cpu_seconds, seed, rnd)
+        import oracle
+        oracle.set_threads(os.cpu_count() or 1)
+        npi = _np_inputs(inp_cpu)
+        od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], seed, rnd)
+        parity = oracle_round_parity(wl, npi, od, gpu_out, seed, rnd)
+        v, cores, sample = oracle_sample(wl, inp_cpu, args.cpu_seconds, seed, rnd, od=od)
         cpu_base = {"value": v, "unit": "rounds/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
@@ -920,6 +985,7 @@ def main():
             "pctree": None if args.no_pctree else _secondary(pctree_timing, peak, cpu_budget_s=cpu_s),
             "roofline": roofline,
             "cpu_baseline": cpu_base,
+            "oracle_parity": parity,
             "e2e": e2e,
             "gpu_launches": launches_per_round * args.steps,
             "launches_per_round": launches_per_round,

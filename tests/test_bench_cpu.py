@@ -48,3 +48,36 @@ def test_sts_oracle_sample_runs_on_cpu():
     c = bench.oracle_sts_sample(make_sts_inputs(5000, 3, 1), sts_grid(8), 15, 0.1)
     assert c["value"] > 0 and c["unit"] == "fits/s" and c["kind"] == "oracle"
     assert bench.oracle_sts_sample(make_sts_inputs(100, 2, 1), sts_grid(4), 15, 0.0) is None
+
+
+def test_round_parity_report_counts():
+    """bench.py's oracle_parity entry: outputs equal to the oracle's give no
+    mismatch; a changed draft token ends that request's draft comparison and
+    drops it from the verify comparison; a changed next anchor counts once."""
+    import sys as _s
+    _s.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import oracle
+    from speculative_decoding_head_gb300.workloads import WORKLOADS, make_inputs
+    wl = WORKLOADS["small"].with_(B=6, V=4096, H=64)
+    npi = bench._np_inputs(make_inputs(wl))
+    od = oracle.draft(npi["U"], npi["W1"], npi["W2"], npi["anchor"], npi["h"], npi["w"], npi["T"], wl.seed, 0)
+    L = bench.oracle_plan_lengths(wl, npi, wl.seed, 0, od)
+    ro = np.zeros(wl.B + 1, np.int32)
+    ro[1:] = np.cumsum(L)
+    P = np.concatenate([npi["P_full"][b, :L[b]] for b in range(wl.B)]).reshape(-1, wl.V)
+    ov = oracle.verify(P, ro, L, npi["anchor"], od["tokens"], npi["U"], npi["W1"], npi["W2"], wl.seed, 0)
+    out = {"tokens": od["tokens"].copy(), "lengths": L, "n_acc": ov["n_acc"].copy(),
+           "next_anchor": ov["next_anchor"].copy()}
+    r = bench.oracle_round_parity(wl, npi, od, out, wl.seed, 0)
+    assert r["draft"]["mismatched"] == 0 and r["draft"]["draws_compared"] + r["draft"]["flagged"] == wl.B * wl.gamma
+    assert r["plan"]["lengths_equal"] and r["verify"]["mismatched"] == 0
+    assert r["verify"]["requests_compared"] + r["verify"]["flagged"] == wl.B
+    out["tokens"][0, 1] = (out["tokens"][0, 1] + 1) % wl.V
+    out["next_anchor"][1] = (out["next_anchor"][1] + 1) % wl.V
+    r = bench.oracle_round_parity(wl, npi, od, out, wl.seed, 0)
+    assert r["draft"]["mismatched"] + r["draft"]["flagged"] >= 1
+    assert r["draft"]["draws_compared"] + r["draft"]["flagged"] == wl.B * wl.gamma - (wl.gamma - 2)
+    assert r["verify"]["requests_skipped_draft_differs"] == 1
+    assert r["verify"]["mismatched"] + r["verify"]["flagged"] >= 1
