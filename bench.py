@@ -802,6 +802,8 @@ def main():
     from speculative_decoding_head_gb300.workloads import WORKLOADS, hbm_bytes, make_inputs, pack_rows
 
     world, rank, local = dist_init(args)
+    if world > 1:  # the oracle's timing (and its parity report) belongs to the one-GPU line
+        args.no_cpu_baseline = True
     torch.cuda.set_device(local)
     bmod.build()
     wl = WORKLOADS[args.workload]
